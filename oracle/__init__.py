@@ -1,0 +1,131 @@
+"""Test infrastructure -- Python entry points of the CPU oracle.
+
+Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline may import this package.  The product path (the CUDA library and
+its binding) never does.
+
+The arithmetic lives in ``oracle.c`` (plain loops, FP64 accumulation); this
+module compiles it with gcc and marshals numpy arrays.  Functions take bf16
+tensors as ``np.uint16`` bit patterns and return float64 results that are
+not rounded to any narrower type.
+
+Every function is pinned by ``tests/test_oracle.py`` against brute force,
+ordinary GEMMs, hand-worked values and invariants of the definitions.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into _build/liboracle.so (gcc, OpenMP, no fast-math)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+           "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        c_p = ctypes.c_void_p
+        lib.oracle_mgemm_rows.argtypes = [c_p, c_p, c_p, ctypes.c_int, ctypes.c_int64,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          c_p, ctypes.c_int64, c_p]
+        lib.oracle_mgemm_rows.restype = ctypes.c_int
+        lib.oracle_kgemm_rows.argtypes = [c_p, c_p, c_p, ctypes.c_int, ctypes.c_int64,
+                                          ctypes.c_int, ctypes.c_int,
+                                          c_p, c_p, ctypes.c_int64, c_p]
+        lib.oracle_kgemm_rows.restype = ctypes.c_int
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint16, a.dtype
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def mgemm(x, w, offsets, transpose_B: bool = False, rows=None) -> np.ndarray:
+    """M-grouped GEMM.
+
+    x: [M,K] bf16 bits; w: [E,N,K] (or [E,K,N] with transpose_B) bf16 bits;
+    offsets: int32 [E+1].  Returns float64 [M,N] with rows >= offsets[E] set
+    to NaN (they belong to no expert), or, when ``rows`` is given, float64
+    [len(rows), N] for those rows only.
+    """
+    x, w = _u16(x), _u16(w)
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    M, K = x.shape
+    E = w.shape[0]
+    N = w.shape[2] if transpose_B else w.shape[1]
+    assert w.shape == ((E, K, N) if transpose_B else (E, N, K)), w.shape
+    assert off.shape == (E + 1,)
+    full = rows is None
+    if full:
+        rows = np.arange(int(off[E]), dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((len(rows), N), dtype=np.float64)
+    rc = _load().oracle_mgemm_rows(_ptr(x), _ptr(w), _ptr(off), E, M, N, K,
+                                   int(bool(transpose_B)), _ptr(rows), len(rows), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_mgemm_rows rejected its arguments")
+    if full:
+        y = np.full((M, N), np.nan, dtype=np.float64)
+        y[: int(off[E])] = out
+        return y
+    return out
+
+
+def kgemm(grad, X, offsets, sel=None) -> np.ndarray:
+    """K-grouped FP32 weight gradient, computed in FP64.
+
+    grad: [M,N] bf16 bits; X: [M,K] bf16 bits; offsets: int32 [E+1].
+    Returns float64 [E,N,K], or, when ``sel`` = (experts, ns) is given,
+    float64 [len(experts), K] with row i = dW[experts[i], ns[i], :].
+    """
+    grad, X = _u16(grad), _u16(X)
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    M, N = grad.shape
+    M2, K = X.shape
+    assert M == M2
+    E = len(off) - 1
+    full = sel is None
+    if full:
+        se = np.repeat(np.arange(E, dtype=np.int32), N)
+        sn = np.tile(np.arange(N, dtype=np.int32), E)
+    else:
+        se = np.ascontiguousarray(sel[0], dtype=np.int32)
+        sn = np.ascontiguousarray(sel[1], dtype=np.int32)
+    out = np.empty((len(se), K), dtype=np.float64)
+    rc = _load().oracle_kgemm_rows(_ptr(grad), _ptr(X), _ptr(off), E, M, N, K,
+                                   _ptr(se), _ptr(sn), len(se), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_kgemm_rows rejected its arguments")
+    return out.reshape(E, N, K) if full else out

@@ -1,0 +1,294 @@
+"""Pins for the CPU oracle (no GPU).
+
+The oracle is trusted only because these tests tie it to things other than
+itself: hand-worked values, an independent brute-force loop, ordinary GEMMs
+from numpy, exact integer arithmetic and invariants of the definitions
+(RapidGEMM README, "Kernels": Mgemm for forward / input gradient, Kgemm for
+the FP32 weight gradient, both over a cumulative row-offset vector with a
+leading zero).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bits(a):
+    """Exact bf16 bit patterns of small integers / bf16-representable values."""
+    return W.f32_to_bf16_bits(np.asarray(a, dtype=np.float32))
+
+
+def rand_bits(rng, shape, scale=1.0):
+    return W.f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32) * np.float32(scale))
+
+
+def f64(b):
+    return W.bf16_bits_to_f32(b).astype(np.float64)
+
+
+# ---------------------------------------------------------------- hand-worked
+
+
+def test_golden_handworked_fwd():
+    g = json.load(open(os.path.join(GOLDEN, "handworked_e3.json")))
+    off = np.array(g["offsets"], dtype=np.int32)
+    f = g["fwd"]
+    y = oracle.mgemm(bits(f["x"]), bits(f["w"]), off)
+    np.testing.assert_array_equal(y[:3], np.array(f["y_rows_0_to_2"], dtype=np.float64))
+    assert np.isnan(y[3]).all()  # row 3 belongs to no expert
+
+
+def test_golden_handworked_dgrad():
+    g = json.load(open(os.path.join(GOLDEN, "handworked_e3.json")))
+    off = np.array(g["offsets"], dtype=np.int32)
+    d = g["dgrad"]
+    y = oracle.mgemm(bits(d["x"]), bits(d["w"]), off, transpose_B=True)
+    np.testing.assert_array_equal(y[:3], np.array(d["y_rows_0_to_2"], dtype=np.float64))
+
+
+def test_golden_handworked_wgrad():
+    g = json.load(open(os.path.join(GOLDEN, "handworked_e3.json")))
+    off = np.array(g["offsets"], dtype=np.int32)
+    d = g["wgrad"]
+    dW = oracle.kgemm(bits(d["grad"]), bits(d["X"]), off)
+    np.testing.assert_array_equal(dW, np.array(d["dW"], dtype=np.float64))
+
+
+# ---------------------------------------------------------------- brute force
+
+
+def brute_mgemm(x, w, offsets, transpose_B):
+    """Independent pure-Python triple loop over plain lists."""
+    M, K = len(x), len(x[0])
+    E = len(offsets) - 1
+    N = len(w[0][0]) if transpose_B else len(w[0])
+    y = [[None] * N for _ in range(M)]
+    for e in range(E):
+        for r in range(offsets[e], offsets[e + 1]):
+            for n in range(N):
+                s = 0.0
+                for k in range(K):
+                    b = w[e][k][n] if transpose_B else w[e][n][k]
+                    s += x[r][k] * b
+                y[r][n] = s
+    return y
+
+
+def brute_kgemm(grad, X, offsets):
+    N, K = len(grad[0]), len(X[0])
+    E = len(offsets) - 1
+    dW = [[[0.0] * K for _ in range(N)] for _ in range(E)]
+    for e in range(E):
+        for n in range(N):
+            for k in range(K):
+                s = 0.0
+                for r in range(offsets[e], offsets[e + 1]):
+                    s += grad[r][n] * X[r][k]
+                dW[e][n][k] = s
+    return dW
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("transpose_B", [False, True])
+def test_mgemm_matches_brute_force(seed, transpose_B):
+    rng = np.random.default_rng(seed)
+    E = 3
+    M = int(rng.integers(4, 13))
+    N = int(rng.integers(1, 8))
+    K = int(rng.integers(1, 8))
+    counts = rng.multinomial(M - 2, [0.5, 0.0, 0.5])  # expert 1 empty, 2 rows past offsets[E]
+    off = W.offsets_from_counts(counts)
+    x = rand_bits(rng, (M, K))
+    w = rand_bits(rng, (E, K, N) if transpose_B else (E, N, K))
+    y = oracle.mgemm(x, w, off, transpose_B=transpose_B)
+    ref = brute_mgemm(f64(x).tolist(), f64(w).tolist(), off.tolist(), transpose_B)
+    for r in range(M):
+        if ref[r][0] is None:
+            assert np.isnan(y[r]).all()
+        else:
+            np.testing.assert_array_equal(y[r], np.array(ref[r]))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_kgemm_matches_brute_force(seed):
+    rng = np.random.default_rng(100 + seed)
+    E = 3
+    M = int(rng.integers(4, 13))
+    N = int(rng.integers(1, 8))
+    K = int(rng.integers(1, 8))
+    counts = rng.multinomial(M - 1, [0.3, 0.0, 0.7])
+    off = W.offsets_from_counts(counts)
+    grad = rand_bits(rng, (M, N))
+    X = rand_bits(rng, (M, K))
+    dW = oracle.kgemm(grad, X, off)
+    ref = np.array(brute_kgemm(f64(grad).tolist(), f64(X).tolist(), off.tolist()))
+    np.testing.assert_array_equal(dW, ref)
+
+
+# ---------------------------------------------------------------- ordinary GEMMs
+
+
+def test_single_group_is_ordinary_gemm():
+    rng = np.random.default_rng(7)
+    M, N, K = 37, 19, 53
+    x = rand_bits(rng, (M, K))
+    w = rand_bits(rng, (1, N, K))
+    off = np.array([0, M], dtype=np.int32)
+    y = oracle.mgemm(x, w, off)
+    np.testing.assert_allclose(y, f64(x) @ f64(w[0]).T, rtol=1e-12, atol=1e-12)
+    wt = rand_bits(rng, (1, K, N))
+    yt = oracle.mgemm(x, wt, off, transpose_B=True)
+    np.testing.assert_allclose(yt, f64(x) @ f64(wt[0]), rtol=1e-12, atol=1e-12)
+    grad = rand_bits(rng, (M, N))
+    dW = oracle.kgemm(grad, x, off)
+    np.testing.assert_allclose(dW[0], f64(grad).T @ f64(x), rtol=1e-12, atol=1e-12)
+
+
+def test_integer_inputs_are_exact():
+    """Integers in {-2..2}: every partial sum is an exact integer, so the
+    result must equal numpy's int64 GEMM per group exactly."""
+    rng = np.random.default_rng(11)
+    E, N, K = 4, 24, 300
+    counts = np.array([130, 0, 1, 97])
+    off = W.offsets_from_counts(counts)
+    M = int(off[-1]) + 5
+    xi = rng.integers(-2, 3, size=(M, K))
+    wi = rng.integers(-2, 3, size=(E, N, K))
+    gi = rng.integers(-2, 3, size=(M, N))
+    y = oracle.mgemm(bits(xi), bits(wi), off)
+    yt = oracle.mgemm(bits(xi), bits(wi.transpose(0, 2, 1).copy()), off, transpose_B=True)
+    dW = oracle.kgemm(bits(gi), bits(xi), off)
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        ref = xi[a:b] @ wi[e].T
+        np.testing.assert_array_equal(y[a:b], ref.astype(np.float64))
+        np.testing.assert_array_equal(yt[a:b], ref.astype(np.float64))
+        np.testing.assert_array_equal(dW[e], (gi[a:b].T @ xi[a:b]).astype(np.float64))
+
+
+# ---------------------------------------------------------------- invariants
+
+
+def test_concatenating_groups_reproduces_grouped_result():
+    rng = np.random.default_rng(3)
+    E, N, K = 5, 11, 29
+    counts = np.array([3, 0, 8, 1, 6])
+    off = W.offsets_from_counts(counts)
+    M = int(off[-1])
+    x = rand_bits(rng, (M, K))
+    w = rand_bits(rng, (E, N, K))
+    y = oracle.mgemm(x, w, off)
+    parts = []
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        one = np.array([0, b - a], dtype=np.int32)
+        parts.append(oracle.mgemm(x[a:b], w[e:e + 1], one))
+    np.testing.assert_array_equal(y, np.concatenate(parts))
+
+
+def test_dgrad_equals_forward_on_transposed_weights():
+    rng = np.random.default_rng(4)
+    E, N, K = 3, 13, 21
+    off = W.offsets_from_counts([5, 7, 2])
+    x = rand_bits(rng, (14, K))
+    w_kn = rand_bits(rng, (E, K, N))
+    a = oracle.mgemm(x, w_kn, off, transpose_B=True)
+    b = oracle.mgemm(x, np.ascontiguousarray(w_kn.transpose(0, 2, 1)), off)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_kgemm_empty_group_is_zero_and_rows_past_end_ignored():
+    rng = np.random.default_rng(5)
+    off = np.array([0, 4, 4, 9], dtype=np.int32)
+    M, N, K = 12, 6, 10
+    grad = rand_bits(rng, (M, N))
+    X = rand_bits(rng, (M, K))
+    dW = oracle.kgemm(grad, X, off)
+    assert (dW[1] == 0).all()
+    grad2 = grad.copy()
+    grad2[9:] = bits(np.full((3, N), 1e30))  # rows past offsets[E] must not matter
+    np.testing.assert_array_equal(oracle.kgemm(grad2, X, off), dW)
+
+
+def test_kgemm_split_group_sums_to_whole():
+    """Splitting a group into two consecutive groups and adding their dW gives
+    the original (exact with integer inputs)."""
+    rng = np.random.default_rng(6)
+    M, N, K = 40, 9, 17
+    gi = rng.integers(-2, 3, size=(M, N))
+    xi = rng.integers(-2, 3, size=(M, K))
+    whole = oracle.kgemm(bits(gi), bits(xi), np.array([0, 3, 40], dtype=np.int32))
+    split = oracle.kgemm(bits(gi), bits(xi), np.array([0, 3, 25, 40], dtype=np.int32))
+    np.testing.assert_array_equal(whole[0], split[0])
+    np.testing.assert_array_equal(whole[1], split[1] + split[2])
+
+
+def test_row_and_pair_subsets_match_full():
+    rng = np.random.default_rng(8)
+    off = W.offsets_from_counts([10, 0, 7, 15])
+    M, N, K = 35, 12, 20
+    x = rand_bits(rng, (M, K))
+    w = rand_bits(rng, (4, N, K))
+    y = oracle.mgemm(x, w, off)
+    rows = np.array([31, 0, 16, 17, 9])
+    np.testing.assert_array_equal(oracle.mgemm(x, w, off, rows=rows), y[rows])
+    grad = rand_bits(rng, (M, N))
+    dW = oracle.kgemm(grad, x, off)
+    se, sn = np.array([3, 0, 1, 2]), np.array([11, 0, 5, 7])
+    np.testing.assert_array_equal(oracle.kgemm(grad, x, off, sel=(se, sn)), dW[se, sn])
+
+
+def test_bad_offsets_rejected():
+    x = bits(np.ones((4, 8)))
+    w = bits(np.ones((2, 8, 8)))
+    for off in ([1, 2, 4], [0, 3, 2], [0, 2, 5]):
+        with pytest.raises(ValueError):
+            oracle.mgemm(x, w, np.array(off, dtype=np.int32))
+
+
+def test_planted_index_mistake_is_caught():
+    """A transposed weight index (w[e,k,n] read as w[e,n,k]) changes the
+    result whenever N != K: the pins above must see it."""
+    rng = np.random.default_rng(9)
+    x = rand_bits(rng, (6, 5))
+    w = rand_bits(rng, (1, 3, 5))
+    off = np.array([0, 6], dtype=np.int32)
+    right = oracle.mgemm(x, w, off)
+    wrong = f64(x) @ f64(w[0]).reshape(5, 3)  # the mistake, planted on the CPU side only
+    assert not np.allclose(right, wrong)
+
+
+# ---------------------------------------------------------------- generator
+
+
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(12)
+    v = rng.standard_normal(100000).astype(np.float32) * 3
+    # add exact ties: values halfway between two bf16 numbers
+    ties = (np.arange(1, 1001, dtype=np.uint32) << 16 | 0x8000).view(np.float32)
+    v = np.concatenate([v, ties, -ties])
+    ours = W.f32_to_bf16_bits(v)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(ours, ref)
+
+
+def test_workload_counts():
+    t = W.tiny()
+    assert t.counts.sum() == 512 and t.counts[2] == 0
+    assert all(c % 128 for c in t.counts[[0, 1, 3]])
+    a = W.a3b_layer()
+    assert a.counts.sum() == 32768 and len(a.counts) == 32
+    s = W.skewed()
+    assert s.counts.sum() == 65536 and len(s.counts) == 128
+    st = W.skewed(tail=True)
+    assert st.counts.sum() == 65536 and (st.counts == 0).sum() >= 4
+    assert (st.counts <= 7).sum() >= 32
+    off = a.offsets
+    assert off[0] == 0 and off[-1] == 32768 and (np.diff(off) >= 0).all()

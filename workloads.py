@@ -1,0 +1,302 @@
+"""Seeded synthetic inputs for the MoE grouped GEMM workloads.
+
+This module only draws numbers: per-expert row counts, the cumulative
+row-offset vector built from them, and bf16 operand tensors.  It holds none
+of the grouped-GEMM arithmetic, so both the CPU oracle (``oracle/``) and the
+CUDA path (``moe_grouped_gemm_device_gb300``) can take their inputs from it
+without sharing any of the method's code.
+
+Conventions (the readings behind them are listed in the design doc):
+
+* Offsets are int32 ``[E+1]`` with a leading zero: expert ``e`` owns rows
+  ``offsets[e] .. offsets[e+1]-1`` (RapidGEMM README, "Kernels": ``cnt`` is
+  the cumulative row-offset tensor with a leading zero).
+* ``N(0, v)`` in a workload description means variance ``v``: weights of a
+  layer whose contraction length is ``K`` are drawn with std ``1/sqrt(K)``.
+* Random numbers come from numpy's PCG64.  A tensor is filled in fixed-size
+  chunks, chunk ``i`` from ``SeedSequence([seed, stream, i])``, so the values
+  do not depend on how many threads generate them.  FP32 normals are rounded
+  to bf16 with round-to-nearest-even.
+* bf16 tensors are returned as ``np.uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import numpy as np
+
+CHUNK = 1 << 22  # elements per independently seeded chunk
+
+# --------------------------------------------------------------------------
+# bf16 bit helpers (number representation only)
+# --------------------------------------------------------------------------
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even); return the bits."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32)
+    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    out = ((u + bias) >> np.uint32(16)).astype(np.uint16)
+    nan = np.isnan(a)
+    if nan.any():
+        out[nan] = np.uint16(0x7FC0)
+    return out
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float32."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+# --------------------------------------------------------------------------
+# Seeded tensor fills
+# --------------------------------------------------------------------------
+
+_POOL: ThreadPoolExecutor | None = None
+
+
+def _pool() -> ThreadPoolExecutor:
+    global _POOL
+    if _POOL is None:
+        _POOL = ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1)))
+    return _POOL
+
+
+def normal_bf16(shape, std: float, seed: int, stream: int) -> np.ndarray:
+    """bf16 bits of N(0, std^2) values of the given shape."""
+    n = int(np.prod(shape, dtype=np.int64))
+    out = np.empty(n, dtype=np.uint16)
+    std32 = np.float32(std)
+
+    def fill(i: int) -> None:
+        lo = i * CHUNK
+        hi = min(n, lo + CHUNK)
+        rng = np.random.default_rng(np.random.SeedSequence([seed, stream, i]))
+        v = rng.standard_normal(hi - lo, dtype=np.float32)
+        if std32 != np.float32(1.0):
+            v *= std32
+        out[lo:hi] = f32_to_bf16_bits(v)
+
+    nchunks = (n + CHUNK - 1) // CHUNK
+    if nchunks <= 1:
+        if n:
+            fill(0)
+    else:
+        list(_pool().map(fill, range(nchunks)))
+    return out.reshape(shape)
+
+
+def integer_bf16(shape, lo: int, hi: int, seed: int, stream: int) -> np.ndarray:
+    """bf16 bits of integers drawn uniformly from [lo, hi] (exact in bf16)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, stream]))
+    v = rng.integers(lo, hi + 1, size=shape).astype(np.float32)
+    return f32_to_bf16_bits(v)
+
+
+# --------------------------------------------------------------------------
+# Row counts and offsets
+# --------------------------------------------------------------------------
+
+
+def offsets_from_counts(counts) -> np.ndarray:
+    counts = np.asarray(counts, dtype=np.int64)
+    assert (counts >= 0).all()
+    off = np.zeros(len(counts) + 1, dtype=np.int64)
+    np.cumsum(counts, out=off[1:])
+    assert off[-1] < 2**31
+    return off.astype(np.int32)
+
+
+def counts_tiny(seed: int = 0) -> np.ndarray:
+    """E=4, M=512: multinomial over experts 0, 1, 3 with expert 2 empty.
+
+    A draw in which some count is a multiple of 128 is replaced by the next
+    draw of the same generator, so every tile boundary is ragged.
+    """
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0]))
+    while True:
+        c3 = rng.multinomial(512, [1 / 3] * 3)
+        if all(c % 128 != 0 for c in c3):
+            break
+    return np.array([c3[0], c3[1], 0, c3[2]], dtype=np.int64)
+
+
+def counts_dirichlet(E: int, M: int, alpha: float, seed: int) -> np.ndarray:
+    """Dirichlet(alpha) shares rounded to integers that sum to M.
+
+    floor(M*p), then one extra row to each of the largest fractional parts
+    (ties to the lower expert index) until the sum is M.
+    """
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0]))
+    p = rng.dirichlet([alpha] * E)
+    raw = M * p
+    base = np.floor(raw).astype(np.int64)
+    rem = int(M - base.sum())
+    frac = raw - base
+    order = np.lexsort((np.arange(E), -frac))
+    base[order[:rem]] += 1
+    assert base.sum() == M
+    return base
+
+
+def counts_zipf(E: int, M: int, s: float, seed: int, tail: bool = False) -> np.ndarray:
+    """Truncated Zipf(s) over a seeded permutation of the experts.
+
+    Rank r (1..E) has probability proportional to r**-s; expert perm[r-1]
+    gets rank r; counts are a multinomial(M) draw.  With ``tail=True`` the 32
+    lowest-probability ranks instead get Uniform{0..7} rows, the 4 lowest of
+    them none at all, and rank 1 absorbs the difference so the sum stays M.
+    """
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0]))
+    perm = rng.permutation(E)
+    ranks = np.arange(1, E + 1, dtype=np.float64)
+    p_rank = ranks ** (-s)
+    p_rank /= p_rank.sum()
+    c_rank = rng.multinomial(M, p_rank).astype(np.int64)
+    if tail:
+        trng = np.random.default_rng(np.random.SeedSequence([seed, 1]))
+        ntail = min(32, E - 1)
+        c_rank[E - ntail:] = trng.integers(0, 8, size=ntail)
+        c_rank[E - min(4, ntail):] = 0
+        c_rank[0] += M - c_rank.sum()
+        assert c_rank[0] >= 0
+    counts = np.zeros(E, dtype=np.int64)
+    counts[perm] = c_rank
+    assert counts.sum() == M
+    return counts
+
+
+# --------------------------------------------------------------------------
+# Workloads
+# --------------------------------------------------------------------------
+
+
+@dataclass
+class Op:
+    """One grouped-GEMM call.
+
+    kind 'mgemm': y[M,N] from a=x[M,K] and b=w ([E,N,K], or [E,K,N] when
+    transpose_B).  kind 'kgemm': dW[E,N,K] fp32 from a=grad[M,N], b=X[M,K].
+    ``a`` and ``b`` name tensors of the owning workload.
+    """
+
+    name: str
+    kind: str
+    a: str
+    b: str
+    N: int
+    K: int
+    transpose_B: bool = False
+
+    def flops(self, counts) -> int:
+        return 2 * int(np.sum(counts)) * self.N * self.K
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    E: int
+    M: int
+    counts: np.ndarray
+    tensors: dict = field(default_factory=dict)  # name -> (shape, std, stream)
+    ops: list = field(default_factory=list)
+
+    @property
+    def offsets(self) -> np.ndarray:
+        return offsets_from_counts(self.counts)
+
+    def tensor(self, name: str) -> np.ndarray:
+        shape, std, stream = self.tensors[name]
+        return normal_bf16(shape, std, self.seed, stream)
+
+    def op(self, name: str) -> Op:
+        for o in self.ops:
+            if o.name == name:
+                return o
+        raise KeyError(name)
+
+    def flops(self) -> int:
+        return sum(o.flops(self.counts) for o in self.ops)
+
+
+def _layer(name, seed, E, M, counts, d_model, d_ffn2, d_ffn):
+    """An MoE expert layer: gate-up [M,d_model]x[E,d_ffn2,d_model]^T, down
+    [M,d_ffn]x[E,d_model,d_ffn]^T, their input gradients and FP32 weight
+    gradients.  Activations and gradients ~N(0,1), weights ~N(0,1/K)."""
+    w = Workload(name, seed, E, M, counts)
+    w.tensors = {
+        "x": ((M, d_model), 1.0, 1),
+        "w13": ((E, d_ffn2, d_model), 1.0 / np.sqrt(d_model), 2),
+        "h": ((M, d_ffn), 1.0, 3),
+        "w2": ((E, d_model, d_ffn), 1.0 / np.sqrt(d_ffn), 4),
+        "dy13": ((M, d_ffn2), 1.0, 5),
+        "dy2": ((M, d_model), 1.0, 6),
+    }
+    w.ops = [
+        Op("fwd_gate_up", "mgemm", "x", "w13", N=d_ffn2, K=d_model),
+        Op("fwd_down", "mgemm", "h", "w2", N=d_model, K=d_ffn),
+        Op("dgrad_down", "mgemm", "dy2", "w2", N=d_ffn, K=d_model, transpose_B=True),
+        Op("dgrad_gate_up", "mgemm", "dy13", "w13", N=d_model, K=d_ffn2, transpose_B=True),
+        Op("wgrad_gw2", "kgemm", "dy2", "h", N=d_model, K=d_ffn),
+        Op("wgrad_gw13", "kgemm", "dy13", "x", N=d_ffn2, K=d_model),
+    ]
+    return w
+
+
+def tiny() -> Workload:
+    """E=4, K=256, N=128, M=512, expert 2 empty (seed 0)."""
+    c = counts_tiny(0)
+    w = Workload("tiny_E4_M512_N128_K256", 0, 4, 512, c)
+    w.tensors = {
+        "x": ((512, 256), 1.0, 1),
+        "w": ((4, 128, 256), 1.0 / 16.0, 2),
+        "grad": ((512, 128), 1.0, 3),
+    }
+    w.ops = [
+        Op("fwd", "mgemm", "x", "w", N=128, K=256),
+        Op("dgrad", "mgemm", "grad", "w", N=256, K=128, transpose_B=True),
+        Op("wgrad", "kgemm", "grad", "x", N=128, K=256),
+    ]
+    return w
+
+
+def uniform(g: int, m: int) -> Workload:
+    """g groups of m rows each, n=768, k=2048, forward only (seed 2)."""
+    c = np.full(g, m, dtype=np.int64)
+    w = Workload(f"uniform_g{g}_m{m}_n768_k2048", 2, g, g * m, c)
+    stream0 = 10 * g
+    w.tensors = {
+        "x": ((g * m, 2048), 1.0, stream0 + 1),
+        "w": ((g, 768, 2048), 1.0 / np.sqrt(2048), stream0 + 2),
+    }
+    w.ops = [Op("fwd", "mgemm", "x", "w", N=768, K=2048)]
+    return w
+
+
+def a3b_layer() -> Workload:
+    """30B-A3B expert layer on one GPU: 32 local experts, 32768 routed rows,
+    Dirichlet(2) counts, d_model 3072, expert FFN 1280 (seed 3)."""
+    c = counts_dirichlet(32, 32768, 2.0, 3)
+    return _layer("a3b_E32_M32768", 3, 32, 32768, c, 3072, 2560, 1280)
+
+
+def skewed(tail: bool = False) -> Workload:
+    """128 experts, 65536 rows, Zipf(1.2) counts over a seeded permutation
+    (seed 5); ``tail`` adds the tiny/empty-expert tail."""
+    c = counts_zipf(128, 65536, 1.2, 5, tail=tail)
+    name = "skewed_zipf_tail_E128_M65536" if tail else "skewed_zipf_E128_M65536"
+    return _layer(name, 5, 128, 65536, c, 3072, 2560, 1280)
+
+
+ALL = {
+    "tiny": tiny,
+    "uniform8": lambda: uniform(8, 4096),
+    "uniform16": lambda: uniform(16, 2048),
+    "a3b": a3b_layer,
+    "skewed": lambda: skewed(False),
+    "skewed_tail": lambda: skewed(True),
+}
