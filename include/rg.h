@@ -1,0 +1,135 @@
+/*
+ * rg.h -- C ABI of the GB300 (sm_103a) MoE grouped-GEMM library (librg.so).
+ *
+ * Two operations, after the RapidGEMM README, section "Kernels":
+ *
+ *   rg_mgemm  M-grouped BF16 GEMM for the forward pass and the input
+ *             gradient ("Mgemm": x [M,K], w [E,N,K], cumulative row offsets
+ *             with a leading zero, optional transpose of B).
+ *   rg_kgemm  K-grouped weight gradient with FP32 output ("Kgemm": grad and
+ *             X hold expert-grouped rows; dW[e] = grad[rows of e]^T X[rows of e]).
+ *
+ * Group boundaries may fall anywhere: they need not be multiples of any tile
+ * size, and groups may be empty.  The offsets vector stays on the device and
+ * is read only by the kernels, so no call synchronises with the host.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are dense and row-major.  "device" pointers must point to
+ *     memory of the current CUDA device; "host" pointers to host memory.
+ *   - The caller owns every buffer.  The library allocates no memory and keeps
+ *     no pointer after a call returns; a call only enqueues work on `stream`
+ *     and returns without waiting for it.
+ *   - Return values: RG_OK (0) or a negative RG_ERR_* code.  Argument errors
+ *     are detected before anything is enqueued.  Errors that only the GPU can
+ *     see (invalid offsets contents, a pipeline wait that ran out) are recorded
+ *     in a per-device status word read by rg_get_device_status().
+ *   - No C++ exception crosses this interface.
+ *   - Thread safety: calls may be made from several host threads.
+ */
+#ifndef RG_H_
+#define RG_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RG_OK 0
+#define RG_ERR_INVALID_ARG (-1) /* null/misaligned pointer, bad size or stride */
+#define RG_ERR_UNSUPPORTED (-2) /* device is not an sm_103 (GB300-class) GPU */
+#define RG_ERR_CUDA (-3)        /* a CUDA call failed; see rg_last_cuda_error() */
+
+/* Bits of the device status word (rg_get_device_status). */
+#define RG_DEV_BAD_OFFSETS 0x1u /* offsets[0] != 0, decreasing, or offsets[E] > M */
+#define RG_DEV_TIMEOUT 0x2u     /* a bounded pipeline wait ran out; the kernel stopped */
+
+/* Largest number of experts one call accepts. */
+#define RG_MAX_EXPERTS 1024
+
+/*
+ * rg_mgemm -- M-grouped GEMM, forward (transpose_B == 0) or input gradient
+ * (transpose_B != 0).  RapidGEMM README, "Kernels", Mgemm.
+ *
+ *   x        device, bf16 [M, K].
+ *   w        device, bf16 [E, N, K] when transpose_B == 0:  y = x . w[e]^T
+ *                    bf16 [E, K, N] when transpose_B != 0:  y = x . w[e]
+ *            (the second form reads a forward weight [E, N_fwd, K_fwd] as B
+ *            without transposing it: K = N_fwd, N = K_fwd).
+ *   offsets  device, int32 [E+1]; offsets[0] == 0, non-decreasing,
+ *            offsets[E] <= M.  Expert e owns rows offsets[e] .. offsets[e+1]-1.
+ *   y        device, bf16 [M, N].  Row r of expert e receives
+ *            y[r, n] = sum_k x[r, k] * B_e[k, n], accumulated in FP32 by the
+ *            tensor cores and rounded to bf16 (nearest even).  Rows
+ *            >= offsets[E] are not written.
+ *   E        1 .. RG_MAX_EXPERTS.   M  0 .. 2^31-1 (M == 0 enqueues nothing).
+ *   N, K     >= 8 and multiples of 8 (16-byte row strides).
+ *   x, w, y must be 16-byte aligned; offsets 4-byte aligned.
+ *   stream   CUDA stream (0 = legacy default stream).
+ *
+ * Invalid offsets contents do not fault: every CTA sees them, writes nothing
+ * and sets RG_DEV_BAD_OFFSETS.
+ */
+int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_t M,
+             int N, int K, int transpose_B, void* y, cudaStream_t stream);
+
+/*
+ * rg_kgemm -- K-grouped weight gradient with FP32 output.  RapidGEMM README,
+ * "Kernels", Kgemm.
+ *
+ *   grad     device, bf16 [M, N].
+ *   X        device, bf16 [M, K].
+ *   offsets  device, int32 [E+1], same rules as rg_mgemm (the README's
+ *            "cumulative expert row ends" are offsets[1..E]).
+ *   dW       device, fp32 [E, N, K], overwritten:
+ *            dW[e, n, k] = sum over rows r of expert e of grad[r, n] * X[r, k],
+ *            accumulated in FP32; an expert with no rows gets dW[e] = 0.
+ *            Rows >= offsets[E] are ignored.
+ *   E, M, N, K, alignment and stream as for rg_mgemm (dW 16-byte aligned).
+ *   M == 0 is valid and zeroes dW.
+ */
+int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M,
+             int N, int K, float* dW, cudaStream_t stream);
+
+/*
+ * rg_get_device_status -- synchronise `stream`, then return through
+ * *status (host pointer) the RG_DEV_* bits that kernels of this library set
+ * on the current device since the previous call, and clear them.
+ * Returns RG_OK, or RG_ERR_CUDA if the synchronisation or the read failed.
+ */
+int rg_get_device_status(cudaStream_t stream, uint32_t* status);
+
+/*
+ * rg_set_wait_timeout_ns -- bound, in nanoseconds, on any single pipeline
+ * wait inside the kernels (default 2e9).  A wait that runs out sets
+ * RG_DEV_TIMEOUT, the kernel drains its in-flight copies, frees its tensor
+ * memory and returns.  Takes effect for launches made after the call.
+ * Returns RG_ERR_INVALID_ARG for 0.
+ */
+int rg_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * rg_selftest_wait_timeout -- enqueue one CTA that waits on a pipeline
+ * barrier which nothing ever signals, bounded by `ns` nanoseconds, and report
+ * through *status (host pointer) the status bits it set (RG_DEV_TIMEOUT when
+ * the bound works).  Synchronises `stream`.  Exercises the timeout path
+ * without a fault or a hang.
+ */
+int rg_selftest_wait_timeout(uint64_t ns, cudaStream_t stream, uint32_t* status);
+
+/* CUDA error code (cudaError_t as int) behind the last RG_ERR_CUDA of the
+ * calling thread, 0 if none. */
+int rg_last_cuda_error(void);
+
+/* 1 if the current device can run the kernels (compute capability 10.3), else 0. */
+int rg_device_supported(void);
+
+/* Library version string, static storage. */
+const char* rg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RG_H_ */

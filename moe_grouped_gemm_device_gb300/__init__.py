@@ -1,0 +1,199 @@
+"""MoE grouped GEMM for GB300 (sm_103a): thin Python binding of librg.so.
+
+The binding only marshals arguments: it checks dtypes and shapes of torch
+tensors, passes their device pointers and the current CUDA stream to the C
+ABI declared in ``include/rg.h``, and turns error codes into exceptions.
+Every step of the computation runs in the library's CUDA kernels; there is
+no fallback path.  If the library is not built, ``load()`` raises.
+
+Operations (RapidGEMM README, "Kernels"):
+
+* ``mgemm(x, w, offsets, transpose_B=False)``: M-grouped GEMM for the forward
+  pass (``y[rows of e] = x[rows of e] @ w[e].T``, w ``[E,N,K]``) or the input
+  gradient (``transpose_B=True``: ``y = x @ w[e]``, w ``[E,K,N]``).
+* ``kgemm(grad, X, offsets)``: K-grouped weight gradient
+  ``dW[e] = grad[rows of e].T @ X[rows of e]`` in FP32.
+
+``offsets`` is a device int32 tensor ``[E+1]`` of cumulative row offsets
+with a leading zero.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+__all__ = ["load", "mgemm", "kgemm", "device_status", "set_wait_timeout_ns",
+           "selftest_wait_timeout", "RGError", "lib_path", "version",
+           "RG_DEV_BAD_OFFSETS", "RG_DEV_TIMEOUT", "EXPORTED_SYMBOLS"]
+
+RG_OK = 0
+RG_ERR_INVALID_ARG = -1
+RG_ERR_UNSUPPORTED = -2
+RG_ERR_CUDA = -3
+RG_DEV_BAD_OFFSETS = 0x1
+RG_DEV_TIMEOUT = 0x2
+RG_MAX_EXPERTS = 1024
+
+EXPORTED_SYMBOLS = ("rg_mgemm", "rg_kgemm", "rg_get_device_status", "rg_set_wait_timeout_ns",
+                    "rg_selftest_wait_timeout", "rg_last_cuda_error", "rg_device_supported",
+                    "rg_version")
+
+_ERRNAMES = {RG_ERR_INVALID_ARG: "RG_ERR_INVALID_ARG", RG_ERR_UNSUPPORTED: "RG_ERR_UNSUPPORTED",
+             RG_ERR_CUDA: "RG_ERR_CUDA"}
+
+_lib = None
+
+
+class RGError(RuntimeError):
+    def __init__(self, fn: str, code: int, cuda_error: int = 0):
+        self.code = code
+        self.cuda_error = cuda_error
+        msg = f"{fn} failed: {_ERRNAMES.get(code, code)}"
+        if code == RG_ERR_CUDA:
+            msg += f" (cudaError {cuda_error})"
+        super().__init__(msg)
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load librg.so (built in-tree by ``_build.build()``); raise if missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
+    lib.rg_mgemm.argtypes = [vp, vp, vp, i32, i64, i32, i32, i32, vp, vp]
+    lib.rg_mgemm.restype = i32
+    lib.rg_kgemm.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp]
+    lib.rg_kgemm.restype = i32
+    lib.rg_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.rg_get_device_status.restype = i32
+    lib.rg_set_wait_timeout_ns.argtypes = [u64]
+    lib.rg_set_wait_timeout_ns.restype = i32
+    lib.rg_selftest_wait_timeout.argtypes = [u64, vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.rg_selftest_wait_timeout.restype = i32
+    lib.rg_last_cuda_error.argtypes = []
+    lib.rg_last_cuda_error.restype = i32
+    lib.rg_device_supported.argtypes = []
+    lib.rg_device_supported.restype = i32
+    lib.rg_version.argtypes = []
+    lib.rg_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def version() -> str:
+    return load().rg_version().decode()
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != RG_OK:
+        raise RGError(fn, rc, load().rg_last_cuda_error() if rc == RG_ERR_CUDA else 0)
+
+
+def _stream_ptr(device, stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, ndim):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must be {ndim}-D, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def mgemm(x, w, offsets, transpose_B: bool = False, out=None, stream=None):
+    """M-grouped BF16 GEMM.  x [M,K] bf16, w [E,N,K] (or [E,K,N] with
+    transpose_B) bf16, offsets int32 [E+1]; returns y [M,N] bf16.  Rows of
+    ``out`` at or past offsets[E] are left as they were."""
+    import torch
+    _need(x, "x", torch.bfloat16, 2)
+    _need(w, "w", torch.bfloat16, 3)
+    _need(offsets, "offsets", torch.int32, 1)
+    M, K = x.shape
+    E = w.shape[0]
+    if transpose_B:
+        if w.shape[1] != K:
+            raise ValueError(f"w {tuple(w.shape)} does not match x {tuple(x.shape)} (want [E,K,N])")
+        N = w.shape[2]
+    else:
+        if w.shape[2] != K:
+            raise ValueError(f"w {tuple(w.shape)} does not match x {tuple(x.shape)} (want [E,N,K])")
+        N = w.shape[1]
+    if offsets.shape[0] != E + 1:
+        raise ValueError(f"offsets must have E+1 = {E + 1} entries")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(out, "out", torch.bfloat16, 2)
+        if tuple(out.shape) != (M, N):
+            raise ValueError(f"out must be [{M},{N}]")
+    lib = load()
+    with torch.cuda.device(x.device):
+        rc = lib.rg_mgemm(x.data_ptr(), w.data_ptr(), offsets.data_ptr(), E, M, N, K,
+                          int(bool(transpose_B)), out.data_ptr(), _stream_ptr(x.device, stream))
+    _check("rg_mgemm", rc)
+    return out
+
+
+def kgemm(grad, X, offsets, out=None, stream=None):
+    """K-grouped weight gradient.  grad [M,N] bf16, X [M,K] bf16, offsets
+    int32 [E+1]; returns dW [E,N,K] fp32 (overwritten)."""
+    import torch
+    _need(grad, "grad", torch.bfloat16, 2)
+    _need(X, "X", torch.bfloat16, 2)
+    _need(offsets, "offsets", torch.int32, 1)
+    M, N = grad.shape
+    if X.shape[0] != M:
+        raise ValueError("grad and X must have the same number of rows")
+    K = X.shape[1]
+    E = offsets.shape[0] - 1
+    if out is None:
+        out = torch.empty((E, N, K), dtype=torch.float32, device=grad.device)
+    else:
+        _need(out, "out", torch.float32, 3)
+        if tuple(out.shape) != (E, N, K):
+            raise ValueError(f"out must be [{E},{N},{K}]")
+    lib = load()
+    with torch.cuda.device(grad.device):
+        rc = lib.rg_kgemm(grad.data_ptr(), X.data_ptr(), offsets.data_ptr(), E, M, N, K,
+                          out.data_ptr(), _stream_ptr(grad.device, stream))
+    _check("rg_kgemm", rc)
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the RG_DEV_* bits."""
+    import torch
+    v = ctypes.c_uint32(0)
+    _check("rg_get_device_status", load().rg_get_device_status(_stream_ptr(torch.cuda.current_device(), stream), ctypes.byref(v)))
+    return int(v.value)
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _check("rg_set_wait_timeout_ns", load().rg_set_wait_timeout_ns(int(ns)))
+
+
+def selftest_wait_timeout(ns: int, stream=None) -> int:
+    import torch
+    v = ctypes.c_uint32(0)
+    _check("rg_selftest_wait_timeout",
+           load().rg_selftest_wait_timeout(int(ns), _stream_ptr(torch.cuda.current_device(), stream), ctypes.byref(v)))
+    return int(v.value)

@@ -1,0 +1,262 @@
+// C-ABI host layer of librg.so: argument validation, TMA tensor-map encoding,
+// per-device setup and kernel launch.  Declared in include/rg.h.
+//
+// Nothing here allocates device or host memory.  The per-device status word is
+// a module-scope __device__ variable (one instance per device context); its
+// device address is looked up once per device.  Tensor maps are encoded on
+// the host for every call and passed by value as kernel parameters, so no
+// host workspace outlives a call.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "rg.h"
+
+namespace {
+
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+thread_local int t_last_cuda_error = 0;
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  int num_sms = 0;
+  unsigned int* status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+int fail_cuda(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return RG_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Per-device one-time setup.  Returns RG_OK / RG_ERR_UNSUPPORTED / RG_ERR_CUDA
+// and, on success, the state of the current device.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return RG_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& ds = g_dev[dev];
+  if (!ds.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return fail_cuda(e);
+    ds.supported = (major == 10 && minor == 3);
+    ds.num_sms = sms;
+    if (ds.supported) {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) return fail_cuda(e);
+      ds.status = static_cast<unsigned int*>(p);
+      if ((e = rg::mgemm_setup()) != cudaSuccess) return fail_cuda(e);
+      if ((e = rg::kgemm_setup()) != cudaSuccess) return fail_cuda(e);
+      if (encode_fn() == nullptr) return fail_cuda(cudaErrorNotSupported);
+    }
+    ds.ready = true;
+  }
+  if (!ds.supported) return RG_ERR_UNSUPPORTED;
+  *out = &ds;
+  return RG_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Encode a tiled tensor map; dims/box innermost first, strides in bytes for
+// dims 1..rank-1.
+bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, const uint64_t* dims,
+            const uint64_t* strides, const uint32_t* box) {
+  const uint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+  const CUresult r = encode_fn()(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), dims,
+                                 strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int check_common(const int32_t* offsets, int E, int64_t M, int N, int K) {
+  if (offsets == nullptr || (reinterpret_cast<uintptr_t>(offsets) & 3u) != 0) return RG_ERR_INVALID_ARG;
+  if (E < 1 || E > RG_MAX_EXPERTS) return RG_ERR_INVALID_ARG;
+  if (M < 0 || M > INT32_MAX) return RG_ERR_INVALID_ARG;
+  if (N < 8 || K < 8 || (N % 8) != 0 || (K % 8) != 0) return RG_ERR_INVALID_ARG;
+  return RG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_t M, int N, int K,
+             int transpose_B, void* y, cudaStream_t stream) {
+  int rc = check_common(offsets, E, M, N, K);
+  if (rc != RG_OK) return rc;
+  if (w == nullptr || !aligned16(w)) return RG_ERR_INVALID_ARG;
+  if (M > 0 && (x == nullptr || y == nullptr || !aligned16(x) || !aligned16(y)))
+    return RG_ERR_INVALID_ARG;
+  // the tile list is indexed with 32-bit integers
+  const int64_t max_tiles = (M / rg::mg::BM + E) * ((N + rg::mg::BN - 1) / rg::mg::BN);
+  if (max_tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != RG_OK) return rc;
+  if (M == 0) return RG_OK;  // no rows, nothing to write
+
+  CUtensorMap tmA, tmB, tmY;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+    const uint64_t str[1] = {static_cast<uint64_t>(K) * 2};
+    const uint32_t box[2] = {64, rg::mg::BM};
+    if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, str, box)) return RG_ERR_INVALID_ARG;
+  }
+  if (!transpose_B) {  // w [E, N, K], K contiguous: one 64 x 256 box per stage
+    const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
+    const uint64_t str[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2};
+    const uint32_t box[3] = {64, rg::mg::BN, 1};
+    if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box)) return RG_ERR_INVALID_ARG;
+  } else {  // w [E, K, N], N contiguous: four 64-column boxes of 64 K rows per stage
+    const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(E)};
+    const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K) * N * 2};
+    const uint32_t box[3] = {64, rg::mg::BK, 1};
+    if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box)) return RG_ERR_INVALID_ARG;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+    const uint64_t str[1] = {static_cast<uint64_t>(N) * 2};
+    const uint32_t box[2] = {64, 32};
+    if (!encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, str, box)) return RG_ERR_INVALID_ARG;
+  }
+  rg::GroupArgs args;
+  args.offsets = offsets;
+  args.E = E;
+  args.M = static_cast<int>(M);
+  args.N = N;
+  args.K = K;
+  args.out = y;
+  args.status = ds->status;
+  args.wait_limit_ns = g_wait_limit_ns.load();
+  const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmB, tmY, args, ds->num_sms, stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return RG_OK;
+}
+
+int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,
+             float* dW, cudaStream_t stream) {
+  int rc = check_common(offsets, E, M, N, K);
+  if (rc != RG_OK) return rc;
+  if (dW == nullptr || !aligned16(dW)) return RG_ERR_INVALID_ARG;
+  if (M > 0 && (grad == nullptr || X == nullptr || !aligned16(grad) || !aligned16(X)))
+    return RG_ERR_INVALID_ARG;
+  const int64_t tiles = static_cast<int64_t>(E) * ((N + rg::kg::BM - 1) / rg::kg::BM) *
+                        ((K + rg::kg::BN - 1) / rg::kg::BN);
+  if (tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != RG_OK) return rc;
+
+  // With M == 0 every valid offsets vector is all zeros, so the kernel only
+  // writes zero tiles; the operand maps then describe one row of dW, which is
+  // never loaded.
+  const void* g_ptr = M > 0 ? grad : static_cast<const void*>(dW);
+  const void* x_ptr = M > 0 ? X : static_cast<const void*>(dW);
+  const uint64_t rows = M > 0 ? static_cast<uint64_t>(M) : 1;
+
+  CUtensorMap tmG, tmX, tmD;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(N), rows};
+    const uint64_t str[1] = {static_cast<uint64_t>(N) * 2};
+    const uint32_t box[2] = {64, rg::kg::BR};
+    if (!encode(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g_ptr, dims, str, box)) return RG_ERR_INVALID_ARG;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), rows};
+    const uint64_t str[1] = {static_cast<uint64_t>(K) * 2};
+    const uint32_t box[2] = {64, rg::kg::BR};
+    if (!encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x_ptr, dims, str, box)) return RG_ERR_INVALID_ARG;
+  }
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
+    const uint64_t str[2] = {static_cast<uint64_t>(K) * 4, static_cast<uint64_t>(N) * K * 4};
+    const uint32_t box[3] = {32, 32, 1};
+    if (!encode(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dW, dims, str, box)) return RG_ERR_INVALID_ARG;
+  }
+  rg::GroupArgs args;
+  args.offsets = offsets;
+  args.E = E;
+  args.M = static_cast<int>(M);
+  args.N = N;
+  args.K = K;
+  args.out = dW;
+  args.status = ds->status;
+  args.wait_limit_ns = g_wait_limit_ns.load();
+  const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->num_sms, stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return RG_OK;
+}
+
+int rg_get_device_status(cudaStream_t stream, uint32_t* status) {
+  if (status == nullptr) return RG_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != RG_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  unsigned int v = 0;
+  if ((e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof v)) != cudaSuccess) return fail_cuda(e);
+  const unsigned int zero = 0;
+  if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero)) != cudaSuccess) return fail_cuda(e);
+  *status = v;
+  return RG_OK;
+}
+
+int rg_set_wait_timeout_ns(uint64_t ns) {
+  if (ns == 0) return RG_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(ns);
+  return RG_OK;
+}
+
+int rg_selftest_wait_timeout(uint64_t ns, cudaStream_t stream, uint32_t* status) {
+  if (ns == 0 || status == nullptr) return RG_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != RG_OK) return rc;
+  uint32_t before = 0;
+  if ((rc = rg_get_device_status(stream, &before)) != RG_OK) return rc;
+  const cudaError_t e = rg::launch_wait_selftest(ds->status, ns, stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return rg_get_device_status(stream, status);
+}
+
+int rg_last_cuda_error(void) { return t_last_cuda_error; }
+
+int rg_device_supported(void) {
+  DeviceState* ds = nullptr;
+  return device_state(&ds) == RG_OK ? 1 : 0;
+}
+
+const char* rg_version(void) { return "rg 0.1.0 (sm_103a tcgen05 grouped GEMM)"; }
+
+}  // extern "C"

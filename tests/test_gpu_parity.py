@@ -1,0 +1,212 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs, at sizes the oracle finishes in seconds that still span
+several tiles with ragged tails, plus the edge cases of grouping."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from parity import (bf16_round_exact, check_bf16, check_fp32, offsets_dev, to_dev,
+                    to_host_bits)
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL_BF16 = 0x4640  # 12288.0
+
+
+def run_mgemm(rg, x, w, off, transpose_B, M, N, sentinel=True):
+    import torch
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    if sentinel:
+        y.view(torch.int16).fill_(SENTINEL_BF16)
+    rg.mgemm(to_dev(x), to_dev(w), offsets_dev(off), transpose_B=transpose_B, out=y)
+    torch.cuda.synchronize()
+    assert rg.device_status() == 0
+    return to_host_bits(y)
+
+
+def run_kgemm(rg, g, x, off, N, K):
+    import torch
+    E = len(off) - 1
+    dW = torch.full((E, N, K), float("nan"), dtype=torch.float32, device="cuda")
+    rg.kgemm(to_dev(g), to_dev(x), offsets_dev(off), out=dW)
+    torch.cuda.synchronize()
+    assert rg.device_status() == 0
+    return dW.cpu().numpy()
+
+
+def ints(shape, seed, stream):
+    return W.integer_bf16(shape, -2, 2, seed, stream)
+
+
+# ------------------------------------------------------------ exact integers
+
+
+INT_COUNTS = [130, 0, 1, 200]  # ragged, empty, single-row groups
+INT_TAIL = 7                   # rows past offsets[E]
+
+
+@pytest.mark.parametrize("transpose_B", [False, True], ids=["fwd", "dgrad"])
+def test_mgemm_integer_inputs_bit_exact(gpu_lib, transpose_B):
+    off = W.offsets_from_counts(INT_COUNTS)
+    M, N, K = int(off[-1]) + INT_TAIL, 384, 320
+    x = ints((M, K), 1, 0)
+    w = ints((4, K, N) if transpose_B else (4, N, K), 1, 1)
+    y = run_mgemm(gpu_lib, x, w, off, transpose_B, M, N)
+    ref = oracle.mgemm(x, w, off, transpose_B=transpose_B)
+    valid = int(off[-1])
+    np.testing.assert_array_equal(y[:valid], bf16_round_exact(ref[:valid]))
+    assert (y[valid:] == SENTINEL_BF16).all(), "rows past offsets[E] were written"
+
+
+def test_kgemm_integer_inputs_bit_exact(gpu_lib):
+    off = W.offsets_from_counts(INT_COUNTS)
+    M, N, K = int(off[-1]) + INT_TAIL, 384, 320
+    g = ints((M, N), 2, 0)
+    x = ints((M, K), 2, 1)
+    dW = run_kgemm(gpu_lib, g, x, off, N, K)
+    ref = oracle.kgemm(g, x, off)
+    np.testing.assert_array_equal(dW.astype(np.float64), ref)
+    assert (dW[1] == 0).all()
+
+
+# ------------------------------------------------------------ tiny workload
+
+
+@pytest.mark.parametrize("opname", ["fwd", "dgrad", "wgrad"])
+def test_tiny_workload(gpu_lib, opname):
+    wl = W.tiny()
+    op = wl.op(opname)
+    a, b = wl.tensor(op.a), wl.tensor(op.b)
+    off = wl.offsets
+    if op.kind == "mgemm":
+        y = run_mgemm(gpu_lib, a, b, off, op.transpose_B, wl.M, op.N)
+        ref = oracle.mgemm(a, b, off, transpose_B=op.transpose_B)
+        check_bf16(y, ref, opname)
+    else:
+        dW = run_kgemm(gpu_lib, a, b, off, op.N, op.K)
+        check_fp32(dW, oracle.kgemm(a, b, off), opname)
+        assert (dW[2] == 0).all()
+
+
+# ------------------------------------------------------------ edge cases
+
+EDGE = {
+    "single_expert": dict(counts=[300], tail=0, N=256, K=128),
+    "all_empty": dict(counts=[0, 0, 0], tail=64, N=128, K=64),
+    "sizes_1_127_128_129": dict(counts=[0, 1, 127, 128, 129, 0], tail=3, N=256, K=192),
+    "smallest_dims": dict(counts=[5, 0, 9], tail=2, N=8, K=8),
+    "ragged_N_K": dict(counts=[70, 190], tail=0, N=200, K=72),
+    "many_experts": dict(counts=list(np.random.default_rng(5).integers(0, 40, size=300)), tail=11, N=128, K=64),
+}
+
+
+@pytest.mark.parametrize("case", sorted(EDGE))
+@pytest.mark.parametrize("kind", ["fwd", "dgrad", "wgrad"])
+def test_edge_cases(gpu_lib, case, kind):
+    c = EDGE[case]
+    off = W.offsets_from_counts(c["counts"])
+    E = len(c["counts"])
+    M = int(off[-1]) + c["tail"]
+    N, K = c["N"], c["K"]
+    seed = 40 + sorted(EDGE).index(case)
+    if kind == "wgrad":
+        g = W.normal_bf16((M, N), 1.0, seed, 0)
+        x = W.normal_bf16((M, K), 1.0, seed, 1)
+        dW = run_kgemm(gpu_lib, g, x, off, N, K)
+        check_fp32(dW, oracle.kgemm(g, x, off), f"{case}/{kind}")
+        for e in range(E):
+            if c["counts"][e] == 0:
+                assert (dW[e] == 0).all()
+        return
+    tb = kind == "dgrad"
+    x = W.normal_bf16((M, K), 1.0, seed, 0)
+    w = W.normal_bf16((E, K, N) if tb else (E, N, K), 1.0 / np.sqrt(K), seed, 1)
+    y = run_mgemm(gpu_lib, x, w, off, tb, M, N)
+    valid = int(off[-1])
+    if valid:
+        check_bf16(y[:valid], oracle.mgemm(x, w, off, transpose_B=tb)[:valid], f"{case}/{kind}")
+    assert (y[valid:] == SENTINEL_BF16).all()
+
+
+def test_zero_rows(gpu_lib):
+    import torch
+    off = offsets_dev(np.zeros(4, dtype=np.int32))
+    w = torch.zeros((3, 64, 64), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    y = gpu_lib.mgemm(x, w, off)
+    assert y.shape == (0, 64)
+    dW = torch.full((3, 64, 64), float("nan"), device="cuda")
+    gpu_lib.kgemm(torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda"), x, off, out=dW)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    assert (dW == 0).all()
+
+
+# ------------------------------------------------------------ medium random
+
+
+def test_medium_random_all_ops(gpu_lib):
+    """E=8 Dirichlet-routed rows, several tiles in every dimension."""
+    counts = W.counts_dirichlet(8, 3000, 2.0, 21)
+    off = W.offsets_from_counts(counts)
+    M, D, F = 3000, 768, 512
+    x = W.normal_bf16((M, D), 1.0, 21, 1)
+    w = W.normal_bf16((8, F, D), 1.0 / np.sqrt(D), 21, 2)
+    dy = W.normal_bf16((M, F), 1.0, 21, 3)
+    y = run_mgemm(gpu_lib, x, w, off, False, M, F)
+    check_bf16(y, oracle.mgemm(x, w, off), "fwd")
+    dx = run_mgemm(gpu_lib, dy, w, off, True, M, D)
+    check_bf16(dx, oracle.mgemm(dy, w, off, transpose_B=True), "dgrad")
+    dW = run_kgemm(gpu_lib, dy, x, off, F, D)
+    check_fp32(dW, oracle.kgemm(dy, x, off), "wgrad")
+
+
+# ------------------------------------------------------------ status / robustness
+
+
+def test_bad_offsets_set_status_and_write_nothing(gpu_lib):
+    import torch
+    M, N, K = 64, 128, 64
+    x = to_dev(W.normal_bf16((M, K), 1.0, 7, 0))
+    w = to_dev(W.normal_bf16((2, N, K), 1.0, 7, 1))
+    for bad in ([0, 40, 30], [1, 10, 20], [0, 10, 65]):
+        y = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")
+        gpu_lib.mgemm(x, w, offsets_dev(np.array(bad)), out=y)
+        assert gpu_lib.device_status() & gpu_lib.RG_DEV_BAD_OFFSETS
+        assert (y == 3.0).all()
+        dW = torch.full((2, N, K), 5.0, device="cuda")
+        gpu_lib.kgemm(to_dev(W.normal_bf16((M, N), 1.0, 7, 2)), x, offsets_dev(np.array(bad)), out=dW)
+        assert gpu_lib.device_status() & gpu_lib.RG_DEV_BAD_OFFSETS
+        assert (dW == 5.0).all()
+    # the status was cleared and good calls still work
+    gpu_lib.mgemm(x, w, offsets_dev(np.array([0, 30, 64])))
+    assert gpu_lib.device_status() == 0
+
+
+def test_deterministic(gpu_lib):
+    import torch
+    wl = W.tiny()
+    x = to_dev(wl.tensor("x"))
+    w = to_dev(wl.tensor("w"))
+    g = to_dev(wl.tensor("grad"))
+    off = offsets_dev(wl.offsets)
+    y1, y2 = gpu_lib.mgemm(x, w, off), gpu_lib.mgemm(x, w, off)
+    d1, d2 = gpu_lib.kgemm(g, x, off), gpu_lib.kgemm(g, x, off)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(d1.view(torch.int32), d2.view(torch.int32))
+
+
+def test_bounded_wait_times_out_with_status(gpu_lib):
+    """A barrier nothing signals: the bounded wait gives up after ~50 ms and
+    reports RG_DEV_TIMEOUT; the context stays usable."""
+    import time
+    import torch
+    t0 = time.time()
+    st = gpu_lib.selftest_wait_timeout(50_000_000)
+    assert st == gpu_lib.RG_DEV_TIMEOUT
+    assert time.time() - t0 < 10
+    assert gpu_lib.device_status() == 0
+    a = torch.ones(4, device="cuda")
+    assert float(a.sum()) == 4.0
