@@ -1,0 +1,459 @@
+"""Benchmark of the MoE grouped GEMM path on GB300.
+
+One step is one pass of the whole path over one batch: the six grouped GEMMs
+of a 30B-A3B-shaped expert layer on one GPU (32 local experts, 32768 routed
+rows with Dirichlet(2) counts, d_model 3072, expert FFN 1280):
+
+    fwd  gate-up   y13 = x  . w13[e]^T     (M-grouped, N=2560, K=3072)
+    fwd  down      y2  = h  . w2[e]^T      (M-grouped, N=3072, K=1280)
+    dgrad down     dh  = dy2 . w2[e]       (M-grouped, transpose_B)
+    dgrad gate-up  dx  = dy13 . w13[e]     (M-grouped, transpose_B)
+    wgrad gw2      dW2[e]  = dy2[e]^T h[e]  (K-grouped, fp32)
+    wgrad gw13     dW13[e] = dy13[e]^T x[e] (K-grouped, fp32)
+
+Metric: grouped-GEMM TFLOP/s = sum over calls of 2*sum_e(M_e)*N*K / time.
+
+    python bench.py [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+prints one JSON line.  ``--impl reference`` times the CPU oracle on the same
+workload (a bounded sample of it per step) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+L2_BYTES = 129 * 2**20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_OF = {"mgemm": "mgemm_kernel<false>", "mgemm_t": "mgemm_kernel<true>", "kgemm": "kgemm_kernel"}
+KERNEL_SOURCES = {"mgemm_kernel<false>": "mgemm.cu", "mgemm_kernel<true>": "mgemm.cu",
+                  "kgemm_kernel": "kgemm.cu"}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="a3b", choices=sorted(W.ALL))
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU baseline budget")
+    p.add_argument("--ops", default="", help="comma-separated subset of the step's ops (profiling)")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_of(op) -> str:
+    if op.kind == "kgemm":
+        return KERNEL_OF["kgemm"]
+    return KERNEL_OF["mgemm_t" if op.transpose_B else "mgemm"]
+
+
+def algorithmic_bytes(op, counts) -> int:
+    M = int(np.sum(counts))
+    E = len(counts)
+    if op.kind == "kgemm":
+        return 2 * M * op.N + 2 * M * op.K + 4 * E * op.N * op.K
+    nonempty = int(np.count_nonzero(counts))
+    return 2 * M * op.K + 2 * op.N * op.K * nonempty + 2 * M * op.N
+
+
+def workload_desc(wl) -> str:
+    ops = ", ".join(f"{o.name}(N={o.N},K={o.K})" for o in wl.ops)
+    c = wl.counts
+    return (f"{wl.name}: E={wl.E}, M={wl.M}, rows/expert min {int(c.min())} max {int(c.max())}; "
+            f"one step = {ops}")
+
+
+def working_set_bytes(wl) -> int:
+    tot = 0
+    for name, (shape, _, _) in wl.tensors.items():
+        tot += 2 * int(np.prod(shape))
+    for op in wl.ops:
+        tot += (4 * wl.E * op.N * op.K) if op.kind == "kgemm" else 2 * wl.M * op.N
+    return tot
+
+
+# --------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.4)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [s.strip() for s in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+
+def oracle_sample_step(wl, tensors, budget_s: float, rng) -> tuple[float, float, str]:
+    """Run the oracle on a sample of every op's outputs; return (flops, seconds,
+    description).  Rows / (expert, n) pairs are drawn uniformly at random; the
+    count per op is sized to the time budget from a one-row probe."""
+    import oracle
+    off = wl.offsets
+    counts = wl.counts
+    per_op = budget_s / len(wl.ops)
+    flops = 0.0
+    secs = 0.0
+    desc = []
+    for op in wl.ops:
+        a, b = tensors[op.a], tensors[op.b]
+        if op.kind == "mgemm":
+            unit = 2.0 * op.N * op.K
+
+            def run(n):
+                rows = rng.integers(0, int(off[-1]), size=n)
+                oracle.mgemm(a, b, off, transpose_B=op.transpose_B, rows=rows)
+                return n * unit
+        else:
+            nz = np.flatnonzero(counts)
+
+            def run(n):
+                es = rng.choice(nz, size=n)
+                ns = rng.integers(0, op.N, size=n)
+                oracle.kgemm(a, b, off, sel=(es, ns))
+                return float(np.sum(2.0 * counts[es] * op.K))
+        t0 = time.perf_counter()
+        f = run(max(1, oracle.num_threads()))
+        dt = time.perf_counter() - t0
+        n = max(1, int(oracle.num_threads() * per_op / max(dt, 1e-6)))
+        t0 = time.perf_counter()
+        f = run(n)
+        dt = time.perf_counter() - t0
+        flops += f
+        secs += dt
+        desc.append(f"{op.name}:{n}")
+    return flops, secs, "random outputs per op (" + ", ".join(desc) + ")"
+
+
+def cpu_baseline(wl, tensors, budget_s: float) -> dict:
+    import oracle
+    rng = np.random.default_rng(1234)
+    flops, secs, desc = oracle_sample_step(wl, tensors, budget_s, rng)
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{desc}; Mgemm ops: sampled rows x all N; Kgemm ops: sampled (expert, n) "
+                      f"rows of dW x all K; {secs:.1f} s of FP64 CPU work"}
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    tensors = {k: wl.tensor(k) for k in wl.tensors}
+    per_step = max(0.05, min(2.0, 90.0 / max(1, args.steps + args.warmup)))
+    rng = np.random.default_rng(99)
+    for _ in range(args.warmup):
+        oracle_sample_step(wl, tensors, per_step, rng)
+    tot_f, tot_s, desc = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        f, s, desc = oracle_sample_step(wl, tensors, per_step, rng)
+        tot_f += f
+        tot_s += s
+    import oracle
+    value = tot_f / tot_s / 1e12
+    line = {
+        "impl": "reference", "metric": "grouped GEMM TFLOP/s (fwd/dgrad/wgrad), 1 GPU",
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * wl.flops() / (value * 1e12),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(wl)},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": f"each step: {desc}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU path
+
+
+def traffic_for(kernel: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current source of that kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    ent = d.get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "moe_grouped_gemm_device_gb300", "csrc", KERNEL_SOURCES[kernel])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if ent.get("source_sha256_16") != h:
+        return None
+    return ent.get("bytes_per_launch")
+
+
+def main():
+    args = parse()
+    wl = W.ALL[args.workload]()
+    if args.ops:
+        keep = args.ops.split(",")
+        wl.ops = [o for o in wl.ops if o.name in keep]
+        assert wl.ops, f"no op of {wl.name} matches {keep}"
+        used = {o.a for o in wl.ops} | {o.b for o in wl.ops}
+        wl.tensors = {k: v for k, v in wl.tensors.items() if k in used}
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    import moe_grouped_gemm_device_gb300 as rg
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rg.load()
+
+    # ---- inputs: seeded on the host, then resident in HBM -------------------
+    host = {k: wl.tensor(k) for k in wl.tensors}
+    off_np = wl.offsets
+    counts = wl.counts
+
+    def dev_bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    d = {k: dev_bf16(v) for k, v in host.items()}
+    off = torch.from_numpy(off_np).to(dev)
+    outs = {}
+    for op in wl.ops:
+        if op.kind == "kgemm":
+            outs[op.name] = torch.empty((wl.E, op.N, op.K), dtype=torch.float32, device=dev)
+        else:
+            outs[op.name] = torch.empty((wl.M, op.N), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(op, tens, out):
+        if op.kind == "kgemm":
+            rg.kgemm(tens[op.a], tens[op.b], off_used[0], out=out)
+        else:
+            rg.mgemm(tens[op.a], tens[op.b], off_used[0], transpose_B=op.transpose_B, out=out)
+
+    off_used = [off]
+    nops = len(wl.ops)
+
+    def step(evs=None):
+        for i, op in enumerate(wl.ops):
+            if evs is not None:
+                evs[i].record(stream)
+            call(op, d, outs[op.name])
+        if evs is not None:
+            evs[nops].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = rg.device_status()
+    if status:
+        raise SystemExit(f"device status {status:#x} after warm-up")
+
+    # ---- timed region -------------------------------------------------------
+    # Events around every launch, on the launching stream, give the per-kernel
+    # durations of the timed steps themselves.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nops + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        step(evs[s])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = evs[0][0].elapsed_time(evs[-1][nops])
+    clocks = sampler.stop() if sampler else None
+    status = rg.device_status()
+    if status:
+        raise SystemExit(f"device status {status:#x} after timed region")
+    per_op_ms = np.zeros(nops)
+    for e in evs:
+        per_op_ms += np.array([e[i].elapsed_time(e[i + 1]) for i in range(nops)])
+    per_op_ms /= args.steps
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    flops_step = wl.flops()
+    value = world * flops_step / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers ---------------
+    e2e = None
+    if rank == 0 and args.e2e_steps > 0:
+        pin = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+               for k, v in host.items()}
+        pin_off = torch.from_numpy(off_np).pin_memory()
+        pin_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+        h2d = sum(t.numel() * t.element_size() for t in pin.values()) + pin_off.numel() * 4
+        d2h = sum(t.numel() * t.element_size() for t in pin_out.values())
+
+        def e2e_step():
+            for k, t in pin.items():
+                d[k].copy_(t, non_blocking=True)
+            off_used[0].copy_(pin_off, non_blocking=True)
+            for op in wl.ops:
+                call(op, d, outs[op.name])
+            for k, t in outs.items():
+                pin_out[k].copy_(t, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b) / args.e2e_steps
+        e2e = {"value": flops_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e_ms}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel ------------------------------------
+    peaks, peak_src = load_peaks()
+    per_kernel = {}
+    per_op = {}
+    for i, op in enumerate(wl.ops):
+        k = kernel_of(op)
+        f = op.flops(counts)
+        ent = per_kernel.setdefault(k, {"ms": 0.0, "flops": 0, "bytes": 0, "launches": 0})
+        ent["ms"] += per_op_ms[i]
+        ent["flops"] += f
+        ent["bytes"] += algorithmic_bytes(op, counts)
+        ent["launches"] += 1
+        per_op[op.name] = {"ms": round(float(per_op_ms[i]), 4),
+                           "tflops": round(f / (per_op_ms[i] * 1e-3) / 1e12, 1),
+                           "pct_peak_sustained": round(100 * f / (per_op_ms[i] * 1e-3) / 1e12
+                                                       / peaks["bf16_tflops_sustained"], 1)}
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
+    de = per_kernel[dom]
+    achieved = de["flops"] / (de["ms"] * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    traffic = traffic_for(dom)
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": dom, "launches_per_step": de["launches"],
+                "algorithmic_flops_per_launch": de["flops"] // de["launches"],
+                "algorithmic_bytes_per_launch": de["bytes"] // de["launches"],
+                "peak_source": f"{peak_src} bf16 sustained (MEASURED_PEAKS.json)" if peak_src == "measured"
+                else "fallback 1.7 PFLOP/s sustained",
+                "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
+                "share_of_step": round(de["ms"] / float(per_op_ms.sum()), 3)}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(wl, host, args.cpu_seconds)
+
+    line = {
+        "metric": "grouped GEMM TFLOP/s (fwd/dgrad/wgrad), 1 GPU",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded normal inputs, random-init weights)",
+        "config": {"workload": workload_desc(wl),
+                   "flops_per_step": flops_step,
+                   "l2": f"inputs larger than L2: step working set {working_set_bytes(wl) / 1e9:.2f} GB vs 129 MB L2",
+                   "pct_of_peak_sustained": round(100 * value / world / peak, 1)},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": nops * args.steps,
+        "clocks": clocks,
+        "per_op": per_op,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -44,6 +44,7 @@ extern "C" {
 /* Bits of the device status word (rg_get_device_status). */
 #define RG_DEV_BAD_OFFSETS 0x1u /* offsets[0] != 0, decreasing, or offsets[E] > M */
 #define RG_DEV_TIMEOUT 0x2u     /* a bounded pipeline wait ran out; the kernel stopped */
+#define RG_DEV_LAUNCH_CONFIG 0x4u /* shared-memory window misaligned; the kernel did nothing */
 
 /* Largest number of experts one call accepts. */
 #define RG_MAX_EXPERTS 1024
@@ -84,7 +85,9 @@ int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_
  *            "cumulative expert row ends" are offsets[1..E]).
  *   dW       device, fp32 [E, N, K], overwritten:
  *            dW[e, n, k] = sum over rows r of expert e of grad[r, n] * X[r, k],
- *            accumulated in FP32; an expert with no rows gets dW[e] = 0.
+ *            accumulated in FP32 by the tensor cores over chunks of at most
+ *            4096 rows, whose partial sums are added in FP32 in row order
+ *            (deterministic); an expert with no rows gets dW[e] = 0.
  *            Rows >= offsets[E] are ignored.
  *   E, M, N, K, alignment and stream as for rg_mgemm (dW 16-byte aligned).
  *   M == 0 is valid and zeroes dW.

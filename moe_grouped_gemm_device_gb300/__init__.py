@@ -34,6 +34,7 @@ RG_ERR_UNSUPPORTED = -2
 RG_ERR_CUDA = -3
 RG_DEV_BAD_OFFSETS = 0x1
 RG_DEV_TIMEOUT = 0x2
+RG_DEV_LAUNCH_CONFIG = 0x4
 RG_MAX_EXPERTS = 1024
 
 EXPORTED_SYMBOLS = ("rg_mgemm", "rg_kgemm", "rg_get_device_status", "rg_set_wait_timeout_ns",

@@ -30,6 +30,7 @@ struct DeviceState {
   bool ready = false;
   bool supported = false;
   int num_sms = 0;
+  size_t max_smem = 0;  // opt-in dynamic shared memory per block
   unsigned int* status = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
@@ -64,19 +65,21 @@ int device_state(DeviceState** out) {
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& ds = g_dev[dev];
   if (!ds.ready) {
-    int major = 0, minor = 0, sms = 0;
+    int major = 0, minor = 0, sms = 0, smem = 0;
     if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
       return fail_cuda(e);
     ds.supported = (major == 10 && minor == 3);
     ds.num_sms = sms;
+    ds.max_smem = static_cast<size_t>(smem);
     if (ds.supported) {
       void* p = nullptr;
       if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) return fail_cuda(e);
       ds.status = static_cast<unsigned int*>(p);
-      if ((e = rg::mgemm_setup()) != cudaSuccess) return fail_cuda(e);
-      if ((e = rg::kgemm_setup()) != cudaSuccess) return fail_cuda(e);
+      if ((e = rg::mgemm_setup(smem)) != cudaSuccess) return fail_cuda(e);
+      if ((e = rg::kgemm_setup(smem)) != cudaSuccess) return fail_cuda(e);
       if (encode_fn() == nullptr) return fail_cuda(cudaErrorNotSupported);
     }
     ds.ready = true;
@@ -124,6 +127,7 @@ int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_
   if (max_tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != RG_OK) return rc;
+  if (rg::mgemm_smem_bytes(E) > ds->max_smem) return RG_ERR_INVALID_ARG;  // too many experts
   if (M == 0) return RG_OK;  // no rows, nothing to write
 
   CUtensorMap tmA, tmB, tmY;
@@ -176,6 +180,7 @@ int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int
   if (tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != RG_OK) return rc;
+  if (rg::kgemm_smem_bytes(E) > ds->max_smem) return RG_ERR_INVALID_ARG;  // too many experts
 
   // With M == 0 every valid offsets vector is all zeros, so the kernel only
   // writes zero tiles; the operand maps then describe one row of dW, which is

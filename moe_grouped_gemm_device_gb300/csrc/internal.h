@@ -28,20 +28,32 @@ constexpr int EPI_WARPS = 4, EPI_BUFS = 1, EPI_BUF_BYTES = 32 * 128;
 constexpr int THREADS = 192;
 }  // namespace mg
 
+#ifndef RG_KG_STAGES
+#define RG_KG_STAGES 4
+#endif
+#ifndef RG_KG_EPI_BUFS
+#define RG_KG_EPI_BUFS 1
+#endif
 namespace kg {
-constexpr int BM = 128, BN = 256, BR = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BR = 64, STAGES = RG_KG_STAGES;
 constexpr int A_BYTES = BM * BR * 2, B_BYTES = BN * BR * 2, STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_WARPS = 4, EPI_BUFS = 1, EPI_BUF_BYTES = 32 * 128;
+constexpr int EPI_WARPS = 4, EPI_BUFS = RG_KG_EPI_BUFS, EPI_BUF_BYTES = 32 * 128;
 constexpr int THREADS = 192;
+// Rows of one expert accumulated in tensor memory before the partial sum is
+// folded into dW (store for the first chunk, fp32 reduce-add for the rest).
+// Bounds the length of each fp32 accumulation chain inside the tensor cores.
+constexpr int CHUNK_ROWS = 4096;
+static_assert(CHUNK_ROWS % BR == 0, "chunks must hold whole row blocks");
 }  // namespace kg
 
 // Bytes of dynamic shared memory a launch with E experts needs.
 size_t mgemm_smem_bytes(int E);
 size_t kgemm_smem_bytes(int E);
 
-// One-time per-device kernel attribute setup (max dynamic shared memory).
-cudaError_t mgemm_setup();
-cudaError_t kgemm_setup();
+// One-time per-device kernel attribute setup: allow up to `max_smem` bytes
+// of dynamic shared memory (the device's opt-in limit).
+cudaError_t mgemm_setup(int max_smem);
+cudaError_t kgemm_setup(int max_smem);
 
 cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmY, const GroupArgs& args, int grid,

@@ -17,10 +17,17 @@
 //     zeroes them in shared memory (both operands, so no NaN/Inf can leak)
 //     and fences them into the async proxy before issuing the MMAs.
 //   * The fp32 accumulator (128 lanes x 256 columns, double-buffered in
-//     tensor memory) is written unrounded: tcgen05.ld -> swizzled shared
-//     memory -> TMA store of 32x32 fp32 boxes.  Experts without rows produce
-//     zero tiles without touching the tensor cores.
+//     tensor memory) holds at most CHUNK_ROWS rows of one expert: a longer
+//     expert is summed chunk by chunk, the first chunk's partial stored to dW
+//     and each later one added to it by a TMA fp32 reduce-add, in order.  This
+//     bounds the fp32 accumulation chain inside the tensor cores (whose error
+//     grows with its length) without any scratch memory.  The path to dW is
+//     tcgen05.ld -> swizzled shared memory -> TMA store / reduce-add of 32x32
+//     fp32 boxes.  Experts without rows produce zero tiles without touching
+//     the tensor cores.
 //   * Same bounded-wait / abort / drain scheme as the M-grouped kernel.
+#include <algorithm>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -30,7 +37,9 @@ namespace {
 using namespace kg;
 
 constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr int SMEM_FIXED = 1024 + STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES +
+// The dynamic shared-memory window of a CTA without static shared memory
+// starts 1024-byte aligned; the kernel checks this instead of padding for it.
+constexpr int SMEM_FIXED = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES +
                            NUM_BARS * 8 + 16;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BOX_BYTES = BR * 128;  // one 64-element-wide box of BR rows
@@ -38,10 +47,12 @@ constexpr int BOX_BYTES = BR * 128;  // one 64-element-wide box of BR rows
 __global__ void __launch_bounds__(THREADS, 1)
     kgemm_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmX,
                  const __grid_constant__ CUtensorMap tmD, const GroupArgs args) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {  // swizzled TMA boxes and MMA descriptors need 1024-byte alignment
+    if (threadIdx.x == 0) atomicOr(args.status, kDevLaunchConfig);
+    return;
+  }
 
   uint8_t* epi = smem + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES);
@@ -162,56 +173,60 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t phase = 0;
     int acc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
       const int e = s_ord[t / tpe];
       const int r_begin = s_off[e], r_end = s_off[e + 1];
-      if (r_end == r_begin) continue;  // zero tile: no MMA, no accumulator
-      const int buf = acc & 1;
-      const uint32_t tph = (acc >> 1) & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(guard, tempty_bar(buf), tph ^ 1u));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem + buf * BN;
-      for (int r = r_begin; r < r_end; r += BR) {
-        ok = __all_sync(0xffffffffu, mbar_wait(guard, full_bar(stage), phase));
+      // zero tile (no rows): no MMA, no accumulator.  Otherwise one
+      // accumulator per chunk of at most CHUNK_ROWS rows.
+      for (int cr = r_begin; cr < r_end && ok; cr += CHUNK_ROWS) {
+        const int c_end = min(r_end, cr + CHUNK_ROWS);
+        const int buf = acc & 1;
+        const uint32_t tph = (acc >> 1) & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(guard, tempty_bar(buf), tph ^ 1u));
         if (!ok) break;
-        const int valid = min(BR, r_end - r);
-        if (valid < BR) {
-          // rows [valid, BR) belong to the next expert (or lie past M): zero
-          // them in all six boxes of the stage before the tensor cores read it
-          uint8_t* st = smem + stage * STAGE_BYTES;
-          const int units = (BR - valid) * 8;  // 16-byte units per box
-          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 1
-          for (int b = 0; b < STAGE_BYTES / BOX_BYTES; ++b) {
-            uint4* bp = reinterpret_cast<uint4*>(st + b * BOX_BYTES + valid * 128);
-            for (int u = lane; u < units; u += 32) bp[u] = z;
-          }
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-          for (int k = 0; k < BR / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(sa + 2048 * k, BOX_BYTES, 1024);
-            const uint64_t bd = sdesc_sw128(sb + 2048 * k, BOX_BYTES, 1024);
-            umma_bf16(d_tmem, ad, bd, IDESC, (r != r_begin) | (k != 0));
+        const uint32_t d_tmem = tmem + buf * BN;
+        for (int r = cr; r < c_end; r += BR) {
+          ok = __all_sync(0xffffffffu, mbar_wait(guard, full_bar(stage), phase));
+          if (!ok) break;
+          const int valid = min(BR, r_end - r);
+          if (valid < BR) {
+            // rows [valid, BR) belong to the next expert (or lie past M): zero
+            // them in all six boxes of the stage before the tensor cores read it
+            uint8_t* st = smem + stage * STAGE_BYTES;
+            const int units = (BR - valid) * 8;  // 16-byte units per box
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+            for (int b = 0; b < STAGE_BYTES / BOX_BYTES; ++b) {
+              uint4* bp = reinterpret_cast<uint4*>(st + b * BOX_BYTES + valid * 128);
+              for (int u = lane; u < units; u += 32) bp[u] = z;
+            }
+            fence_proxy_async_smem();
           }
-          umma_commit(empty_bar(stage));
+          __syncwarp();
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = sbase + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BR / 16; ++k) {
+              const uint64_t ad = sdesc_sw128(sa + 2048 * k, BOX_BYTES, 1024);
+              const uint64_t bd = sdesc_sw128(sb + 2048 * k, BOX_BYTES, 1024);
+              umma_bf16(d_tmem, ad, bd, IDESC, (r != cr) | (k != 0));
+            }
+            umma_commit(empty_bar(stage));
+          }
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
+        if (!ok) break;
+        if (lane == 0) umma_commit(tfull_bar(buf));
         __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        ++acc;
       }
-      if (!ok) break;
-      if (lane == 0) umma_commit(tfull_bar(buf));
-      __syncwarp();
-      ++acc;
     }
     if (!ok && lane == 0) {
       umma_commit(drain_bar);
@@ -220,63 +235,80 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else {
     // ======================= epilogue (warps 2..5) ===========================
+    // Warp q owns rows n0 + 32q .. +31 of the tile; each 32x32 fp32 box goes
+    // through one of EPI_BUFS rotating staging buffers.  The first chunk of
+    // an expert's rows is stored, later chunks are reduce-added; before a
+    // later chunk the warp waits until its previous writes have landed, so
+    // the adds are applied in chunk order (deterministic).
     const int q = warp & 3;
-    uint8_t* ebuf = epi + (warp - 2) * EPI_BUFS * EPI_BUF_BYTES;
-    const uint32_t ebuf_s = smem_u32(ebuf);
-    uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * 128);
+    uint8_t* ebase = epi + (warp - 2) * EPI_BUFS * EPI_BUF_BYTES;
     int acc = 0;
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    uint32_t nstore = 0;
+    bool ok = true;
+    auto stage_buf = [&](const uint32_t (&v)[32]) -> uint32_t {
+      const uint32_t b = nstore % EPI_BUFS;
+      if (lane == 0) bulk_wait_read<EPI_BUFS - 1>();  // buffer b is no longer read
+      __syncwarp();
+      uint4* rowp = reinterpret_cast<uint4*>(ebase + b * EPI_BUF_BYTES + lane * 128);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        rowp[j ^ (lane & 7)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      ++nstore;
+      return smem_u32(ebase + b * EPI_BUF_BYTES);
+    };
+    for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
       const int p = t / tpe;
       const int e = s_ord[p];
       const int local = t - p * tpe;
       const int n0 = (local / nbk) * BM;
       const int k0 = (local % nbk) * BN;
-      const bool empty = s_off[e + 1] == s_off[e];
+      const int r_begin = s_off[e], r_end = s_off[e + 1];
       const bool warp_rows = n0 + q * 32 < N;  // this warp's 32 rows of dW exist
-      if (empty) {
+      if (r_end == r_begin) {  // expert without rows: dW tile = 0
         if (!warp_rows) continue;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          if (k0 + 32 * c >= K) break;
-          if (lane == 0) bulk_wait_read<0>();
-          __syncwarp();
+        uint32_t z[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) rowp[j] = make_uint4(0u, 0u, 0u, 0u);
-          fence_proxy_async_smem();
-          __syncwarp();
+        for (int j = 0; j < 32; ++j) z[j] = 0u;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32 && k0 + 32 * c < K; ++c) {
+          const uint32_t src = stage_buf(z);
           if (lane == 0) {
-            tma_store_3d(&tmD, ebuf_s, k0 + 32 * c, n0 + q * 32, e);
+            tma_store_3d(&tmD, src, k0 + 32 * c, n0 + q * 32, e);
             bulk_commit();
           }
         }
         continue;
       }
-      const int buf = acc & 1;
-      const uint32_t tph = (acc >> 1) & 1;
-      ++acc;
-      if (!__all_sync(0xffffffffu, mbar_wait(guard, tfull_bar(buf), tph))) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+      for (int cr = r_begin; cr < r_end; cr += CHUNK_ROWS) {
+        const bool first = cr == r_begin;
+        const int buf = acc & 1;
+        const uint32_t tph = (acc >> 1) & 1;
+        ++acc;
+        ok = __all_sync(0xffffffffu, mbar_wait(guard, tfull_bar(buf), tph));
+        if (!ok) break;
+        tc_fence_after();
+        if (!first && lane == 0) bulk_wait<0>();  // previous partial of this tile is in dW
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr + 32 * c, v);
-        tmem_ld_wait();
-        if (c == BN / 32 - 1) {
-          tc_fence_before();
-          mbar_arrive(tempty_bar(buf));
-        }
-        if (!warp_rows || k0 + 32 * c >= K) continue;
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          rowp[j ^ (lane & 7)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&tmD, ebuf_s, k0 + 32 * c, n0 + q * 32, e);
-          bulk_commit();
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + 32 * c, v);
+          tmem_ld_wait();
+          if (c == BN / 32 - 1) {  // accumulator fully read: hand it back
+            tc_fence_before();
+            mbar_arrive(tempty_bar(buf));
+          }
+          if (!warp_rows || k0 + 32 * c >= K) continue;
+          const uint32_t src = stage_buf(v);
+          if (lane == 0) {
+            if (first)
+              tma_store_3d(&tmD, src, k0 + 32 * c, n0 + q * 32, e);
+            else
+              tma_reduce_add_3d(&tmD, src, k0 + 32 * c, n0 + q * 32, e);
+            bulk_commit();
+          }
         }
       }
     }
@@ -311,9 +343,9 @@ __global__ void wait_selftest_kernel(unsigned int* status, unsigned long long li
 
 size_t kgemm_smem_bytes(int E) { return SMEM_FIXED + (2 * static_cast<size_t>(E) + 1) * 4; }
 
-cudaError_t kgemm_setup() {
+cudaError_t kgemm_setup(int max_smem) {
   return cudaFuncSetAttribute(kgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kgemm_smem_bytes(1024)));
+                              static_cast<int>(std::min<size_t>(kgemm_smem_bytes(1024), max_smem)));
 }
 
 cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,

@@ -25,6 +25,8 @@
 //   * Every mbarrier wait is bounded (WaitGuard).  A wait that runs out sets
 //     the device status, all roles stop, in-flight copies and MMAs are drained
 //     with bounded waits, and tensor memory is freed before the CTA exits.
+#include <algorithm>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -293,8 +295,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 size_t mgemm_smem_bytes(int E) { return SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4; }
 
-cudaError_t mgemm_setup() {
-  const int max_bytes = static_cast<int>(mgemm_smem_bytes(1024));
+cudaError_t mgemm_setup(int max_smem) {
+  const int max_bytes = static_cast<int>(std::min<size_t>(mgemm_smem_bytes(1024), max_smem));
   cudaError_t e = cudaFuncSetAttribute(mgemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(mgemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);

@@ -14,6 +14,7 @@ namespace rg {
 // Device status bits (mirrors RG_DEV_* in rg.h).
 constexpr unsigned int kDevBadOffsets = 0x1u;
 constexpr unsigned int kDevTimeout = 0x2u;
+constexpr unsigned int kDevLaunchConfig = 0x4u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -133,6 +134,16 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src,
   asm volatile(
       "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// dW[box] += smem box, fp32 add performed by the TMA unit (round to nearest).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t src, int32_t c0,
+                                                  int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(m)),
       "r"(src), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }

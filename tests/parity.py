@@ -9,6 +9,9 @@ Tolerances (from the specification of the grouped GEMM):
     on the same bf16 inputs.  Products of bf16 values are exact in fp32, so the
     error is that of fp32 accumulation over at most one expert's rows.
 """
+import json
+import os
+
 import numpy as np
 
 import workloads as W
@@ -39,12 +42,20 @@ def rel_fro(g: np.ndarray, r: np.ndarray) -> float:
     return float(ne / nr) if nr > 0 else float(ne)
 
 
+def _log(what: str, rec: dict) -> None:
+    path = os.environ.get("RG_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": what, **rec}) + "\n")
+
+
 def check_bf16(gpu_bits: np.ndarray, ref: np.ndarray, what: str = "") -> dict:
     g = W.bf16_bits_to_f32(gpu_bits).astype(np.float64)
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     fro = rel_fro(g, ref)
     err = np.abs(g - ref)
     worst = float(np.max(err / (np.abs(ref) + 1))) if err.size else 0.0
+    _log(what, {"rel_fro": fro, "elem": worst, "tol_fro": BF16_REL_FRO, "tol_elem": BF16_ELEM})
     assert fro <= BF16_REL_FRO, f"{what}: relative Frobenius error {fro:.3e} > {BF16_REL_FRO}"
     assert worst <= BF16_ELEM, f"{what}: element error {worst:.3e}*(|ref|+1) > {BF16_ELEM}"
     return {"rel_fro": fro, "elem": worst}
@@ -54,6 +65,7 @@ def check_fp32(gpu: np.ndarray, ref: np.ndarray, what: str = "") -> dict:
     g = np.asarray(gpu, dtype=np.float64)
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     fro = rel_fro(g, ref)
+    _log(what, {"rel_fro": fro, "tol_fro": FP32_REL_FRO})
     assert fro <= FP32_REL_FRO, f"{what}: relative Frobenius error {fro:.3e} > {FP32_REL_FRO}"
     return {"rel_fro": fro}
 

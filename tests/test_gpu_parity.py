@@ -70,6 +70,28 @@ def test_kgemm_integer_inputs_bit_exact(gpu_lib):
     assert (dW[1] == 0).all()
 
 
+def test_kgemm_long_experts_bit_exact(gpu_lib):
+    """Experts longer than one accumulation chunk (4096 rows): the partial
+    sums folded into dW must reproduce the exact integer result."""
+    counts = [9000, 0, 4100, 37, 8192]
+    off = W.offsets_from_counts(counts)
+    M, N, K = int(off[-1]) + 5, 256, 320
+    g = ints((M, N), 3, 0)
+    x = ints((M, K), 3, 1)
+    dW = run_kgemm(gpu_lib, g, x, off, N, K)
+    np.testing.assert_array_equal(dW.astype(np.float64), oracle.kgemm(g, x, off))
+
+
+def test_kgemm_long_experts_random(gpu_lib):
+    counts = [12000, 5000, 4096, 4097]
+    off = W.offsets_from_counts(counts)
+    M, N, K = int(off[-1]), 384, 256
+    g = W.normal_bf16((M, N), 1.0, 31, 0)
+    x = W.normal_bf16((M, K), 1.0, 31, 1)
+    dW = run_kgemm(gpu_lib, g, x, off, N, K)
+    check_fp32(dW, oracle.kgemm(g, x, off), "long experts")
+
+
 # ------------------------------------------------------------ tiny workload
 
 
