@@ -6,6 +6,7 @@
 // device address is looked up once per device.  Tensor maps are encoded on
 // the host for every call and passed by value as kernel parameters, so no
 // host workspace outlives a call.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -30,6 +31,8 @@ struct DeviceState {
   bool ready = false;
   bool supported = false;
   int num_sms = 0;
+  int mg_grid = 0;      // persistent grid of each kernel (CTAs)
+  int kg_grid = 0;
   size_t max_smem = 0;  // opt-in dynamic shared memory per block
   unsigned int* status = nullptr;
 };
@@ -81,6 +84,17 @@ int device_state(DeviceState** out) {
       if ((e = rg::mgemm_setup(smem)) != cudaSuccess) return fail_cuda(e);
       if ((e = rg::kgemm_setup(smem)) != cudaSuccess) return fail_cuda(e);
       if (encode_fn() == nullptr) return fail_cuda(cudaErrorNotSupported);
+      // One CTA per SM (shared memory limits residency to one); with CTA
+      // pairs, as many 2-CTA clusters as can be resident at once.
+      ds.mg_grid = ds.kg_grid = sms;
+      if (rg::kCtaGroup == 2) {
+        int mc = 0, kc = 0;
+        if ((e = rg::mgemm_max_clusters(&mc, smem)) != cudaSuccess) return fail_cuda(e);
+        if ((e = rg::kgemm_max_clusters(&kc, smem)) != cudaSuccess) return fail_cuda(e);
+        if (mc < 1 || kc < 1) return fail_cuda(cudaErrorLaunchOutOfResources);
+        ds.mg_grid = 2 * std::min(mc, sms / 2);
+        ds.kg_grid = 2 * std::min(kc, sms / 2);
+      }
     }
     ds.ready = true;
   }
@@ -123,7 +137,7 @@ int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_
   if (M > 0 && (x == nullptr || y == nullptr || !aligned16(x) || !aligned16(y)))
     return RG_ERR_INVALID_ARG;
   // the tile list is indexed with 32-bit integers
-  const int64_t max_tiles = (M / rg::mg::BM + E) * ((N + rg::mg::BN - 1) / rg::mg::BN);
+  const int64_t max_tiles = (M / rg::mg::TILE_M + E) * ((N + rg::mg::BN - 1) / rg::mg::BN);
   if (max_tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != RG_OK) return rc;
@@ -137,12 +151,12 @@ int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_
     const uint32_t box[2] = {64, rg::mg::BM};
     if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, str, box)) return RG_ERR_INVALID_ARG;
   }
-  if (!transpose_B) {  // w [E, N, K], K contiguous: one 64 x 256 box per stage
+  if (!transpose_B) {  // w [E, N, K], K contiguous: one 64 x BN_CTA box per stage and CTA
     const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
     const uint64_t str[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2};
-    const uint32_t box[3] = {64, rg::mg::BN, 1};
+    const uint32_t box[3] = {64, rg::mg::BN_CTA, 1};
     if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box)) return RG_ERR_INVALID_ARG;
-  } else {  // w [E, K, N], N contiguous: four 64-column boxes of 64 K rows per stage
+  } else {  // w [E, K, N], N contiguous: 64-column boxes of 64 K rows
     const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(E)};
     const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K) * N * 2};
     const uint32_t box[3] = {64, rg::mg::BK, 1};
@@ -163,7 +177,7 @@ int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_
   args.out = y;
   args.status = ds->status;
   args.wait_limit_ns = g_wait_limit_ns.load();
-  const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmB, tmY, args, ds->num_sms, stream);
+  const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmB, tmY, args, ds->mg_grid, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
 }
@@ -175,7 +189,7 @@ int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int
   if (dW == nullptr || !aligned16(dW)) return RG_ERR_INVALID_ARG;
   if (M > 0 && (grad == nullptr || X == nullptr || !aligned16(grad) || !aligned16(X)))
     return RG_ERR_INVALID_ARG;
-  const int64_t tiles = static_cast<int64_t>(E) * ((N + rg::kg::BM - 1) / rg::kg::BM) *
+  const int64_t tiles = static_cast<int64_t>(E) * ((N + rg::kg::TILE_M - 1) / rg::kg::TILE_M) *
                         ((K + rg::kg::BN - 1) / rg::kg::BN);
   if (tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
   DeviceState* ds = nullptr;
@@ -217,7 +231,7 @@ int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int
   args.out = dW;
   args.status = ds->status;
   args.wait_limit_ns = g_wait_limit_ns.load();
-  const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->num_sms, stream);
+  const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->kg_grid, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
 }

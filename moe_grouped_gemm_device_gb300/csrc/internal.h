@@ -20,25 +20,35 @@ struct GroupArgs {
   unsigned long long wait_limit_ns;
 };
 
-// Tile shapes (also used by the host to size shared memory).
+// CTA group of the tensor-core MMAs: 2 (default) = a CTA pair computes one
+// tile with tcgen05.mma.cta_group::2; 1 = one CTA per tile.
+#ifndef RG_CTA_PAIR
+#define RG_CTA_PAIR 1
+#endif
+constexpr int kCtaGroup = RG_CTA_PAIR ? 2 : 1;
+// Largest E the kernels are set up for (shared-memory tables of E+1 ints).
+constexpr int RG_MAX_EXPERTS_CFG = 1024;
+
+// Kgemm pipeline overrides for tuning builds (0 stages = default for the CTA
+// group).
+#ifndef RG_KG_STAGES
+#define RG_KG_STAGES 0
+#endif
+
+// Tile geometry the host needs for tensor-map boxes and size checks.
 namespace mg {
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_WARPS = 4, EPI_BUFS = 1, EPI_BUF_BYTES = 32 * 128;
-constexpr int THREADS = 192;
+constexpr int BM = 128;                  // rows per CTA
+constexpr int TILE_M = BM * kCtaGroup;   // rows per tile
+constexpr int BN = 256;                  // output columns per tile
+constexpr int BN_CTA = BN / kCtaGroup;   // B rows loaded per CTA
+constexpr int BK = 64;
 }  // namespace mg
 
-#ifndef RG_KG_STAGES
-#define RG_KG_STAGES 4
-#endif
-#ifndef RG_KG_EPI_BUFS
-#define RG_KG_EPI_BUFS 1
-#endif
 namespace kg {
-constexpr int BM = 128, BN = 256, BR = 64, STAGES = RG_KG_STAGES;
-constexpr int A_BYTES = BM * BR * 2, B_BYTES = BN * BR * 2, STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_WARPS = 4, EPI_BUFS = RG_KG_EPI_BUFS, EPI_BUF_BYTES = 32 * 128;
-constexpr int THREADS = 192;
+constexpr int BM = 128;                  // dW rows per CTA
+constexpr int TILE_M = BM * kCtaGroup;   // dW rows per tile
+constexpr int BN = 256;                  // dW columns per tile
+constexpr int BR = 64;                   // contraction rows per stage
 // Rows of one expert accumulated in tensor memory before the partial sum is
 // folded into dW (store for the first chunk, fp32 reduce-add for the rest).
 // Bounds the length of each fp32 accumulation chain inside the tensor cores.
@@ -55,12 +65,15 @@ size_t kgemm_smem_bytes(int E);
 cudaError_t mgemm_setup(int max_smem);
 cudaError_t kgemm_setup(int max_smem);
 
+// Number of 2-CTA clusters of each kernel that can be resident at once.
+cudaError_t mgemm_max_clusters(int* clusters, int max_smem);
+cudaError_t kgemm_max_clusters(int* clusters, int max_smem);
+
 cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmY, const GroupArgs& args, int grid,
                          cudaStream_t stream);
 cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
                          const GroupArgs& args, int grid, cudaStream_t stream);
-cudaError_t launch_zero_f32(float* p, int64_t n, int grid, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,
                                  cudaStream_t stream);
 

@@ -4,27 +4,37 @@
 // offsets[e] .. offsets[e+1]-1 of expert e, whose bounds may fall anywhere.
 //
 // Design
-//   * Output tiles are (e, n-block of 128, k-block of 256); every expert has
-//     the same number of tiles, so the tile list is E x ceil(N/128) x
-//     ceil(K/256).  Experts are visited in decreasing row count (ties by
-//     index), which every CTA computes itself in shared memory; CTA b takes
-//     tiles b, b+G, ..., so each round of G tiles has near-equal cost
-//     (longest-first list scheduling) without global scratch or host sync.
-//   * The contraction is fed 64 rows at a time: A = grad[r:r+64, n0:n0+128]
-//     and B = X[r:r+64, k0:k0+256], both N/K-contiguous, i.e. MN-major
-//     operands of tcgen05.mma (M=128, N=256, K=16).  Rows of the last block
-//     that lie past the expert's end belong to the next expert: the MMA warp
-//     zeroes them in shared memory (both operands, so no NaN/Inf can leak)
-//     and fences them into the async proxy before issuing the MMAs.
-//   * The fp32 accumulator (128 lanes x 256 columns, double-buffered in
-//     tensor memory) holds at most CHUNK_ROWS rows of one expert: a longer
+//   * Output tiles are (e, n-block of TILE_M, k-block of 256); every expert
+//     has the same number of tiles, so the tile list is E x ceil(N/TILE_M) x
+//     ceil(K/256).  Every CTA sorts the experts by decreasing row count (ties
+//     by index) in shared memory; worker w takes the w-th tile of each round
+//     of W tiles, rounds alternating between the heaviest and the lightest
+//     remaining tiles, so every round has near-equal cost and every worker
+//     overlaps the fp32 stores of a light tile with the MMAs of a heavy one --
+//     without global scratch or host sync.
+//   * The contraction is fed 64 rows at a time.  With CG = 2 (default) a CTA
+//     pair computes a 256x256 dW tile with tcgen05.mma.cta_group::2: CTA r
+//     loads grad[r:r+64, n0+128r : +128] (A, its 128 rows of dW) and
+//     X[r:r+64, k0+128r : +128] (its half of B); both are N/K-contiguous, i.e.
+//     MN-major operands.  32 KB per stage and CTA, six stages.  CG = 1: one
+//     CTA, 128x256 tiles, four 48 KB stages.
+//   * The copies of both CTAs complete their bytes directly on the issuing
+//     CTA's stage barrier (.cta_group::2).  Rows of an expert's last block that
+//     lie past its end belong to the next expert: only the 16-row MMA steps
+//     holding valid rows are issued, and the (at most 15) foreign rows of the
+//     last step are zeroed in both operands, so no NaN/Inf can leak.  That
+//     block lands on each CTA's own barrier: the issuing CTA's MMA warp zeroes
+//     its rows, warp 1 of the peer CTA zeroes the peer's and then arrives on
+//     the issuing CTA's ready barrier (one cluster arrive per ragged block).
+//   * The fp32 accumulator (128 lanes x 256 columns per CTA, double-buffered
+//     in tensor memory) holds at most CHUNK_ROWS rows of one expert: a longer
 //     expert is summed chunk by chunk, the first chunk's partial stored to dW
 //     and each later one added to it by a TMA fp32 reduce-add, in order.  This
 //     bounds the fp32 accumulation chain inside the tensor cores (whose error
 //     grows with its length) without any scratch memory.  The path to dW is
 //     tcgen05.ld -> swizzled shared memory -> TMA store / reduce-add of 32x32
-//     fp32 boxes.  Experts without rows produce zero tiles without touching
-//     the tensor cores.
+//     fp32 boxes (whole 128-byte lines).  Experts without rows produce zero
+//     tiles without touching the tensor cores.
 //   * Same bounded-wait / abort / drain scheme as the M-grouped kernel.
 #include <algorithm>
 
@@ -34,45 +44,70 @@
 namespace rg {
 namespace {
 
-using namespace kg;
+template <int CG>
+struct Cfg {
+  static constexpr int BM = 128;           // dW rows per CTA (MMA M per CTA)
+  static constexpr int TILE_M = BM * CG;   // dW rows per tile
+  static constexpr int BN = 256;           // dW columns per tile (MMA N)
+  static constexpr int BN_CTA = BN / CG;   // X columns loaded per CTA
+  static constexpr int BR = 64;            // rows of the contraction per stage
+  static constexpr int STAGES = RG_KG_STAGES > 0 ? RG_KG_STAGES : (CG == 2 ? 6 : 4);
+  static constexpr int BOX_BYTES = BR * 128;  // one 64-element-wide box of BR rows
+  static constexpr int A_BYTES = BM * BR * 2;
+  static constexpr int B_BYTES = BN_CTA * BR * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_BUF_BYTES = 32 * 128;  // one 32x32 fp32 box per epilogue warp
+  static constexpr int THREADS = 192;             // producer, MMA, 4 epilogue
+  // full[S], empty[S], ready[S], tfull[2], tempty[2], drain
+  static constexpr int NUM_BARS = 3 * STAGES + 5;
+  // The dynamic shared-memory window of a CTA without static shared memory
+  // starts 1024-byte aligned; the kernel checks this instead of padding.
+  static constexpr int SMEM_FIXED =
+      STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 + 16;
+};
 
-constexpr int NUM_BARS = 2 * STAGES + 5;
-// The dynamic shared-memory window of a CTA without static shared memory
-// starts 1024-byte aligned; the kernel checks this instead of padding for it.
-constexpr int SMEM_FIXED = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES +
-                           NUM_BARS * 8 + 16;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int BOX_BYTES = BR * 128;  // one 64-element-wide box of BR rows
+constexpr int CHUNK_ROWS = kg::CHUNK_ROWS;
 
-__global__ void __launch_bounds__(THREADS, 1)
+template <int CG>
+__global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     kgemm_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmX,
                  const __grid_constant__ CUtensorMap tmD, const GroupArgs args) {
+  using C = Cfg<CG>;
+  constexpr int BM = C::BM, TILE_M = C::TILE_M, BN = C::BN, BN_CTA = C::BN_CTA, BR = C::BR;
+  constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
+  constexpr int BOX_BYTES = C::BOX_BYTES, EPI_BUF_BYTES = C::EPI_BUF_BYTES;
+
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // swizzled TMA boxes and MMA descriptors need 1024-byte alignment
     if (threadIdx.x == 0) atomicOr(args.status, kDevLaunchConfig);
     return;
   }
-
   uint8_t* epi = smem + STAGES * STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES);
-  int* misc = reinterpret_cast<int*>(bars + NUM_BARS);  // [0] tmem base, [1] abort
-  int* s_off = misc + 4;                                // [E+1] offsets
-  int* s_ord = s_off + (args.E + 1);                    // [E] experts by decreasing rows
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_WARPS * EPI_BUF_BYTES);
+  int* misc = reinterpret_cast<int*>(bars + C::NUM_BARS);  // [0] tmem base, [1] abort
+  int* s_off = misc + 4;                                   // [E+1] offsets
+  int* s_ord = s_off + (args.E + 1);                       // [E] experts by decreasing rows
 
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto ready_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;  // rank 0 issues the MMAs
+  const int worker = blockIdx.x / CG;
+  const int nworkers = gridDim.x / CG;
   const int E = args.E;
   const int N = args.N;
   const int K = args.K;
-  const int nbn = (N + BM - 1) / BM;
+  const int nbn = (N + TILE_M - 1) / TILE_M;
   const int nbk = (K + BN - 1) / BN;
   const int tpe = nbn * nbk;
   const int T = E * tpe;
@@ -84,21 +119,21 @@ __global__ void __launch_bounds__(THREADS, 1)
   int bad = 0;
   for (int i = threadIdx.x; i < E; i += blockDim.x) bad |= (s_off[i + 1] < s_off[i]);
   if (threadIdx.x == 0) bad |= (s_off[0] != 0) | (s_off[E] > args.M);
-  if (__syncthreads_or(bad)) {
+  if (__syncthreads_or(bad)) {  // both CTAs of a pair see the same offsets and leave together
     if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.status, kDevBadOffsets);
     return;
   }
-  if (static_cast<int>(blockIdx.x) >= T) return;
+  if (worker >= T) return;
 
   // ---- experts ordered by decreasing row count (stable) ---------------------
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int ce = s_off[e + 1] - s_off[e];
-    int rank = 0;
+    int rank_e = 0;
     for (int f = 0; f < E; ++f) {
       const int cf = s_off[f + 1] - s_off[f];
-      rank += (cf > ce) | ((cf == ce) & (f < e));
+      rank_e += (cf > ce) | ((cf == ce) & (f < e));
     }
-    s_ord[rank] = e;
+    s_ord[rank_e] = e;
   }
 
   // ---- barriers and tensor memory -------------------------------------------
@@ -106,23 +141,57 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(ready_bar(s), 1);  // the peer CTA's half of a ragged block is zeroed
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), EPI_WARPS * 32);
+      mbar_init(tempty_bar(b), C::EPI_WARPS * CG);
     }
     mbar_init(drain_bar, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&misc[0]), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<CG>(smem_u32(&misc[0]), TMEM_COLS);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
   const WaitGuard guard{args.status, args.wait_limit_ns, reinterpret_cast<volatile int*>(&misc[1])};
+  auto wait_pair = [&](uint32_t bar, uint32_t par) {
+    if constexpr (CG == 2) return mbar_wait_cl(guard, bar, par);
+    else return mbar_wait(guard, bar, par);
+  };
+  // Position t of this worker's sequence (round i = t / W) -> index into the
+  // list of tiles sorted by decreasing rows: even rounds take the next W
+  // heaviest tiles, odd rounds the next W lightest.  Each worker alternates a
+  // contraction-heavy tile with a store-heavy one, so the fp32 stores of one
+  // overlap the MMAs of the next.  (The front and back index sets are
+  // contiguous and disjoint for any T and W, so this is a permutation.)
+  auto tile_at = [&](int t, int& e, int& local) {
+    const int i = t / nworkers, w = t - i * nworkers;
+    const int j = (i >> 1) * nworkers + w;
+    const int idx = (i & 1) ? T - 1 - j : j;
+    const int p = idx / tpe;
+    e = s_ord[p];
+    local = idx - p * tpe;
+  };
+  // Zero rows [lo, hi) of every box of `stage` in this CTA (whole 128-byte
+  // rows, so the swizzle does not matter) and publish the writes to the async
+  // proxy.
+  auto zero_rows = [&](int stage, int lo, int hi) {
+    uint8_t* st = smem + stage * STAGE_BYTES;
+    const int units = (hi - lo) * 8;  // 16-byte units per box
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+    for (int b = 0; b < STAGE_BYTES / BOX_BYTES; ++b) {
+      uint4* bp = reinterpret_cast<uint4*>(st + b * BOX_BYTES + lo * 128);
+      for (int u = lane; u < units; u += 32) bp[u] = z;
+    }
+    fence_proxy_async_smem();
+  };
 
   if (warp == 0) {
     // ======================= TMA producer (one thread) =======================
@@ -132,49 +201,75 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;
+      uint32_t own_par = 0;  // peer CTA: parity of the next phase of each own full barrier
+      const uint32_t full_issuer = CG == 2 ? mapa_shared(full_bar(0), 0) : full_bar(0);
       bool ok = true;
-      for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-        const int p = t / tpe;
-        const int e = s_ord[p];
-        const int local = t - p * tpe;
-        const int n0 = (local / nbk) * BM;
-        const int k0 = (local % nbk) * BN;
+      for (int t = worker; t < T && ok; t += nworkers) {
+        int e, local;
+        tile_at(t, e, local);
+        const int n0 = (local / nbk) * TILE_M + static_cast<int>(rank) * BM;
+        const int k0 = (local % nbk) * BN + static_cast<int>(rank) * BN_CTA;
         const int r_begin = s_off[e], r_end = s_off[e + 1];
         for (int r = r_begin; r < r_end; r += BR) {
-          if (!mbar_wait(guard, empty_bar(stage), phase ^ 1u)) {
+          if (!wait_pair(empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
           }
-          const uint32_t fb = full_bar(stage);
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          // A full block: both CTAs' copies complete on the issuing CTA's full
+          // barrier, which expects the bytes of the whole pair.  The expert's
+          // ragged last block: each CTA's copies complete on its own full
+          // barrier, so each CTA can zero its foreign rows once they landed.
+          const bool tail = r + BR > r_end;
+          if (CG == 1 || tail) {
+            const uint32_t fb = full_bar(stage);
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
 #pragma unroll
-          for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * BOX_BYTES, &tmG, fb, n0 + 64 * j, r);
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * BOX_BYTES, &tmG, fb, n0 + 64 * j, r);
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, r);
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+            for (int j = 0; j < BN_CTA / 64; ++j) tma_load_2d(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, r);
+          } else {
+            const uint32_t fb = full_issuer + 8u * stage;
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES * CG);
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d_cg<CG>(sa + j * BOX_BYTES, &tmG, fb, n0 + 64 * j, r);
+#pragma unroll
+            for (int j = 0; j < BN_CTA / 64; ++j)
+              tma_load_2d_cg<CG>(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, r);
+          }
+          // parity of the phase just armed on this CTA's own full barrier: it
+          // advances with every use in the issuing CTA, only with ragged
+          // blocks in the peer
+          if (rank == 0 || tail) {
+            const uint32_t par = rank == 0 ? phase : (own_par >> stage) & 1u;
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (par << stage);
+            if (rank != 0) own_par ^= 1u << stage;
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
+      if (!ok) {  // let issued loads land before the CTA exits
         for (int s = 0; s < STAGES; ++s)
           if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u, guard.limit_ns);
+        if (rank != 0) spin_ns(200000);  // the peer's copies signal the issuer's barriers
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && rank == 0) {
     // ========================= MMA issuer (warp 1) ===========================
-    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, true, true);
+    constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN, true, true);
     int stage = 0;
     uint32_t phase = 0;
+    uint32_t ready_par = 0;  // parity of the next phase of each ready barrier (tail blocks only)
     int acc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-      const int e = s_ord[t / tpe];
+    for (int t = worker; t < T && ok; t += nworkers) {
+      int e, local;
+      tile_at(t, e, local);
       const int r_begin = s_off[e], r_end = s_off[e + 1];
       // zero tile (no rows): no MMA, no accumulator.  Otherwise one
       // accumulator per chunk of at most CHUNK_ROWS rows.
@@ -182,39 +277,41 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int c_end = min(r_end, cr + CHUNK_ROWS);
         const int buf = acc & 1;
         const uint32_t tph = (acc >> 1) & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(guard, tempty_bar(buf), tph ^ 1u));
+        ok = __all_sync(0xffffffffu, wait_pair(tempty_bar(buf), tph ^ 1u));
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + buf * BN;
         for (int r = cr; r < c_end; r += BR) {
-          ok = __all_sync(0xffffffffu, mbar_wait(guard, full_bar(stage), phase));
+          ok = __all_sync(0xffffffffu, wait_pair(full_bar(stage), phase));
           if (!ok) break;
+          // Ragged last block: only the 16-row MMA steps that hold valid rows
+          // are issued, and the (at most 15) rows past the expert inside the
+          // last of them are zeroed in both operands of both CTAs: here for
+          // this CTA, by warp 1 of the peer for its half (then `ready`).
           const int valid = min(BR, r_end - r);
+          const int ksteps = (valid + 15) / 16;
           if (valid < BR) {
-            // rows [valid, BR) belong to the next expert (or lie past M): zero
-            // them in all six boxes of the stage before the tensor cores read it
-            uint8_t* st = smem + stage * STAGE_BYTES;
-            const int units = (BR - valid) * 8;  // 16-byte units per box
-            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 1
-            for (int b = 0; b < STAGE_BYTES / BOX_BYTES; ++b) {
-              uint4* bp = reinterpret_cast<uint4*>(st + b * BOX_BYTES + valid * 128);
-              for (int u = lane; u < units; u += 32) bp[u] = z;
+            if (valid < 16 * ksteps) zero_rows(stage, valid, 16 * ksteps);
+            __syncwarp();
+            if (CG == 2) {
+              ok = __all_sync(0xffffffffu, wait_pair(ready_bar(stage), (ready_par >> stage) & 1u));
+              if (!ok) break;
+              ready_par ^= 1u << stage;
             }
-            fence_proxy_async_smem();
           }
-          __syncwarp();
           tc_fence_after();
           if (lane == 0) {
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_BYTES;
 #pragma unroll
             for (int k = 0; k < BR / 16; ++k) {
-              const uint64_t ad = sdesc_sw128(sa + 2048 * k, BOX_BYTES, 1024);
-              const uint64_t bd = sdesc_sw128(sb + 2048 * k, BOX_BYTES, 1024);
-              umma_bf16(d_tmem, ad, bd, IDESC, (r != cr) | (k != 0));
+              if (k < ksteps) {
+                const uint64_t ad = sdesc_sw128(sa + 2048 * k, BOX_BYTES, 1024);
+                const uint64_t bd = sdesc_sw128(sb + 2048 * k, BOX_BYTES, 1024);
+                umma_bf16<CG>(d_tmem, ad, bd, IDESC, (r != cr) | (k != 0));
+              }
             }
-            umma_commit(empty_bar(stage));
+            umma_commit<CG>(empty_bar(stage));
           }
           __syncwarp();
           if (++stage == STAGES) {
@@ -223,46 +320,80 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
         if (!ok) break;
-        if (lane == 0) umma_commit(tfull_bar(buf));
+        if (lane == 0) umma_commit<CG>(tfull_bar(buf));
         __syncwarp();
         ++acc;
       }
     }
     if (!ok && lane == 0) {
-      umma_commit(drain_bar);
+      umma_commit_local<CG>(drain_bar);
       mbar_wait_drain(drain_bar, 0, guard.limit_ns);
     }
     __syncwarp();
+  } else if (warp == 1) {
+    // ============ peer CTA of a pair: zero its half of ragged blocks =========
+    // Each expert's ragged last block lands on this CTA's own full barrier
+    // (which completes only for such blocks, in order); zero the foreign rows
+    // of its last 16-row MMA step in both operands, then tell the issuing CTA.
+    int stage = 0;
+    uint32_t own_par = 0;  // parity of the next phase of each own full barrier
+    bool ok = true;
+    const uint32_t ready_issuer = mapa_shared(ready_bar(0), 0);
+    for (int t = worker; t < T && ok; t += nworkers) {
+      int e, local;
+      tile_at(t, e, local);
+      const int r_begin = s_off[e], r_end = s_off[e + 1];
+      for (int r = r_begin; r < r_end; r += BR) {
+        const int valid = min(BR, r_end - r);
+        if (valid < BR) {
+          ok = __all_sync(0xffffffffu, mbar_wait(guard, full_bar(stage), (own_par >> stage) & 1u));
+          if (!ok) break;
+          own_par ^= 1u << stage;
+          const int ksteps = (valid + 15) / 16;
+          if (valid < 16 * ksteps) zero_rows(stage, valid, 16 * ksteps);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(ready_issuer + 8u * stage);
+          __syncwarp();
+        }
+        if (++stage == STAGES) stage = 0;
+      }
+    }
   } else {
     // ======================= epilogue (warps 2..5) ===========================
-    // Warp q owns rows n0 + 32q .. +31 of the tile; each 32x32 fp32 box goes
-    // through one of EPI_BUFS rotating staging buffers.  The first chunk of
-    // an expert's rows is stored, later chunks are reduce-added; before a
-    // later chunk the warp waits until its previous writes have landed, so
-    // the adds are applied in chunk order (deterministic).
+    // Warp q owns dW rows n0 + 32q .. +31 of this CTA's half of the tile; each
+    // 32x32 fp32 box goes tcgen05.ld -> registers -> swizzled staging buffer ->
+    // TMA store (whole 128-byte lines).  The first chunk of an expert's rows is
+    // stored, later chunks are TMA reduce-added; before a later chunk the warp
+    // waits until its previous writes have landed, so the adds are applied in
+    // chunk order (deterministic).
     const int q = warp & 3;
-    uint8_t* ebase = epi + (warp - 2) * EPI_BUFS * EPI_BUF_BYTES;
+    uint8_t* ebuf = epi + (warp - 2) * EPI_BUF_BYTES;
+    const uint32_t ebuf_s = smem_u32(ebuf);
+    uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * 128);
+    const uint32_t tempty_issuer = CG == 2 ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
     int acc = 0;
-    uint32_t nstore = 0;
     bool ok = true;
-    auto stage_buf = [&](const uint32_t (&v)[32]) -> uint32_t {
-      const uint32_t b = nstore % EPI_BUFS;
-      if (lane == 0) bulk_wait_read<EPI_BUFS - 1>();  // buffer b is no longer read
+    auto stage_box = [&](const uint32_t (&v)[32]) {
+      if (lane == 0) bulk_wait_read<0>();  // the previous store has left the buffer
       __syncwarp();
-      uint4* rowp = reinterpret_cast<uint4*>(ebase + b * EPI_BUF_BYTES + lane * 128);
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         rowp[j ^ (lane & 7)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
       fence_proxy_async_smem();
       __syncwarp();
-      ++nstore;
-      return smem_u32(ebase + b * EPI_BUF_BYTES);
     };
-    for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-      const int p = t / tpe;
-      const int e = s_ord[p];
-      const int local = t - p * tpe;
-      const int n0 = (local / nbk) * BM;
+    auto release_acc = [&](int buf) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 2) mbar_arrive_cluster(tempty_issuer + 8u * buf);
+        else mbar_arrive(tempty_bar(buf));
+      }
+    };
+    for (int t = worker; t < T && ok; t += nworkers) {
+      int e, local;
+      tile_at(t, e, local);
+      const int n0 = (local / nbk) * TILE_M + static_cast<int>(rank) * BM;
       const int k0 = (local % nbk) * BN;
       const int r_begin = s_off[e], r_end = s_off[e + 1];
       const bool warp_rows = n0 + q * 32 < N;  // this warp's 32 rows of dW exist
@@ -273,9 +404,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int j = 0; j < 32; ++j) z[j] = 0u;
 #pragma unroll 1
         for (int c = 0; c < BN / 32 && k0 + 32 * c < K; ++c) {
-          const uint32_t src = stage_buf(z);
+          stage_box(z);
           if (lane == 0) {
-            tma_store_3d(&tmD, src, k0 + 32 * c, n0 + q * 32, e);
+            tma_store_3d(&tmD, ebuf_s, k0 + 32 * c, n0 + q * 32, e);
             bulk_commit();
           }
         }
@@ -286,9 +417,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int buf = acc & 1;
         const uint32_t tph = (acc >> 1) & 1;
         ++acc;
-        ok = __all_sync(0xffffffffu, mbar_wait(guard, tfull_bar(buf), tph));
+        ok = __all_sync(0xffffffffu, wait_pair(tfull_bar(buf), tph));
         if (!ok) break;
         tc_fence_after();
+        if (!warp_rows) {
+          release_acc(buf);
+          continue;
+        }
         if (!first && lane == 0) bulk_wait<0>();  // previous partial of this tile is in dW
         const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
 #pragma unroll 1
@@ -296,17 +431,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + 32 * c, v);
           tmem_ld_wait();
-          if (c == BN / 32 - 1) {  // accumulator fully read: hand it back
-            tc_fence_before();
-            mbar_arrive(tempty_bar(buf));
-          }
-          if (!warp_rows || k0 + 32 * c >= K) continue;
-          const uint32_t src = stage_buf(v);
+          if (c == BN / 32 - 1) release_acc(buf);  // accumulator fully read: hand it back
+          if (k0 + 32 * c >= K) continue;
+          stage_box(v);
           if (lane == 0) {
             if (first)
-              tma_store_3d(&tmD, src, k0 + 32 * c, n0 + q * 32, e);
+              tma_store_3d(&tmD, ebuf_s, k0 + 32 * c, n0 + q * 32, e);
             else
-              tma_reduce_add_3d(&tmD, src, k0 + 32 * c, n0 + q * 32, e);
+              tma_reduce_add_3d(&tmD, ebuf_s, k0 + 32 * c, n0 + q * 32, e);
             bulk_commit();
           }
         }
@@ -318,9 +450,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc<CG>(tmem, TMEM_COLS);
   }
 }
 
@@ -339,23 +472,49 @@ __global__ void wait_selftest_kernel(unsigned int* status, unsigned long long li
   __syncthreads();
 }
 
+void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, size_t smem,
+                 cudaStream_t stream) {
+  *cfg = cudaLaunchConfig_t{};
+  cfg->gridDim = dim3(grid);
+  cfg->blockDim = dim3(Cfg<kCtaGroup>::THREADS);
+  cfg->dynamicSmemBytes = smem;
+  cfg->stream = stream;
+  if (kCtaGroup == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+  }
+}
+
 }  // namespace
 
-size_t kgemm_smem_bytes(int E) { return SMEM_FIXED + (2 * static_cast<size_t>(E) + 1) * 4; }
+size_t kgemm_smem_bytes(int E) {
+  return Cfg<kCtaGroup>::SMEM_FIXED + (2 * static_cast<size_t>(E) + 1) * 4;
+}
 
 cudaError_t kgemm_setup(int max_smem) {
-  return cudaFuncSetAttribute(kgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(std::min<size_t>(kgemm_smem_bytes(1024), max_smem)));
+  return cudaFuncSetAttribute(
+      kgemm_kernel<kCtaGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      static_cast<int>(std::min<size_t>(kgemm_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem)));
+}
+
+cudaError_t kgemm_max_clusters(int* clusters, int max_smem) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  fill_config(&cfg, attr, 2 * kCtaGroup, std::min<size_t>(kgemm_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem),
+              nullptr);
+  return cudaOccupancyMaxActiveClusters(clusters, kgemm_kernel<kCtaGroup>, &cfg);
 }
 
 cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
                          const GroupArgs& args, int grid, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = kgemm_smem_bytes(args.E);
-  cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kgemm_kernel, tmG, tmX, tmD, args);
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  fill_config(&cfg, attr, grid, kgemm_smem_bytes(args.E), stream);
+  return cudaLaunchKernelEx(&cfg, kgemm_kernel<kCtaGroup>, tmG, tmX, tmD, args);
 }
 
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,

@@ -3,22 +3,30 @@
 // cumulative offsets vector (RapidGEMM README, "Kernels", Mgemm).
 //
 // Design
-//   * Persistent grid, one CTA per SM.  Every CTA reads offsets[0..E] into
-//     shared memory, validates it, and builds the tile list itself: expert e
-//     contributes ceil(M_e/128) x ceil(N/256) tiles, laid out expert by expert
-//     (prefix sums in shared memory).  CTA b takes tiles b, b+G, b+2G, ... so
-//     no host synchronisation and no global scratch are needed; empty experts
-//     contribute no tiles, tiny ones a single ragged tile.
-//   * A tile is rows [offsets[e] + 128 m, +128) x columns [256 n, +256).  Its
-//     row window starts at the expert's first row, so it never straddles a
-//     group start; rows past the expert's end (which belong to the next
-//     expert) are loaded but never stored.
-//   * Warp roles (192 threads): warp 0 lane 0 issues TMA loads into a
-//     4-stage ring of 48 KB stages (A 128x64 and B 256x64 bf16, 128-byte
-//     swizzle); warp 1 owns tensor memory and lane 0 issues tcgen05.mma
-//     (M=128, N=256, K=16) into one of two 256-column fp32 accumulators;
-//     warps 2-5 drain the other accumulator (tcgen05.ld -> bf16 -> shared
-//     memory -> TMA store), so the epilogue overlaps the next tile's MMAs.
+//   * Persistent grid.  Every CTA reads offsets[0..E] into shared memory,
+//     validates it, and builds the tile list itself: expert e contributes
+//     ceil(M_e/TILE_M) x ceil(N/256) tiles, laid out expert by expert (prefix
+//     sums in shared memory).  Worker w (a CTA pair, or a CTA) takes tiles
+//     w, w+W, w+2W, ... so no host synchronisation and no global scratch are
+//     needed; empty experts contribute no tiles, tiny ones a single ragged one.
+//   * A tile is rows [offsets[e] + TILE_M m, +TILE_M) x columns [256 n, +256).
+//     Its row window starts at the expert's first row, so it never straddles a
+//     group start; rows past the expert's end (they belong to the next expert)
+//     are loaded but never stored.
+//   * CG = 2 (default): a CTA pair (cluster of 2) computes a 256x256 tile with
+//     tcgen05.mma.cta_group::2 (M=256, N=256, K=16).  Each CTA loads its own
+//     128 rows of A and 128 rows of B (output columns), so one 64-deep stage is
+//     32 KB per CTA and six stages are in flight.  Each CTA's tensor memory
+//     receives its 128 rows of D.  The peer CTA's TMA copies complete their
+//     bytes directly on the issuing CTA's stage barrier (.cta_group::2), and
+//     MMA completion is multicast to the barriers of both CTAs.
+//     CG = 1: one CTA computes a 128x256 tile (tcgen05 M=128), four 48 KB stages.
+//   * Warp roles (192 threads per CTA): warp 0 lane 0 issues TMA loads;
+//     warp 1 owns tensor memory, and in the issuing CTA lane 0 issues the MMAs
+//     into one of two 256-column fp32 accumulators; warps 2-5 drain the other
+//     accumulator
+//     (tcgen05.ld -> bf16 -> swizzled shared memory -> TMA store), so the
+//     epilogue overlaps the next tile's MMAs.
 //   * Tail rows: a warp whose 32 rows are all inside the expert stores them
 //     with one TMA store per 64 columns; otherwise each valid row is written
 //     with plain 16-byte stores.
@@ -33,37 +41,63 @@
 namespace rg {
 namespace {
 
-using namespace mg;
+template <int CG>
+struct Cfg {
+  static constexpr int BM = 128;            // rows of A (and of D) per CTA
+  static constexpr int TILE_M = BM * CG;    // rows per tile
+  static constexpr int BN = 256;            // tile columns = MMA N
+  static constexpr int BN_CTA = BN / CG;    // B rows (output columns) loaded per CTA
+  static constexpr int BK = 64;
+  static constexpr int STAGES = CG == 2 ? 6 : 4;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN_CTA * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_BUF_BYTES = 32 * 128;
+  static constexpr int THREADS = 192;
+  // full[S], empty[S], ready[S], tfull[2], tempty[2], drain
+  static constexpr int NUM_BARS = 3 * STAGES + 5;
+  // The dynamic shared-memory window of a CTA without static shared memory
+  // starts 1024-byte aligned; the kernel checks this instead of padding.
+  static constexpr int SMEM_FIXED =
+      STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 + 16;
+};
 
-constexpr int NUM_BARS = 2 * STAGES + 5;  // full[S], empty[S], tfull[2], tempty[2], drain
-constexpr int SMEM_FIXED = 1024 /* alignment slack */ + STAGES * STAGE_BYTES +
-                           EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES + NUM_BARS * 8 + 16;
 constexpr uint32_t TMEM_COLS = 512;
 
-template <bool TRANS_B>
-__global__ void __launch_bounds__(THREADS, 1)
+template <bool TRANS_B, int CG>
+__global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     mgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmY, const GroupArgs args) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  const uint32_t sbase = smem_u32(smem);
+  using C = Cfg<CG>;
+  constexpr int BM = C::BM, TILE_M = C::TILE_M, BN = C::BN, BN_CTA = C::BN_CTA, BK = C::BK;
+  constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
 
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {  // swizzled TMA boxes and MMA descriptors need 1024-byte alignment
+    if (threadIdx.x == 0) atomicOr(args.status, kDevLaunchConfig);
+    return;
+  }
   uint8_t* epi = smem + STAGES * STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES);
-  int* misc = reinterpret_cast<int*>(bars + NUM_BARS);  // [0] tmem base, [1] abort
-  int* s_off = misc + 4;                                // [E+1] offsets
-  int* s_pre = s_off + (args.E + 1);                    // [E+1] tile prefix
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_WARPS * C::EPI_BUF_BYTES);
+  int* misc = reinterpret_cast<int*>(bars + C::NUM_BARS);  // [0] tmem base, [1] abort
+  int* s_off = misc + 4;                                   // [E+1] offsets
+  int* s_pre = s_off + (args.E + 1);                       // [E+1] tile prefix
 
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto ready_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;  // rank 0 issues the MMAs
+  const int worker = blockIdx.x / CG;
+  const int nworkers = gridDim.x / CG;
   const int E = args.E;
   const int N = args.N;
   const int K = args.K;
@@ -77,7 +111,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   int bad = 0;
   for (int i = threadIdx.x; i < E; i += blockDim.x) bad |= (s_off[i + 1] < s_off[i]);
   if (threadIdx.x == 0) bad |= (s_off[0] != 0) | (s_off[E] > args.M);
-  if (__syncthreads_or(bad)) {
+  if (__syncthreads_or(bad)) {  // both CTAs of a pair see the same offsets and leave together
     if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.status, kDevBadOffsets);
     return;
   }
@@ -87,7 +121,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int per = (E + 31) / 32;
     const int lo = min(E, lane * per), hi = min(E, lo + per);
     int s = 0;
-    for (int e = lo; e < hi; ++e) s += ((s_off[e + 1] - s_off[e] + BM - 1) / BM) * nbn;
+    for (int e = lo; e < hi; ++e) s += ((s_off[e + 1] - s_off[e] + TILE_M - 1) / TILE_M) * nbn;
     int incl = s;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -97,36 +131,43 @@ __global__ void __launch_bounds__(THREADS, 1)
     int run = incl - s;
     for (int e = lo; e < hi; ++e) {
       s_pre[e] = run;
-      run += ((s_off[e + 1] - s_off[e] + BM - 1) / BM) * nbn;
+      run += ((s_off[e + 1] - s_off[e] + TILE_M - 1) / TILE_M) * nbn;
     }
     if (lane == 31) s_pre[E] = incl;
   }
   __syncthreads();
   const int T = s_pre[E];
-  if (static_cast<int>(blockIdx.x) >= T) return;
+  if (worker >= T) return;  // same decision in both CTAs of a pair
 
   // ---- barriers and tensor memory -------------------------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(ready_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), EPI_WARPS * 32);
+      mbar_init(tempty_bar(b), C::EPI_WARPS * CG);  // one arrival per epilogue warp of the pair
     }
     mbar_init(drain_bar, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&misc[0]), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<CG>(smem_u32(&misc[0]), TMEM_COLS);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // peer barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
   const WaitGuard guard{args.status, args.wait_limit_ns, reinterpret_cast<volatile int*>(&misc[1])};
+  // barriers that threads of the peer CTA (or its tensor-core commits) arrive on
+  auto wait_pair = [&](uint32_t bar, uint32_t par) {
+    if constexpr (CG == 2) return mbar_wait_cl(guard, bar, par);
+    else return mbar_wait(guard, bar, par);
+  };
 
   if (warp == 0) {
     // ======================= TMA producer (one thread) =======================
@@ -138,26 +179,30 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t armed = 0, armed_par = 0;  // stages with a load issued, and its parity
       bool ok = true;
       int e = 0;
-      for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+      const uint32_t full_issuer = CG == 2 ? mapa_shared(full_bar(0), 0) : full_bar(0);
+      for (int t = worker; t < T && ok; t += nworkers) {
         while (s_pre[e + 1] <= t) ++e;
         const int local = t - s_pre[e];
-        const int row0 = s_off[e] + (local / nbn) * BM;
-        const int n0 = (local % nbn) * BN;
+        const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * BM;
+        const int n0 = (local % nbn) * BN + static_cast<int>(rank) * BN_CTA;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(guard, empty_bar(stage), phase ^ 1u)) {
+          if (!wait_pair(empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
           }
-          const uint32_t fb = full_bar(stage);
+          // both CTAs' copies complete on the issuing CTA's full barrier,
+          // which expects the bytes of the whole pair
+          const uint32_t fb = full_issuer + 8u * stage;
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          tma_load_2d(sa, &tmA, fb, kb * BK, row0);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES * CG);
+          tma_load_2d_cg<CG>(sa, &tmA, fb, kb * BK, row0);
           if constexpr (!TRANS_B) {
-            tma_load_3d(sb, &tmB, fb, kb * BK, n0, e);
+            tma_load_3d_cg<CG>(sb, &tmB, fb, kb * BK, n0, e);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * 8192, &tmB, fb, n0 + 64 * j, kb * BK, e);
+            for (int j = 0; j < BN_CTA / 64; ++j)
+              tma_load_3d_cg<CG>(sb + j * 8192, &tmB, fb, n0 + 64 * j, kb * BK, e);
           }
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -168,26 +213,30 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (!ok) {  // let issued loads land before the CTA exits
-        for (int s = 0; s < STAGES; ++s)
-          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u, guard.limit_ns);
+        if (rank == 0) {
+          for (int s = 0; s < STAGES; ++s)
+            if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u, guard.limit_ns);
+        } else {
+          spin_ns(200000);  // the peer's copies signal the issuer's barriers
+        }
       }
     }
-  } else if (warp == 1) {
-    // ========================= MMA issuer (warp 1) ===========================
-    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, TRANS_B);
+  } else if (warp == 1 && rank == 0) {
+    // ================= MMA issuer (warp 1 of the issuing CTA) =================
+    constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN, false, TRANS_B);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < T; t += gridDim.x, ++acc) {
+    for (int t = worker; t < T; t += nworkers, ++acc) {
       const int buf = acc & 1;
       const uint32_t tph = (acc >> 1) & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(guard, tempty_bar(buf), tph ^ 1u));
+      ok = __all_sync(0xffffffffu, wait_pair(tempty_bar(buf), tph ^ 1u));
       if (!ok) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem + buf * BN;
       for (int kb = 0; kb < nk; ++kb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(guard, full_bar(stage), phase));
+        ok = __all_sync(0xffffffffu, wait_pair(full_bar(stage), phase));
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -198,9 +247,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t ad = sdesc_sw128(sa + 32 * k, 16, 1024);
             const uint64_t bd = TRANS_B ? sdesc_sw128(sb + 2048 * k, 8192, 1024)
                                         : sdesc_sw128(sb + 32 * k, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0);
+            umma_bf16<CG>(d_tmem, ad, bd, IDESC, (kb | k) != 0);
           }
-          umma_commit(empty_bar(stage));  // frees the stage once these MMAs finish
+          umma_commit<CG>(empty_bar(stage));  // frees the stage (in both CTAs) once these MMAs finish
         }
         __syncwarp();
         if (++stage == STAGES) {
@@ -209,35 +258,50 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) umma_commit(tfull_bar(buf));  // accumulator ready for the epilogue
+      if (lane == 0) umma_commit<CG>(tfull_bar(buf));  // accumulator ready for the epilogue(s)
       __syncwarp();
     }
     if (!ok && lane == 0) {  // wait for issued MMAs before tensor memory is freed
-      umma_commit(drain_bar);
+      umma_commit_local<CG>(drain_bar);
       mbar_wait_drain(drain_bar, 0, guard.limit_ns);
     }
     __syncwarp();
+  } else if (warp == 1) {
+    // warp 1 of the peer CTA only takes part in the tensor-memory allocation
   } else {
     // ======================= epilogue (warps 2..5) ===========================
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int r_in_tile = q * 32 + lane;
-    uint8_t* ebuf = epi + (warp - 2) * EPI_BUFS * EPI_BUF_BYTES;
+    const int r_in_cta = q * 32 + lane;
+    uint8_t* ebuf = epi + (warp - 2) * C::EPI_BUF_BYTES;
     const uint32_t ebuf_s = smem_u32(ebuf);
     __nv_bfloat16* y = static_cast<__nv_bfloat16*>(args.out);
+    const uint32_t tempty_issuer = CG == 2 ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+    auto release_acc = [&](int buf) {  // this warp is done with accumulator `buf`
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 2) mbar_arrive_cluster(tempty_issuer + 8u * buf);
+        else mbar_arrive(tempty_bar(buf));
+      }
+    };
     int acc = 0;
     int e = 0;
-    for (int t = blockIdx.x; t < T; t += gridDim.x, ++acc) {
+    for (int t = worker; t < T; t += nworkers, ++acc) {
       while (s_pre[e + 1] <= t) ++e;
       const int local = t - s_pre[e];
-      const int row0 = s_off[e] + (local / nbn) * BM;
-      const int rows_valid = min(BM, s_off[e + 1] - row0);
+      const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * BM;
+      const int rows_valid = min(BM, s_off[e + 1] - row0);  // <= 0: this CTA's half is past the expert
       const int n0 = (local % nbn) * BN;
       const int buf = acc & 1;
       const uint32_t tph = (acc >> 1) & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(guard, tfull_bar(buf), tph))) break;
+      if (!__all_sync(0xffffffffu, wait_pair(tfull_bar(buf), tph))) break;
       tc_fence_after();
+      if (q * 32 >= rows_valid) {  // none of this warp's rows belong to the expert
+        release_acc(buf);
+        continue;
+      }
       const bool warp_full = q * 32 + 32 <= rows_valid;
-      const bool row_ok = r_in_tile < rows_valid;
+      const bool row_ok = r_in_cta < rows_valid;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
 #pragma unroll 1
       for (int c = 0; c < BN / 64; ++c) {
@@ -245,10 +309,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld_32x32b_x32(taddr + 64 * c, v0);
         tmem_ld_32x32b_x32(taddr + 64 * c + 32, v1);
         tmem_ld_wait();
-        if (c == BN / 64 - 1) {  // accumulator fully read: hand it back to the MMA warp
-          tc_fence_before();
-          mbar_arrive(tempty_bar(buf));
-        }
+        if (c == BN / 64 - 1) release_acc(buf);
         uint32_t p[32];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -271,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             bulk_commit();
           }
         } else if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(y + (static_cast<int64_t>(row0 + r_in_tile) * N + col0));
+          uint4* dst = reinterpret_cast<uint4*>(y + (static_cast<int64_t>(row0 + r_in_cta) * N + col0));
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             if (col0 + 8 * j < N) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
@@ -285,33 +346,65 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- teardown --------------------------------------------------------------
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // no remote arrive or MMA still targets either CTA
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc<CG>(tmem, TMEM_COLS);
+  }
+}
+
+template <bool TB>
+cudaError_t set_smem(int max_smem) {
+  const int bytes = static_cast<int>(std::min<size_t>(mgemm_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem));
+  return cudaFuncSetAttribute(mgemm_kernel<TB, kCtaGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              bytes);
+}
+
+void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, size_t smem,
+                 cudaStream_t stream) {
+  *cfg = cudaLaunchConfig_t{};
+  cfg->gridDim = dim3(grid);
+  cfg->blockDim = dim3(Cfg<kCtaGroup>::THREADS);
+  cfg->dynamicSmemBytes = smem;
+  cfg->stream = stream;
+  if (kCtaGroup == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
   }
 }
 
 }  // namespace
 
-size_t mgemm_smem_bytes(int E) { return SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4; }
+size_t mgemm_smem_bytes(int E) {
+  return Cfg<kCtaGroup>::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4;
+}
 
 cudaError_t mgemm_setup(int max_smem) {
-  const int max_bytes = static_cast<int>(std::min<size_t>(mgemm_smem_bytes(1024), max_smem));
-  cudaError_t e = cudaFuncSetAttribute(mgemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
+  cudaError_t e = set_smem<false>(max_smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(mgemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
+  return set_smem<true>(max_smem);
+}
+
+cudaError_t mgemm_max_clusters(int* clusters, int max_smem) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  fill_config(&cfg, attr, 2 * kCtaGroup, std::min<size_t>(mgemm_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem),
+              nullptr);
+  return cudaOccupancyMaxActiveClusters(clusters, mgemm_kernel<false, kCtaGroup>, &cfg);
 }
 
 cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmY, const GroupArgs& args, int grid,
                          cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = mgemm_smem_bytes(args.E);
-  cfg.stream = stream;
-  if (transpose_B) return cudaLaunchKernelEx(&cfg, mgemm_kernel<true>, tmA, tmB, tmY, args);
-  return cudaLaunchKernelEx(&cfg, mgemm_kernel<false>, tmA, tmB, tmY, args);
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  fill_config(&cfg, attr, grid, mgemm_smem_bytes(args.E), stream);
+  if (transpose_B) return cudaLaunchKernelEx(&cfg, mgemm_kernel<true, kCtaGroup>, tmA, tmB, tmY, args);
+  return cudaLaunchKernelEx(&cfg, mgemm_kernel<false, kCtaGroup>, tmA, tmB, tmY, args);
 }
 
 }  // namespace rg

@@ -57,6 +57,50 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-suspending test with cluster-scope acquire: for barriers that the peer
+// CTA of a pair arrives on (remote arrives, multicast MMA commits).  A thread
+// suspended in try_wait is not woken promptly by such arrivals, so these
+// barriers are polled.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// ----------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (own or peer CTA).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
 // Shared state of the bounded waits of one CTA.
 struct WaitGuard {
   unsigned int* status;   // device status word
@@ -65,12 +109,13 @@ struct WaitGuard {
 };
 
 // Slow path of mbar_wait: spin with a deadline.
-static __device__ __noinline__ bool mbar_wait_slow(const WaitGuard& g, uint32_t bar, uint32_t parity) {
+static __device__ __noinline__ bool mbar_wait_slow(const WaitGuard& g, uint32_t bar, uint32_t parity,
+                                                   bool cluster_scope) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*g.abort) return false;
     if (globaltimer_ns() - t0 > g.limit_ns) {
       atomicOr(g.status, kDevTimeout);
@@ -85,7 +130,13 @@ static __device__ __noinline__ bool mbar_wait_slow(const WaitGuard& g, uint32_t 
 // wait that runs out sets kDevTimeout and raises the CTA's abort flag.
 __device__ __forceinline__ bool mbar_wait(const WaitGuard& g, uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(g, bar, parity);
+  return mbar_wait_slow(g, bar, parity, false);
+}
+
+// mbar_wait for barriers that the peer CTA of a CTA pair also arrives on.
+__device__ __forceinline__ bool mbar_wait_cl(const WaitGuard& g, uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  return mbar_wait_slow(g, bar, parity, true);
 }
 
 // Bounded wait used while draining after an abort: ignores the abort flag.
@@ -119,6 +170,49 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// Loads whose completion is signalled on an mbarrier of either CTA of a pair
+// (`bar` is a shared::cluster address): the peer CTA's copies complete their
+// bytes directly on the issuing CTA's barrier.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                 int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                 int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+template <int CG>
+__device__ __forceinline__ void tma_load_2d_cg(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                               int32_t c0, int32_t c1) {
+  if constexpr (CG == 1) tma_load_2d(dst, m, bar, c0, c1);
+  else tma_load_2d_pair(dst, m, bar, c0, c1);
+}
+
+template <int CG>
+__device__ __forceinline__ void tma_load_3d_cg(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                               int32_t c0, int32_t c1, int32_t c2) {
+  if constexpr (CG == 1) tma_load_3d(dst, m, bar, c0, c1, c2);
+  else tma_load_3d_pair(dst, m, bar, c0, c1, c2);
+}
+
+// Bounded spin (used by a peer CTA after an abort, whose own copies signal the
+// issuing CTA's barriers, to let them land before it leaves).
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) {
+  }
 }
 
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t c0,
@@ -170,21 +264,48 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Same for writes into the shared memory of any CTA of the cluster.
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
+// 16 zero bytes at a shared::cluster address (own or peer CTA).
+__device__ __forceinline__ void st_cluster_zero16(uint32_t addr) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05
 
+// Tensor-memory allocation.  With CG == 2 one warp of each CTA of the pair
+// executes these together; the allocation has the same address in both.
+template <int CG>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
 }
 
+template <int CG>
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 
+template <int CG>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -195,23 +316,63 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, one CTA.
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate.  With
+// CG == 2 the issuing (even) CTA drives both tensor cores of the pair: A rows
+// [0,M/2) and B rows [0,N/2) come from its shared memory, the other halves
+// from the same addresses in the peer CTA, and each CTA's tensor memory
+// receives its M/2 rows of D.
+template <int CG>
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if constexpr (CG == 1)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
-// Arrive once on `bar` when all tcgen05 operations issued so far by this
-// thread have completed.
+// Arrive once on `bar` (same shared-memory offset in every CTA of the pair
+// when CG == 2) when all tcgen05 operations issued so far by this thread have
+// completed.
+template <int CG>
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+  if constexpr (CG == 1) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+  } else {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+  }
+}
+
+// Arrive only on this CTA's `bar` (CG == 2: commit from the issuing CTA to
+// its own barrier).
+template <int CG>
+__device__ __forceinline__ void umma_commit_local(uint32_t bar) {
+  if constexpr (CG == 1) {
+    umma_commit<1>(bar);
+  } else {
+    const uint16_t mask = 0x1;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+  }
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives
