@@ -235,21 +235,23 @@ def run_reference(args, wl):
 # ------------------------------------------------------------------ GPU path
 
 
-def traffic_for(kernel: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current source of that kernel; else None."""
+def traffic_for(kernel: str, op_names):
+    """Mean per-launch DRAM bytes of `kernel` over the given ops, from the
+    committed ncu captures (profiles/traffic.json), if they were taken on the
+    current source of that kernel and cover every op; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    d = json.load(open(path))
-    ent = d.get(kernel)
+    ent = json.load(open(path)).get(kernel)
     if not ent:
         return None
     src = os.path.join(ROOT, "moe_grouped_gemm_device_gb300", "csrc", KERNEL_SOURCES[kernel])
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if ent.get("source_sha256_16") != h:
+    if ent.get("source_sha256_16") != hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]:
         return None
-    return ent.get("bytes_per_launch")
+    per_op = ent.get("per_op", {})
+    if not op_names or any(o not in per_op for o in op_names):
+        return None
+    return sum(per_op[o] for o in op_names) // len(op_names)
 
 
 def main():
@@ -410,7 +412,7 @@ def main():
     de = per_kernel[dom]
     achieved = de["flops"] / (de["ms"] * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
-    traffic = traffic_for(dom)
+    traffic = traffic_for(dom, [op.name for op in wl.ops if kernel_of(op) == dom])
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "kernel": dom, "launches_per_step": de["launches"],

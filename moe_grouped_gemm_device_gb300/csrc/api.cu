@@ -194,7 +194,7 @@ int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int
   if (tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != RG_OK) return rc;
-  if (rg::kgemm_smem_bytes(E) > ds->max_smem) return RG_ERR_INVALID_ARG;  // too many experts
+  if (rg::kgemm_smem_bytes(E, ds->max_smem) > ds->max_smem) return RG_ERR_INVALID_ARG;  // too many experts
 
   // With M == 0 every valid offsets vector is all zeros, so the kernel only
   // writes zero tiles; the operand maps then describe one row of dW, which is
@@ -231,7 +231,7 @@ int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int
   args.out = dW;
   args.status = ds->status;
   args.wait_limit_ns = g_wait_limit_ns.load();
-  const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->kg_grid, stream);
+  const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->kg_grid, ds->max_smem, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
 }

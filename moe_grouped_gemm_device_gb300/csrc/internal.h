@@ -29,11 +29,6 @@ constexpr int kCtaGroup = RG_CTA_PAIR ? 2 : 1;
 // Largest E the kernels are set up for (shared-memory tables of E+1 ints).
 constexpr int RG_MAX_EXPERTS_CFG = 1024;
 
-// Kgemm pipeline overrides for tuning builds (0 stages = default for the CTA
-// group).
-#ifndef RG_KG_STAGES
-#define RG_KG_STAGES 0
-#endif
 
 // Tile geometry the host needs for tensor-map boxes and size checks.
 namespace mg {
@@ -58,7 +53,7 @@ static_assert(CHUNK_ROWS % BR == 0, "chunks must hold whole row blocks");
 
 // Bytes of dynamic shared memory a launch with E experts needs.
 size_t mgemm_smem_bytes(int E);
-size_t kgemm_smem_bytes(int E);
+size_t kgemm_smem_bytes(int E, size_t max_smem);  // of the configuration a launch uses
 
 // One-time per-device kernel attribute setup: allow up to `max_smem` bytes
 // of dynamic shared memory (the device's opt-in limit).
@@ -73,7 +68,7 @@ cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtenso
                          const CUtensorMap& tmY, const GroupArgs& args, int grid,
                          cudaStream_t stream);
 cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
-                         const GroupArgs& args, int grid, cudaStream_t stream);
+                         const GroupArgs& args, int grid, size_t max_smem, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,
                                  cudaStream_t stream);
 

@@ -44,21 +44,21 @@
 namespace rg {
 namespace {
 
-template <int CG>
+template <int CG, int ST>
 struct Cfg {
   static constexpr int BM = 128;           // dW rows per CTA (MMA M per CTA)
   static constexpr int TILE_M = BM * CG;   // dW rows per tile
   static constexpr int BN = 256;           // dW columns per tile (MMA N)
   static constexpr int BN_CTA = BN / CG;   // X columns loaded per CTA
   static constexpr int BR = 64;            // rows of the contraction per stage
-  static constexpr int STAGES = RG_KG_STAGES > 0 ? RG_KG_STAGES : (CG == 2 ? 6 : 4);
+  static constexpr int STAGES = ST;
   static constexpr int BOX_BYTES = BR * 128;  // one 64-element-wide box of BR rows
   static constexpr int A_BYTES = BM * BR * 2;
   static constexpr int B_BYTES = BN_CTA * BR * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_WARPS = 8;              // two per TMEM lane quarter
   static constexpr int EPI_BUF_BYTES = 32 * 128;  // one 32x32 fp32 box per epilogue warp
-  static constexpr int THREADS = 192;             // producer, MMA, 4 epilogue
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer, MMA, epilogue             // producer, MMA, 4 epilogue
   // full[S], empty[S], ready[S], tfull[2], tempty[2], drain
   static constexpr int NUM_BARS = 3 * STAGES + 5;
   // The dynamic shared-memory window of a CTA without static shared memory
@@ -70,11 +70,11 @@ struct Cfg {
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int CHUNK_ROWS = kg::CHUNK_ROWS;
 
-template <int CG>
-__global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
+template <int CG, int ST>
+__global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     kgemm_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmX,
                  const __grid_constant__ CUtensorMap tmD, const GroupArgs args) {
-  using C = Cfg<CG>;
+  using C = Cfg<CG, ST>;
   constexpr int BM = C::BM, TILE_M = C::TILE_M, BN = C::BN, BN_CTA = C::BN_CTA, BR = C::BR;
   constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
   constexpr int BOX_BYTES = C::BOX_BYTES, EPI_BUF_BYTES = C::EPI_BUF_BYTES;
@@ -359,21 +359,26 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       }
     }
   } else {
-    // ======================= epilogue (warps 2..5) ===========================
-    // Warp q owns dW rows n0 + 32q .. +31 of this CTA's half of the tile; each
-    // 32x32 fp32 box goes tcgen05.ld -> registers -> swizzled staging buffer ->
-    // TMA store (whole 128-byte lines).  The first chunk of an expert's rows is
-    // stored, later chunks are TMA reduce-added; before a later chunk the warp
-    // waits until its previous writes have landed, so the adds are applied in
-    // chunk order (deterministic).
+    // ======================= epilogue (warps 2..9) ===========================
+    // Warp w owns TMEM lane quarter q = w % 4 (dW rows n0 + 32q .. +31 of this
+    // CTA's half of the tile) and column half h (128 of the 256 columns).  It
+    // pulls its whole 32x128 slice into registers with four back-to-back
+    // tcgen05.ld, hands the accumulator back at once -- so the MMAs of the
+    // next-but-one tile never wait for the stores -- and then writes the four
+    // 32x32 fp32 boxes: registers -> swizzled staging buffer -> TMA store
+    // (whole 128-byte lines).  The first chunk of an expert's rows is stored,
+    // later chunks are TMA reduce-added; before a later chunk the warp waits
+    // until its previous writes have landed, so the adds are applied in chunk
+    // order (deterministic).
     const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
     uint8_t* ebuf = epi + (warp - 2) * EPI_BUF_BYTES;
     const uint32_t ebuf_s = smem_u32(ebuf);
     uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * 128);
     const uint32_t tempty_issuer = CG == 2 ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
     int acc = 0;
     bool ok = true;
-    auto stage_box = [&](const uint32_t (&v)[32]) {
+    auto stage_box = [&](const uint32_t* v) {
       if (lane == 0) bulk_wait_read<0>();  // the previous store has left the buffer
       __syncwarp();
 #pragma unroll
@@ -394,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       int e, local;
       tile_at(t, e, local);
       const int n0 = (local / nbk) * TILE_M + static_cast<int>(rank) * BM;
-      const int k0 = (local % nbk) * BN;
+      const int kh = (local % nbk) * BN + h * (BN / 2);  // first dW column of this warp
       const int r_begin = s_off[e], r_end = s_off[e + 1];
       const bool warp_rows = n0 + q * 32 < N;  // this warp's 32 rows of dW exist
       if (r_end == r_begin) {  // expert without rows: dW tile = 0
@@ -403,10 +408,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) z[j] = 0u;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32 && k0 + 32 * c < K; ++c) {
+        for (int c = 0; c < BN / 64 && kh + 32 * c < K; ++c) {
           stage_box(z);
           if (lane == 0) {
-            tma_store_3d(&tmD, ebuf_s, k0 + 32 * c, n0 + q * 32, e);
+            tma_store_3d(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e);
             bulk_commit();
           }
         }
@@ -424,21 +429,23 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
           release_acc(buf);
           continue;
         }
+        uint32_t v[BN / 2];
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + h * (BN / 2);
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c)
+          tmem_ld_32x32b_x32(taddr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+        tmem_ld_wait();
+        release_acc(buf);  // accumulator fully read: hand it back
         if (!first && lane == 0) bulk_wait<0>();  // previous partial of this tile is in dW
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(taddr + 32 * c, v);
-          tmem_ld_wait();
-          if (c == BN / 32 - 1) release_acc(buf);  // accumulator fully read: hand it back
-          if (k0 + 32 * c >= K) continue;
-          stage_box(v);
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) {
+          if (kh + 32 * c >= K) break;
+          stage_box(v + 32 * c);
           if (lane == 0) {
             if (first)
-              tma_store_3d(&tmD, ebuf_s, k0 + 32 * c, n0 + q * 32, e);
+              tma_store_3d(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e);
             else
-              tma_reduce_add_3d(&tmD, ebuf_s, k0 + 32 * c, n0 + q * 32, e);
+              tma_reduce_add_3d(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e);
             bulk_commit();
           }
         }
@@ -472,11 +479,21 @@ __global__ void wait_selftest_kernel(unsigned int* status, unsigned long long li
   __syncthreads();
 }
 
+// Stage counts: the deep ring when the shared-memory tables of E experts
+// still fit beside it, otherwise one stage less.
+constexpr int kStagesDeep = kCtaGroup == 2 ? 6 : 4;
+constexpr int kStagesShallow = kStagesDeep - 1;
+
+template <int ST>
+size_t smem_bytes(int E) {
+  return Cfg<kCtaGroup, ST>::SMEM_FIXED + (2 * static_cast<size_t>(E) + 1) * 4;
+}
+
 void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, size_t smem,
                  cudaStream_t stream) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(grid);
-  cfg->blockDim = dim3(Cfg<kCtaGroup>::THREADS);
+  cfg->blockDim = dim3(Cfg<kCtaGroup, kStagesDeep>::THREADS);
   cfg->dynamicSmemBytes = smem;
   cfg->stream = stream;
   if (kCtaGroup == 2) {
@@ -491,30 +508,39 @@ void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, s
 
 }  // namespace
 
-size_t kgemm_smem_bytes(int E) {
-  return Cfg<kCtaGroup>::SMEM_FIXED + (2 * static_cast<size_t>(E) + 1) * 4;
+size_t kgemm_smem_bytes(int E, size_t max_smem) {
+  const size_t deep = smem_bytes<kStagesDeep>(E);
+  return deep <= max_smem ? deep : smem_bytes<kStagesShallow>(E);
 }
 
 cudaError_t kgemm_setup(int max_smem) {
+  cudaError_t e = cudaFuncSetAttribute(
+      kgemm_kernel<kCtaGroup, kStagesDeep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      static_cast<int>(std::min<size_t>(smem_bytes<kStagesDeep>(RG_MAX_EXPERTS_CFG), max_smem)));
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(
-      kgemm_kernel<kCtaGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      static_cast<int>(std::min<size_t>(kgemm_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem)));
+      kgemm_kernel<kCtaGroup, kStagesShallow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      static_cast<int>(std::min<size_t>(smem_bytes<kStagesShallow>(RG_MAX_EXPERTS_CFG), max_smem)));
 }
 
 cudaError_t kgemm_max_clusters(int* clusters, int max_smem) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  fill_config(&cfg, attr, 2 * kCtaGroup, std::min<size_t>(kgemm_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem),
-              nullptr);
-  return cudaOccupancyMaxActiveClusters(clusters, kgemm_kernel<kCtaGroup>, &cfg);
+  fill_config(&cfg, attr, 2 * kCtaGroup, std::min<size_t>(smem_bytes<kStagesDeep>(1), max_smem), nullptr);
+  return cudaOccupancyMaxActiveClusters(clusters, kgemm_kernel<kCtaGroup, kStagesDeep>, &cfg);
 }
 
 cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
-                         const GroupArgs& args, int grid, cudaStream_t stream) {
+                         const GroupArgs& args, int grid, size_t max_smem, cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  fill_config(&cfg, attr, grid, kgemm_smem_bytes(args.E), stream);
-  return cudaLaunchKernelEx(&cfg, kgemm_kernel<kCtaGroup>, tmG, tmX, tmD, args);
+  const size_t deep = smem_bytes<kStagesDeep>(args.E);
+  if (deep <= max_smem) {
+    fill_config(&cfg, attr, grid, deep, stream);
+    return cudaLaunchKernelEx(&cfg, kgemm_kernel<kCtaGroup, kStagesDeep>, tmG, tmX, tmD, args);
+  }
+  fill_config(&cfg, attr, grid, smem_bytes<kStagesShallow>(args.E), stream);
+  return cudaLaunchKernelEx(&cfg, kgemm_kernel<kCtaGroup, kStagesShallow>, tmG, tmX, tmD, args);
 }
 
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,
