@@ -264,9 +264,63 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN, true, true);
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t ready_par = 0;  // parity of the next phase of each ready barrier (tail blocks only)
+    uint32_t ready_par = 0;  // parity of the next phase of each ready barrier (ragged blocks only)
     int acc = 0;
     bool ok = true;
+    // Issue the MMAs of one stage: the first `ksteps` 16-row steps into the
+    // accumulator at column d_tmem, then free the stage.
+    auto issue = [&](int st, uint32_t d_tmem, int ksteps, bool fresh) {
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sa = sbase + st * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+        for (int k = 0; k < BR / 16; ++k) {
+          if (k < ksteps) {
+            const uint64_t ad = sdesc_sw128(sa + 2048 * k, BOX_BYTES, 1024);
+            const uint64_t bd = sdesc_sw128(sb + 2048 * k, BOX_BYTES, 1024);
+            umma_bf16<CG>(d_tmem, ad, bd, IDESC, (!fresh) | (k != 0));
+          }
+        }
+        umma_commit<CG>(empty_bar(st));
+      }
+      __syncwarp();
+    };
+    // A ragged last block (rows past the expert inside its last 16-row step
+    // are zeroed: here for this CTA, by warp 1 of the peer for its half, which
+    // then arrives on `ready`).  With CTA pairs the peer's hand-shake is not
+    // waited for on the spot: the block is kept pending while the next
+    // tile's blocks are issued into the other accumulator, and completed as
+    // soon as it is ready -- at the latest before the ring comes back to its
+    // stage or its accumulator is needed again.
+    bool pend = false;
+    int p_stage = 0, p_valid = 0, p_buf = 0;
+    uint32_t p_phase = 0;
+    bool p_fresh = false;
+    auto finish_ragged = [&](int st, uint32_t par, int valid, int buf, bool fresh) {
+      const int ksteps = (valid + 15) / 16;
+      if (valid < 16 * ksteps) zero_rows(st, valid, 16 * ksteps);
+      __syncwarp();
+      issue(st, tmem + buf * BN, ksteps, fresh);
+      if (lane == 0) umma_commit<CG>(tfull_bar(buf));  // the ragged block ends its accumulator
+      __syncwarp();
+    };
+    // Complete the pending block; `block` = wait for it, else only if ready now.
+    auto resolve = [&](bool block) -> bool {
+      if (!pend) return true;
+      const uint32_t rbit = (ready_par >> p_stage) & 1u;
+      if (block) {
+        if (!__all_sync(0xffffffffu, wait_pair(full_bar(p_stage), p_phase))) return false;
+        if (!__all_sync(0xffffffffu, wait_pair(ready_bar(p_stage), rbit))) return false;
+      } else if (!__all_sync(0xffffffffu, mbar_try_wait_cluster(full_bar(p_stage), p_phase) &&
+                                              mbar_try_wait_cluster(ready_bar(p_stage), rbit))) {
+        return true;
+      }
+      ready_par ^= 1u << p_stage;
+      finish_ragged(p_stage, p_phase, p_valid, p_buf, p_fresh);
+      pend = false;
+      return true;
+    };
     for (int t = worker; t < T && ok; t += nworkers) {
       int e, local;
       tile_at(t, e, local);
@@ -277,54 +331,50 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         const int c_end = min(r_end, cr + CHUNK_ROWS);
         const int buf = acc & 1;
         const uint32_t tph = (acc >> 1) & 1;
+        if (pend && p_buf == buf && !(ok = resolve(true))) break;  // its accumulator is needed again
         ok = __all_sync(0xffffffffu, wait_pair(tempty_bar(buf), tph ^ 1u));
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + buf * BN;
+        bool deferred = false;
         for (int r = cr; r < c_end; r += BR) {
-          ok = __all_sync(0xffffffffu, wait_pair(full_bar(stage), phase));
+          // the ring is back at the pending block's stage: finish it first
+          ok = resolve(pend && p_stage == stage);
           if (!ok) break;
-          // Ragged last block: only the 16-row MMA steps that hold valid rows
-          // are issued, and the (at most 15) rows past the expert inside the
-          // last of them are zeroed in both operands of both CTAs: here for
-          // this CTA, by warp 1 of the peer for its half (then `ready`).
           const int valid = min(BR, r_end - r);
-          const int ksteps = (valid + 15) / 16;
-          if (valid < BR) {
-            if (valid < 16 * ksteps) zero_rows(stage, valid, 16 * ksteps);
-            __syncwarp();
-            if (CG == 2) {
-              ok = __all_sync(0xffffffffu, wait_pair(ready_bar(stage), (ready_par >> stage) & 1u));
-              if (!ok) break;
-              ready_par ^= 1u << stage;
+          if (CG == 2 && valid < BR) {
+            if (pend && !(ok = resolve(true))) break;  // one pending block at a time
+            pend = true;
+            p_stage = stage;
+            p_phase = phase;
+            p_valid = valid;
+            p_buf = buf;
+            p_fresh = r == cr;
+            deferred = true;
+          } else {
+            ok = __all_sync(0xffffffffu, wait_pair(full_bar(stage), phase));
+            if (!ok) break;
+            const int ksteps = (valid + 15) / 16;
+            if (valid < 16 * ksteps) {  // single CTA: zero the foreign rows here
+              zero_rows(stage, valid, 16 * ksteps);
+              __syncwarp();
             }
+            issue(stage, d_tmem, ksteps, r == cr);
           }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t sa = sbase + stage * STAGE_BYTES;
-            const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-            for (int k = 0; k < BR / 16; ++k) {
-              if (k < ksteps) {
-                const uint64_t ad = sdesc_sw128(sa + 2048 * k, BOX_BYTES, 1024);
-                const uint64_t bd = sdesc_sw128(sb + 2048 * k, BOX_BYTES, 1024);
-                umma_bf16<CG>(d_tmem, ad, bd, IDESC, (r != cr) | (k != 0));
-              }
-            }
-            umma_commit<CG>(empty_bar(stage));
-          }
-          __syncwarp();
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        if (lane == 0) umma_commit<CG>(tfull_bar(buf));
-        __syncwarp();
+        if (!deferred) {
+          if (lane == 0) umma_commit<CG>(tfull_bar(buf));
+          __syncwarp();
+        }
         ++acc;
       }
     }
+    if (ok) ok = resolve(true);
     if (!ok && lane == 0) {
       umma_commit_local<CG>(drain_bar);
       mbar_wait_drain(drain_bar, 0, guard.limit_ns);
