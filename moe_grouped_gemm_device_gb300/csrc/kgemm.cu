@@ -7,11 +7,9 @@
 //   * Output tiles are (e, n-block of TILE_M, k-block of 256); every expert
 //     has the same number of tiles, so the tile list is E x ceil(N/TILE_M) x
 //     ceil(K/256).  Every CTA sorts the experts by decreasing row count (ties
-//     by index) in shared memory; worker w takes the w-th tile of each round
-//     of W tiles, rounds alternating between the heaviest and the lightest
-//     remaining tiles, so every round has near-equal cost and every worker
-//     overlaps the fp32 stores of a light tile with the MMAs of a heavy one --
-//     without global scratch or host sync.
+//     by index) in shared memory; worker w takes tiles w, w+W, ... of that
+//     list, so every round of W tiles has near-equal cost (longest-first list
+//     scheduling) -- without global scratch or host sync.
 //   * The contraction is fed 64 rows at a time.  With CG = 2 (default) a CTA
 //     pair computes a 256x256 dW tile with tcgen05.mma.cta_group::2: CTA r
 //     loads grad[r:r+64, n0+128r : +128] (A, its 128 rows of dW) and
@@ -164,19 +162,13 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     if constexpr (CG == 2) return mbar_wait_cl(guard, bar, par);
     else return mbar_wait(guard, bar, par);
   };
-  // Position t of this worker's sequence (round i = t / W) -> index into the
-  // list of tiles sorted by decreasing rows: even rounds take the next W
-  // heaviest tiles, odd rounds the next W lightest.  Each worker alternates a
-  // contraction-heavy tile with a store-heavy one, so the fp32 stores of one
-  // overlap the MMAs of the next.  (The front and back index sets are
-  // contiguous and disjoint for any T and W, so this is a permutation.)
+  // Tile t of the list sorted by decreasing expert rows (longest first);
+  // worker w takes tiles w, w+W, ..., so every round of W tiles has
+  // near-equal cost.
   auto tile_at = [&](int t, int& e, int& local) {
-    const int i = t / nworkers, w = t - i * nworkers;
-    const int j = (i >> 1) * nworkers + w;
-    const int idx = (i & 1) ? T - 1 - j : j;
-    const int p = idx / tpe;
+    const int p = t / tpe;
     e = s_ord[p];
-    local = idx - p * tpe;
+    local = t - p * tpe;
   };
   // Zero rows [lo, hi) of every box of `stage` in this CTA (whole 128-byte
   // rows, so the swizzle does not matter) and publish the writes to the async
