@@ -96,6 +96,20 @@ int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int
              int N, int K, float* dW, cudaStream_t stream);
 
 /*
+ * rg_kgemm_acc -- as rg_kgemm, but accumulates into dW instead of
+ * overwriting it:  dW[e, n, k] += sum over rows r of expert e of
+ * grad[r, n] * X[r, k].  dW must hold the values to add to (for example an
+ * FP32 main gradient); experts without rows leave dW[e] unchanged.  The sum of
+ * each expert's rows is formed as in rg_kgemm and added to dW in FP32 (round
+ * to nearest), chunk by chunk in row order, so results are deterministic.
+ * TransformerEngine PR #2045 discussion (fuse_wgrad_accumulation: the weight
+ * gradient GEMM accumulating into an FP32 main_grad whose dtype differs from
+ * its BF16 inputs).
+ */
+int rg_kgemm_acc(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M,
+                 int N, int K, float* dW, cudaStream_t stream);
+
+/*
  * rg_get_device_status -- synchronise `stream`, then return through
  * *status (host pointer) the RG_DEV_* bits that kernels of this library set
  * on the current device since the previous call, and clear them.

@@ -37,7 +37,7 @@ RG_DEV_TIMEOUT = 0x2
 RG_DEV_LAUNCH_CONFIG = 0x4
 RG_MAX_EXPERTS = 1024
 
-EXPORTED_SYMBOLS = ("rg_mgemm", "rg_kgemm", "rg_get_device_status", "rg_set_wait_timeout_ns",
+EXPORTED_SYMBOLS = ("rg_mgemm", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_set_wait_timeout_ns",
                     "rg_selftest_wait_timeout", "rg_last_cuda_error", "rg_device_supported",
                     "rg_version")
 
@@ -75,6 +75,8 @@ def load() -> ctypes.CDLL:
     lib.rg_mgemm.restype = i32
     lib.rg_kgemm.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp]
     lib.rg_kgemm.restype = i32
+    lib.rg_kgemm_acc.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp]
+    lib.rg_kgemm_acc.restype = i32
     lib.rg_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.rg_get_device_status.restype = i32
     lib.rg_set_wait_timeout_ns.argtypes = [u64]
@@ -154,9 +156,10 @@ def mgemm(x, w, offsets, transpose_B: bool = False, out=None, stream=None):
     return out
 
 
-def kgemm(grad, X, offsets, out=None, stream=None):
+def kgemm(grad, X, offsets, out=None, stream=None, accumulate: bool = False):
     """K-grouped weight gradient.  grad [M,N] bf16, X [M,K] bf16, offsets
-    int32 [E+1]; returns dW [E,N,K] fp32 (overwritten)."""
+    int32 [E+1]; returns dW [E,N,K] fp32, overwritten -- or, with
+    ``accumulate=True``, added to the given ``out`` (e.g. an FP32 main grad)."""
     import torch
     _need(grad, "grad", torch.bfloat16, 2)
     _need(X, "X", torch.bfloat16, 2)
@@ -167,16 +170,19 @@ def kgemm(grad, X, offsets, out=None, stream=None):
     K = X.shape[1]
     E = offsets.shape[0] - 1
     if out is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs the dW to add to as `out`")
         out = torch.empty((E, N, K), dtype=torch.float32, device=grad.device)
     else:
         _need(out, "out", torch.float32, 3)
         if tuple(out.shape) != (E, N, K):
             raise ValueError(f"out must be [{E},{N},{K}]")
     lib = load()
+    fn = lib.rg_kgemm_acc if accumulate else lib.rg_kgemm
     with torch.cuda.device(grad.device):
-        rc = lib.rg_kgemm(grad.data_ptr(), X.data_ptr(), offsets.data_ptr(), E, M, N, K,
-                          out.data_ptr(), _stream_ptr(grad.device, stream))
-    _check("rg_kgemm", rc)
+        rc = fn(grad.data_ptr(), X.data_ptr(), offsets.data_ptr(), E, M, N, K,
+                out.data_ptr(), _stream_ptr(grad.device, stream))
+    _check("rg_kgemm_acc" if accumulate else "rg_kgemm", rc)
     return out
 
 

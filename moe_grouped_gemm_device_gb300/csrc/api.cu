@@ -177,13 +177,17 @@ int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_
   args.out = y;
   args.status = ds->status;
   args.wait_limit_ns = g_wait_limit_ns.load();
+  args.accumulate = 0;
   const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmB, tmY, args, ds->mg_grid, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
 }
 
-int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,
-             float* dW, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,
+               float* dW, int accumulate, cudaStream_t stream) {
   int rc = check_common(offsets, E, M, N, K);
   if (rc != RG_OK) return rc;
   if (dW == nullptr || !aligned16(dW)) return RG_ERR_INVALID_ARG;
@@ -231,9 +235,24 @@ int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int
   args.out = dW;
   args.status = ds->status;
   args.wait_limit_ns = g_wait_limit_ns.load();
+  args.accumulate = accumulate;
   const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->kg_grid, ds->max_smem, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,
+             float* dW, cudaStream_t stream) {
+  return kgemm_impl(grad, X, offsets, E, M, N, K, dW, 0, stream);
+}
+
+int rg_kgemm_acc(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N,
+                 int K, float* dW, cudaStream_t stream) {
+  return kgemm_impl(grad, X, offsets, E, M, N, K, dW, 1, stream);
 }
 
 int rg_get_device_status(cudaStream_t stream, uint32_t* status) {

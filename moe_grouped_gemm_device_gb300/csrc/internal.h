@@ -18,6 +18,7 @@ struct GroupArgs {
   void* out;                // y (bf16) for Mgemm, dW (fp32) for Kgemm
   unsigned int* status;     // device status word
   unsigned long long wait_limit_ns;
+  int accumulate;           // Kgemm: 1 = dW += result, 0 = dW = result
 };
 
 // CTA group of the tensor-core MMAs: 2 (default) = a CTA pair computes one

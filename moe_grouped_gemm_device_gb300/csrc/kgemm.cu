@@ -408,8 +408,9 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     // tcgen05.ld, hands the accumulator back at once -- so the MMAs of the
     // next-but-one tile never wait for the stores -- and then writes the four
     // 32x32 fp32 boxes: registers -> swizzled staging buffer -> TMA store
-    // (whole 128-byte lines).  The first chunk of an expert's rows is stored,
-    // later chunks are TMA reduce-added; before a later chunk the warp waits
+    // (whole 128-byte lines).  The first chunk of an expert's rows is stored
+    // (reduce-added when accumulating into dW), later chunks are TMA
+    // reduce-added; before a later chunk the warp waits
     // until its previous writes have landed, so the adds are applied in chunk
     // order (deterministic).
     const int q = warp & 3;
@@ -444,8 +445,8 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
       const int kh = (local % nbk) * BN + h * (BN / 2);  // first dW column of this warp
       const int r_begin = s_off[e], r_end = s_off[e + 1];
       const bool warp_rows = n0 + q * 32 < N;  // this warp's 32 rows of dW exist
-      if (r_end == r_begin) {  // expert without rows: dW tile = 0
-        if (!warp_rows) continue;
+      if (r_end == r_begin) {  // expert without rows: dW tile = 0 (unchanged when accumulating)
+        if (!warp_rows || args.accumulate) continue;
         uint32_t z[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) z[j] = 0u;
@@ -461,6 +462,7 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
       }
       for (int cr = r_begin; cr < r_end; cr += CHUNK_ROWS) {
         const bool first = cr == r_begin;
+        const bool overwrite = first && !args.accumulate;
         const int buf = acc & 1;
         const uint32_t tph = (acc >> 1) & 1;
         ++acc;
@@ -484,7 +486,7 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
           if (kh + 32 * c >= K) break;
           stage_box(v + 32 * c);
           if (lane == 0) {
-            if (first)
+            if (overwrite)
               tma_store_3d(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e);
             else
               tma_reduce_add_3d(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e);

@@ -65,10 +65,11 @@ def test_mgemm_rejects_bad_arguments(lib, args):
     [dict(grad=None), dict(X=None), dict(dW=None), dict(offsets=None), dict(dW=BAD),
      dict(E=0), dict(N=7), dict(K=0), dict(M=-5)],
 )
-def test_kgemm_rejects_bad_arguments(lib, args):
+@pytest.mark.parametrize("fn", ["rg_kgemm", "rg_kgemm_acc"])
+def test_kgemm_rejects_bad_arguments(lib, args, fn):
     a = dict(grad=DEV, X=DEV, offsets=DEV, E=4, M=512, N=128, K=256, dW=DEV, s=None)
     a.update(args)
-    rc = lib.rg_kgemm(a["grad"], a["X"], a["offsets"], a["E"], a["M"], a["N"], a["K"], a["dW"], a["s"])
+    rc = getattr(lib, fn)(a["grad"], a["X"], a["offsets"], a["E"], a["M"], a["N"], a["K"], a["dW"], a["s"])
     assert rc == rg.RG_ERR_INVALID_ARG
 
 

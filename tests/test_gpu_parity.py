@@ -92,6 +92,45 @@ def test_kgemm_long_experts_random(gpu_lib):
     check_fp32(dW, oracle.kgemm(g, x, off), "long experts")
 
 
+# ------------------------------------------------------------ accumulation
+
+
+def run_kgemm_acc(rg, g, x, off, init):
+    import torch
+    dW = torch.from_numpy(np.ascontiguousarray(init, dtype=np.float32)).cuda()
+    rg.kgemm(to_dev(g), to_dev(x), offsets_dev(off), out=dW, accumulate=True)
+    torch.cuda.synchronize()
+    assert rg.device_status() == 0
+    return dW.cpu().numpy()
+
+
+def test_kgemm_accumulate_bit_exact(gpu_lib):
+    """dW += sum: integer data keeps every partial sum exact, including the
+    chunk-by-chunk additions of experts longer than 4096 rows; the empty
+    expert keeps its initial values."""
+    counts = [5000, 0, 130, 1]
+    off = W.offsets_from_counts(counts)
+    M, N, K = int(off[-1]) + 3, 256, 192
+    g = ints((M, N), 8, 0)
+    x = ints((M, K), 8, 1)
+    init = np.random.default_rng(8).integers(-50, 51, size=(4, N, K)).astype(np.float32)
+    dW = run_kgemm_acc(gpu_lib, g, x, off, init)
+    np.testing.assert_array_equal(dW.astype(np.float64), init.astype(np.float64) + oracle.kgemm(g, x, off))
+    np.testing.assert_array_equal(dW[1], init[1])
+
+
+def test_kgemm_accumulate_random(gpu_lib):
+    counts = [3000, 700, 0, 6000]
+    off = W.offsets_from_counts(counts)
+    M, N, K = int(off[-1]), 256, 512
+    g = W.normal_bf16((M, N), 1.0, 33, 0)
+    x = W.normal_bf16((M, K), 1.0, 33, 1)
+    init = np.random.default_rng(9).standard_normal((4, N, K)).astype(np.float32) * 30
+    dW = run_kgemm_acc(gpu_lib, g, x, off, init)
+    check_fp32(dW, init.astype(np.float64) + oracle.kgemm(g, x, off), "accumulate")
+    np.testing.assert_array_equal(dW[2], init[2])
+
+
 # ------------------------------------------------------------ tiny workload
 
 
