@@ -76,6 +76,28 @@ int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_
              int N, int K, int transpose_B, void* y, cudaStream_t stream);
 
 /*
+ * rg_mgemm_swiglu -- M-grouped forward gate-up GEMM with the SwiGLU
+ * activation applied in the epilogue (the fused activation named in the
+ * DeepGEMM issue discussion of wgrad utilities, "fused with SwiGLU"; the
+ * standard SwiGLU is used: h = SiLU(gate) * up, SiLU(z) = z / (1 + e^-z)).
+ *
+ *   x        device, bf16 [M, K].
+ *   w13      device, bf16 [E, 2F, K]: rows 0..F-1 of w13[e] are the gate
+ *            projection, rows F..2F-1 the up projection.
+ *   offsets  device, int32 [E+1], as for rg_mgemm.
+ *   y13      device, bf16 [M, 2F], or NULL.  If given it receives the gate-up
+ *            output x . w13[e]^T rounded to bf16 (what rg_mgemm would write),
+ *            e.g. for the backward pass.
+ *   h        device, bf16 [M, F]: h[r, f] = SiLU(g) * u with g, u the fp32
+ *            accumulators of gate column f and up column F+f, rounded to bf16
+ *            once.  Rows >= offsets[E] are not written.
+ *   F        >= 8, multiple of 8.  Other rules as for rg_mgemm.
+ * Returns RG_ERR_UNSUPPORTED in builds without CTA pairs.
+ */
+int rg_mgemm_swiglu(const void* x, const void* w13, const int32_t* offsets, int E, int64_t M,
+                    int F, int K, void* y13, void* h, cudaStream_t stream);
+
+/*
  * rg_kgemm -- K-grouped weight gradient with FP32 output.  RapidGEMM README,
  * "Kernels", Kgemm.
  *

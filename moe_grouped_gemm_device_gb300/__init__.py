@@ -24,7 +24,7 @@ import os
 
 from . import _build
 
-__all__ = ["load", "mgemm", "kgemm", "device_status", "set_wait_timeout_ns",
+__all__ = ["load", "mgemm", "mgemm_swiglu", "kgemm", "device_status", "set_wait_timeout_ns",
            "selftest_wait_timeout", "RGError", "lib_path", "version",
            "RG_DEV_BAD_OFFSETS", "RG_DEV_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -37,7 +37,7 @@ RG_DEV_TIMEOUT = 0x2
 RG_DEV_LAUNCH_CONFIG = 0x4
 RG_MAX_EXPERTS = 1024
 
-EXPORTED_SYMBOLS = ("rg_mgemm", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_set_wait_timeout_ns",
+EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_swiglu", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_set_wait_timeout_ns",
                     "rg_selftest_wait_timeout", "rg_last_cuda_error", "rg_device_supported",
                     "rg_version")
 
@@ -73,6 +73,8 @@ def load() -> ctypes.CDLL:
     vp, i32, i64, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
     lib.rg_mgemm.argtypes = [vp, vp, vp, i32, i64, i32, i32, i32, vp, vp]
     lib.rg_mgemm.restype = i32
+    lib.rg_mgemm_swiglu.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp, vp]
+    lib.rg_mgemm_swiglu.restype = i32
     lib.rg_kgemm.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp]
     lib.rg_kgemm.restype = i32
     lib.rg_kgemm_acc.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp]
@@ -154,6 +156,41 @@ def mgemm(x, w, offsets, transpose_B: bool = False, out=None, stream=None):
                           int(bool(transpose_B)), out.data_ptr(), _stream_ptr(x.device, stream))
     _check("rg_mgemm", rc)
     return out
+
+
+def mgemm_swiglu(x, w13, offsets, out=None, y13=False, stream=None):
+    """Forward gate-up GEMM with SwiGLU in the epilogue.  x [M,K] bf16, w13
+    [E,2F,K] bf16 (gate rows then up rows), offsets int32 [E+1]; returns h
+    [M,F] bf16, or (h, y13) with y13 [M,2F] bf16 when ``y13`` is True (or a
+    tensor to write into)."""
+    import torch
+    _need(x, "x", torch.bfloat16, 2)
+    _need(w13, "w13", torch.bfloat16, 3)
+    _need(offsets, "offsets", torch.int32, 1)
+    M, K = x.shape
+    E, N2 = w13.shape[0], w13.shape[1]
+    if w13.shape[2] != K or N2 % 2:
+        raise ValueError(f"w13 {tuple(w13.shape)} does not match x {tuple(x.shape)} (want [E,2F,K])")
+    F = N2 // 2
+    if offsets.shape[0] != E + 1:
+        raise ValueError(f"offsets must have E+1 = {E + 1} entries")
+    h = out if out is not None else torch.empty((M, F), dtype=torch.bfloat16, device=x.device)
+    _need(h, "out", torch.bfloat16, 2)
+    if tuple(h.shape) != (M, F):
+        raise ValueError(f"out must be [{M},{F}]")
+    y = None
+    if y13 is not False and y13 is not None:
+        y = torch.empty((M, N2), dtype=torch.bfloat16, device=x.device) if y13 is True else y13
+        _need(y, "y13", torch.bfloat16, 2)
+        if tuple(y.shape) != (M, N2):
+            raise ValueError(f"y13 must be [{M},{N2}]")
+    lib = load()
+    with torch.cuda.device(x.device):
+        rc = lib.rg_mgemm_swiglu(x.data_ptr(), w13.data_ptr(), offsets.data_ptr(), E, M, F, K,
+                                 y.data_ptr() if y is not None else None, h.data_ptr(),
+                                 _stream_ptr(x.device, stream))
+    _check("rg_mgemm_swiglu", rc)
+    return (h, y) if y is not None else h
 
 
 def kgemm(grad, X, offsets, out=None, stream=None, accumulate: bool = False):

@@ -117,6 +117,38 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, c
   return r == CUDA_SUCCESS;
 }
 
+// Row-major bf16 [rows, cols] tensor, boxes of 64 columns x box_rows rows.
+bool encode_rows(CUtensorMap* m, const void* ptr, int64_t rows, int cols, uint32_t box_rows) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+  const uint64_t str[1] = {static_cast<uint64_t>(cols) * 2};
+  const uint32_t box[2] = {64, box_rows};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, str, box);
+}
+
+// Forward weight [E, N, K] (K contiguous): boxes of 64 K x BN_CTA rows.
+bool encode_weight(CUtensorMap* m, const void* w, int E, int N, int K) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
+  const uint64_t str[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2};
+  const uint32_t box[3] = {64, rg::mg::BN_CTA, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box);
+}
+
+rg::GroupArgs group_args(const DeviceState* ds, const int32_t* offsets, int E, int64_t M, int N, int K,
+                         void* out) {
+  rg::GroupArgs a;
+  a.offsets = offsets;
+  a.E = E;
+  a.M = static_cast<int>(M);
+  a.N = N;
+  a.K = K;
+  a.out = out;
+  a.out2 = nullptr;
+  a.status = ds->status;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.accumulate = 0;
+  return a;
+}
+
 int check_common(const int32_t* offsets, int E, int64_t M, int N, int K) {
   if (offsets == nullptr || (reinterpret_cast<uintptr_t>(offsets) & 3u) != 0) return RG_ERR_INVALID_ARG;
   if (E < 1 || E > RG_MAX_EXPERTS) return RG_ERR_INVALID_ARG;
@@ -145,40 +177,52 @@ int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_
   if (M == 0) return RG_OK;  // no rows, nothing to write
 
   CUtensorMap tmA, tmB, tmY;
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
-    const uint64_t str[1] = {static_cast<uint64_t>(K) * 2};
-    const uint32_t box[2] = {64, rg::mg::BM};
-    if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, str, box)) return RG_ERR_INVALID_ARG;
-  }
+  if (!encode_rows(&tmA, x, M, K, rg::mg::BM)) return RG_ERR_INVALID_ARG;
   if (!transpose_B) {  // w [E, N, K], K contiguous: one 64 x BN_CTA box per stage and CTA
-    const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
-    const uint64_t str[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2};
-    const uint32_t box[3] = {64, rg::mg::BN_CTA, 1};
-    if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box)) return RG_ERR_INVALID_ARG;
+    if (!encode_weight(&tmB, w, E, N, K)) return RG_ERR_INVALID_ARG;
   } else {  // w [E, K, N], N contiguous: 64-column boxes of 64 K rows
     const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(E)};
     const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K) * N * 2};
     const uint32_t box[3] = {64, rg::mg::BK, 1};
     if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box)) return RG_ERR_INVALID_ARG;
   }
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
-    const uint64_t str[1] = {static_cast<uint64_t>(N) * 2};
-    const uint32_t box[2] = {64, 32};
-    if (!encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, str, box)) return RG_ERR_INVALID_ARG;
-  }
-  rg::GroupArgs args;
-  args.offsets = offsets;
-  args.E = E;
-  args.M = static_cast<int>(M);
-  args.N = N;
-  args.K = K;
-  args.out = y;
-  args.status = ds->status;
-  args.wait_limit_ns = g_wait_limit_ns.load();
-  args.accumulate = 0;
+  if (!encode_rows(&tmY, y, M, N, 32)) return RG_ERR_INVALID_ARG;
+  rg::GroupArgs args = group_args(ds, offsets, E, M, N, K, y);
   const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmB, tmY, args, ds->mg_grid, stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return RG_OK;
+}
+
+int rg_mgemm_swiglu(const void* x, const void* w13, const int32_t* offsets, int E, int64_t M, int F,
+                    int K, void* y13, void* h, cudaStream_t stream) {
+  if (F < 8 || F % 8 != 0 || F > INT32_MAX / 2) return RG_ERR_INVALID_ARG;  // h rows: 16-byte strides
+  const int N = 2 * F;
+  int rc = check_common(offsets, E, M, N, K);
+  if (rc != RG_OK) return rc;
+  if (w13 == nullptr || !aligned16(w13)) return RG_ERR_INVALID_ARG;
+  if (M > 0 && (x == nullptr || h == nullptr || !aligned16(x) || !aligned16(h)))
+    return RG_ERR_INVALID_ARG;
+  if (y13 != nullptr && !aligned16(y13)) return RG_ERR_INVALID_ARG;
+  const int64_t max_tiles = (M / rg::mg::TILE_M + E) * ((F + rg::mg::BN_CTA - 1) / rg::mg::BN_CTA);
+  if (max_tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
+  if (rg::kCtaGroup != 2) return RG_ERR_UNSUPPORTED;  // gate and up halves come from the two CTAs
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != RG_OK) return rc;
+  if (rg::mgemm_smem_bytes(E) > ds->max_smem) return RG_ERR_INVALID_ARG;
+  if (M == 0) return RG_OK;
+
+  CUtensorMap tmA, tmB, tmH, tmY13;
+  if (!encode_rows(&tmA, x, M, K, rg::mg::BM)) return RG_ERR_INVALID_ARG;
+  if (!encode_weight(&tmB, w13, E, N, K)) return RG_ERR_INVALID_ARG;
+  if (!encode_rows(&tmH, h, M, F, 32)) return RG_ERR_INVALID_ARG;
+  if (y13 != nullptr) {
+    if (!encode_rows(&tmY13, y13, M, N, 32)) return RG_ERR_INVALID_ARG;
+  } else {
+    tmY13 = tmH;  // not used
+  }
+  rg::GroupArgs args = group_args(ds, offsets, E, M, N, K, h);
+  args.out2 = y13;
+  const cudaError_t e = rg::launch_mgemm_swiglu(tmA, tmB, tmH, tmY13, args, ds->mg_grid, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
 }
@@ -226,15 +270,7 @@ int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, i
     const uint32_t box[3] = {32, 32, 1};
     if (!encode(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dW, dims, str, box)) return RG_ERR_INVALID_ARG;
   }
-  rg::GroupArgs args;
-  args.offsets = offsets;
-  args.E = E;
-  args.M = static_cast<int>(M);
-  args.N = N;
-  args.K = K;
-  args.out = dW;
-  args.status = ds->status;
-  args.wait_limit_ns = g_wait_limit_ns.load();
+  rg::GroupArgs args = group_args(ds, offsets, E, M, N, K, dW);
   args.accumulate = accumulate;
   const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->kg_grid, ds->max_smem, stream);
   if (e != cudaSuccess) return fail_cuda(e);

@@ -15,7 +15,8 @@ struct GroupArgs {
   int M;                    // rows of the activation tensors
   int N;
   int K;
-  void* out;                // y (bf16) for Mgemm, dW (fp32) for Kgemm
+  void* out;                // y (bf16) for Mgemm (h for the SwiGLU variant), dW (fp32) for Kgemm
+  void* out2;               // SwiGLU variant: the gate-up output y13 (bf16), or null
   unsigned int* status;     // device status word
   unsigned long long wait_limit_ns;
   int accumulate;           // Kgemm: 1 = dW += result, 0 = dW = result
@@ -68,6 +69,12 @@ cudaError_t kgemm_max_clusters(int* clusters, int max_smem);
 cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmY, const GroupArgs& args, int grid,
                          cudaStream_t stream);
+// Forward gate-up GEMM with the SwiGLU activation in the epilogue: B = w13
+// [E, 2F, K] (gate rows then up rows), args.N = 2F, tmH/args.out = h [M, F],
+// tmY13/args.out2 = y13 [M, 2F] or null.  CTA pairs only.
+cudaError_t launch_mgemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmH,
+                                const CUtensorMap& tmY13, const GroupArgs& args, int grid,
+                                cudaStream_t stream);
 cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
                          const GroupArgs& args, int grid, size_t max_smem, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,

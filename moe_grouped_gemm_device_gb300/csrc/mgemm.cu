@@ -65,10 +65,16 @@ struct Cfg {
 
 constexpr uint32_t TMEM_COLS = 512;
 
-template <bool TRANS_B, int CG>
+// SWIGLU: forward gate-up GEMM with h = SiLU(gate) * up in the epilogue.  B
+// is w13 [E, 2F, K] with the gate rows first; a tile covers output features
+// [f0, f0+128): CTA 0 of the pair loads gate rows f0.., CTA 1 up rows F+f0..,
+// so every accumulator holds gate in columns 0..127 and up in 128..255.
+template <bool TRANS_B, int CG, bool SWIGLU = false>
 __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     mgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ CUtensorMap tmY, const GroupArgs args) {
+                 const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmY2,
+                 const GroupArgs args) {
+  static_assert(!SWIGLU || (CG == 2 && !TRANS_B), "SwiGLU variant: forward, CTA pairs");
   using C = Cfg<CG>;
   constexpr int BM = C::BM, TILE_M = C::TILE_M, BN = C::BN, BN_CTA = C::BN_CTA, BK = C::BK;
   constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
@@ -101,7 +107,9 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   const int E = args.E;
   const int N = args.N;
   const int K = args.K;
-  const int nbn = (N + BN - 1) / BN;
+  const int F = N / 2;  // SwiGLU: output features
+  // output-column blocks per row block: 256 columns, or 128 SwiGLU features
+  const int nbn = SWIGLU ? (F + BN_CTA - 1) / BN_CTA : (N + BN - 1) / BN;
   const int nk = (K + BK - 1) / BK;
 
   // ---- offsets -> shared memory, validation ---------------------------------
@@ -184,7 +192,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         while (s_pre[e + 1] <= t) ++e;
         const int local = t - s_pre[e];
         const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * BM;
-        const int n0 = (local % nbn) * BN + static_cast<int>(rank) * BN_CTA;
+        // B rows this CTA loads: its half of the 256 output columns, or (SwiGLU)
+        // the gate rows (CTA 0) / the matching up rows (CTA 1) of 128 features
+        const int n0 = SWIGLU ? (local % nbn) * BN_CTA + static_cast<int>(rank) * F
+                              : (local % nbn) * BN + static_cast<int>(rank) * BN_CTA;
         for (int kb = 0; kb < nk; ++kb) {
           if (!wait_pair(empty_bar(stage), phase ^ 1u)) {
             ok = false;
@@ -284,6 +295,33 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         else mbar_arrive(tempty_bar(buf));
       }
     };
+    // Write one 32-row x 64-column bf16 chunk of this warp (packed pairs p)
+    // to out[row0 + q*32 + lane, col0 ..]: a TMA store when all 32 rows
+    // belong to the expert and all 64 columns are below col_limit, otherwise
+    // masked 16-byte stores of the valid rows and columns.
+    auto emit = [&](const uint32_t (&p)[32], const CUtensorMap* map, __nv_bfloat16* out, int ld,
+                    int row0, int rows_valid, int col0, int col_limit) {
+      if (col0 >= col_limit) return;
+      if (q * 32 + 32 <= rows_valid && col0 + 64 <= col_limit) {
+        if (lane == 0) bulk_wait_read<0>();  // previous store has left the buffer
+        __syncwarp();
+        uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * 128);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          rowp[j ^ (lane & 7)] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(map, ebuf_s, col0, row0 + q * 32);
+          bulk_commit();
+        }
+      } else if (r_in_cta < rows_valid) {
+        uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<int64_t>(row0 + r_in_cta) * ld + col0));
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (col0 + 8 * j < col_limit) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+      }
+    };
     int acc = 0;
     int e = 0;
     for (int t = worker; t < T; t += nworkers, ++acc) {
@@ -291,7 +329,6 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       const int local = t - s_pre[e];
       const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * BM;
       const int rows_valid = min(BM, s_off[e + 1] - row0);  // <= 0: this CTA's half is past the expert
-      const int n0 = (local % nbn) * BN;
       const int buf = acc & 1;
       const uint32_t tph = (acc >> 1) & 1;
       if (!__all_sync(0xffffffffu, wait_pair(tfull_bar(buf), tph))) break;
@@ -300,42 +337,57 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         release_acc(buf);
         continue;
       }
-      const bool warp_full = q * 32 + 32 <= rows_valid;
-      const bool row_ok = r_in_cta < rows_valid;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+      if constexpr (!SWIGLU) {
+        const int n0 = (local % nbn) * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t v0[32], v1[32];
-        tmem_ld_32x32b_x32(taddr + 64 * c, v0);
-        tmem_ld_32x32b_x32(taddr + 64 * c + 32, v1);
-        tmem_ld_wait();
-        if (c == BN / 64 - 1) release_acc(buf);
-        uint32_t p[32];
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(taddr + 64 * c, v0);
+          tmem_ld_32x32b_x32(taddr + 64 * c + 32, v1);
+          tmem_ld_wait();
+          if (c == BN / 64 - 1) release_acc(buf);
+          uint32_t p[32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          p[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
-          p[16 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
-        }
-        const int col0 = n0 + 64 * c;
-        if (col0 >= N) continue;
-        if (warp_full) {
-          if (lane == 0) bulk_wait_read<0>();  // previous store has left the buffer
-          __syncwarp();
-          uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * 128);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            rowp[j ^ (lane & 7)] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmY, ebuf_s, col0, row0 + q * 32);
-            bulk_commit();
+          for (int j = 0; j < 16; ++j) {
+            p[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
+            p[16 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
           }
-        } else if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(y + (static_cast<int64_t>(row0 + r_in_cta) * N + col0));
+          emit(p, &tmY, y, N, row0, rows_valid, n0 + 64 * c, N);
+        }
+      } else {
+        // columns 0..127 hold gate(f0 + j), 128..255 up(f0 + j)
+        const int f0 = (local % nbn) * BN_CTA;
+        __nv_bfloat16* y13 = static_cast<__nv_bfloat16*>(args.out2);
+#pragma unroll 1
+        for (int c = 0; c < BN_CTA / 64; ++c) {
+          uint32_t g[64], u[64];
+          tmem_ld_32x32b_x32(taddr + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(g));
+          tmem_ld_32x32b_x32(taddr + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(g + 32));
+          tmem_ld_32x32b_x32(taddr + BN_CTA + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(u));
+          tmem_ld_32x32b_x32(taddr + BN_CTA + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+          tmem_ld_wait();
+          if (c == BN_CTA / 64 - 1) release_acc(buf);
+          uint32_t p[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (col0 + 8 * j < N) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+          for (int j = 0; j < 32; ++j) {  // SiLU(gate) * up in fp32, then bf16
+            float hv[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const float gv = __uint_as_float(g[2 * j + k]);
+              hv[k] = gv / (1.0f + __expf(-gv)) * __uint_as_float(u[2 * j + k]);
+            }
+            p[j] = pack_bf16x2(__float_as_uint(hv[0]), __float_as_uint(hv[1]));
+          }
+          emit(p, &tmY, y, F, row0, rows_valid, f0 + 64 * c, F);
+          if (y13 != nullptr) {  // keep the pre-activation for the backward pass
+#pragma unroll
+            for (int j = 0; j < 32; ++j) p[j] = pack_bf16x2(g[2 * j], g[2 * j + 1]);
+            emit(p, &tmY2, y13, N, row0, rows_valid, f0 + 64 * c, F);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) p[j] = pack_bf16x2(u[2 * j], u[2 * j + 1]);
+            emit(p, &tmY2, y13, N, row0, rows_valid, F + f0 + 64 * c, N);
+          }
         }
       }
     }
@@ -353,10 +405,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   }
 }
 
-template <bool TB>
+template <bool TB, bool SW = false>
 cudaError_t set_smem(int max_smem) {
   const int bytes = static_cast<int>(std::min<size_t>(mgemm_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem));
-  return cudaFuncSetAttribute(mgemm_kernel<TB, kCtaGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(mgemm_kernel<TB, kCtaGroup, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               bytes);
 }
 
@@ -386,6 +438,7 @@ size_t mgemm_smem_bytes(int E) {
 cudaError_t mgemm_setup(int max_smem) {
   cudaError_t e = set_smem<false>(max_smem);
   if (e != cudaSuccess) return e;
+  if (kCtaGroup == 2 && (e = set_smem<false, kCtaGroup == 2>(max_smem)) != cudaSuccess) return e;
   return set_smem<true>(max_smem);
 }
 
@@ -403,8 +456,21 @@ cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtenso
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   fill_config(&cfg, attr, grid, mgemm_smem_bytes(args.E), stream);
-  if (transpose_B) return cudaLaunchKernelEx(&cfg, mgemm_kernel<true, kCtaGroup>, tmA, tmB, tmY, args);
-  return cudaLaunchKernelEx(&cfg, mgemm_kernel<false, kCtaGroup>, tmA, tmB, tmY, args);
+  if (transpose_B) return cudaLaunchKernelEx(&cfg, mgemm_kernel<true, kCtaGroup>, tmA, tmB, tmY, tmY, args);
+  return cudaLaunchKernelEx(&cfg, mgemm_kernel<false, kCtaGroup>, tmA, tmB, tmY, tmY, args);
+}
+
+cudaError_t launch_mgemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmH,
+                                const CUtensorMap& tmY13, const GroupArgs& args, int grid,
+                                cudaStream_t stream) {
+  if constexpr (kCtaGroup != 2) {
+    return cudaErrorNotSupported;
+  } else {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    fill_config(&cfg, attr, grid, mgemm_smem_bytes(args.E), stream);
+    return cudaLaunchKernelEx(&cfg, mgemm_kernel<false, kCtaGroup, true>, tmA, tmB, tmH, tmY13, args);
+  }
 }
 
 }  // namespace rg

@@ -11,6 +11,12 @@ not rounded to any narrower type.
 
 Every function is pinned by ``tests/test_oracle.py`` against brute force,
 ordinary GEMMs, hand-worked values and invariants of the definitions.
+
+``swiglu`` follows the fused-activation mention in the DeepGEMM issue
+thread (wgrad utilities "fused with SwiGLU"); the pages do not define it, so
+the standard definition is used: the gate-up output holds the gate half in
+columns [0, F) and the up half in [F, 2F), and h = SiLU(gate) * up with
+SiLU(z) = z / (1 + exp(-z)), evaluated in FP64.
 """
 from __future__ import annotations
 
@@ -129,3 +135,13 @@ def kgemm(grad, X, offsets, sel=None) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle_kgemm_rows rejected its arguments")
     return out.reshape(E, N, K) if full else out
+
+
+def swiglu(y13) -> np.ndarray:
+    """h[r, f] = SiLU(y13[r, f]) * y13[r, F + f] in FP64, for y13 [M, 2F]
+    (float64, e.g. the exact output of ``mgemm``); rows of NaN stay NaN."""
+    y = np.asarray(y13, dtype=np.float64)
+    F = y.shape[1] // 2
+    assert y.shape[1] == 2 * F
+    gate, up = y[:, :F], y[:, F:]
+    return gate / (1.0 + np.exp(-gate)) * up

@@ -62,6 +62,19 @@ def test_mgemm_rejects_bad_arguments(lib, args):
 
 @pytest.mark.parametrize(
     "args",
+    [dict(x=None), dict(w13=None), dict(offsets=None), dict(h=None), dict(h=BAD), dict(y13=BAD),
+     dict(F=0), dict(F=4), dict(F=100), dict(F=2**30), dict(K=100), dict(E=0), dict(M=-1)],
+)
+def test_mgemm_swiglu_rejects_bad_arguments(lib, args):
+    a = dict(x=DEV, w13=DEV, offsets=DEV, E=4, M=512, F=128, K=256, y13=None, h=DEV, s=None)
+    a.update(args)
+    rc = lib.rg_mgemm_swiglu(a["x"], a["w13"], a["offsets"], a["E"], a["M"], a["F"], a["K"],
+                             a["y13"], a["h"], a["s"])
+    assert rc == rg.RG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize(
+    "args",
     [dict(grad=None), dict(X=None), dict(dW=None), dict(offsets=None), dict(dW=BAD),
      dict(E=0), dict(N=7), dict(K=0), dict(M=-5)],
 )

@@ -292,3 +292,28 @@ def test_workload_counts():
     assert (st.counts <= 7).sum() >= 32
     off = a.offsets
     assert off[0] == 0 and off[-1] == 32768 and (np.diff(off) >= 0).all()
+
+
+# ---------------------------------------------------------------- SwiGLU
+
+
+def test_swiglu_handworked_and_limits():
+    e = np.e
+    y = np.array([[0.0, 1.0, 5.0, 2.0],      # F=2: gate (0, 1), up (5, 2)
+                  [-50.0, 40.0, 3.0, -1.0]])  # gate (-50, 40), up (3, -1)
+    h = oracle.swiglu(y)
+    # by hand: silu(0)*5 = 0;  silu(1)*2 = 2/(1+1/e);  silu(-50)*3 ~ -150*e^-50;  silu(40)*-1 ~ -40
+    np.testing.assert_allclose(h[0], [0.0, 2.0 / (1.0 + 1.0 / e)], rtol=1e-15)
+    assert abs(h[1, 0]) < 1e-18 and h[1, 0] <= 0.0
+    np.testing.assert_allclose(h[1, 1], -40.0, rtol=1e-15)
+
+
+def test_swiglu_matches_library_sigmoid_and_layout():
+    scipy_special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(21)
+    y = rng.standard_normal((7, 10)) * 4
+    h = oracle.swiglu(y)
+    gate, up = y[:, :5], y[:, 5:]
+    np.testing.assert_allclose(h, gate * scipy_special.expit(gate) * up, rtol=1e-13, atol=1e-300)
+    # swapping the halves changes the result (the gate half is the first one)
+    assert not np.allclose(h, oracle.swiglu(np.concatenate([up, gate], axis=1)))
