@@ -98,6 +98,27 @@ int rg_mgemm_swiglu(const void* x, const void* w13, const int32_t* offsets, int 
                     int F, int K, void* y13, void* h, cudaStream_t stream);
 
 /*
+ * rg_mgemm_swiglu_dgrad -- input gradient of the down projection followed by
+ * the SwiGLU backward, in one M-grouped GEMM (the activation's backward fused
+ * with the GEMM, per the same DeepGEMM issue discussion).
+ *
+ *   dy       device, bf16 [M, K]: gradient of the down projection's output.
+ *   w2       device, bf16 [E, K, F]: the down projection's weight in its
+ *            forward layout (rg_mgemm with w2 computes y = h . w2[e]^T).
+ *   offsets  device, int32 [E+1], as for rg_mgemm.
+ *   y13      device, bf16 [M, 2F]: the gate-up output saved by the forward
+ *            pass (rg_mgemm_swiglu's y13).  Must not overlap dy13.
+ *   dy13     device, bf16 [M, 2F]: with dh = dy . w2[e] kept in fp32, g, u the
+ *            gate and up values of y13 and s = 1 / (1 + e^-g):
+ *              dy13[r, f]     = dh[r, f] * u * s * (1 + g * (1 - s))
+ *              dy13[r, F + f] = dh[r, f] * g * s
+ *            rounded to bf16 once.  Rows >= offsets[E] are not written.
+ *   F        >= 8, multiple of 8; K >= 8, multiple of 8.
+ */
+int rg_mgemm_swiglu_dgrad(const void* dy, const void* w2, const int32_t* offsets, int E, int64_t M,
+                          int F, int K, const void* y13, void* dy13, cudaStream_t stream);
+
+/*
  * rg_kgemm -- K-grouped weight gradient with FP32 output.  RapidGEMM README,
  * "Kernels", Kgemm.
  *

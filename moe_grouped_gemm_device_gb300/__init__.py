@@ -24,7 +24,7 @@ import os
 
 from . import _build
 
-__all__ = ["load", "mgemm", "mgemm_swiglu", "kgemm", "device_status", "set_wait_timeout_ns",
+__all__ = ["load", "mgemm", "mgemm_swiglu", "mgemm_swiglu_dgrad", "kgemm", "device_status", "set_wait_timeout_ns",
            "selftest_wait_timeout", "RGError", "lib_path", "version",
            "RG_DEV_BAD_OFFSETS", "RG_DEV_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -37,7 +37,7 @@ RG_DEV_TIMEOUT = 0x2
 RG_DEV_LAUNCH_CONFIG = 0x4
 RG_MAX_EXPERTS = 1024
 
-EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_swiglu", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_set_wait_timeout_ns",
+EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_set_wait_timeout_ns",
                     "rg_selftest_wait_timeout", "rg_last_cuda_error", "rg_device_supported",
                     "rg_version")
 
@@ -75,6 +75,8 @@ def load() -> ctypes.CDLL:
     lib.rg_mgemm.restype = i32
     lib.rg_mgemm_swiglu.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp, vp]
     lib.rg_mgemm_swiglu.restype = i32
+    lib.rg_mgemm_swiglu_dgrad.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp, vp]
+    lib.rg_mgemm_swiglu_dgrad.restype = i32
     lib.rg_kgemm.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp]
     lib.rg_kgemm.restype = i32
     lib.rg_kgemm_acc.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp]
@@ -191,6 +193,35 @@ def mgemm_swiglu(x, w13, offsets, out=None, y13=False, stream=None):
                                  _stream_ptr(x.device, stream))
     _check("rg_mgemm_swiglu", rc)
     return (h, y) if y is not None else h
+
+
+def mgemm_swiglu_dgrad(dy, w2, offsets, y13, out=None, stream=None):
+    """Input gradient of the down projection fused with the SwiGLU backward.
+    dy [M,K] bf16, w2 [E,K,F] bf16 (forward layout of the down weight), y13
+    [M,2F] bf16 saved by the forward pass; returns dy13 [M,2F] bf16."""
+    import torch
+    _need(dy, "dy", torch.bfloat16, 2)
+    _need(w2, "w2", torch.bfloat16, 3)
+    _need(offsets, "offsets", torch.int32, 1)
+    _need(y13, "y13", torch.bfloat16, 2)
+    M, K = dy.shape
+    E, F = w2.shape[0], w2.shape[2]
+    if w2.shape[1] != K:
+        raise ValueError(f"w2 {tuple(w2.shape)} does not match dy {tuple(dy.shape)} (want [E,K,F])")
+    if tuple(y13.shape) != (M, 2 * F):
+        raise ValueError(f"y13 must be [{M},{2 * F}]")
+    if offsets.shape[0] != E + 1:
+        raise ValueError(f"offsets must have E+1 = {E + 1} entries")
+    dy13 = out if out is not None else torch.empty((M, 2 * F), dtype=torch.bfloat16, device=dy.device)
+    _need(dy13, "out", torch.bfloat16, 2)
+    if tuple(dy13.shape) != (M, 2 * F):
+        raise ValueError(f"out must be [{M},{2 * F}]")
+    lib = load()
+    with torch.cuda.device(dy.device):
+        rc = lib.rg_mgemm_swiglu_dgrad(dy.data_ptr(), w2.data_ptr(), offsets.data_ptr(), E, M, F, K,
+                                       y13.data_ptr(), dy13.data_ptr(), _stream_ptr(dy.device, stream))
+    _check("rg_mgemm_swiglu_dgrad", rc)
+    return dy13
 
 
 def kgemm(grad, X, offsets, out=None, stream=None, accumulate: bool = False):

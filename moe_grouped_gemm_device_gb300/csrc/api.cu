@@ -227,6 +227,44 @@ int rg_mgemm_swiglu(const void* x, const void* w13, const int32_t* offsets, int 
   return RG_OK;
 }
 
+int rg_mgemm_swiglu_dgrad(const void* dy, const void* w2, const int32_t* offsets, int E, int64_t M,
+                          int F, int K, const void* y13, void* dy13, cudaStream_t stream) {
+  if (F < 8 || F % 8 != 0 || F > INT32_MAX / 2) return RG_ERR_INVALID_ARG;
+  int rc = check_common(offsets, E, M, 2 * F, K);
+  if (rc != RG_OK) return rc;
+  if (w2 == nullptr || !aligned16(w2)) return RG_ERR_INVALID_ARG;
+  if (M > 0) {
+    if (dy == nullptr || y13 == nullptr || dy13 == nullptr || !aligned16(dy) || !aligned16(y13) ||
+        !aligned16(dy13))
+      return RG_ERR_INVALID_ARG;
+    // y13 is read through the non-coherent cache while dy13 is written
+    const uintptr_t a = reinterpret_cast<uintptr_t>(y13), b = reinterpret_cast<uintptr_t>(dy13);
+    const uintptr_t bytes = static_cast<uintptr_t>(M) * static_cast<uintptr_t>(2 * F) * 2;
+    if (a < b + bytes && b < a + bytes) return RG_ERR_INVALID_ARG;
+  }
+  const int64_t max_tiles = (M / rg::mg::TILE_M + E) * ((F + rg::mg::BN - 1) / rg::mg::BN);
+  if (max_tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != RG_OK) return rc;
+  if (rg::mgemm_smem_bytes(E) > ds->max_smem) return RG_ERR_INVALID_ARG;
+  if (M == 0) return RG_OK;
+
+  CUtensorMap tmA, tmB, tmD;
+  if (!encode_rows(&tmA, dy, M, K, rg::mg::BM)) return RG_ERR_INVALID_ARG;
+  {  // w2 [E, K, F], F contiguous: 64-column boxes of 64 K rows
+    const uint64_t dims[3] = {static_cast<uint64_t>(F), static_cast<uint64_t>(K), static_cast<uint64_t>(E)};
+    const uint64_t str[2] = {static_cast<uint64_t>(F) * 2, static_cast<uint64_t>(K) * F * 2};
+    const uint32_t box[3] = {64, rg::mg::BK, 1};
+    if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w2, dims, str, box)) return RG_ERR_INVALID_ARG;
+  }
+  if (!encode_rows(&tmD, dy13, M, 2 * F, 32)) return RG_ERR_INVALID_ARG;
+  rg::GroupArgs args = group_args(ds, offsets, E, M, F, K, dy13);
+  args.out2 = const_cast<void*>(y13);
+  const cudaError_t e = rg::launch_mgemm_swiglu_dgrad(tmA, tmB, tmD, args, ds->mg_grid, stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return RG_OK;
+}
+
 }  // extern "C"
 
 namespace {

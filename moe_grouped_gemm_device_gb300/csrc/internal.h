@@ -16,7 +16,8 @@ struct GroupArgs {
   int N;
   int K;
   void* out;                // y (bf16) for Mgemm (h for the SwiGLU variant), dW (fp32) for Kgemm
-  void* out2;               // SwiGLU variant: the gate-up output y13 (bf16), or null
+  void* out2;               // SwiGLU: the gate-up output y13 (bf16) -- written (forward, or
+                            // null) or read (backward)
   unsigned int* status;     // device status word
   unsigned long long wait_limit_ns;
   int accumulate;           // Kgemm: 1 = dW += result, 0 = dW = result
@@ -75,6 +76,12 @@ cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtenso
 cudaError_t launch_mgemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmH,
                                 const CUtensorMap& tmY13, const GroupArgs& args, int grid,
                                 cudaStream_t stream);
+// Input gradient of the down projection fused with the SwiGLU backward:
+// A = dy [M, K], B = w2 [E, K, F] (transpose_B), args.N = F, args.out2 = y13
+// [M, 2F] (read), tmDy13/args.out = dy13 [M, 2F] (written).
+cudaError_t launch_mgemm_swiglu_dgrad(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                      const CUtensorMap& tmDy13, const GroupArgs& args, int grid,
+                                      cudaStream_t stream);
 cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
                          const GroupArgs& args, int grid, size_t max_smem, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,

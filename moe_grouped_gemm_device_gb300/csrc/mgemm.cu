@@ -65,16 +65,27 @@ struct Cfg {
 
 constexpr uint32_t TMEM_COLS = 512;
 
-// SWIGLU: forward gate-up GEMM with h = SiLU(gate) * up in the epilogue.  B
-// is w13 [E, 2F, K] with the gate rows first; a tile covers output features
-// [f0, f0+128): CTA 0 of the pair loads gate rows f0.., CTA 1 up rows F+f0..,
-// so every accumulator holds gate in columns 0..127 and up in 128..255.
-template <bool TRANS_B, int CG, bool SWIGLU = false>
+// Epilogue variants.
+//   kEpiPlain:     y = accumulator (bf16).
+//   kEpiSwiglu:    forward gate-up GEMM with h = SiLU(gate) * up in the
+//                  epilogue.  B is w13 [E, 2F, K] with the gate rows first; a
+//                  tile covers output features [f0, f0+128): CTA 0 of the pair
+//                  loads gate rows f0.., CTA 1 up rows F+f0.., so every
+//                  accumulator holds gate in columns 0..127 and up in 128..255.
+//   kEpiSwigluBwd: input gradient of the down projection (transpose_B,
+//                  N = F) followed by the SwiGLU backward: the accumulator is
+//                  dh, args.out2 holds the saved gate-up output y13 [M, 2F],
+//                  and the epilogue writes dy13 = [dh*up*SiLU'(gate), dh*SiLU(gate)].
+constexpr int kEpiPlain = 0, kEpiSwiglu = 1, kEpiSwigluBwd = 2;
+
+template <bool TRANS_B, int CG, int EPI = kEpiPlain>
 __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     mgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmY2,
                  const GroupArgs args) {
+  constexpr bool SWIGLU = EPI == kEpiSwiglu;
   static_assert(!SWIGLU || (CG == 2 && !TRANS_B), "SwiGLU variant: forward, CTA pairs");
+  static_assert(EPI != kEpiSwigluBwd || TRANS_B, "SwiGLU backward: input-gradient GEMM");
   using C = Cfg<CG>;
   constexpr int BM = C::BM, TILE_M = C::TILE_M, BN = C::BN, BN_CTA = C::BN_CTA, BK = C::BK;
   constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
@@ -338,7 +349,56 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         continue;
       }
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
-      if constexpr (!SWIGLU) {
+      if constexpr (EPI == kEpiSwigluBwd) {
+        // dh columns n0.. of this tile; gate/up of the same rows from y13
+        const int n0 = (local % nbn) * BN;
+        const __nv_bfloat16* y13 = static_cast<const __nv_bfloat16*>(args.out2);
+        const bool row_ok = r_in_cta < rows_valid;
+        const int64_t rbase = static_cast<int64_t>(row0 + r_in_cta) * (2 * N);
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          const int col0 = n0 + 64 * c;
+          uint4 gq[8], uq[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (row_ok && col0 + 8 * j < N) {
+              gq[j] = __ldg(reinterpret_cast<const uint4*>(y13 + rbase + col0 + 8 * j));
+              uq[j] = __ldg(reinterpret_cast<const uint4*>(y13 + rbase + N + col0 + 8 * j));
+            } else {
+              gq[j] = make_uint4(0, 0, 0, 0);
+              uq[j] = make_uint4(0, 0, 0, 0);
+            }
+          }
+          uint32_t v[64];
+          tmem_ld_32x32b_x32(taddr + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(v));
+          tmem_ld_32x32b_x32(taddr + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+          tmem_ld_wait();
+          if (c == BN / 64 - 1 || col0 + 64 >= N) release_acc(buf);
+          const uint32_t* gw = reinterpret_cast<const uint32_t*>(gq);
+          const uint32_t* uw = reinterpret_cast<const uint32_t*>(uq);
+          uint32_t pg[32], pu[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {  // fp32 math on the fp32 dh and bf16 gate/up
+            // (__expf / __fdividef: fast intrinsics, relative error ~1e-6, far
+            // below the final bf16 rounding; e^-g = inf for g << 0 gives s = 0)
+            float dg[2], du[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const float gv = __uint_as_float(k ? (gw[j] & 0xffff0000u) : (gw[j] << 16));
+              const float uv = __uint_as_float(k ? (uw[j] & 0xffff0000u) : (uw[j] << 16));
+              const float dh = __uint_as_float(v[2 * j + k]);
+              const float sg = __fdividef(1.0f, 1.0f + __expf(-gv));
+              du[k] = dh * (gv * sg);
+              dg[k] = dh * uv * (sg * (1.0f + gv * (1.0f - sg)));
+            }
+            pg[j] = pack_bf16x2(__float_as_uint(dg[0]), __float_as_uint(dg[1]));
+            pu[j] = pack_bf16x2(__float_as_uint(du[0]), __float_as_uint(du[1]));
+          }
+          emit(pg, &tmY, y, 2 * N, row0, rows_valid, col0, N);
+          emit(pu, &tmY, y, 2 * N, row0, rows_valid, N + col0, 2 * N);
+          if (col0 + 64 >= N) break;
+        }
+      } else if constexpr (!SWIGLU) {
         const int n0 = (local % nbn) * BN;
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
@@ -375,7 +435,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               const float gv = __uint_as_float(g[2 * j + k]);
-              hv[k] = gv / (1.0f + __expf(-gv)) * __uint_as_float(u[2 * j + k]);
+              hv[k] = __fdividef(gv, 1.0f + __expf(-gv)) * __uint_as_float(u[2 * j + k]);
             }
             p[j] = pack_bf16x2(__float_as_uint(hv[0]), __float_as_uint(hv[1]));
           }
@@ -405,10 +465,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   }
 }
 
-template <bool TB, bool SW = false>
+template <bool TB, int EPI = kEpiPlain>
 cudaError_t set_smem(int max_smem) {
   const int bytes = static_cast<int>(std::min<size_t>(mgemm_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem));
-  return cudaFuncSetAttribute(mgemm_kernel<TB, kCtaGroup, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(mgemm_kernel<TB, kCtaGroup, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               bytes);
 }
 
@@ -438,7 +498,9 @@ size_t mgemm_smem_bytes(int E) {
 cudaError_t mgemm_setup(int max_smem) {
   cudaError_t e = set_smem<false>(max_smem);
   if (e != cudaSuccess) return e;
-  if (kCtaGroup == 2 && (e = set_smem<false, kCtaGroup == 2>(max_smem)) != cudaSuccess) return e;
+  if (kCtaGroup == 2 && (e = set_smem<false, kCtaGroup == 2 ? kEpiSwiglu : kEpiPlain>(max_smem)) != cudaSuccess)
+    return e;
+  if ((e = set_smem<true, kEpiSwigluBwd>(max_smem)) != cudaSuccess) return e;
   return set_smem<true>(max_smem);
 }
 
@@ -469,8 +531,18 @@ cudaError_t launch_mgemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, 
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     fill_config(&cfg, attr, grid, mgemm_smem_bytes(args.E), stream);
-    return cudaLaunchKernelEx(&cfg, mgemm_kernel<false, kCtaGroup, true>, tmA, tmB, tmH, tmY13, args);
+    return cudaLaunchKernelEx(&cfg, mgemm_kernel<false, kCtaGroup, kEpiSwiglu>, tmA, tmB, tmH, tmY13, args);
   }
+}
+
+cudaError_t launch_mgemm_swiglu_dgrad(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                      const CUtensorMap& tmDy13, const GroupArgs& args, int grid,
+                                      cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  fill_config(&cfg, attr, grid, mgemm_smem_bytes(args.E), stream);
+  return cudaLaunchKernelEx(&cfg, mgemm_kernel<true, kCtaGroup, kEpiSwigluBwd>, tmA, tmB, tmDy13, tmDy13,
+                            args);
 }
 
 }  // namespace rg

@@ -145,3 +145,18 @@ def swiglu(y13) -> np.ndarray:
     assert y.shape[1] == 2 * F
     gate, up = y[:, :F], y[:, F:]
     return gate / (1.0 + np.exp(-gate)) * up
+
+
+def swiglu_bwd(dh, y13) -> np.ndarray:
+    """Gradient of sum(dh * swiglu(y13)) with respect to y13, in FP64: the
+    backward of the activation that is fused after the down projection's
+    input gradient (same DeepGEMM issue discussion, "fused with SwiGLU").
+    With s = sigmoid(gate): d gate = dh * up * s * (1 + gate * (1 - s)),
+    d up = dh * gate * s.  dh [M, F], y13 [M, 2F] -> dy13 [M, 2F]."""
+    d = np.asarray(dh, dtype=np.float64)
+    y = np.asarray(y13, dtype=np.float64)
+    F = y.shape[1] // 2
+    assert y.shape[1] == 2 * F and d.shape == (y.shape[0], F)
+    gate, up = y[:, :F], y[:, F:]
+    s = 1.0 / (1.0 + np.exp(-gate))
+    return np.concatenate([d * up * s * (1.0 + gate * (1.0 - s)), d * gate * s], axis=1)

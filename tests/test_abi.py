@@ -75,6 +75,22 @@ def test_mgemm_swiglu_rejects_bad_arguments(lib, args):
 
 @pytest.mark.parametrize(
     "args",
+    [dict(dy=None), dict(w2=None), dict(y13=None), dict(dy13=None), dict(y13=BAD), dict(F=4),
+     dict(F=100), dict(K=12), dict(E=0), dict(M=-1),
+     dict(dy13=ctypes.c_void_p(0x10000 + 512 * 256 * 2 - 16)),  # overlaps y13
+     dict(y13=ctypes.c_void_p(0x10000 + 512 * 256 * 2 - 16))],
+)
+def test_mgemm_swiglu_dgrad_rejects_bad_arguments(lib, args):
+    a = dict(dy=DEV, w2=DEV, offsets=DEV, E=4, M=512, F=128, K=256, y13=DEV,
+             dy13=ctypes.c_void_p(0x10000 + 512 * 256 * 2), s=None)
+    a.update(args)
+    rc = lib.rg_mgemm_swiglu_dgrad(a["dy"], a["w2"], a["offsets"], a["E"], a["M"], a["F"], a["K"],
+                                   a["y13"], a["dy13"], a["s"])
+    assert rc == rg.RG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize(
+    "args",
     [dict(grad=None), dict(X=None), dict(dW=None), dict(offsets=None), dict(dW=BAD),
      dict(E=0), dict(N=7), dict(K=0), dict(M=-5)],
 )

@@ -118,3 +118,79 @@ def test_swiglu_zero_rows(gpu_lib):
     torch.cuda.synchronize()
     assert h.shape == (0, 128) and y13.shape == (0, 256)
     assert gpu_lib.device_status() == 0
+
+
+# ------------------------------------------------------------ backward
+
+
+def run_swiglu_dgrad(rg, dy, w2, off, y13):
+    import torch
+    M, F = dy.shape[0], w2.shape[2]
+    dy13 = torch.empty((M, 2 * F), dtype=torch.bfloat16, device="cuda")
+    dy13.view(torch.int16).fill_(SENTINEL_BF16)
+    rg.mgemm_swiglu_dgrad(to_dev(dy), to_dev(w2), offsets_dev(off), to_dev(y13), out=dy13)
+    torch.cuda.synchronize()
+    assert rg.device_status() == 0
+    return to_host_bits(dy13)
+
+
+def check_bwd_case(rg, counts, tail, F, K, seed, gate_scale=2.0):
+    off = W.offsets_from_counts(counts)
+    E = len(counts)
+    M = int(off[-1]) + tail
+    dy = W.normal_bf16((M, K), 1.0, seed, 0)
+    w2 = W.normal_bf16((E, K, F), 1.0 / np.sqrt(K), seed, 1)
+    y13 = W.normal_bf16((M, 2 * F), gate_scale, seed, 2)
+    dy13 = run_swiglu_dgrad(rg, dy, w2, off, y13)
+    valid = int(off[-1])
+    if valid:
+        dh = oracle.mgemm(dy, w2, off, transpose_B=True)
+        ref = oracle.swiglu_bwd(dh[:valid], W.bf16_bits_to_f32(y13[:valid]))
+        check_bf16(dy13[:valid], ref, "swiglu_dgrad")
+    assert (dy13[valid:] == SENTINEL_BF16).all(), "rows past offsets[E] were written"
+
+
+BWD_CASES = {
+    "ragged_rows": dict(counts=[300, 0, 1, 129, 77], tail=5, F=256, K=192),
+    "F_not_tile_multiple": dict(counts=[200, 90], tail=0, F=200, K=136),
+    "F_smallest": dict(counts=[5, 0, 9], tail=2, F=8, K=8),
+    "F_320": dict(counts=[40, 300], tail=1, F=320, K=64),
+    "all_empty": dict(counts=[0, 0, 0], tail=64, F=128, K=64),
+    "many_experts": dict(counts=list(np.random.default_rng(7).integers(0, 40, size=300)), tail=11,
+                         F=128, K=64),
+}
+
+
+@pytest.mark.parametrize("case", sorted(BWD_CASES))
+def test_swiglu_dgrad_cases(gpu_lib, case):
+    c = BWD_CASES[case]
+    check_bwd_case(gpu_lib, c["counts"], c["tail"], c["F"], c["K"], 90 + sorted(BWD_CASES).index(case))
+
+
+def test_swiglu_dgrad_medium_a3b_shape(gpu_lib):
+    """Down-projection input gradient of one layer (hidden 2048 -> F 768) on
+    8 experts with Dirichlet-routed rows, then the SwiGLU backward."""
+    counts = W.counts_dirichlet(8, 2500, 2.0, 33)
+    check_bwd_case(gpu_lib, counts, 3, 768, 2048, 33)
+
+
+def test_swiglu_dgrad_saturated_gates(gpu_lib):
+    check_bwd_case(gpu_lib, [257, 300], 0, 256, 256, 43, gate_scale=20.0)
+
+
+def test_swiglu_forward_backward_chain(gpu_lib):
+    """y13 saved by rg_mgemm_swiglu feeds rg_mgemm_swiglu_dgrad: the result
+    matches the oracle's chain on the same bf16 y13."""
+    off = W.offsets_from_counts([190, 3, 260, 0])
+    M, D, F = int(off[-1]) + 4, 256, 384
+    x = W.normal_bf16((M, D), 1.0, 61, 0)
+    w13 = W.normal_bf16((4, 2 * F, D), 1.0 / np.sqrt(D), 61, 1)
+    w2 = W.normal_bf16((4, D, F), 1.0 / np.sqrt(F), 61, 2)
+    dy = W.normal_bf16((M, D), 1.0, 61, 3)
+    _, y13 = run_swiglu(gpu_lib, x, w13, off)
+    valid = int(off[-1])
+    y13[valid:] = 0
+    dy13 = run_swiglu_dgrad(gpu_lib, dy, w2, off, y13)
+    ref = oracle.swiglu_bwd(oracle.mgemm(dy, w2, off, transpose_B=True)[:valid],
+                            W.bf16_bits_to_f32(y13[:valid]))
+    check_bf16(dy13[:valid], ref, "swiglu_chain")

@@ -317,3 +317,34 @@ def test_swiglu_matches_library_sigmoid_and_layout():
     np.testing.assert_allclose(h, gate * scipy_special.expit(gate) * up, rtol=1e-13, atol=1e-300)
     # swapping the halves changes the result (the gate half is the first one)
     assert not np.allclose(h, oracle.swiglu(np.concatenate([up, gate], axis=1)))
+
+
+def test_swiglu_bwd_is_the_gradient_of_swiglu():
+    """Central differences of <dh, swiglu(y13)> reproduce swiglu_bwd."""
+    rng = np.random.default_rng(22)
+    y = rng.standard_normal((3, 8)) * 3
+    dh = rng.standard_normal((3, 4))
+    g = oracle.swiglu_bwd(dh, y)
+    eps = 1e-6
+    num = np.zeros_like(y)
+    for i in range(y.shape[0]):
+        for j in range(y.shape[1]):
+            yp, ym = y.copy(), y.copy()
+            yp[i, j] += eps
+            ym[i, j] -= eps
+            num[i, j] = (np.sum(dh * oracle.swiglu(yp)) - np.sum(dh * oracle.swiglu(ym))) / (2 * eps)
+    np.testing.assert_allclose(g, num, rtol=1e-7, atol=1e-8)
+
+
+def test_swiglu_bwd_matches_autograd_and_handworked():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(23)
+    y = rng.standard_normal((5, 12)) * 4
+    dh = rng.standard_normal((5, 6))
+    yt = torch.tensor(y, requires_grad=True)
+    h = torch.nn.functional.silu(yt[:, :6]) * yt[:, 6:]
+    h.backward(torch.tensor(dh))
+    np.testing.assert_allclose(oracle.swiglu_bwd(dh, y), yt.grad.numpy(), rtol=1e-12, atol=1e-14)
+    # gate 0: s = 1/2, so d gate = dh*up/2 and d up = 0; a large gate passes dh through
+    d = oracle.swiglu_bwd(np.array([[2.0, 1.0]]), np.array([[0.0, 60.0, 3.0, 5.0]]))
+    np.testing.assert_allclose(d[0], [3.0, 5.0, 0.0, 60.0], rtol=1e-12, atol=1e-20)
