@@ -15,6 +15,10 @@ Metric: grouped-GEMM TFLOP/s = sum over calls of 2*sum_e(M_e)*N*K / time.
 
     python bench.py [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
+``--workload a3b_swiglu`` (or skewed_tail_swiglu) runs the same layer with
+the SwiGLU activation fused into the gate-up forward and into the down
+projection's input gradient.
+
 prints one JSON line.  ``--impl reference`` times the CPU oracle on the same
 workload (a bounded sample of it per step) on the host cores.
 """
@@ -38,8 +42,10 @@ import workloads as W  # noqa: E402
 
 L2_BYTES = 129 * 2**20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_OF = {"mgemm": "mgemm_kernel<false>", "mgemm_t": "mgemm_kernel<true>", "kgemm": "kgemm_kernel"}
+KERNEL_OF = {"mgemm": "mgemm_kernel<false>", "mgemm_t": "mgemm_kernel<true>", "kgemm": "kgemm_kernel",
+             "swiglu": "mgemm_kernel<false,swiglu>", "swiglu_bwd": "mgemm_kernel<true,swiglu_bwd>"}
 KERNEL_SOURCES = {"mgemm_kernel<false>": "mgemm.cu", "mgemm_kernel<true>": "mgemm.cu",
+                  "mgemm_kernel<false,swiglu>": "mgemm.cu", "mgemm_kernel<true,swiglu_bwd>": "mgemm.cu",
                   "kgemm_kernel": "kgemm.cu"}
 
 
@@ -66,6 +72,8 @@ def load_peaks():
 
 
 def kernel_of(op) -> str:
+    if op.fuse:
+        return KERNEL_OF[op.fuse]
     if op.kind == "kgemm":
         return KERNEL_OF["kgemm"]
     return KERNEL_OF["mgemm_t" if op.transpose_B else "mgemm"]
@@ -77,7 +85,12 @@ def algorithmic_bytes(op, counts) -> int:
     if op.kind == "kgemm":
         return 2 * M * op.N + 2 * M * op.K + 4 * E * op.N * op.K
     nonempty = int(np.count_nonzero(counts))
-    return 2 * M * op.K + 2 * op.N * op.K * nonempty + 2 * M * op.N
+    operands = 2 * M * op.K + 2 * op.N * op.K * nonempty
+    if op.fuse == "swiglu":      # h [M, N/2] and y13 [M, N] written
+        return operands + 2 * M * (op.N // 2) + 2 * M * op.N
+    if op.fuse == "swiglu_bwd":  # y13 [M, 2N] read, dy13 [M, 2N] written
+        return operands + 2 * 2 * M * (2 * op.N)
+    return operands + 2 * M * op.N
 
 
 def workload_desc(wl) -> str:
@@ -92,7 +105,14 @@ def working_set_bytes(wl) -> int:
     for name, (shape, _, _) in wl.tensors.items():
         tot += 2 * int(np.prod(shape))
     for op in wl.ops:
-        tot += (4 * wl.E * op.N * op.K) if op.kind == "kgemm" else 2 * wl.M * op.N
+        if op.kind == "kgemm":
+            tot += 4 * wl.E * op.N * op.K
+        elif op.fuse == "swiglu":
+            tot += 2 * wl.M * (op.N // 2) + 2 * wl.M * op.N
+        elif op.fuse == "swiglu_bwd":
+            tot += 2 * wl.M * 2 * op.N
+        else:
+            tot += 2 * wl.M * op.N
     return tot
 
 
@@ -168,7 +188,11 @@ def oracle_sample_step(wl, tensors, budget_s: float, rng) -> tuple[float, float,
 
             def run(n):
                 rows = rng.integers(0, int(off[-1]), size=n)
-                oracle.mgemm(a, b, off, transpose_B=op.transpose_B, rows=rows)
+                y = oracle.mgemm(a, b, off, transpose_B=op.transpose_B, rows=rows)
+                if op.fuse == "swiglu":
+                    oracle.swiglu(y)
+                elif op.fuse == "swiglu_bwd":
+                    oracle.swiglu_bwd(y, W.bf16_bits_to_f32(tensors[op.c][rows]))
                 return n * unit
         else:
             nz = np.flatnonzero(counts)
@@ -261,7 +285,7 @@ def main():
         keep = args.ops.split(",")
         wl.ops = [o for o in wl.ops if o.name in keep]
         assert wl.ops, f"no op of {wl.name} matches {keep}"
-        used = {o.a for o in wl.ops} | {o.b for o in wl.ops}
+        used = {o.a for o in wl.ops} | {o.b for o in wl.ops} | {o.c for o in wl.ops if o.c}
         wl.tensors = {k: v for k, v in wl.tensors.items() if k in used}
     if args.impl == "reference":
         return run_reference(args, wl)
@@ -295,6 +319,11 @@ def main():
     for op in wl.ops:
         if op.kind == "kgemm":
             outs[op.name] = torch.empty((wl.E, op.N, op.K), dtype=torch.float32, device=dev)
+        elif op.fuse == "swiglu":
+            outs[op.name] = torch.empty((wl.M, op.N // 2), dtype=torch.bfloat16, device=dev)
+            outs[op.name + ":y13"] = torch.empty((wl.M, op.N), dtype=torch.bfloat16, device=dev)
+        elif op.fuse == "swiglu_bwd":
+            outs[op.name] = torch.empty((wl.M, 2 * op.N), dtype=torch.bfloat16, device=dev)
         else:
             outs[op.name] = torch.empty((wl.M, op.N), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -302,6 +331,10 @@ def main():
     def call(op, tens, out):
         if op.kind == "kgemm":
             rg.kgemm(tens[op.a], tens[op.b], off_used[0], out=out)
+        elif op.fuse == "swiglu":
+            rg.mgemm_swiglu(tens[op.a], tens[op.b], off_used[0], out=out, y13=outs[op.name + ":y13"])
+        elif op.fuse == "swiglu_bwd":
+            rg.mgemm_swiglu_dgrad(tens[op.a], tens[op.b], off_used[0], tens[op.c], out=out)
         else:
             rg.mgemm(tens[op.a], tens[op.b], off_used[0], transpose_B=op.transpose_B, out=out)
 

@@ -65,6 +65,39 @@ CASES = [("uniform8", "fwd"), ("uniform16", "fwd")] + [
     for op in ("fwd_gate_up", "fwd_down", "dgrad_down", "dgrad_gate_up", "wgrad_gw2", "wgrad_gw13")]
 
 
+FUSED = [(w, op) for w in ("a3b_swiglu", "skewed_tail_swiglu")
+         for op in ("fwd_gate_up_swiglu", "dgrad_down_swiglu")]
+
+
+@pytest.mark.parametrize("wname,opname", FUSED, ids=[f"{w}-{o}" for w, o in FUSED])
+def test_full_size_sampled_swiglu(gpu_lib, wname, opname):
+    import torch
+    wl = W.ALL[wname]()
+    op = wl.op(opname)
+    off = wl.offsets
+    rng = np.random.default_rng(zlib.crc32(f"{wname}/{opname}".encode()))
+    a_h, b_h = host_tensor(wl, op.a), host_tensor(wl, op.b)
+    a_d, b_d = dev_tensor(wl, op.a), dev_tensor(wl, op.b)
+    doff = offsets_dev(off)
+    rows = sample_rows(off, rng)
+    sel = torch.from_numpy(rows).cuda()
+    if op.fuse == "swiglu":
+        h, y13 = gpu_lib.mgemm_swiglu(a_d, b_d, doff, y13=True)
+        torch.cuda.synchronize()
+        assert gpu_lib.device_status() == 0
+        y_ref = oracle.mgemm(a_h, b_h, off, rows=rows)
+        check_bf16(to_host_bits(y13[sel]), y_ref, f"{wname}/{opname}/y13")
+        check_bf16(to_host_bits(h[sel]), oracle.swiglu(y_ref), f"{wname}/{opname}/h")
+    else:
+        c_h, c_d = host_tensor(wl, op.c), dev_tensor(wl, op.c)
+        dy13 = gpu_lib.mgemm_swiglu_dgrad(a_d, b_d, doff, c_d)
+        torch.cuda.synchronize()
+        assert gpu_lib.device_status() == 0
+        dh = oracle.mgemm(a_h, b_h, off, transpose_B=True, rows=rows)
+        ref = oracle.swiglu_bwd(dh, W.bf16_bits_to_f32(c_h[rows]))
+        check_bf16(to_host_bits(dy13[sel]), ref, f"{wname}/{opname}")
+
+
 @pytest.mark.parametrize("wname,opname", CASES, ids=[f"{w}-{o}" for w, o in CASES])
 def test_full_size_sampled(gpu_lib, wname, opname):
     import torch

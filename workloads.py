@@ -190,6 +190,12 @@ class Op:
     N: int
     K: int
     transpose_B: bool = False
+    # "" (plain GEMM), "swiglu" (forward gate-up with SwiGLU in the epilogue:
+    # writes h [M, N/2] and y13 [M, N]) or "swiglu_bwd" (input gradient of the
+    # down projection followed by the SwiGLU backward; ``c`` names the saved
+    # y13 [M, 2N] it reads, and it writes dy13 [M, 2N])
+    fuse: str = ""
+    c: str = ""
 
     def flops(self, counts) -> int:
         return 2 * int(np.sum(counts)) * self.N * self.K
@@ -247,6 +253,28 @@ def _layer(name, seed, E, M, counts, d_model, d_ffn2, d_ffn):
     return w
 
 
+def with_swiglu(w: Workload) -> Workload:
+    """The same layer with the SwiGLU activation fused into its GEMMs: the
+    gate-up forward also applies SwiGLU (h = SiLU(gate) * up), and the
+    down projection's input gradient also applies the SwiGLU backward to a
+    saved gate-up output y13 ~N(0,1).  GEMM shapes and FLOPs are unchanged."""
+    import copy
+    f = copy.deepcopy(w)
+    f.name = w.name + "_swiglu"
+    d_ffn2 = w.op("fwd_gate_up").N
+    f.tensors["y13"] = ((w.M, d_ffn2), 1.0, 7)
+    ops = []
+    for o in w.ops:
+        if o.name == "fwd_gate_up":
+            o = Op("fwd_gate_up_swiglu", "mgemm", o.a, o.b, N=o.N, K=o.K, fuse="swiglu")
+        elif o.name == "dgrad_down":
+            o = Op("dgrad_down_swiglu", "mgemm", o.a, o.b, N=o.N, K=o.K, transpose_B=True,
+                   fuse="swiglu_bwd", c="y13")
+        ops.append(o)
+    f.ops = ops
+    return f
+
+
 def tiny() -> Workload:
     """E=4, K=256, N=128, M=512, expert 2 empty (seed 0)."""
     c = counts_tiny(0)
@@ -299,4 +327,6 @@ ALL = {
     "a3b": a3b_layer,
     "skewed": lambda: skewed(False),
     "skewed_tail": lambda: skewed(True),
+    "a3b_swiglu": lambda: with_swiglu(a3b_layer()),
+    "skewed_tail_swiglu": lambda: with_swiglu(skewed(True)),
 }
