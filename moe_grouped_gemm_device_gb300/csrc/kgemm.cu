@@ -56,7 +56,10 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_WARPS = 8;              // two per TMEM lane quarter
   static constexpr int EPI_BUF_BYTES = 32 * 128;  // one 32x32 fp32 box per epilogue warp
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer, MMA, epilogue             // producer, MMA, 4 epilogue
+  // warp 0 and the last warp: TMA producers (alternate stages), warp 1: MMA,
+  // warps 2..9: epilogue
+  static constexpr int PRODUCER2 = 2 + EPI_WARPS;
+  static constexpr int THREADS = 32 * (PRODUCER2 + 1);
   // full[S], empty[S], ready[S], tfull[2], tempty[2], drain
   static constexpr int NUM_BARS = 3 * STAGES + 5;
   // The dynamic shared-memory window of a CTA without static shared memory
@@ -67,6 +70,10 @@ struct Cfg {
 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int CHUNK_ROWS = kg::CHUNK_ROWS;
+
+#ifndef RG_KG_ORDER_MIX
+#define RG_KG_ORDER_MIX 0
+#endif
 
 template <int CG, int ST>
 __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
@@ -166,9 +173,20 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
   // worker w takes tiles w, w+W, ..., so every round of W tiles has
   // near-equal cost.
   auto tile_at = [&](int t, int& e, int& local) {
-    const int p = t / tpe;
-    e = s_ord[p];
-    local = t - p * tpe;
+#if RG_KG_ORDER_MIX
+    int p = t;
+    {
+      const int r = t / nworkers, j = t - r * nworkers;
+      if ((nworkers & 1) == 0 && (r + 1) * nworkers <= T) p = r * nworkers + (j + r) % nworkers;
+      const int i = p >> 1;
+      p = (p & 1) ? T - 1 - i : i;
+    }
+#else
+    const int p = t;
+#endif
+    const int pe = p / tpe;
+    e = s_ord[pe];
+    local = p - pe * tpe;
   };
   // Zero rows [lo, hi) of every box of `stage` in this CTA (whole 128-byte
   // rows, so the swizzle does not matter) and publish the writes to the async
@@ -185,11 +203,16 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     fence_proxy_async_smem();
   };
 
-  if (warp == 0) {
-    // ======================= TMA producer (one thread) =======================
+  if (warp == 0 || warp == C::PRODUCER2) {
+    // ============ TMA producers (lane 0 of warp 0 and of the last warp) =====
+    // One thread issuing every copy caps the copy rate of a CTA below what
+    // the tensor cores consume, so two threads take turns: each walks the
+    // whole (tile, row-block) sequence and fills every other stage.
     if (lane == 0) {
       tma_prefetch_desc(&tmG);
       tma_prefetch_desc(&tmX);
+      const uint32_t pid = warp == 0 ? 0u : 1u;
+      uint32_t it = 0;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;
@@ -203,6 +226,15 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         const int k0 = (local % nbk) * BN + static_cast<int>(rank) * BN_CTA;
         const int r_begin = s_off[e], r_end = s_off[e + 1];
         for (int r = r_begin; r < r_end; r += BR) {
+          const bool tail = r + BR > r_end;
+          if ((it++ & 1u) != pid) {  // the other producer's stage
+            if (rank != 0 && tail) own_par ^= 1u << stage;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (!wait_pair(empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
@@ -213,7 +245,6 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
           // barrier, which expects the bytes of the whole pair.  The expert's
           // ragged last block: each CTA's copies complete on its own full
           // barrier, so each CTA can zero its foreign rows once they landed.
-          const bool tail = r + BR > r_end;
           if (CG == 1 || tail) {
             const uint32_t fb = full_bar(stage);
             mbar_arrive_expect_tx(fb, STAGE_BYTES);

@@ -21,7 +21,8 @@
 //     bytes directly on the issuing CTA's stage barrier (.cta_group::2), and
 //     MMA completion is multicast to the barriers of both CTAs.
 //     CG = 1: one CTA computes a 128x256 tile (tcgen05 M=128), four 48 KB stages.
-//   * Warp roles (192 threads per CTA): warp 0 lane 0 issues TMA loads;
+//   * Warp roles (224 threads per CTA): lane 0 of warps 0 and 6 issue the TMA
+//     loads of alternate stages;
 //     warp 1 owns tensor memory, and in the issuing CTA lane 0 issues the MMAs
 //     into one of two 256-column fp32 accumulators; warps 2-5 drain the other
 //     accumulator
@@ -54,7 +55,10 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_WARPS = 4;
   static constexpr int EPI_BUF_BYTES = 32 * 128;
-  static constexpr int THREADS = 192;
+  // warp 0 and warp 6: TMA producers (alternate stages), warp 1: MMA,
+  // warps 2-5: epilogue
+  static constexpr int PRODUCER2 = 6;
+  static constexpr int THREADS = 224;
   // full[S], empty[S], ready[S], tfull[2], tempty[2], drain
   static constexpr int NUM_BARS = 3 * STAGES + 5;
   // The dynamic shared-memory window of a CTA without static shared memory
@@ -188,11 +192,16 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     else return mbar_wait(guard, bar, par);
   };
 
-  if (warp == 0) {
-    // ======================= TMA producer (one thread) =======================
+  if (warp == 0 || warp == C::PRODUCER2) {
+    // ============ TMA producers (lane 0 of warps 0 and 6) ====================
+    // One thread issuing every copy caps the copy rate of a CTA below what
+    // the tensor cores consume, so two threads take turns: each walks the
+    // whole (tile, k-block) sequence and fills every other stage.
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      const uint32_t pid = warp == 0 ? 0u : 1u;
+      uint32_t it = 0;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;  // stages with a load issued, and its parity
@@ -208,26 +217,28 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         const int n0 = SWIGLU ? (local % nbn) * BN_CTA + static_cast<int>(rank) * F
                               : (local % nbn) * BN + static_cast<int>(rank) * BN_CTA;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!wait_pair(empty_bar(stage), phase ^ 1u)) {
-            ok = false;
-            break;
-          }
-          // both CTAs' copies complete on the issuing CTA's full barrier,
-          // which expects the bytes of the whole pair
-          const uint32_t fb = full_issuer + 8u * stage;
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES * CG);
-          tma_load_2d_cg<CG>(sa, &tmA, fb, kb * BK, row0);
-          if constexpr (!TRANS_B) {
-            tma_load_3d_cg<CG>(sb, &tmB, fb, kb * BK, n0, e);
-          } else {
+          if ((it++ & 1u) == pid) {
+            if (!wait_pair(empty_bar(stage), phase ^ 1u)) {
+              ok = false;
+              break;
+            }
+            // both CTAs' copies complete on the issuing CTA's full barrier,
+            // which expects the bytes of the whole pair
+            const uint32_t fb = full_issuer + 8u * stage;
+            const uint32_t sa = sbase + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_BYTES;
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES * CG);
+            tma_load_2d_cg<CG>(sa, &tmA, fb, kb * BK, row0);
+            if constexpr (!TRANS_B) {
+              tma_load_3d_cg<CG>(sb, &tmB, fb, kb * BK, n0, e);
+            } else {
 #pragma unroll
-            for (int j = 0; j < BN_CTA / 64; ++j)
-              tma_load_3d_cg<CG>(sb + j * 8192, &tmB, fb, n0 + 64 * j, kb * BK, e);
+              for (int j = 0; j < BN_CTA / 64; ++j)
+                tma_load_3d_cg<CG>(sb + j * 8192, &tmB, fb, n0 + 64 * j, kb * BK, e);
+            }
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
