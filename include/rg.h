@@ -48,6 +48,8 @@ extern "C" {
 
 /* Largest number of experts one call accepts. */
 #define RG_MAX_EXPERTS 1024
+/* Largest number of outer groups of rg_mgemm_nested. */
+#define RG_MAX_OUTER 65536
 
 /*
  * rg_mgemm -- M-grouped GEMM, forward (transpose_B == 0) or input gradient
@@ -74,6 +76,37 @@ extern "C" {
  */
 int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_t M,
              int N, int K, int transpose_B, void* y, cudaStream_t stream);
+
+/*
+ * rg_mgemm_nested -- nested grouped GEMM, flattened: O outer groups split
+ * the columns of x and y, and inside each, L inner groups split the rows
+ * (CUTLASS discussion #1452, "Grouped GEMM where each subproblem is another
+ * grouped gemm instance": batched LoRA over MoE, and an A matrix [M, 3K]
+ * grouped along its columns for the outer problem and along its rows for the
+ * inner one; both levels share one row-offset vector, so the problem is
+ * flattened into O * L groups served by one launch).
+ *
+ *   x        device, bf16 [M, O*K]; outer group o reads columns o*K .. o*K+K-1.
+ *   w        device, bf16 [O, L, N, K] when transpose_B == 0,
+ *                    bf16 [O, L, K, N] when transpose_B != 0.
+ *   offsets  device, int32 [L+1], rules as for rg_mgemm with E = L; inner
+ *            group l owns rows offsets[l] .. offsets[l+1]-1 in every outer
+ *            group.
+ *   y        device, bf16 [M, O*N].  Row r of inner group l receives, for
+ *            every o and n,
+ *              y[r, o*N + n] = sum_k x[r, o*K + k] * B_{o,l}[k, n]
+ *            with B_{o,l} = w[o, l]^T (or w[o, l] with transpose_B),
+ *            accumulated in FP32 and rounded to bf16 (nearest even).  Rows
+ *            >= offsets[L] are not written.
+ *   O        1 .. RG_MAX_OUTER (O == 1 is rg_mgemm with E = L).
+ *   L        1 .. RG_MAX_EXPERTS.   N, K >= 8, multiples of 8 (K may be a
+ *            LoRA rank such as 16).  O*N, O*K and O*L must fit in int32.
+ *   Alignment, M and stream as for rg_mgemm.
+ * LoRA over MoE (adapter a, expert e) is the case O == 1 with the inner
+ * groups ordered (a, e) and w = the stacked [A*E, N, K] adapter weights.
+ */
+int rg_mgemm_nested(const void* x, const void* w, const int32_t* offsets, int O, int L, int64_t M,
+                    int N, int K, int transpose_B, void* y, cudaStream_t stream);
 
 /*
  * rg_mgemm_swiglu -- M-grouped forward gate-up GEMM with the SwiGLU

@@ -13,6 +13,9 @@ Operations (RapidGEMM README, "Kernels"):
   gradient (``transpose_B=True``: ``y = x @ w[e]``, w ``[E,K,N]``).
 * ``kgemm(grad, X, offsets)``: K-grouped weight gradient
   ``dW[e] = grad[rows of e].T @ X[rows of e]`` in FP32.
+* ``mgemm_nested(x, w, offsets)``: nested grouped GEMM (CUTLASS discussion
+  #1452): O outer groups over the columns of x ``[M,O*K]`` and y ``[M,O*N]``,
+  L inner row groups, w ``[O,L,N,K]``.
 
 ``offsets`` is a device int32 tensor ``[E+1]`` of cumulative row offsets
 with a leading zero.
@@ -24,7 +27,7 @@ import os
 
 from . import _build
 
-__all__ = ["load", "mgemm", "mgemm_swiglu", "mgemm_swiglu_dgrad", "kgemm", "device_status", "set_wait_timeout_ns",
+__all__ = ["load", "mgemm", "mgemm_nested", "mgemm_swiglu", "mgemm_swiglu_dgrad", "kgemm", "device_status", "set_wait_timeout_ns",
            "selftest_wait_timeout", "RGError", "lib_path", "version",
            "RG_DEV_BAD_OFFSETS", "RG_DEV_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -36,8 +39,9 @@ RG_DEV_BAD_OFFSETS = 0x1
 RG_DEV_TIMEOUT = 0x2
 RG_DEV_LAUNCH_CONFIG = 0x4
 RG_MAX_EXPERTS = 1024
+RG_MAX_OUTER = 65536
 
-EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_set_wait_timeout_ns",
+EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_nested", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_set_wait_timeout_ns",
                     "rg_selftest_wait_timeout", "rg_last_cuda_error", "rg_device_supported",
                     "rg_version")
 
@@ -73,6 +77,8 @@ def load() -> ctypes.CDLL:
     vp, i32, i64, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
     lib.rg_mgemm.argtypes = [vp, vp, vp, i32, i64, i32, i32, i32, vp, vp]
     lib.rg_mgemm.restype = i32
+    lib.rg_mgemm_nested.argtypes = [vp, vp, vp, i32, i32, i64, i32, i32, i32, vp, vp]
+    lib.rg_mgemm_nested.restype = i32
     lib.rg_mgemm_swiglu.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp, vp]
     lib.rg_mgemm_swiglu.restype = i32
     lib.rg_mgemm_swiglu_dgrad.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp, vp]
@@ -157,6 +163,40 @@ def mgemm(x, w, offsets, transpose_B: bool = False, out=None, stream=None):
         rc = lib.rg_mgemm(x.data_ptr(), w.data_ptr(), offsets.data_ptr(), E, M, N, K,
                           int(bool(transpose_B)), out.data_ptr(), _stream_ptr(x.device, stream))
     _check("rg_mgemm", rc)
+    return out
+
+
+def mgemm_nested(x, w, offsets, transpose_B: bool = False, out=None, stream=None):
+    """Nested grouped GEMM, flattened into one launch.  x [M, O*K] bf16, w
+    [O,L,N,K] (or [O,L,K,N] with transpose_B) bf16, offsets int32 [L+1];
+    returns y [M, O*N] bf16 with y[r, o*N:(o+1)*N] = x[r, o*K:(o+1)*K] @ B_{o,l}
+    for row r of inner group l.  Rows at or past offsets[L] are left as they
+    were."""
+    import torch
+    _need(x, "x", torch.bfloat16, 2)
+    _need(w, "w", torch.bfloat16, 4)
+    _need(offsets, "offsets", torch.int32, 1)
+    O, L = w.shape[0], w.shape[1]
+    if transpose_B:
+        K, N = w.shape[2], w.shape[3]
+    else:
+        N, K = w.shape[2], w.shape[3]
+    M = x.shape[0]
+    if x.shape[1] != O * K:
+        raise ValueError(f"x {tuple(x.shape)} does not match w {tuple(w.shape)} (want [M, O*K])")
+    if offsets.shape[0] != L + 1:
+        raise ValueError(f"offsets must have L+1 = {L + 1} entries")
+    if out is None:
+        out = torch.empty((M, O * N), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(out, "out", torch.bfloat16, 2)
+        if tuple(out.shape) != (M, O * N):
+            raise ValueError(f"out must be [{M},{O * N}]")
+    lib = load()
+    with torch.cuda.device(x.device):
+        rc = lib.rg_mgemm_nested(x.data_ptr(), w.data_ptr(), offsets.data_ptr(), O, L, M, N, K,
+                                 int(bool(transpose_B)), out.data_ptr(), _stream_ptr(x.device, stream))
+    _check("rg_mgemm_nested", rc)
     return out
 
 

@@ -146,6 +146,7 @@ rg::GroupArgs group_args(const DeviceState* ds, const int32_t* offsets, int E, i
   a.status = ds->status;
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.accumulate = 0;
+  a.outer = 1;
   return a;
 }
 
@@ -188,6 +189,57 @@ int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_
   }
   if (!encode_rows(&tmY, y, M, N, 32)) return RG_ERR_INVALID_ARG;
   rg::GroupArgs args = group_args(ds, offsets, E, M, N, K, y);
+  const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmB, tmY, args, ds->mg_grid, stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return RG_OK;
+}
+
+int rg_mgemm_nested(const void* x, const void* w, const int32_t* offsets, int O, int L, int64_t M, int N,
+                    int K, int transpose_B, void* y, cudaStream_t stream) {
+  if (O < 1 || O > RG_MAX_OUTER) return RG_ERR_INVALID_ARG;
+  int rc = check_common(offsets, L, M, N, K);
+  if (rc != RG_OK) return rc;
+  if (static_cast<int64_t>(O) * N > INT32_MAX || static_cast<int64_t>(O) * K > INT32_MAX ||
+      static_cast<int64_t>(O) * L > INT32_MAX)
+    return RG_ERR_INVALID_ARG;
+  if (w == nullptr || !aligned16(w)) return RG_ERR_INVALID_ARG;
+  if (M > 0 && (x == nullptr || y == nullptr || !aligned16(x) || !aligned16(y)))
+    return RG_ERR_INVALID_ARG;
+  const int64_t max_tiles = (M / rg::mg::TILE_M + L) * ((N + rg::mg::BN - 1) / rg::mg::BN) * O;
+  if (max_tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != RG_OK) return rc;
+  if (rg::mgemm_smem_bytes(L) > ds->max_smem) return RG_ERR_INVALID_ARG;
+  if (M == 0) return RG_OK;
+
+  // The weights of all (outer, inner) groups form one stack of O*L matrices.
+  const int G = O * L;
+  CUtensorMap tmA, tmB, tmY;
+  if (O == 1) {
+    if (!encode_rows(&tmA, x, M, K, rg::mg::BM)) return RG_ERR_INVALID_ARG;
+    if (!encode_rows(&tmY, y, M, N, 32)) return RG_ERR_INVALID_ARG;
+  } else {
+    // x [M, O*K] as {K, O, M}; y [M, O*N] as {N, O, M}: one outer group's
+    // column block per box, so a box never reads or writes a neighbour's columns
+    const uint64_t xd[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(O), static_cast<uint64_t>(M)};
+    const uint64_t xs[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(O) * K * 2};
+    const uint32_t xb[3] = {64, 1, rg::mg::BM};
+    if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, xd, xs, xb)) return RG_ERR_INVALID_ARG;
+    const uint64_t yd[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(O), static_cast<uint64_t>(M)};
+    const uint64_t ys[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(O) * N * 2};
+    const uint32_t yb[3] = {64, 1, 32};
+    if (!encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, yd, ys, yb)) return RG_ERR_INVALID_ARG;
+  }
+  if (!transpose_B) {
+    if (!encode_weight(&tmB, w, G, N, K)) return RG_ERR_INVALID_ARG;
+  } else {
+    const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(G)};
+    const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K) * N * 2};
+    const uint32_t box[3] = {64, rg::mg::BK, 1};
+    if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box)) return RG_ERR_INVALID_ARG;
+  }
+  rg::GroupArgs args = group_args(ds, offsets, L, M, N, K, y);
+  args.outer = O;
   const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmB, tmY, args, ds->mg_grid, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;

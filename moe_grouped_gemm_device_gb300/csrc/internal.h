@@ -21,6 +21,8 @@ struct GroupArgs {
   unsigned int* status;     // device status word
   unsigned long long wait_limit_ns;
   int accumulate;           // Kgemm: 1 = dW += result, 0 = dW = result
+  int outer;                // Mgemm: outer groups O along the columns of x and y (1 = plain);
+                            // with O > 1 the x and y maps are 3-D {cols, O, rows}
 };
 
 // CTA group of the tensor-core MMAs: 2 (default) = a CTA pair computes one

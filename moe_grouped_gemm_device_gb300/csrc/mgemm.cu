@@ -159,7 +159,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     if (lane == 31) s_pre[E] = incl;
   }
   __syncthreads();
-  const int T = s_pre[E];
+  // Outer groups (nested grouped GEMM): every inner tile is repeated for
+  // o = 0..O-1, tile t = inner tile (t / O), outer group (t % O).
+  const int O = args.outer;
+  const int T = s_pre[E] * O;
   if (worker >= T) return;  // same decision in both CTAs of a pair
 
   // ---- barriers and tensor memory -------------------------------------------
@@ -209,8 +212,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       int e = 0;
       const uint32_t full_issuer = CG == 2 ? mapa_shared(full_bar(0), 0) : full_bar(0);
       for (int t = worker; t < T && ok; t += nworkers) {
-        while (s_pre[e + 1] <= t) ++e;
-        const int local = t - s_pre[e];
+        const int ti = t / O, o = t - ti * O;
+        while (s_pre[e + 1] <= ti) ++e;
+        const int local = ti - s_pre[e];
+        const int eb = o * E + e;  // weight slot: w[o][e]
         const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * BM;
         // B rows this CTA loads: its half of the 256 output columns, or (SwiGLU)
         // the gate rows (CTA 0) / the matching up rows (CTA 1) of 128 features
@@ -228,13 +233,14 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_BYTES;
             if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES * CG);
-            tma_load_2d_cg<CG>(sa, &tmA, fb, kb * BK, row0);
+            if (O == 1) tma_load_2d_cg<CG>(sa, &tmA, fb, kb * BK, row0);
+            else tma_load_3d_cg<CG>(sa, &tmA, fb, kb * BK, o, row0);
             if constexpr (!TRANS_B) {
-              tma_load_3d_cg<CG>(sb, &tmB, fb, kb * BK, n0, e);
+              tma_load_3d_cg<CG>(sb, &tmB, fb, kb * BK, n0, eb);
             } else {
 #pragma unroll
               for (int j = 0; j < BN_CTA / 64; ++j)
-                tma_load_3d_cg<CG>(sb + j * 8192, &tmB, fb, n0 + 64 * j, kb * BK, e);
+                tma_load_3d_cg<CG>(sb + j * 8192, &tmB, fb, n0 + 64 * j, kb * BK, eb);
             }
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -317,10 +323,13 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         else mbar_arrive(tempty_bar(buf));
       }
     };
+    int o = 0;  // outer group of the current tile
     // Write one 32-row x 64-column bf16 chunk of this warp (packed pairs p)
     // to out[row0 + q*32 + lane, col0 ..]: a TMA store when all 32 rows
     // belong to the expert and all 64 columns are below col_limit, otherwise
-    // masked 16-byte stores of the valid rows and columns.
+    // masked 16-byte stores of the valid rows and columns.  With outer groups
+    // the map is 3-D (o selects the column block) and `out` already points
+    // at column block o of a row of length ld.
     auto emit = [&](const uint32_t (&p)[32], const CUtensorMap* map, __nv_bfloat16* out, int ld,
                     int row0, int rows_valid, int col0, int col_limit) {
       if (col0 >= col_limit) return;
@@ -334,7 +343,8 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(map, ebuf_s, col0, row0 + q * 32);
+          if (O == 1) tma_store_2d(map, ebuf_s, col0, row0 + q * 32);
+          else tma_store_3d(map, ebuf_s, col0, o, row0 + q * 32);
           bulk_commit();
         }
       } else if (r_in_cta < rows_valid) {
@@ -347,8 +357,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     int acc = 0;
     int e = 0;
     for (int t = worker; t < T; t += nworkers, ++acc) {
-      while (s_pre[e + 1] <= t) ++e;
-      const int local = t - s_pre[e];
+      const int ti = t / O;
+      o = t - ti * O;
+      while (s_pre[e + 1] <= ti) ++e;
+      const int local = ti - s_pre[e];
       const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * BM;
       const int rows_valid = min(BM, s_off[e + 1] - row0);  // <= 0: this CTA's half is past the expert
       const int buf = acc & 1;
@@ -424,7 +436,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
             p[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
             p[16 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
           }
-          emit(p, &tmY, y, N, row0, rows_valid, n0 + 64 * c, N);
+          emit(p, &tmY, y + static_cast<int64_t>(o) * N, O * N, row0, rows_valid, n0 + 64 * c, N);
         }
       } else {
         // columns 0..127 hold gate(f0 + j), 128..255 up(f0 + j)

@@ -55,6 +55,10 @@ def _load():
                                           ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           c_p, ctypes.c_int64, c_p]
         lib.oracle_mgemm_rows.restype = ctypes.c_int
+        lib.oracle_mgemm_nested_rows.argtypes = [c_p, c_p, c_p, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, c_p, ctypes.c_int64, c_p]
+        lib.oracle_mgemm_nested_rows.restype = ctypes.c_int
         lib.oracle_kgemm_rows.argtypes = [c_p, c_p, c_p, ctypes.c_int, ctypes.c_int64,
                                           ctypes.c_int, ctypes.c_int,
                                           c_p, c_p, ctypes.c_int64, c_p]
@@ -105,6 +109,39 @@ def mgemm(x, w, offsets, transpose_B: bool = False, rows=None) -> np.ndarray:
     if full:
         y = np.full((M, N), np.nan, dtype=np.float64)
         y[: int(off[E])] = out
+        return y
+    return out
+
+
+def mgemm_nested(x, w, offsets, transpose_B: bool = False, rows=None) -> np.ndarray:
+    """Nested grouped GEMM (CUTLASS discussion #1452): O outer groups over
+    the columns, L inner groups over the rows.
+
+    x: [M, O*K] bf16 bits; w: [O, L, N, K] (or [O, L, K, N] with
+    transpose_B) bf16 bits; offsets: int32 [L+1].  Returns float64 [M, O*N]
+    with y[r, o*N + n] = sum_k x[r, o*K + k] * B_{o,l}[k, n] for r in inner
+    group l, rows >= offsets[L] set to NaN; or, when ``rows`` is given,
+    float64 [len(rows), O*N] for those rows only.
+    """
+    x, w = _u16(x), _u16(w)
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    O, L = w.shape[0], w.shape[1]
+    K, N = (w.shape[2], w.shape[3]) if transpose_B else (w.shape[3], w.shape[2])
+    M = x.shape[0]
+    assert x.shape == (M, O * K), (x.shape, w.shape)
+    assert off.shape == (L + 1,)
+    full = rows is None
+    if full:
+        rows = np.arange(int(off[L]), dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((len(rows), O * N), dtype=np.float64)
+    rc = _load().oracle_mgemm_nested_rows(_ptr(x), _ptr(w), _ptr(off), O, L, M, N, K,
+                                          int(bool(transpose_B)), _ptr(rows), len(rows), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_mgemm_nested_rows rejected its arguments")
+    if full:
+        y = np.full((M, O * N), np.nan, dtype=np.float64)
+        y[: int(off[L])] = out
         return y
     return out
 

@@ -18,6 +18,13 @@
  *       dW[e,n,k] = sum_{r in group e} grad[r,n] * X[r,k]
  *   An expert with no rows has dW[e] = 0.
  *
+ *   Nested grouped GEMM (CUTLASS discussion #1452: each subproblem of the
+ *   grouped GEMM is itself a grouped GEMM, e.g. an A matrix [M, 3K] grouped
+ *   along its columns for the outer problem and along its rows for the inner
+ *   one).  x is [M, O*K], w is [O, L, N, K] (or [O, L, K, N]), offsets [L+1]
+ *   splits the rows into inner groups shared by every outer group o:
+ *       y[r, o*N + n] = sum_k x[r, o*K + k] * w[o, l, n, k]   (r in group l)
+ *
  * Inputs are bf16 bit patterns; each value is widened exactly to double.
  * Products of two bf16 values are exact in double, so the result depends only
  * on the summation order, which is ascending k (Mgemm) or ascending r (Kgemm).
@@ -81,6 +88,37 @@ int oracle_mgemm_rows(const uint16_t *x, const uint16_t *w, const int32_t *offse
                     acc += bf16_to_double(xr[k]) * bf16_to_double(we[(int64_t)k * N + n]);
             }
             out[i * (int64_t)N + n] = acc;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Nested grouped GEMM on a list of rows.  out is [nrows, O*N] doubles:
+ * out[i, o*N + n] = y[rows[i], o*N + n].  Returns 0, or -1 on bad arguments.
+ */
+int oracle_mgemm_nested_rows(const uint16_t *x, const uint16_t *w, const int32_t *offsets,
+                             int O, int L, int64_t M, int N, int K, int transpose_B,
+                             const int64_t *rows, int64_t nrows, double *out) {
+    if (O < 1 || N < 1 || K < 1 || check_offsets(offsets, L, M) != 0) return -1;
+    for (int64_t i = 0; i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= (int64_t)offsets[L]) return -1;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int64_t r = rows[i];
+        const int l = expert_of_row(offsets, L, r);
+        for (int o = 0; o < O; ++o) {
+            const uint16_t *xr = x + r * (int64_t)O * K + (int64_t)o * K; /* x[r, o*K + :] */
+            const uint16_t *wg = w + ((int64_t)o * L + l) * N * K;        /* w[o, l] */
+            for (int n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int k = 0; k < K; ++k) {
+                    const uint16_t b = transpose_B ? wg[(int64_t)k * N + n] : wg[(int64_t)n * K + k];
+                    acc += bf16_to_double(xr[k]) * bf16_to_double(b);
+                }
+                out[i * (int64_t)O * N + (int64_t)o * N + n] = acc;
+            }
         }
     }
     return 0;

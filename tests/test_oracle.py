@@ -348,3 +348,135 @@ def test_swiglu_bwd_matches_autograd_and_handworked():
     # gate 0: s = 1/2, so d gate = dh*up/2 and d up = 0; a large gate passes dh through
     d = oracle.swiglu_bwd(np.array([[2.0, 1.0]]), np.array([[0.0, 60.0, 3.0, 5.0]]))
     np.testing.assert_allclose(d[0], [3.0, 5.0, 0.0, 60.0], rtol=1e-12, atol=1e-20)
+
+
+# ------------------------------------------------ nested grouped GEMM (CUTLASS #1452)
+
+
+@pytest.mark.parametrize("transpose_B", [False, True])
+def test_nested_golden_handworked(transpose_B):
+    g = json.load(open(os.path.join(GOLDEN, "handworked_nested.json")))
+    off = np.array(g["offsets"], dtype=np.int32)
+    y = oracle.mgemm_nested(bits(g["x"]), bits(g["w"]), off, transpose_B=transpose_B)
+    want = g["dgrad" if transpose_B else "fwd"]["y_rows_0_to_1"]
+    np.testing.assert_array_equal(y[:2], np.array(want, dtype=np.float64))
+    assert np.isnan(y[2]).all()  # row 2 belongs to no inner group
+
+
+def brute_nested(x, w, offsets, O, transpose_B):
+    """Independent pure-Python loop: outer group, inner group, row, column, k."""
+    M = len(x)
+    K = len(w[0][0]) if transpose_B else len(w[0][0][0])
+    N = len(w[0][0][0]) if transpose_B else len(w[0][0])
+    L = len(offsets) - 1
+    y = [[None] * (O * N) for _ in range(M)]
+    for o in range(O):
+        for l in range(L):
+            for r in range(offsets[l], offsets[l + 1]):
+                for n in range(N):
+                    s = 0.0
+                    for k in range(K):
+                        b = w[o][l][k][n] if transpose_B else w[o][l][n][k]
+                        s += x[r][o * K + k] * b
+                    y[r][o * N + n] = s
+    return y
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("transpose_B", [False, True])
+def test_nested_matches_brute_force(seed, transpose_B):
+    rng = np.random.default_rng(500 + seed)
+    O = int(rng.integers(1, 4))
+    L = 3
+    M = int(rng.integers(4, 11))
+    N = int(rng.integers(1, 6))
+    K = int(rng.integers(1, 6))
+    counts = rng.multinomial(M - 1, [0.5, 0.0, 0.5])  # inner group 1 empty, 1 row past offsets[L]
+    off = W.offsets_from_counts(counts)
+    x = rand_bits(rng, (M, O * K))
+    w = rand_bits(rng, (O, L, K, N) if transpose_B else (O, L, N, K))
+    y = oracle.mgemm_nested(x, w, off, transpose_B=transpose_B)
+    ref = brute_nested(f64(x).tolist(), f64(w).tolist(), off.tolist(), O, transpose_B)
+    for r in range(M):
+        if ref[r][0] is None:
+            assert np.isnan(y[r]).all()
+        else:
+            np.testing.assert_array_equal(y[r], np.array(ref[r]))
+
+
+@pytest.mark.parametrize("transpose_B", [False, True])
+def test_nested_blocks_are_ordinary_gemms_on_integers(transpose_B):
+    """Every (outer, inner) block is an ordinary GEMM of a column slice of x
+    with one weight matrix; integer inputs make both sides exact."""
+    rng = np.random.default_rng(7)
+    O, L, N, K = 3, 4, 5, 6
+    counts = np.array([3, 0, 4, 2])
+    off = W.offsets_from_counts(counts)
+    M = int(off[-1]) + 2
+    xi = rng.integers(-2, 3, size=(M, O * K))
+    wi = rng.integers(-2, 3, size=(O, L, K, N) if transpose_B else (O, L, N, K))
+    y = oracle.mgemm_nested(bits(xi), bits(wi), off, transpose_B=transpose_B)
+    for o in range(O):
+        for l in range(L):
+            r0, r1 = int(off[l]), int(off[l + 1])
+            b = wi[o, l] if transpose_B else wi[o, l].T
+            np.testing.assert_array_equal(y[r0:r1, o * N:(o + 1) * N],
+                                          (xi[r0:r1, o * K:(o + 1) * K] @ b).astype(np.float64))
+    assert np.isnan(y[int(off[-1]):]).all()
+
+
+@pytest.mark.parametrize("transpose_B", [False, True])
+def test_nested_flattens_to_grouped_gemms(transpose_B):
+    """Both flattenings of the discussion: (1) column block o equals the plain
+    grouped GEMM of x's column slice o with the weight stack w[o]; (2) LoRA over
+    MoE -- inner groups ordered (adapter, expert) with O = 1 -- equals one
+    grouped GEMM per adapter over that adapter's rows and expert stack."""
+    rng = np.random.default_rng(11)
+    O, L, N, K = 2, 6, 7, 5
+    counts = rng.multinomial(40, [1 / L] * L)
+    counts[2] = 0
+    off = W.offsets_from_counts(counts)
+    M = int(off[-1])
+    x = rand_bits(rng, (M, O * K))
+    w = rand_bits(rng, (O, L, K, N) if transpose_B else (O, L, N, K))
+    y = oracle.mgemm_nested(x, w, off, transpose_B=transpose_B)
+    for o in range(O):
+        xo = np.ascontiguousarray(x[:, o * K:(o + 1) * K])
+        np.testing.assert_array_equal(y[:, o * N:(o + 1) * N],
+                                      oracle.mgemm(xo, w[o], off, transpose_B=transpose_B))
+    # (2): 2 adapters x 3 experts, inner group l = 3 * adapter + expert
+    x1 = np.ascontiguousarray(x[:, :K])
+    y1 = oracle.mgemm_nested(x1, np.ascontiguousarray(w[:1]), off, transpose_B=transpose_B)
+    for a in range(2):
+        r0, r1 = int(off[3 * a]), int(off[3 * a + 3])
+        sub = (off[3 * a:3 * a + 4] - off[3 * a]).astype(np.int32)
+        ya = oracle.mgemm(np.ascontiguousarray(x1[r0:r1]), np.ascontiguousarray(w[0, 3 * a:3 * a + 3]),
+                          sub, transpose_B=transpose_B)
+        np.testing.assert_array_equal(y1[r0:r1], ya)
+
+
+def test_nested_row_subset_matches_full():
+    rng = np.random.default_rng(12)
+    off = W.offsets_from_counts(np.array([5, 0, 7]))
+    x = rand_bits(rng, (14, 2 * 8))
+    w = rand_bits(rng, (2, 3, 9, 8))
+    full = oracle.mgemm_nested(x, w, off)
+    rows = np.array([11, 0, 4, 5, 4])
+    np.testing.assert_array_equal(oracle.mgemm_nested(x, w, off, rows=rows), full[rows])
+    with pytest.raises(ValueError):
+        oracle.mgemm_nested(x, w, off, rows=np.array([12]))  # past offsets[L]
+
+
+def test_nested_planted_column_offset_mistake_is_caught():
+    """Reading every outer group's contraction from x's first column block
+    (a dropped o*K offset) must differ from the oracle whenever the blocks
+    differ: the pins above must see it."""
+    rng = np.random.default_rng(13)
+    off = W.offsets_from_counts(np.array([3, 4]))
+    x = rand_bits(rng, (7, 2 * 4))
+    w = rand_bits(rng, (2, 2, 3, 4))
+    right = oracle.mgemm_nested(x, w, off)
+    wrong = np.concatenate(  # the mistake, planted on the CPU side only
+        [np.concatenate([f64(x[r0:r1, :4]) @ f64(w[o, l]).T for l, (r0, r1) in enumerate([(0, 3), (3, 7)])])
+         for o in range(2)], axis=1)
+    assert not np.allclose(right, wrong)

@@ -60,6 +60,27 @@ def sample_pairs(counts, N, rng):
     return np.array(es, dtype=np.int32), np.array(ns, dtype=np.int32)
 
 
+NESTED = [("lora_a3b", "lora_shrink"), ("lora_a3b", "lora_expand")]
+
+
+@pytest.mark.parametrize("wname,opname", NESTED, ids=[f"{w}-{o}" for w, o in NESTED])
+def test_full_size_sampled_nested(gpu_lib, wname, opname):
+    import torch
+    wl = W.ALL[wname]()
+    op = wl.op(opname)
+    off = wl.offsets
+    rng = np.random.default_rng(zlib.crc32(f"{wname}/{opname}".encode()))
+    a_h, b_h = host_tensor(wl, op.a), host_tensor(wl, op.b)
+    y = gpu_lib.mgemm_nested(dev_tensor(wl, op.a), dev_tensor(wl, op.b), offsets_dev(off),
+                             transpose_B=op.transpose_B)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    rows = sample_rows(off, rng)
+    got = to_host_bits(y[torch.from_numpy(rows).cuda()])
+    ref = oracle.mgemm_nested(a_h, b_h, off, transpose_B=op.transpose_B, rows=rows)
+    check_bf16(got, ref, f"{wname}/{opname}")
+
+
 CASES = [("uniform8", "fwd"), ("uniform16", "fwd")] + [
     (w, op) for w in ("a3b", "skewed", "skewed_tail")
     for op in ("fwd_gate_up", "fwd_down", "dgrad_down", "dgrad_gate_up", "wgrad_gw2", "wgrad_gw13")]

@@ -196,9 +196,12 @@ class Op:
     # y13 [M, 2N] it reads, and it writes dy13 [M, 2N])
     fuse: str = ""
     c: str = ""
+    # kind 'nested': O outer groups over the columns (a = x [M, O*K], b = w
+    # [O, L, N, K], output [M, O*N])
+    outer: int = 1
 
     def flops(self, counts) -> int:
-        return 2 * int(np.sum(counts)) * self.N * self.K
+        return 2 * int(np.sum(counts)) * self.outer * self.N * self.K
 
 
 @dataclass
@@ -320,6 +323,38 @@ def skewed(tail: bool = False) -> Workload:
     return _layer(name, 5, 128, 65536, c, 3072, 2560, 1280)
 
 
+def lora_a3b(adapters: int = 4, rank: int = 16) -> Workload:
+    """Batched LoRA over the 30B-A3B expert layer's gate-up projection (the
+    nested grouped GEMM of CUTLASS discussion #1452): the a3b routed rows
+    (seed 3) are split over `adapters` LoRA adapters per expert (a seeded
+    multinomial with equal shares) and ordered (adapter, expert), giving
+    L = adapters * 32 inner row groups.
+
+      lora_shrink  s = x . A[l]^T     x [M, 3072], A [1, L, 2r, 3072] (gate
+                                      and up adapters' A stacked): N = 2r
+      lora_expand  y[:, o*1280:] = s[:, o*r:] . B[o, l]^T for o = gate, up:
+                                      s [M, 2r], B [2, L, 1280, r]: O = 2
+
+    All values ~N(0,1) except weights ~N(0, 1/K)."""
+    base = counts_dirichlet(32, 32768, 2.0, 3)
+    rng = np.random.default_rng(np.random.SeedSequence([3, 2]))
+    split = np.stack([rng.multinomial(int(c), [1.0 / adapters] * adapters) for c in base], axis=1)
+    counts = split.reshape(-1).astype(np.int64)  # index = adapter * 32 + expert
+    L, M, d_model, d_half = adapters * 32, 32768, 3072, 1280
+    w = Workload(f"lora_a3b_A{adapters}_r{rank}_L{L}_M{M}", 3, L, M, counts)
+    w.tensors = {
+        "x": ((M, d_model), 1.0, 1),
+        "lora_a": ((1, L, 2 * rank, d_model), 1.0 / np.sqrt(d_model), 11),
+        "s": ((M, 2 * rank), 1.0, 12),
+        "lora_b": ((2, L, d_half, rank), 1.0 / np.sqrt(rank), 13),
+    }
+    w.ops = [
+        Op("lora_shrink", "nested", "x", "lora_a", N=2 * rank, K=d_model, outer=1),
+        Op("lora_expand", "nested", "s", "lora_b", N=d_half, K=rank, outer=2),
+    ]
+    return w
+
+
 ALL = {
     "tiny": tiny,
     "uniform8": lambda: uniform(8, 4096),
@@ -329,4 +364,5 @@ ALL = {
     "skewed_tail": lambda: skewed(True),
     "a3b_swiglu": lambda: with_swiglu(a3b_layer()),
     "skewed_tail_swiglu": lambda: with_swiglu(skewed(True)),
+    "lora_a3b": lora_a3b,
 }
