@@ -40,7 +40,7 @@ def build(force: bool = False) -> str:
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-           "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC]
+           "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -59,6 +59,15 @@ def _load():
                                                  ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_int, c_p, ctypes.c_int64, c_p]
         lib.oracle_mgemm_nested_rows.restype = ctypes.c_int
+        lib.oracle_mgemm_mx_rows.argtypes = [c_p, c_p, c_p, c_p, c_p, ctypes.c_int, ctypes.c_int64,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             c_p, ctypes.c_int64, c_p]
+        lib.oracle_mgemm_mx_rows.restype = ctypes.c_int
+        lib.oracle_mx_decode_tables.argtypes = [c_p, c_p]
+        lib.oracle_mx_decode_tables.restype = None
+        lib.oracle_mx_blocked.argtypes = [c_p, ctypes.c_int64, ctypes.c_int, c_p, ctypes.c_int,
+                                          c_p, ctypes.c_int64]
+        lib.oracle_mx_blocked.restype = ctypes.c_int64
         lib.oracle_kgemm_rows.argtypes = [c_p, c_p, c_p, ctypes.c_int, ctypes.c_int64,
                                           ctypes.c_int, ctypes.c_int,
                                           c_p, c_p, ctypes.c_int64, c_p]
@@ -144,6 +153,73 @@ def mgemm_nested(x, w, offsets, transpose_B: bool = False, rows=None) -> np.ndar
         y[: int(off[L])] = out
         return y
     return out
+
+
+def _u8(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint8, a.dtype
+    return a
+
+
+def mx_decode_tables() -> tuple[np.ndarray, np.ndarray]:
+    """(E4M3 values, E8M0 values) of all 256 codes each, float64."""
+    a = np.empty(256, dtype=np.float64)
+    b = np.empty(256, dtype=np.float64)
+    _load().oracle_mx_decode_tables(_ptr(a), _ptr(b))
+    return a, b
+
+
+def mgemm_mx(xq, sx, wq, sw, offsets, transpose_B: bool = False, rows=None) -> np.ndarray:
+    """MXFP8 M-grouped GEMM: E4M3 element codes with one E8M0 scale per 32
+    elements along K.
+
+    xq: uint8 [M,K]; sx: uint8 [M,K/32]; wq: uint8 [E,N,K] (or [E,K,N] with
+    transpose_B); sw: uint8 [E,N,K/32] (scale of B element (k, n) of expert
+    e is sw[e, n, k//32] in both layouts); offsets: int32 [E+1].  Returns
+    float64 [M,N] with rows >= offsets[E] set to NaN, or [len(rows), N].
+    """
+    xq, sx, wq, sw = _u8(xq), _u8(sx), _u8(wq), _u8(sw)
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    M, K = xq.shape
+    E = wq.shape[0]
+    N = wq.shape[2] if transpose_B else wq.shape[1]
+    assert wq.shape == ((E, K, N) if transpose_B else (E, N, K)), wq.shape
+    assert K % 32 == 0 and sx.shape == (M, K // 32) and sw.shape == (E, N, K // 32)
+    assert off.shape == (E + 1,)
+    full = rows is None
+    if full:
+        rows = np.arange(int(off[E]), dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((len(rows), N), dtype=np.float64)
+    rc = _load().oracle_mgemm_mx_rows(_ptr(xq), _ptr(sx), _ptr(wq), _ptr(sw), _ptr(off), E, M, N, K,
+                                      int(bool(transpose_B)), _ptr(rows), len(rows), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_mgemm_mx_rows rejected its arguments")
+    if full:
+        y = np.full((M, N), np.nan, dtype=np.float64)
+        y[: int(off[E])] = out
+        return y
+    return out
+
+
+def mx_blocked_bytes(R: int, KS: int, G: int) -> int:
+    """Upper bound of the blocked layout's size for R rows in G groups."""
+    return (R // 128 + G) * ((KS + 3) // 4) * 512
+
+
+def mx_blocked(scales, offsets, fill: int = 0) -> np.ndarray:
+    """Blocked ("128x4") layout of grouped E8M0 scales [R, KS]: see
+    oracle_mx_blocked in oracle.c.  Returns uint8 [mx_blocked_bytes(R, KS, G)]
+    with bytes past the last block set to ``fill``."""
+    src = _u8(scales)
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    R, KS = src.shape
+    G = len(off) - 1
+    dst = np.full(mx_blocked_bytes(R, KS, G), fill, dtype=np.uint8)
+    nb = _load().oracle_mx_blocked(_ptr(src), R, KS, _ptr(off), G, _ptr(dst), dst.size)
+    if nb < 0:
+        raise ValueError("oracle_mx_blocked rejected its arguments")
+    return dst
 
 
 def kgemm(grad, X, offsets, sel=None) -> np.ndarray:

@@ -25,7 +25,15 @@
  *   splits the rows into inner groups shared by every outer group o:
  *       y[r, o*N + n] = sum_k x[r, o*K + k] * w[o, l, n, k]   (r in group l)
  *
- * Inputs are bf16 bit patterns; each value is widened exactly to double.
+ *   MXFP8 M-grouped GEMM (the MXFP8 grouped GEMM of the torchao MoE-training
+ *   PR and the FP8 block-scaling thread of the DeepGEMM issue; element and
+ *   scale encodings after the OCP Microscaling (MX) formats: FP8 E4M3
+ *   elements, one E8M0 power-of-two scale per 32 consecutive elements along
+ *   the contraction).  xq [M,K] and wq [E,N,K] (or [E,K,N]) are E4M3 codes,
+ *   sx [M,K/32] and sw [E,N,K/32] E8M0 codes:
+ *       y[r,n] = sum_k (xq[r,k] * 2^(sx[r,k/32]-127)) * (wq[e,n,k] * 2^(sw[e,n,k/32]-127))
+ *
+ * Inputs are bf16 bit patterns (E4M3 / E8M0 codes for the MXFP8 GEMM); each value is widened exactly to double.
  * Products of two bf16 values are exact in double, so the result depends only
  * on the summation order, which is ascending k (Mgemm) or ascending r (Kgemm).
  *
@@ -34,12 +42,27 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <math.h>
 
 static double bf16_to_double(uint16_t b) {
     uint32_t u = ((uint32_t)b) << 16;
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* FP8 E4M3 (OCP): sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent
+ * 0 is subnormal (m * 2^-9); S.1111.111 is NaN; there is no infinity. */
+static double e4m3_to_double(uint8_t b) {
+    const int e = (b >> 3) & 0xF, m = b & 0x7;
+    if (e == 0xF && m == 0x7) return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return (b & 0x80) ? -v : v;
+}
+
+/* E8M0 (OCP MX scale): 2^(s - 127); 0xFF is NaN. */
+static double e8m0_to_double(uint8_t s) {
+    return s == 0xFF ? NAN : ldexp(1.0, (int)s - 127);
 }
 
 /* 0 if offsets is a valid cumulative vector for M rows, else -1. */
@@ -122,6 +145,84 @@ int oracle_mgemm_nested_rows(const uint16_t *x, const uint16_t *w, const int32_t
         }
     }
     return 0;
+}
+
+/*
+ * MXFP8 Mgemm on a list of rows (K a multiple of 32).  out is [nrows, N]
+ * doubles.  Each operand element is decoded and multiplied by its block's
+ * scale (exact in double), then the products are summed in ascending k.
+ */
+int oracle_mgemm_mx_rows(const uint8_t *xq, const uint8_t *sx, const uint8_t *wq, const uint8_t *sw,
+                         const int32_t *offsets, int E, int64_t M, int N, int K, int transpose_B,
+                         const int64_t *rows, int64_t nrows, double *out) {
+    if (N < 1 || K < 32 || K % 32 != 0 || check_offsets(offsets, E, M) != 0) return -1;
+    for (int64_t i = 0; i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= (int64_t)offsets[E]) return -1;
+    const int KS = K / 32;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int64_t r = rows[i];
+        const int e = expert_of_row(offsets, E, r);
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) {
+                const double a = e4m3_to_double(xq[r * (int64_t)K + k]) *
+                                 e8m0_to_double(sx[r * (int64_t)KS + k / 32]);
+                const uint8_t bq = transpose_B ? wq[((int64_t)e * K + k) * N + n]   /* w[e,k,n] */
+                                               : wq[((int64_t)e * N + n) * K + k];  /* w[e,n,k] */
+                const double b = e4m3_to_double(bq) * e8m0_to_double(sw[((int64_t)e * N + n) * KS + k / 32]);
+                acc += a * b;
+            }
+            out[i * (int64_t)N + n] = acc;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Blocked scale layout for a grouped operand (the scale-to-blocked-format
+ * conversion of the torchao MoE-training PR, "128x4" blocks): the rows of
+ * src [R, KS] (E8M0 codes, KS scales per row) are grouped by offsets [G+1];
+ * each group is cut into blocks of 128 rows starting at its first row, so no
+ * block mixes two groups, and the blocks of all groups are numbered in
+ * order.  Block b, column chunk c (scale columns 4c..4c+3) occupies bytes
+ * (b * ceil(KS/4) + c) * 512 .. +511 of dst, where row i (0..127) of the
+ * block and column j (0..3) of the chunk sit at byte 16*(i%32) + 4*(i/32) + j.
+ * Positions past a group's last row or past column KS-1 hold 0x7F (scale
+ * 1.0).  Bytes of dst past the last block are not written.  dst_bytes must
+ * cover every block; returns the number of blocks, or -1.
+ */
+int64_t oracle_mx_blocked(const uint8_t *src, int64_t R, int KS, const int32_t *offsets, int G,
+                          uint8_t *dst, int64_t dst_bytes) {
+    if (KS < 1 || check_offsets(offsets, G, R) != 0) return -1;
+    const int nc = (KS + 3) / 4;
+    int64_t b = 0;
+    for (int g = 0; g < G; ++g) {
+        const int64_t r0 = offsets[g], r1 = offsets[g + 1];
+        for (int64_t base = r0; base < r1; base += 128, ++b) {
+            if ((b + 1) * nc * 512 > dst_bytes) return -1;
+            for (int c = 0; c < nc; ++c) {
+                uint8_t *blk = dst + (b * nc + c) * 512;
+                for (int i = 0; i < 128; ++i)
+                    for (int j = 0; j < 4; ++j) {
+                        const int64_t r = base + i;
+                        const int col = 4 * c + j;
+                        blk[16 * (i % 32) + 4 * (i / 32) + j] =
+                            (r < r1 && col < KS) ? src[r * KS + col] : (uint8_t)0x7F;
+                    }
+            }
+        }
+    }
+    return b;
+}
+
+/* Decoded values of the 256 E4M3 codes and of the 256 E8M0 codes. */
+void oracle_mx_decode_tables(double *e4m3, double *e8m0) {
+    for (int c = 0; c < 256; ++c) {
+        e4m3[c] = e4m3_to_double((uint8_t)c);
+        e8m0[c] = e8m0_to_double((uint8_t)c);
+    }
 }
 
 /*

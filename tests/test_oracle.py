@@ -480,3 +480,157 @@ def test_nested_planted_column_offset_mistake_is_caught():
         [np.concatenate([f64(x[r0:r1, :4]) @ f64(w[o, l]).T for l, (r0, r1) in enumerate([(0, 3), (3, 7)])])
          for o in range(2)], axis=1)
     assert not np.allclose(right, wrong)
+
+
+# ------------------------------------------------ MXFP8 (E4M3 elements, E8M0 block scales)
+
+
+def test_mx_decode_tables_match_closed_forms_and_torch():
+    e4, e8 = oracle.mx_decode_tables()
+    # closed forms of the OCP E4M3 / E8M0 encodings
+    assert e4[0x00] == 0.0 and e4[0x80] == 0.0
+    assert e4[0x01] == 2.0 ** -9 and e4[0x07] == 7 * 2.0 ** -9  # subnormals
+    assert e4[0x08] == 2.0 ** -6 and e4[0x38] == 1.0 and e4[0x40] == 2.0
+    assert e4[0x7E] == 448.0 and e4[0xFE] == -448.0 and e4[0xB8] == -1.0
+    assert np.isnan(e4[0x7F]) and np.isnan(e4[0xFF])
+    assert e8[127] == 1.0 and e8[0] == 2.0 ** -127 and e8[254] == 2.0 ** 127 and np.isnan(e8[255])
+    torch = pytest.importorskip("torch")
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    t4 = codes.view(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(e4, t4)
+    if hasattr(torch, "float8_e8m0fnu"):
+        t8 = codes.view(torch.float8_e8m0fnu).double().numpy()
+        np.testing.assert_array_equal(e8, t8)
+
+
+def _mx_tiny(rng, E, M, N, K, transpose_B):
+    xq = W.e4m3_codes((M, K), int(rng.integers(1 << 30)), 0)
+    wq = W.e4m3_codes((E, K, N) if transpose_B else (E, N, K), int(rng.integers(1 << 30)), 1)
+    sx = W.e8m0_codes((M, K // 32), 118, 130, int(rng.integers(1 << 30)), 2)
+    sw = W.e8m0_codes((E, N, K // 32), 118, 130, int(rng.integers(1 << 30)), 3)
+    return xq, sx, wq, sw
+
+
+@pytest.mark.parametrize("transpose_B", [False, True])
+def test_mx_mgemm_matches_brute_force(transpose_B):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(31)
+    E, M, N, K = 3, 7, 3, 64
+    off = W.offsets_from_counts([3, 0, 3])  # one row past offsets[E]
+    xq, sx, wq, sw = _mx_tiny(rng, E, M, N, K, transpose_B)
+    dec = lambda q: torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy().tolist()  # noqa: E731
+    X, Wt, SX, SW = dec(xq), dec(wq), sx.tolist(), sw.tolist()
+    y = oracle.mgemm_mx(xq, sx, wq, sw, off, transpose_B=transpose_B)
+    for e in range(E):
+        for r in range(off[e], off[e + 1]):
+            for n in range(N):
+                s = 0.0
+                for k in range(K):
+                    b = Wt[e][k][n] if transpose_B else Wt[e][n][k]
+                    s += (X[r][k] * 2.0 ** (SX[r][k // 32] - 127)) * (b * 2.0 ** (SW[e][n][k // 32] - 127))
+                assert y[r, n] == s
+    assert np.isnan(y[6]).all()
+
+
+@pytest.mark.parametrize("transpose_B", [False, True])
+def test_mx_mgemm_equals_bf16_grouped_gemm_on_dequantized_inputs(transpose_B):
+    """Every scaled E4M3 value (4 significant bits, moderate exponent) is a
+    bf16 value: dequantizing both operands exactly and running the pinned
+    bf16 grouped GEMM must give the identical FP64 result."""
+    rng = np.random.default_rng(32)
+    E, N, K = 4, 9, 96
+    off = W.offsets_from_counts([5, 0, 11, 6])
+    M = int(off[-1]) + 2
+    xq, sx, wq, sw = _mx_tiny(rng, E, M, N, K, transpose_B)
+    e4, e8 = oracle.mx_decode_tables()
+    xv = e4[xq] * e8[np.repeat(sx, 32, axis=1)]
+    swk = e8[np.repeat(sw, 32, axis=2)]  # scale of w element (n, k): [E, N, K]
+    wv = e4[wq] * (np.transpose(swk, (0, 2, 1)) if transpose_B else swk)
+    xb, wb = W.f32_to_bf16_bits(xv.astype(np.float32)), W.f32_to_bf16_bits(wv.astype(np.float32))
+    assert (W.bf16_bits_to_f32(xb) == xv).all() and (W.bf16_bits_to_f32(wb) == wv).all()
+    np.testing.assert_array_equal(oracle.mgemm_mx(xq, sx, wq, sw, off, transpose_B=transpose_B),
+                                  oracle.mgemm(xb, wb, off, transpose_B=transpose_B))
+
+
+def test_mx_mgemm_integer_codes_exact():
+    """Integer elements and scales of 1/2, 1 and 2: the result is an exact
+    small multiple of 1/4, equal to an int64 numpy GEMM per group."""
+    e4, _ = oracle.mx_decode_tables()
+    code_of = {v: int(np.flatnonzero(e4 == v)[0]) for v in (-2.0, -1.0, 0.0, 1.0, 2.0)}
+    rng = np.random.default_rng(33)
+    E, N, K = 2, 5, 64
+    off = W.offsets_from_counts([4, 3])
+    M = 7
+    xi = rng.integers(-2, 3, size=(M, K))
+    wi = rng.integers(-2, 3, size=(E, N, K))
+    sxe = rng.integers(-1, 2, size=(M, K // 32))
+    swe = rng.integers(-1, 2, size=(E, N, K // 32))
+    enc = np.vectorize(lambda v: code_of[float(v)])
+    y = oracle.mgemm_mx(enc(xi).astype(np.uint8), (127 + sxe).astype(np.uint8),
+                        enc(wi).astype(np.uint8), (127 + swe).astype(np.uint8), off)
+    xs = xi * 2.0 ** np.repeat(sxe, 32, axis=1)
+    for e in range(E):
+        ws = wi[e] * 2.0 ** np.repeat(swe[e], 32, axis=1)
+        r0, r1 = off[e], off[e + 1]
+        np.testing.assert_array_equal(y[r0:r1], xs[r0:r1] @ ws.T)
+
+
+def test_mx_planted_scale_index_mistake_is_caught():
+    """Indexing the scale with k % 32 instead of k // 32 must change the
+    result: the pins above must see it."""
+    rng = np.random.default_rng(34)
+    off = W.offsets_from_counts([4])
+    xq, sx, wq, sw = _mx_tiny(rng, 1, 4, 3, 64, False)
+    e4, e8 = oracle.mx_decode_tables()
+    right = oracle.mgemm_mx(xq, sx, wq, sw, off)
+    k = np.arange(64)
+    wrong = (e4[xq] * e8[sx[:, (k % 32) % 2]]) @ (e4[wq[0]] * e8[sw[0][:, k // 32]]).T  # planted on the CPU
+    assert not np.allclose(right, wrong)
+
+
+def test_mx_blocked_golden_handworked():
+    g = json.load(open(os.path.join(GOLDEN, "mx_blocked_handworked.json")))
+    for case in g["cases"]:
+        R, KS = case["R"], case["KS"]
+        r, c = np.meshgrid(np.arange(R), np.arange(KS), indexing="ij")
+        src = eval(case["src"], {}, {"r": r, "c": c}).astype(np.uint8)
+        dst = oracle.mx_blocked(src, np.array(case["offsets"], dtype=np.int32))
+        for x in case["expect"]:
+            assert int(dst[x["byte"]]) == x["value"], x["why"]
+
+
+def test_mx_blocked_is_a_bijection_with_pad():
+    """Every (row, scale column) lands on its own byte, read back by the
+    inverse of the layout; every other byte of the used blocks is the pad."""
+    rng = np.random.default_rng(35)
+    counts = np.array([130, 0, 1, 255, 128, 7])
+    off = W.offsets_from_counts(counts)
+    R, KS = int(off[-1]) + 3, 7
+    src = rng.integers(0, 256, size=(R, KS), dtype=np.int64).astype(np.uint8)
+    dst = oracle.mx_blocked(src, off, fill=0xEE)
+    nc = (KS + 3) // 4
+    seen = np.zeros(dst.size, dtype=bool)
+    blk = 0
+    for g in range(len(counts)):
+        for base in range(int(off[g]), int(off[g + 1]), 128):
+            for i in range(128):
+                for col in range(nc * 4):
+                    pos = (blk * nc + col // 4) * 512 + 16 * (i % 32) + 4 * (i // 32) + col % 4
+                    assert not seen[pos]
+                    seen[pos] = True
+                    rr = base + i
+                    want = src[rr, col] if (rr < off[g + 1] and col < KS) else 0x7F
+                    assert dst[pos] == want
+            blk += 1
+    assert (dst[~seen] == 0xEE).all() and seen[: blk * nc * 512].all()
+
+
+def test_mx_blocked_full_blocks_are_a_reshape():
+    """Groups of exactly 128 rows and KS a multiple of 4: each 512-byte block
+    is the 128x4 tile reshaped (i//32, i%32, j) -> (i%32, i//32, j)."""
+    rng = np.random.default_rng(36)
+    G, KS = 3, 8
+    src = rng.integers(0, 256, size=(128 * G, KS), dtype=np.int64).astype(np.uint8)
+    dst = oracle.mx_blocked(src, W.offsets_from_counts([128] * G))
+    want = src.reshape(G, 4, 32, KS // 4, 4).transpose(0, 3, 2, 1, 4).reshape(-1)
+    np.testing.assert_array_equal(dst[: want.size], want)

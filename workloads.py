@@ -96,6 +96,39 @@ def integer_bf16(shape, lo: int, hi: int, seed: int, stream: int) -> np.ndarray:
     return f32_to_bf16_bits(v)
 
 
+def e4m3_codes(shape, seed: int, stream: int) -> np.ndarray:
+    """Random FP8 E4M3 codes (uint8): sign, exponent field and mantissa field
+    drawn uniformly (exponent field 4..15), the NaN code S.1111.111 redrawn as
+    S.1111.110.  No value is rounded: the codes are the random draw."""
+    n = int(np.prod(shape, dtype=np.int64))
+    out = np.empty(n, dtype=np.uint8)
+
+    def fill(i: int) -> None:
+        lo = i * CHUNK
+        hi = min(n, lo + CHUNK)
+        rng = np.random.default_rng(np.random.SeedSequence([seed, stream, i]))
+        sign = rng.integers(0, 2, size=hi - lo, dtype=np.uint8) << np.uint8(7)
+        expo = rng.integers(4, 16, size=hi - lo, dtype=np.uint8) << np.uint8(3)
+        mant = rng.integers(0, 8, size=hi - lo, dtype=np.uint8)
+        c = sign | expo | mant
+        c[(c & np.uint8(0x7F)) == np.uint8(0x7F)] -= np.uint8(1)
+        out[lo:hi] = c
+
+    nchunks = (n + CHUNK - 1) // CHUNK
+    if nchunks <= 1:
+        if n:
+            fill(0)
+    else:
+        list(_pool().map(fill, range(nchunks)))
+    return out.reshape(shape)
+
+
+def e8m0_codes(shape, lo: int, hi: int, seed: int, stream: int) -> np.ndarray:
+    """Random E8M0 scale codes (uint8) drawn uniformly from [lo, hi]."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, stream]))
+    return rng.integers(lo, hi + 1, size=shape, dtype=np.int64).astype(np.uint8)
+
+
 # --------------------------------------------------------------------------
 # Row counts and offsets
 # --------------------------------------------------------------------------
@@ -199,6 +232,10 @@ class Op:
     # kind 'nested': O outer groups over the columns (a = x [M, O*K], b = w
     # [O, L, N, K], output [M, O*N])
     outer: int = 1
+    # kind 'mx': MXFP8 Mgemm; a, b are E4M3 code tensors, sa [M, K/32] and sb
+    # [E, N, K/32] their E8M0 scale tensors
+    sa: str = ""
+    sb: str = ""
 
     def flops(self, counts) -> int:
         return 2 * int(np.sum(counts)) * self.outer * self.N * self.K
@@ -220,6 +257,10 @@ class Workload:
 
     def tensor(self, name: str) -> np.ndarray:
         shape, std, stream = self.tensors[name]
+        if std == "e4m3":
+            return e4m3_codes(shape, self.seed, stream)
+        if isinstance(std, tuple) and std[0] == "e8m0":
+            return e8m0_codes(shape, std[1], std[2], self.seed, stream)
         return normal_bf16(shape, std, self.seed, stream)
 
     def op(self, name: str) -> Op:
@@ -323,6 +364,37 @@ def skewed(tail: bool = False) -> Workload:
     return _layer(name, 5, 128, 65536, c, 3072, 2560, 1280)
 
 
+def a3b_mxfp8() -> Workload:
+    """The 30B-A3B expert layer's M-grouped GEMMs (forward and input
+    gradient) in MXFP8: E4M3 operands with one E8M0 scale per 32 elements
+    along each contraction, same counts (seed 3, Dirichlet(2), 32 experts,
+    M = 32768).  The weights carry one scale tensor per direction (row-wise
+    for the forward, column-wise for the input gradient), as a training step
+    that quantizes each weight once per GEMM direction would hold.  Codes and
+    scales are random draws (scales 2^-8 .. 2^1)."""
+    c = counts_dirichlet(32, 32768, 2.0, 3)
+    E, M, dm, d2, d1 = 32, 32768, 3072, 2560, 1280
+    sc = ("e8m0", 119, 128)
+    w = Workload("a3b_mxfp8_E32_M32768", 3, E, M, c)
+    w.tensors = {
+        "xq": ((M, dm), "e4m3", 21), "sx": ((M, dm // 32), sc, 22),
+        "w13q": ((E, d2, dm), "e4m3", 23), "sw13": ((E, d2, dm // 32), sc, 24),
+        "hq": ((M, d1), "e4m3", 25), "sh": ((M, d1 // 32), sc, 26),
+        "w2q": ((E, dm, d1), "e4m3", 27), "sw2": ((E, dm, d1 // 32), sc, 28),
+        "dy2q": ((M, dm), "e4m3", 29), "sdy2": ((M, dm // 32), sc, 30),
+        "sw2t": ((E, d1, dm // 32), sc, 31),
+        "dy13q": ((M, d2), "e4m3", 32), "sdy13": ((M, d2 // 32), sc, 33),
+        "sw13t": ((E, dm, d2 // 32), sc, 34),
+    }
+    w.ops = [
+        Op("mx_fwd_gate_up", "mx", "xq", "w13q", N=d2, K=dm, sa="sx", sb="sw13"),
+        Op("mx_fwd_down", "mx", "hq", "w2q", N=dm, K=d1, sa="sh", sb="sw2"),
+        Op("mx_dgrad_down", "mx", "dy2q", "w2q", N=d1, K=dm, transpose_B=True, sa="sdy2", sb="sw2t"),
+        Op("mx_dgrad_gate_up", "mx", "dy13q", "w13q", N=dm, K=d2, transpose_B=True, sa="sdy13", sb="sw13t"),
+    ]
+    return w
+
+
 def lora_a3b(adapters: int = 4, rank: int = 16) -> Workload:
     """Batched LoRA over the 30B-A3B expert layer's gate-up projection (the
     nested grouped GEMM of CUTLASS discussion #1452): the a3b routed rows
@@ -365,4 +437,5 @@ ALL = {
     "a3b_swiglu": lambda: with_swiglu(a3b_layer()),
     "skewed_tail_swiglu": lambda: with_swiglu(skewed(True)),
     "lora_a3b": lora_a3b,
+    "a3b_mxfp8": a3b_mxfp8,
 }
