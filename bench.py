@@ -45,10 +45,19 @@ import workloads as W  # noqa: E402
 L2_BYTES = 129 * 2**20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_OF = {"mgemm": "mgemm_kernel<false>", "mgemm_t": "mgemm_kernel<true>", "kgemm": "kgemm_kernel",
-             "swiglu": "mgemm_kernel<false,swiglu>", "swiglu_bwd": "mgemm_kernel<true,swiglu_bwd>"}
+             "swiglu": "mgemm_kernel<false,swiglu>", "swiglu_bwd": "mgemm_kernel<true,swiglu_bwd>",
+             "mx": "mx_mgemm_kernel<false>", "mx_t": "mx_mgemm_kernel<true>", "mx_blocked": "mx_blocked_kernel"}
 KERNEL_SOURCES = {"mgemm_kernel<false>": "mgemm.cu", "mgemm_kernel<true>": "mgemm.cu",
                   "mgemm_kernel<false,swiglu>": "mgemm.cu", "mgemm_kernel<true,swiglu_bwd>": "mgemm.cu",
-                  "kgemm_kernel": "kgemm.cu"}
+                  "kgemm_kernel": "kgemm.cu", "mx_mgemm_kernel<false>": "mxgemm.cu",
+                  "mx_mgemm_kernel<true>": "mxgemm.cu", "mx_blocked_kernel": "mxgemm.cu"}
+FP8_KERNELS = ("mx_mgemm_kernel<false>", "mx_mgemm_kernel<true>")
+
+
+def tensor_peak(kernel: str, peaks) -> float:
+    """Sustained dense tensor peak of the kernel's input type: the measured
+    bf16 figure, times the nominal dense FP8/BF16 ratio (4.5 / 2.25) for FP8."""
+    return peaks["bf16_tflops_sustained"] * (2.0 if kernel in FP8_KERNELS else 1.0)
 
 
 def parse():
@@ -74,6 +83,8 @@ def load_peaks():
 
 
 def kernel_of(op) -> str:
+    if op.kind == "mx":
+        return KERNEL_OF["mx_t" if op.transpose_B else "mx"]
     if op.kind == "nested":
         return KERNEL_OF["mgemm_t" if op.transpose_B else "mgemm"]
     if op.fuse:
@@ -89,6 +100,8 @@ def algorithmic_bytes(op, counts) -> int:
     if op.kind == "kgemm":
         return 2 * M * op.N + 2 * M * op.K + 4 * E * op.N * op.K
     nonempty = int(np.count_nonzero(counts))
+    if op.kind == "mx":  # FP8 operands, their scales (1 byte per 32), bf16 y
+        return M * op.K + op.N * op.K * nonempty + (M + op.N * nonempty) * (op.K // 32) + 2 * M * op.N
     if op.kind == "nested":  # x [M, O*K], w [O, L, N, K] (non-empty groups), y [M, O*N]
         return op.outer * (2 * M * op.K + 2 * op.N * op.K * nonempty + 2 * M * op.N)
     operands = 2 * M * op.K + 2 * op.N * op.K * nonempty
@@ -108,8 +121,8 @@ def workload_desc(wl) -> str:
 
 def working_set_bytes(wl) -> int:
     tot = 0
-    for name, (shape, _, _) in wl.tensors.items():
-        tot += 2 * int(np.prod(shape))
+    for name, (shape, kind, _) in wl.tensors.items():
+        tot += (1 if isinstance(kind, (str, tuple)) else 2) * int(np.prod(shape))
     for op in wl.ops:
         if op.kind == "kgemm":
             tot += 4 * wl.E * op.N * op.K
@@ -191,7 +204,14 @@ def oracle_sample_step(wl, tensors, budget_s: float, rng) -> tuple[float, float,
     desc = []
     for op in wl.ops:
         a, b = tensors[op.a], tensors[op.b]
-        if op.kind == "nested":
+        if op.kind == "mx":
+            unit = 2.0 * op.N * op.K
+
+            def run(n):
+                rows = rng.integers(0, int(off[-1]), size=n)
+                oracle.mgemm_mx(a, tensors[op.sa], b, tensors[op.sb], off, transpose_B=op.transpose_B, rows=rows)
+                return n * unit
+        elif op.kind == "nested":
             unit = 2.0 * op.outer * op.N * op.K
 
             def run(n):
@@ -293,6 +313,55 @@ def traffic_for(kernel: str, op_names):
     return sum(per_op[o] for o in op_names) // len(op_names)
 
 
+class Unit:
+    """One timed launch of the step: a grouped GEMM, or (MXFP8) the scale
+    layout conversions that precede it."""
+
+    def __init__(self, name, kernel, flops, nbytes, call, op=None):
+        self.name, self.kernel, self.flops, self.bytes, self.call, self.op = name, kernel, flops, nbytes, call, op
+
+
+def build_units(wl, rg, tensors, outs, off_ref, scratch):
+    counts = wl.counts
+    E, M = wl.E, wl.M
+    units = []
+    for op in wl.ops:
+        if op.kind == "mx":
+            KS = op.K // 32
+            sa, sb = tensors[op.sa], tensors[op.sb]
+            sab, sbb = scratch[op.name + ":sa"], scratch[op.name + ":sb"]
+            woff = scratch["woff:" + str(op.N)]
+            # the scale layout of both operands is converted every step (scales
+            # change whenever activations or weights are re-quantized)
+            conv_bytes = (M + E * op.N) * KS + sab.numel() + sbb.numel()
+
+            def conv(op=op, sa=sa, sb=sb, sab=sab, sbb=sbb, woff=woff):
+                rg.mx_scales_blocked(sa, off_ref[0], out=sab)
+                rg.mx_scales_blocked(sb.view(-1, sb.shape[-1]), woff, out=sbb)
+            units.append(Unit(op.name + ".scales", KERNEL_OF["mx_blocked"], 0, conv_bytes, conv))
+
+            def gemm(op=op, sab=sab, sbb=sbb):
+                rg.mgemm_mxfp8(tensors[op.a], sab, tensors[op.b], sbb, off_ref[0], transpose_B=op.transpose_B,
+                               out=outs[op.name])
+            units.append(Unit(op.name, kernel_of(op), op.flops(counts), algorithmic_bytes(op, counts), gemm, op))
+            continue
+
+        def call(op=op):
+            out = outs[op.name]
+            if op.kind == "kgemm":
+                rg.kgemm(tensors[op.a], tensors[op.b], off_ref[0], out=out)
+            elif op.kind == "nested":
+                rg.mgemm_nested(tensors[op.a], tensors[op.b], off_ref[0], transpose_B=op.transpose_B, out=out)
+            elif op.fuse == "swiglu":
+                rg.mgemm_swiglu(tensors[op.a], tensors[op.b], off_ref[0], out=out, y13=outs[op.name + ":y13"])
+            elif op.fuse == "swiglu_bwd":
+                rg.mgemm_swiglu_dgrad(tensors[op.a], tensors[op.b], off_ref[0], tensors[op.c], out=out)
+            else:
+                rg.mgemm(tensors[op.a], tensors[op.b], off_ref[0], transpose_B=op.transpose_B, out=out)
+        units.append(Unit(op.name, kernel_of(op), op.flops(counts), algorithmic_bytes(op, counts), call, op))
+    return units
+
+
 def main():
     args = parse()
     wl = W.ALL[args.workload]()
@@ -300,7 +369,8 @@ def main():
         keep = args.ops.split(",")
         wl.ops = [o for o in wl.ops if o.name in keep]
         assert wl.ops, f"no op of {wl.name} matches {keep}"
-        used = {o.a for o in wl.ops} | {o.b for o in wl.ops} | {o.c for o in wl.ops if o.c}
+        used = ({o.a for o in wl.ops} | {o.b for o in wl.ops} | {o.c for o in wl.ops if o.c}
+                | {o.sa for o in wl.ops if o.sa} | {o.sb for o in wl.ops if o.sb})
         wl.tensors = {k: v for k, v in wl.tensors.items() if k in used}
     if args.impl == "reference":
         return run_reference(args, wl)
@@ -325,12 +395,15 @@ def main():
     off_np = wl.offsets
     counts = wl.counts
 
-    def dev_bf16(bits):
-        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    def as_torch(a):  # bf16 bit patterns (uint16) or FP8 / E8M0 codes (uint8)
+        if a.dtype == np.uint8:
+            return torch.from_numpy(a)
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
 
-    d = {k: dev_bf16(v) for k, v in host.items()}
+    d = {k: as_torch(v).to(dev) for k, v in host.items()}
     off = torch.from_numpy(off_np).to(dev)
-    outs = {}
+    outs, scratch = {}, {}
+    is_mx = any(op.kind == "mx" for op in wl.ops)
     for op in wl.ops:
         if op.kind == "kgemm":
             outs[op.name] = torch.empty((wl.E, op.N, op.K), dtype=torch.float32, device=dev)
@@ -343,30 +416,25 @@ def main():
             outs[op.name] = torch.empty((wl.M, 2 * op.N), dtype=torch.bfloat16, device=dev)
         else:
             outs[op.name] = torch.empty((wl.M, op.N), dtype=torch.bfloat16, device=dev)
+        if op.kind == "mx":
+            KS = op.K // 32
+            scratch[op.name + ":sa"] = torch.empty((rg.mx_blocked_bytes(wl.M, KS, wl.E),), dtype=torch.uint8,
+                                                   device=dev)
+            scratch[op.name + ":sb"] = torch.empty((rg.mx_blocked_bytes(wl.E * op.N, KS, wl.E),),
+                                                   dtype=torch.uint8, device=dev)
+            scratch["woff:" + str(op.N)] = rg.mx_weight_offsets(wl.E, op.N, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    def call(op, tens, out):
-        if op.kind == "kgemm":
-            rg.kgemm(tens[op.a], tens[op.b], off_used[0], out=out)
-        elif op.kind == "nested":
-            rg.mgemm_nested(tens[op.a], tens[op.b], off_used[0], transpose_B=op.transpose_B, out=out)
-        elif op.fuse == "swiglu":
-            rg.mgemm_swiglu(tens[op.a], tens[op.b], off_used[0], out=out, y13=outs[op.name + ":y13"])
-        elif op.fuse == "swiglu_bwd":
-            rg.mgemm_swiglu_dgrad(tens[op.a], tens[op.b], off_used[0], tens[op.c], out=out)
-        else:
-            rg.mgemm(tens[op.a], tens[op.b], off_used[0], transpose_B=op.transpose_B, out=out)
-
     off_used = [off]
-    nops = len(wl.ops)
+    units = build_units(wl, rg, d, outs, off_used, scratch)
+    nu = len(units)
 
     def step(evs=None):
-        for i, op in enumerate(wl.ops):
+        for i, u in enumerate(units):
             if evs is not None:
                 evs[i].record(stream)
-            call(op, d, outs[op.name])
+            u.call()
         if evs is not None:
-            evs[nops].record(stream)
+            evs[nu].record(stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -378,7 +446,7 @@ def main():
     # ---- timed region -------------------------------------------------------
     # Events around every launch, on the launching stream, give the per-kernel
     # durations of the timed steps themselves.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nops + 1)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nu + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -390,15 +458,15 @@ def main():
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    ms = evs[0][0].elapsed_time(evs[-1][nops])
+    ms = evs[0][0].elapsed_time(evs[-1][nu])
     clocks = sampler.stop() if sampler else None
     status = rg.device_status()
     if status:
         raise SystemExit(f"device status {status:#x} after timed region")
-    per_op_ms = np.zeros(nops)
+    per_unit_ms = np.zeros(nu)
     for e in evs:
-        per_op_ms += np.array([e[i].elapsed_time(e[i + 1]) for i in range(nops)])
-    per_op_ms /= args.steps
+        per_unit_ms += np.array([e[i].elapsed_time(e[i + 1]) for i in range(nu)])
+    per_unit_ms /= args.steps
     if dist:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -410,8 +478,7 @@ def main():
     # ---- end to end through the public API with host buffers ---------------
     e2e = None
     if rank == 0 and args.e2e_steps > 0:
-        pin = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
-               for k, v in host.items()}
+        pin = {k: as_torch(v).pin_memory() for k, v in host.items()}
         pin_off = torch.from_numpy(off_np).pin_memory()
         pin_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
         h2d = sum(t.numel() * t.element_size() for t in pin.values()) + pin_off.numel() * 4
@@ -421,8 +488,8 @@ def main():
             for k, t in pin.items():
                 d[k].copy_(t, non_blocking=True)
             off_used[0].copy_(pin_off, non_blocking=True)
-            for op in wl.ops:
-                call(op, d, outs[op.name])
+            for u in units:
+                u.call()
             for k, t in outs.items():
                 pin_out[k].copy_(t, non_blocking=True)
 
@@ -448,33 +515,36 @@ def main():
     peaks, peak_src = load_peaks()
     per_kernel = {}
     per_op = {}
-    for i, op in enumerate(wl.ops):
-        k = kernel_of(op)
-        f = op.flops(counts)
-        ent = per_kernel.setdefault(k, {"ms": 0.0, "flops": 0, "bytes": 0, "launches": 0})
-        ent["ms"] += per_op_ms[i]
-        ent["flops"] += f
-        ent["bytes"] += algorithmic_bytes(op, counts)
+    for i, u in enumerate(units):
+        ent = per_kernel.setdefault(u.kernel, {"ms": 0.0, "flops": 0, "bytes": 0, "launches": 0, "ops": []})
+        ent["ms"] += per_unit_ms[i]
+        ent["flops"] += u.flops
+        ent["bytes"] += u.bytes
         ent["launches"] += 1
-        per_op[op.name] = {"ms": round(float(per_op_ms[i]), 4),
-                           "tflops": round(f / (per_op_ms[i] * 1e-3) / 1e12, 1),
-                           "pct_peak_sustained": round(100 * f / (per_op_ms[i] * 1e-3) / 1e12
-                                                       / peaks["bf16_tflops_sustained"], 1),
-                           "algorithmic_gbs": round(algorithmic_bytes(op, counts) / (per_op_ms[i] * 1e-3) / 1e9, 1)}
+        ent["ops"].append(u.name)
+        sec = per_unit_ms[i] * 1e-3
+        rec = {"ms": round(float(per_unit_ms[i]), 4), "algorithmic_gbs": round(u.bytes / sec / 1e9, 1)}
+        if u.flops:
+            pk = tensor_peak(u.kernel, peaks)
+            rec["tflops"] = round(u.flops / sec / 1e12, 1)
+            rec["pct_peak_sustained"] = round(100 * u.flops / sec / 1e12 / pk, 1)
+        per_op[u.name] = rec
     dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
     de = per_kernel[dom]
-    peak = peaks["bf16_tflops_sustained"]
-    traffic = traffic_for(dom, [op.name for op in wl.ops if kernel_of(op) == dom])
+    traffic = traffic_for(dom, de["ops"])
+    fp8 = dom in FP8_KERNELS
+    peak = tensor_peak(dom, peaks)
+    peak_name = ("measured bf16 sustained x 2 (nominal dense FP8/BF16 ratio 4.5/2.25; MEASURED_PEAKS.json)" if fp8
+                 else "measured bf16 sustained (MEASURED_PEAKS.json)")
     # The kernel's bound: tensor cores when its arithmetic intensity is above
     # the ridge of the measured peaks, HBM below it (e.g. LoRA rank-16 GEMMs).
-    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if de["flops"] / de["bytes"] >= ridge:
         achieved = de["flops"] / (de["ms"] * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
                     "frac": round(achieved / peak, 4),
-                    "peak_source": f"{peak_src} bf16 sustained (MEASURED_PEAKS.json)" if peak_src == "measured"
-                    else "fallback 1.7 PFLOP/s sustained",
-                    "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4)}
+                    "peak_source": peak_name if peak_src == "measured" else "fallback 1.7 PFLOP/s sustained",
+                    "frac_of_burst": round(achieved / (peaks["bf16_tflops"] * (2 if fp8 else 1)), 4)}
     else:
         achieved = de["bytes"] / (de["ms"] * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -484,7 +554,7 @@ def main():
     roofline.update({"traffic": traffic, "kernel": dom, "launches_per_step": de["launches"],
                      "algorithmic_flops_per_launch": de["flops"] // de["launches"],
                      "algorithmic_bytes_per_launch": de["bytes"] // de["launches"],
-                     "share_of_step": round(de["ms"] / float(per_op_ms.sum()), 3)})
+                     "share_of_step": round(de["ms"] / float(per_unit_ms.sum()), 3)})
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -501,8 +571,9 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic (seeded normal inputs, random-init weights)",
+        "dtype": "e4m3 (MXFP8: E8M0 scale per 32)" if is_mx else "bf16",
+        "data": "synthetic (seeded random E4M3 codes and E8M0 scales)" if is_mx
+                else "synthetic (seeded normal inputs, random-init weights)",
         "config": {"workload": workload_desc(wl),
                    "flops_per_step": flops_step,
                    "l2": f"inputs larger than L2: step working set {working_set_bytes(wl) / 1e9:.2f} GB vs 129 MB L2",
@@ -510,7 +581,7 @@ def main():
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": nops * args.steps,
+        "gpu_launches": sum(2 if u.kernel == KERNEL_OF["mx_blocked"] else 1 for u in units) * args.steps,
         "clocks": clocks,
         "per_op": per_op,
     }

@@ -109,6 +109,69 @@ int rg_mgemm_nested(const void* x, const void* w, const int32_t* offsets, int O,
                     int N, int K, int transpose_B, void* y, cudaStream_t stream);
 
 /*
+ * rg_mx_blocked_bytes -- size in bytes that rg_mx_scales_blocked may write
+ * for R scale rows of KS columns in G groups: (R/128 + G) * ceil(KS/4) * 512
+ * (an upper bound of the blocks the groups need).  -1 on bad arguments.
+ * Host-only; touches no device.
+ */
+int64_t rg_mx_blocked_bytes(int64_t R, int KS, int G);
+
+/*
+ * rg_mx_scales_blocked -- convert grouped E8M0 block scales to the blocked
+ * ("128x4") layout that rg_mgemm_mxfp8 reads: the scale conversion for
+ * grouped GEMMs of the torchao MoE-training PR (blocks of 128 rows x 4 scale
+ * columns with a per-block swizzle, no block straddling two groups).
+ *
+ *   scales   device, uint8 [R, KS] row-major: E8M0 codes, KS scales per row
+ *            (one per 32 elements of the row's contraction).
+ *   offsets  device, int32 [G+1], same rules as rg_mgemm's (offsets[G] <= R).
+ *            For an activation: the expert offsets.  For a weight stack
+ *            [E, N, K/32]: G = E groups of N rows, offsets[g] = g*N.
+ *   out      device, uint8, 16-byte aligned, out_bytes >= rg_mx_blocked_bytes.
+ *            Each group is cut into 128-row blocks from its first row; the
+ *            blocks of all groups are numbered in order; block b, chunk c
+ *            (scale columns 4c..4c+3) is the 512 bytes at (b*ceil(KS/4)+c)*512,
+ *            with row i of the block, column j of the chunk at byte
+ *            16*(i%32) + 4*(i/32) + j.  Positions past a group's last row or
+ *            past column KS-1 are 0x7F (scale 1.0).  Bytes past the last
+ *            block are not written.
+ *   G        1 .. RG_MAX_EXPERTS.  R 0 .. 2^31-1.  KS >= 1.
+ * Invalid offsets contents set RG_DEV_BAD_OFFSETS and write nothing.
+ */
+int rg_mx_scales_blocked(const uint8_t* scales, const int32_t* offsets, int G, int64_t R, int KS,
+                         uint8_t* out, int64_t out_bytes, cudaStream_t stream);
+
+/*
+ * rg_mgemm_mxfp8 -- M-grouped MXFP8 GEMM: FP8 E4M3 operands with one E8M0
+ * power-of-two scale per 32 consecutive elements along the contraction
+ * (the MXFP8 grouped GEMM of the torchao MoE-training PR; the block-scaled
+ * FP8 GEMMs of the DeepGEMM issue discussion), forward (transpose_B == 0) or
+ * input gradient (transpose_B != 0), over the Mgemm row grouping.
+ *
+ *   xq          device, uint8 [M, K]: E4M3 codes.
+ *   sx_blocked  device: the scales sx [M, K/32] of xq (sx[r, k/32] scales
+ *               xq[r, k]) in the blocked layout of rg_mx_scales_blocked with
+ *               the same offsets.
+ *   wq          device, uint8 E4M3 codes, [E, N, K] when transpose_B == 0,
+ *               [E, K, N] when transpose_B != 0.
+ *   sw_blocked  device: the scales sw [E, N, K/32] of B (sw[e, n, k/32]
+ *               scales B element (k, n) of expert e, in both layouts) in the
+ *               blocked layout with G = E groups of N rows.
+ *   offsets     device, int32 [E+1], as for rg_mgemm.
+ *   y           device, bf16 [M, N]: for row r of expert e
+ *                 y[r, n] = sum_k xq[r,k] 2^(sx[r,k/32]-127) * B[k,n] 2^(sw[e,n,k/32]-127)
+ *               accumulated in FP32 by the tensor cores, rounded to bf16
+ *               (nearest even).  Rows >= offsets[E] are not written.
+ *   N >= 16, multiple of 16.  K >= 32, multiple of 32.  E 1..RG_MAX_EXPERTS.
+ *   xq, wq, the scale buffers and y 16-byte aligned.
+ * An E4M3 NaN code or an E8M0 code 0xFF in a valid row or column makes the
+ * outputs it reaches NaN.
+ */
+int rg_mgemm_mxfp8(const void* xq, const void* sx_blocked, const void* wq, const void* sw_blocked,
+                   const int32_t* offsets, int E, int64_t M, int N, int K, int transpose_B, void* y,
+                   cudaStream_t stream);
+
+/*
  * rg_mgemm_swiglu -- M-grouped forward gate-up GEMM with the SwiGLU
  * activation applied in the epilogue (the fused activation named in the
  * DeepGEMM issue discussion of wgrad utilities, "fused with SwiGLU"; the

@@ -13,6 +13,9 @@ Operations (RapidGEMM README, "Kernels"):
   gradient (``transpose_B=True``: ``y = x @ w[e]``, w ``[E,K,N]``).
 * ``kgemm(grad, X, offsets)``: K-grouped weight gradient
   ``dW[e] = grad[rows of e].T @ X[rows of e]`` in FP32.
+* ``mgemm_mxfp8(xq, sx_blocked, wq, sw_blocked, offsets)``: MXFP8 M-grouped
+  GEMM (E4M3 codes, E8M0 scale per 32 K elements, scales in the blocked
+  layout made by ``mx_scales_blocked``).
 * ``mgemm_nested(x, w, offsets)``: nested grouped GEMM (CUTLASS discussion
   #1452): O outer groups over the columns of x ``[M,O*K]`` and y ``[M,O*N]``,
   L inner row groups, w ``[O,L,N,K]``.
@@ -27,7 +30,7 @@ import os
 
 from . import _build
 
-__all__ = ["load", "mgemm", "mgemm_nested", "mgemm_swiglu", "mgemm_swiglu_dgrad", "kgemm", "device_status", "set_wait_timeout_ns",
+__all__ = ["load", "mgemm", "mgemm_nested", "mgemm_mxfp8", "mx_scales_blocked", "mx_blocked_bytes", "mgemm_swiglu", "mgemm_swiglu_dgrad", "kgemm", "device_status", "set_wait_timeout_ns",
            "selftest_wait_timeout", "RGError", "lib_path", "version",
            "RG_DEV_BAD_OFFSETS", "RG_DEV_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -41,7 +44,7 @@ RG_DEV_LAUNCH_CONFIG = 0x4
 RG_MAX_EXPERTS = 1024
 RG_MAX_OUTER = 65536
 
-EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_nested", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_set_wait_timeout_ns",
+EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_nested", "rg_mgemm_mxfp8", "rg_mx_scales_blocked", "rg_mx_blocked_bytes", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_set_wait_timeout_ns",
                     "rg_selftest_wait_timeout", "rg_last_cuda_error", "rg_device_supported",
                     "rg_version")
 
@@ -79,6 +82,12 @@ def load() -> ctypes.CDLL:
     lib.rg_mgemm.restype = i32
     lib.rg_mgemm_nested.argtypes = [vp, vp, vp, i32, i32, i64, i32, i32, i32, vp, vp]
     lib.rg_mgemm_nested.restype = i32
+    lib.rg_mgemm_mxfp8.argtypes = [vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, vp]
+    lib.rg_mgemm_mxfp8.restype = i32
+    lib.rg_mx_scales_blocked.argtypes = [vp, vp, i32, i64, i32, vp, i64, vp]
+    lib.rg_mx_scales_blocked.restype = i32
+    lib.rg_mx_blocked_bytes.argtypes = [i64, i32, i32]
+    lib.rg_mx_blocked_bytes.restype = i64
     lib.rg_mgemm_swiglu.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp, vp]
     lib.rg_mgemm_swiglu.restype = i32
     lib.rg_mgemm_swiglu_dgrad.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp, vp]
@@ -197,6 +206,82 @@ def mgemm_nested(x, w, offsets, transpose_B: bool = False, out=None, stream=None
         rc = lib.rg_mgemm_nested(x.data_ptr(), w.data_ptr(), offsets.data_ptr(), O, L, M, N, K,
                                  int(bool(transpose_B)), out.data_ptr(), _stream_ptr(x.device, stream))
     _check("rg_mgemm_nested", rc)
+    return out
+
+
+def mx_blocked_bytes(R: int, KS: int, G: int) -> int:
+    """Bytes ``mx_scales_blocked`` may write for R rows of KS scales in G groups."""
+    n = load().rg_mx_blocked_bytes(int(R), int(KS), int(G))
+    if n < 0:
+        raise ValueError("bad arguments to rg_mx_blocked_bytes")
+    return int(n)
+
+
+def mx_scales_blocked(scales, offsets, out=None, stream=None):
+    """Blocked ("128x4") layout of grouped E8M0 scales.  scales uint8 [R, KS]
+    (device), offsets int32 [G+1] (device); returns uint8
+    [mx_blocked_bytes(R, KS, G)] (bytes past the used blocks are unspecified)."""
+    import torch
+    _need(scales, "scales", torch.uint8, 2)
+    _need(offsets, "offsets", torch.int32, 1)
+    R, KS = scales.shape
+    G = offsets.shape[0] - 1
+    nbytes = mx_blocked_bytes(R, KS, G)
+    if out is None:
+        out = torch.empty((nbytes,), dtype=torch.uint8, device=scales.device)
+    else:
+        _need(out, "out", torch.uint8, 1)
+        if out.numel() < nbytes:
+            raise ValueError(f"out must hold at least {nbytes} bytes")
+    lib = load()
+    with torch.cuda.device(scales.device):
+        rc = lib.rg_mx_scales_blocked(scales.data_ptr(), offsets.data_ptr(), G, R, KS, out.data_ptr(),
+                                      out.numel(), _stream_ptr(scales.device, stream))
+    _check("rg_mx_scales_blocked", rc)
+    return out
+
+
+def mx_weight_offsets(E: int, N: int, device="cuda"):
+    """Offsets [E+1] that group a weight stack's scales [E*N, K/32] into E
+    groups of N rows (for ``mx_scales_blocked`` of sw)."""
+    import torch
+    return torch.arange(0, (E + 1) * N, N, dtype=torch.int32, device=device)
+
+
+def mgemm_mxfp8(xq, sx_blocked, wq, sw_blocked, offsets, transpose_B: bool = False, out=None, stream=None):
+    """MXFP8 M-grouped GEMM.  xq uint8 [M,K] E4M3 codes, wq uint8 [E,N,K] (or
+    [E,K,N] with transpose_B), sx_blocked / sw_blocked uint8 blocked scales
+    (``mx_scales_blocked`` of sx [M,K/32] with ``offsets`` and of sw
+    [E*N,K/32] with ``mx_weight_offsets``), offsets int32 [E+1]; returns y
+    [M,N] bf16."""
+    import torch
+    _need(xq, "xq", torch.uint8, 2)
+    _need(wq, "wq", torch.uint8, 3)
+    _need(sx_blocked, "sx_blocked", torch.uint8, 1)
+    _need(sw_blocked, "sw_blocked", torch.uint8, 1)
+    _need(offsets, "offsets", torch.int32, 1)
+    M, K = xq.shape
+    E = wq.shape[0]
+    N = wq.shape[2] if transpose_B else wq.shape[1]
+    if wq.shape[1 if transpose_B else 2] != K:
+        raise ValueError(f"wq {tuple(wq.shape)} does not match xq {tuple(xq.shape)}")
+    if offsets.shape[0] != E + 1:
+        raise ValueError(f"offsets must have E+1 = {E + 1} entries")
+    KS = K // 32
+    if sx_blocked.numel() < mx_blocked_bytes(M, KS, E) or sw_blocked.numel() < mx_blocked_bytes(E * N, KS, E):
+        raise ValueError("blocked scale buffers are smaller than mx_blocked_bytes")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    else:
+        _need(out, "out", torch.bfloat16, 2)
+        if tuple(out.shape) != (M, N):
+            raise ValueError(f"out must be [{M},{N}]")
+    lib = load()
+    with torch.cuda.device(xq.device):
+        rc = lib.rg_mgemm_mxfp8(xq.data_ptr(), sx_blocked.data_ptr(), wq.data_ptr(), sw_blocked.data_ptr(),
+                                offsets.data_ptr(), E, M, N, K, int(bool(transpose_B)), out.data_ptr(),
+                                _stream_ptr(xq.device, stream))
+    _check("rg_mgemm_mxfp8", rc)
     return out
 
 

@@ -83,6 +83,7 @@ int device_state(DeviceState** out) {
       ds.status = static_cast<unsigned int*>(p);
       if ((e = rg::mgemm_setup(smem)) != cudaSuccess) return fail_cuda(e);
       if ((e = rg::kgemm_setup(smem)) != cudaSuccess) return fail_cuda(e);
+      if ((e = rg::mx_setup(smem)) != cudaSuccess) return fail_cuda(e);
       if (encode_fn() == nullptr) return fail_cuda(cudaErrorNotSupported);
       // One CTA per SM (shared memory limits residency to one); with CTA
       // pairs, as many 2-CTA clusters as can be resident at once.
@@ -114,6 +115,16 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, c
                                  strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Tiled tensor map with an explicit swizzle mode.
+bool encode_sw(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, const uint64_t* dims,
+               const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw) {
+  const uint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+  const CUresult r = encode_fn()(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), dims, strides,
+                                 box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -313,6 +324,93 @@ int rg_mgemm_swiglu_dgrad(const void* dy, const void* w2, const int32_t* offsets
   rg::GroupArgs args = group_args(ds, offsets, E, M, F, K, dy13);
   args.out2 = const_cast<void*>(y13);
   const cudaError_t e = rg::launch_mgemm_swiglu_dgrad(tmA, tmB, tmD, args, ds->mg_grid, stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return RG_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+int64_t rg_mx_blocked_bytes(int64_t R, int KS, int G) {
+  if (R < 0 || KS < 1 || G < 1) return -1;
+  return (R / 128 + G) * ((KS + 3) / 4) * 512;
+}
+
+int rg_mx_scales_blocked(const uint8_t* scales, const int32_t* offsets, int G, int64_t R, int KS, uint8_t* out,
+                         int64_t out_bytes, cudaStream_t stream) {
+  if (offsets == nullptr || (reinterpret_cast<uintptr_t>(offsets) & 3u) != 0) return RG_ERR_INVALID_ARG;
+  if (G < 1 || G > RG_MAX_EXPERTS || R < 0 || R > INT32_MAX || KS < 1) return RG_ERR_INVALID_ARG;
+  if (R * static_cast<int64_t>(KS) > INT64_MAX / 2) return RG_ERR_INVALID_ARG;
+  if (out == nullptr || !aligned16(out) || out_bytes < rg_mx_blocked_bytes(R, KS, G)) return RG_ERR_INVALID_ARG;
+  if (R > 0 && scales == nullptr) return RG_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != RG_OK) return rc;
+  const cudaError_t e = rg::launch_mx_blocked(scales, offsets, G, static_cast<int>(R), KS, out, ds->status,
+                                              ds->num_sms, stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return RG_OK;
+}
+
+int rg_mgemm_mxfp8(const void* xq, const void* sx_blocked, const void* wq, const void* sw_blocked,
+                   const int32_t* offsets, int E, int64_t M, int N, int K, int transpose_B, void* y,
+                   cudaStream_t stream) {
+  if (offsets == nullptr || (reinterpret_cast<uintptr_t>(offsets) & 3u) != 0) return RG_ERR_INVALID_ARG;
+  if (E < 1 || E > RG_MAX_EXPERTS || M < 0 || M > INT32_MAX) return RG_ERR_INVALID_ARG;
+  if (N < 16 || N % 16 != 0 || K < 32 || K % 32 != 0) return RG_ERR_INVALID_ARG;
+  if (wq == nullptr || sw_blocked == nullptr || !aligned16(wq) || !aligned16(sw_blocked)) return RG_ERR_INVALID_ARG;
+  if (M > 0 && (xq == nullptr || sx_blocked == nullptr || y == nullptr || !aligned16(xq) ||
+                !aligned16(sx_blocked) || !aligned16(y)))
+    return RG_ERR_INVALID_ARG;
+  const int64_t max_tiles = (M / 128 + E) * ((N + 255) / 256);
+  if (max_tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != RG_OK) return rc;
+  if (rg::mx_smem_bytes(E) > ds->max_smem) return RG_ERR_INVALID_ARG;
+  if (M == 0) return RG_OK;
+
+  CUtensorMap tmA, tmB, tmY;
+  {  // xq [M, K] bytes: 128 x 128 boxes
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+    const uint64_t str[1] = {static_cast<uint64_t>(K)};
+    const uint32_t box[2] = {128, 128};
+    if (!encode_sw(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, xq, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return RG_ERR_INVALID_ARG;
+  }
+  if (!transpose_B) {  // wq [E, N, K]: one 128 (K) x 256 (N) box per stage
+    const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
+    const uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N) * K};
+    const uint32_t box[3] = {128, 256, 1};
+    if (!encode_sw(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, wq, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return RG_ERR_INVALID_ARG;
+  } else {  // wq [E, K, N]: two 128 (N) x 128 (K) boxes per stage
+    const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(E)};
+    const uint64_t str[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K) * N};
+    const uint32_t box[3] = {128, 128, 1};
+    if (!encode_sw(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, wq, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return RG_ERR_INVALID_ARG;
+  }
+  {  // y [M, N] bf16: 32 x 32 boxes, 64-byte swizzle
+    const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+    const uint64_t str[1] = {static_cast<uint64_t>(N) * 2};
+    const uint32_t box[2] = {32, 32};
+    if (!encode_sw(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B))
+      return RG_ERR_INVALID_ARG;
+  }
+  rg::MxArgs a;
+  a.offsets = offsets;
+  a.sfa = static_cast<const uint8_t*>(sx_blocked);
+  a.sfb = static_cast<const uint8_t*>(sw_blocked);
+  a.E = E;
+  a.M = static_cast<int>(M);
+  a.N = N;
+  a.K = K;
+  a.out = y;
+  a.status = ds->status;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  const cudaError_t e = rg::launch_mx_mgemm(transpose_B != 0, tmA, tmB, tmY, a, ds->num_sms, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
 }

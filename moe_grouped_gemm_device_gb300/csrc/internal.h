@@ -25,6 +25,17 @@ struct GroupArgs {
                             // with O > 1 the x and y maps are 3-D {cols, O, rows}
 };
 
+// Arguments of the MXFP8 Mgemm besides its tensor maps.
+struct MxArgs {
+  const int32_t* offsets;   // device [E+1]
+  const uint8_t* sfa;       // blocked E8M0 scales of A (rows grouped by offsets)
+  const uint8_t* sfb;       // blocked E8M0 scales of B (E groups of N rows)
+  int E, M, N, K;
+  void* out;                // y (bf16)
+  unsigned int* status;
+  unsigned long long wait_limit_ns;
+};
+
 // CTA group of the tensor-core MMAs: 2 (default) = a CTA pair computes one
 // tile with tcgen05.mma.cta_group::2; 1 = one CTA per tile.
 #ifndef RG_CTA_PAIR
@@ -86,6 +97,14 @@ cudaError_t launch_mgemm_swiglu_dgrad(const CUtensorMap& tmA, const CUtensorMap&
                                       cudaStream_t stream);
 cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
                          const GroupArgs& args, int grid, size_t max_smem, cudaStream_t stream);
+// MXFP8 Mgemm (FP8 E4M3 operands, E8M0 scales per 32 K elements in the
+// blocked layout) and the conversion of grouped scales to that layout.
+size_t mx_smem_bytes(int E);
+cudaError_t mx_setup(int max_smem);
+cudaError_t launch_mx_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                            const CUtensorMap& tmY, const MxArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_mx_blocked(const uint8_t* src, const int32_t* offsets, int G, int R, int KS, uint8_t* dst,
+                              unsigned int* status, int num_sms, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,
                                  cudaStream_t stream);
 

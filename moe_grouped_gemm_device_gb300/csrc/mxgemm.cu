@@ -1,0 +1,434 @@
+// MXFP8 M-grouped GEMM for sm_103a (FP8 E4M3 operands, one E8M0 scale per 32
+// elements along the contraction, fp32 accumulation, bf16 output), and the
+// conversion of grouped E8M0 scales into the blocked ("128x4") layout the
+// tensor cores read them in.  The MXFP8 grouped GEMM of the torchao MoE
+// training PR and the block-scaled FP8 GEMMs of the DeepGEMM issue thread,
+// over the Mgemm grouping of the RapidGEMM README ("Kernels").
+//
+// Blocked scale layout (rg_mx_scales_blocked).  The rows of a scale matrix
+// [R, KS] are grouped by an offsets vector; every group is cut into blocks of
+// 128 rows starting at its first row, and the blocks of all groups are
+// numbered in order.  Block b, chunk c (scale columns 4c..4c+3) is the
+// 512-byte range at (b * ceil(KS/4) + c) * 512; row i of the block and column
+// j of the chunk sit at byte 16*(i%32) + 4*(i/32) + j.  Positions past a
+// group's end or past column KS-1 hold 0x7F (scale 1.0).  One such range is
+// exactly what tcgen05.cp.32x128b.warpx4 moves into tensor memory: lane l
+// (of every 32-lane quarter) receives rows l, l+32, l+64, l+96 in four
+// consecutive 32-bit columns, one scale byte per 32-element K block.
+//
+// GEMM design (mx_mgemm_kernel)
+//   * Persistent grid, one CTA per SM, tile = 128 rows of one expert x 256
+//     output columns, tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale
+//     (M=128, N=256, K=32).  The tile list is built on the device from the
+//     offsets exactly as in the BF16 Mgemm (expert by expert, n fastest).
+//   * One stage = 128 K elements: A 128x128 B (16 KB), B 256x128 B (32 KB,
+//     K-major; or two 128x128 MN-major boxes for transpose_B), the A scale
+//     block (512 B) and the two B scale blocks (1 KB) -- four stages.
+//   * Warp 0 lane 0: TMA loads and bulk copies of the scale blocks.  Warp 1:
+//     tensor memory; its lane 0 copies each stage's scales into a per-stage
+//     slot of tensor memory (tcgen05.cp) and issues the four MMAs of the
+//     stage, scale byte k of each 32-bit scale word for MMA k.  Warps 2..9:
+//     epilogue, two per tensor-memory lane quarter (128 columns each).
+//   * Tensor memory: the fp32 accumulator (256 columns) and 4 x 12 scale
+//     columns; a second accumulator does not fit, so the epilogue drains the
+//     accumulator into registers and releases it before converting and
+//     storing, which lets the next tile's MMAs start almost at once.
+//   * Epilogue: bf16 (round to nearest even), 32-row x 32-column TMA stores
+//     through a 64-byte-swizzled staging buffer when all 32 rows belong to
+//     the expert, masked 16-byte stores otherwise.
+//   * Bounded waits as in the BF16 kernels (WaitGuard): a wait that runs out
+//     sets the device status, the CTA drains and frees tensor memory.
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace rg {
+namespace {
+
+struct MxCfg {
+  static constexpr int BM = 128;
+  static constexpr int BN = 256;
+  static constexpr int BK = 128;  // K elements (bytes) per stage
+  static constexpr int STAGES = 4;
+  static constexpr int A_BYTES = BM * BK;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int SFA_BYTES = 512;
+  static constexpr int SFB_BYTES = 1024;
+  static constexpr int AB_BYTES = A_BYTES + B_BYTES;   // operand tiles of a stage (1024-aligned)
+  static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGE_BYTES = AB_BYTES + SF_BYTES;  // bytes one stage's copies deliver
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_BUF_BYTES = 32 * 64;  // 32 rows x 32 bf16 columns
+  static constexpr int THREADS = 32 * (2 + EPI_WARPS);
+  // full[S], empty[S], tfull, tempty, drain
+  static constexpr int NUM_BARS = 2 * STAGES + 3;
+  // [operand tiles of every stage][scale blocks of every stage][epilogue buffers][barriers][misc]
+  static constexpr int SMEM_FIXED = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 + 16;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t SF_COL0 = 256;  // scale slots: stage s at SF_COL0 + 16 s (A: 4 cols, B: 8 cols)
+};
+static_assert(MxCfg::AB_BYTES % 1024 == 0, "operand tiles must keep the 1024-byte swizzle alignment");
+
+template <bool TRANS_B>
+__global__ void __launch_bounds__(MxCfg::THREADS, 1)
+    mx_mgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmY, const MxArgs args) {
+  using C = MxCfg;
+  constexpr int BM = C::BM, BN = C::BN, BK = C::BK, STAGES = C::STAGES;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicOr(args.status, kDevLaunchConfig);
+    return;
+  }
+  uint8_t* epi = smem + STAGES * C::STAGE_BYTES;  // after the operand tiles and the scale blocks
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_WARPS * C::EPI_BUF_BYTES);
+  int* misc = reinterpret_cast<int*>(bars + C::NUM_BARS);  // [0] tmem base, [1] abort
+  int* s_off = misc + 4;
+  int* s_pre = s_off + (args.E + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES);
+  const uint32_t tempty_bar = bar0 + 8u * (2 * STAGES + 1);
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int E = args.E, N = args.N, K = args.K;
+  const int nbn = (N + BN - 1) / BN;
+  const int nkc = (K + BK - 1) / BK;      // stages per tile = scale chunks per block
+  const int nb_w = (N + BM - 1) / BM;     // 128-row scale blocks of one expert's B
+
+  // ---- offsets -> shared memory, validation, tile prefix ---------------------
+  if (threadIdx.x == 0) misc[1] = 0;
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = args.offsets[i];
+  __syncthreads();
+  int bad = 0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) bad |= (s_off[i + 1] < s_off[i]);
+  if (threadIdx.x == 0) bad |= (s_off[0] != 0) | (s_off[E] > args.M);
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.status, kDevBadOffsets);
+    return;
+  }
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int lo = min(E, lane * per), hi = min(E, lo + per);
+    int s = 0;
+    for (int e = lo; e < hi; ++e) s += ((s_off[e + 1] - s_off[e] + BM - 1) / BM) * nbn;
+    int incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - s;
+    for (int e = lo; e < hi; ++e) {
+      s_pre[e] = run;
+      run += ((s_off[e + 1] - s_off[e] + BM - 1) / BM) * nbn;
+    }
+    if (lane == 31) s_pre[E] = incl;
+  }
+  __syncthreads();
+  const int T = s_pre[E];
+  if (static_cast<int>(blockIdx.x) >= T) return;
+
+  // ---- barriers and tensor memory -------------------------------------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, C::EPI_WARPS);
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc<1>(smem_u32(&misc[0]), C::TMEM_COLS);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = static_cast<uint32_t>(misc[0]);
+  const WaitGuard guard{args.status, args.wait_limit_ns, reinterpret_cast<volatile int*>(&misc[1])};
+  // stage s: A at s*AB_BYTES and B after it; its scale blocks after all operand tiles
+  auto sa_of = [&](int s) { return sbase + s * C::AB_BYTES; };
+  auto sb_of = [&](int s) { return sa_of(s) + C::A_BYTES; };
+  auto sfa_of = [&](int s) { return sbase + STAGES * C::AB_BYTES + s * C::SF_BYTES; };
+  auto sfb_of = [&](int s) { return sfa_of(s) + C::SFA_BYTES; };
+
+  if (warp == 0) {
+    // ======================= producer (warp 0, lane 0) =======================
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_par = 0;
+      bool ok = true;
+      int e = 0;
+      for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+        while (s_pre[e + 1] <= t) ++e;
+        const int local = t - s_pre[e];
+        const int mb = local / nbn, nt = local % nbn;
+        const int row0 = s_off[e] + mb * BM;
+        const int n0 = nt * BN;
+        // scale blocks: A block (rows of expert e, block mb), B blocks 2nt and
+        // 2nt+1 of expert e (the second repeats the first past the last
+        // block: those B rows are zero-filled, any finite scale will do)
+        const int blk_a = s_pre[e] / nbn + mb;
+        const int blk_b0 = e * nb_w + 2 * nt;
+        const int blk_b1 = e * nb_w + min(2 * nt + 1, nb_w - 1);
+        for (int kc = 0; kc < nkc; ++kc) {
+          if (!mbar_wait(guard, empty_bar(stage), phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          tma_load_2d(sa_of(stage), &tmA, fb, kc * BK, row0);
+          if constexpr (!TRANS_B) {
+            tma_load_3d(sb_of(stage), &tmB, fb, kc * BK, n0, e);
+          } else {
+            tma_load_3d(sb_of(stage), &tmB, fb, n0, kc * BK, e);
+            tma_load_3d(sb_of(stage) + 16384, &tmB, fb, n0 + 128, kc * BK, e);
+          }
+          bulk_load(sfa_of(stage), args.sfa + (static_cast<int64_t>(blk_a) * nkc + kc) * 512, 512, fb);
+          bulk_load(sfb_of(stage), args.sfb + (static_cast<int64_t>(blk_b0) * nkc + kc) * 512, 512, fb);
+          bulk_load(sfb_of(stage) + 512, args.sfb + (static_cast<int64_t>(blk_b1) * nkc + kc) * 512, 512, fb);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u, guard.limit_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ============= scale copies and MMAs (warp 1, lane 0) =====================
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < T; t += gridDim.x, ++acc) {
+      ok = __all_sync(0xffffffffu, mbar_wait(guard, tempty_bar, (acc & 1) ^ 1u));
+      if (!ok) break;
+      tc_fence_after();
+      for (int kc = 0; kc < nkc; ++kc) {
+        ok = __all_sync(0xffffffffu, mbar_wait(guard, full_bar(stage), phase));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sfa_t = tmem + C::SF_COL0 + 16u * stage;
+          const uint32_t sfb_t = sfa_t + 4u;
+          tmem_cp_32x128b_x4(sfa_t, sdesc_plain16(sfa_of(stage)));
+          tmem_cp_32x128b_x4(sfb_t, sdesc_plain16(sfb_of(stage)));
+          tmem_cp_32x128b_x4(sfb_t + 4u, sdesc_plain16(sfb_of(stage) + 512));
+          const uint32_t sa = sa_of(stage), sb = sb_of(stage);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k) {
+            const uint64_t ad = sdesc_sw128(sa + 32 * k, 16, 1024);
+            const uint64_t bd = TRANS_B ? sdesc_sw128(sb + 4096 * k, 16384, 1024)
+                                        : sdesc_sw128(sb + 32 * k, 16, 1024);
+            umma_mxf8(tmem, ad, bd, idesc_mxf8_f32(BM, BN, false, TRANS_B, k), sfa_t, sfb_t,
+                      (kc | k) != 0);
+          }
+          umma_commit<1>(empty_bar(stage));
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit<1>(tfull_bar);
+      __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      umma_commit<1>(drain_bar);
+      mbar_wait_drain(drain_bar, 0, guard.limit_ns);
+    }
+    __syncwarp();
+  } else {
+    // ======================= epilogue (warps 2..9) ===========================
+    // Warp w reads TMEM lane quarter q = w % 4 and column half h.
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int r_in = q * 32 + lane;
+    uint8_t* ebuf = epi + (warp - 2) * C::EPI_BUF_BYTES;
+    const uint32_t ebuf_s = smem_u32(ebuf);
+    __nv_bfloat16* y = static_cast<__nv_bfloat16*>(args.out);
+    int acc = 0;
+    int e = 0;
+    for (int t = blockIdx.x; t < T; t += gridDim.x, ++acc) {
+      while (s_pre[e + 1] <= t) ++e;
+      const int local = t - s_pre[e];
+      const int row0 = s_off[e] + (local / nbn) * BM;
+      const int n0 = (local % nbn) * BN + 128 * h;
+      const int rows_valid = min(BM, s_off[e + 1] - row0);
+      if (!__all_sync(0xffffffffu, mbar_wait(guard, tfull_bar, acc & 1))) break;
+      tc_fence_after();
+      uint32_t v[128];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + 128u * h;
+      tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_32x32b_x32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+      tmem_ld_32x32b_x32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar);  // the accumulator is free for the next tile
+      if (q * 32 >= rows_valid || n0 >= N) continue;
+      uint32_t p[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) p[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+      if (q * 32 + 32 <= rows_valid) {
+        // 4 TMA stores of 32 rows x 32 columns; columns >= N are clipped by the map
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (n0 + 32 * c >= N) break;
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * 64);
+          const int sw = (lane >> 1) & 3;  // 64-byte swizzle: 16-byte chunk ^= (row / 2) % 4
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            rowp[j ^ sw] = make_uint4(p[16 * c + 4 * j], p[16 * c + 4 * j + 1], p[16 * c + 4 * j + 2],
+                                      p[16 * c + 4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmY, ebuf_s, n0 + 32 * c, row0 + q * 32);
+            bulk_commit();
+          }
+        }
+      } else if (r_in < rows_valid) {
+        uint4* dst = reinterpret_cast<uint4*>(y + static_cast<int64_t>(row0 + r_in) * N + n0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (n0 + 8 * j < N) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  // ---- teardown --------------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<1>(tmem, C::TMEM_COLS);
+  }
+}
+
+// Blocked scale layout: one warp per 512-byte (block, chunk) range; lane l
+// gathers rows l, l+32, l+64, l+96 of the block (4 scale columns each) and
+// writes its 16 bytes, so each warp's store is one contiguous 512-byte line.
+__global__ void __launch_bounds__(256) mx_blocked_kernel(const uint8_t* __restrict__ src,
+                                                         const int32_t* __restrict__ offsets, int G, int R,
+                                                         int KS, uint8_t* __restrict__ dst,
+                                                         unsigned int* status) {
+  extern __shared__ int s_tab[];
+  int* s_off = s_tab;        // [G+1]
+  int* s_bp = s_tab + G + 1;  // [G+1] first block of each group
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i <= G; i += blockDim.x) s_off[i] = offsets[i];
+  __syncthreads();
+  int bad = 0;
+  for (int i = threadIdx.x; i < G; i += blockDim.x) bad |= (s_off[i + 1] < s_off[i]);
+  if (threadIdx.x == 0) bad |= (s_off[0] != 0) | (s_off[G] > R);
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, kDevBadOffsets);
+    return;
+  }
+  if (warp == 0) {
+    const int per = (G + 31) / 32;
+    const int lo = min(G, lane * per), hi = min(G, lo + per);
+    int s = 0;
+    for (int g = lo; g < hi; ++g) s += (s_off[g + 1] - s_off[g] + 127) / 128;
+    int incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - s;
+    for (int g = lo; g < hi; ++g) {
+      s_bp[g] = run;
+      run += (s_off[g + 1] - s_off[g] + 127) / 128;
+    }
+    if (lane == 31) s_bp[G] = incl;
+  }
+  __syncthreads();
+  const int nc = (KS + 3) / 4;
+  const int64_t items = static_cast<int64_t>(s_bp[G]) * nc;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t it = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp; it < items; it += nwarps) {
+    const int b = static_cast<int>(it / nc), c = static_cast<int>(it % nc);
+    int lo = 0, hi = G;  // the group of block b: the last g with s_bp[g] <= b
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_bp[mid] <= b) lo = mid;
+      else hi = mid;
+    }
+    const int base = s_off[lo] + 128 * (b - s_bp[lo]);
+    const int end = s_off[lo + 1];
+    uint32_t w[4];
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      const int r = base + lane + 32 * qq;
+      uint32_t v = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int col = 4 * c + j;
+        const uint32_t byte = (r < end && col < KS) ? src[static_cast<int64_t>(r) * KS + col] : 0x7Fu;
+        v |= byte << (8 * j);
+      }
+      w[qq] = v;
+    }
+    reinterpret_cast<uint4*>(dst + it * 512)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+}  // namespace
+
+size_t mx_smem_bytes(int E) { return MxCfg::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4; }
+
+cudaError_t mx_setup(int max_smem) {
+  const int bytes = static_cast<int>(std::min<size_t>(mx_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem));
+  cudaError_t e = cudaFuncSetAttribute(mx_mgemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mx_mgemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+cudaError_t launch_mx_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                            const CUtensorMap& tmY, const MxArgs& args, int grid, cudaStream_t stream) {
+  const size_t smem = mx_smem_bytes(args.E);
+  if (transpose_B)
+    mx_mgemm_kernel<true><<<grid, MxCfg::THREADS, smem, stream>>>(tmA, tmB, tmY, args);
+  else
+    mx_mgemm_kernel<false><<<grid, MxCfg::THREADS, smem, stream>>>(tmA, tmB, tmY, args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_blocked(const uint8_t* src, const int32_t* offsets, int G, int R, int KS, uint8_t* dst,
+                              unsigned int* status, int num_sms, cudaStream_t stream) {
+  const int64_t items_ub = (static_cast<int64_t>(R) / 128 + G) * ((KS + 3) / 4);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((items_ub + 7) / 8, 4 * num_sms)));
+  const size_t smem = 2 * (static_cast<size_t>(G) + 1) * sizeof(int);
+  mx_blocked_kernel<<<grid, 256, smem, stream>>>(src, offsets, G, R, KS, dst, status);
+  return cudaGetLastError();
+}
+
+}  // namespace rg

@@ -420,6 +420,57 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ---------------------------------------------------- block-scaled (MXFP8)
+
+// Untiled bulk copy global -> shared, completion on an mbarrier of this CTA.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// D[tmem] (+)= (A * 2^sfA) (B * 2^sfB)^T with FP8 E4M3 A/B in shared memory,
+// fp32 accumulate, one E8M0 scale per row and 32-element K block read from
+// tensor memory (kind::mxf8f6f4, block size 32, K = 32 per instruction).
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy a 32-row x 16-byte matrix from shared memory (descriptor) into tensor
+// memory columns [taddr, taddr+4) of lanes 0..31, replicated into each of the
+// four 32-lane quarters.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Descriptor of a contiguous, unswizzled K-major shared-memory matrix whose
+// rows are 16 bytes: 8-row core matrices 128 bytes apart (SBO), one core
+// matrix along K (LBO unused).  Layout type 0 (no swizzle).
+__device__ __forceinline__ uint64_t sdesc_plain16(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(128u >> 4) << 16) |
+         (static_cast<uint64_t>(128u >> 4) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4 with E4M3 A and B,
+// E8M0 scales and fp32 D.  Bits: [4,6) B scale-factor id (byte of the scale
+// word), [7,10) A format (0 = E4M3), [10,13) B format (0 = E4M3), 15 A major,
+// 16 B major (1 = MN), [17,23) N>>3, 23 scale format (1 = E8M0), [24,29) M>>4,
+// [29,31) A scale-factor id.
+__host__ __device__ constexpr uint32_t idesc_mxf8_f32(int M, int N, bool a_mn, bool b_mn, uint32_t sf_id) {
+  return ((sf_id & 3u) << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
+         ((sf_id & 3u) << 29);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32_bits, uint32_t hi_f32_bits) {
   __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo_f32_bits), __uint_as_float(hi_f32_bits));
   return *reinterpret_cast<uint32_t*>(&h);

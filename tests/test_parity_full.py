@@ -60,6 +60,48 @@ def sample_pairs(counts, N, rng):
     return np.array(es, dtype=np.int32), np.array(ns, dtype=np.int32)
 
 
+MX = [("a3b_mxfp8", op) for op in ("mx_fwd_gate_up", "mx_fwd_down", "mx_dgrad_down", "mx_dgrad_gate_up")]
+
+
+def dev_u8(wl, name):
+    shape, kind, stream = wl.tensors[name]
+    key = (wl.seed, stream, tuple(shape), str(kind))
+    if key not in _DEV:
+        import torch
+        _DEV[key] = torch.from_numpy(host_u8(wl, name)).cuda()
+    return _DEV[key]
+
+
+def host_u8(wl, name):
+    shape, kind, stream = wl.tensors[name]
+    key = (wl.seed, stream, tuple(shape), str(kind))
+    if key not in _HOST:
+        _HOST[key] = wl.tensor(name)
+    return _HOST[key]
+
+
+@pytest.mark.parametrize("wname,opname", MX, ids=[f"{w}-{o}" for w, o in MX])
+def test_full_size_sampled_mxfp8(gpu_lib, wname, opname):
+    """Scale layout conversion and MXFP8 GEMM as the benchmark runs them."""
+    import torch
+    wl = W.ALL[wname]()
+    op = wl.op(opname)
+    off = wl.offsets
+    rng = np.random.default_rng(zlib.crc32(f"{wname}/{opname}".encode()))
+    doff = offsets_dev(off)
+    sa, sb = dev_u8(wl, op.sa), dev_u8(wl, op.sb)
+    sab = gpu_lib.mx_scales_blocked(sa, doff)
+    sbb = gpu_lib.mx_scales_blocked(sb.view(-1, sb.shape[-1]), gpu_lib.mx_weight_offsets(wl.E, op.N))
+    y = gpu_lib.mgemm_mxfp8(dev_u8(wl, op.a), sab, dev_u8(wl, op.b), sbb, doff, transpose_B=op.transpose_B)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    rows = sample_rows(off, rng, n_random=32)
+    got = to_host_bits(y[torch.from_numpy(rows).cuda()])
+    ref = oracle.mgemm_mx(host_u8(wl, op.a), host_u8(wl, op.sa), host_u8(wl, op.b), host_u8(wl, op.sb), off,
+                          transpose_B=op.transpose_B, rows=rows)
+    check_bf16(got, ref, f"{wname}/{opname}")
+
+
 NESTED = [("lora_a3b", "lora_shrink"), ("lora_a3b", "lora_expand")]
 
 

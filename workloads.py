@@ -129,6 +129,17 @@ def e8m0_codes(shape, lo: int, hi: int, seed: int, stream: int) -> np.ndarray:
     return rng.integers(lo, hi + 1, size=shape, dtype=np.int64).astype(np.uint8)
 
 
+# RMS of the values of e4m3_codes is about 119 (2^6.9): scale codes around
+# 120 (2^-7) give activations of RMS ~1, and 120 - log2(sqrt(K)) weights of
+# RMS ~1/sqrt(K), the magnitudes of the bf16 workloads.
+MX_ACT_SCALES = (119, 121)
+
+
+def mx_weight_scales(K: int) -> tuple:
+    c = 120 - int(round(np.log2(np.sqrt(K))))
+    return (c - 1, c + 1)
+
+
 # --------------------------------------------------------------------------
 # Row counts and offsets
 # --------------------------------------------------------------------------
@@ -371,20 +382,25 @@ def a3b_mxfp8() -> Workload:
     M = 32768).  The weights carry one scale tensor per direction (row-wise
     for the forward, column-wise for the input gradient), as a training step
     that quantizes each weight once per GEMM direction would hold.  Codes and
-    scales are random draws (scales 2^-8 .. 2^1)."""
+    scales are random draws; scales put activations at RMS ~1 and weights at
+    RMS ~1/sqrt(K), like the bf16 layer."""
     c = counts_dirichlet(32, 32768, 2.0, 3)
     E, M, dm, d2, d1 = 32, 32768, 3072, 2560, 1280
-    sc = ("e8m0", 119, 128)
+    act = ("e8m0",) + MX_ACT_SCALES
+
+    def wsc(K):
+        return ("e8m0",) + mx_weight_scales(K)
+
     w = Workload("a3b_mxfp8_E32_M32768", 3, E, M, c)
     w.tensors = {
-        "xq": ((M, dm), "e4m3", 21), "sx": ((M, dm // 32), sc, 22),
-        "w13q": ((E, d2, dm), "e4m3", 23), "sw13": ((E, d2, dm // 32), sc, 24),
-        "hq": ((M, d1), "e4m3", 25), "sh": ((M, d1 // 32), sc, 26),
-        "w2q": ((E, dm, d1), "e4m3", 27), "sw2": ((E, dm, d1 // 32), sc, 28),
-        "dy2q": ((M, dm), "e4m3", 29), "sdy2": ((M, dm // 32), sc, 30),
-        "sw2t": ((E, d1, dm // 32), sc, 31),
-        "dy13q": ((M, d2), "e4m3", 32), "sdy13": ((M, d2 // 32), sc, 33),
-        "sw13t": ((E, dm, d2 // 32), sc, 34),
+        "xq": ((M, dm), "e4m3", 21), "sx": ((M, dm // 32), act, 22),
+        "w13q": ((E, d2, dm), "e4m3", 23), "sw13": ((E, d2, dm // 32), wsc(dm), 24),
+        "hq": ((M, d1), "e4m3", 25), "sh": ((M, d1 // 32), act, 26),
+        "w2q": ((E, dm, d1), "e4m3", 27), "sw2": ((E, dm, d1 // 32), wsc(d1), 28),
+        "dy2q": ((M, dm), "e4m3", 29), "sdy2": ((M, dm // 32), act, 30),
+        "sw2t": ((E, d1, dm // 32), wsc(dm), 31),
+        "dy13q": ((M, d2), "e4m3", 32), "sdy13": ((M, d2 // 32), act, 33),
+        "sw13t": ((E, dm, d2 // 32), wsc(d2), 34),
     }
     w.ops = [
         Op("mx_fwd_gate_up", "mx", "xq", "w13q", N=d2, K=dm, sa="sx", sb="sw13"),
