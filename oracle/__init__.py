@@ -68,6 +68,12 @@ def _load():
         lib.oracle_mx_blocked.argtypes = [c_p, ctypes.c_int64, ctypes.c_int, c_p, ctypes.c_int,
                                           c_p, ctypes.c_int64]
         lib.oracle_mx_blocked.restype = ctypes.c_int64
+        lib.oracle_kgemm_mx_rows.argtypes = [c_p, c_p, c_p, c_p, c_p, ctypes.c_int, ctypes.c_int64,
+                                             ctypes.c_int, ctypes.c_int, c_p, c_p, ctypes.c_int64, c_p]
+        lib.oracle_kgemm_mx_rows.restype = ctypes.c_int
+        lib.oracle_mx_blocked_k.argtypes = [c_p, ctypes.c_int64, ctypes.c_int, c_p, ctypes.c_int,
+                                            c_p, ctypes.c_int64]
+        lib.oracle_mx_blocked_k.restype = ctypes.c_int64
         lib.oracle_kgemm_rows.argtypes = [c_p, c_p, c_p, ctypes.c_int, ctypes.c_int64,
                                           ctypes.c_int, ctypes.c_int,
                                           c_p, c_p, ctypes.c_int64, c_p]
@@ -219,6 +225,51 @@ def mx_blocked(scales, offsets, fill: int = 0) -> np.ndarray:
     nb = _load().oracle_mx_blocked(_ptr(src), R, KS, _ptr(off), G, _ptr(dst), dst.size)
     if nb < 0:
         raise ValueError("oracle_mx_blocked rejected its arguments")
+    return dst
+
+
+def kgemm_mx(gq, sg, xq, sx, offsets, sel=None) -> np.ndarray:
+    """MXFP8 K-grouped weight gradient in FP64.  gq uint8 [M,N], xq uint8
+    [M,K] (E4M3), sg uint8 [N,M/32], sx uint8 [K,M/32] (E8M0, one scale per
+    column and 32-row block), offsets int32 [E+1], all multiples of 32.
+    Returns float64 [E,N,K], or [len(experts), K] for sel = (experts, ns)."""
+    gq, sg, xq, sx = _u8(gq), _u8(sg), _u8(xq), _u8(sx)
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    M, N = gq.shape
+    K = xq.shape[1]
+    E = len(off) - 1
+    assert xq.shape[0] == M and M % 32 == 0 and sg.shape == (N, M // 32) and sx.shape == (K, M // 32)
+    full = sel is None
+    if full:
+        se = np.repeat(np.arange(E, dtype=np.int32), N)
+        sn = np.tile(np.arange(N, dtype=np.int32), E)
+    else:
+        se = np.ascontiguousarray(sel[0], dtype=np.int32)
+        sn = np.ascontiguousarray(sel[1], dtype=np.int32)
+    out = np.empty((len(se), K), dtype=np.float64)
+    rc = _load().oracle_kgemm_mx_rows(_ptr(gq), _ptr(sg), _ptr(xq), _ptr(sx), _ptr(off), E, M, N, K,
+                                      _ptr(se), _ptr(sn), len(se), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_kgemm_mx_rows rejected its arguments")
+    return out.reshape(E, N, K) if full else out
+
+
+def mx_blocked_k_bytes(R: int, KS: int, G: int) -> int:
+    """Upper bound of the K-grouped blocked layout's size."""
+    return ((R + 127) // 128) * (KS // 4 + G) * 512
+
+
+def mx_blocked_k(scales, offsets, fill: int = 0) -> np.ndarray:
+    """Blocked layout of scales [R, KS] grouped along the contraction by
+    offsets (multiples of 32): see oracle_mx_blocked_k in oracle.c."""
+    src = _u8(scales)
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    R, KS = src.shape
+    G = len(off) - 1
+    dst = np.full(mx_blocked_k_bytes(R, KS, G), fill, dtype=np.uint8)
+    nq = _load().oracle_mx_blocked_k(_ptr(src), R, KS, _ptr(off), G, _ptr(dst), dst.size)
+    if nq < 0:
+        raise ValueError("oracle_mx_blocked_k rejected its arguments")
     return dst
 
 

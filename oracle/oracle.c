@@ -33,7 +33,14 @@
  *   sx [M,K/32] and sw [E,N,K/32] E8M0 codes:
  *       y[r,n] = sum_k (xq[r,k] * 2^(sx[r,k/32]-127)) * (wq[e,n,k] * 2^(sw[e,n,k/32]-127))
  *
- * Inputs are bf16 bit patterns (E4M3 / E8M0 codes for the MXFP8 GEMM); each value is widened exactly to double.
+ *   MXFP8 K-grouped weight gradient (the wgrad of the same MXFP8 MoE
+ *   training: operands quantized along the contraction, which runs over each
+ *   expert's rows, so every expert's row range is a whole number of 32-row
+ *   scale blocks).  gq [M,N], xq [M,K] E4M3 codes, sg [N,M/32] and
+ *   sx [K,M/32] E8M0 codes (one scale per column and 32-row block):
+ *       dW[e,n,k] = sum_{r in group e} (gq[r,n] * 2^(sg[n,r/32]-127)) * (xq[r,k] * 2^(sx[k,r/32]-127))
+ *
+ * Inputs are bf16 bit patterns (E4M3 / E8M0 codes for the MXFP8 GEMMs); each value is widened exactly to double.
  * Products of two bf16 values are exact in double, so the result depends only
  * on the summation order, which is ascending k (Mgemm) or ascending r (Kgemm).
  *
@@ -215,6 +222,74 @@ int64_t oracle_mx_blocked(const uint8_t *src, int64_t R, int KS, const int32_t *
         }
     }
     return b;
+}
+
+/*
+ * MXFP8 Kgemm on a list of (expert, n) pairs: out[i, k] = dW[sel_e[i],
+ * sel_n[i], k].  Every offset must be a multiple of 32.  Returns 0 or -1.
+ */
+int oracle_kgemm_mx_rows(const uint8_t *gq, const uint8_t *sg, const uint8_t *xq, const uint8_t *sx,
+                         const int32_t *offsets, int E, int64_t M, int N, int K,
+                         const int32_t *sel_e, const int32_t *sel_n, int64_t nsel, double *out) {
+    if (N < 1 || K < 1 || M % 32 != 0 || check_offsets(offsets, E, M) != 0) return -1;
+    for (int e = 0; e <= E; ++e)
+        if (offsets[e] % 32 != 0) return -1;
+    for (int64_t i = 0; i < nsel; ++i)
+        if (sel_e[i] < 0 || sel_e[i] >= E || sel_n[i] < 0 || sel_n[i] >= N) return -1;
+    const int64_t MS = M / 32;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nsel; ++i) {
+        const int e = sel_e[i];
+        const int n = sel_n[i];
+        double *o = out + i * (int64_t)K;
+        for (int k = 0; k < K; ++k) o[k] = 0.0;
+        for (int64_t r = offsets[e]; r < (int64_t)offsets[e + 1]; ++r) {
+            const double g = e4m3_to_double(gq[r * (int64_t)N + n]) * e8m0_to_double(sg[(int64_t)n * MS + r / 32]);
+            for (int k = 0; k < K; ++k)
+                o[k] += g * (e4m3_to_double(xq[r * (int64_t)K + k]) * e8m0_to_double(sx[(int64_t)k * MS + r / 32]));
+        }
+    }
+    return 0;
+}
+
+/*
+ * Blocked scale layout for groups along the contraction (the torchao PR's
+ * conversion "for groups along K"): src [R, KS] holds, for each of R rows
+ * (an operand's columns), KS scales along the contraction; offsets [G+1]
+ * are contraction indices (multiples of 32, offsets[G] <= 32*KS), so group g
+ * owns scale columns offsets[g]/32 .. offsets[g+1]/32 - 1.  Each group's
+ * scale columns are cut into chunks of 4 from its first column; the chunks
+ * of all groups are numbered in order (NQ in total).  Row block rb (rows
+ * 128rb ..), chunk q is the 512 bytes at (rb * NQ + q) * 512, with row i
+ * and column j of the chunk at byte 16*(i%32) + 4*(i/32) + j; positions past
+ * row R-1 or past the group's last scale column hold 0x7F.  Returns NQ or -1.
+ */
+int64_t oracle_mx_blocked_k(const uint8_t *src, int64_t R, int KS, const int32_t *offsets, int G,
+                            uint8_t *dst, int64_t dst_bytes) {
+    if (R < 1 || KS < 1 || check_offsets(offsets, G, (int64_t)KS * 32) != 0) return -1;
+    for (int g = 0; g <= G; ++g)
+        if (offsets[g] % 32 != 0) return -1;
+    int64_t NQ = 0;
+    for (int g = 0; g < G; ++g) NQ += (offsets[g + 1] - offsets[g] + 127) / 128;
+    const int64_t NRB = (R + 127) / 128;
+    if (NRB * NQ * 512 > dst_bytes) return -1;
+    int64_t q = 0;
+    for (int g = 0; g < G; ++g) {
+        const int c0 = offsets[g] / 32, c1 = offsets[g + 1] / 32;
+        for (int cb = c0; cb < c1; cb += 4, ++q)
+            for (int64_t rb = 0; rb < NRB; ++rb) {
+                uint8_t *blk = dst + (rb * NQ + q) * 512;
+                for (int i = 0; i < 128; ++i)
+                    for (int j = 0; j < 4; ++j) {
+                        const int64_t r = 128 * rb + i;
+                        const int col = cb + j;
+                        blk[16 * (i % 32) + 4 * (i / 32) + j] =
+                            (r < R && col < c1) ? src[r * KS + col] : (uint8_t)0x7F;
+                    }
+            }
+    }
+    return NQ;
 }
 
 /* Decoded values of the 256 E4M3 codes and of the 256 E8M0 codes. */

@@ -634,3 +634,95 @@ def test_mx_blocked_full_blocks_are_a_reshape():
     dst = oracle.mx_blocked(src, W.offsets_from_counts([128] * G))
     want = src.reshape(G, 4, 32, KS // 4, 4).transpose(0, 3, 2, 1, 4).reshape(-1)
     np.testing.assert_array_equal(dst[: want.size], want)
+
+
+def test_mx_blocked_k_golden_handworked():
+    g = json.load(open(os.path.join(GOLDEN, "mx_blocked_k_handworked.json")))
+    r, c = np.meshgrid(np.arange(g["R"]), np.arange(g["KS"]), indexing="ij")
+    src = eval(g["src"], {}, {"r": r, "c": c}).astype(np.uint8)
+    dst = oracle.mx_blocked_k(src, np.array(g["offsets"], dtype=np.int32))
+    for x in g["expect"]:
+        assert int(dst[x["byte"]]) == x["value"], x["why"]
+
+
+def test_mx_blocked_k_reduces_to_row_layout_for_whole_chunks():
+    """Groups whose lengths are multiples of 128 (whole chunks): the chunks
+    run through the scale columns in order, which is the row-grouped layout
+    of the whole matrix taken as one group."""
+    rng = np.random.default_rng(37)
+    R, KS = 300, 16
+    src = rng.integers(0, 256, size=(R, KS), dtype=np.int64).astype(np.uint8)
+    off = np.array([0, 128, 128, 384, 512], dtype=np.int32)
+    a = oracle.mx_blocked_k(src, off)
+    b = oracle.mx_blocked(src, np.array([0, R], dtype=np.int32))
+    n = ((R + 127) // 128) * (KS // 4) * 512
+    np.testing.assert_array_equal(a[:n], b[:n])
+
+
+def test_mx_blocked_k_is_a_bijection_with_pad():
+    rng = np.random.default_rng(38)
+    off = np.array([0, 64, 64, 96, 416], dtype=np.int32)
+    R, KS = 200, 13
+    src = rng.integers(0, 256, size=(R, KS), dtype=np.int64).astype(np.uint8)
+    dst = oracle.mx_blocked_k(src, off, fill=0xEE)
+    seen = np.zeros(dst.size, dtype=bool)
+    chunks = [(g, cb) for g in range(4) for cb in range(off[g] // 32, off[g + 1] // 32, 4)]
+    NQ = len(chunks)
+    for rb in range((R + 127) // 128):
+        for q, (g, cb) in enumerate(chunks):
+            for i in range(128):
+                for j in range(4):
+                    pos = (rb * NQ + q) * 512 + 16 * (i % 32) + 4 * (i // 32) + j
+                    assert not seen[pos]
+                    seen[pos] = True
+                    r, col = 128 * rb + i, cb + j
+                    want = src[r, col] if (r < R and col < off[g + 1] // 32) else 0x7F
+                    assert dst[pos] == want
+    assert (dst[~seen] == 0xEE).all()
+
+
+def _mxk_tiny(rng, M, N, K):
+    s = int(rng.integers(1 << 30))
+    gq, xq = W.e4m3_codes((M, N), s, 0), W.e4m3_codes((M, K), s, 1)
+    sg = W.e8m0_codes((N, M // 32), 118, 130, s, 2)
+    sx = W.e8m0_codes((K, M // 32), 118, 130, s, 3)
+    return gq, sg, xq, sx
+
+
+def test_mx_kgemm_matches_brute_force():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(39)
+    M, N, K = 96, 3, 4
+    off = np.array([0, 32, 32, 96], dtype=np.int32)
+    gq, sg, xq, sx = _mxk_tiny(rng, M, N, K)
+    dec = lambda q: torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy().tolist()  # noqa: E731
+    G, X, SG, SX = dec(gq), dec(xq), sg.tolist(), sx.tolist()
+    dW = oracle.kgemm_mx(gq, sg, xq, sx, off)
+    for e in range(3):
+        for n in range(N):
+            for k in range(K):
+                s = 0.0
+                for r in range(off[e], off[e + 1]):
+                    s += (G[r][n] * 2.0 ** (SG[n][r // 32] - 127)) * (X[r][k] * 2.0 ** (SX[k][r // 32] - 127))
+                assert dW[e, n, k] == s
+    assert (dW[1] == 0).all()
+
+
+def test_mx_kgemm_equals_bf16_kgemm_on_dequantized_inputs():
+    rng = np.random.default_rng(40)
+    M, N, K = 192, 9, 11
+    off = np.array([0, 64, 64, 160, 192], dtype=np.int32)
+    gq, sg, xq, sx = _mxk_tiny(rng, M, N, K)
+    e4, e8 = oracle.mx_decode_tables()
+    gv = e4[gq] * e8[np.repeat(sg, 32, axis=1).T]
+    xv = e4[xq] * e8[np.repeat(sx, 32, axis=1).T]
+    gb, xb = W.f32_to_bf16_bits(gv.astype(np.float32)), W.f32_to_bf16_bits(xv.astype(np.float32))
+    assert (W.bf16_bits_to_f32(gb) == gv).all() and (W.bf16_bits_to_f32(xb) == xv).all()
+    np.testing.assert_array_equal(oracle.kgemm_mx(gq, sg, xq, sx, off), oracle.kgemm(gb, xb, off))
+
+
+def test_mx_kgemm_rejects_unaligned_groups():
+    rng = np.random.default_rng(41)
+    gq, sg, xq, sx = _mxk_tiny(rng, 64, 2, 2)
+    with pytest.raises(ValueError):
+        oracle.kgemm_mx(gq, sg, xq, sx, np.array([0, 40, 64], dtype=np.int32))
