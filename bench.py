@@ -46,12 +46,15 @@ L2_BYTES = 129 * 2**20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_OF = {"mgemm": "mgemm_kernel<false>", "mgemm_t": "mgemm_kernel<true>", "kgemm": "kgemm_kernel",
              "swiglu": "mgemm_kernel<false,swiglu>", "swiglu_bwd": "mgemm_kernel<true,swiglu_bwd>",
-             "mx": "mx_mgemm_kernel<false>", "mx_t": "mx_mgemm_kernel<true>", "mx_blocked": "mx_blocked_kernel"}
+             "mx": "mx_mgemm_kernel<false>", "mx_t": "mx_mgemm_kernel<true>", "mx_blocked": "mx_blocked_kernel",
+             "mxk": "mx_kgemm_kernel", "mx_blocked_k": "mx_blocked_k_kernel"}
 KERNEL_SOURCES = {"mgemm_kernel<false>": "mgemm.cu", "mgemm_kernel<true>": "mgemm.cu",
                   "mgemm_kernel<false,swiglu>": "mgemm.cu", "mgemm_kernel<true,swiglu_bwd>": "mgemm.cu",
                   "kgemm_kernel": "kgemm.cu", "mx_mgemm_kernel<false>": "mxgemm.cu",
-                  "mx_mgemm_kernel<true>": "mxgemm.cu", "mx_blocked_kernel": "mxgemm.cu"}
-FP8_KERNELS = ("mx_mgemm_kernel<false>", "mx_mgemm_kernel<true>")
+                  "mx_mgemm_kernel<true>": "mxgemm.cu", "mx_blocked_kernel": "mxgemm.cu",
+                  "mx_kgemm_kernel": "mxgemm.cu", "mx_blocked_k_kernel": "mxgemm.cu"}
+FP8_KERNELS = ("mx_mgemm_kernel<false>", "mx_mgemm_kernel<true>", "mx_kgemm_kernel")
+CONVERSION_KERNELS = ("mx_blocked_kernel", "mx_blocked_k_kernel")
 
 
 def tensor_peak(kernel: str, peaks) -> float:
@@ -83,6 +86,8 @@ def load_peaks():
 
 
 def kernel_of(op) -> str:
+    if op.kind == "mxk":
+        return KERNEL_OF["mxk"]
     if op.kind == "mx":
         return KERNEL_OF["mx_t" if op.transpose_B else "mx"]
     if op.kind == "nested":
@@ -100,6 +105,8 @@ def algorithmic_bytes(op, counts) -> int:
     if op.kind == "kgemm":
         return 2 * M * op.N + 2 * M * op.K + 4 * E * op.N * op.K
     nonempty = int(np.count_nonzero(counts))
+    if op.kind == "mxk":  # FP8 grad and X, their scales, fp32 dW
+        return M * op.N + M * op.K + (op.N + op.K) * (M // 32) + 4 * E * op.N * op.K
     if op.kind == "mx":  # FP8 operands, their scales (1 byte per 32), bf16 y
         return M * op.K + op.N * op.K * nonempty + (M + op.N * nonempty) * (op.K // 32) + 2 * M * op.N
     if op.kind == "nested":  # x [M, O*K], w [O, L, N, K] (non-empty groups), y [M, O*N]
@@ -124,7 +131,7 @@ def working_set_bytes(wl) -> int:
     for name, (shape, kind, _) in wl.tensors.items():
         tot += (1 if isinstance(kind, (str, tuple)) else 2) * int(np.prod(shape))
     for op in wl.ops:
-        if op.kind == "kgemm":
+        if op.kind in ("kgemm", "mxk"):
             tot += 4 * wl.E * op.N * op.K
         elif op.kind == "nested":
             tot += 2 * wl.M * op.outer * op.N
@@ -211,6 +218,14 @@ def oracle_sample_step(wl, tensors, budget_s: float, rng) -> tuple[float, float,
                 rows = rng.integers(0, int(off[-1]), size=n)
                 oracle.mgemm_mx(a, tensors[op.sa], b, tensors[op.sb], off, transpose_B=op.transpose_B, rows=rows)
                 return n * unit
+        elif op.kind == "mxk":
+            nz = np.flatnonzero(counts)
+
+            def run(n):
+                es = rng.choice(nz, size=n)
+                ns = rng.integers(0, op.N, size=n)
+                oracle.kgemm_mx(a, tensors[op.sa], b, tensors[op.sb], off, sel=(es, ns))
+                return float(np.sum(2.0 * counts[es] * op.K))
         elif op.kind == "nested":
             unit = 2.0 * op.outer * op.N * op.K
 
@@ -345,6 +360,20 @@ def build_units(wl, rg, tensors, outs, off_ref, scratch):
                                out=outs[op.name])
             units.append(Unit(op.name, kernel_of(op), op.flops(counts), algorithmic_bytes(op, counts), gemm, op))
             continue
+        if op.kind == "mxk":
+            sa, sb = tensors[op.sa], tensors[op.sb]
+            sab, sbb = scratch[op.name + ":sa"], scratch[op.name + ":sb"]
+            conv_bytes = (op.N + op.K) * (M // 32) + sab.numel() + sbb.numel()
+
+            def conv(sa=sa, sb=sb, sab=sab, sbb=sbb):
+                rg.mx_scales_blocked_k(sa, off_ref[0], out=sab)
+                rg.mx_scales_blocked_k(sb, off_ref[0], out=sbb)
+            units.append(Unit(op.name + ".scales", KERNEL_OF["mx_blocked_k"], 0, conv_bytes, conv))
+
+            def wgrad(op=op, sab=sab, sbb=sbb):
+                rg.kgemm_mxfp8(tensors[op.a], sab, tensors[op.b], sbb, off_ref[0], out=outs[op.name])
+            units.append(Unit(op.name, kernel_of(op), op.flops(counts), algorithmic_bytes(op, counts), wgrad, op))
+            continue
 
         def call(op=op):
             out = outs[op.name]
@@ -405,7 +434,7 @@ def main():
     outs, scratch = {}, {}
     is_mx = any(op.kind == "mx" for op in wl.ops)
     for op in wl.ops:
-        if op.kind == "kgemm":
+        if op.kind in ("kgemm", "mxk"):
             outs[op.name] = torch.empty((wl.E, op.N, op.K), dtype=torch.float32, device=dev)
         elif op.kind == "nested":
             outs[op.name] = torch.empty((wl.M, op.outer * op.N), dtype=torch.bfloat16, device=dev)
@@ -423,6 +452,12 @@ def main():
             scratch[op.name + ":sb"] = torch.empty((rg.mx_blocked_bytes(wl.E * op.N, KS, wl.E),),
                                                    dtype=torch.uint8, device=dev)
             scratch["woff:" + str(op.N)] = rg.mx_weight_offsets(wl.E, op.N, device=dev)
+        if op.kind == "mxk":
+            MS = wl.M // 32
+            scratch[op.name + ":sa"] = torch.empty((rg.mx_blocked_k_bytes(op.N, MS, wl.E),), dtype=torch.uint8,
+                                                   device=dev)
+            scratch[op.name + ":sb"] = torch.empty((rg.mx_blocked_k_bytes(op.K, MS, wl.E),), dtype=torch.uint8,
+                                                   device=dev)
     stream = torch.cuda.current_stream(dev)
     off_used = [off]
     units = build_units(wl, rg, d, outs, off_used, scratch)
@@ -581,7 +616,7 @@ def main():
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": sum(2 if u.kernel == KERNEL_OF["mx_blocked"] else 1 for u in units) * args.steps,
+        "gpu_launches": sum(2 if u.kernel in CONVERSION_KERNELS else 1 for u in units) * args.steps,
         "clocks": clocks,
         "per_op": per_op,
     }

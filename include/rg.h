@@ -172,6 +172,65 @@ int rg_mgemm_mxfp8(const void* xq, const void* sx_blocked, const void* wq, const
                    cudaStream_t stream);
 
 /*
+ * rg_mx_blocked_k_bytes -- size in bytes that rg_mx_scales_blocked_k may
+ * write for R rows of KS scales in G contraction groups:
+ * ceil(R/128) * (KS/4 + G) * 512.  -1 on bad arguments.  Host-only.
+ */
+int64_t rg_mx_blocked_k_bytes(int64_t R, int KS, int G);
+
+/*
+ * rg_mx_scales_blocked_k -- blocked ("128x4") layout of E8M0 scales whose
+ * groups run along the contraction: the conversion "for groups along K" of
+ * the torchao MoE-training PR, which the K-grouped weight gradient reads.
+ *
+ *   scales   device, uint8 [R, KS]: R rows (an operand's columns, e.g. the N
+ *            columns of the output gradient), KS scales along the contraction
+ *            (one per 32 rows of the expert-grouped operand).
+ *   offsets  device, int32 [G+1]: contraction indices with a leading zero,
+ *            non-decreasing, all multiples of 32, offsets[G] <= 32*KS (the
+ *            expert row offsets of rg_kgemm_mxfp8).  Group g owns scale
+ *            columns offsets[g]/32 .. offsets[g+1]/32 - 1.
+ *   out      device, uint8, 16-byte aligned, out_bytes >= rg_mx_blocked_k_bytes.
+ *            Each group's scale columns are cut into chunks of 4 from its
+ *            first column; the chunks of all groups are numbered in order
+ *            (NQ in total); row block rb (rows 128rb ..), chunk q is the 512
+ *            bytes at (rb*NQ + q)*512 with row i, column j of the chunk at
+ *            byte 16*(i%32) + 4*(i/32) + j.  Positions past row R-1 or past
+ *            the group's last column are 0x7F.  Later bytes are not written.
+ *   G 1 .. RG_MAX_EXPERTS, R >= 1, KS >= 1.
+ * Invalid offsets contents (including a multiple-of-32 violation) set
+ * RG_DEV_BAD_OFFSETS and write nothing.
+ */
+int rg_mx_scales_blocked_k(const uint8_t* scales, const int32_t* offsets, int G, int64_t R, int KS,
+                           uint8_t* out, int64_t out_bytes, cudaStream_t stream);
+
+/*
+ * rg_kgemm_mxfp8 -- K-grouped MXFP8 weight gradient with FP32 output (the
+ * wgrad of MXFP8 MoE training in the torchao PR; the DeepGEMM issue thread
+ * asks for FP8 wgrad with per-expert row counts that are not multiples of
+ * 128 -- here they need only be multiples of the 32-row scale block).
+ *
+ *   gq          device, uint8 [M, N]: E4M3 codes of the output gradient.
+ *   sg_blocked  device: its scales sg [N, M/32] (sg[n, r/32] scales gq[r, n])
+ *               in the layout of rg_mx_scales_blocked_k with these offsets.
+ *   xq          device, uint8 [M, K]: E4M3 codes of the layer input.
+ *   sx_blocked  device: its scales sx [K, M/32], same layout.
+ *   offsets     device, int32 [E+1]: expert row offsets, all multiples of 32.
+ *   dW          device, fp32 [E, N, K]:
+ *                 dW[e,n,k] (+)= sum over rows r of expert e of
+ *                   gq[r,n] 2^(sg[n,r/32]-127) * xq[r,k] 2^(sx[k,r/32]-127)
+ *               overwritten (accumulate == 0; an expert without rows gets 0)
+ *               or added to (accumulate != 0; experts without rows unchanged).
+ *               The rows of an expert are summed in FP32 by the tensor cores in
+ *               chunks of at most 4096 rows, added in FP32 in row order.
+ *   M multiple of 32; N, K >= 16 and multiples of 16; E 1..RG_MAX_EXPERTS.
+ *   Pointers 16-byte aligned.  M == 0 is valid (zeroes dW unless accumulating).
+ */
+int rg_kgemm_mxfp8(const void* gq, const void* sg_blocked, const void* xq, const void* sx_blocked,
+                   const int32_t* offsets, int E, int64_t M, int N, int K, float* dW, int accumulate,
+                   cudaStream_t stream);
+
+/*
  * rg_mgemm_swiglu -- M-grouped forward gate-up GEMM with the SwiGLU
  * activation applied in the epilogue (the fused activation named in the
  * DeepGEMM issue discussion of wgrad utilities, "fused with SwiGLU"; the

@@ -30,7 +30,7 @@ import os
 
 from . import _build
 
-__all__ = ["load", "mgemm", "mgemm_nested", "mgemm_mxfp8", "mx_scales_blocked", "mx_blocked_bytes", "mgemm_swiglu", "mgemm_swiglu_dgrad", "kgemm", "device_status", "set_wait_timeout_ns",
+__all__ = ["load", "mgemm", "mgemm_nested", "mgemm_mxfp8", "mx_scales_blocked", "mx_blocked_bytes", "kgemm_mxfp8", "mx_scales_blocked_k", "mx_blocked_k_bytes", "mgemm_swiglu", "mgemm_swiglu_dgrad", "kgemm", "device_status", "set_wait_timeout_ns",
            "selftest_wait_timeout", "RGError", "lib_path", "version",
            "RG_DEV_BAD_OFFSETS", "RG_DEV_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -44,7 +44,7 @@ RG_DEV_LAUNCH_CONFIG = 0x4
 RG_MAX_EXPERTS = 1024
 RG_MAX_OUTER = 65536
 
-EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_nested", "rg_mgemm_mxfp8", "rg_mx_scales_blocked", "rg_mx_blocked_bytes", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_set_wait_timeout_ns",
+EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_nested", "rg_mgemm_mxfp8", "rg_mx_scales_blocked", "rg_mx_blocked_bytes", "rg_kgemm_mxfp8", "rg_mx_scales_blocked_k", "rg_mx_blocked_k_bytes", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_set_wait_timeout_ns",
                     "rg_selftest_wait_timeout", "rg_last_cuda_error", "rg_device_supported",
                     "rg_version")
 
@@ -88,6 +88,12 @@ def load() -> ctypes.CDLL:
     lib.rg_mx_scales_blocked.restype = i32
     lib.rg_mx_blocked_bytes.argtypes = [i64, i32, i32]
     lib.rg_mx_blocked_bytes.restype = i64
+    lib.rg_kgemm_mxfp8.argtypes = [vp, vp, vp, vp, vp, i32, i64, i32, i32, vp, i32, vp]
+    lib.rg_kgemm_mxfp8.restype = i32
+    lib.rg_mx_scales_blocked_k.argtypes = [vp, vp, i32, i64, i32, vp, i64, vp]
+    lib.rg_mx_scales_blocked_k.restype = i32
+    lib.rg_mx_blocked_k_bytes.argtypes = [i64, i32, i32]
+    lib.rg_mx_blocked_k_bytes.restype = i64
     lib.rg_mgemm_swiglu.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp, vp]
     lib.rg_mgemm_swiglu.restype = i32
     lib.rg_mgemm_swiglu_dgrad.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp, vp]
@@ -282,6 +288,76 @@ def mgemm_mxfp8(xq, sx_blocked, wq, sw_blocked, offsets, transpose_B: bool = Fal
                                 offsets.data_ptr(), E, M, N, K, int(bool(transpose_B)), out.data_ptr(),
                                 _stream_ptr(xq.device, stream))
     _check("rg_mgemm_mxfp8", rc)
+    return out
+
+
+def mx_blocked_k_bytes(R: int, KS: int, G: int) -> int:
+    """Bytes ``mx_scales_blocked_k`` may write for R rows of KS scales in G groups."""
+    n = load().rg_mx_blocked_k_bytes(int(R), int(KS), int(G))
+    if n < 0:
+        raise ValueError("bad arguments to rg_mx_blocked_k_bytes")
+    return int(n)
+
+
+def mx_scales_blocked_k(scales, offsets, out=None, stream=None):
+    """Blocked layout of E8M0 scales [R, KS] grouped along the contraction
+    by offsets (device int32 [G+1], multiples of 32); returns uint8
+    [mx_blocked_k_bytes(R, KS, G)]."""
+    import torch
+    _need(scales, "scales", torch.uint8, 2)
+    _need(offsets, "offsets", torch.int32, 1)
+    R, KS = scales.shape
+    G = offsets.shape[0] - 1
+    nbytes = mx_blocked_k_bytes(R, KS, G)
+    if out is None:
+        out = torch.empty((nbytes,), dtype=torch.uint8, device=scales.device)
+    else:
+        _need(out, "out", torch.uint8, 1)
+        if out.numel() < nbytes:
+            raise ValueError(f"out must hold at least {nbytes} bytes")
+    lib = load()
+    with torch.cuda.device(scales.device):
+        rc = lib.rg_mx_scales_blocked_k(scales.data_ptr(), offsets.data_ptr(), G, R, KS, out.data_ptr(),
+                                        out.numel(), _stream_ptr(scales.device, stream))
+    _check("rg_mx_scales_blocked_k", rc)
+    return out
+
+
+def kgemm_mxfp8(gq, sg_blocked, xq, sx_blocked, offsets, out=None, accumulate: bool = False, stream=None):
+    """MXFP8 K-grouped weight gradient.  gq uint8 [M,N], xq uint8 [M,K] (E4M3
+    codes), sg_blocked / sx_blocked: ``mx_scales_blocked_k`` of sg [N,M/32]
+    and sx [K,M/32] with ``offsets`` (int32 [E+1], multiples of 32).  Returns
+    dW [E,N,K] fp32, overwritten, or added to ``out`` with accumulate=True."""
+    import torch
+    _need(gq, "gq", torch.uint8, 2)
+    _need(xq, "xq", torch.uint8, 2)
+    _need(sg_blocked, "sg_blocked", torch.uint8, 1)
+    _need(sx_blocked, "sx_blocked", torch.uint8, 1)
+    _need(offsets, "offsets", torch.int32, 1)
+    M, N = gq.shape
+    if xq.shape[0] != M:
+        raise ValueError("gq and xq must have the same number of rows")
+    K = xq.shape[1]
+    E = offsets.shape[0] - 1
+    if M % 32:
+        raise ValueError("M must be a multiple of 32")
+    if M and (sg_blocked.numel() < mx_blocked_k_bytes(N, M // 32, E)
+              or sx_blocked.numel() < mx_blocked_k_bytes(K, M // 32, E)):
+        raise ValueError("blocked scale buffers are smaller than mx_blocked_k_bytes")
+    if out is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs the dW to add to as `out`")
+        out = torch.empty((E, N, K), dtype=torch.float32, device=gq.device)
+    else:
+        _need(out, "out", torch.float32, 3)
+        if tuple(out.shape) != (E, N, K):
+            raise ValueError(f"out must be [{E},{N},{K}]")
+    lib = load()
+    with torch.cuda.device(gq.device):
+        rc = lib.rg_kgemm_mxfp8(gq.data_ptr(), sg_blocked.data_ptr(), xq.data_ptr(), sx_blocked.data_ptr(),
+                                offsets.data_ptr(), E, M, N, K, out.data_ptr(), int(bool(accumulate)),
+                                _stream_ptr(gq.device, stream))
+    _check("rg_kgemm_mxfp8", rc)
     return out
 
 

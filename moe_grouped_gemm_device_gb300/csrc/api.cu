@@ -84,6 +84,7 @@ int device_state(DeviceState** out) {
       if ((e = rg::mgemm_setup(smem)) != cudaSuccess) return fail_cuda(e);
       if ((e = rg::kgemm_setup(smem)) != cudaSuccess) return fail_cuda(e);
       if ((e = rg::mx_setup(smem)) != cudaSuccess) return fail_cuda(e);
+      if ((e = rg::mxk_setup(smem)) != cudaSuccess) return fail_cuda(e);
       if (encode_fn() == nullptr) return fail_cuda(cudaErrorNotSupported);
       // One CTA per SM (shared memory limits residency to one); with CTA
       // pairs, as many 2-CTA clusters as can be resident at once.
@@ -410,7 +411,90 @@ int rg_mgemm_mxfp8(const void* xq, const void* sx_blocked, const void* wq, const
   a.out = y;
   a.status = ds->status;
   a.wait_limit_ns = g_wait_limit_ns.load();
+  a.accumulate = 0;
   const cudaError_t e = rg::launch_mx_mgemm(transpose_B != 0, tmA, tmB, tmY, a, ds->num_sms, stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return RG_OK;
+}
+
+int64_t rg_mx_blocked_k_bytes(int64_t R, int KS, int G) {
+  if (R < 1 || KS < 1 || G < 1) return -1;
+  return (R + 127) / 128 * (KS / 4 + G) * 512;
+}
+
+int rg_mx_scales_blocked_k(const uint8_t* scales, const int32_t* offsets, int G, int64_t R, int KS, uint8_t* out,
+                           int64_t out_bytes, cudaStream_t stream) {
+  if (offsets == nullptr || (reinterpret_cast<uintptr_t>(offsets) & 3u) != 0) return RG_ERR_INVALID_ARG;
+  if (G < 1 || G > RG_MAX_EXPERTS || R < 1 || R > INT32_MAX || KS < 1 || KS > INT32_MAX / 32)
+    return RG_ERR_INVALID_ARG;
+  if (scales == nullptr || out == nullptr || !aligned16(out) || out_bytes < rg_mx_blocked_k_bytes(R, KS, G))
+    return RG_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != RG_OK) return rc;
+  const cudaError_t e = rg::launch_mx_blocked_k(scales, offsets, G, static_cast<int>(R), KS, out, ds->status,
+                                                ds->num_sms, stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return RG_OK;
+}
+
+int rg_kgemm_mxfp8(const void* gq, const void* sg_blocked, const void* xq, const void* sx_blocked,
+                   const int32_t* offsets, int E, int64_t M, int N, int K, float* dW, int accumulate,
+                   cudaStream_t stream) {
+  if (offsets == nullptr || (reinterpret_cast<uintptr_t>(offsets) & 3u) != 0) return RG_ERR_INVALID_ARG;
+  if (E < 1 || E > RG_MAX_EXPERTS || M < 0 || M > INT32_MAX || M % 32 != 0) return RG_ERR_INVALID_ARG;
+  if (N < 16 || N % 16 != 0 || K < 16 || K % 16 != 0) return RG_ERR_INVALID_ARG;
+  if (dW == nullptr || !aligned16(dW)) return RG_ERR_INVALID_ARG;
+  if (M > 0 && (gq == nullptr || xq == nullptr || sg_blocked == nullptr || sx_blocked == nullptr ||
+                !aligned16(gq) || !aligned16(xq) || !aligned16(sg_blocked) || !aligned16(sx_blocked)))
+    return RG_ERR_INVALID_ARG;
+  const int64_t tiles = static_cast<int64_t>(E) * ((N + 127) / 128) * ((K + 255) / 256);
+  if (tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != RG_OK) return rc;
+  if (rg::mxk_smem_bytes(E) > ds->max_smem) return RG_ERR_INVALID_ARG;
+
+  // With M == 0 every valid offsets vector is all zeros: only zero tiles are
+  // written, and the operand maps describe one row of dW that is never read.
+  const void* g_ptr = M > 0 ? gq : static_cast<const void*>(dW);
+  const void* x_ptr = M > 0 ? xq : static_cast<const void*>(dW);
+  const uint64_t rows = M > 0 ? static_cast<uint64_t>(M) : 1;
+  CUtensorMap tmG, tmX, tmD;
+  {  // gq [M, N] bytes: 128 (n) x 128 (rows) boxes
+    const uint64_t dims[2] = {static_cast<uint64_t>(N), rows};
+    const uint64_t str[1] = {static_cast<uint64_t>(N)};
+    const uint32_t box[2] = {128, 128};
+    if (!encode_sw(&tmG, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g_ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return RG_ERR_INVALID_ARG;
+  }
+  {  // xq [M, K] bytes: 128 (k) x 128 (rows) boxes
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), rows};
+    const uint64_t str[1] = {static_cast<uint64_t>(K)};
+    const uint32_t box[2] = {128, 128};
+    if (!encode_sw(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, x_ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return RG_ERR_INVALID_ARG;
+  }
+  {  // dW [E, N, K] fp32: 16 (k) x 32 (n) boxes, 64-byte swizzle
+    const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
+    const uint64_t str[2] = {static_cast<uint64_t>(K) * 4, static_cast<uint64_t>(N) * K * 4};
+    const uint32_t box[3] = {16, 32, 1};
+    if (!encode_sw(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dW, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B))
+      return RG_ERR_INVALID_ARG;
+  }
+  rg::MxArgs a;
+  a.offsets = offsets;
+  a.sfa = static_cast<const uint8_t*>(sg_blocked);
+  a.sfb = static_cast<const uint8_t*>(sx_blocked);
+  a.E = E;
+  a.M = static_cast<int>(M);
+  a.N = N;
+  a.K = K;
+  a.out = dW;
+  a.status = ds->status;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.accumulate = accumulate != 0;
+  const cudaError_t e = rg::launch_mx_kgemm(tmG, tmX, tmD, a, ds->num_sms, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
 }

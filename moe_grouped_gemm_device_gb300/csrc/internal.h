@@ -31,9 +31,10 @@ struct MxArgs {
   const uint8_t* sfa;       // blocked E8M0 scales of A (rows grouped by offsets)
   const uint8_t* sfb;       // blocked E8M0 scales of B (E groups of N rows)
   int E, M, N, K;
-  void* out;                // y (bf16)
+  void* out;                // y (bf16), or dW (fp32) for the K-grouped GEMM
   unsigned int* status;
   unsigned long long wait_limit_ns;
+  int accumulate;           // K-grouped: 1 = dW += result, 0 = dW = result
 };
 
 // CTA group of the tensor-core MMAs: 2 (default) = a CTA pair computes one
@@ -105,6 +106,14 @@ cudaError_t launch_mx_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUte
                             const CUtensorMap& tmY, const MxArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_mx_blocked(const uint8_t* src, const int32_t* offsets, int G, int R, int KS, uint8_t* dst,
                               unsigned int* status, int num_sms, cudaStream_t stream);
+// MXFP8 Kgemm (FP8 operands quantized along the rows, experts on 32-row
+// boundaries) and the scale layout for groups along the contraction.
+size_t mxk_smem_bytes(int E);
+cudaError_t mxk_setup(int max_smem);
+cudaError_t launch_mx_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
+                            const MxArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_mx_blocked_k(const uint8_t* src, const int32_t* offsets, int G, int R, int KS, uint8_t* dst,
+                                unsigned int* status, int num_sms, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,
                                  cudaStream_t stream);
 

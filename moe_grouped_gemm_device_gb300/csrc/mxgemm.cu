@@ -401,6 +401,413 @@ __global__ void __launch_bounds__(256) mx_blocked_kernel(const uint8_t* __restri
   }
 }
 
+
+// Blocked scale layout for groups along the contraction: one warp per
+// 512-byte (row block, chunk) range.  Chunk q belongs to the group g whose
+// chunks start at s_qp[g] <= q; its scale columns are offsets[g]/32 +
+// 4*(q - s_qp[g]) .. +3, those at or past offsets[g+1]/32 are padding.
+__global__ void __launch_bounds__(256) mx_blocked_k_kernel(const uint8_t* __restrict__ src,
+                                                           const int32_t* __restrict__ offsets, int G, int R,
+                                                           int KS, uint8_t* __restrict__ dst,
+                                                           unsigned int* status) {
+  extern __shared__ int s_tab[];
+  int* s_off = s_tab;         // [G+1]
+  int* s_qp = s_tab + G + 1;  // [G+1] first chunk of each group
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i <= G; i += blockDim.x) s_off[i] = offsets[i];
+  __syncthreads();
+  int bad = 0;
+  for (int i = threadIdx.x; i < G; i += blockDim.x) bad |= (s_off[i + 1] < s_off[i]);
+  for (int i = threadIdx.x; i <= G; i += blockDim.x) bad |= (s_off[i] & 31) != 0;
+  if (threadIdx.x == 0) bad |= (s_off[0] != 0) | (static_cast<int64_t>(s_off[G]) > 32ll * KS);
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, kDevBadOffsets);
+    return;
+  }
+  if (warp == 0) {
+    const int per = (G + 31) / 32;
+    const int lo = min(G, lane * per), hi = min(G, lo + per);
+    int s = 0;
+    for (int g = lo; g < hi; ++g) s += (s_off[g + 1] - s_off[g] + 127) / 128;
+    int incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - s;
+    for (int g = lo; g < hi; ++g) {
+      s_qp[g] = run;
+      run += (s_off[g + 1] - s_off[g] + 127) / 128;
+    }
+    if (lane == 31) s_qp[G] = incl;
+  }
+  __syncthreads();
+  const int NQ = s_qp[G];
+  const int nrb = (R + 127) / 128;
+  const int64_t items = static_cast<int64_t>(nrb) * NQ;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t it = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp; it < items; it += nwarps) {
+    const int rb = static_cast<int>(it / NQ), q = static_cast<int>(it % NQ);
+    int lo = 0, hi = G;  // the group of chunk q: the last g with s_qp[g] <= q
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_qp[mid] <= q) lo = mid;
+      else hi = mid;
+    }
+    const int cb = s_off[lo] / 32 + 4 * (q - s_qp[lo]);
+    const int c1 = s_off[lo + 1] / 32;
+    uint32_t w[4];
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      const int r = 128 * rb + lane + 32 * qq;
+      uint32_t v = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int col = cb + j;
+        const uint32_t byte = (r < R && col < c1) ? src[static_cast<int64_t>(r) * KS + col] : 0x7Fu;
+        v |= byte << (8 * j);
+      }
+      w[qq] = v;
+    }
+    reinterpret_cast<uint4*>(dst + it * 512)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// ------------------------------------------------------------------ MX Kgemm
+//
+// dW[e] (fp32, [E, N, K]) = sum over the rows of expert e of
+// (gq * 2^sg)^T (xq * 2^sx): FP8 E4M3 operands quantized along the rows
+// (one E8M0 scale per column and 32-row block), every expert's row range a
+// whole number of 32-row blocks.  Tile = 128 dW rows (n) x 256 dW columns (k)
+// of one expert, tcgen05 M=128 N=256 with both operands MN-major.  A stage is
+// 128 rows of the expert: the MMAs of the 32-row steps that lie inside the
+// expert are issued, so no row of the next expert enters an accumulation and
+// nothing needs zeroing.  Scales come from the layout for groups along the
+// contraction.  Tiles are taken longest expert first; rows are summed in
+// tensor memory in chunks of at most CHUNK_ROWS, the first chunk's partial
+// stored (or reduce-added when accumulating into dW), later ones TMA
+// reduce-added in row order.  Empty experts get dW[e] = 0 (unchanged when
+// accumulating).
+struct MxkCfg {
+  static constexpr int BM = 128;  // dW rows per tile (MMA M)
+  static constexpr int BN = 256;  // dW columns per tile (MMA N)
+  static constexpr int BR = 128;  // expert rows per stage (4 scale blocks)
+  static constexpr int STAGES = 4;
+  static constexpr int A_BYTES = BM * BR;
+  static constexpr int B_BYTES = BN * BR;
+  static constexpr int AB_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SF_BYTES = 512 + 1024;
+  static constexpr int STAGE_BYTES = AB_BYTES + SF_BYTES;
+  static constexpr int CHUNK_STAGES = kg::CHUNK_ROWS / BR;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_BUF_BYTES = 32 * 64;  // 32 rows x 16 fp32 columns
+  static constexpr int THREADS = 32 * (2 + EPI_WARPS);
+  static constexpr int NUM_BARS = 2 * STAGES + 3;
+  static constexpr int SMEM_FIXED = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 + 16;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t SF_COL0 = 256;
+};
+static_assert(MxkCfg::AB_BYTES % 1024 == 0, "operand tiles must keep the 1024-byte swizzle alignment");
+static_assert(kg::CHUNK_ROWS % MxkCfg::BR == 0, "chunks must hold whole stages");
+
+__global__ void __launch_bounds__(MxkCfg::THREADS, 1)
+    mx_kgemm_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmX,
+                    const __grid_constant__ CUtensorMap tmD, const MxArgs args) {
+  using C = MxkCfg;
+  constexpr int BM = C::BM, BN = C::BN, BR = C::BR, STAGES = C::STAGES;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicOr(args.status, kDevLaunchConfig);
+    return;
+  }
+  uint8_t* epi = smem + STAGES * C::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_WARPS * C::EPI_BUF_BYTES);
+  int* misc = reinterpret_cast<int*>(bars + C::NUM_BARS);  // [0] tmem base, [1] abort
+  int* s_off = misc + 4;           // [E+1]
+  int* s_qp = s_off + (args.E + 1);  // [E+1] first scale chunk of each expert
+  int* s_ord = s_qp + (args.E + 1);  // [E] experts by decreasing rows
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES);
+  const uint32_t tempty_bar = bar0 + 8u * (2 * STAGES + 1);
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int E = args.E, N = args.N, K = args.K;
+  const int nbn = (N + BM - 1) / BM;
+  const int nbk = (K + BN - 1) / BN;
+  const int nrb_x = (K + 127) / 128;  // 128-row scale blocks of X's columns
+  const int tpe = nbn * nbk;
+  const int T = E * tpe;
+
+  // ---- offsets -> shared memory, validation, chunk prefix, order -----------
+  if (threadIdx.x == 0) misc[1] = 0;
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = args.offsets[i];
+  __syncthreads();
+  int bad = 0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) bad |= (s_off[i + 1] < s_off[i]);
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) bad |= (s_off[i] & 31) != 0;
+  if (threadIdx.x == 0) bad |= (s_off[0] != 0) | (s_off[E] > args.M);
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.status, kDevBadOffsets);
+    return;
+  }
+  if (static_cast<int>(blockIdx.x) >= T) return;
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int lo = min(E, lane * per), hi = min(E, lo + per);
+    int s = 0;
+    for (int e = lo; e < hi; ++e) s += (s_off[e + 1] - s_off[e] + BR - 1) / BR;
+    int incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - s;
+    for (int e = lo; e < hi; ++e) {
+      s_qp[e] = run;
+      run += (s_off[e + 1] - s_off[e] + BR - 1) / BR;
+    }
+    if (lane == 31) s_qp[E] = incl;
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int ce = s_off[e + 1] - s_off[e];
+    int rank_e = 0;
+    for (int f = 0; f < E; ++f) {
+      const int cf = s_off[f + 1] - s_off[f];
+      rank_e += (cf > ce) | ((cf == ce) & (f < e));
+    }
+    s_ord[rank_e] = e;
+  }
+  __syncthreads();
+  const int NQ = s_qp[E];
+
+  // ---- barriers and tensor memory -------------------------------------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, C::EPI_WARPS);
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc<1>(smem_u32(&misc[0]), C::TMEM_COLS);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = static_cast<uint32_t>(misc[0]);
+  const WaitGuard guard{args.status, args.wait_limit_ns, reinterpret_cast<volatile int*>(&misc[1])};
+  auto sa_of = [&](int s) { return sbase + s * C::AB_BYTES; };
+  auto sb_of = [&](int s) { return sa_of(s) + C::A_BYTES; };
+  auto sfa_of = [&](int s) { return sbase + STAGES * C::AB_BYTES + s * C::SF_BYTES; };
+  auto sfb_of = [&](int s) { return sfa_of(s) + 512; };
+  auto tile_at = [&](int t, int& e, int& nb, int& kb) {
+    const int pe = t / tpe, local = t - pe * tpe;
+    e = s_ord[pe];
+    nb = local / nbk;
+    kb = local - nb * nbk;
+  };
+
+  if (warp == 0) {
+    // ======================= producer (warp 0, lane 0) =======================
+    if (lane == 0) {
+      tma_prefetch_desc(&tmG);
+      tma_prefetch_desc(&tmX);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+        int e, nb, kb;
+        tile_at(t, e, nb, kb);
+        const int r_begin = s_off[e], r_end = s_off[e + 1];
+        const int n0 = nb * BM, k0 = kb * BN;
+        const int xb0 = 2 * kb, xb1 = min(2 * kb + 1, nrb_x - 1);  // past K: zero-filled rows, any scale
+        for (int r = r_begin, c = 0; r < r_end; r += BR, ++c) {
+          if (!mbar_wait(guard, empty_bar(stage), phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          tma_load_2d(sa_of(stage), &tmG, fb, n0, r);
+          tma_load_2d(sb_of(stage), &tmX, fb, k0, r);
+          tma_load_2d(sb_of(stage) + 16384, &tmX, fb, k0 + 128, r);
+          const int q = s_qp[e] + c;
+          bulk_load(sfa_of(stage), args.sfa + (static_cast<int64_t>(nb) * NQ + q) * 512, 512, fb);
+          bulk_load(sfb_of(stage), args.sfb + (static_cast<int64_t>(xb0) * NQ + q) * 512, 512, fb);
+          bulk_load(sfb_of(stage) + 512, args.sfb + (static_cast<int64_t>(xb1) * NQ + q) * 512, 512, fb);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u, guard.limit_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ============= scale copies and MMAs (warp 1, lane 0) =====================
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+      int e, nb, kb;
+      tile_at(t, e, nb, kb);
+      const int rows = s_off[e + 1] - s_off[e];
+      const int nst = (rows + BR - 1) / BR;
+      for (int c0 = 0; c0 < nst && ok; c0 += C::CHUNK_STAGES, ++acc) {
+        ok = __all_sync(0xffffffffu, mbar_wait(guard, tempty_bar, (acc & 1) ^ 1u));
+        if (!ok) break;
+        tc_fence_after();
+        const int c1 = min(nst, c0 + C::CHUNK_STAGES);
+        for (int c = c0; c < c1; ++c) {
+          ok = __all_sync(0xffffffffu, mbar_wait(guard, full_bar(stage), phase));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sfa_t = tmem + C::SF_COL0 + 16u * stage;
+            const uint32_t sfb_t = sfa_t + 4u;
+            tmem_cp_32x128b_x4(sfa_t, sdesc_plain16(sfa_of(stage)));
+            tmem_cp_32x128b_x4(sfb_t, sdesc_plain16(sfb_of(stage)));
+            tmem_cp_32x128b_x4(sfb_t + 4u, sdesc_plain16(sfb_of(stage) + 512));
+            const int ksteps = min(4, (rows - BR * c) / 32);  // 32-row steps inside the expert
+            const uint32_t sa = sa_of(stage), sb = sb_of(stage);
+            for (int k = 0; k < ksteps; ++k) {
+              const uint64_t ad = sdesc_sw128(sa + 4096 * k, 16384, 1024);
+              const uint64_t bd = sdesc_sw128(sb + 4096 * k, 16384, 1024);
+              umma_mxf8(tmem, ad, bd, idesc_mxf8_f32(BM, BN, true, true, k), sfa_t, sfb_t,
+                        (c != c0) | (k != 0));
+            }
+            umma_commit<1>(empty_bar(stage));
+          }
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) umma_commit<1>(tfull_bar);
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0) {
+      umma_commit<1>(drain_bar);
+      mbar_wait_drain(drain_bar, 0, guard.limit_ns);
+    }
+    __syncwarp();
+  } else {
+    // ======================= epilogue (warps 2..9) ===========================
+    // Warp w owns TMEM lane quarter q = w % 4 (dW rows n0 + 32q ..) and
+    // column half h (128 of the 256 columns): 8 boxes of 32 rows x 16 fp32.
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    uint8_t* ebuf = epi + (warp - 2) * C::EPI_BUF_BYTES;
+    const uint32_t ebuf_s = smem_u32(ebuf);
+    const int sw = (lane >> 1) & 3;  // 64-byte swizzle: 16-byte chunk ^= (row / 2) % 4
+    int acc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+      int e, nb, kb;
+      tile_at(t, e, nb, kb);
+      const int rows = s_off[e + 1] - s_off[e];
+      const int nst = (rows + BR - 1) / BR;
+      const int n0 = nb * BM + 32 * q;
+      const int kc0 = kb * BN + 128 * h;
+      const bool mine = n0 < N && kc0 < K;  // this warp's boxes hold valid dW elements
+      if (rows == 0) {  // no rows: dW[e] = 0 (left unchanged when accumulating)
+        if (!args.accumulate && mine) {
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          reinterpret_cast<uint4*>(ebuf)[lane] = make_uint4(0u, 0u, 0u, 0u);
+          reinterpret_cast<uint4*>(ebuf)[lane + 32] = make_uint4(0u, 0u, 0u, 0u);
+          reinterpret_cast<uint4*>(ebuf)[lane + 64] = make_uint4(0u, 0u, 0u, 0u);
+          reinterpret_cast<uint4*>(ebuf)[lane + 96] = make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            for (int b = 0; b < 8 && kc0 + 16 * b < K; ++b) tma_store_3d(&tmD, ebuf_s, kc0 + 16 * b, n0, e);
+            bulk_commit();
+          }
+        }
+        continue;
+      }
+      for (int c0 = 0; c0 < nst; c0 += C::CHUNK_STAGES, ++acc) {
+        if (!__all_sync(0xffffffffu, mbar_wait(guard, tfull_bar, acc & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v[128];
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + 128u * h;
+        tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld_32x32b_x32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+        tmem_ld_32x32b_x32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar);  // the accumulator is free again
+        if (!mine) continue;
+        const bool reduce = args.accumulate || c0 > 0;
+        // a later chunk is added onto the earlier chunk's writes: let them land first
+        if (lane == 0) {
+          if (c0 > 0) bulk_wait<0>();
+          else bulk_wait_read<0>();
+        }
+        __syncwarp();
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (kc0 + 16 * b >= K) break;
+          if (b > 0) {
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+          }
+          uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * 64);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            rowp[j ^ sw] = make_uint4(v[16 * b + 4 * j], v[16 * b + 4 * j + 1], v[16 * b + 4 * j + 2],
+                                      v[16 * b + 4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (reduce) tma_reduce_add_3d(&tmD, ebuf_s, kc0 + 16 * b, n0, e);
+            else tma_store_3d(&tmD, ebuf_s, kc0 + 16 * b, n0, e);
+            bulk_commit();
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  // ---- teardown --------------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<1>(tmem, C::TMEM_COLS);
+  }
+}
+
 }  // namespace
 
 size_t mx_smem_bytes(int E) { return MxCfg::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4; }
@@ -428,6 +835,32 @@ cudaError_t launch_mx_blocked(const uint8_t* src, const int32_t* offsets, int G,
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((items_ub + 7) / 8, 4 * num_sms)));
   const size_t smem = 2 * (static_cast<size_t>(G) + 1) * sizeof(int);
   mx_blocked_kernel<<<grid, 256, smem, stream>>>(src, offsets, G, R, KS, dst, status);
+  return cudaGetLastError();
+}
+
+}  // namespace rg
+
+namespace rg {
+
+size_t mxk_smem_bytes(int E) { return MxkCfg::SMEM_FIXED + 3 * (static_cast<size_t>(E) + 1) * 4; }
+
+cudaError_t mxk_setup(int max_smem) {
+  const int bytes = static_cast<int>(std::min<size_t>(mxk_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem));
+  return cudaFuncSetAttribute(mx_kgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+cudaError_t launch_mx_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
+                            const MxArgs& args, int grid, cudaStream_t stream) {
+  mx_kgemm_kernel<<<grid, MxkCfg::THREADS, mxk_smem_bytes(args.E), stream>>>(tmG, tmX, tmD, args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_blocked_k(const uint8_t* src, const int32_t* offsets, int G, int R, int KS, uint8_t* dst,
+                                unsigned int* status, int num_sms, cudaStream_t stream) {
+  const int64_t items_ub = (static_cast<int64_t>(R) + 127) / 128 * (KS / 4 + G);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((items_ub + 7) / 8, 4 * num_sms)));
+  const size_t smem = 2 * (static_cast<size_t>(G) + 1) * sizeof(int);
+  mx_blocked_k_kernel<<<grid, 256, smem, stream>>>(src, offsets, G, R, KS, dst, status);
   return cudaGetLastError();
 }
 

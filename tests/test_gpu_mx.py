@@ -177,3 +177,116 @@ def test_mx_bad_arguments(gpu_lib):
     assert lib.rg_mx_blocked_bytes(100, 0, 1) == -1
     torch.cuda.synchronize()
     assert gpu_lib.device_status() == 0
+
+
+# ------------------------------------------------ K-grouped MXFP8 (weight gradient)
+
+
+@pytest.mark.parametrize("off,R,KS", [([0, 96, 96, 320], 130, 10), ([0, 4096], 256, 128), ([0, 0, 0], 8, 3),
+                                      ([0, 32, 64, 1024, 1056], 300, 33)],
+                         ids=["ragged", "one_group", "all_empty", "mixed"])
+def test_mx_blocked_k_bit_exact(gpu_lib, off, R, KS):
+    import torch
+    off = np.array(off, dtype=np.int32)
+    G = len(off) - 1
+    src = W.e8m0_codes((R, KS), 0, 254, 52, G)
+    want = oracle.mx_blocked_k(src, off)
+    nq = sum((int(off[g + 1]) - int(off[g]) + 127) // 128 for g in range(G))
+    used = ((R + 127) // 128) * nq * 512
+    out = torch.full((gpu_lib.mx_blocked_k_bytes(R, KS, G),), 0xEE, dtype=torch.uint8, device="cuda")
+    gpu_lib.mx_scales_blocked_k(u8_dev(src), offsets_dev(off), out=out)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    got = out.cpu().numpy()
+    np.testing.assert_array_equal(got[:used], want[:used])
+    assert (got[used:] == 0xEE).all()
+
+
+def test_mx_blocked_k_unaligned_offsets_flagged(gpu_lib):
+    import torch
+    out = torch.full((gpu_lib.mx_blocked_k_bytes(64, 4, 2),), 0xEE, dtype=torch.uint8, device="cuda")
+    gpu_lib.mx_scales_blocked_k(u8_dev(np.zeros((64, 4), np.uint8)), offsets_dev(np.array([0, 40, 96], np.int32)),
+                                out=out)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == gpu_lib.RG_DEV_BAD_OFFSETS
+    assert bool((out == 0xEE).all())
+
+
+def run_mxk(rg, gq, sg, xq, sx, off, init=None):
+    import torch
+    E = len(off) - 1
+    M, N = gq.shape
+    K = xq.shape[1]
+    doff = offsets_dev(off)
+    sgb = rg.mx_scales_blocked_k(u8_dev(sg), doff)
+    sxb = rg.mx_scales_blocked_k(u8_dev(sx), doff)
+    if init is None:
+        dW = torch.full((E, N, K), float("nan"), dtype=torch.float32, device="cuda")
+        rg.kgemm_mxfp8(u8_dev(gq), sgb, u8_dev(xq), sxb, doff, out=dW)
+    else:
+        dW = torch.from_numpy(init.copy()).cuda()
+        rg.kgemm_mxfp8(u8_dev(gq), sgb, u8_dev(xq), sxb, doff, out=dW, accumulate=True)
+    torch.cuda.synchronize()
+    assert rg.device_status() == 0
+    return dW.cpu().numpy()
+
+
+def test_mx_kgemm_integer_inputs_bit_exact(gpu_lib):
+    """Integer codes and scales 1/2..2 make every fp32 partial sum exact, so
+    dW must equal the exact result; the 4160-row expert spans two
+    accumulation chunks, N and K end inside a tile."""
+    counts = [128, 0, 32, 4160, 96]
+    off = W.offsets_from_counts(counts)
+    M, N, K = int(off[-1]) + 64, 272, 320
+    gq, xq = int_codes((M, N), 62, 0), int_codes((M, K), 62, 1)
+    sg = W.e8m0_codes((N, M // 32), 126, 128, 62, 2)
+    sx = W.e8m0_codes((K, M // 32), 126, 128, 62, 3)
+    dW = run_mxk(gpu_lib, gq, sg, xq, sx, off)
+    ref = oracle.kgemm_mx(gq, sg, xq, sx, off)
+    np.testing.assert_array_equal(dW.astype(np.float64), ref)
+    assert (dW[1] == 0).all()
+
+
+def mxk_random(seed, counts, N, K, extra=32):
+    off = W.offsets_from_counts(counts)
+    M = int(off[-1]) + extra
+    gq, xq = W.e4m3_codes((M, N), seed, 0), W.e4m3_codes((M, K), seed, 1)
+    sg = W.e8m0_codes((N, M // 32), *W.MX_ACT_SCALES, seed, 2)
+    sx = W.e8m0_codes((K, M // 32), *W.MX_ACT_SCALES, seed, 3)
+    return off, gq, sg, xq, sx
+
+
+@pytest.mark.parametrize("counts,N,K", [([320, 0, 96, 1024, 32], 384, 512), ([64] * 6, 256, 256),
+                                        ([2048, 0], 128, 1024), ([32], 16, 16)],
+                         ids=["mixed", "six_equal", "one_long", "min_16"])
+def test_mx_kgemm_random_codes(gpu_lib, counts, N, K):
+    from parity import check_fp32
+    off, gq, sg, xq, sx = mxk_random(zlib.crc32(f"mxk/{counts}/{N}/{K}".encode()), counts, N, K)
+    dW = run_mxk(gpu_lib, gq, sg, xq, sx, off)
+    ref = oracle.kgemm_mx(gq, sg, xq, sx, off)
+    check_fp32(dW, ref, f"mxfp8 wgrad counts={counts} N={N} K={K}")
+    for e in np.flatnonzero(np.array(counts) == 0):
+        assert (dW[e] == 0).all()
+
+
+def test_mx_kgemm_accumulate(gpu_lib):
+    from parity import check_fp32
+    off, gq, sg, xq, sx = mxk_random(81, [320, 0, 96, 4224], 256, 384)
+    E = len(off) - 1
+    init = W.bf16_bits_to_f32(W.normal_bf16((E, 256, 384), 1.0, 81, 9))  # the gradient to add to
+    dW = run_mxk(gpu_lib, gq, sg, xq, sx, off, init=init)
+    ref = oracle.kgemm_mx(gq, sg, xq, sx, off) + init.astype(np.float64)
+    check_fp32(dW, ref, "mxfp8 wgrad accumulate")
+    assert (dW[1] == init[1]).all(), "an expert without rows changed dW when accumulating"
+
+
+def test_mx_kgemm_no_rows_zeroes(gpu_lib):
+    import torch
+    dW = torch.full((3, 64, 64), 5.0, dtype=torch.float32, device="cuda")
+    z = torch.zeros((32, 64), dtype=torch.uint8, device="cuda")
+    d = offsets_dev(np.zeros(4, np.int32))
+    sb = gpu_lib.mx_scales_blocked_k(torch.zeros((64, 1), dtype=torch.uint8, device="cuda"), d)
+    gpu_lib.kgemm_mxfp8(z, sb, z, sb, d, out=dW)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    assert bool((dW == 0).all())

@@ -60,7 +60,8 @@ def sample_pairs(counts, N, rng):
     return np.array(es, dtype=np.int32), np.array(ns, dtype=np.int32)
 
 
-MX = [("a3b_mxfp8", op) for op in ("mx_fwd_gate_up", "mx_fwd_down", "mx_dgrad_down", "mx_dgrad_gate_up")]
+MX = [("a3b_mxfp8", op) for op in ("mx_fwd_gate_up", "mx_fwd_down", "mx_dgrad_down", "mx_dgrad_gate_up",
+                                    "mx_wgrad_gw2", "mx_wgrad_gw13")]
 
 
 def dev_u8(wl, name):
@@ -90,6 +91,17 @@ def test_full_size_sampled_mxfp8(gpu_lib, wname, opname):
     rng = np.random.default_rng(zlib.crc32(f"{wname}/{opname}".encode()))
     doff = offsets_dev(off)
     sa, sb = dev_u8(wl, op.sa), dev_u8(wl, op.sb)
+    if op.kind == "mxk":
+        dW = gpu_lib.kgemm_mxfp8(dev_u8(wl, op.a), gpu_lib.mx_scales_blocked_k(sa, doff), dev_u8(wl, op.b),
+                                 gpu_lib.mx_scales_blocked_k(sb, doff), doff)
+        torch.cuda.synchronize()
+        assert gpu_lib.device_status() == 0
+        es, ns = sample_pairs(wl.counts, op.N, rng)
+        got = dW[torch.from_numpy(es).long().cuda(), torch.from_numpy(ns).long().cuda()].cpu().numpy()
+        ref = oracle.kgemm_mx(host_u8(wl, op.a), host_u8(wl, op.sa), host_u8(wl, op.b), host_u8(wl, op.sb), off,
+                              sel=(es, ns))
+        check_fp32(got, ref, f"{wname}/{opname}")
+        return
     sab = gpu_lib.mx_scales_blocked(sa, doff)
     sbb = gpu_lib.mx_scales_blocked(sb.view(-1, sb.shape[-1]), gpu_lib.mx_weight_offsets(wl.E, op.N))
     y = gpu_lib.mgemm_mxfp8(dev_u8(wl, op.a), sab, dev_u8(wl, op.b), sbb, doff, transpose_B=op.transpose_B)

@@ -244,7 +244,8 @@ class Op:
     # [O, L, N, K], output [M, O*N])
     outer: int = 1
     # kind 'mx': MXFP8 Mgemm; a, b are E4M3 code tensors, sa [M, K/32] and sb
-    # [E, N, K/32] their E8M0 scale tensors
+    # [E, N, K/32] their E8M0 scale tensors.  kind 'mxk': MXFP8 Kgemm; a =
+    # grad [M, N], b = X [M, K] E4M3 codes, sa [N, M/32] and sb [K, M/32]
     sa: str = ""
     sb: str = ""
 
@@ -376,15 +377,18 @@ def skewed(tail: bool = False) -> Workload:
 
 
 def a3b_mxfp8() -> Workload:
-    """The 30B-A3B expert layer's M-grouped GEMMs (forward and input
-    gradient) in MXFP8: E4M3 operands with one E8M0 scale per 32 elements
-    along each contraction, same counts (seed 3, Dirichlet(2), 32 experts,
-    M = 32768).  The weights carry one scale tensor per direction (row-wise
+    """The 30B-A3B expert layer's six grouped GEMMs in MXFP8: E4M3 operands
+    with one E8M0 scale per 32 elements along each contraction (seed 3,
+    Dirichlet(2) shares over 32 experts, M = 32768, every expert a whole
+    number of 32-row blocks so that the weight gradient's row-wise scale
+    blocks never straddle two experts).  The weights carry one scale tensor per direction (row-wise
     for the forward, column-wise for the input gradient), as a training step
     that quantizes each weight once per GEMM direction would hold.  Codes and
     scales are random draws; scales put activations at RMS ~1 and weights at
     RMS ~1/sqrt(K), like the bf16 layer."""
-    c = counts_dirichlet(32, 32768, 2.0, 3)
+    # expert row counts in whole 32-row scale blocks: Dirichlet(2) shares of
+    # the 1024 blocks of 32 rows
+    c = counts_dirichlet(32, 1024, 2.0, 3) * 32
     E, M, dm, d2, d1 = 32, 32768, 3072, 2560, 1280
     act = ("e8m0",) + MX_ACT_SCALES
 
@@ -401,12 +405,17 @@ def a3b_mxfp8() -> Workload:
         "sw2t": ((E, d1, dm // 32), wsc(dm), 31),
         "dy13q": ((M, d2), "e4m3", 32), "sdy13": ((M, d2 // 32), act, 33),
         "sw13t": ((E, dm, d2 // 32), wsc(d2), 34),
+        # column-wise scales (one per column and 32-row block) for the wgrad
+        "sdy2c": ((dm, M // 32), act, 35), "shc": ((d1, M // 32), act, 36),
+        "sdy13c": ((d2, M // 32), act, 37), "sxc": ((dm, M // 32), act, 38),
     }
     w.ops = [
         Op("mx_fwd_gate_up", "mx", "xq", "w13q", N=d2, K=dm, sa="sx", sb="sw13"),
         Op("mx_fwd_down", "mx", "hq", "w2q", N=dm, K=d1, sa="sh", sb="sw2"),
         Op("mx_dgrad_down", "mx", "dy2q", "w2q", N=d1, K=dm, transpose_B=True, sa="sdy2", sb="sw2t"),
         Op("mx_dgrad_gate_up", "mx", "dy13q", "w13q", N=dm, K=d2, transpose_B=True, sa="sdy13", sb="sw13t"),
+        Op("mx_wgrad_gw2", "mxk", "dy2q", "hq", N=dm, K=d1, sa="sdy2c", sb="shc"),
+        Op("mx_wgrad_gw13", "mxk", "dy13q", "xq", N=d2, K=dm, sa="sdy13c", sb="sxc"),
     ]
     return w
 
