@@ -432,7 +432,7 @@ def main():
     d = {k: as_torch(v).to(dev) for k, v in host.items()}
     off = torch.from_numpy(off_np).to(dev)
     outs, scratch = {}, {}
-    is_mx = any(op.kind == "mx" for op in wl.ops)
+    is_mx = any(op.kind in ("mx", "mxk") for op in wl.ops)
     for op in wl.ops:
         if op.kind in ("kgemm", "mxk"):
             outs[op.name] = torch.empty((wl.E, op.N, op.K), dtype=torch.float32, device=dev)
