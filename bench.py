@@ -431,33 +431,39 @@ def main():
 
     d = {k: as_torch(v).to(dev) for k, v in host.items()}
     off = torch.from_numpy(off_np).to(dev)
-    outs, scratch = {}, {}
     is_mx = any(op.kind in ("mx", "mxk") for op in wl.ops)
-    for op in wl.ops:
-        if op.kind in ("kgemm", "mxk"):
-            outs[op.name] = torch.empty((wl.E, op.N, op.K), dtype=torch.float32, device=dev)
-        elif op.kind == "nested":
-            outs[op.name] = torch.empty((wl.M, op.outer * op.N), dtype=torch.bfloat16, device=dev)
-        elif op.fuse == "swiglu":
-            outs[op.name] = torch.empty((wl.M, op.N // 2), dtype=torch.bfloat16, device=dev)
-            outs[op.name + ":y13"] = torch.empty((wl.M, op.N), dtype=torch.bfloat16, device=dev)
-        elif op.fuse == "swiglu_bwd":
-            outs[op.name] = torch.empty((wl.M, 2 * op.N), dtype=torch.bfloat16, device=dev)
-        else:
-            outs[op.name] = torch.empty((wl.M, op.N), dtype=torch.bfloat16, device=dev)
-        if op.kind == "mx":
-            KS = op.K // 32
-            scratch[op.name + ":sa"] = torch.empty((rg.mx_blocked_bytes(wl.M, KS, wl.E),), dtype=torch.uint8,
-                                                   device=dev)
-            scratch[op.name + ":sb"] = torch.empty((rg.mx_blocked_bytes(wl.E * op.N, KS, wl.E),),
-                                                   dtype=torch.uint8, device=dev)
-            scratch["woff:" + str(op.N)] = rg.mx_weight_offsets(wl.E, op.N, device=dev)
-        if op.kind == "mxk":
-            MS = wl.M // 32
-            scratch[op.name + ":sa"] = torch.empty((rg.mx_blocked_k_bytes(op.N, MS, wl.E),), dtype=torch.uint8,
-                                                   device=dev)
-            scratch[op.name + ":sb"] = torch.empty((rg.mx_blocked_k_bytes(op.K, MS, wl.E),), dtype=torch.uint8,
-                                                   device=dev)
+
+    def make_buffers():
+        """Output tensors of every op and the scale-layout buffers (MXFP8)."""
+        outs, scratch = {}, {}
+        for op in wl.ops:
+            if op.kind in ("kgemm", "mxk"):
+                outs[op.name] = torch.empty((wl.E, op.N, op.K), dtype=torch.float32, device=dev)
+            elif op.kind == "nested":
+                outs[op.name] = torch.empty((wl.M, op.outer * op.N), dtype=torch.bfloat16, device=dev)
+            elif op.fuse == "swiglu":
+                outs[op.name] = torch.empty((wl.M, op.N // 2), dtype=torch.bfloat16, device=dev)
+                outs[op.name + ":y13"] = torch.empty((wl.M, op.N), dtype=torch.bfloat16, device=dev)
+            elif op.fuse == "swiglu_bwd":
+                outs[op.name] = torch.empty((wl.M, 2 * op.N), dtype=torch.bfloat16, device=dev)
+            else:
+                outs[op.name] = torch.empty((wl.M, op.N), dtype=torch.bfloat16, device=dev)
+            if op.kind == "mx":
+                KS = op.K // 32
+                scratch[op.name + ":sa"] = torch.empty((rg.mx_blocked_bytes(wl.M, KS, wl.E),), dtype=torch.uint8,
+                                                       device=dev)
+                scratch[op.name + ":sb"] = torch.empty((rg.mx_blocked_bytes(wl.E * op.N, KS, wl.E),),
+                                                       dtype=torch.uint8, device=dev)
+                scratch["woff:" + str(op.N)] = rg.mx_weight_offsets(wl.E, op.N, device=dev)
+            if op.kind == "mxk":
+                MS = wl.M // 32
+                scratch[op.name + ":sa"] = torch.empty((rg.mx_blocked_k_bytes(op.N, MS, wl.E),),
+                                                       dtype=torch.uint8, device=dev)
+                scratch[op.name + ":sb"] = torch.empty((rg.mx_blocked_k_bytes(op.K, MS, wl.E),),
+                                                       dtype=torch.uint8, device=dev)
+        return outs, scratch
+
+    outs, scratch = make_buffers()
     stream = torch.cuda.current_stream(dev)
     off_used = [off]
     units = build_units(wl, rg, d, outs, off_used, scratch)
@@ -511,35 +517,67 @@ def main():
     value = world * flops_step / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers ---------------
+    # Every step copies its inputs from pinned host memory, runs the ops and
+    # copies every output back.  Consecutive steps are pipelined over two
+    # device buffer sets: step i's host->device copies (one stream) overlap
+    # step i-1's kernels (the compute stream) and step i-2's device->host
+    # copies (a third stream); events order each buffer set's reuse.
     e2e = None
     if rank == 0 and args.e2e_steps > 0:
         pin = {k: as_torch(v).pin_memory() for k, v in host.items()}
         pin_off = torch.from_numpy(off_np).pin_memory()
-        pin_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
         h2d = sum(t.numel() * t.element_size() for t in pin.values()) + pin_off.numel() * 4
-        d2h = sum(t.numel() * t.element_size() for t in pin_out.values())
+        d1 = {k: torch.empty_like(v) for k, v in d.items()}
+        off1 = [torch.empty_like(off)]
+        outs1, scratch1 = make_buffers()
+        sets = [(d, off_used, outs, units), (d1, off1, outs1, build_units(wl, rg, d1, outs1, off1, scratch1))]
+        pin_out = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in o.items()} for _, _, o, _ in sets]
+        d2h = sum(t.numel() * t.element_size() for t in pin_out[0].values())
+        s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = [{n: torch.cuda.Event() for n in ("h2d", "comp", "d2h")} for _ in sets]
+        started = [False, False]
 
-        def e2e_step():
-            for k, t in pin.items():
-                d[k].copy_(t, non_blocking=True)
-            off_used[0].copy_(pin_off, non_blocking=True)
-            for u in units:
+        def e2e_step(i):
+            b = i & 1
+            dd, oo, outs_b, units_b = sets[b]
+            e = ev[b]
+            with torch.cuda.stream(s_h2d):
+                if started[b]:
+                    s_h2d.wait_event(e["comp"])  # step i-2's kernels are done with this input set
+                for k, t in pin.items():
+                    dd[k].copy_(t, non_blocking=True)
+                oo[0].copy_(pin_off, non_blocking=True)
+                e["h2d"].record(s_h2d)
+            stream.wait_event(e["h2d"])
+            if started[b]:
+                stream.wait_event(e["d2h"])  # step i-2's outputs have left this set
+            for u in units_b:
                 u.call()
-            for k, t in outs.items():
-                pin_out[k].copy_(t, non_blocking=True)
+            e["comp"].record(stream)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(e["comp"])
+                for k, t in outs_b.items():
+                    pin_out[b][k].copy_(t, non_blocking=True)
+                e["d2h"].record(s_d2h)
+            started[b] = True
 
-        e2e_step()
+        for i in range(2):  # warm both buffer sets
+            e2e_step(i)
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
+        a.record(s_h2d)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        stream.wait_stream(s_d2h)
         b.record(stream)
         torch.cuda.synchronize()
         e_ms = a.elapsed_time(b) / args.e2e_steps
         e2e = {"value": flops_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e_ms}
+               "ms_per_step": e_ms, "pipelined": "h2d / kernels / d2h of consecutive steps on three streams"}
+        status = rg.device_status()
+        if status:
+            raise SystemExit(f"device status {status:#x} after the end-to-end steps")
 
     if rank != 0:
         if dist:

@@ -475,12 +475,12 @@ int rg_kgemm_mxfp8(const void* gq, const void* sg_blocked, const void* xq, const
     if (!encode_sw(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, x_ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return RG_ERR_INVALID_ARG;
   }
-  {  // dW [E, N, K] fp32: 16 (k) x 32 (n) boxes, 64-byte swizzle
+  {  // dW [E, N, K] fp32: BOX_COLS (k) x 32 (n) boxes, one swizzle row per box row
     const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
     const uint64_t str[2] = {static_cast<uint64_t>(K) * 4, static_cast<uint64_t>(N) * K * 4};
-    const uint32_t box[3] = {16, 32, 1};
-    if (!encode_sw(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dW, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B))
-      return RG_ERR_INVALID_ARG;
+    const uint32_t box[3] = {static_cast<uint32_t>(rg::mxk::BOX_COLS), 32, 1};
+    const CUtensorMapSwizzle sw = rg::mxk::BOX_COLS == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!encode_sw(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dW, dims, str, box, sw)) return RG_ERR_INVALID_ARG;
   }
   rg::MxArgs a;
   a.offsets = offsets;

@@ -24,7 +24,8 @@
 //   * One stage = 128 K elements: A 128x128 B (16 KB), B 256x128 B (32 KB,
 //     K-major; or two 128x128 MN-major boxes for transpose_B), the A scale
 //     block (512 B) and the two B scale blocks (1 KB) -- four stages.
-//   * Warp 0 lane 0: TMA loads and bulk copies of the scale blocks.  Warp 1:
+//   * Lane 0 of warps 0 and 10: TMA loads and bulk copies of the scale
+//     blocks, alternate stages (one thread cannot issue copies fast enough).  Warp 1:
 //     tensor memory; its lane 0 copies each stage's scales into a per-stage
 //     slot of tensor memory (tcgen05.cp) and issues the four MMAs of the
 //     stage, scale byte k of each 32-bit scale word for MMA k.  Warps 2..9:
@@ -60,7 +61,9 @@ struct MxCfg {
   static constexpr int STAGE_BYTES = AB_BYTES + SF_BYTES;  // bytes one stage's copies deliver
   static constexpr int EPI_WARPS = 8;
   static constexpr int EPI_BUF_BYTES = 32 * 64;  // 32 rows x 32 bf16 columns
-  static constexpr int THREADS = 32 * (2 + EPI_WARPS);
+  // warps 0 and 10: producers (alternate stages), 1: MMA, 2..9: epilogue
+  static constexpr int PRODUCER2 = 2 + EPI_WARPS;
+  static constexpr int THREADS = 32 * (PRODUCER2 + 1);
   // full[S], empty[S], tfull, tempty, drain
   static constexpr int NUM_BARS = 2 * STAGES + 3;
   // [operand tiles of every stage][scale blocks of every stage][epilogue buffers][barriers][misc]
@@ -161,11 +164,15 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
   auto sfa_of = [&](int s) { return sbase + STAGES * C::AB_BYTES + s * C::SF_BYTES; };
   auto sfb_of = [&](int s) { return sfa_of(s) + C::SFA_BYTES; };
 
-  if (warp == 0) {
-    // ======================= producer (warp 0, lane 0) =======================
+  if (warp == 0 || warp == C::PRODUCER2) {
+    // ================ producers (lane 0 of warps 0 and 10) ===================
+    // Two threads take turns: each walks the whole (tile, k-chunk) sequence
+    // and fills every other stage, doubling the rate at which copies issue.
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      const uint32_t pid = warp == 0 ? 0u : 1u;
+      uint32_t it = 0;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;
@@ -184,6 +191,13 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
         const int blk_b0 = e * nb_w + 2 * nt;
         const int blk_b1 = e * nb_w + min(2 * nt + 1, nb_w - 1);
         for (int kc = 0; kc < nkc; ++kc) {
+          if ((it++ & 1u) != pid) {  // the other producer's stage
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (!mbar_wait(guard, empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
@@ -493,7 +507,7 @@ struct MxkCfg {
   static constexpr int BM = 128;  // dW rows per tile (MMA M)
   static constexpr int BN = 256;  // dW columns per tile (MMA N)
   static constexpr int BR = 128;  // expert rows per stage (4 scale blocks)
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = mxk::STAGES;
   static constexpr int A_BYTES = BM * BR;
   static constexpr int B_BYTES = BN * BR;
   static constexpr int AB_BYTES = A_BYTES + B_BYTES;
@@ -501,14 +515,22 @@ struct MxkCfg {
   static constexpr int STAGE_BYTES = AB_BYTES + SF_BYTES;
   static constexpr int CHUNK_STAGES = kg::CHUNK_ROWS / BR;
   static constexpr int EPI_WARPS = 8;
-  static constexpr int EPI_BUF_BYTES = 32 * 64;  // 32 rows x 16 fp32 columns
-  static constexpr int THREADS = 32 * (2 + EPI_WARPS);
+  static constexpr int BOX_COLS = mxk::BOX_COLS;
+  static constexpr int EPI_BUF_BYTES = 32 * BOX_COLS * 4;  // 32 rows x BOX_COLS fp32 (one TMA box)
+  static constexpr int EPI_BUFS = mxk::EPI_BUFS;          // per epilogue warp
+  // warps 0 and 10: producers (alternate stages), 1: MMA, 2..9: epilogue
+  static constexpr int PRODUCER2 = 2 + EPI_WARPS;
+  static constexpr int THREADS = 32 * (PRODUCER2 + 1);
   static constexpr int NUM_BARS = 2 * STAGES + 3;
-  static constexpr int SMEM_FIXED = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 + 16;
+  static constexpr int SMEM_FIXED =
+      STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES + NUM_BARS * 8 + 16;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SF_COL0 = 256;
 };
-static_assert(MxkCfg::AB_BYTES % 1024 == 0, "operand tiles must keep the 1024-byte swizzle alignment");
+static_assert(MxkCfg::AB_BYTES % 1024 == 0 && MxkCfg::EPI_BUF_BYTES % (MxkCfg::BOX_COLS * 32) == 0,
+              "operand tiles and epilogue boxes must keep their swizzle alignment");
+static_assert(MxkCfg::SMEM_FIXED + 3 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448,
+              "MXFP8 wgrad configuration exceeds the shared memory of a CTA");
 static_assert(kg::CHUNK_ROWS % MxkCfg::BR == 0, "chunks must hold whole stages");
 
 __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
@@ -522,8 +544,11 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
     if (threadIdx.x == 0) atomicOr(args.status, kDevLaunchConfig);
     return;
   }
-  uint8_t* epi = smem + STAGES * C::STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_WARPS * C::EPI_BUF_BYTES);
+  // [operand tiles of every stage][epilogue buffers][scale blocks][barriers][misc]
+  // (the 128-byte-swizzled epilogue boxes need 1024-byte alignment)
+  uint8_t* epi = smem + STAGES * C::AB_BYTES;
+  uint8_t* sf_area = epi + C::EPI_WARPS * C::EPI_BUFS * C::EPI_BUF_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_area + STAGES * C::SF_BYTES);
   int* misc = reinterpret_cast<int*>(bars + C::NUM_BARS);  // [0] tmem base, [1] abort
   int* s_off = misc + 4;           // [E+1]
   int* s_qp = s_off + (args.E + 1);  // [E+1] first scale chunk of each expert
@@ -610,7 +635,8 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
   const WaitGuard guard{args.status, args.wait_limit_ns, reinterpret_cast<volatile int*>(&misc[1])};
   auto sa_of = [&](int s) { return sbase + s * C::AB_BYTES; };
   auto sb_of = [&](int s) { return sa_of(s) + C::A_BYTES; };
-  auto sfa_of = [&](int s) { return sbase + STAGES * C::AB_BYTES + s * C::SF_BYTES; };
+  const uint32_t sf_base = smem_u32(sf_area);
+  auto sfa_of = [&](int s) { return sf_base + s * C::SF_BYTES; };
   auto sfb_of = [&](int s) { return sfa_of(s) + 512; };
   auto tile_at = [&](int t, int& e, int& nb, int& kb) {
     const int pe = t / tpe, local = t - pe * tpe;
@@ -619,11 +645,13 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
     kb = local - nb * nbk;
   };
 
-  if (warp == 0) {
-    // ======================= producer (warp 0, lane 0) =======================
+  if (warp == 0 || warp == C::PRODUCER2) {
+    // ======== producers (lane 0 of warps 0 and 10, alternate stages) =========
     if (lane == 0) {
       tma_prefetch_desc(&tmG);
       tma_prefetch_desc(&tmX);
+      const uint32_t pid = warp == 0 ? 0u : 1u;
+      uint32_t it = 0;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;
@@ -635,6 +663,13 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
         const int n0 = nb * BM, k0 = kb * BN;
         const int xb0 = 2 * kb, xb1 = min(2 * kb + 1, nrb_x - 1);  // past K: zero-filled rows, any scale
         for (int r = r_begin, c = 0; r < r_end; r += BR, ++c) {
+          if ((it++ & 1u) != pid) {  // the other producer's stage
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (!mbar_wait(guard, empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
@@ -716,12 +751,13 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
   } else {
     // ======================= epilogue (warps 2..9) ===========================
     // Warp w owns TMEM lane quarter q = w % 4 (dW rows n0 + 32q ..) and
-    // column half h (128 of the 256 columns): 8 boxes of 32 rows x 16 fp32.
+    // column half h (128 of the 256 columns), stored as boxes of 32 rows x
+    // BOX_COLS fp32 through EPI_BUFS staging buffers (with two, one box is
+    // written while the previous one is still being read by the TMA unit).
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
-    uint8_t* ebuf = epi + (warp - 2) * C::EPI_BUF_BYTES;
+    uint8_t* ebuf = epi + (warp - 2) * C::EPI_BUFS * C::EPI_BUF_BYTES;
     const uint32_t ebuf_s = smem_u32(ebuf);
-    const int sw = (lane >> 1) & 3;  // 64-byte swizzle: 16-byte chunk ^= (row / 2) % 4
     int acc = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
@@ -736,14 +772,14 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
         if (!args.accumulate && mine) {
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
-          reinterpret_cast<uint4*>(ebuf)[lane] = make_uint4(0u, 0u, 0u, 0u);
-          reinterpret_cast<uint4*>(ebuf)[lane + 32] = make_uint4(0u, 0u, 0u, 0u);
-          reinterpret_cast<uint4*>(ebuf)[lane + 64] = make_uint4(0u, 0u, 0u, 0u);
-          reinterpret_cast<uint4*>(ebuf)[lane + 96] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int u = 0; u < C::EPI_BUF_BYTES / 512; ++u)
+            reinterpret_cast<uint4*>(ebuf)[lane + 32 * u] = make_uint4(0u, 0u, 0u, 0u);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            for (int b = 0; b < 8 && kc0 + 16 * b < K; ++b) tma_store_3d(&tmD, ebuf_s, kc0 + 16 * b, n0, e);
+            for (int b = 0; b < 128 / C::BOX_COLS && kc0 + C::BOX_COLS * b < K; ++b)
+              tma_store_3d(&tmD, ebuf_s, kc0 + C::BOX_COLS * b, n0, e);
             bulk_commit();
           }
         }
@@ -768,28 +804,27 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
         if (!mine) continue;
         const bool reduce = args.accumulate || c0 > 0;
         // a later chunk is added onto the earlier chunk's writes: let them land first
-        if (lane == 0) {
-          if (c0 > 0) bulk_wait<0>();
-          else bulk_wait_read<0>();
-        }
-        __syncwarp();
+        if (lane == 0 && c0 > 0) bulk_wait<0>();
+        constexpr int BC = C::BOX_COLS, CH = BC / 4;  // 16-byte chunks per box row
+        // swizzle: chunk ^= row % 8 (128-byte rows) or (row / 2) % 4 (64-byte rows)
+        const int sw = BC == 32 ? (lane & 7) : ((lane >> 1) & 3);
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          if (kc0 + 16 * b >= K) break;
-          if (b > 0) {
-            if (lane == 0) bulk_wait_read<0>();
-            __syncwarp();
-          }
-          uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * 64);
+        for (int b = 0; b < 128 / BC; ++b) {
+          if (kc0 + BC * b >= K) break;
+          if (lane == 0) bulk_wait_read<C::EPI_BUFS - 1>();  // the buffer's previous box has left
+          __syncwarp();
+          uint8_t* buf = ebuf + (b % C::EPI_BUFS) * C::EPI_BUF_BYTES;
+          uint4* rowp = reinterpret_cast<uint4*>(buf + lane * BC * 4);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            rowp[j ^ sw] = make_uint4(v[16 * b + 4 * j], v[16 * b + 4 * j + 1], v[16 * b + 4 * j + 2],
-                                      v[16 * b + 4 * j + 3]);
+          for (int j = 0; j < CH; ++j)
+            rowp[j ^ sw] = make_uint4(v[BC * b + 4 * j], v[BC * b + 4 * j + 1], v[BC * b + 4 * j + 2],
+                                      v[BC * b + 4 * j + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (reduce) tma_reduce_add_3d(&tmD, ebuf_s, kc0 + 16 * b, n0, e);
-            else tma_store_3d(&tmD, ebuf_s, kc0 + 16 * b, n0, e);
+            const uint32_t src = ebuf_s + (b % C::EPI_BUFS) * C::EPI_BUF_BYTES;
+            if (reduce) tma_reduce_add_3d(&tmD, src, kc0 + BC * b, n0, e);
+            else tma_store_3d(&tmD, src, kc0 + BC * b, n0, e);
             bulk_commit();
           }
         }
