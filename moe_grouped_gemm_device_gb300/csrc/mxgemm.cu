@@ -346,25 +346,33 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
   }
 }
 
-// Blocked scale layout: one warp per 512-byte (block, chunk) range; lane l
-// gathers rows l, l+32, l+64, l+96 of the block (4 scale columns each) and
-// writes its 16 bytes, so each warp's store is one contiguous 512-byte line.
-__global__ void __launch_bounds__(256) mx_blocked_kernel(const uint8_t* __restrict__ src,
-                                                         const int32_t* __restrict__ offsets, int G, int R,
-                                                         int KS, uint8_t* __restrict__ dst,
-                                                         unsigned int* status) {
-  extern __shared__ int s_tab[];
-  int* s_off = s_tab;        // [G+1]
-  int* s_bp = s_tab + G + 1;  // [G+1] first block of each group
+// ------------------------------------------------- blocked scale conversions
+//
+// Both conversions stage a 128-row slab of the scale matrix in shared memory
+// with coalesced loads (consecutive threads read consecutive bytes) and then
+// emit 512-byte blocks, one warp per block: lane l gathers rows l, l+32,
+// l+64, l+96 (4 scale columns each) and writes its 16 bytes, so every block
+// is one contiguous store line.  A pass covers at most PASS_COLS scale
+// columns (PASS_COLS / 4 chunks).
+constexpr int kConvThreads = 256;
+constexpr int kPassCols = 256;
+
+// Offsets -> shared memory, validation (leading zero, non-decreasing, last
+// <= limit, multiples of `align`), and s_pre[g] = sum over g' < g of
+// ceil((offsets[g'+1] - offsets[g']) / 128).  Returns false (after setting
+// the status bit once) when the offsets are invalid.
+__device__ bool conv_prologue(const int32_t* offsets, int G, int64_t limit, int align, int* s_off, int* s_pre,
+                              unsigned int* status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i <= G; i += blockDim.x) s_off[i] = offsets[i];
   __syncthreads();
   int bad = 0;
   for (int i = threadIdx.x; i < G; i += blockDim.x) bad |= (s_off[i + 1] < s_off[i]);
-  if (threadIdx.x == 0) bad |= (s_off[0] != 0) | (s_off[G] > R);
+  for (int i = threadIdx.x; i <= G; i += blockDim.x) bad |= (s_off[i] % align) != 0;
+  if (threadIdx.x == 0) bad |= (s_off[0] != 0) | (static_cast<int64_t>(s_off[G]) > limit);
   if (__syncthreads_or(bad)) {
     if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, kDevBadOffsets);
-    return;
+    return false;
   }
   if (warp == 0) {
     const int per = (G + 31) / 32;
@@ -379,112 +387,188 @@ __global__ void __launch_bounds__(256) mx_blocked_kernel(const uint8_t* __restri
     }
     int run = incl - s;
     for (int g = lo; g < hi; ++g) {
-      s_bp[g] = run;
+      s_pre[g] = run;
       run += (s_off[g + 1] - s_off[g] + 127) / 128;
     }
-    if (lane == 31) s_bp[G] = incl;
+    if (lane == 31) s_pre[G] = incl;
   }
   __syncthreads();
+  return true;
+}
+
+// The last g with s_pre[g] <= x (the group owning block / chunk x).
+__device__ __forceinline__ int group_of(const int* s_pre, int G, int x) {
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_pre[mid] <= x) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// One warp: the 512-byte block made of chunk columns [4c, 4c+4) of the
+// 128-row slab `tile` (row stride `ld` bytes), written to dst.
+__device__ __forceinline__ void emit_block(const uint8_t* tile, int ld, int c, uint8_t* dst, int lane) {
+  uint32_t w[4];
+#pragma unroll
+  for (int qq = 0; qq < 4; ++qq) w[qq] = *reinterpret_cast<const uint32_t*>(tile + (lane + 32 * qq) * ld + 4 * c);
+  reinterpret_cast<uint4*>(dst)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Groups along the rows: block b = rows base .. base+127 of group g.
+__global__ void __launch_bounds__(kConvThreads) mx_blocked_kernel(const uint8_t* __restrict__ src,
+                                                                  const int32_t* __restrict__ offsets, int G,
+                                                                  int R, int KS, uint8_t* __restrict__ dst,
+                                                                  unsigned int* status) {
+  __shared__ __align__(16) uint8_t tile[128 * kPassCols];
+  extern __shared__ int s_tab[];
+  int* s_off = s_tab;
+  int* s_pre = s_tab + G + 1;
+  if (!conv_prologue(offsets, G, R, 1, s_off, s_pre, status)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nc = (KS + 3) / 4;
-  const int64_t items = static_cast<int64_t>(s_bp[G]) * nc;
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t it = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp; it < items; it += nwarps) {
-    const int b = static_cast<int>(it / nc), c = static_cast<int>(it % nc);
-    int lo = 0, hi = G;  // the group of block b: the last g with s_bp[g] <= b
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_bp[mid] <= b) lo = mid;
-      else hi = mid;
-    }
-    const int base = s_off[lo] + 128 * (b - s_bp[lo]);
-    const int end = s_off[lo + 1];
-    uint32_t w[4];
+  const int NB = s_pre[G];
+  for (int b = blockIdx.x; b < NB; b += gridDim.x) {
+    const int g = group_of(s_pre, G, b);
+    const int base = s_off[g] + 128 * (b - s_pre[g]);
+    const int rows = min(128, s_off[g + 1] - base);
+    for (int c0 = 0; c0 < nc; c0 += kPassCols / 4) {
+      const int cols = min(kPassCols, 4 * (nc - c0));  // staged width (whole chunks)
+      const int col0 = 4 * c0;
+      if (cols == KS && (reinterpret_cast<uintptr_t>(src) & 3) == 0) {
+        // the pass covers whole rows: the slab is one contiguous run of
+        // 32-bit words (KS is a multiple of 4 here); eight loads in flight
+        const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src + static_cast<int64_t>(base) * KS);
+        uint32_t* t32 = reinterpret_cast<uint32_t*>(tile);
+        const int valid_w = rows * KS / 4, total_w = 128 * KS / 4;
+        for (int i0 = threadIdx.x; i0 < total_w; i0 += 8 * blockDim.x) {
+          uint32_t v[8];
 #pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-      const int r = base + lane + 32 * qq;
-      uint32_t v = 0;
+          for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * blockDim.x;
+            v[u] = i < valid_w ? __ldg(s32 + i) : 0x7F7F7F7Fu;
+          }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int col = 4 * c + j;
-        const uint32_t byte = (r < end && col < KS) ? src[static_cast<int64_t>(r) * KS + col] : 0x7Fu;
-        v |= byte << (8 * j);
+          for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * blockDim.x;
+            if (i < total_w) t32[i] = v[u];
+          }
+        }
+      } else {
+        for (int i0 = threadIdx.x; i0 < 128 * cols; i0 += 8 * blockDim.x) {
+          uint8_t v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * blockDim.x;
+            const int r = i / cols, col = col0 + (i - r * cols);
+            v[u] = (i < 128 * cols && r < rows && col < KS) ? src[static_cast<int64_t>(base + r) * KS + col] : 0x7F;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * blockDim.x;
+            if (i < 128 * cols) tile[i] = v[u];
+          }
+        }
       }
-      w[qq] = v;
+      __syncthreads();
+      for (int c = warp; c < cols / 4; c += blockDim.x >> 5)
+        emit_block(tile, cols, c, dst + (static_cast<int64_t>(b) * nc + c0 + c) * 512, lane);
+      __syncthreads();
     }
-    reinterpret_cast<uint4*>(dst + it * 512)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
+// Groups along the contraction: chunk q of group g covers scale columns
+// cb = offsets[g]/32 + 4 (q - s_pre[g]) .. cb+3, those at or past
+// offsets[g+1]/32 are padding.  A work item is a 128-row slab times up to
+// kKChunks consecutive chunks, whose columns form one contiguous range; the
+// range is staged from its start rounded down to 4 bytes, so that rows whose
+// length is a multiple of 4 are read as aligned 32-bit words.
+constexpr int kKChunks = 32;
+constexpr int kKStride = 4 * kKChunks + 8;  // staged bytes per row (range + alignment slack)
 
-// Blocked scale layout for groups along the contraction: one warp per
-// 512-byte (row block, chunk) range.  Chunk q belongs to the group g whose
-// chunks start at s_qp[g] <= q; its scale columns are offsets[g]/32 +
-// 4*(q - s_qp[g]) .. +3, those at or past offsets[g+1]/32 are padding.
-__global__ void __launch_bounds__(256) mx_blocked_k_kernel(const uint8_t* __restrict__ src,
-                                                           const int32_t* __restrict__ offsets, int G, int R,
-                                                           int KS, uint8_t* __restrict__ dst,
-                                                           unsigned int* status) {
+__global__ void __launch_bounds__(kConvThreads) mx_blocked_k_kernel(const uint8_t* __restrict__ src,
+                                                                    const int32_t* __restrict__ offsets, int G,
+                                                                    int R, int KS, uint8_t* __restrict__ dst,
+                                                                    unsigned int* status) {
+  __shared__ __align__(16) uint8_t tile[128 * kKStride];
+  __shared__ int s_cb[kKChunks], s_c1[kKChunks];
   extern __shared__ int s_tab[];
-  int* s_off = s_tab;         // [G+1]
-  int* s_qp = s_tab + G + 1;  // [G+1] first chunk of each group
+  int* s_off = s_tab;
+  int* s_pre = s_tab + G + 1;
+  if (!conv_prologue(offsets, G, 32ll * KS, 32, s_off, s_pre, status)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i <= G; i += blockDim.x) s_off[i] = offsets[i];
-  __syncthreads();
-  int bad = 0;
-  for (int i = threadIdx.x; i < G; i += blockDim.x) bad |= (s_off[i + 1] < s_off[i]);
-  for (int i = threadIdx.x; i <= G; i += blockDim.x) bad |= (s_off[i] & 31) != 0;
-  if (threadIdx.x == 0) bad |= (s_off[0] != 0) | (static_cast<int64_t>(s_off[G]) > 32ll * KS);
-  if (__syncthreads_or(bad)) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, kDevBadOffsets);
-    return;
-  }
-  if (warp == 0) {
-    const int per = (G + 31) / 32;
-    const int lo = min(G, lane * per), hi = min(G, lo + per);
-    int s = 0;
-    for (int g = lo; g < hi; ++g) s += (s_off[g + 1] - s_off[g] + 127) / 128;
-    int incl = s;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
-    }
-    int run = incl - s;
-    for (int g = lo; g < hi; ++g) {
-      s_qp[g] = run;
-      run += (s_off[g + 1] - s_off[g] + 127) / 128;
-    }
-    if (lane == 31) s_qp[G] = incl;
-  }
-  __syncthreads();
-  const int NQ = s_qp[G];
+  const int NQ = s_pre[G];
   const int nrb = (R + 127) / 128;
-  const int64_t items = static_cast<int64_t>(nrb) * NQ;
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t it = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp; it < items; it += nwarps) {
-    const int rb = static_cast<int>(it / NQ), q = static_cast<int>(it % NQ);
-    int lo = 0, hi = G;  // the group of chunk q: the last g with s_qp[g] <= q
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_qp[mid] <= q) lo = mid;
-      else hi = mid;
+  const int nqp = (NQ + kKChunks - 1) / kKChunks;
+  const bool words = (KS & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 3) == 0;
+  for (int it = blockIdx.x; it < nrb * nqp; it += gridDim.x) {
+    const int rb = it / nqp, q0 = (it - rb * nqp) * kKChunks;
+    const int nq = min(kKChunks, NQ - q0);
+    for (int k = threadIdx.x; k < nq; k += blockDim.x) {
+      const int g = group_of(s_pre, G, q0 + k);
+      s_cb[k] = s_off[g] / 32 + 4 * (q0 + k - s_pre[g]);
+      s_c1[k] = s_off[g + 1] / 32;
     }
-    const int cb = s_off[lo] / 32 + 4 * (q - s_qp[lo]);
-    const int c1 = s_off[lo + 1] / 32;
-    uint32_t w[4];
+    __syncthreads();
+    const int cs = words ? (s_cb[0] & ~3) : s_cb[0];   // first staged column
+    const int ce = min(KS, s_cb[nq - 1] + 4);          // one past the last needed column
+    if (words) {
+      const int wpr = (ce - cs + 3) / 4;  // ends inside the row: KS is a multiple of 4
+      for (int i0 = threadIdx.x; i0 < 128 * wpr; i0 += 8 * blockDim.x) {
+        uint32_t v[8];
 #pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-      const int r = 128 * rb + lane + 32 * qq;
-      uint32_t v = 0;
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * blockDim.x;
+          const int r = i / wpr, row = 128 * rb + r;
+          v[u] = (i < 128 * wpr && row < R)
+                     ? __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<int64_t>(row) * KS + cs) + (i - r * wpr))
+                     : 0x7F7F7F7Fu;
+        }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int col = cb + j;
-        const uint32_t byte = (r < R && col < c1) ? src[static_cast<int64_t>(r) * KS + col] : 0x7Fu;
-        v |= byte << (8 * j);
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * blockDim.x;
+          const int r = i / wpr;
+          if (i < 128 * wpr) reinterpret_cast<uint32_t*>(tile + r * kKStride)[i - r * wpr] = v[u];
+        }
       }
-      w[qq] = v;
+    } else {
+      const int width = ce - cs;
+      for (int i0 = threadIdx.x; i0 < 128 * width; i0 += 8 * blockDim.x) {
+        uint8_t v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * blockDim.x;
+          const int r = i / width, row = 128 * rb + r;
+          v[u] = (i < 128 * width && row < R) ? src[static_cast<int64_t>(row) * KS + cs + (i - r * width)] : 0x7F;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * blockDim.x;
+          const int r = i / width;
+          if (i < 128 * width) tile[r * kKStride + (i - r * width)] = v[u];
+        }
+      }
     }
-    reinterpret_cast<uint4*>(dst + it * 512)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+    __syncthreads();
+    for (int k = warp; k < nq; k += blockDim.x >> 5) {
+      const int cb = s_cb[k] - cs, c1 = s_c1[k] - cs;  // relative to the staged range
+      uint32_t w[4];
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t byte = cb + j < c1 ? tile[(lane + 32 * qq) * kKStride + cb + j] : 0x7Fu;
+          v |= byte << (8 * j);
+        }
+        w[qq] = v;
+      }
+      reinterpret_cast<uint4*>(dst + (static_cast<int64_t>(rb) * NQ + q0 + k) * 512)[lane] =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
   }
 }
 
@@ -866,10 +950,10 @@ cudaError_t launch_mx_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUte
 
 cudaError_t launch_mx_blocked(const uint8_t* src, const int32_t* offsets, int G, int R, int KS, uint8_t* dst,
                               unsigned int* status, int num_sms, cudaStream_t stream) {
-  const int64_t items_ub = (static_cast<int64_t>(R) / 128 + G) * ((KS + 3) / 4);
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((items_ub + 7) / 8, 4 * num_sms)));
+  const int64_t blocks_ub = static_cast<int64_t>(R) / 128 + G;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(blocks_ub, 8 * num_sms)));
   const size_t smem = 2 * (static_cast<size_t>(G) + 1) * sizeof(int);
-  mx_blocked_kernel<<<grid, 256, smem, stream>>>(src, offsets, G, R, KS, dst, status);
+  mx_blocked_kernel<<<grid, kConvThreads, smem, stream>>>(src, offsets, G, R, KS, dst, status);
   return cudaGetLastError();
 }
 
@@ -892,10 +976,10 @@ cudaError_t launch_mx_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, cons
 
 cudaError_t launch_mx_blocked_k(const uint8_t* src, const int32_t* offsets, int G, int R, int KS, uint8_t* dst,
                                 unsigned int* status, int num_sms, cudaStream_t stream) {
-  const int64_t items_ub = (static_cast<int64_t>(R) + 127) / 128 * (KS / 4 + G);
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((items_ub + 7) / 8, 4 * num_sms)));
+  const int64_t items_ub = (static_cast<int64_t>(R) + 127) / 128 * ((KS / 4 + G + kKChunks - 1) / kKChunks);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(items_ub, 8 * num_sms)));
   const size_t smem = 2 * (static_cast<size_t>(G) + 1) * sizeof(int);
-  mx_blocked_k_kernel<<<grid, 256, smem, stream>>>(src, offsets, G, R, KS, dst, status);
+  mx_blocked_k_kernel<<<grid, kConvThreads, smem, stream>>>(src, offsets, G, R, KS, dst, status);
   return cudaGetLastError();
 }
 
