@@ -151,12 +151,14 @@ int rg_mx_scales_blocked(const uint8_t* scales, const int32_t* offsets, int G, i
  *   xq          device, uint8 [M, K]: E4M3 codes.
  *   sx_blocked  device: the scales sx [M, K/32] of xq (sx[r, k/32] scales
  *               xq[r, k]) in the blocked layout of rg_mx_scales_blocked with
- *               the same offsets.
+ *               the same offsets; the buffer holds rg_mx_blocked_bytes(M,
+ *               K/32, E) bytes.
  *   wq          device, uint8 E4M3 codes, [E, N, K] when transpose_B == 0,
  *               [E, K, N] when transpose_B != 0.
  *   sw_blocked  device: the scales sw [E, N, K/32] of B (sw[e, n, k/32]
  *               scales B element (k, n) of expert e, in both layouts) in the
- *               blocked layout with G = E groups of N rows.
+ *               blocked layout with G = E groups of N rows; the buffer holds
+ *               rg_mx_blocked_bytes(E*N, K/32, E) bytes.
  *   offsets     device, int32 [E+1], as for rg_mgemm.
  *   y           device, bf16 [M, N]: for row r of expert e
  *                 y[r, n] = sum_k xq[r,k] 2^(sx[r,k/32]-127) * B[k,n] 2^(sw[e,n,k/32]-127)
