@@ -290,3 +290,57 @@ def test_mx_kgemm_no_rows_zeroes(gpu_lib):
     torch.cuda.synchronize()
     assert gpu_lib.device_status() == 0
     assert bool((dW == 0).all())
+
+
+# ------------------------------------------------------------------ edge cases
+
+
+def test_mx_many_small_experts(gpu_lib):
+    """300 experts of 0..7 and a few long ones: the device tile lists and the
+    scale-block prefix sums span many groups; empty experts write nothing."""
+    rng = np.random.default_rng(91)
+    counts = rng.integers(0, 8, size=300)
+    counts[[5, 150, 299]] = [300, 260, 129]
+    counts[[0, 1, 200]] = 0
+    off = W.offsets_from_counts(counts)
+    E, N, K = 300, 64, 64
+    M = int(off[-1]) + 4
+    xq, wq = W.e4m3_codes((M, K), 91, 0), W.e4m3_codes((E, N, K), 91, 1)
+    sx = W.e8m0_codes((M, K // 32), *W.MX_ACT_SCALES, 91, 2)
+    sw = W.e8m0_codes((E, N, K // 32), *W.mx_weight_scales(K), 91, 3)
+    y = run_mx(gpu_lib, xq, sx, wq, sw, off, False)
+    ref = oracle.mgemm_mx(xq, sx, wq, sw, off)
+    valid = int(off[-1])
+    check_bf16(y[:valid], ref[:valid], "mxfp8 300 experts")
+    assert (y[valid:] == SENTINEL_BF16).all()
+
+
+def test_mx_kgemm_many_experts(gpu_lib):
+    from parity import check_fp32
+    rng = np.random.default_rng(92)
+    counts = 32 * rng.integers(0, 3, size=300)
+    counts[[7, 100]] = [4128, 320]
+    off, gq, sg, xq, sx = mxk_random(92, counts, 32, 48)
+    dW = run_mxk(gpu_lib, gq, sg, xq, sx, off)
+    ref = oracle.kgemm_mx(gq, sg, xq, sx, off)
+    check_fp32(dW, ref, "mxfp8 wgrad 300 experts")
+    assert (dW[np.flatnonzero(counts == 0)] == 0).all()
+
+
+def test_mx_no_rows(gpu_lib):
+    """M = 0: the Mgemm writes nothing, the Kgemm zeroes dW."""
+    import torch
+    E, N, K = 3, 32, 64
+    off = offsets_dev(np.zeros(E + 1, np.int32))
+    wq = torch.zeros((E, N, K), dtype=torch.uint8, device="cuda")
+    sb = torch.zeros((gpu_lib.mx_blocked_bytes(E * N, K // 32, E),), dtype=torch.uint8, device="cuda")
+    xq = torch.zeros((0, K), dtype=torch.uint8, device="cuda")
+    sa = torch.zeros((gpu_lib.mx_blocked_bytes(0, K // 32, E),), dtype=torch.uint8, device="cuda")
+    y = gpu_lib.mgemm_mxfp8(xq, sa, wq, sb, off)
+    assert tuple(y.shape) == (0, N)
+    dW = torch.full((E, N, K), 3.0, dtype=torch.float32, device="cuda")
+    g0 = torch.zeros((0, N), dtype=torch.uint8, device="cuda")
+    gpu_lib.kgemm_mxfp8(g0, sb, xq, sb, off, out=dW)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    assert bool((dW == 0).all())
