@@ -124,3 +124,69 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(rg, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         rg.load()
+
+
+@pytest.mark.parametrize(
+    "args",
+    [dict(x=None), dict(w=None), dict(offsets=None), dict(y=None), dict(x=BAD), dict(O=0), dict(O=-2),
+     dict(O=rg.RG_MAX_OUTER + 1), dict(L=0), dict(L=1025), dict(N=12), dict(K=4), dict(M=-1),
+     dict(O=65536, N=65536)],  # O*N past int32
+)
+def test_mgemm_nested_rejects_bad_arguments(lib, args):
+    a = dict(x=DEV, w=DEV, offsets=DEV, O=2, L=4, M=512, N=128, K=16, t=0, y=DEV, s=None)
+    a.update(args)
+    rc = lib.rg_mgemm_nested(a["x"], a["w"], a["offsets"], a["O"], a["L"], a["M"], a["N"], a["K"], a["t"],
+                             a["y"], a["s"])
+    assert rc == rg.RG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize(
+    "args",
+    [dict(xq=None), dict(sx=None), dict(wq=None), dict(sw=None), dict(offsets=None), dict(y=None),
+     dict(xq=BAD), dict(sw=BAD), dict(E=0), dict(E=1025), dict(M=-1), dict(N=8), dict(N=40), dict(K=16),
+     dict(K=48)],
+)
+def test_mgemm_mxfp8_rejects_bad_arguments(lib, args):
+    a = dict(xq=DEV, sx=DEV, wq=DEV, sw=DEV, offsets=DEV, E=4, M=512, N=128, K=256, t=0, y=DEV, s=None)
+    a.update(args)
+    rc = lib.rg_mgemm_mxfp8(a["xq"], a["sx"], a["wq"], a["sw"], a["offsets"], a["E"], a["M"], a["N"], a["K"],
+                            a["t"], a["y"], a["s"])
+    assert rc == rg.RG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize(
+    "args",
+    [dict(gq=None), dict(sg=None), dict(xq=None), dict(sx=None), dict(offsets=None), dict(dW=None),
+     dict(dW=BAD), dict(E=0), dict(M=-32), dict(M=100), dict(N=8), dict(K=24)],
+)
+def test_kgemm_mxfp8_rejects_bad_arguments(lib, args):
+    a = dict(gq=DEV, sg=DEV, xq=DEV, sx=DEV, offsets=DEV, E=4, M=512, N=128, K=256, dW=DEV, acc=0, s=None)
+    a.update(args)
+    rc = lib.rg_kgemm_mxfp8(a["gq"], a["sg"], a["xq"], a["sx"], a["offsets"], a["E"], a["M"], a["N"], a["K"],
+                            a["dW"], a["acc"], a["s"])
+    assert rc == rg.RG_ERR_INVALID_ARG
+
+
+def test_mx_scale_layout_entry_points_validate(lib):
+    assert lib.rg_mx_blocked_bytes(300, 7, 6) == (300 // 128 + 6) * 2 * 512
+    assert lib.rg_mx_blocked_bytes(-1, 7, 6) == -1 and lib.rg_mx_blocked_bytes(10, 0, 1) == -1
+    assert lib.rg_mx_blocked_k_bytes(300, 10, 3) == 3 * (10 // 4 + 3) * 512
+    assert lib.rg_mx_blocked_k_bytes(0, 10, 3) == -1
+    need = lib.rg_mx_blocked_bytes(512, 8, 4)
+    for fn, n in (("rg_mx_scales_blocked", need), ("rg_mx_scales_blocked_k", lib.rg_mx_blocked_k_bytes(512, 8, 4))):
+        f = getattr(lib, fn)
+        assert f(DEV, DEV, 4, 512, 8, DEV, n - 1, None) == rg.RG_ERR_INVALID_ARG  # too small
+        assert f(DEV, None, 4, 512, 8, DEV, n, None) == rg.RG_ERR_INVALID_ARG
+        assert f(DEV, DEV, 4, 512, 8, BAD, n, None) == rg.RG_ERR_INVALID_ARG
+        assert f(DEV, DEV, 0, 512, 8, DEV, n, None) == rg.RG_ERR_INVALID_ARG
+        assert f(DEV, DEV, 4, 512, 0, DEV, n, None) == rg.RG_ERR_INVALID_ARG
+
+
+def test_oracle_blocked_sizes_match_the_library(lib):
+    """The size bounds the library states equal the oracle's (both written
+    from the same definition of the layouts, checked here against each other)."""
+    import oracle
+    for R, KS, G in ((300, 7, 6), (1, 1, 1), (65536, 96, 128), (0, 3, 2)):
+        assert lib.rg_mx_blocked_bytes(R, KS, G) == oracle.mx_blocked_bytes(R, KS, G)
+    for R, KS, G in ((300, 10, 3), (2560, 1024, 32), (1, 1, 1)):
+        assert lib.rg_mx_blocked_k_bytes(R, KS, G) == oracle.mx_blocked_k_bytes(R, KS, G)
