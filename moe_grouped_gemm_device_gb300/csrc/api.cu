@@ -137,11 +137,12 @@ bool encode_rows(CUtensorMap* m, const void* ptr, int64_t rows, int cols, uint32
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, str, box);
 }
 
-// Forward weight [E, N, K] (K contiguous): boxes of 64 K x BN_CTA rows.
-bool encode_weight(CUtensorMap* m, const void* w, int E, int N, int K) {
+// Forward weight [E, N, K] (K contiguous): boxes of 64 K x (B rows per CTA of
+// the tile the launch uses).
+bool encode_weight(CUtensorMap* m, const void* w, int E, int N, int K, int box_rows) {
   const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
   const uint64_t str[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2};
-  const uint32_t box[3] = {64, rg::mg::BN_CTA, 1};
+  const uint32_t box[3] = {64, static_cast<uint32_t>(box_rows), 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box);
 }
 
@@ -192,7 +193,7 @@ int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_
   CUtensorMap tmA, tmB, tmY;
   if (!encode_rows(&tmA, x, M, K, rg::mg::BM)) return RG_ERR_INVALID_ARG;
   if (!transpose_B) {  // w [E, N, K], K contiguous: one 64 x BN_CTA box per stage and CTA
-    if (!encode_weight(&tmB, w, E, N, K)) return RG_ERR_INVALID_ARG;
+    if (!encode_weight(&tmB, w, E, N, K, rg::mgemm_b_box_rows(false, N))) return RG_ERR_INVALID_ARG;
   } else {  // w [E, K, N], N contiguous: 64-column boxes of 64 K rows
     const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(E)};
     const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K) * N * 2};
@@ -243,7 +244,7 @@ int rg_mgemm_nested(const void* x, const void* w, const int32_t* offsets, int O,
     if (!encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, yd, ys, yb)) return RG_ERR_INVALID_ARG;
   }
   if (!transpose_B) {
-    if (!encode_weight(&tmB, w, G, N, K)) return RG_ERR_INVALID_ARG;
+    if (!encode_weight(&tmB, w, G, N, K, rg::mgemm_b_box_rows(false, N))) return RG_ERR_INVALID_ARG;
   } else {
     const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(G)};
     const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K) * N * 2};
@@ -277,7 +278,7 @@ int rg_mgemm_swiglu(const void* x, const void* w13, const int32_t* offsets, int 
 
   CUtensorMap tmA, tmB, tmH, tmY13;
   if (!encode_rows(&tmA, x, M, K, rg::mg::BM)) return RG_ERR_INVALID_ARG;
-  if (!encode_weight(&tmB, w13, E, N, K)) return RG_ERR_INVALID_ARG;
+  if (!encode_weight(&tmB, w13, E, N, K, rg::mg::BN_CTA)) return RG_ERR_INVALID_ARG;  // fused epilogue: default tile
   if (!encode_rows(&tmH, h, M, F, 32)) return RG_ERR_INVALID_ARG;
   if (y13 != nullptr) {
     if (!encode_rows(&tmY13, y13, M, N, 32)) return RG_ERR_INVALID_ARG;

@@ -88,6 +88,13 @@ constexpr int CHUNK_ROWS = 4096;
 static_assert(CHUNK_ROWS % BR == 0, "chunks must hold whole row blocks");
 }  // namespace kg
 
+// Mgemm tile variants (CTA pairs only): 64-column tiles for forward outputs at
+// most 64 wide, eight epilogue warps when the contraction fits one 64-deep
+// stage.  The host encodes B's tensor map for the tile the launch uses.
+inline bool mgemm_narrow(bool transpose_B, int N) { return kCtaGroup == 2 && !transpose_B && N <= 64; }
+inline bool mgemm_wide_epilogue(int K) { return kCtaGroup == 2 && K <= mg::BK; }
+inline int mgemm_b_box_rows(bool transpose_B, int N) { return mgemm_narrow(transpose_B, N) ? 32 : mg::BN_CTA; }
+
 // Bytes of dynamic shared memory a launch with E experts needs.
 size_t mgemm_smem_bytes(int E);
 size_t kgemm_smem_bytes(int E, size_t max_smem);  // of the configuration a launch uses

@@ -42,23 +42,27 @@
 namespace rg {
 namespace {
 
-template <int CG>
+// BNT: tile columns (256; 64 for outputs at most 64 wide, whose MMAs would
+// otherwise be mostly padding).  EPIW: epilogue warps (4; 8 when the
+// contraction fits one stage and the epilogue, not the MMAs, sets the pace --
+// two warps per tensor-memory lane quarter then split the columns).
+template <int CG, int BNT = 256, int EPIW = 4>
 struct Cfg {
   static constexpr int BM = 128;            // rows of A (and of D) per CTA
   static constexpr int TILE_M = BM * CG;    // rows per tile
-  static constexpr int BN = 256;            // tile columns = MMA N
+  static constexpr int BN = BNT;            // tile columns = MMA N
   static constexpr int BN_CTA = BN / CG;    // B rows (output columns) loaded per CTA
   static constexpr int BK = 64;
-  static constexpr int STAGES = CG == 2 ? 6 : 4;
+  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 8 : (EPIW == 8 ? 5 : 6)) : 4;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN_CTA * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_WARPS = EPIW;
   static constexpr int EPI_BUF_BYTES = 32 * 128;
-  // warp 0 and warp 6: TMA producers (alternate stages), warp 1: MMA,
-  // warps 2-5: epilogue
-  static constexpr int PRODUCER2 = 6;
-  static constexpr int THREADS = 224;
+  // warp 0 and warp 2 + EPIW: TMA producers (alternate stages), warp 1: MMA,
+  // warps 2 .. 1 + EPIW: epilogue
+  static constexpr int PRODUCER2 = 2 + EPIW;
+  static constexpr int THREADS = 32 * (3 + EPIW);
   // full[S], empty[S], ready[S], tfull[2], tempty[2], drain
   static constexpr int NUM_BARS = 3 * STAGES + 5;
   // The dynamic shared-memory window of a CTA without static shared memory
@@ -82,15 +86,18 @@ constexpr uint32_t TMEM_COLS = 512;
 //                  and the epilogue writes dy13 = [dh*up*SiLU'(gate), dh*SiLU(gate)].
 constexpr int kEpiPlain = 0, kEpiSwiglu = 1, kEpiSwigluBwd = 2;
 
-template <bool TRANS_B, int CG, int EPI = kEpiPlain>
-__global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
+template <bool TRANS_B, int CG, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4>
+__global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
     mgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmY2,
                  const GroupArgs args) {
   constexpr bool SWIGLU = EPI == kEpiSwiglu;
   static_assert(!SWIGLU || (CG == 2 && !TRANS_B), "SwiGLU variant: forward, CTA pairs");
   static_assert(EPI != kEpiSwigluBwd || TRANS_B, "SwiGLU backward: input-gradient GEMM");
-  using C = Cfg<CG>;
+  static_assert((BNT == 256 && (EPIW == 4 || EPIW == 8)) || (BNT == 64 && EPIW == 4 && CG == 2 && !TRANS_B),
+                "tile variants: 256 columns with 4 or 8 epilogue warps; 64 columns (forward, CTA pairs)");
+  static_assert(EPI == kEpiPlain || (BNT == 256 && EPIW == 4), "fused epilogues use the default tile");
+  using C = Cfg<CG, BNT, EPIW>;
   constexpr int BM = C::BM, TILE_M = C::TILE_M, BN = C::BN, BN_CTA = C::BN_CTA, BK = C::BK;
   constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
 
@@ -308,8 +315,12 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   } else if (warp == 1) {
     // warp 1 of the peer CTA only takes part in the tensor-memory allocation
   } else {
-    // ======================= epilogue (warps 2..5) ===========================
+    // =================== epilogue (warps 2 .. 1 + EPIW) ======================
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // 64-column chunks of the tile this warp converts: all of them, or with 8
+    // epilogue warps the first or second half
+    constexpr int CH = BN / 64 / (C::EPI_WARPS / 4);
+    const int c_first = ((warp - 2) >> 2) * CH;
     const int r_in_cta = q * 32 + lane;
     uint8_t* ebuf = epi + (warp - 2) * C::EPI_BUF_BYTES;
     const uint32_t ebuf_s = smem_u32(ebuf);
@@ -424,12 +435,12 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       } else if constexpr (!SWIGLU) {
         const int n0 = (local % nbn) * BN;
 #pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
+        for (int c = c_first; c < c_first + CH; ++c) {
           uint32_t v0[32], v1[32];
           tmem_ld_32x32b_x32(taddr + 64 * c, v0);
           tmem_ld_32x32b_x32(taddr + 64 * c + 32, v1);
           tmem_ld_wait();
-          if (c == BN / 64 - 1) release_acc(buf);
+          if (c == c_first + CH - 1) release_acc(buf);
           uint32_t p[32];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -488,18 +499,23 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   }
 }
 
-template <bool TB, int EPI = kEpiPlain>
-cudaError_t set_smem(int max_smem) {
-  const int bytes = static_cast<int>(std::min<size_t>(mgemm_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem));
-  return cudaFuncSetAttribute(mgemm_kernel<TB, kCtaGroup, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              bytes);
+template <int BNT, int EPIW>
+size_t smem_of(int E) {
+  return Cfg<kCtaGroup, BNT, EPIW>::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4;
 }
 
-void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, size_t smem,
+template <bool TB, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4>
+cudaError_t set_smem(int max_smem) {
+  const int bytes = static_cast<int>(std::min<size_t>(smem_of<BNT, EPIW>(RG_MAX_EXPERTS_CFG), max_smem));
+  return cudaFuncSetAttribute(mgemm_kernel<TB, kCtaGroup, EPI, BNT, EPIW>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, size_t smem, int threads,
                  cudaStream_t stream) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(grid);
-  cfg->blockDim = dim3(Cfg<kCtaGroup>::THREADS);
+  cfg->blockDim = dim3(threads);
   cfg->dynamicSmemBytes = smem;
   cfg->stream = stream;
   if (kCtaGroup == 2) {
@@ -512,37 +528,56 @@ void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, s
   }
 }
 
+template <bool TB, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4>
+cudaError_t launch_variant(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
+                           const CUtensorMap& tmY2, const GroupArgs& args, int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  fill_config(&cfg, attr, grid, smem_of<BNT, EPIW>(args.E), Cfg<kCtaGroup, BNT, EPIW>::THREADS, stream);
+  return cudaLaunchKernelEx(&cfg, mgemm_kernel<TB, kCtaGroup, EPI, BNT, EPIW>, tmA, tmB, tmY, tmY2, args);
+}
+
 }  // namespace
 
-size_t mgemm_smem_bytes(int E) {
-  return Cfg<kCtaGroup>::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4;
+size_t mgemm_smem_bytes(int E) {  // the largest of the variants (the default tile)
+  return std::max({smem_of<256, 4>(E), smem_of<256, 8>(E), smem_of<64, 4>(E)});
 }
 
 cudaError_t mgemm_setup(int max_smem) {
   cudaError_t e = set_smem<false>(max_smem);
   if (e != cudaSuccess) return e;
-  if (kCtaGroup == 2 && (e = set_smem<false, kCtaGroup == 2 ? kEpiSwiglu : kEpiPlain>(max_smem)) != cudaSuccess)
-    return e;
+  if ((e = set_smem<true>(max_smem)) != cudaSuccess) return e;
   if ((e = set_smem<true, kEpiSwigluBwd>(max_smem)) != cudaSuccess) return e;
-  return set_smem<true>(max_smem);
+  if constexpr (kCtaGroup == 2) {
+    if ((e = set_smem<false, kEpiSwiglu>(max_smem)) != cudaSuccess) return e;
+    if ((e = set_smem<false, kEpiPlain, 64, 4>(max_smem)) != cudaSuccess) return e;
+    if ((e = set_smem<false, kEpiPlain, 256, 8>(max_smem)) != cudaSuccess) return e;
+    if ((e = set_smem<true, kEpiPlain, 256, 8>(max_smem)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t mgemm_max_clusters(int* clusters, int max_smem) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  fill_config(&cfg, attr, 2 * kCtaGroup, std::min<size_t>(mgemm_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem),
-              nullptr);
+  fill_config(&cfg, attr, 2 * kCtaGroup, std::min<size_t>(smem_of<256, 4>(RG_MAX_EXPERTS_CFG), max_smem),
+              Cfg<kCtaGroup>::THREADS, nullptr);
   return cudaOccupancyMaxActiveClusters(clusters, mgemm_kernel<false, kCtaGroup>, &cfg);
 }
 
 cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmY, const GroupArgs& args, int grid,
                          cudaStream_t stream) {
-  cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  fill_config(&cfg, attr, grid, mgemm_smem_bytes(args.E), stream);
-  if (transpose_B) return cudaLaunchKernelEx(&cfg, mgemm_kernel<true, kCtaGroup>, tmA, tmB, tmY, tmY, args);
-  return cudaLaunchKernelEx(&cfg, mgemm_kernel<false, kCtaGroup>, tmA, tmB, tmY, tmY, args);
+  if constexpr (kCtaGroup == 2) {
+    if (mgemm_narrow(transpose_B != 0, args.N))
+      return launch_variant<false, kEpiPlain, 64, 4>(tmA, tmB, tmY, tmY, args, grid, stream);
+    if (mgemm_wide_epilogue(args.K)) {
+      if (transpose_B) return launch_variant<true, kEpiPlain, 256, 8>(tmA, tmB, tmY, tmY, args, grid, stream);
+      return launch_variant<false, kEpiPlain, 256, 8>(tmA, tmB, tmY, tmY, args, grid, stream);
+    }
+  }
+  if (transpose_B) return launch_variant<true>(tmA, tmB, tmY, tmY, args, grid, stream);
+  return launch_variant<false>(tmA, tmB, tmY, tmY, args, grid, stream);
 }
 
 cudaError_t launch_mgemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmH,
@@ -551,21 +586,14 @@ cudaError_t launch_mgemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, 
   if constexpr (kCtaGroup != 2) {
     return cudaErrorNotSupported;
   } else {
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
-    fill_config(&cfg, attr, grid, mgemm_smem_bytes(args.E), stream);
-    return cudaLaunchKernelEx(&cfg, mgemm_kernel<false, kCtaGroup, kEpiSwiglu>, tmA, tmB, tmH, tmY13, args);
+    return launch_variant<false, kEpiSwiglu>(tmA, tmB, tmH, tmY13, args, grid, stream);
   }
 }
 
 cudaError_t launch_mgemm_swiglu_dgrad(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                       const CUtensorMap& tmDy13, const GroupArgs& args, int grid,
                                       cudaStream_t stream) {
-  cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  fill_config(&cfg, attr, grid, mgemm_smem_bytes(args.E), stream);
-  return cudaLaunchKernelEx(&cfg, mgemm_kernel<true, kCtaGroup, kEpiSwigluBwd>, tmA, tmB, tmDy13, tmDy13,
-                            args);
+  return launch_variant<true, kEpiSwigluBwd>(tmA, tmB, tmDy13, tmDy13, args, grid, stream);
 }
 
 }  // namespace rg

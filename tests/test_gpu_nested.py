@@ -126,3 +126,23 @@ def test_nested_bad_offsets_flagged(gpu_lib):
     torch.cuda.synchronize()
     assert gpu_lib.device_status() == gpu_lib.RG_DEV_BAD_OFFSETS
     assert bool((y == 7.0).all()), "a call with invalid offsets wrote its output"
+
+
+@pytest.mark.parametrize("N,K,transpose_B", [(48, 320, False), (64, 128, False), (16, 2048, False),
+                                             (384, 40, False), (384, 64, True), (200, 16, True), (72, 8, False)],
+                         ids=["narrow48", "narrow64", "narrow16_longK", "shallow40", "shallow64_dgrad",
+                              "shallow16_dgrad", "shallow8"])
+def test_mgemm_small_tile_variants_bit_exact(gpu_lib, N, K, transpose_B):
+    """Outputs at most 64 wide (64-column tiles) and contractions of one
+    64-deep stage (eight epilogue warps) run their own tile variants; integer
+    inputs make the expected bf16 outputs exact."""
+    counts = [300, 0, 1, 129, 77]
+    off = W.offsets_from_counts(counts)
+    M = int(off[-1]) + 5
+    x = W.integer_bf16((M, K), -2, 2, 23, 0)
+    w = W.integer_bf16((5, K, N) if transpose_B else (5, N, K), -2, 2, 23, 1)
+    y = run_nested(gpu_lib, x, w[None], off, transpose_B, M, 1, N)
+    ref = oracle.mgemm(x, w, off, transpose_B=transpose_B)
+    valid = int(off[-1])
+    np.testing.assert_array_equal(y[:valid], bf16_round_exact(ref[:valid]))
+    assert (y[valid:] == SENTINEL_BF16).all()
