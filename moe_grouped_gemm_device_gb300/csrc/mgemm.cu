@@ -53,7 +53,7 @@ struct Cfg {
   static constexpr int BN = BNT;            // tile columns = MMA N
   static constexpr int BN_CTA = BN / CG;    // B rows (output columns) loaded per CTA
   static constexpr int BK = 64;
-  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 8 : (EPIW == 8 ? 5 : 6)) : 4;
+  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 10 : (EPIW == 8 ? 5 : 6)) : 4;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN_CTA * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
