@@ -48,6 +48,9 @@ extern "C" {
 
 /* Largest number of experts one call accepts. */
 #define RG_MAX_EXPERTS 1024
+/* Largest number of experts of rg_kgemm / rg_kgemm_acc: their per-expert
+ * tables share a CTA's shared memory with the six-stage operand ring. */
+#define RG_KGEMM_MAX_EXPERTS 358
 /* Largest number of outer groups of rg_mgemm_nested. */
 #define RG_MAX_OUTER 65536
 
@@ -289,8 +292,8 @@ int rg_mgemm_swiglu_dgrad(const void* dy, const void* w2, const int32_t* offsets
  *            4096 rows, whose partial sums are added in FP32 in row order
  *            (deterministic); an expert with no rows gets dW[e] = 0.
  *            Rows >= offsets[E] are ignored.
- *   E, M, N, K, alignment and stream as for rg_mgemm (dW 16-byte aligned).
- *   M == 0 is valid and zeroes dW.
+ *   E 1 .. RG_KGEMM_MAX_EXPERTS; M, N, K, alignment and stream as for
+ *   rg_mgemm (dW 16-byte aligned).  M == 0 is valid and zeroes dW.
  */
 int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M,
              int N, int K, float* dW, cudaStream_t stream);

@@ -507,6 +507,7 @@ int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, i
                float* dW, int accumulate, cudaStream_t stream) {
   int rc = check_common(offsets, E, M, N, K);
   if (rc != RG_OK) return rc;
+  if (E > RG_KGEMM_MAX_EXPERTS) return RG_ERR_INVALID_ARG;
   if (dW == nullptr || !aligned16(dW)) return RG_ERR_INVALID_ARG;
   if (M > 0 && (grad == nullptr || X == nullptr || !aligned16(grad) || !aligned16(X)))
     return RG_ERR_INVALID_ARG;
@@ -515,7 +516,7 @@ int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, i
   if (tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != RG_OK) return rc;
-  if (rg::kgemm_smem_bytes(E, ds->max_smem) > ds->max_smem) return RG_ERR_INVALID_ARG;  // too many experts
+  if (rg::kgemm_smem_bytes(E) > ds->max_smem) return RG_ERR_INVALID_ARG;
 
   // With M == 0 every valid offsets vector is all zeros, so the kernel only
   // writes zero tiles; the operand maps then describe one row of dW, which is
@@ -545,7 +546,7 @@ int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, i
   }
   rg::GroupArgs args = group_args(ds, offsets, E, M, N, K, dW);
   args.accumulate = accumulate;
-  const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->kg_grid, ds->max_smem, stream);
+  const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->kg_grid, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
 }

@@ -97,7 +97,7 @@ inline int mgemm_b_box_rows(bool transpose_B, int N) { return mgemm_narrow(trans
 
 // Bytes of dynamic shared memory a launch with E experts needs.
 size_t mgemm_smem_bytes(int E);
-size_t kgemm_smem_bytes(int E, size_t max_smem);  // of the configuration a launch uses
+size_t kgemm_smem_bytes(int E);
 
 // One-time per-device kernel attribute setup: allow up to `max_smem` bytes
 // of dynamic shared memory (the device's opt-in limit).
@@ -124,7 +124,7 @@ cudaError_t launch_mgemm_swiglu_dgrad(const CUtensorMap& tmA, const CUtensorMap&
                                       const CUtensorMap& tmDy13, const GroupArgs& args, int grid,
                                       cudaStream_t stream);
 cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
-                         const GroupArgs& args, int grid, size_t max_smem, cudaStream_t stream);
+                         const GroupArgs& args, int grid, cudaStream_t stream);
 // MXFP8 Mgemm (FP8 E4M3 operands, E8M0 scales per 32 K elements in the
 // blocked layout) and the conversion of grouped scales to that layout.
 size_t mx_smem_bytes(int E);

@@ -38,6 +38,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "rg.h"
 
 namespace rg {
 namespace {
@@ -554,10 +555,11 @@ __global__ void wait_selftest_kernel(unsigned int* status, unsigned long long li
   __syncthreads();
 }
 
-// Stage counts: the deep ring when the shared-memory tables of E experts
-// still fit beside it, otherwise one stage less.
+// Ring depth.  The shared-memory tables of the experts sit beside it, which
+// bounds E (RG_KGEMM_MAX_EXPERTS in rg.h; the host rejects larger E).
 constexpr int kStagesDeep = kCtaGroup == 2 ? 6 : 4;
-constexpr int kStagesShallow = kStagesDeep - 1;
+static_assert(Cfg<kCtaGroup, kStagesDeep>::SMEM_FIXED + (2 * RG_KGEMM_MAX_EXPERTS + 1) * 4 <= 232448,
+              "the expert tables of RG_KGEMM_MAX_EXPERTS experts must fit beside the ring");
 
 template <int ST>
 size_t smem_bytes(int E) {
@@ -583,19 +585,12 @@ void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, s
 
 }  // namespace
 
-size_t kgemm_smem_bytes(int E, size_t max_smem) {
-  const size_t deep = smem_bytes<kStagesDeep>(E);
-  return deep <= max_smem ? deep : smem_bytes<kStagesShallow>(E);
-}
+size_t kgemm_smem_bytes(int E) { return smem_bytes<kStagesDeep>(E); }
 
 cudaError_t kgemm_setup(int max_smem) {
-  cudaError_t e = cudaFuncSetAttribute(
-      kgemm_kernel<kCtaGroup, kStagesDeep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      static_cast<int>(std::min<size_t>(smem_bytes<kStagesDeep>(RG_MAX_EXPERTS_CFG), max_smem)));
-  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(
-      kgemm_kernel<kCtaGroup, kStagesShallow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      static_cast<int>(std::min<size_t>(smem_bytes<kStagesShallow>(RG_MAX_EXPERTS_CFG), max_smem)));
+      kgemm_kernel<kCtaGroup, kStagesDeep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      static_cast<int>(std::min<size_t>(smem_bytes<kStagesDeep>(RG_KGEMM_MAX_EXPERTS), max_smem)));
 }
 
 cudaError_t kgemm_max_clusters(int* clusters, int max_smem) {
@@ -606,16 +601,11 @@ cudaError_t kgemm_max_clusters(int* clusters, int max_smem) {
 }
 
 cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
-                         const GroupArgs& args, int grid, size_t max_smem, cudaStream_t stream) {
+                         const GroupArgs& args, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  const size_t deep = smem_bytes<kStagesDeep>(args.E);
-  if (deep <= max_smem) {
-    fill_config(&cfg, attr, grid, deep, stream);
-    return cudaLaunchKernelEx(&cfg, kgemm_kernel<kCtaGroup, kStagesDeep>, tmG, tmX, tmD, args);
-  }
-  fill_config(&cfg, attr, grid, smem_bytes<kStagesShallow>(args.E), stream);
-  return cudaLaunchKernelEx(&cfg, kgemm_kernel<kCtaGroup, kStagesShallow>, tmG, tmX, tmD, args);
+  fill_config(&cfg, attr, grid, smem_bytes<kStagesDeep>(args.E), stream);
+  return cudaLaunchKernelEx(&cfg, kgemm_kernel<kCtaGroup, kStagesDeep>, tmG, tmX, tmD, args);
 }
 
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,

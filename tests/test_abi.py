@@ -92,7 +92,7 @@ def test_mgemm_swiglu_dgrad_rejects_bad_arguments(lib, args):
 @pytest.mark.parametrize(
     "args",
     [dict(grad=None), dict(X=None), dict(dW=None), dict(offsets=None), dict(dW=BAD),
-     dict(E=0), dict(N=7), dict(K=0), dict(M=-5)],
+     dict(E=0), dict(E=rg.RG_KGEMM_MAX_EXPERTS + 1), dict(N=7), dict(K=0), dict(M=-5)],
 )
 @pytest.mark.parametrize("fn", ["rg_kgemm", "rg_kgemm_acc"])
 def test_kgemm_rejects_bad_arguments(lib, args, fn):

@@ -271,3 +271,19 @@ def test_bounded_wait_times_out_with_status(gpu_lib):
     assert gpu_lib.device_status() == 0
     a = torch.ones(4, device="cuda")
     assert float(a.sum()) == 4.0
+
+
+def test_kgemm_most_experts(gpu_lib):
+    """RG_KGEMM_MAX_EXPERTS experts (the largest expert tables beside the
+    ring), most of them tiny or empty, against the oracle."""
+    E = gpu_lib.RG_KGEMM_MAX_EXPERTS
+    rng = np.random.default_rng(77)
+    counts = rng.integers(0, 6, size=E)
+    counts[[3, 200, E - 1]] = [400, 129, 64]
+    off = W.offsets_from_counts(counts)
+    M, N, K = int(off[-1]) + 3, 64, 72
+    g = W.normal_bf16((M, N), 1.0, 77, 0)
+    x = W.normal_bf16((M, K), 1.0, 77, 1)
+    dW = run_kgemm(gpu_lib, g, x, off, N, K)
+    check_fp32(dW, oracle.kgemm(g, x, off), f"kgemm E={E}")
+    assert (dW[np.flatnonzero(counts == 0)] == 0).all()
