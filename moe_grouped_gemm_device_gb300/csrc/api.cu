@@ -171,44 +171,10 @@ int check_common(const int32_t* offsets, int E, int64_t M, int N, int K) {
   return RG_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_t M, int N, int K,
-             int transpose_B, void* y, cudaStream_t stream) {
-  int rc = check_common(offsets, E, M, N, K);
-  if (rc != RG_OK) return rc;
-  if (w == nullptr || !aligned16(w)) return RG_ERR_INVALID_ARG;
-  if (M > 0 && (x == nullptr || y == nullptr || !aligned16(x) || !aligned16(y)))
-    return RG_ERR_INVALID_ARG;
-  // the tile list is indexed with 32-bit integers
-  const int64_t max_tiles = (M / rg::mg::TILE_M + E) * ((N + rg::mg::BN - 1) / rg::mg::BN);
-  if (max_tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
-  DeviceState* ds = nullptr;
-  if ((rc = device_state(&ds)) != RG_OK) return rc;
-  if (rg::mgemm_smem_bytes(E) > ds->max_smem) return RG_ERR_INVALID_ARG;  // too many experts
-  if (M == 0) return RG_OK;  // no rows, nothing to write
-
-  CUtensorMap tmA, tmB, tmY;
-  if (!encode_rows(&tmA, x, M, K, rg::mg::BM)) return RG_ERR_INVALID_ARG;
-  if (!transpose_B) {  // w [E, N, K], K contiguous: one 64 x BN_CTA box per stage and CTA
-    if (!encode_weight(&tmB, w, E, N, K, rg::mgemm_b_box_rows(false, N))) return RG_ERR_INVALID_ARG;
-  } else {  // w [E, K, N], N contiguous: 64-column boxes of 64 K rows
-    const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(E)};
-    const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K) * N * 2};
-    const uint32_t box[3] = {64, rg::mg::BK, 1};
-    if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box)) return RG_ERR_INVALID_ARG;
-  }
-  if (!encode_rows(&tmY, y, M, N, 32)) return RG_ERR_INVALID_ARG;
-  rg::GroupArgs args = group_args(ds, offsets, E, M, N, K, y);
-  const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmB, tmY, args, ds->mg_grid, stream);
-  if (e != cudaSuccess) return fail_cuda(e);
-  return RG_OK;
-}
-
-int rg_mgemm_nested(const void* x, const void* w, const int32_t* offsets, int O, int L, int64_t M, int N,
-                    int K, int transpose_B, void* y, cudaStream_t stream) {
+// The M-grouped GEMM of both entry points: O outer groups over the columns
+// of x and y (1 = plain Mgemm), L row groups.
+int mgemm_impl(const void* x, const void* w, const int32_t* offsets, int O, int L, int64_t M, int N, int K,
+               int transpose_B, void* y, cudaStream_t stream) {
   if (O < 1 || O > RG_MAX_OUTER) return RG_ERR_INVALID_ARG;
   int rc = check_common(offsets, L, M, N, K);
   if (rc != RG_OK) return rc;
@@ -218,12 +184,13 @@ int rg_mgemm_nested(const void* x, const void* w, const int32_t* offsets, int O,
   if (w == nullptr || !aligned16(w)) return RG_ERR_INVALID_ARG;
   if (M > 0 && (x == nullptr || y == nullptr || !aligned16(x) || !aligned16(y)))
     return RG_ERR_INVALID_ARG;
+  // the tile list is indexed with 32-bit integers
   const int64_t max_tiles = (M / rg::mg::TILE_M + L) * ((N + rg::mg::BN - 1) / rg::mg::BN) * O;
   if (max_tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != RG_OK) return rc;
-  if (rg::mgemm_smem_bytes(L) > ds->max_smem) return RG_ERR_INVALID_ARG;
-  if (M == 0) return RG_OK;
+  if (rg::mgemm_smem_bytes(L) > ds->max_smem) return RG_ERR_INVALID_ARG;  // too many groups
+  if (M == 0) return RG_OK;  // no rows, nothing to write
 
   // The weights of all (outer, inner) groups form one stack of O*L matrices.
   const int G = O * L;
@@ -243,9 +210,9 @@ int rg_mgemm_nested(const void* x, const void* w, const int32_t* offsets, int O,
     const uint32_t yb[3] = {64, 1, 32};
     if (!encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, yd, ys, yb)) return RG_ERR_INVALID_ARG;
   }
-  if (!transpose_B) {
+  if (!transpose_B) {  // w [G, N, K], K contiguous: one 64-wide K box of the tile's B rows per stage and CTA
     if (!encode_weight(&tmB, w, G, N, K, rg::mgemm_b_box_rows(false, N))) return RG_ERR_INVALID_ARG;
-  } else {
+  } else {  // w [G, K, N], N contiguous: 64-column boxes of 64 K rows
     const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(G)};
     const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K) * N * 2};
     const uint32_t box[3] = {64, rg::mg::BK, 1};
@@ -256,6 +223,20 @@ int rg_mgemm_nested(const void* x, const void* w, const int32_t* offsets, int O,
   const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmB, tmY, args, ds->mg_grid, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rg_mgemm(const void* x, const void* w, const int32_t* offsets, int E, int64_t M, int N, int K,
+             int transpose_B, void* y, cudaStream_t stream) {
+  return mgemm_impl(x, w, offsets, 1, E, M, N, K, transpose_B, y, stream);
+}
+
+int rg_mgemm_nested(const void* x, const void* w, const int32_t* offsets, int O, int L, int64_t M, int N,
+                    int K, int transpose_B, void* y, cudaStream_t stream) {
+  return mgemm_impl(x, w, offsets, O, L, M, N, K, transpose_B, y, stream);
 }
 
 int rg_mgemm_swiglu(const void* x, const void* w13, const int32_t* offsets, int E, int64_t M, int F,
