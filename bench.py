@@ -328,6 +328,23 @@ def traffic_for(kernel: str, op_names):
     return sum(per_op[o] for o in op_names) // len(op_names)
 
 
+def slowest_rank_ms(ms: float, dist, device) -> float:
+    """The timed region's length on the slowest rank (max over ranks; the
+    value itself with one process)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, ms_per_step: float, world: int) -> float:
+    """Whole-job TFLOP/s: every rank runs the same per-GPU step (expert-shard
+    replicas), so the job does world x the step's FLOPs per slowest step."""
+    return world * flops_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 class Unit:
     """One timed launch of the step: a grouped GEMM, or (MXFP8) the scale
     layout conversions that precede it."""
@@ -508,13 +525,10 @@ def main():
     for e in evs:
         per_unit_ms += np.array([e[i].elapsed_time(e[i + 1]) for i in range(nu)])
     per_unit_ms /= args.steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank_ms(ms, dist, dev)
     ms_per_step = ms / args.steps
     flops_step = wl.flops()
-    value = world * flops_step / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(flops_step, ms_per_step, world)
 
     # ---- end to end through the public API with host buffers ---------------
     # Every step copies its inputs from pinned host memory, runs the ops and
