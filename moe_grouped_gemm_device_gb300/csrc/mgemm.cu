@@ -172,6 +172,22 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
   const int T = s_pre[E] * O;
   if (worker >= T) return;  // same decision in both CTAs of a pair
 
+  // Half tiles: an expert's last row block with at most 128 rows runs as an
+  // M=128 pair MMA (64 rows per CTA) instead of an M=256 one with half of it
+  // padding.  Each CTA's 64 rows x 256 columns then sit in 128 tensor-memory
+  // columns: lanes 0..63 hold output columns 0..127, lanes 64..127 columns
+  // 128..255.  Plain epilogue, 256-column tiles, CTA pairs only.
+  constexpr bool HALF_TILES = EPI == kEpiPlain && BNT == 256 && CG == 2;
+  auto is_half = [&](int e, int local) {
+    if constexpr (!HALF_TILES) {
+      return false;
+    } else {
+      const int rows = s_off[e + 1] - s_off[e];
+      const int mt = local / nbn;
+      return mt == (rows - 1) / TILE_M && rows - mt * TILE_M <= BM;
+    }
+  };
+
   // ---- barriers and tensor memory -------------------------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -223,7 +239,8 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
         while (s_pre[e + 1] <= ti) ++e;
         const int local = ti - s_pre[e];
         const int eb = o * E + e;  // weight slot: w[o][e]
-        const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * BM;
+        // a half tile's rows are split 64 / 64 between the CTAs
+        const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * (is_half(e, local) ? BM / 2 : BM);
         // B rows this CTA loads: its half of the 256 output columns, or (SwiGLU)
         // the gate rows (CTA 0) / the matching up rows (CTA 1) of 128 features
         const int n0 = SWIGLU ? (local % nbn) * BN_CTA + static_cast<int>(rank) * F
@@ -270,11 +287,16 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
   } else if (warp == 1 && rank == 0) {
     // ================= MMA issuer (warp 1 of the issuing CTA) =================
     constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN, false, TRANS_B);
+    constexpr uint32_t IDESC_HALF = idesc_bf16_f32(TILE_M / 2, BN, false, TRANS_B);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     bool ok = true;
+    int e = 0;
     for (int t = worker; t < T; t += nworkers, ++acc) {
+      const int ti = t / O;
+      while (s_pre[e + 1] <= ti) ++e;
+      const uint32_t idesc = is_half(e, ti - s_pre[e]) ? IDESC_HALF : IDESC;
       const int buf = acc & 1;
       const uint32_t tph = (acc >> 1) & 1;
       ok = __all_sync(0xffffffffu, wait_pair(tempty_bar(buf), tph ^ 1u));
@@ -293,7 +315,7 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
             const uint64_t ad = sdesc_sw128(sa + 32 * k, 16, 1024);
             const uint64_t bd = TRANS_B ? sdesc_sw128(sb + 2048 * k, 8192, 1024)
                                         : sdesc_sw128(sb + 32 * k, 16, 1024);
-            umma_bf16<CG>(d_tmem, ad, bd, IDESC, (kb | k) != 0);
+            umma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
           umma_commit<CG>(empty_bar(stage));  // frees the stage (in both CTAs) once these MMAs finish
         }
@@ -341,10 +363,11 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
     // masked 16-byte stores of the valid rows and columns.  With outer groups
     // the map is 3-D (o selects the column block) and `out` already points
     // at column block o of a row of length ld.
+    int wrow = q * 32;  // first row (within this CTA's rows of the tile) of this warp's lanes
     auto emit = [&](const uint32_t (&p)[32], const CUtensorMap* map, __nv_bfloat16* out, int ld,
                     int row0, int rows_valid, int col0, int col_limit) {
       if (col0 >= col_limit) return;
-      if (q * 32 + 32 <= rows_valid && col0 + 64 <= col_limit) {
+      if (wrow + 32 <= rows_valid && col0 + 64 <= col_limit) {
         if (lane == 0) bulk_wait_read<0>();  // previous store has left the buffer
         __syncwarp();
         uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * 128);
@@ -354,12 +377,12 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if (O == 1) tma_store_2d(map, ebuf_s, col0, row0 + q * 32);
-          else tma_store_3d(map, ebuf_s, col0, o, row0 + q * 32);
+          if (O == 1) tma_store_2d(map, ebuf_s, col0, row0 + wrow);
+          else tma_store_3d(map, ebuf_s, col0, o, row0 + wrow);
           bulk_commit();
         }
-      } else if (r_in_cta < rows_valid) {
-        uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<int64_t>(row0 + r_in_cta) * ld + col0));
+      } else if (wrow + lane < rows_valid) {
+        uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<int64_t>(row0 + wrow + lane) * ld + col0));
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           if (col0 + 8 * j < col_limit) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
@@ -372,13 +395,17 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
       o = t - ti * O;
       while (s_pre[e + 1] <= ti) ++e;
       const int local = ti - s_pre[e];
-      const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * BM;
-      const int rows_valid = min(BM, s_off[e + 1] - row0);  // <= 0: this CTA's half is past the expert
+      const bool half = is_half(e, local);
+      const int cta_rows = half ? BM / 2 : BM;  // rows of the tile this CTA holds
+      const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * cta_rows;
+      const int rows_valid = min(cta_rows, s_off[e + 1] - row0);  // <= 0: this CTA's part is past the expert
+      // a half tile's lane quarter q holds rows 32 (q % 2) .. and columns 128 (q / 2) ..
+      wrow = half ? (q & 1) * 32 : q * 32;
       const int buf = acc & 1;
       const uint32_t tph = (acc >> 1) & 1;
       if (!__all_sync(0xffffffffu, wait_pair(tfull_bar(buf), tph))) break;
       tc_fence_after();
-      if (q * 32 >= rows_valid) {  // none of this warp's rows belong to the expert
+      if (wrow >= rows_valid) {  // none of this warp's rows belong to the expert
         release_acc(buf);
         continue;
       }
@@ -433,14 +460,18 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
           if (col0 + 64 >= N) break;
         }
       } else if constexpr (!SWIGLU) {
-        const int n0 = (local % nbn) * BN;
+        // chunk c: tensor-memory columns 64c.., output columns n0 + 64c.. (full
+        // tile) or n0 + 128 (q / 2) + 64c.. (half tile, 128 columns per lane quarter)
+        const int n0 = (local % nbn) * BN + (half ? (q >> 1) * 128 : 0);
+        const int nch = half ? CH / 2 : CH;
+        const int cf = half ? c_first / 2 : c_first;
 #pragma unroll 1
-        for (int c = c_first; c < c_first + CH; ++c) {
+        for (int c = cf; c < cf + nch; ++c) {
           uint32_t v0[32], v1[32];
           tmem_ld_32x32b_x32(taddr + 64 * c, v0);
           tmem_ld_32x32b_x32(taddr + 64 * c + 32, v1);
           tmem_ld_wait();
-          if (c == c_first + CH - 1) release_acc(buf);
+          if (c == cf + nch - 1) release_acc(buf);
           uint32_t p[32];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
