@@ -506,18 +506,22 @@ int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, i
   const void* x_ptr = M > 0 ? X : static_cast<const void*>(dW);
   const uint64_t rows = M > 0 ? static_cast<uint64_t>(M) : 1;
 
+  // Operands as 3-D views {cols, i < BR, j}: element (c, i, j) is row j + i,
+  // so a box starting at i = v - BR < 0 zero-fills its leading BR - v rows
+  // (an expert's ragged last block).  Every element the kernel reads lies in
+  // rows offsets[e] .. offsets[e+1]-1 of some expert.
   CUtensorMap tmG, tmX, tmD;
   {
-    const uint64_t dims[2] = {static_cast<uint64_t>(N), rows};
-    const uint64_t str[1] = {static_cast<uint64_t>(N) * 2};
-    const uint32_t box[2] = {64, rg::kg::BR};
-    if (!encode(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g_ptr, dims, str, box)) return RG_ERR_INVALID_ARG;
+    const uint64_t dims[3] = {static_cast<uint64_t>(N), rg::kg::BR, rows};
+    const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(N) * 2};
+    const uint32_t box[3] = {64, rg::kg::BR, 1};
+    if (!encode(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, g_ptr, dims, str, box)) return RG_ERR_INVALID_ARG;
   }
   {
-    const uint64_t dims[2] = {static_cast<uint64_t>(K), rows};
-    const uint64_t str[1] = {static_cast<uint64_t>(K) * 2};
-    const uint32_t box[2] = {64, rg::kg::BR};
-    if (!encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x_ptr, dims, str, box)) return RG_ERR_INVALID_ARG;
+    const uint64_t dims[3] = {static_cast<uint64_t>(K), rg::kg::BR, rows};
+    const uint64_t str[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(K) * 2};
+    const uint32_t box[3] = {64, rg::kg::BR, 1};
+    if (!encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x_ptr, dims, str, box)) return RG_ERR_INVALID_ARG;
   }
   {
     const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};

@@ -16,14 +16,16 @@
 //     X[r:r+64, k0+128r : +128] (its half of B); both are N/K-contiguous, i.e.
 //     MN-major operands.  32 KB per stage and CTA, six stages.  CG = 1: one
 //     CTA, 128x256 tiles, four 48 KB stages.
-//   * The copies of both CTAs complete their bytes directly on the issuing
-//     CTA's stage barrier (.cta_group::2).  Rows of an expert's last block that
-//     lie past its end belong to the next expert: only the 16-row MMA steps
-//     holding valid rows are issued, and the (at most 15) foreign rows of the
-//     last step are zeroed in both operands, so no NaN/Inf can leak.  That
-//     block lands on each CTA's own barrier: the issuing CTA's MMA warp zeroes
-//     its rows, warp 1 of the peer CTA zeroes the peer's and then arrives on
-//     the issuing CTA's ready barrier (one cluster arrive per ragged block).
+//   * Both operands are read through 3-D views {columns, i < 64, j} of the
+//     row-major tensors in which element (c, i, j) is row i + j (both row
+//     strides equal the pitch).  A full block loads box (c, 0, r): rows
+//     r .. r+63.  An expert's ragged last block of v < 64 rows loads box
+//     (c, v-64, r): its first 64-v rows have i < 0 and are zero-filled by the
+//     copy engine, the expert's rows r .. r+v-1 land in the last v rows, and
+//     no row past the expert is read.  The MMAs skip the leading all-zero
+//     16-row steps.  So no block needs fixing up in shared memory, and the
+//     copies of both CTAs complete their bytes on the issuing CTA's stage
+//     barrier (.cta_group::2) for every block alike.
 //   * The fp32 accumulator (128 lanes x 256 columns per CTA, double-buffered
 //     in tensor memory) holds at most CHUNK_ROWS rows of one expert: a longer
 //     expert is summed chunk by chunk, the first chunk's partial stored to dW
@@ -61,8 +63,8 @@ struct Cfg {
   // warps 2..9: epilogue
   static constexpr int PRODUCER2 = 2 + EPI_WARPS;
   static constexpr int THREADS = 32 * (PRODUCER2 + 1);
-  // full[S], empty[S], ready[S], tfull[2], tempty[2], drain
-  static constexpr int NUM_BARS = 3 * STAGES + 5;
+  // full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
   // The dynamic shared-memory window of a CTA without static shared memory
   // starts 1024-byte aligned; the kernel checks this instead of padding.
   static constexpr int SMEM_FIXED =
@@ -100,10 +102,9 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto ready_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 4);
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -147,7 +148,6 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
-      mbar_init(ready_bar(s), 1);  // the peer CTA's half of a ragged block is zeroed
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -189,21 +189,6 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     e = s_ord[pe];
     local = p - pe * tpe;
   };
-  // Zero rows [lo, hi) of every box of `stage` in this CTA (whole 128-byte
-  // rows, so the swizzle does not matter) and publish the writes to the async
-  // proxy.
-  auto zero_rows = [&](int stage, int lo, int hi) {
-    uint8_t* st = smem + stage * STAGE_BYTES;
-    const int units = (hi - lo) * 8;  // 16-byte units per box
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 1
-    for (int b = 0; b < STAGE_BYTES / BOX_BYTES; ++b) {
-      uint4* bp = reinterpret_cast<uint4*>(st + b * BOX_BYTES + lo * 128);
-      for (int u = lane; u < units; u += 32) bp[u] = z;
-    }
-    fence_proxy_async_smem();
-  };
-
   if (warp == 0 || warp == C::PRODUCER2) {
     // ============ TMA producers (lane 0 of warp 0 and of the last warp) =====
     // One thread issuing every copy caps the copy rate of a CTA below what
@@ -216,8 +201,7 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
       uint32_t it = 0;
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0, armed_par = 0;
-      uint32_t own_par = 0;  // peer CTA: parity of the next phase of each own full barrier
+      uint32_t armed = 0, armed_par = 0;  // issuing CTA: stages armed, and their parities
       const uint32_t full_issuer = CG == 2 ? mapa_shared(full_bar(0), 0) : full_bar(0);
       bool ok = true;
       for (int t = worker; t < T && ok; t += nworkers) {
@@ -227,9 +211,7 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         const int k0 = (local % nbk) * BN + static_cast<int>(rank) * BN_CTA;
         const int r_begin = s_off[e], r_end = s_off[e + 1];
         for (int r = r_begin; r < r_end; r += BR) {
-          const bool tail = r + BR > r_end;
           if ((it++ & 1u) != pid) {  // the other producer's stage
-            if (rank != 0 && tail) own_par ^= 1u << stage;
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -242,34 +224,19 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
           }
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
-          // A full block: both CTAs' copies complete on the issuing CTA's full
-          // barrier, which expects the bytes of the whole pair.  The expert's
-          // ragged last block: each CTA's copies complete on its own full
-          // barrier, so each CTA can zero its foreign rows once they landed.
-          if (CG == 1 || tail) {
-            const uint32_t fb = full_bar(stage);
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          // i0 < 0 for the expert's ragged last block: its leading -i0 rows
+          // are zero-filled and its last rows are r .. r_end-1.
+          const int i0 = min(0, r_end - r - BR);
+          const uint32_t fb = full_issuer + 8u * stage;
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES * CG);
 #pragma unroll
-            for (int j = 0; j < BM / 64; ++j) tma_load_2d(sa + j * BOX_BYTES, &tmG, fb, n0 + 64 * j, r);
+          for (int j = 0; j < BM / 64; ++j) tma_load_3d_cg<CG>(sa + j * BOX_BYTES, &tmG, fb, n0 + 64 * j, i0, r);
 #pragma unroll
-            for (int j = 0; j < BN_CTA / 64; ++j) tma_load_2d(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, r);
-          } else {
-            const uint32_t fb = full_issuer + 8u * stage;
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES * CG);
-#pragma unroll
-            for (int j = 0; j < BM / 64; ++j) tma_load_2d_cg<CG>(sa + j * BOX_BYTES, &tmG, fb, n0 + 64 * j, r);
-#pragma unroll
-            for (int j = 0; j < BN_CTA / 64; ++j)
-              tma_load_2d_cg<CG>(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, r);
-          }
-          // parity of the phase just armed on this CTA's own full barrier: it
-          // advances with every use in the issuing CTA, only with ragged
-          // blocks in the peer
-          if (rank == 0 || tail) {
-            const uint32_t par = rank == 0 ? phase : (own_par >> stage) & 1u;
+          for (int j = 0; j < BN_CTA / 64; ++j)
+            tma_load_3d_cg<CG>(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, i0, r);
+          if (rank == 0) {
             armed |= 1u << stage;
-            armed_par = (armed_par & ~(1u << stage)) | (par << stage);
-            if (rank != 0) own_par ^= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -288,63 +255,8 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN, true, true);
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t ready_par = 0;  // parity of the next phase of each ready barrier (ragged blocks only)
     int acc = 0;
     bool ok = true;
-    // Issue the MMAs of one stage: the first `ksteps` 16-row steps into the
-    // accumulator at column d_tmem, then free the stage.
-    auto issue = [&](int st, uint32_t d_tmem, int ksteps, bool fresh) {
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sa = sbase + st * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-        for (int k = 0; k < BR / 16; ++k) {
-          if (k < ksteps) {
-            const uint64_t ad = sdesc_sw128(sa + 2048 * k, BOX_BYTES, 1024);
-            const uint64_t bd = sdesc_sw128(sb + 2048 * k, BOX_BYTES, 1024);
-            umma_bf16<CG>(d_tmem, ad, bd, IDESC, (!fresh) | (k != 0));
-          }
-        }
-        umma_commit<CG>(empty_bar(st));
-      }
-      __syncwarp();
-    };
-    // A ragged last block (rows past the expert inside its last 16-row step
-    // are zeroed: here for this CTA, by warp 1 of the peer for its half, which
-    // then arrives on `ready`).  With CTA pairs the peer's hand-shake is not
-    // waited for on the spot: the block is kept pending while the next
-    // tile's blocks are issued into the other accumulator, and completed as
-    // soon as it is ready -- at the latest before the ring comes back to its
-    // stage or its accumulator is needed again.
-    bool pend = false;
-    int p_stage = 0, p_valid = 0, p_buf = 0;
-    uint32_t p_phase = 0;
-    bool p_fresh = false;
-    auto finish_ragged = [&](int st, uint32_t par, int valid, int buf, bool fresh) {
-      const int ksteps = (valid + 15) / 16;
-      if (valid < 16 * ksteps) zero_rows(st, valid, 16 * ksteps);
-      __syncwarp();
-      issue(st, tmem + buf * BN, ksteps, fresh);
-      if (lane == 0) umma_commit<CG>(tfull_bar(buf));  // the ragged block ends its accumulator
-      __syncwarp();
-    };
-    // Complete the pending block; `block` = wait for it, else only if ready now.
-    auto resolve = [&](bool block) -> bool {
-      if (!pend) return true;
-      const uint32_t rbit = (ready_par >> p_stage) & 1u;
-      if (block) {
-        if (!__all_sync(0xffffffffu, wait_pair(full_bar(p_stage), p_phase))) return false;
-        if (!__all_sync(0xffffffffu, wait_pair(ready_bar(p_stage), rbit))) return false;
-      } else if (!__all_sync(0xffffffffu, mbar_try_wait_cluster(full_bar(p_stage), p_phase) &&
-                                              mbar_try_wait_cluster(ready_bar(p_stage), rbit))) {
-        return true;
-      }
-      ready_par ^= 1u << p_stage;
-      finish_ragged(p_stage, p_phase, p_valid, p_buf, p_fresh);
-      pend = false;
-      return true;
-    };
     for (int t = worker; t < T && ok; t += nworkers) {
       int e, local;
       tile_at(t, e, local);
@@ -355,83 +267,48 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         const int c_end = min(r_end, cr + CHUNK_ROWS);
         const int buf = acc & 1;
         const uint32_t tph = (acc >> 1) & 1;
-        if (pend && p_buf == buf && !(ok = resolve(true))) break;  // its accumulator is needed again
         ok = __all_sync(0xffffffffu, wait_pair(tempty_bar(buf), tph ^ 1u));
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + buf * BN;
-        bool deferred = false;
         for (int r = cr; r < c_end; r += BR) {
-          // the ring is back at the pending block's stage: finish it first
-          ok = resolve(pend && p_stage == stage);
+          ok = __all_sync(0xffffffffu, wait_pair(full_bar(stage), phase));
           if (!ok) break;
-          const int valid = min(BR, r_end - r);
-          if (CG == 2 && valid < BR) {
-            if (pend && !(ok = resolve(true))) break;  // one pending block at a time
-            pend = true;
-            p_stage = stage;
-            p_phase = phase;
-            p_valid = valid;
-            p_buf = buf;
-            p_fresh = r == cr;
-            deferred = true;
-          } else {
-            ok = __all_sync(0xffffffffu, wait_pair(full_bar(stage), phase));
-            if (!ok) break;
-            const int ksteps = (valid + 15) / 16;
-            if (valid < 16 * ksteps) {  // single CTA: zero the foreign rows here
-              zero_rows(stage, valid, 16 * ksteps);
-              __syncwarp();
+          tc_fence_after();
+          if (lane == 0) {
+            // the expert's ragged last block starts with all-zero 16-row steps
+            const int k_first = max(0, r + BR - r_end) / 16;
+            const uint32_t sa = sbase + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BR / 16; ++k) {
+              if (k >= k_first) {
+                const uint64_t ad = sdesc_sw128(sa + 2048 * k, BOX_BYTES, 1024);
+                const uint64_t bd = sdesc_sw128(sb + 2048 * k, BOX_BYTES, 1024);
+                umma_bf16<CG>(d_tmem, ad, bd, IDESC, (r != cr) | (k != k_first));
+              }
             }
-            issue(stage, d_tmem, ksteps, r == cr);
+            umma_commit<CG>(empty_bar(stage));
           }
+          __syncwarp();
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        if (!deferred) {
-          if (lane == 0) umma_commit<CG>(tfull_bar(buf));
-          __syncwarp();
-        }
+        if (lane == 0) umma_commit<CG>(tfull_bar(buf));
+        __syncwarp();
         ++acc;
       }
     }
-    if (ok) ok = resolve(true);
     if (!ok && lane == 0) {
       umma_commit_local<CG>(drain_bar);
       mbar_wait_drain(drain_bar, 0, guard.limit_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ============ peer CTA of a pair: zero its half of ragged blocks =========
-    // Each expert's ragged last block lands on this CTA's own full barrier
-    // (which completes only for such blocks, in order); zero the foreign rows
-    // of its last 16-row MMA step in both operands, then tell the issuing CTA.
-    int stage = 0;
-    uint32_t own_par = 0;  // parity of the next phase of each own full barrier
-    bool ok = true;
-    const uint32_t ready_issuer = mapa_shared(ready_bar(0), 0);
-    for (int t = worker; t < T && ok; t += nworkers) {
-      int e, local;
-      tile_at(t, e, local);
-      const int r_begin = s_off[e], r_end = s_off[e + 1];
-      for (int r = r_begin; r < r_end; r += BR) {
-        const int valid = min(BR, r_end - r);
-        if (valid < BR) {
-          ok = __all_sync(0xffffffffu, mbar_wait(guard, full_bar(stage), (own_par >> stage) & 1u));
-          if (!ok) break;
-          own_par ^= 1u << stage;
-          const int ksteps = (valid + 15) / 16;
-          if (valid < 16 * ksteps) zero_rows(stage, valid, 16 * ksteps);
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(ready_issuer + 8u * stage);
-          __syncwarp();
-        }
-        if (++stage == STAGES) stage = 0;
-      }
-    }
+    // peer CTA of a pair: its tensor cores are driven by the issuing CTA
   } else {
     // ======================= epilogue (warps 2..9) ===========================
     // Warp w owns TMEM lane quarter q = w % 4 (dW rows n0 + 32q .. +31 of this

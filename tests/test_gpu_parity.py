@@ -70,6 +70,39 @@ def test_kgemm_integer_inputs_bit_exact(gpu_lib):
     assert (dW[1] == 0).all()
 
 
+def test_kgemm_ragged_blocks_at_both_ends_bit_exact(gpu_lib):
+    """Ragged last blocks of every kind: the first expert's only block starts
+    at row 0, blocks of 1, 15, 16, 17, 63 and 65 rows, and the last expert ends
+    at the last row of the operands (no rows past offsets[E])."""
+    counts = [5, 1, 15, 16, 17, 0, 63, 65, 3]
+    off = W.offsets_from_counts(counts)
+    M, N, K = int(off[-1]), 320, 384
+    g = ints((M, N), 7, 0)
+    x = ints((M, K), 7, 1)
+    dW = run_kgemm(gpu_lib, g, x, off, N, K)
+    np.testing.assert_array_equal(dW.astype(np.float64), oracle.kgemm(g, x, off))
+
+
+def test_kgemm_nonfinite_rows_stay_in_their_expert(gpu_lib):
+    """Inf and NaN in one expert's rows of grad and X reach only that expert's
+    dW: the neighbouring experts' ragged blocks never contract them."""
+    counts = [37, 50, 70, 9]
+    off = W.offsets_from_counts(counts)
+    M, N, K = int(off[-1]), 256, 256
+    g = ints((M, N), 8, 0)
+    x = ints((M, K), 8, 1)
+    lo, hi = int(off[1]), int(off[2])
+    g[lo, 3] = 0x7F80       # +Inf (bf16 bits)
+    g[hi - 1, 5] = 0x7FC0   # NaN
+    x[lo + 1, 7] = 0xFF80   # -Inf
+    x[hi - 1, 0] = 0x7FC0
+    dW = run_kgemm(gpu_lib, g, x, off, N, K)
+    ref = oracle.kgemm(g, x, off)
+    for e in (0, 2, 3):
+        np.testing.assert_array_equal(dW[e].astype(np.float64), ref[e])
+    assert not np.isfinite(dW[1]).all()
+
+
 def test_kgemm_long_experts_bit_exact(gpu_lib):
     """Experts longer than one accumulation chunk (4096 rows): the partial
     sums folded into dW must reproduce the exact integer result."""
