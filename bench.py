@@ -521,10 +521,12 @@ def main():
     status = rg.device_status()
     if status:
         raise SystemExit(f"device status {status:#x} after timed region")
-    per_unit_ms = np.zeros(nu)
-    for e in evs:
-        per_unit_ms += np.array([e[i].elapsed_time(e[i + 1]) for i in range(nu)])
-    per_unit_ms /= args.steps
+    # [steps, units] launch durations; the mean feeds the throughput and the
+    # roofline, the median and best decile (10th percentile of the duration)
+    # describe the spread
+    unit_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(nu)] for e in evs])
+    per_unit_ms = unit_ms.mean(axis=0)
+    step_ms = unit_ms.sum(axis=1)
     ms = slowest_rank_ms(ms, dist, dev)
     ms_per_step = ms / args.steps
     flops_step = wl.flops()
@@ -610,10 +612,14 @@ def main():
         ent["launches"] += 1
         ent["ops"].append(u.name)
         sec = per_unit_ms[i] * 1e-3
-        rec = {"ms": round(float(per_unit_ms[i]), 4), "algorithmic_gbs": round(u.bytes / sec / 1e9, 1)}
+        med, p10 = float(np.median(unit_ms[:, i])), float(np.percentile(unit_ms[:, i], 10))
+        rec = {"ms": round(float(per_unit_ms[i]), 4), "ms_median": round(med, 4), "ms_best_decile": round(p10, 4),
+               "algorithmic_gbs": round(u.bytes / sec / 1e9, 1)}
         if u.flops:
             pk = tensor_peak(u.kernel, peaks)
             rec["tflops"] = round(u.flops / sec / 1e12, 1)
+            rec["tflops_median"] = round(u.flops / (med * 1e-3) / 1e12, 1)
+            rec["tflops_best_decile"] = round(u.flops / (p10 * 1e-3) / 1e12, 1)
             rec["pct_peak_sustained"] = round(100 * u.flops / sec / 1e12 / pk, 1)
         per_op[u.name] = rec
     dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
@@ -655,6 +661,8 @@ def main():
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5),
+        "step_ms_median": round(float(np.median(step_ms)), 5),
+        "step_ms_best_decile": round(float(np.percentile(step_ms, 10)), 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
