@@ -6,7 +6,7 @@ of the grouped-GEMM arithmetic, so both the CPU oracle (``oracle/``) and the
 CUDA path (``moe_grouped_gemm_device_gb300``) can take their inputs from it
 without sharing any of the method's code.
 
-Conventions (the readings behind them are listed in the design doc):
+Conventions:
 
 * Offsets are int32 ``[E+1]`` with a leading zero: expert ``e`` owns rows
   ``offsets[e] .. offsets[e+1]-1`` (RapidGEMM README, "Kernels": ``cnt`` is
