@@ -328,6 +328,9 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     const uint32_t ebuf_s = smem_u32(ebuf);
     uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * 128);
     const uint32_t tempty_issuer = CG == 2 ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+    // dW is written once and never read here: first out of L2, so that the
+    // operand rows other tiles of the expert still need stay resident
+    const uint64_t dw_policy = l2_policy_evict_first();
     int acc = 0;
     bool ok = true;
     auto stage_box = [&](const uint32_t* v) {
@@ -396,9 +399,9 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
           stage_box(v + 32 * c);
           if (lane == 0) {
             if (overwrite)
-              tma_store_3d(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e);
+              tma_store_3d_hint(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e, dw_policy);
             else
-              tma_reduce_add_3d(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e);
+              tma_reduce_add_3d_hint(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e, dw_policy);
             bulk_commit();
           }
         }
