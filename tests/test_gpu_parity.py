@@ -115,6 +115,19 @@ def test_kgemm_long_experts_bit_exact(gpu_lib):
     np.testing.assert_array_equal(dW.astype(np.float64), oracle.kgemm(g, x, off))
 
 
+def test_kgemm_several_rounds_bit_exact(gpu_lib):
+    """More tiles than CTA pairs (160 tiles: E=8 x 5 row blocks x 4 column
+    blocks), so tiles of later rounds walk their expert's rows in the other
+    direction; multi-chunk, ragged, single-row and empty experts included."""
+    counts = [9000, 37, 0, 4100, 130, 1, 5000, 64]
+    off = W.offsets_from_counts(counts)
+    M, N, K = int(off[-1]) + 3, 1280, 1024
+    g = ints((M, N), 9, 0)
+    x = ints((M, K), 9, 1)
+    dW = run_kgemm(gpu_lib, g, x, off, N, K)
+    np.testing.assert_array_equal(dW.astype(np.float64), oracle.kgemm(g, x, off))
+
+
 def test_kgemm_long_experts_random(gpu_lib):
     counts = [12000, 5000, 4096, 4097]
     off = W.offsets_from_counts(counts)
