@@ -194,9 +194,10 @@ int mgemm_impl(const void* x, const void* w, const int32_t* offsets, int O, int 
 
   // The weights of all (outer, inner) groups form one stack of O*L matrices.
   const int G = O * L;
-  CUtensorMap tmA, tmB, tmY;
+  CUtensorMap tmA, tmAh, tmB, tmY;
   if (O == 1) {
     if (!encode_rows(&tmA, x, M, K, rg::mg::BM)) return RG_ERR_INVALID_ARG;
+    if (!encode_rows(&tmAh, x, M, K, rg::mg::BM / 2)) return RG_ERR_INVALID_ARG;
     if (!encode_rows(&tmY, y, M, N, 32)) return RG_ERR_INVALID_ARG;
   } else {
     // x [M, O*K] as {K, O, M}; y [M, O*N] as {N, O, M}: one outer group's
@@ -205,6 +206,8 @@ int mgemm_impl(const void* x, const void* w, const int32_t* offsets, int O, int 
     const uint64_t xs[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(O) * K * 2};
     const uint32_t xb[3] = {64, 1, rg::mg::BM};
     if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, xd, xs, xb)) return RG_ERR_INVALID_ARG;
+    const uint32_t xbh[3] = {64, 1, rg::mg::BM / 2};
+    if (!encode(&tmAh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, xd, xs, xbh)) return RG_ERR_INVALID_ARG;
     const uint64_t yd[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(O), static_cast<uint64_t>(M)};
     const uint64_t ys[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(O) * N * 2};
     const uint32_t yb[3] = {64, 1, 32};
@@ -220,7 +223,7 @@ int mgemm_impl(const void* x, const void* w, const int32_t* offsets, int O, int 
   }
   rg::GroupArgs args = group_args(ds, offsets, L, M, N, K, y);
   args.outer = O;
-  const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmB, tmY, args, ds->mg_grid, stream);
+  const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmAh, tmB, tmY, args, ds->mg_grid, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
 }

@@ -108,8 +108,11 @@ cudaError_t kgemm_setup(int max_smem);
 cudaError_t mgemm_max_clusters(int* clusters, int max_smem);
 cudaError_t kgemm_max_clusters(int* clusters, int max_smem);
 
-cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                         const CUtensorMap& tmY, const GroupArgs& args, int grid,
+// tmA: x with boxes of 128 rows; tmAh: the same tensor with boxes of 64 rows
+// (an expert's last row block of at most 128 rows, split 64 / 64 between the
+// CTAs of a pair).
+cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmAh,
+                         const CUtensorMap& tmB, const CUtensorMap& tmY, const GroupArgs& args, int grid,
                          cudaStream_t stream);
 // Forward gate-up GEMM with the SwiGLU activation in the epilogue: B = w13
 // [E, 2F, K] (gate rows then up rows), args.N = 2F, tmH/args.out = h [M, F],

@@ -88,7 +88,8 @@ constexpr int kEpiPlain = 0, kEpiSwiglu = 1, kEpiSwigluBwd = 2;
 
 template <bool TRANS_B, int CG, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4>
 __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
-    mgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    mgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAh,
+                 const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmY2,
                  const GroupArgs args) {
   constexpr bool SWIGLU = EPI == kEpiSwiglu;
@@ -225,6 +226,7 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
     // whole (tile, k-block) sequence and fills every other stage.
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
+      if constexpr (HALF_TILES) tma_prefetch_desc(&tmAh);
       tma_prefetch_desc(&tmB);
       const uint32_t pid = warp == 0 ? 0u : 1u;
       uint32_t it = 0;
@@ -239,8 +241,12 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
         while (s_pre[e + 1] <= ti) ++e;
         const int local = ti - s_pre[e];
         const int eb = o * E + e;  // weight slot: w[o][e]
-        // a half tile's rows are split 64 / 64 between the CTAs
-        const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * (is_half(e, local) ? BM / 2 : BM);
+        // a half tile's rows are split 64 / 64 between the CTAs, each loading
+        // its 64 rows of A through the 64-row map
+        const bool half = is_half(e, local);
+        const CUtensorMap* am = half ? &tmAh : &tmA;
+        const uint32_t stage_tx = (half ? STAGE_BYTES - A_BYTES / 2 : STAGE_BYTES) * CG;
+        const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * (half ? BM / 2 : BM);
         // B rows this CTA loads: its half of the 256 output columns, or (SwiGLU)
         // the gate rows (CTA 0) / the matching up rows (CTA 1) of 128 features
         const int n0 = SWIGLU ? (local % nbn) * BN_CTA + static_cast<int>(rank) * F
@@ -256,9 +262,9 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
             const uint32_t fb = full_issuer + 8u * stage;
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_BYTES;
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES * CG);
-            if (O == 1) tma_load_2d_cg<CG>(sa, &tmA, fb, kb * BK, row0);
-            else tma_load_3d_cg<CG>(sa, &tmA, fb, kb * BK, o, row0);
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), stage_tx);
+            if (O == 1) tma_load_2d_cg<CG>(sa, am, fb, kb * BK, row0);
+            else tma_load_3d_cg<CG>(sa, am, fb, kb * BK, o, row0);
             if constexpr (!TRANS_B) {
               tma_load_3d_cg<CG>(sb, &tmB, fb, kb * BK, n0, eb);
             } else {
@@ -560,12 +566,13 @@ void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, s
 }
 
 template <bool TB, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4>
-cudaError_t launch_variant(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
-                           const CUtensorMap& tmY2, const GroupArgs& args, int grid, cudaStream_t stream) {
+cudaError_t launch_variant(const CUtensorMap& tmA, const CUtensorMap& tmAh, const CUtensorMap& tmB,
+                           const CUtensorMap& tmY, const CUtensorMap& tmY2, const GroupArgs& args, int grid,
+                           cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   fill_config(&cfg, attr, grid, smem_of<BNT, EPIW>(args.E), Cfg<kCtaGroup, BNT, EPIW>::THREADS, stream);
-  return cudaLaunchKernelEx(&cfg, mgemm_kernel<TB, kCtaGroup, EPI, BNT, EPIW>, tmA, tmB, tmY, tmY2, args);
+  return cudaLaunchKernelEx(&cfg, mgemm_kernel<TB, kCtaGroup, EPI, BNT, EPIW>, tmA, tmAh, tmB, tmY, tmY2, args);
 }
 
 }  // namespace
@@ -596,19 +603,20 @@ cudaError_t mgemm_max_clusters(int* clusters, int max_smem) {
   return cudaOccupancyMaxActiveClusters(clusters, mgemm_kernel<false, kCtaGroup>, &cfg);
 }
 
-cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                         const CUtensorMap& tmY, const GroupArgs& args, int grid,
+cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmAh,
+                         const CUtensorMap& tmB, const CUtensorMap& tmY, const GroupArgs& args, int grid,
                          cudaStream_t stream) {
   if constexpr (kCtaGroup == 2) {
     if (mgemm_narrow(transpose_B != 0, args.N))
-      return launch_variant<false, kEpiPlain, 64, 4>(tmA, tmB, tmY, tmY, args, grid, stream);
+      return launch_variant<false, kEpiPlain, 64, 4>(tmA, tmAh, tmB, tmY, tmY, args, grid, stream);
     if (mgemm_wide_epilogue(args.K)) {
-      if (transpose_B) return launch_variant<true, kEpiPlain, 256, 8>(tmA, tmB, tmY, tmY, args, grid, stream);
-      return launch_variant<false, kEpiPlain, 256, 8>(tmA, tmB, tmY, tmY, args, grid, stream);
+      if (transpose_B)
+        return launch_variant<true, kEpiPlain, 256, 8>(tmA, tmAh, tmB, tmY, tmY, args, grid, stream);
+      return launch_variant<false, kEpiPlain, 256, 8>(tmA, tmAh, tmB, tmY, tmY, args, grid, stream);
     }
   }
-  if (transpose_B) return launch_variant<true>(tmA, tmB, tmY, tmY, args, grid, stream);
-  return launch_variant<false>(tmA, tmB, tmY, tmY, args, grid, stream);
+  if (transpose_B) return launch_variant<true>(tmA, tmAh, tmB, tmY, tmY, args, grid, stream);
+  return launch_variant<false>(tmA, tmAh, tmB, tmY, tmY, args, grid, stream);
 }
 
 cudaError_t launch_mgemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmH,
@@ -617,14 +625,14 @@ cudaError_t launch_mgemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, 
   if constexpr (kCtaGroup != 2) {
     return cudaErrorNotSupported;
   } else {
-    return launch_variant<false, kEpiSwiglu>(tmA, tmB, tmH, tmY13, args, grid, stream);
+    return launch_variant<false, kEpiSwiglu>(tmA, tmA, tmB, tmH, tmY13, args, grid, stream);  // no half tiles
   }
 }
 
 cudaError_t launch_mgemm_swiglu_dgrad(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                       const CUtensorMap& tmDy13, const GroupArgs& args, int grid,
                                       cudaStream_t stream) {
-  return launch_variant<true, kEpiSwigluBwd>(tmA, tmB, tmDy13, tmDy13, args, grid, stream);
+  return launch_variant<true, kEpiSwigluBwd>(tmA, tmA, tmB, tmDy13, tmDy13, args, grid, stream);  // no half tiles
 }
 
 }  // namespace rg
