@@ -53,12 +53,14 @@ struct Cfg {
   static constexpr int BN = BNT;            // tile columns = MMA N
   static constexpr int BN_CTA = BN / CG;    // B rows (output columns) loaded per CTA
   static constexpr int BK = 64;
-  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 10 : (EPIW == 8 ? 5 : 6)) : 4;
+  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 10 : (EPIW == 8 ? 3 : 6)) : 4;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN_CTA * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_WARPS = EPIW;
-  static constexpr int EPI_BUF_BYTES = 32 * 128;
+  // staging per epilogue warp: one 32-row x 64-column bf16 box, or with 8
+  // epilogue warps (two chunks per warp and tile) two, written together
+  static constexpr int EPI_BUF_BYTES = 32 * 128 * (EPIW == 8 ? 2 : 1);
   // warp 0 and warp 2 + EPIW: TMA producers (alternate stages), warp 1: MMA,
   // warps 2 .. 1 + EPIW: epilogue
   static constexpr int PRODUCER2 = 2 + EPIW;
@@ -471,6 +473,48 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
         const int n0 = (local % nbn) * BN + (half ? (q >> 1) * 128 : 0);
         const int nch = half ? CH / 2 : CH;
         const int cf = half ? c_first / 2 : c_first;
+        if constexpr (C::EPI_WARPS == 8) {
+          // both chunks of this warp in one go when both are whole boxes:
+          // two staging buffers, one proxy fence, one bulk group
+          const int col0 = n0 + 64 * cf;
+          if (nch == 2 && wrow + 32 <= rows_valid && col0 + 128 <= N) {
+            uint32_t p[2][32];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t v0[32], v1[32];
+              tmem_ld_32x32b_x32(taddr + 64 * (cf + h2), v0);
+              tmem_ld_32x32b_x32(taddr + 64 * (cf + h2) + 32, v1);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                p[h2][j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
+                p[h2][16 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
+              }
+            }
+            release_acc(buf);
+            if (lane == 0) bulk_wait_read<0>();  // the previous stores have left both buffers
+            __syncwarp();
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint4* rowp = reinterpret_cast<uint4*>(ebuf + h2 * 4096 + lane * 128);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                rowp[j ^ (lane & 7)] =
+                    make_uint4(p[h2][4 * j], p[h2][4 * j + 1], p[h2][4 * j + 2], p[h2][4 * j + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                if (O == 1) tma_store_2d(&tmY, ebuf_s + h2 * 4096, col0 + 64 * h2, row0 + wrow);
+                else tma_store_3d(&tmY, ebuf_s + h2 * 4096, col0 + 64 * h2, o, row0 + wrow);
+              }
+              bulk_commit();
+            }
+            continue;
+          }
+        }
 #pragma unroll 1
         for (int c = cf; c < cf + nch; ++c) {
           uint32_t v0[32], v1[32];
