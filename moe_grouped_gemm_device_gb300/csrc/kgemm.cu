@@ -11,10 +11,10 @@
 //     list, so every round of W tiles has near-equal cost (longest-first list
 //     scheduling) -- without global scratch or host sync.
 //   * The contraction is fed 64 rows at a time.  With CG = 2 (default) a CTA
-//     pair computes a 256x256 dW tile with tcgen05.mma.cta_group::2: CTA r
-//     loads grad[r:r+64, n0+128r : +128] (A, its 128 rows of dW) and
-//     X[r:r+64, k0+128r : +128] (its half of B); both are N/K-contiguous, i.e.
-//     MN-major operands.  32 KB per stage and CTA, six stages.  CG = 1: one
+//     pair computes a 256x256 dW tile with tcgen05.mma.cta_group::2: for the
+//     row block starting at r, CTA c loads grad[r:r+64, n0+128c : +128] (A,
+//     its 128 rows of dW) and X[r:r+64, k0+128c : +128] (its half of B); both
+//     are N/K-contiguous, i.e. MN-major operands.  32 KB per stage and CTA, six stages.  CG = 1: one
 //     CTA, 128x256 tiles, four 48 KB stages.
 //   * Both operands are read through 3-D views {columns, i < 64, j} of the
 //     row-major tensors in which element (c, i, j) is row i + j (both row
@@ -33,7 +33,8 @@
 //     bounds the fp32 accumulation chain inside the tensor cores (whose error
 //     grows with its length) without any scratch memory.  The path to dW is
 //     tcgen05.ld -> swizzled shared memory -> TMA store / reduce-add of 32x32
-//     fp32 boxes (whole 128-byte lines).  Experts without rows produce zero
+//     fp32 boxes (whole 128-byte lines) with an L2 evict-first policy (dW is
+//     written once and not read here).  Experts without rows produce zero
 //     tiles without touching the tensor cores.
 //   * Same bounded-wait / abort / drain scheme as the M-grouped kernel.
 #include <algorithm>

@@ -21,6 +21,9 @@
 //     bytes directly on the issuing CTA's stage barrier (.cta_group::2), and
 //     MMA completion is multicast to the barriers of both CTAs.
 //     CG = 1: one CTA computes a 128x256 tile (tcgen05 M=128), four 48 KB stages.
+//   * Half tiles (CTA pairs, plain epilogue): an expert's last row block of at
+//     most 128 rows runs as an M=128 pair MMA; each CTA loads only its 64 rows
+//     of A, through a second tensor map with 64-row boxes.
 //   * Warp roles (224 threads per CTA): lane 0 of warps 0 and 6 issue the TMA
 //     loads of alternate stages;
 //     warp 1 owns tensor memory, and in the issuing CTA lane 0 issues the MMAs
