@@ -102,8 +102,8 @@ def kernel_of(op) -> str:
 def algorithmic_bytes(op, counts) -> int:
     M = int(np.sum(counts))
     E = len(counts)
-    if op.kind == "kgemm":
-        return 2 * M * op.N + 2 * M * op.K + 4 * E * op.N * op.K
+    if op.kind == "kgemm":  # grad and X read, dW written (and read first when accumulating)
+        return 2 * M * op.N + 2 * M * op.K + (8 if op.accumulate else 4) * E * op.N * op.K
     nonempty = int(np.count_nonzero(counts))
     if op.kind == "mxk":  # FP8 grad and X, their scales, fp32 dW
         return M * op.N + M * op.K + (op.N + op.K) * (M // 32) + 4 * E * op.N * op.K
@@ -395,7 +395,7 @@ def build_units(wl, rg, tensors, outs, off_ref, scratch):
         def call(op=op):
             out = outs[op.name]
             if op.kind == "kgemm":
-                rg.kgemm(tensors[op.a], tensors[op.b], off_ref[0], out=out)
+                rg.kgemm(tensors[op.a], tensors[op.b], off_ref[0], out=out, accumulate=op.accumulate)
             elif op.kind == "nested":
                 rg.mgemm_nested(tensors[op.a], tensors[op.b], off_ref[0], transpose_B=op.transpose_B, out=out)
             elif op.fuse == "swiglu":
@@ -455,7 +455,9 @@ def main():
         outs, scratch = {}, {}
         for op in wl.ops:
             if op.kind in ("kgemm", "mxk"):
-                outs[op.name] = torch.empty((wl.E, op.N, op.K), dtype=torch.float32, device=dev)
+                # a main grad that steps accumulate into starts at zero
+                alloc = torch.zeros if getattr(op, "accumulate", False) else torch.empty
+                outs[op.name] = alloc((wl.E, op.N, op.K), dtype=torch.float32, device=dev)
             elif op.kind == "nested":
                 outs[op.name] = torch.empty((wl.M, op.outer * op.N), dtype=torch.bfloat16, device=dev)
             elif op.fuse == "swiglu":

@@ -202,3 +202,28 @@ def test_full_size_sampled(gpu_lib, wname, opname):
         for e in np.flatnonzero(wl.counts == 0):
             assert bool((dW[int(e)] == 0).all()), f"expert {e} has no rows but dW[e] != 0"
         del dW
+
+
+ACC = [("a3b_acc", "wgrad_gw2_acc"), ("a3b_acc", "wgrad_gw13_acc")]
+
+
+@pytest.mark.parametrize("wname,opname", ACC, ids=[f"{w}-{o}" for w, o in ACC])
+def test_full_size_sampled_accumulate(gpu_lib, wname, opname):
+    """Fused wgrad accumulation at full size: a seeded FP32 main grad plus the
+    grouped weight gradient, on sampled dW rows."""
+    import torch
+    wl = W.ALL[wname]()
+    op = wl.op(opname)
+    off = wl.offsets
+    rng = np.random.default_rng(zlib.crc32(f"{wname}/{opname}".encode()))
+    a_h, b_h = host_tensor(wl, op.a), host_tensor(wl, op.b)
+    init = W.bf16_bits_to_f32(W.normal_bf16((wl.E, op.N, op.K), 1.0, wl.seed, 90))
+    dW = torch.from_numpy(init).cuda()
+    gpu_lib.kgemm(dev_tensor(wl, op.a), dev_tensor(wl, op.b), offsets_dev(off), out=dW, accumulate=True)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    es, ns = sample_pairs(wl.counts, op.N, rng)
+    got = dW[torch.from_numpy(es).long().cuda(), torch.from_numpy(ns).long().cuda()].cpu().numpy()
+    ref = init[es, ns].astype(np.float64) + oracle.kgemm(a_h, b_h, off, sel=(es, ns))
+    check_fp32(got, ref, f"{wname}/{opname}")
+    del dW

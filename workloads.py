@@ -248,6 +248,9 @@ class Op:
     # grad [M, N], b = X [M, K] E4M3 codes, sa [N, M/32] and sb [K, M/32]
     sa: str = ""
     sb: str = ""
+    # kind 'kgemm': add dW to the existing FP32 output (main grad) instead of
+    # overwriting it
+    accumulate: bool = False
 
     def flops(self, counts) -> int:
         return 2 * int(np.sum(counts)) * self.outer * self.N * self.K
@@ -328,6 +331,17 @@ def with_swiglu(w: Workload) -> Workload:
                    fuse="swiglu_bwd", c="y13")
         ops.append(o)
     f.ops = ops
+    return f
+
+
+def with_wgrad_accumulation(w: Workload) -> Workload:
+    """The same layer with both weight gradients added to an existing FP32
+    main grad (fused wgrad accumulation) instead of overwriting dW."""
+    import copy
+    f = copy.deepcopy(w)
+    f.name = w.name + "_acc"
+    f.ops = [Op(o.name + "_acc", o.kind, o.a, o.b, N=o.N, K=o.K, accumulate=True) if o.kind == "kgemm" else o
+             for o in w.ops]
     return f
 
 
@@ -460,6 +474,7 @@ ALL = {
     "skewed": lambda: skewed(False),
     "skewed_tail": lambda: skewed(True),
     "a3b_swiglu": lambda: with_swiglu(a3b_layer()),
+    "a3b_acc": lambda: with_wgrad_accumulation(a3b_layer()),
     "skewed_tail_swiglu": lambda: with_swiglu(skewed(True)),
     "lora_a3b": lora_a3b,
     "a3b_mxfp8": a3b_mxfp8,
