@@ -583,6 +583,12 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
   }
 }
 
+// every variant holds the tables of RG_MAX_EXPERTS_CFG groups beside its pipeline
+static_assert(Cfg<kCtaGroup, 256, 4>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 &&
+                  Cfg<kCtaGroup, 256, 8>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 &&
+                  Cfg<kCtaGroup, 64, 4>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448,
+              "an Mgemm variant exceeds the shared memory of a CTA at the largest group count");
+
 template <int BNT, int EPIW>
 size_t smem_of(int E) {
   return Cfg<kCtaGroup, BNT, EPIW>::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4;

@@ -929,6 +929,8 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
 
 }  // namespace
 
+static_assert(MxCfg::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448,
+              "MXFP8 Mgemm configuration exceeds the shared memory of a CTA at the largest group count");
 size_t mx_smem_bytes(int E) { return MxCfg::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4; }
 
 cudaError_t mx_setup(int max_smem) {
