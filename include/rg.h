@@ -291,7 +291,9 @@ int rg_mgemm_swiglu_dgrad(const void* dy, const void* w2, const int32_t* offsets
  *            accumulated in FP32 by the tensor cores over chunks of at most
  *            4096 rows, whose partial sums are added in FP32 in row order
  *            (deterministic); an expert with no rows gets dW[e] = 0.
- *            Rows >= offsets[E] are ignored.
+ *            Rows >= offsets[E] are ignored, and no row outside an
+ *            expert's range is read for its dW[e]: Inf or NaN in one
+ *            expert's rows reaches that expert's dW only.
  *   E 1 .. RG_KGEMM_MAX_EXPERTS; M, N, K, alignment and stream as for
  *   rg_mgemm (dW 16-byte aligned).  M == 0 is valid and zeroes dW.
  */
