@@ -160,6 +160,7 @@ rg::GroupArgs group_args(const DeviceState* ds, const int32_t* offsets, int E, i
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.accumulate = 0;
   a.outer = 1;
+  a.kg_wide = 0;
   return a;
 }
 
@@ -509,23 +510,31 @@ int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, i
   const void* x_ptr = M > 0 ? X : static_cast<const void*>(dW);
   const uint64_t rows = M > 0 ? static_cast<uint64_t>(M) : 1;
 
-  // Operands as 3-D views {cols, i < BR, j}: element (c, i, j) is row j + i,
-  // so a box starting at i = v - BR < 0 zero-fills its leading BR - v rows
-  // (an expert's ragged last block).  Every element the kernel reads lies in
-  // rows offsets[e] .. offsets[e+1]-1 of some expert.
+  // Operands as overlapping views in which element (.., i, .., j) is row
+  // j + i (i < BR): a box starting at i = v - BR < 0 zero-fills its leading
+  // BR - v rows (an expert's ragged last block), and every element the
+  // kernel reads lies in rows offsets[e] .. offsets[e+1]-1 of some expert.
+  // With N and K multiples of 64 the views are 4-D {64 cols, i, column
+  // block, j} and one copy brings a CTA's 64-column boxes of an operand
+  // (column block stride 128 bytes); otherwise 3-D {cols, i, j}, one copy
+  // per box.
+  const bool wide = N % 64 == 0 && K % 64 == 0;
   CUtensorMap tmG, tmX, tmD;
-  {
-    const uint64_t dims[3] = {static_cast<uint64_t>(N), rg::kg::BR, rows};
-    const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(N) * 2};
+  auto operand_map = [&](CUtensorMap* m, const void* p, int cols, int boxes) {
+    const uint64_t pitch = static_cast<uint64_t>(cols) * 2;
+    if (wide) {
+      const uint64_t dims[4] = {64, rg::kg::BR, static_cast<uint64_t>(cols / 64), rows};
+      const uint64_t str[3] = {pitch, 128, pitch};
+      const uint32_t box[4] = {64, rg::kg::BR, static_cast<uint32_t>(boxes), 1};
+      return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p, dims, str, box);
+    }
+    const uint64_t dims[3] = {static_cast<uint64_t>(cols), rg::kg::BR, rows};
+    const uint64_t str[2] = {pitch, pitch};
     const uint32_t box[3] = {64, rg::kg::BR, 1};
-    if (!encode(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, g_ptr, dims, str, box)) return RG_ERR_INVALID_ARG;
-  }
-  {
-    const uint64_t dims[3] = {static_cast<uint64_t>(K), rg::kg::BR, rows};
-    const uint64_t str[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(K) * 2};
-    const uint32_t box[3] = {64, rg::kg::BR, 1};
-    if (!encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x_ptr, dims, str, box)) return RG_ERR_INVALID_ARG;
-  }
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p, dims, str, box);
+  };
+  if (!operand_map(&tmG, g_ptr, N, rg::kg::BM / 64)) return RG_ERR_INVALID_ARG;
+  if (!operand_map(&tmX, x_ptr, K, rg::kg::BN_CTA / 64)) return RG_ERR_INVALID_ARG;
   {
     const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
     const uint64_t str[2] = {static_cast<uint64_t>(K) * 4, static_cast<uint64_t>(N) * K * 4};
@@ -534,6 +543,7 @@ int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, i
   }
   rg::GroupArgs args = group_args(ds, offsets, E, M, N, K, dW);
   args.accumulate = accumulate;
+  args.kg_wide = wide ? 1 : 0;
   const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->kg_grid, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;

@@ -23,7 +23,9 @@
 //     (c, v-64, r): its first 64-v rows have i < 0 and are zero-filled by the
 //     copy engine, the expert's rows r .. r+v-1 land in the last v rows, and
 //     no row past the expert is read.  The MMAs skip the leading all-zero
-//     16-row steps.  So no block needs fixing up in shared memory, and the
+//     16-row steps.  With N and K multiples of 64 the views are 4-D,
+//     {64 cols, i, column block, j}, and one copy per operand and stage
+//     brings both of the CTA's 64-column boxes.  So no block needs fixing up in shared memory, and the
 //     copies of both CTAs complete their bytes on the issuing CTA's stage
 //     barrier (.cta_group::2) for every block alike.
 //   * The fp32 accumulator (128 lanes x 256 columns per CTA, double-buffered
@@ -230,11 +232,17 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
           const int i0 = min(0, r_end - r - BR);
           const uint32_t fb = full_issuer + 8u * stage;
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES * CG);
+          if (args.kg_wide) {  // one copy per operand: column blocks n0/64 .. and k0/64 ..
+            tma_load_4d_cg<CG>(sa, &tmG, fb, 0, i0, n0 / 64, r);
+            tma_load_4d_cg<CG>(sb, &tmX, fb, 0, i0, k0 / 64, r);
+          } else {
 #pragma unroll
-          for (int j = 0; j < BM / 64; ++j) tma_load_3d_cg<CG>(sa + j * BOX_BYTES, &tmG, fb, n0 + 64 * j, i0, r);
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_3d_cg<CG>(sa + j * BOX_BYTES, &tmG, fb, n0 + 64 * j, i0, r);
 #pragma unroll
-          for (int j = 0; j < BN_CTA / 64; ++j)
-            tma_load_3d_cg<CG>(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, i0, r);
+            for (int j = 0; j < BN_CTA / 64; ++j)
+              tma_load_3d_cg<CG>(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, i0, r);
+          }
           if (rank == 0) {
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);

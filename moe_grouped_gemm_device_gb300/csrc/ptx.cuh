@@ -200,6 +200,31 @@ __device__ __forceinline__ void tma_load_2d_cg(uint32_t dst, const CUtensorMap* 
   else tma_load_2d_pair(dst, m, bar, c0, c1);
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0,
+                                                 int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+template <int CG>
+__device__ __forceinline__ void tma_load_4d_cg(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0,
+                                               int32_t c1, int32_t c2, int32_t c3) {
+  if constexpr (CG == 1) tma_load_4d(dst, m, bar, c0, c1, c2, c3);
+  else tma_load_4d_pair(dst, m, bar, c0, c1, c2, c3);
+}
+
 template <int CG>
 __device__ __forceinline__ void tma_load_3d_cg(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                                int32_t c0, int32_t c1, int32_t c2) {

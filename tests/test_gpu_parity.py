@@ -70,6 +70,20 @@ def test_kgemm_integer_inputs_bit_exact(gpu_lib):
     assert (dW[1] == 0).all()
 
 
+@pytest.mark.parametrize("N,K", [(384, 320), (200, 136), (72, 520), (128, 64)],
+                         ids=["wide-boxes", "3d-views", "narrow-N", "one-column-block"])
+def test_kgemm_operand_views_bit_exact(gpu_lib, N, K):
+    """Both operand-view forms: N and K multiples of 64 (one copy per operand
+    and stage) and not (one copy per 64-column box, the last one clipped)."""
+    counts = [130, 0, 1, 64, 200, 17]
+    off = W.offsets_from_counts(counts)
+    M = int(off[-1]) + 9
+    g = ints((M, N), 10, 0)
+    x = ints((M, K), 10, 1)
+    dW = run_kgemm(gpu_lib, g, x, off, N, K)
+    np.testing.assert_array_equal(dW.astype(np.float64), oracle.kgemm(g, x, off))
+
+
 def test_kgemm_ragged_blocks_at_both_ends_bit_exact(gpu_lib):
     """Ragged last blocks of every kind: the first expert's only block starts
     at row 0, blocks of 1, 15, 16, 17, 63 and 65 rows, and the last expert ends
