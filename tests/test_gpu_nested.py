@@ -63,6 +63,26 @@ def test_nested_lora_shapes(gpu_lib, O, N, K):
     assert (y[valid:] == SENTINEL_BF16).all()
 
 
+@pytest.mark.parametrize("transpose_B,N,K", [(False, 8, 8), (True, 16, 8), (False, 72, 8)],
+                         ids=["fwd-narrow", "dgrad", "fwd-partial-tile"])
+def test_nested_max_outer_bit_exact(gpu_lib, transpose_B, N, K):
+    """RG_MAX_OUTER outer groups: the tile index (inner tile x O + o) and the
+    weight slot (o x L + l) at their largest, every outer group's column
+    block in its place."""
+    O = gpu_lib.RG_MAX_OUTER
+    counts = [3, 0, 130]
+    off = W.offsets_from_counts(counts)
+    L = len(counts)
+    M = int(off[-1]) + 2
+    x = W.integer_bf16((M, O * K), -2, 2, 23, 0)
+    w = W.integer_bf16((O, L, K, N) if transpose_B else (O, L, N, K), -2, 2, 23, 1)
+    y = run_nested(gpu_lib, x, w, off, transpose_B, M, O, N)
+    ref = oracle.mgemm_nested(x, w, off, transpose_B=transpose_B)
+    valid = int(off[-1])
+    np.testing.assert_array_equal(y[:valid], bf16_round_exact(ref[:valid]))
+    assert (y[valid:] == SENTINEL_BF16).all()
+
+
 def test_nested_outer_one_equals_mgemm(gpu_lib):
     """O = 1 is the plain grouped GEMM: same kernel, bit-identical output."""
     import torch
