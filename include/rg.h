@@ -24,7 +24,12 @@
  *     see (invalid offsets contents, a pipeline wait that ran out) are recorded
  *     in a per-device status word read by rg_get_device_status().
  *   - No C++ exception crosses this interface.
- *   - Thread safety: calls may be made from several host threads.
+ *   - Thread safety: calls may be made from several host threads, on one or
+ *     several streams; calls on different streams are independent.
+ *   - CUDA graphs: the first call on a device sets up the library's state for
+ *     it (kernel attributes, grid sizes); every later call enqueues only
+ *     kernel launches, so a sequence of calls may be captured in a CUDA graph
+ *     and replayed with new contents in the same buffers.
  */
 #ifndef RG_H_
 #define RG_H_
