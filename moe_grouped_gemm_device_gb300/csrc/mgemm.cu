@@ -55,10 +55,17 @@ struct Cfg {
   static constexpr int TILE_M = BM * CG;    // rows per tile
   static constexpr int BN = BNT;            // tile columns = MMA N
   static constexpr int BN_CTA = BN / CG;    // B rows (output columns) loaded per CTA
-  static constexpr int BK = 64;
-  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 10 : (EPIW == 8 ? 3 : 6)) : 4;
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN_CTA * BK * 2;
+  static constexpr int BK = 64;             // K of one 128-byte swizzle atom (bf16)
+  // Atoms per stage: the default tile takes two, so that one barrier round of
+  // the MMA warp issues eight MMAs (four cost a fixed share of its time);
+  // three 64 KB stages hold as many bytes as six of 32 KB.
+  static constexpr int KATOMS = CG == 2 && BNT == 256 && EPIW == 4 ? 2 : 1;
+  static constexpr int BKS = BK * KATOMS;   // K per stage
+  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 10 : (EPIW == 8 ? 3 : 3)) : 4;
+  static constexpr int A_ATOM = BM * BK * 2;       // one atom of A (bytes)
+  static constexpr int B_ATOM = BN_CTA * BK * 2;   // one atom of B
+  static constexpr int A_BYTES = A_ATOM * KATOMS;
+  static constexpr int B_BYTES = B_ATOM * KATOMS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_WARPS = EPIW;
   // staging per epilogue warp: one 32-row x 64-column bf16 box, or with 8
@@ -105,6 +112,7 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
   static_assert(EPI == kEpiPlain || (BNT == 256 && EPIW == 4), "fused epilogues use the default tile");
   using C = Cfg<CG, BNT, EPIW>;
   constexpr int BM = C::BM, TILE_M = C::TILE_M, BN = C::BN, BN_CTA = C::BN_CTA, BK = C::BK;
+  constexpr int KATOMS = C::KATOMS, BKS = C::BKS, A_ATOM = C::A_ATOM, B_ATOM = C::B_ATOM;
   constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
 
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -138,7 +146,7 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
   const int F = N / 2;  // SwiGLU: output features
   // output-column blocks per row block: 256 columns, or 128 SwiGLU features
   const int nbn = SWIGLU ? (F + BN_CTA - 1) / BN_CTA : (N + BN - 1) / BN;
-  const int nk = (K + BK - 1) / BK;
+  const int nk = (K + BKS - 1) / BKS;  // stages per tile
 
   // ---- offsets -> shared memory, validation ---------------------------------
   if (threadIdx.x == 0) misc[1] = 0;
@@ -268,14 +276,21 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_BYTES;
             if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), stage_tx);
-            if (O == 1) tma_load_2d_cg<CG>(sa, am, fb, kb * BK, row0);
-            else tma_load_3d_cg<CG>(sa, am, fb, kb * BK, o, row0);
-            if constexpr (!TRANS_B) {
-              tma_load_3d_cg<CG>(sb, &tmB, fb, kb * BK, n0, eb);
-            } else {
+            // one copy of A and of B per 64-deep atom (atoms past K are
+            // zero-filled boxes; the MMA warp skips them)
 #pragma unroll
-              for (int j = 0; j < BN_CTA / 64; ++j)
-                tma_load_3d_cg<CG>(sb + j * 8192, &tmB, fb, n0 + 64 * j, kb * BK, eb);
+            for (int j = 0; j < KATOMS; ++j) {
+              const int kc = kb * BKS + BK * j;
+              const uint32_t saj = sa + j * A_ATOM, sbj = sb + j * B_ATOM;
+              if (O == 1) tma_load_2d_cg<CG>(saj, am, fb, kc, row0);
+              else tma_load_3d_cg<CG>(saj, am, fb, kc, o, row0);
+              if constexpr (!TRANS_B) {
+                tma_load_3d_cg<CG>(sbj, &tmB, fb, kc, n0, eb);
+              } else {
+#pragma unroll
+                for (int jj = 0; jj < BN_CTA / 64; ++jj)
+                  tma_load_3d_cg<CG>(sbj + jj * 8192, &tmB, fb, n0 + 64 * jj, kc, eb);
+              }
             }
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -322,11 +337,15 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(sa + 32 * k, 16, 1024);
-            const uint64_t bd = TRANS_B ? sdesc_sw128(sb + 2048 * k, 8192, 1024)
-                                        : sdesc_sw128(sb + 32 * k, 16, 1024);
-            umma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0);
+          for (int k = 0; k < BKS / 16; ++k) {
+            const int j = k / (BK / 16), kk = k % (BK / 16);  // atom, 16-deep step in it
+            if (kb * BKS + BK * j < K) {
+              const uint32_t saj = sa + j * A_ATOM, sbj = sb + j * B_ATOM;
+              const uint64_t ad = sdesc_sw128(saj + 32 * kk, 16, 1024);
+              const uint64_t bd = TRANS_B ? sdesc_sw128(sbj + 2048 * kk, 8192, 1024)
+                                          : sdesc_sw128(sbj + 32 * kk, 16, 1024);
+              umma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            }
           }
           umma_commit<CG>(empty_bar(stage));  // frees the stage (in both CTAs) once these MMAs finish
         }
