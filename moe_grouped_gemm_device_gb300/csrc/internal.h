@@ -23,9 +23,9 @@ struct GroupArgs {
   int accumulate;           // Kgemm: 1 = dW += result, 0 = dW = result
   int outer;                // Mgemm: outer groups O along the columns of x and y (1 = plain);
                             // with O > 1 the x and y maps are 3-D {cols, O, rows}
-  int kg_wide;              // Kgemm: 1 = operand maps are 4-D {64 cols, 64 rows, column block,
+  int kg_wide;              // Kgemm: 1 = operand maps are 4-D {64 cols, BR rows, column block,
                             // row} and one copy loads both 64-column boxes of a CTA (N and K
-                            // multiples of 64); 0 = 3-D maps {cols, 64 rows, row}, one copy per box
+                            // multiples of 64); 0 = 3-D maps {cols, BR rows, row}, one copy per box
 };
 
 // Arguments of the MXFP8 Mgemm besides its tensor maps.
@@ -84,7 +84,7 @@ constexpr int BM = 128;                  // dW rows per CTA
 constexpr int TILE_M = BM * kCtaGroup;   // dW rows per tile
 constexpr int BN = 256;                  // dW columns per tile
 constexpr int BN_CTA = BN / kCtaGroup;   // X columns loaded per CTA
-constexpr int BR = 64;                   // contraction rows per stage
+constexpr int BR = 128;                  // contraction rows per stage (eight 16-row MMA steps)
 // Rows of one expert accumulated in tensor memory before the partial sum is
 // folded into dW (store for the first chunk, fp32 reduce-add for the rest).
 // Bounds the length of each fp32 accumulation chain inside the tensor cores.

@@ -10,24 +10,25 @@
 //     by index) in shared memory; worker w takes tiles w, w+W, ... of that
 //     list, so every round of W tiles has near-equal cost (longest-first list
 //     scheduling) -- without global scratch or host sync.
-//   * The contraction is fed 64 rows at a time.  With CG = 2 (default) a CTA
+//   * The contraction is fed BR = 128 rows at a time, eight MMA steps of 16
+//     rows per barrier round of the MMA warp.  With CG = 2 (default) a CTA
 //     pair computes a 256x256 dW tile with tcgen05.mma.cta_group::2: for the
-//     row block starting at r, CTA c loads grad[r:r+64, n0+128c : +128] (A,
-//     its 128 rows of dW) and X[r:r+64, k0+128c : +128] (its half of B); both
-//     are N/K-contiguous, i.e. MN-major operands.  32 KB per stage and CTA, six stages.  CG = 1: one
-//     CTA, 128x256 tiles, four 48 KB stages.
-//   * Both operands are read through 3-D views {columns, i < 64, j} of the
+//     row block starting at r, CTA c loads grad[r:r+BR, n0+128c : +128] (A,
+//     its 128 rows of dW) and X[r:r+BR, k0+128c : +128] (its half of B); both
+//     are N/K-contiguous, i.e. MN-major operands.  64 KB per stage and CTA,
+//     three stages.  CG = 1: one CTA, 128x256 tiles, two 96 KB stages.
+//   * Both operands are read through 3-D views {columns, i < BR, j} of the
 //     row-major tensors in which element (c, i, j) is row i + j (both row
 //     strides equal the pitch).  A full block loads box (c, 0, r): rows
-//     r .. r+63.  An expert's ragged last block of v < 64 rows loads box
-//     (c, v-64, r): its first 64-v rows have i < 0 and are zero-filled by the
+//     r .. r+BR-1.  An expert's ragged last block of v < BR rows loads box
+//     (c, v-BR, r): its first BR-v rows have i < 0 and are zero-filled by the
 //     copy engine, the expert's rows r .. r+v-1 land in the last v rows, and
 //     no row past the expert is read.  The MMAs skip the leading all-zero
 //     16-row steps.  With N and K multiples of 64 the views are 4-D,
 //     {64 cols, i, column block, j}, and one copy per operand and stage
-//     brings both of the CTA's 64-column boxes.  So no block needs fixing up in shared memory, and the
-//     copies of both CTAs complete their bytes on the issuing CTA's stage
-//     barrier (.cta_group::2) for every block alike.
+//     brings both of the CTA's 64-column boxes.  So no block needs fixing up
+//     in shared memory, and the copies of both CTAs complete their bytes on
+//     the issuing CTA's stage barrier (.cta_group::2) for every block alike.
 //   * The fp32 accumulator (128 lanes x 256 columns per CTA, double-buffered
 //     in tensor memory) holds at most CHUNK_ROWS rows of one expert: a longer
 //     expert is summed chunk by chunk, the first chunk's partial stored to dW
@@ -54,7 +55,7 @@ struct Cfg {
   static constexpr int TILE_M = BM * CG;   // dW rows per tile
   static constexpr int BN = 256;           // dW columns per tile (MMA N)
   static constexpr int BN_CTA = BN / CG;   // X columns loaded per CTA
-  static constexpr int BR = 64;            // rows of the contraction per stage
+  static constexpr int BR = kg::BR;        // rows of the contraction per stage
   static constexpr int STAGES = ST;
   static constexpr int BOX_BYTES = BR * 128;  // one 64-element-wide box of BR rows
   static constexpr int A_BYTES = BM * BR * 2;
@@ -446,7 +447,7 @@ __global__ void wait_selftest_kernel(unsigned int* status, unsigned long long li
 
 // Ring depth.  The shared-memory tables of the experts sit beside it, which
 // bounds E (RG_KGEMM_MAX_EXPERTS in rg.h; the host rejects larger E).
-constexpr int kStagesDeep = kCtaGroup == 2 ? 6 : 4;
+constexpr int kStagesDeep = kCtaGroup == 2 ? 3 : 2;
 static_assert(Cfg<kCtaGroup, kStagesDeep>::SMEM_FIXED + (2 * RG_KGEMM_MAX_EXPERTS + 1) * 4 <= 232448,
               "the expert tables of RG_KGEMM_MAX_EXPERTS experts must fit beside the ring");
 
