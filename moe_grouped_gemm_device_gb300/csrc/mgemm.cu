@@ -56,12 +56,14 @@ struct Cfg {
   static constexpr int BN = BNT;            // tile columns = MMA N
   static constexpr int BN_CTA = BN / CG;    // B rows (output columns) loaded per CTA
   static constexpr int BK = 64;             // K of one 128-byte swizzle atom (bf16)
-  // Atoms per stage: the default tile takes two, so that one barrier round of
-  // the MMA warp issues eight MMAs (four cost a fixed share of its time);
-  // three 64 KB stages hold as many bytes as six of 32 KB.
-  static constexpr int KATOMS = CG == 2 && BNT == 256 && EPIW == 4 ? 2 : 1;
+  // Atoms per stage: two for the 256- and 64-column tiles, so that one
+  // barrier round of the MMA warp issues eight MMAs (four cost a fixed share
+  // of its time); the 8-epilogue-warp tile (K <= 64) has one.
+  static constexpr int KATOMS = CG == 2 && (EPIW == 4) ? 2 : 1;
   static constexpr int BKS = BK * KATOMS;   // K per stage
-  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 10 : (EPIW == 8 ? 3 : 3)) : 4;
+  // 256-column tiles: three 64 KB stages; 64-column tiles (N = 64 MMAs, a
+  // quarter as long): five 40 KB stages; one-stage contractions: three
+  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 5 : 3) : 4;
   static constexpr int A_ATOM = BM * BK * 2;       // one atom of A (bytes)
   static constexpr int B_ATOM = BN_CTA * BK * 2;   // one atom of B
   static constexpr int A_BYTES = A_ATOM * KATOMS;
