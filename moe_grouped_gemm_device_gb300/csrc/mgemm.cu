@@ -15,8 +15,9 @@
 //     are loaded but never stored.
 //   * CG = 2 (default): a CTA pair (cluster of 2) computes a 256x256 tile with
 //     tcgen05.mma.cta_group::2 (M=256, N=256, K=16).  Each CTA loads its own
-//     128 rows of A and 128 rows of B (output columns), so one 64-deep stage is
-//     32 KB per CTA and six stages are in flight.  Each CTA's tensor memory
+//     128 rows of A and 128 rows of B (output columns); a stage holds two
+//     64-deep atoms of both (64 KB per CTA, eight MMAs per barrier round of
+//     the MMA warp) and three stages are in flight.  Each CTA's tensor memory
 //     receives its 128 rows of D.  The peer CTA's TMA copies complete their
 //     bytes directly on the issuing CTA's stage barrier (.cta_group::2), and
 //     MMA completion is multicast to the barriers of both CTAs.
