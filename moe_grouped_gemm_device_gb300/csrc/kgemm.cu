@@ -78,9 +78,6 @@ struct Cfg {
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int CHUNK_ROWS = kg::CHUNK_ROWS;
 
-#ifndef RG_KG_ORDER_MIX
-#define RG_KG_ORDER_MIX 0
-#endif
 
 template <int CG, int ST>
 __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
@@ -178,20 +175,9 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
   // worker w takes tiles w, w+W, ..., so every round of W tiles has
   // near-equal cost.
   auto tile_at = [&](int t, int& e, int& local) {
-#if RG_KG_ORDER_MIX
-    int p = t;
-    {
-      const int r = t / nworkers, j = t - r * nworkers;
-      if ((nworkers & 1) == 0 && (r + 1) * nworkers <= T) p = r * nworkers + (j + r) % nworkers;
-      const int i = p >> 1;
-      p = (p & 1) ? T - 1 - i : i;
-    }
-#else
-    const int p = t;
-#endif
-    const int pe = p / tpe;
+    const int pe = t / tpe;
     e = s_ord[pe];
-    local = p - pe * tpe;
+    local = t - pe * tpe;
   };
   if (warp == 0 || warp == C::PRODUCER2) {
     // ============ TMA producers (lane 0 of warp 0 and of the last warp) =====
