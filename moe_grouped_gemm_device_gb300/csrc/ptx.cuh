@@ -316,16 +316,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Same for writes into the shared memory of any CTA of the cluster.
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
-
-// 16 zero bytes at a shared::cluster address (own or peer CTA).
-__device__ __forceinline__ void st_cluster_zero16(uint32_t addr) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
-}
-
 // ----------------------------------------------------------------- tcgen05
 
 // Tensor-memory allocation.  With CG == 2 one warp of each CTA of the pair
