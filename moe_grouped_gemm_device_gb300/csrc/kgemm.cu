@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         const int buf = acc & 1;
         const uint32_t tph = (acc >> 1) & 1;
         ++acc;
-        ok = __all_sync(0xffffffffu, wait_pair(tfull_bar(buf), tph));
+        ok = warp_wait_acc<CG>(guard, tfull_bar(buf), tph);
         if (!ok) break;
         tc_fence_after();
         if (!warp_rows) {

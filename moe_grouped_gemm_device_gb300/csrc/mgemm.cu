@@ -78,8 +78,8 @@ struct Cfg {
   // warps 2 .. 1 + EPIW: epilogue
   static constexpr int PRODUCER2 = 2 + EPIW;
   static constexpr int THREADS = 32 * (3 + EPIW);
-  // full[S], empty[S], ready[S], tfull[2], tempty[2], drain
-  static constexpr int NUM_BARS = 3 * STAGES + 5;
+  // full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
   // The dynamic shared-memory window of a CTA without static shared memory
   // starts 1024-byte aligned; the kernel checks this instead of padding.
   static constexpr int SMEM_FIXED =
@@ -133,10 +133,9 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto ready_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (3 * STAGES + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (3 * STAGES + 4);
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -210,7 +209,6 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
-      mbar_init(ready_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -436,7 +434,7 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
       wrow = half ? (q & 1) * 32 : q * 32;
       const int buf = acc & 1;
       const uint32_t tph = (acc >> 1) & 1;
-      if (!__all_sync(0xffffffffu, wait_pair(tfull_bar(buf), tph))) break;
+      if (!warp_wait_acc<CG>(guard, tfull_bar(buf), tph)) break;
       tc_fence_after();
       if (wrow >= rows_valid) {  // none of this warp's rows belong to the expert
         release_acc(buf);

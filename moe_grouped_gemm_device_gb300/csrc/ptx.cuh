@@ -139,6 +139,41 @@ __device__ __forceinline__ bool mbar_wait_cl(const WaitGuard& g, uint32_t bar, u
   return mbar_wait_slow(g, bar, parity, true);
 }
 
+// Bounded wait, by one thread, for a barrier the peer CTA of a pair arrives
+// on, sleeping `sleep_ns` between polls: for a wait whose latency hardly
+// matters (an epilogue that waits out a whole mainloop), so that its polling
+// does not compete with the copies and MMAs for the shared-memory pipe.
+static __device__ __noinline__ bool mbar_wait_cl_sleep(const WaitGuard& g, uint32_t bar, uint32_t parity,
+                                                       uint32_t sleep_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    __nanosleep(sleep_ns);
+    if (*g.abort) return false;
+    if (globaltimer_ns() - t0 > g.limit_ns) {
+      atomicOr(g.status, kDevTimeout);
+      *g.abort = 1;
+      return false;
+    }
+  }
+}
+
+// Warp-wide bounded wait for an accumulator barrier, for epilogue warps that
+// wait out a whole mainloop: with CTA pairs lane 0 alone polls, sleeping 1 us
+// between polls, and the warp takes its answer (measured: the pair kernels'
+// epilogues polling flat out cost the weight-gradient GEMM ~1%); single CTAs
+// use the suspending wait.
+template <int CG>
+__device__ __forceinline__ bool warp_wait_acc(const WaitGuard& g, uint32_t bar, uint32_t parity) {
+  if constexpr (CG == 1) {
+    return __all_sync(0xffffffffu, mbar_wait(g, bar, parity)) != 0;
+  } else {
+    bool got = true;
+    if ((threadIdx.x & 31) == 0) got = mbar_wait_cl_sleep(g, bar, parity, 1000);
+    return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+  }
+}
+
 // Bounded wait used while draining after an abort: ignores the abort flag.
 static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
