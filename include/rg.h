@@ -337,11 +337,14 @@ int rg_get_device_status(cudaStream_t stream, uint32_t* status);
 int rg_set_wait_timeout_ns(uint64_t ns);
 
 /*
- * rg_selftest_wait_timeout -- enqueue one CTA that waits on a pipeline
- * barrier which nothing ever signals, bounded by `ns` nanoseconds, and report
- * through *status (host pointer) the status bits it set (RG_DEV_TIMEOUT when
- * the bound works).  Synchronises `stream`.  Exercises the timeout path
- * without a fault or a hang.
+ * rg_selftest_wait_timeout -- enqueue one CTA whose warps wait on pipeline
+ * barriers which nothing ever signals, one through each form of bounded wait
+ * the kernels use (suspending, cluster-scope polling, the epilogues' sleeping
+ * poll), each bounded by `ns` nanoseconds, and report through *status (host
+ * pointer) the status bits the CTA set: RG_DEV_TIMEOUT when every form gave
+ * up by itself, 0 when any of them returned as if its barrier had completed.
+ * Synchronises `stream`.  Exercises the timeout path without a fault or a
+ * hang.
  */
 int rg_selftest_wait_timeout(uint64_t ns, cudaStream_t stream, uint32_t* status);
 

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "librg.so")
-SOURCES = ["api.cu", "mgemm.cu", "kgemm.cu", "mxgemm.cu"]
+SOURCES = ["api.cu", "mgemm.cu", "kgemm.cu", "mxgemm.cu", "selftest.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("ptx.cuh", "internal.h")] + [os.path.join(INCLUDE, "rg.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -416,21 +416,6 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
   }
 }
 
-__global__ void wait_selftest_kernel(unsigned int* status, unsigned long long limit_ns) {
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ int abort_flag;
-  if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&bar), 1);
-    abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  const WaitGuard g{status, limit_ns, &abort_flag};
-  // Nothing ever arrives on `bar`: the wait must give up after limit_ns.
-  if (threadIdx.x == 0) mbar_wait(g, smem_u32(&bar), 0);
-  __syncthreads();
-}
-
 // Ring depth.  The shared-memory tables of the experts sit beside it, which
 // bounds E (RG_KGEMM_MAX_EXPERTS in rg.h; the host rejects larger E).
 constexpr int kStagesDeep = kCtaGroup == 2 ? 3 : 2;
@@ -482,15 +467,6 @@ cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const C
   cudaLaunchAttribute attr[1];
   fill_config(&cfg, attr, grid, smem_bytes<kStagesDeep>(args.E), stream);
   return cudaLaunchKernelEx(&cfg, kgemm_kernel<kCtaGroup, kStagesDeep>, tmG, tmX, tmD, args);
-}
-
-cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long limit_ns,
-                                 cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(32);
-  cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, wait_selftest_kernel, status, limit_ns);
 }
 
 }  // namespace rg
