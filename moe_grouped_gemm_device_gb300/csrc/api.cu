@@ -129,6 +129,26 @@ bool encode_sw(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr
   return r == CUDA_SUCCESS;
 }
 
+// Transposed weights w [G, K, N] (N contiguous) as read by the input-gradient
+// Mgemm: 64 columns x 64 K rows per box.  With N a multiple of 64 the map is
+// the 4-D view {64 cols, K, column block, group} (column-block stride 128
+// bytes), whose boxes of two column blocks land in shared memory exactly as
+// two 64-column boxes side by side: one copy per atom instead of two.
+// Returns the view used (1 = 4-D) or -1 when encoding fails.
+int encode_weight_t(CUtensorMap* m, const void* w, int G, int N, int K) {
+  if (N % 64 == 0) {
+    const uint64_t dims[4] = {64, static_cast<uint64_t>(K), static_cast<uint64_t>(N / 64),
+                              static_cast<uint64_t>(G)};
+    const uint64_t str[3] = {static_cast<uint64_t>(N) * 2, 128, static_cast<uint64_t>(K) * N * 2};
+    const uint32_t box[4] = {64, rg::mg::BK, rg::mg::BN_CTA / 64, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, w, dims, str, box) ? 1 : -1;
+  }
+  const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(G)};
+  const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K) * N * 2};
+  const uint32_t box[3] = {64, rg::mg::BK, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box) ? 0 : -1;
+}
+
 // Row-major bf16 [rows, cols] tensor, boxes of 64 columns x box_rows rows.
 bool encode_rows(CUtensorMap* m, const void* ptr, int64_t rows, int cols, uint32_t box_rows) {
   const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
@@ -161,6 +181,7 @@ rg::GroupArgs group_args(const DeviceState* ds, const int32_t* offsets, int E, i
   a.accumulate = 0;
   a.outer = 1;
   a.kg_wide = 0;
+  a.mg_wide_b = 0;
   return a;
 }
 
@@ -214,16 +235,15 @@ int mgemm_impl(const void* x, const void* w, const int32_t* offsets, int O, int 
     const uint32_t yb[3] = {64, 1, 32};
     if (!encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, yd, ys, yb)) return RG_ERR_INVALID_ARG;
   }
+  int wide_b = 0;
   if (!transpose_B) {  // w [G, N, K], K contiguous: one 64-wide K box of the tile's B rows per stage and CTA
     if (!encode_weight(&tmB, w, G, N, K, rg::mgemm_b_box_rows(false, N))) return RG_ERR_INVALID_ARG;
-  } else {  // w [G, K, N], N contiguous: 64-column boxes of 64 K rows
-    const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(G)};
-    const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K) * N * 2};
-    const uint32_t box[3] = {64, rg::mg::BK, 1};
-    if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box)) return RG_ERR_INVALID_ARG;
+  } else if ((wide_b = encode_weight_t(&tmB, w, G, N, K)) < 0) {  // w [G, K, N], N contiguous
+    return RG_ERR_INVALID_ARG;
   }
   rg::GroupArgs args = group_args(ds, offsets, L, M, N, K, y);
   args.outer = O;
+  args.mg_wide_b = wide_b;
   const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmAh, tmB, tmY, args, ds->mg_grid, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
@@ -301,14 +321,11 @@ int rg_mgemm_swiglu_dgrad(const void* dy, const void* w2, const int32_t* offsets
 
   CUtensorMap tmA, tmB, tmD;
   if (!encode_rows(&tmA, dy, M, K, rg::mg::BM)) return RG_ERR_INVALID_ARG;
-  {  // w2 [E, K, F], F contiguous: 64-column boxes of 64 K rows
-    const uint64_t dims[3] = {static_cast<uint64_t>(F), static_cast<uint64_t>(K), static_cast<uint64_t>(E)};
-    const uint64_t str[2] = {static_cast<uint64_t>(F) * 2, static_cast<uint64_t>(K) * F * 2};
-    const uint32_t box[3] = {64, rg::mg::BK, 1};
-    if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w2, dims, str, box)) return RG_ERR_INVALID_ARG;
-  }
+  const int wide_b = encode_weight_t(&tmB, w2, E, F, K);  // w2 [E, K, F], F contiguous
+  if (wide_b < 0) return RG_ERR_INVALID_ARG;
   if (!encode_rows(&tmD, dy13, M, 2 * F, 32)) return RG_ERR_INVALID_ARG;
   rg::GroupArgs args = group_args(ds, offsets, E, M, F, K, dy13);
+  args.mg_wide_b = wide_b;
   args.out2 = const_cast<void*>(y13);
   const cudaError_t e = rg::launch_mgemm_swiglu_dgrad(tmA, tmB, tmD, args, ds->mg_grid, stream);
   if (e != cudaSuccess) return fail_cuda(e);

@@ -26,6 +26,9 @@ struct GroupArgs {
   int kg_wide;              // Kgemm: 1 = operand maps are 4-D {64 cols, BR rows, column block,
                             // row} and one copy loads both 64-column boxes of a CTA (N and K
                             // multiples of 64); 0 = 3-D maps {cols, BR rows, row}, one copy per box
+  int mg_wide_b;            // Mgemm with transpose_B: 1 = the w map is 4-D {64 cols, K, column
+                            // block, group} and one copy loads both 64-column boxes of a CTA's
+                            // atom (N a multiple of 64); 0 = 3-D {N, K, group}, one copy per box
 };
 
 // Arguments of the MXFP8 Mgemm besides its tensor maps.

@@ -287,6 +287,8 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
               else tma_load_3d_cg<CG>(saj, am, fb, kc, o, row0);
               if constexpr (!TRANS_B) {
                 tma_load_3d_cg<CG>(sbj, &tmB, fb, kc, n0, eb);
+              } else if (args.mg_wide_b) {  // both 64-column boxes in one copy (4-D view)
+                tma_load_4d_cg<CG>(sbj, &tmB, fb, 0, kc, n0 / 64, eb);
               } else {
 #pragma unroll
                 for (int jj = 0; jj < BN_CTA / 64; ++jj)
@@ -604,9 +606,11 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
 }
 
 // every variant holds the tables of RG_MAX_EXPERTS_CFG groups beside its pipeline
+// (the 8-epilogue-warp and 64-column tiles exist for CTA pairs only)
 static_assert(Cfg<kCtaGroup, 256, 4>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 &&
-                  Cfg<kCtaGroup, 256, 8>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 &&
-                  Cfg<kCtaGroup, 64, 4>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448,
+                  (kCtaGroup == 1 ||
+                   (Cfg<kCtaGroup, 256, 8>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 &&
+                    Cfg<kCtaGroup, 64, 4>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448)),
               "an Mgemm variant exceeds the shared memory of a CTA at the largest group count");
 
 template <int BNT, int EPIW>
@@ -650,7 +654,8 @@ cudaError_t launch_variant(const CUtensorMap& tmA, const CUtensorMap& tmAh, cons
 
 }  // namespace
 
-size_t mgemm_smem_bytes(int E) {  // the largest of the variants (the default tile)
+size_t mgemm_smem_bytes(int E) {  // the largest of the variants built
+  if constexpr (kCtaGroup == 1) return smem_of<256, 4>(E);
   return std::max({smem_of<256, 4>(E), smem_of<256, 8>(E), smem_of<64, 4>(E)});
 }
 
