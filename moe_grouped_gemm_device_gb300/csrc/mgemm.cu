@@ -22,6 +22,9 @@
 //     bytes directly on the issuing CTA's stage barrier (.cta_group::2), and
 //     MMA completion is multicast to the barriers of both CTAs.
 //     CG = 1: one CTA computes a 128x256 tile (tcgen05 M=128), four 48 KB stages.
+//   * Transposed B (input gradient, w [E, K, N]) is read N-contiguous in
+//     64-column boxes; with N a multiple of 64 the map is a 4-D view whose
+//     box of two column blocks fills both boxes of a CTA's atom in one copy.
 //   * Half tiles (CTA pairs, plain epilogue): an expert's last row block of at
 //     most 128 rows runs as an M=128 pair MMA; each CTA loads only its 64 rows
 //     of A, through a second tensor map with 64-row boxes.
