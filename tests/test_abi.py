@@ -190,3 +190,50 @@ def test_oracle_blocked_sizes_match_the_library(lib):
         assert lib.rg_mx_blocked_bytes(R, KS, G) == oracle.mx_blocked_bytes(R, KS, G)
     for R, KS, G in ((300, 10, 3), (2560, 1024, 32), (1, 1, 1)):
         assert lib.rg_mx_blocked_k_bytes(R, KS, G) == oracle.mx_blocked_k_bytes(R, KS, G)
+
+
+def host_calls():
+    """Every compute entry point of the binding, called with host (CPU)
+    tensors of the right types and shapes."""
+    import torch
+    bf, u8, i32 = torch.bfloat16, torch.uint8, torch.int32
+    off = torch.tensor([0, 32, 64], dtype=i32)
+    x, w = torch.zeros(64, 64, dtype=bf), torch.zeros(2, 64, 64, dtype=bf)
+    q, wq, s = torch.zeros(64, 64, dtype=u8), torch.zeros(2, 64, 64, dtype=u8), torch.zeros(4096, dtype=u8)
+    return {
+        "mgemm": lambda: rg.mgemm(x, w, off),
+        "mgemm_dgrad": lambda: rg.mgemm(x, w, off, transpose_B=True),
+        "mgemm_nested": lambda: rg.mgemm_nested(torch.zeros(64, 128, dtype=bf),
+                                                torch.zeros(2, 2, 64, 64, dtype=bf), off),
+        "mgemm_swiglu": lambda: rg.mgemm_swiglu(x, torch.zeros(2, 128, 64, dtype=bf), off),
+        "mgemm_swiglu_dgrad": lambda: rg.mgemm_swiglu_dgrad(x, w, off, torch.zeros(64, 128, dtype=bf)),
+        "kgemm": lambda: rg.kgemm(x, x, off),
+        "mgemm_mxfp8": lambda: rg.mgemm_mxfp8(q, s, wq, s, off),
+        "kgemm_mxfp8": lambda: rg.kgemm_mxfp8(q, s, q, s, off),
+        "mx_scales_blocked": lambda: rg.mx_scales_blocked(torch.zeros(64, 2, dtype=u8), off),
+        "mx_scales_blocked_k": lambda: rg.mx_scales_blocked_k(torch.zeros(64, 2, dtype=u8), off),
+    }
+
+
+@pytest.mark.parametrize("name", sorted(host_calls()))
+def test_binding_refuses_host_tensors(lib, name):
+    """No CPU fallback: every compute call refuses host tensors loudly
+    instead of computing anything."""
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        host_calls()[name]()
+
+
+def test_binding_checks_types_and_shapes(lib):
+    """Type and rank checks come before the device check (host tensors here,
+    so only the first argument's checks are reachable)."""
+    import torch
+    off = torch.tensor([0, 32, 64], dtype=torch.int32)
+    x, w = torch.zeros(64, 64, dtype=torch.bfloat16), torch.zeros(2, 64, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError, match="bfloat16"):
+        rg.mgemm(x.float(), w, off)
+    with pytest.raises(ValueError, match="2-D"):
+        rg.mgemm(x[0], w, off)
+    with pytest.raises(TypeError, match="torch.Tensor"):
+        rg.kgemm([0], x, off)
+    with pytest.raises(TypeError, match="uint8"):
+        rg.mx_scales_blocked(torch.zeros(64, 2, dtype=torch.int8), off)
