@@ -43,6 +43,8 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 L2_BYTES = 129 * 2**20
+L2_FLUSH_BYTES = 512 * 2**20
+METRIC = "grouped GEMM TFLOP/s (fwd/dgrad/wgrad), 1 GPU"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_OF = {"mgemm": "mgemm_kernel<false>", "mgemm_t": "mgemm_kernel<true>", "kgemm": "kgemm_kernel",
              "swiglu": "mgemm_kernel<false,swiglu>", "swiglu_bwd": "mgemm_kernel<true,swiglu_bwd>",
@@ -57,10 +59,26 @@ FP8_KERNELS = ("mx_mgemm_kernel<false>", "mx_mgemm_kernel<true>", "mx_kgemm_kern
 CONVERSION_KERNELS = ("mx_blocked_kernel", "mx_blocked_k_kernel")
 
 
-def tensor_peak(kernel: str, peaks) -> float:
-    """Sustained dense tensor peak of the kernel's input type: the measured
-    bf16 figure, times the nominal dense FP8/BF16 ratio (4.5 / 2.25) for FP8."""
-    return peaks["bf16_tflops_sustained"] * (2.0 if kernel in FP8_KERNELS else 1.0)
+PEAK_KEY = {"burst": "bf16_tflops", "sustained": "bf16_tflops_sustained"}
+# A timed region shorter than this runs at burst clocks whatever the clock
+# record says: the power cap takes seconds of load to bring the clocks down.
+SUSTAINED_MIN_S = 1.0
+
+
+def peak_kind(timed_s: float, clocks) -> str:
+    """Which measured tensor peak a timed region is compared with: 'sustained'
+    (the seconds-long power-capped GEMM loop) when the region lasted at least
+    SUSTAINED_MIN_S and the clock record saw the power cap during it, else
+    'burst' (the GEMM timed alone at full clocks)."""
+    capped = bool(clocks) and "sw_power_cap" in clocks.get("reasons", [])
+    return "sustained" if timed_s >= SUSTAINED_MIN_S and capped else "burst"
+
+
+def tensor_peak(kernel: str, peaks, kind: str = "sustained") -> float:
+    """Dense tensor peak of the kernel's input type: the measured bf16 figure
+    of the given kind, times the nominal dense FP8/BF16 ratio (4.5 / 2.25) for
+    FP8."""
+    return peaks[PEAK_KEY[kind]] * (2.0 if kernel in FP8_KERNELS else 1.0)
 
 
 def parse():
@@ -74,6 +92,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU baseline budget")
     p.add_argument("--ops", default="", help="comma-separated subset of the step's ops (profiling)")
+    p.add_argument("--no-extra", dest="extra", action="store_false",
+                   help="time only the headline workload (not the uniform and skewed shapes after it)")
     return p.parse_args()
 
 
@@ -200,8 +220,10 @@ class ClockSampler:
 
 def oracle_sample_step(wl, tensors, budget_s: float, rng) -> tuple[float, float, str]:
     """Run the oracle on a sample of every op's outputs; return (flops, seconds,
-    description).  Rows / (expert, n) pairs are drawn uniformly at random; the
-    count per op is sized to the time budget from a one-row probe."""
+    description), the seconds and flops covering all the oracle work done
+    (a one-row-per-thread probe that sizes the sample, then the sample).  Rows
+    / (expert, n) pairs are drawn uniformly at random; the count per op is
+    sized to the time budget from the probe."""
     import oracle
     off = wl.offsets
     counts = wl.counts
@@ -256,11 +278,9 @@ def oracle_sample_step(wl, tensors, budget_s: float, rng) -> tuple[float, float,
         f = run(max(1, oracle.num_threads()))
         dt = time.perf_counter() - t0
         n = max(1, int(oracle.num_threads() * per_op / max(dt, 1e-6)))
-        t0 = time.perf_counter()
-        f = run(n)
-        dt = time.perf_counter() - t0
+        f += run(n)
         flops += f
-        secs += dt
+        secs += time.perf_counter() - t0
         desc.append(f"{op.name}:{n}")
     return flops, secs, "random outputs per op (" + ", ".join(desc) + ")"
 
@@ -275,31 +295,55 @@ def cpu_baseline(wl, tensors, budget_s: float) -> dict:
                       f"rows of dW x all K; {secs:.1f} s of FP64 CPU work"}
 
 
+def config_of(wl) -> dict:
+    """The workload description both arms print (no measured quantity)."""
+    ws = working_set_bytes(wl)
+    return {"workload": workload_desc(wl), "flops_per_step": wl.flops(),
+            "l2": f"inputs larger than L2: step working set {ws / 1e9:.2f} GB vs 129 MB L2" if ws >= 4 * L2_BYTES
+                  else f"L2 flushed between steps (a {L2_FLUSH_BYTES >> 20} MB buffer is written; "
+                       f"step working set {ws / 1e6:.0f} MB)"}
+
+
+def reference_budget_s(steps: int, warmup: int) -> float:
+    """Seconds of oracle work per step: the whole run stays within about
+    1.5 minutes of CPU time (at least 0.05 s a step, at most 2 s)."""
+    return max(0.05, min(2.0, 90.0 / max(1, steps + warmup)))
+
+
 def run_reference(args, wl):
+    """The reference arm: the CPU oracle, as it stands, timed on the host
+    cores.  Each step is a bounded sample of the workload (random output rows
+    of every op), so `ms_per_step` is the wall time of the oracle work a step
+    actually did and `value` that work's rate; the time the oracle would take
+    for a whole step at that rate is reported beside it."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     tensors = {k: wl.tensor(k) for k in wl.tensors}
-    per_step = max(0.05, min(2.0, 90.0 / max(1, args.steps + args.warmup)))
+    per_step = reference_budget_s(args.steps, args.warmup)
     rng = np.random.default_rng(99)
     for _ in range(args.warmup):
         oracle_sample_step(wl, tensors, per_step, rng)
-    tot_f, tot_s, desc = 0.0, 0.0, ""
+    tot_f, desc = 0.0, ""
+    t0 = time.perf_counter()
     for _ in range(args.steps):
-        f, s, desc = oracle_sample_step(wl, tensors, per_step, rng)
+        f, _, desc = oracle_sample_step(wl, tensors, per_step, rng)
         tot_f += f
-        tot_s += s
+    wall = time.perf_counter() - t0
     import oracle
-    value = tot_f / tot_s / 1e12
+    value = tot_f / wall / 1e12
     line = {
-        "impl": "reference", "metric": "grouped GEMM TFLOP/s (fwd/dgrad/wgrad), 1 GPU",
+        "impl": "reference", "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * wl.flops() / (value * 1e12),
+        "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
+        "sample_flops_per_step": tot_f / args.steps,
+        "extrapolated_ms_per_full_step": 1e3 * wl.flops() / (value * 1e12),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": workload_desc(wl)},
+        "config": config_of(wl),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
-                         "kind": "oracle", "sample": f"each step: {desc}"},
+                         "kind": "oracle",
+                         "sample": f"each step: {desc}; {per_step:.2f} s budget of FP64 CPU work"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -309,10 +353,11 @@ def run_reference(args, wl):
 # ------------------------------------------------------------------ GPU path
 
 
-def traffic_for(kernel: str, op_names):
-    """Mean per-launch DRAM bytes of `kernel` over the given ops, from the
-    committed ncu captures (profiles/traffic.json), if they were taken on the
-    current source of that kernel and cover every op; else None."""
+def traffic_for(kernel: str, op_names, workload: str):
+    """Mean per-launch DRAM bytes of `kernel` over the given ops of a workload,
+    from the committed ncu captures (profiles/traffic.json), if they were
+    taken on the current source of that kernel and cover every op; else
+    None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -322,7 +367,7 @@ def traffic_for(kernel: str, op_names):
     src = os.path.join(ROOT, "moe_grouped_gemm_device_gb300", "csrc", KERNEL_SOURCES[kernel])
     if ent.get("source_sha256_16") != hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]:
         return None
-    per_op = ent.get("per_op", {})
+    per_op = ent.get("workloads", {}).get(workload, {})
     if not op_names or any(o not in per_op for o in op_names):
         return None
     return sum(per_op[o] for o in op_names) // len(op_names)
@@ -351,6 +396,10 @@ class Unit:
 
     def __init__(self, name, kernel, flops, nbytes, call, op=None):
         self.name, self.kernel, self.flops, self.bytes, self.call, self.op = name, kernel, flops, nbytes, call, op
+
+    @property
+    def launches(self) -> int:
+        return 2 if self.kernel in CONVERSION_KERNELS else 1
 
 
 def build_units(wl, rg, tensors, outs, off_ref, scratch):
@@ -408,6 +457,251 @@ def build_units(wl, rg, tensors, outs, off_ref, scratch):
     return units
 
 
+def as_torch(a):
+    """bf16 bit patterns (uint16) or FP8 / E8M0 codes (uint8) as a torch tensor."""
+    import torch
+    if a.dtype == np.uint8:
+        return torch.from_numpy(a)
+    return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+
+
+def make_buffers(wl, rg, dev):
+    """Output tensors of every op and the scale-layout buffers (MXFP8)."""
+    import torch
+    outs, scratch = {}, {}
+    for op in wl.ops:
+        if op.kind in ("kgemm", "mxk"):
+            # a main grad that steps accumulate into starts at zero
+            alloc = torch.zeros if getattr(op, "accumulate", False) else torch.empty
+            outs[op.name] = alloc((wl.E, op.N, op.K), dtype=torch.float32, device=dev)
+        elif op.kind == "nested":
+            outs[op.name] = torch.empty((wl.M, op.outer * op.N), dtype=torch.bfloat16, device=dev)
+        elif op.fuse == "swiglu":
+            outs[op.name] = torch.empty((wl.M, op.N // 2), dtype=torch.bfloat16, device=dev)
+            outs[op.name + ":y13"] = torch.empty((wl.M, op.N), dtype=torch.bfloat16, device=dev)
+        elif op.fuse == "swiglu_bwd":
+            outs[op.name] = torch.empty((wl.M, 2 * op.N), dtype=torch.bfloat16, device=dev)
+        else:
+            outs[op.name] = torch.empty((wl.M, op.N), dtype=torch.bfloat16, device=dev)
+        if op.kind == "mx":
+            KS = op.K // 32
+            scratch[op.name + ":sa"] = torch.empty((rg.mx_blocked_bytes(wl.M, KS, wl.E),), dtype=torch.uint8,
+                                                   device=dev)
+            scratch[op.name + ":sb"] = torch.empty((rg.mx_blocked_bytes(wl.E * op.N, KS, wl.E),),
+                                                   dtype=torch.uint8, device=dev)
+            scratch["woff:" + str(op.N)] = rg.mx_weight_offsets(wl.E, op.N, device=dev)
+        if op.kind == "mxk":
+            MS = wl.M // 32
+            scratch[op.name + ":sa"] = torch.empty((rg.mx_blocked_k_bytes(op.N, MS, wl.E),),
+                                                   dtype=torch.uint8, device=dev)
+            scratch[op.name + ":sb"] = torch.empty((rg.mx_blocked_k_bytes(op.K, MS, wl.E),),
+                                                   dtype=torch.uint8, device=dev)
+    return outs, scratch
+
+
+class Timed:
+    """What one timed region measured: the region's length (max over ranks),
+    the [steps, units] launch durations and the clock record."""
+
+    def __init__(self, ms, unit_ms, clocks):
+        self.ms, self.unit_ms, self.clocks = ms, unit_ms, clocks
+
+
+def time_steps(units, steps, warmup, rg, stream, dev, dist, rank, local, flush=None) -> Timed:
+    """W warm-up steps, then K timed steps between a barrier and a device
+    synchronisation on both sides, with CUDA events around every launch on the
+    launching stream.  With `flush` (a device buffer larger than L2) the buffer
+    is rewritten before every step and the region's length is the sum of the
+    launch durations, which excludes the flushes."""
+    import torch
+    nu = len(units)
+
+    def step(evs=None):
+        if flush is not None:
+            flush.fill_(1)
+        for i, u in enumerate(units):
+            if evs is not None:
+                evs[i].record(stream)
+            u.call()
+        if evs is not None:
+            evs[nu].record(stream)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = rg.device_status()
+    if status:
+        raise SystemExit(f"device status {status:#x} after warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nu + 1)] for _ in range(steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for s in range(steps):
+        step(evs[s])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    status = rg.device_status()
+    if status:
+        raise SystemExit(f"device status {status:#x} after the timed region")
+    unit_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(nu)] for e in evs])
+    ms = float(unit_ms.sum()) if flush is not None else evs[0][0].elapsed_time(evs[-1][nu])
+    return Timed(slowest_rank_ms(ms, dist, dev), unit_ms, clocks)
+
+
+def analyse(wl, units, t: Timed, steps: int, world: int, peaks, peak_src) -> dict:
+    """Throughput, per-op rates and the roofline of the dominant kernel of one
+    timed region.  The tensor peak is the measured burst or sustained figure,
+    chosen by the region's length and clock record (peak_kind)."""
+    ms_per_step = t.ms / steps
+    kind = peak_kind(t.ms * 1e-3, t.clocks)
+    per_unit_ms = t.unit_ms.mean(axis=0)
+    step_ms = t.unit_ms.sum(axis=1)
+    per_kernel, per_op = {}, {}
+    for i, u in enumerate(units):
+        ent = per_kernel.setdefault(u.kernel, {"ms": 0.0, "flops": 0, "bytes": 0, "launches": 0, "ops": []})
+        ent["ms"] += per_unit_ms[i]
+        ent["flops"] += u.flops
+        ent["bytes"] += u.bytes
+        ent["launches"] += 1
+        ent["ops"].append(u.name)
+        sec = per_unit_ms[i] * 1e-3
+        med, p10 = float(np.median(t.unit_ms[:, i])), float(np.percentile(t.unit_ms[:, i], 10))
+        gbs = u.bytes / sec / 1e9
+        rec = {"ms": round(float(per_unit_ms[i]), 4), "ms_median": round(med, 4), "ms_best_decile": round(p10, 4),
+               "algorithmic_gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        if u.flops:
+            tf = u.flops / sec / 1e12
+            rec["tflops"] = round(tf, 1)
+            rec["tflops_median"] = round(u.flops / (med * 1e-3) / 1e12, 1)
+            rec["tflops_best_decile"] = round(u.flops / (p10 * 1e-3) / 1e12, 1)
+            rec["frac_burst"] = round(tf / tensor_peak(u.kernel, peaks, "burst"), 4)
+            rec["frac_sustained"] = round(tf / tensor_peak(u.kernel, peaks, "sustained"), 4)
+        per_op[u.name] = rec
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
+    de = per_kernel[dom]
+    fp8 = dom in FP8_KERNELS
+    peak = tensor_peak(dom, peaks, kind)
+    src = "MEASURED_PEAKS.json" if peak_src == "measured" else "fallback"
+    peak_name = (f"measured bf16 {kind} x 2 (nominal dense FP8/BF16 ratio 4.5/2.25; {src})" if fp8
+                 else f"measured bf16 {kind} ({src})")
+    # The kernel's bound: tensor cores when its arithmetic intensity is above
+    # the ridge of the measured peaks, HBM below it (e.g. LoRA rank-16 GEMMs).
+    ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tflops = de["flops"] / (de["ms"] * 1e-3) / 1e12
+    gbs = de["bytes"] / (de["ms"] * 1e-3) / 1e9
+    if de["flops"] / de["bytes"] >= ridge:
+        roofline = {"bound": "tensor", "achieved": round(tflops, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+                    "frac": round(tflops / peak, 4), "peak_kind": kind, "peak_source": peak_name}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{src} HBM copy"}
+    roofline.update({
+        "frac_of_burst": round(tflops / tensor_peak(dom, peaks, "burst"), 4) if de["flops"] else None,
+        "frac_of_sustained": round(tflops / tensor_peak(dom, peaks, "sustained"), 4) if de["flops"] else None,
+        "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+        "traffic": traffic_for(dom, de["ops"], wl.name), "kernel": dom, "launches_per_step": de["launches"],
+        "algorithmic_flops_per_launch": de["flops"] // de["launches"],
+        "algorithmic_bytes_per_launch": de["bytes"] // de["launches"],
+        "share_of_step": round(de["ms"] / float(per_unit_ms.sum()), 3)})
+    value = job_throughput(wl.flops(), ms_per_step, world)
+    step_peak = peaks[PEAK_KEY[kind]] * (2.0 if any(u.kernel in FP8_KERNELS for u in units) else 1.0)
+    return {"value": round(value, 2), "ms_per_step": round(ms_per_step, 5),
+            "step_ms_median": round(float(np.median(step_ms)), 5),
+            "step_ms_best_decile": round(float(np.percentile(step_ms, 10)), 5),
+            "timed_region_s": round(t.ms * 1e-3, 4),
+            "peak_kind": kind, f"pct_of_{kind}_peak": round(100 * value / world / step_peak, 1),
+            "roofline": roofline, "per_op": per_op,
+            "gpu_launches": sum(u.launches for u in units) * steps, "clocks": t.clocks}
+
+
+def prepare(wl, rg, dev):
+    """Seeded inputs generated on the host and made resident in HBM; outputs
+    and the units of one step."""
+    import torch
+    host = {k: wl.tensor(k) for k in wl.tensors}
+    d = {k: as_torch(v).to(dev) for k, v in host.items()}
+    off = torch.from_numpy(wl.offsets).to(dev)
+    outs, scratch = make_buffers(wl, rg, dev)
+    off_used = [off]
+    units = build_units(wl, rg, d, outs, off_used, scratch)
+    return host, d, off_used, outs, units
+
+
+def end_to_end(wl, rg, dev, host, d, off_used, outs, units, stream, e2e_steps) -> dict:
+    """The same step through the public API with host buffers: every step
+    copies its inputs from pinned host memory, runs the ops and copies every
+    output back.  Consecutive steps are pipelined over two device buffer sets:
+    step i's host->device copies (one stream) overlap step i-1's kernels (the
+    compute stream) and step i-2's device->host copies (a third stream);
+    events order each buffer set's reuse."""
+    import torch
+    pin = {k: as_torch(v).pin_memory() for k, v in host.items()}
+    pin_off = torch.from_numpy(wl.offsets).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pin.values()) + pin_off.numel() * 4
+    d1 = {k: torch.empty_like(v) for k, v in d.items()}
+    off1 = [torch.empty_like(off_used[0])]
+    outs1, scratch1 = make_buffers(wl, rg, dev)
+    sets = [(d, off_used, outs, units), (d1, off1, outs1, build_units(wl, rg, d1, outs1, off1, scratch1))]
+    pin_out = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in o.items()} for _, _, o, _ in sets]
+    d2h = sum(t.numel() * t.element_size() for t in pin_out[0].values())
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = [{n: torch.cuda.Event() for n in ("h2d", "comp", "d2h")} for _ in sets]
+    started = [False, False]
+
+    def e2e_step(i):
+        b = i & 1
+        dd, oo, outs_b, units_b = sets[b]
+        e = ev[b]
+        with torch.cuda.stream(s_h2d):
+            if started[b]:
+                s_h2d.wait_event(e["comp"])  # step i-2's kernels are done with this input set
+            for k, t in pin.items():
+                dd[k].copy_(t, non_blocking=True)
+            oo[0].copy_(pin_off, non_blocking=True)
+            e["h2d"].record(s_h2d)
+        stream.wait_event(e["h2d"])
+        if started[b]:
+            stream.wait_event(e["d2h"])  # step i-2's outputs have left this set
+        for u in units_b:
+            u.call()
+        e["comp"].record(stream)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(e["comp"])
+            for k, t in outs_b.items():
+                pin_out[b][k].copy_(t, non_blocking=True)
+            e["d2h"].record(s_d2h)
+        started[b] = True
+
+    for i in range(2):  # warm both buffer sets
+        e2e_step(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_h2d)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    stream.wait_stream(s_d2h)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e_ms = a.elapsed_time(b) / e2e_steps
+    status = rg.device_status()
+    if status:
+        raise SystemExit(f"device status {status:#x} after the end-to-end steps")
+    return {"value": wl.flops() / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": e_ms, "pipelined": "h2d / kernels / d2h of consecutive steps on three streams"}
+
+
+# The other benchmark shapes, timed after the headline step in the same run:
+# uniform groups (8 x 4096 and 16 x 2048 rows, n=768, k=2048: the shape of the
+# TransformerEngine PR's grouped-GEMM table) and the skewed Zipf(1.2) layer.
+EXTRA_WORKLOADS = ("uniform8", "uniform16", "skewed")
+
+
 def main():
     args = parse()
     wl = W.ALL[args.workload]()
@@ -423,7 +717,6 @@ def main():
 
     import torch
     import moe_grouped_gemm_device_gb300 as rg
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -435,252 +728,69 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     rg.load()
-
-    # ---- inputs: seeded on the host, then resident in HBM -------------------
-    host = {k: wl.tensor(k) for k in wl.tensors}
-    off_np = wl.offsets
-    counts = wl.counts
-
-    def as_torch(a):  # bf16 bit patterns (uint16) or FP8 / E8M0 codes (uint8)
-        if a.dtype == np.uint8:
-            return torch.from_numpy(a)
-        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
-
-    d = {k: as_torch(v).to(dev) for k, v in host.items()}
-    off = torch.from_numpy(off_np).to(dev)
-    is_mx = any(op.kind in ("mx", "mxk") for op in wl.ops)
-
-    def make_buffers():
-        """Output tensors of every op and the scale-layout buffers (MXFP8)."""
-        outs, scratch = {}, {}
-        for op in wl.ops:
-            if op.kind in ("kgemm", "mxk"):
-                # a main grad that steps accumulate into starts at zero
-                alloc = torch.zeros if getattr(op, "accumulate", False) else torch.empty
-                outs[op.name] = alloc((wl.E, op.N, op.K), dtype=torch.float32, device=dev)
-            elif op.kind == "nested":
-                outs[op.name] = torch.empty((wl.M, op.outer * op.N), dtype=torch.bfloat16, device=dev)
-            elif op.fuse == "swiglu":
-                outs[op.name] = torch.empty((wl.M, op.N // 2), dtype=torch.bfloat16, device=dev)
-                outs[op.name + ":y13"] = torch.empty((wl.M, op.N), dtype=torch.bfloat16, device=dev)
-            elif op.fuse == "swiglu_bwd":
-                outs[op.name] = torch.empty((wl.M, 2 * op.N), dtype=torch.bfloat16, device=dev)
-            else:
-                outs[op.name] = torch.empty((wl.M, op.N), dtype=torch.bfloat16, device=dev)
-            if op.kind == "mx":
-                KS = op.K // 32
-                scratch[op.name + ":sa"] = torch.empty((rg.mx_blocked_bytes(wl.M, KS, wl.E),), dtype=torch.uint8,
-                                                       device=dev)
-                scratch[op.name + ":sb"] = torch.empty((rg.mx_blocked_bytes(wl.E * op.N, KS, wl.E),),
-                                                       dtype=torch.uint8, device=dev)
-                scratch["woff:" + str(op.N)] = rg.mx_weight_offsets(wl.E, op.N, device=dev)
-            if op.kind == "mxk":
-                MS = wl.M // 32
-                scratch[op.name + ":sa"] = torch.empty((rg.mx_blocked_k_bytes(op.N, MS, wl.E),),
-                                                       dtype=torch.uint8, device=dev)
-                scratch[op.name + ":sb"] = torch.empty((rg.mx_blocked_k_bytes(op.K, MS, wl.E),),
-                                                       dtype=torch.uint8, device=dev)
-        return outs, scratch
-
-    outs, scratch = make_buffers()
     stream = torch.cuda.current_stream(dev)
-    off_used = [off]
-    units = build_units(wl, rg, d, outs, off_used, scratch)
-    nu = len(units)
+    peaks, peak_src = load_peaks()
 
-    def step(evs=None):
-        for i, u in enumerate(units):
-            if evs is not None:
-                evs[i].record(stream)
-            u.call()
-        if evs is not None:
-            evs[nu].record(stream)
+    def flush_buffer(w):
+        if working_set_bytes(w) >= 4 * L2_BYTES:
+            return None
+        return torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    status = rg.device_status()
-    if status:
-        raise SystemExit(f"device status {status:#x} after warm-up")
-
-    # ---- timed region -------------------------------------------------------
-    # Events around every launch, on the launching stream, give the per-kernel
-    # durations of the timed steps themselves.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nu + 1)] for _ in range(args.steps)]
-    sampler = ClockSampler(local) if rank == 0 else None
-    if sampler:
-        sampler.start()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    for s in range(args.steps):
-        step(evs[s])
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ms = evs[0][0].elapsed_time(evs[-1][nu])
-    clocks = sampler.stop() if sampler else None
-    status = rg.device_status()
-    if status:
-        raise SystemExit(f"device status {status:#x} after timed region")
-    # [steps, units] launch durations; the mean feeds the throughput and the
-    # roofline, the median and best decile (10th percentile of the duration)
-    # describe the spread
-    unit_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(nu)] for e in evs])
-    per_unit_ms = unit_ms.mean(axis=0)
-    step_ms = unit_ms.sum(axis=1)
-    ms = slowest_rank_ms(ms, dist, dev)
-    ms_per_step = ms / args.steps
-    flops_step = wl.flops()
-    value = job_throughput(flops_step, ms_per_step, world)
-
-    # ---- end to end through the public API with host buffers ---------------
-    # Every step copies its inputs from pinned host memory, runs the ops and
-    # copies every output back.  Consecutive steps are pipelined over two
-    # device buffer sets: step i's host->device copies (one stream) overlap
-    # step i-1's kernels (the compute stream) and step i-2's device->host
-    # copies (a third stream); events order each buffer set's reuse.
+    # ---- headline workload: inputs resident in HBM --------------------------
+    host, d, off_used, outs, units = prepare(wl, rg, dev)
+    t = time_steps(units, args.steps, args.warmup, rg, stream, dev, dist, rank, local, flush_buffer(wl))
+    res = analyse(wl, units, t, args.steps, world, peaks, peak_src)
     e2e = None
     if rank == 0 and args.e2e_steps > 0:
-        pin = {k: as_torch(v).pin_memory() for k, v in host.items()}
-        pin_off = torch.from_numpy(off_np).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in pin.values()) + pin_off.numel() * 4
-        d1 = {k: torch.empty_like(v) for k, v in d.items()}
-        off1 = [torch.empty_like(off)]
-        outs1, scratch1 = make_buffers()
-        sets = [(d, off_used, outs, units), (d1, off1, outs1, build_units(wl, rg, d1, outs1, off1, scratch1))]
-        pin_out = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in o.items()} for _, _, o, _ in sets]
-        d2h = sum(t.numel() * t.element_size() for t in pin_out[0].values())
-        s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev = [{n: torch.cuda.Event() for n in ("h2d", "comp", "d2h")} for _ in sets]
-        started = [False, False]
+        e2e = end_to_end(wl, rg, dev, host, d, off_used, outs, units, stream, args.e2e_steps)
+    del host, d, off_used, outs, units
+    torch.cuda.empty_cache()
 
-        def e2e_step(i):
-            b = i & 1
-            dd, oo, outs_b, units_b = sets[b]
-            e = ev[b]
-            with torch.cuda.stream(s_h2d):
-                if started[b]:
-                    s_h2d.wait_event(e["comp"])  # step i-2's kernels are done with this input set
-                for k, t in pin.items():
-                    dd[k].copy_(t, non_blocking=True)
-                oo[0].copy_(pin_off, non_blocking=True)
-                e["h2d"].record(s_h2d)
-            stream.wait_event(e["h2d"])
-            if started[b]:
-                stream.wait_event(e["d2h"])  # step i-2's outputs have left this set
-            for u in units_b:
-                u.call()
-            e["comp"].record(stream)
-            with torch.cuda.stream(s_d2h):
-                s_d2h.wait_event(e["comp"])
-                for k, t in outs_b.items():
-                    pin_out[b][k].copy_(t, non_blocking=True)
-                e["d2h"].record(s_d2h)
-            started[b] = True
-
-        for i in range(2):  # warm both buffer sets
-            e2e_step(i)
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(s_h2d)
-        for i in range(args.e2e_steps):
-            e2e_step(i)
-        stream.wait_stream(s_d2h)
-        b.record(stream)
-        torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b) / args.e2e_steps
-        e2e = {"value": flops_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e_ms, "pipelined": "h2d / kernels / d2h of consecutive steps on three streams"}
-        status = rg.device_status()
-        if status:
-            raise SystemExit(f"device status {status:#x} after the end-to-end steps")
+    # ---- the other benchmark shapes ------------------------------------------
+    per_config = {}
+    if args.extra and args.workload == "a3b" and not args.ops:
+        for name in EXTRA_WORKLOADS:
+            xw = W.ALL[name]()
+            _, _, _, _, xu = prepare(xw, rg, dev)
+            xt = time_steps(xu, args.steps, args.warmup, rg, stream, dev, dist, rank, local, flush_buffer(xw))
+            xr = analyse(xw, xu, xt, args.steps, world, peaks, peak_src)
+            per_config[name] = {"metric": METRIC, "unit": "TFLOP/s", "config": config_of(xw), **xr}
+            del xu
+            torch.cuda.empty_cache()
 
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return 0
 
-    # ---- roofline of the dominant kernel ------------------------------------
-    peaks, peak_src = load_peaks()
-    per_kernel = {}
-    per_op = {}
-    for i, u in enumerate(units):
-        ent = per_kernel.setdefault(u.kernel, {"ms": 0.0, "flops": 0, "bytes": 0, "launches": 0, "ops": []})
-        ent["ms"] += per_unit_ms[i]
-        ent["flops"] += u.flops
-        ent["bytes"] += u.bytes
-        ent["launches"] += 1
-        ent["ops"].append(u.name)
-        sec = per_unit_ms[i] * 1e-3
-        med, p10 = float(np.median(unit_ms[:, i])), float(np.percentile(unit_ms[:, i], 10))
-        rec = {"ms": round(float(per_unit_ms[i]), 4), "ms_median": round(med, 4), "ms_best_decile": round(p10, 4),
-               "algorithmic_gbs": round(u.bytes / sec / 1e9, 1)}
-        if u.flops:
-            pk = tensor_peak(u.kernel, peaks)
-            rec["tflops"] = round(u.flops / sec / 1e12, 1)
-            rec["tflops_median"] = round(u.flops / (med * 1e-3) / 1e12, 1)
-            rec["tflops_best_decile"] = round(u.flops / (p10 * 1e-3) / 1e12, 1)
-            rec["pct_peak_sustained"] = round(100 * u.flops / sec / 1e12 / pk, 1)
-        per_op[u.name] = rec
-    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
-    de = per_kernel[dom]
-    traffic = traffic_for(dom, de["ops"])
-    fp8 = dom in FP8_KERNELS
-    peak = tensor_peak(dom, peaks)
-    peak_name = ("measured bf16 sustained x 2 (nominal dense FP8/BF16 ratio 4.5/2.25; MEASURED_PEAKS.json)" if fp8
-                 else "measured bf16 sustained (MEASURED_PEAKS.json)")
-    # The kernel's bound: tensor cores when its arithmetic intensity is above
-    # the ridge of the measured peaks, HBM below it (e.g. LoRA rank-16 GEMMs).
-    ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if de["flops"] / de["bytes"] >= ridge:
-        achieved = de["flops"] / (de["ms"] * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
-                    "frac": round(achieved / peak, 4),
-                    "peak_source": peak_name if peak_src == "measured" else "fallback 1.7 PFLOP/s sustained",
-                    "frac_of_burst": round(achieved / (peaks["bf16_tflops"] * (2 if fp8 else 1)), 4)}
-    else:
-        achieved = de["bytes"] / (de["ms"] * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(achieved / peaks["hbm_gbs"], 4),
-                    "peak_source": f"{peak_src} HBM copy (MEASURED_PEAKS.json)" if peak_src == "measured"
-                    else "fallback 6.8 TB/s"}
-    roofline.update({"traffic": traffic, "kernel": dom, "launches_per_step": de["launches"],
-                     "algorithmic_flops_per_launch": de["flops"] // de["launches"],
-                     "algorithmic_bytes_per_launch": de["bytes"] // de["launches"],
-                     "share_of_step": round(de["ms"] / float(per_unit_ms.sum()), 3)})
-
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(wl, host, args.cpu_seconds)
+        cpu = cpu_baseline(wl, {k: wl.tensor(k) for k in wl.tensors}, args.cpu_seconds)
 
     line = {
-        "metric": "grouped GEMM TFLOP/s (fwd/dgrad/wgrad), 1 GPU",
-        "value": round(value, 2),
+        "metric": METRIC,
+        "value": res["value"],
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 5),
-        "step_ms_median": round(float(np.median(step_ms)), 5),
-        "step_ms_best_decile": round(float(np.percentile(step_ms, 10)), 5),
+        "ms_per_step": res["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3 (MXFP8: E8M0 scale per 32)" if is_mx else "bf16",
-        "data": "synthetic (seeded random E4M3 codes and E8M0 scales)" if is_mx
+        "dtype": "e4m3 (MXFP8: E8M0 scale per 32)" if any(op.kind in ("mx", "mxk") for op in wl.ops) else "bf16",
+        "data": "synthetic (seeded random E4M3 codes and E8M0 scales)"
+                if any(op.kind in ("mx", "mxk") for op in wl.ops)
                 else "synthetic (seeded normal inputs, random-init weights)",
-        "config": {"workload": workload_desc(wl),
-                   "flops_per_step": flops_step,
-                   "l2": f"inputs larger than L2: step working set {working_set_bytes(wl) / 1e9:.2f} GB vs 129 MB L2",
-                   "pct_of_peak_sustained": round(100 * value / world / peak, 1)},
-        "roofline": roofline,
+        "config": config_of(wl),
+        "roofline": res["roofline"],
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": sum(2 if u.kernel in CONVERSION_KERNELS else 1 for u in units) * args.steps,
-        "clocks": clocks,
-        "per_op": per_op,
+        "gpu_launches": res["gpu_launches"],
+        "clocks": res["clocks"],
+        **{k: res[k] for k in ("step_ms_median", "step_ms_best_decile", "timed_region_s", "peak_kind",
+                               f"pct_of_{res['peak_kind']}_peak", "per_op")},
+        "per_config": per_config or None,
     }
     print(json.dumps(line), flush=True)
     if dist:

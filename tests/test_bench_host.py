@@ -21,29 +21,72 @@ def fake_tree(tmp_path, source: bytes, entry: dict):
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"kgemm_kernel": entry}))
 
 
-def test_traffic_only_for_the_captured_source(tmp_path, monkeypatch):
+def test_traffic_only_for_the_captured_source_and_workload(tmp_path, monkeypatch):
     src = b"// kernel source as captured\n"
     h = hashlib.sha256(src).hexdigest()[:16]
-    fake_tree(tmp_path, src, {"source_sha256_16": h, "per_op": {"wgrad_gw2": 700, "wgrad_gw13": 1300}})
+    fake_tree(tmp_path, src, {"source_sha256_16": h,
+                              "workloads": {"a3b": {"wgrad_gw2": 700, "wgrad_gw13": 1300},
+                                            "skewed": {"wgrad_gw13": 5000}}})
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw2", "wgrad_gw13"]) == 1000
-    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw13"]) == 1300
-    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw2", "other_op"]) is None  # an op not captured
-    assert bench.traffic_for("kgemm_kernel", []) is None
-    assert bench.traffic_for("mx_kgemm_kernel", ["wgrad_gw2"]) is None  # no entry
+    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw2", "wgrad_gw13"], "a3b") == 1000
+    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw13"], "a3b") == 1300
+    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw13"], "skewed") == 5000
+    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw2", "wgrad_gw13"], "skewed") is None  # gw2 not captured
+    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw13"], "uniform") is None  # workload not captured
+    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw2", "other_op"], "a3b") is None  # an op not captured
+    assert bench.traffic_for("kgemm_kernel", [], "a3b") is None
+    assert bench.traffic_for("mx_kgemm_kernel", ["wgrad_gw2"], "a3b") is None  # no entry
     # the kernel changed since the capture: no traffic figure
     (tmp_path / "moe_grouped_gemm_device_gb300" / "csrc" / "kgemm.cu").write_bytes(src + b"// edit\n")
-    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw2"]) is None
+    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw2"], "a3b") is None
 
 
-def test_committed_traffic_entries_name_known_kernels():
+def test_committed_traffic_entries_name_known_kernels_and_workloads():
     d = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    names = {W.ALL[n]().name for n in W.ALL}
     for k, ent in d.items():
         if k.startswith("_"):
             continue
         assert k in bench.KERNEL_SOURCES, k
         assert len(ent["source_sha256_16"]) == 16
-        assert all(isinstance(v, int) and v > 0 for v in ent["per_op"].values())
+        for wl, per_op in ent["workloads"].items():
+            assert wl in names, wl
+            assert all(isinstance(v, int) and v > 0 for v in per_op.values())
+
+
+def test_peak_kind_follows_the_timed_region():
+    capped = {"sm_mhz": 1600.0, "reasons": ["sw_power_cap"]}
+    free = {"sm_mhz": 2070.0, "reasons": []}
+    # a short region runs at burst clocks whatever the record says
+    assert bench.peak_kind(0.03, capped) == "burst"
+    assert bench.peak_kind(0.03, free) == "burst"
+    assert bench.peak_kind(0.03, None) == "burst"
+    # a long region is compared with the sustained figure only when it was power-capped
+    assert bench.peak_kind(2.0, capped) == "sustained"
+    assert bench.peak_kind(2.0, free) == "burst"
+    assert bench.peak_kind(2.0, None) == "burst"
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    assert bench.tensor_peak("kgemm_kernel", peaks, "burst") == 1900.0
+    assert bench.tensor_peak("kgemm_kernel", peaks, "sustained") == 1700.0
+
+
+def test_both_arms_print_the_same_config():
+    """The reference arm's config is the GPU arm's (config_of), and it holds
+    nothing measured."""
+    wl = W.ALL["a3b"]()
+    c = bench.config_of(wl)
+    assert c == bench.config_of(W.ALL["a3b"]())
+    assert set(c) == {"workload", "flops_per_step", "l2"}
+    assert c["flops_per_step"] == wl.flops()
+    assert "larger than L2" in c["l2"]
+    assert "flushed" in bench.config_of(W.ALL["uniform8"]())["l2"]
+
+
+def test_reference_budget_keeps_the_run_short():
+    for steps, warmup in ((20, 5), (1000, 20), (1, 0)):
+        b = bench.reference_budget_s(steps, warmup)
+        assert 0.05 <= b <= 2.0
+        assert (steps + warmup) * b <= max(90.0, 0.05 * (steps + warmup)) + 1e-9
 
 
 COUNTS = np.array([3, 0, 5, 9])  # one empty group
@@ -74,11 +117,12 @@ def test_algorithmic_bytes_match_tensor_sizes():
 
 
 def test_fp8_kernels_take_twice_the_bf16_peak():
-    peaks = {"bf16_tflops_sustained": 1000.0}
+    peaks = {"bf16_tflops": 1100.0, "bf16_tflops_sustained": 1000.0}
     for k in bench.FP8_KERNELS:
-        assert bench.tensor_peak(k, peaks) == 2000.0
-    assert bench.tensor_peak("kgemm_kernel", peaks) == 1000.0
-    assert bench.tensor_peak("mgemm_kernel<true>", peaks) == 1000.0
+        assert bench.tensor_peak(k, peaks, "sustained") == 2000.0
+        assert bench.tensor_peak(k, peaks, "burst") == 2200.0
+    assert bench.tensor_peak("kgemm_kernel", peaks, "sustained") == 1000.0
+    assert bench.tensor_peak("mgemm_kernel<true>", peaks, "burst") == 1100.0
 
 
 @pytest.mark.parametrize("name", sorted(W.ALL))
