@@ -320,19 +320,25 @@ int rg_kgemm_acc(const void* grad, const void* X, const int32_t* offsets, int E,
                  int N, int K, float* dW, cudaStream_t stream);
 
 /*
- * rg_get_device_status -- synchronise `stream`, then return through
- * *status (host pointer) the RG_DEV_* bits that kernels of this library set
- * on the current device since the previous call, and clear them.
- * Returns RG_OK, or RG_ERR_CUDA if the synchronisation or the read failed.
+ * rg_get_device_status -- after the work already queued on `stream`, read
+ * and clear, in one atomic step, the RG_DEV_* bits that kernels of this
+ * library set on the current device since the previous call; wait for the
+ * read (synchronises `stream`) and return the bits (>= 0), or RG_ERR_CUDA /
+ * RG_ERR_UNSUPPORTED (< 0).  The status is per device, not per stream: it
+ * holds the bits of kernels on every stream of the device that finished
+ * before the read, and a bit set concurrently by a kernel on another stream
+ * is kept for the next call.  Not for use inside CUDA-graph capture.
  */
-int rg_get_device_status(cudaStream_t stream, uint32_t* status);
+int rg_get_device_status(cudaStream_t stream);
 
 /*
  * rg_set_wait_timeout_ns -- bound, in nanoseconds, on any single pipeline
- * wait inside the kernels (default 2e9).  A wait that runs out sets
- * RG_DEV_TIMEOUT, the kernel drains its in-flight copies, frees its tensor
- * memory and returns.  Takes effect for launches made after the call.
- * Returns RG_ERR_INVALID_ARG for 0.
+ * wait inside the kernels (default 2e9, at least 1e6).  A wait that runs out
+ * sets RG_DEV_TIMEOUT and every role of the kernel stops; issued MMAs and
+ * copies are then waited for (those waits have their own fixed bound,
+ * independent of this one), tensor memory is freed and the kernel returns.
+ * Takes effect for launches made after the call.  Returns RG_ERR_INVALID_ARG
+ * for a bound below 1e6 (1 ms).
  */
 int rg_set_wait_timeout_ns(uint64_t ns);
 
@@ -343,10 +349,23 @@ int rg_set_wait_timeout_ns(uint64_t ns);
  * poll), each bounded by `ns` nanoseconds, and report through *status (host
  * pointer) the status bits the CTA set: RG_DEV_TIMEOUT when every form gave
  * up by itself, 0 when any of them returned as if its barrier had completed.
- * Synchronises `stream`.  Exercises the timeout path without a fault or a
- * hang.
+ * The self-test reports through a status word of its own, so bits pending
+ * for rg_get_device_status are left as they are.  Synchronises `stream`.
+ * Exercises the timeout path without a fault or a hang.
  */
 int rg_selftest_wait_timeout(uint64_t ns, cudaStream_t stream, uint32_t* status);
+
+/*
+ * rg_shutdown -- forget the per-device set-up of every device (the kernels'
+ * shared-memory attributes, grid sizes and the device addresses of the
+ * status words), so that the next call on a device sets it up again.  The
+ * library holds no memory, stream or other resource to release (its status
+ * words are module variables of each device context), so this is needed
+ * only after a device's context was destroyed (cudaDeviceReset) and before
+ * the library is used on it again.  Must not run concurrently with other
+ * calls into the library.  Returns RG_OK.
+ */
+int rg_shutdown(void);
 
 /* CUDA error code (cudaError_t as int) behind the last RG_ERR_CUDA of the
  * calling thread, 0 if none. */

@@ -30,7 +30,7 @@ import os
 
 from . import _build
 
-__all__ = ["load", "mgemm", "mgemm_nested", "mgemm_mxfp8", "mx_scales_blocked", "mx_blocked_bytes", "kgemm_mxfp8", "mx_scales_blocked_k", "mx_blocked_k_bytes", "mgemm_swiglu", "mgemm_swiglu_dgrad", "kgemm", "device_status", "set_wait_timeout_ns",
+__all__ = ["load", "mgemm", "mgemm_nested", "mgemm_mxfp8", "mx_scales_blocked", "mx_blocked_bytes", "kgemm_mxfp8", "mx_scales_blocked_k", "mx_blocked_k_bytes", "mgemm_swiglu", "mgemm_swiglu_dgrad", "kgemm", "device_status", "shutdown", "set_wait_timeout_ns",
            "selftest_wait_timeout", "RGError", "lib_path", "version",
            "RG_DEV_BAD_OFFSETS", "RG_DEV_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -45,7 +45,7 @@ RG_MAX_EXPERTS = 1024
 RG_MAX_OUTER = 65536
 RG_KGEMM_MAX_EXPERTS = 358
 
-EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_nested", "rg_mgemm_mxfp8", "rg_mx_scales_blocked", "rg_mx_blocked_bytes", "rg_kgemm_mxfp8", "rg_mx_scales_blocked_k", "rg_mx_blocked_k_bytes", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_set_wait_timeout_ns",
+EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_nested", "rg_mgemm_mxfp8", "rg_mx_scales_blocked", "rg_mx_blocked_bytes", "rg_kgemm_mxfp8", "rg_mx_scales_blocked_k", "rg_mx_blocked_k_bytes", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_shutdown", "rg_set_wait_timeout_ns",
                     "rg_selftest_wait_timeout", "rg_last_cuda_error", "rg_device_supported",
                     "rg_version")
 
@@ -103,8 +103,10 @@ def load() -> ctypes.CDLL:
     lib.rg_kgemm.restype = i32
     lib.rg_kgemm_acc.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp]
     lib.rg_kgemm_acc.restype = i32
-    lib.rg_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.rg_get_device_status.argtypes = [vp]
     lib.rg_get_device_status.restype = i32
+    lib.rg_shutdown.argtypes = []
+    lib.rg_shutdown.restype = i32
     lib.rg_set_wait_timeout_ns.argtypes = [u64]
     lib.rg_set_wait_timeout_ns.restype = i32
     lib.rg_selftest_wait_timeout.argtypes = [u64, vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -457,11 +459,18 @@ def kgemm(grad, X, offsets, out=None, stream=None, accumulate: bool = False):
 
 
 def device_status(stream=None) -> int:
-    """Synchronise the stream and return (and clear) the RG_DEV_* bits."""
+    """Return (and clear) the RG_DEV_* bits of the current device after the
+    work queued on the stream; synchronises the stream."""
     import torch
-    v = ctypes.c_uint32(0)
-    _check("rg_get_device_status", load().rg_get_device_status(_stream_ptr(torch.cuda.current_device(), stream), ctypes.byref(v)))
-    return int(v.value)
+    rc = load().rg_get_device_status(_stream_ptr(torch.cuda.current_device(), stream))
+    if rc < 0:
+        _check("rg_get_device_status", rc)
+    return int(rc)
+
+
+def shutdown() -> None:
+    """Forget the per-device set-up (see rg_shutdown in include/rg.h)."""
+    _check("rg_shutdown", load().rg_shutdown())
 
 
 def set_wait_timeout_ns(ns: int) -> None:

@@ -1,11 +1,11 @@
 // C-ABI host layer of librg.so: argument validation, TMA tensor-map encoding,
 // per-device setup and kernel launch.  Declared in include/rg.h.
 //
-// Nothing here allocates device or host memory.  The per-device status word is
-// a module-scope __device__ variable (one instance per device context); its
-// device address is looked up once per device.  Tensor maps are encoded on
-// the host for every call and passed by value as kernel parameters, so no
-// host workspace outlives a call.
+// Nothing here allocates device or host memory.  The per-device status words
+// are module-scope __device__ variables (one instance per device context);
+// their device addresses are looked up once per device.  Tensor maps are
+// encoded on the host for every call and passed by value as kernel
+// parameters, so no host workspace outlives a call.
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
@@ -21,9 +21,17 @@
 
 namespace {
 
-__device__ unsigned int g_status_word;
+__device__ unsigned int g_status_word;    // bits set by the GEMM and conversion kernels
+__device__ unsigned int g_selftest_word;  // bits set by the wait self-test
+__device__ unsigned int g_status_taken;   // last value taken from a status word, read by the host
+
+// Read a status word and clear it in one atomic step, on the caller's stream.
+__global__ void take_status_kernel(unsigned int* word, unsigned int* taken) { *taken = atomicExch(word, 0u); }
 
 constexpr int kMaxDevices = 64;
+// Smallest accepted bound on a pipeline wait: a wait can legitimately last a
+// whole tile's mainloop, or longer on a GPU shared with other work.
+constexpr unsigned long long kMinWaitLimitNs = 1000000ull;
 thread_local int t_last_cuda_error = 0;
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
@@ -34,10 +42,13 @@ struct DeviceState {
   int mg_grid = 0;      // persistent grid of each kernel (CTAs)
   int kg_grid = 0;
   size_t max_smem = 0;  // opt-in dynamic shared memory per block
-  unsigned int* status = nullptr;
+  unsigned int* status = nullptr;    // &g_status_word on this device
+  unsigned int* selftest = nullptr;  // &g_selftest_word
+  unsigned int* taken = nullptr;     // &g_status_taken
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
+std::mutex g_take_mu[kMaxDevices];  // one reader of g_status_taken per device at a time
 
 int fail_cuda(cudaError_t e) {
   t_last_cuda_error = static_cast<int>(e);
@@ -81,6 +92,10 @@ int device_state(DeviceState** out) {
       void* p = nullptr;
       if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) return fail_cuda(e);
       ds.status = static_cast<unsigned int*>(p);
+      if ((e = cudaGetSymbolAddress(&p, g_selftest_word)) != cudaSuccess) return fail_cuda(e);
+      ds.selftest = static_cast<unsigned int*>(p);
+      if ((e = cudaGetSymbolAddress(&p, g_status_taken)) != cudaSuccess) return fail_cuda(e);
+      ds.taken = static_cast<unsigned int*>(p);
       if ((e = rg::mgemm_setup(smem)) != cudaSuccess) return fail_cuda(e);
       if ((e = rg::kgemm_setup(smem)) != cudaSuccess) return fail_cuda(e);
       if ((e = rg::mx_setup(smem)) != cudaSuccess) return fail_cuda(e);
@@ -106,6 +121,24 @@ int device_state(DeviceState** out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Take (read and clear atomically) the status word `word` of the current
+// device after the work queued on `stream`, and wait for the result.
+// Returns the bits (>= 0) or RG_ERR_CUDA.
+int take_status(const DeviceState* ds, unsigned int* word, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  std::lock_guard<std::mutex> lock(g_take_mu[dev]);
+  take_status_kernel<<<1, 1, 0, stream>>>(word, ds->taken);
+  if ((e = cudaGetLastError()) != cudaSuccess) return fail_cuda(e);
+  unsigned int v = 0;
+  if ((e = cudaMemcpyFromSymbolAsync(&v, g_status_taken, sizeof v, 0, cudaMemcpyDeviceToHost, stream)) !=
+      cudaSuccess)
+    return fail_cuda(e);
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return fail_cuda(e);
+  return static_cast<int>(v & 0x7fffffffu);
+}
 
 // Encode a tiled tensor map; dims/box innermost first, strides in bytes for
 // dims 1..rank-1.
@@ -580,23 +613,15 @@ int rg_kgemm_acc(const void* grad, const void* X, const int32_t* offsets, int E,
   return kgemm_impl(grad, X, offsets, E, M, N, K, dW, 1, stream);
 }
 
-int rg_get_device_status(cudaStream_t stream, uint32_t* status) {
-  if (status == nullptr) return RG_ERR_INVALID_ARG;
+int rg_get_device_status(cudaStream_t stream) {
   DeviceState* ds = nullptr;
   int rc = device_state(&ds);
   if (rc != RG_OK) return rc;
-  cudaError_t e = cudaStreamSynchronize(stream);
-  if (e != cudaSuccess) return fail_cuda(e);
-  unsigned int v = 0;
-  if ((e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof v)) != cudaSuccess) return fail_cuda(e);
-  const unsigned int zero = 0;
-  if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero)) != cudaSuccess) return fail_cuda(e);
-  *status = v;
-  return RG_OK;
+  return take_status(ds, ds->status, stream);
 }
 
 int rg_set_wait_timeout_ns(uint64_t ns) {
-  if (ns == 0) return RG_ERR_INVALID_ARG;
+  if (ns < kMinWaitLimitNs) return RG_ERR_INVALID_ARG;
   g_wait_limit_ns.store(ns);
   return RG_OK;
 }
@@ -606,11 +631,20 @@ int rg_selftest_wait_timeout(uint64_t ns, cudaStream_t stream, uint32_t* status)
   DeviceState* ds = nullptr;
   int rc = device_state(&ds);
   if (rc != RG_OK) return rc;
-  uint32_t before = 0;
-  if ((rc = rg_get_device_status(stream, &before)) != RG_OK) return rc;
-  const cudaError_t e = rg::launch_wait_selftest(ds->status, ns, stream);
+  // the self-test reports through its own word: bits pending in the status
+  // word of the GEMM kernels stay there for rg_get_device_status
+  if ((rc = take_status(ds, ds->selftest, stream)) < 0) return rc;
+  const cudaError_t e = rg::launch_wait_selftest(ds->selftest, ns, stream);
   if (e != cudaSuccess) return fail_cuda(e);
-  return rg_get_device_status(stream, status);
+  if ((rc = take_status(ds, ds->selftest, stream)) < 0) return rc;
+  *status = static_cast<uint32_t>(rc);
+  return RG_OK;
+}
+
+int rg_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (DeviceState& ds : g_dev) ds = DeviceState{};
+  return RG_OK;
 }
 
 int rg_last_cuda_error(void) { return t_last_cuda_error; }

@@ -51,7 +51,7 @@ struct MxArgs {
 constexpr int kCtaGroup = RG_CTA_PAIR ? 2 : 1;
 // MXFP8 weight-gradient pipeline: stages of 128 expert rows, and the fp32
 // epilogue's TMA boxes (32 rows x BOX_COLS columns; 16 columns use a 64-byte
-// swizzle, 32 a 128-byte one) and staging buffers per epilogue warp.
+// swizzle, 32 a 128-byte one), one staging buffer per epilogue warp.
 // Compile-time switches for comparison builds.
 #ifndef RG_MXK_STAGES
 #define RG_MXK_STAGES 4
@@ -59,13 +59,9 @@ constexpr int kCtaGroup = RG_CTA_PAIR ? 2 : 1;
 #ifndef RG_MXK_BOX_COLS
 #define RG_MXK_BOX_COLS 16
 #endif
-#ifndef RG_MXK_EPI_BUFS
-#define RG_MXK_EPI_BUFS 1
-#endif
 namespace mxk {
 constexpr int STAGES = RG_MXK_STAGES;
 constexpr int BOX_COLS = RG_MXK_BOX_COLS;
-constexpr int EPI_BUFS = RG_MXK_EPI_BUFS;
 static_assert(BOX_COLS == 16 || BOX_COLS == 32, "dW boxes are 16 or 32 fp32 columns wide");
 }  // namespace mxk
 

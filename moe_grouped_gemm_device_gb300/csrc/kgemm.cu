@@ -39,7 +39,9 @@
 //     fp32 boxes (whole 128-byte lines) with an L2 evict-first policy (dW is
 //     written once and not read here).  Experts without rows produce zero
 //     tiles without touching the tensor cores.
-//   * Same bounded-wait / abort / drain scheme as the M-grouped kernel.
+//   * Same bounded-wait / abort / drain scheme as the M-grouped kernel: every
+//     wait is bounded, a wait that runs out stops every role of the CTA, and
+//     at the end the issuing CTA waits for every copy either CTA issued.
 #include <algorithm>
 
 #include "internal.h"
@@ -71,8 +73,8 @@ struct Cfg {
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   // The dynamic shared-memory window of a CTA without static shared memory
   // starts 1024-byte aligned; the kernel checks this instead of padding.
-  static constexpr int SMEM_FIXED =
-      STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 + 16;
+  static constexpr int SMEM_FIXED = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 +
+                                    static_cast<int>(sizeof(IssueLog<STAGES>)) + 16;
 };
 
 constexpr uint32_t TMEM_COLS = 512;
@@ -96,7 +98,8 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
   }
   uint8_t* epi = smem + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_WARPS * EPI_BUF_BYTES);
-  int* misc = reinterpret_cast<int*>(bars + C::NUM_BARS);  // [0] tmem base, [1] abort
+  IssueLog<STAGES>* ilog = reinterpret_cast<IssueLog<STAGES>*>(bars + C::NUM_BARS);
+  int* misc = reinterpret_cast<int*>(ilog + 1);  // [0] tmem base, [1] abort
   int* s_off = misc + 4;                                   // [E+1] offsets
   int* s_ord = s_off + (args.E + 1);                       // [E] experts by decreasing rows
 
@@ -188,10 +191,10 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
       tma_prefetch_desc(&tmG);
       tma_prefetch_desc(&tmX);
       const uint32_t pid = warp == 0 ? 0u : 1u;
+      issue_log_init(ilog, pid);
       uint32_t it = 0;
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0, armed_par = 0;  // issuing CTA: stages armed, and their parities
       const uint32_t full_issuer = CG == 2 ? mapa_shared(full_bar(0), 0) : full_bar(0);
       bool ok = true;
       for (int t = worker; t < T && ok; t += nworkers) {
@@ -230,20 +233,13 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
             for (int j = 0; j < BN_CTA / 64; ++j)
               tma_load_3d_cg<CG>(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, i0, r);
           }
-          if (rank == 0) {
-            armed |= 1u << stage;
-            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          }
+          ilog->it[pid][stage] = static_cast<int>(it - 1);
+          ilog->bytes[pid][stage] = STAGE_BYTES;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-      }
-      if (!ok) {  // let issued loads land before the CTA exits
-        for (int s = 0; s < STAGES; ++s)
-          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u, guard.limit_ns);
-        if (rank != 0) spin_ns(200000);  // the peer's copies signal the issuer's barriers
       }
     }
   } else if (warp == 1 && rank == 0) {
@@ -298,9 +294,9 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         ++acc;
       }
     }
-    if (!ok && lane == 0) {
+    if (!ok && lane == 0) {  // wait for issued MMAs before tensor memory is freed
       umma_commit_local<CG>(drain_bar);
-      mbar_wait_drain(drain_bar, 0, guard.limit_ns);
+      mbar_wait_drain(drain_bar, 0);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -407,9 +403,18 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     __syncwarp();
   }
 
+  // ---- teardown --------------------------------------------------------------
+  // Once no producer of either CTA issues any more, the issuing CTA settles
+  // every stage (drain_stages) -- after a normal run a formality, after an
+  // abort the wait for copies still in flight -- and the peer leaves only
+  // after that, since its copies complete on the issuer's barriers.
   tc_fence_before();
   __syncthreads();
   if constexpr (CG == 2) cluster_sync();
+  if (threadIdx.x == 0 && rank == 0)
+    drain_stages<STAGES>(full_bar(0), ilog, CG == 2 ? mapa_shared(smem_u32(ilog), 1) : 0u);
+  if constexpr (CG == 2) cluster_sync();
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<CG>(tmem, TMEM_COLS);

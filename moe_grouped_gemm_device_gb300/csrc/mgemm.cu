@@ -39,8 +39,10 @@
 //     with one TMA store per 64 columns; otherwise each valid row is written
 //     with plain 16-byte stores.
 //   * Every mbarrier wait is bounded (WaitGuard).  A wait that runs out sets
-//     the device status, all roles stop, in-flight copies and MMAs are drained
-//     with bounded waits, and tensor memory is freed before the CTA exits.
+//     the device status and all roles stop; issued MMAs are waited for, and
+//     at the end the issuing CTA waits for every copy either CTA of the pair
+//     issued (drain_stages), with bounded waits, before tensor memory is freed
+//     and the CTAs exit.
 #include <algorithm>
 
 #include "internal.h"
@@ -85,8 +87,8 @@ struct Cfg {
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   // The dynamic shared-memory window of a CTA without static shared memory
   // starts 1024-byte aligned; the kernel checks this instead of padding.
-  static constexpr int SMEM_FIXED =
-      STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 + 16;
+  static constexpr int SMEM_FIXED = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 +
+                                    static_cast<int>(sizeof(IssueLog<STAGES>)) + 16;
 };
 
 constexpr uint32_t TMEM_COLS = 512;
@@ -129,7 +131,8 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
   }
   uint8_t* epi = smem + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_WARPS * C::EPI_BUF_BYTES);
-  int* misc = reinterpret_cast<int*>(bars + C::NUM_BARS);  // [0] tmem base, [1] abort
+  IssueLog<STAGES>* ilog = reinterpret_cast<IssueLog<STAGES>*>(bars + C::NUM_BARS);
+  int* misc = reinterpret_cast<int*>(ilog + 1);  // [0] tmem base, [1] abort
   int* s_off = misc + 4;                                   // [E+1] offsets
   int* s_pre = s_off + (args.E + 1);                       // [E+1] tile prefix
 
@@ -246,10 +249,10 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
       if constexpr (HALF_TILES) tma_prefetch_desc(&tmAh);
       tma_prefetch_desc(&tmB);
       const uint32_t pid = warp == 0 ? 0u : 1u;
+      issue_log_init(ilog, pid);
       uint32_t it = 0;
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0, armed_par = 0;  // stages with a load issued, and its parity
       bool ok = true;
       int e = 0;
       const uint32_t full_issuer = CG == 2 ? mapa_shared(full_bar(0), 0) : full_bar(0);
@@ -298,21 +301,13 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
                   tma_load_3d_cg<CG>(sbj + jj * 8192, &tmB, fb, n0 + 64 * jj, kc, eb);
               }
             }
-            armed |= 1u << stage;
-            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+            ilog->it[pid][stage] = static_cast<int>(it - 1);
+            ilog->bytes[pid][stage] = stage_tx / CG;
           }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
-        }
-      }
-      if (!ok) {  // let issued loads land before the CTA exits
-        if (rank == 0) {
-          for (int s = 0; s < STAGES; ++s)
-            if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u, guard.limit_ns);
-        } else {
-          spin_ns(200000);  // the peer's copies signal the issuer's barriers
         }
       }
     }
@@ -367,7 +362,7 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
     }
     if (!ok && lane == 0) {  // wait for issued MMAs before tensor memory is freed
       umma_commit_local<CG>(drain_bar);
-      mbar_wait_drain(drain_bar, 0, guard.limit_ns);
+      mbar_wait_drain(drain_bar, 0);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -599,9 +594,17 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
   }
 
   // ---- teardown --------------------------------------------------------------
+  // Once no producer of either CTA issues any more, the issuing CTA settles
+  // every stage (drain_stages): after a normal run a formality, after an
+  // abort the wait for copies still in flight.  The peer leaves only after
+  // that, since its copies complete on the issuer's barriers.
   tc_fence_before();
   __syncthreads();
   if constexpr (CG == 2) cluster_sync();  // no remote arrive or MMA still targets either CTA
+  if (threadIdx.x == 0 && rank == 0)
+    drain_stages<STAGES>(full_bar(0), ilog, CG == 2 ? mapa_shared(smem_u32(ilog), 1) : 0u);
+  if constexpr (CG == 2) cluster_sync();
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<CG>(tmem, TMEM_COLS);

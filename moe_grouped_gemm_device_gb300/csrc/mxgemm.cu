@@ -67,7 +67,8 @@ struct MxCfg {
   // full[S], empty[S], tfull, tempty, drain
   static constexpr int NUM_BARS = 2 * STAGES + 3;
   // [operand tiles of every stage][scale blocks of every stage][epilogue buffers][barriers][misc]
-  static constexpr int SMEM_FIXED = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 + 16;
+  static constexpr int SMEM_FIXED = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 +
+                                    static_cast<int>(sizeof(IssueLog<STAGES>)) + 16;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SF_COL0 = 256;  // scale slots: stage s at SF_COL0 + 16 s (A: 4 cols, B: 8 cols)
 };
@@ -87,7 +88,8 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
   }
   uint8_t* epi = smem + STAGES * C::STAGE_BYTES;  // after the operand tiles and the scale blocks
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_WARPS * C::EPI_BUF_BYTES);
-  int* misc = reinterpret_cast<int*>(bars + C::NUM_BARS);  // [0] tmem base, [1] abort
+  IssueLog<STAGES>* ilog = reinterpret_cast<IssueLog<STAGES>*>(bars + C::NUM_BARS);
+  int* misc = reinterpret_cast<int*>(ilog + 1);  // [0] tmem base, [1] abort
   int* s_off = misc + 4;
   int* s_pre = s_off + (args.E + 1);
 
@@ -172,10 +174,10 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       const uint32_t pid = warp == 0 ? 0u : 1u;
+      issue_log_init(ilog, pid);
       uint32_t it = 0;
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0, armed_par = 0;
       bool ok = true;
       int e = 0;
       for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
@@ -214,17 +216,13 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
           bulk_load(sfa_of(stage), args.sfa + (static_cast<int64_t>(blk_a) * nkc + kc) * 512, 512, fb);
           bulk_load(sfb_of(stage), args.sfb + (static_cast<int64_t>(blk_b0) * nkc + kc) * 512, 512, fb);
           bulk_load(sfb_of(stage) + 512, args.sfb + (static_cast<int64_t>(blk_b1) * nkc + kc) * 512, 512, fb);
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          ilog->it[pid][stage] = static_cast<int>(it - 1);
+          ilog->bytes[pid][stage] = C::STAGE_BYTES;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-      }
-      if (!ok) {
-        for (int s = 0; s < STAGES; ++s)
-          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u, guard.limit_ns);
       }
     }
   } else if (warp == 1) {
@@ -270,7 +268,7 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
     }
     if (!ok && lane == 0) {
       umma_commit<1>(drain_bar);
-      mbar_wait_drain(drain_bar, 0, guard.limit_ns);
+      mbar_wait_drain(drain_bar, 0);
     }
     __syncwarp();
   } else {
@@ -338,7 +336,11 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
   }
 
   // ---- teardown --------------------------------------------------------------
+  // the last phase each stage was filled in has landed (after an abort, the
+  // wait for copies still in flight) before the CTA exits
   tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) drain_stages<STAGES>(full_bar(0), ilog, 0u);
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -601,13 +603,12 @@ struct MxkCfg {
   static constexpr int EPI_WARPS = 8;
   static constexpr int BOX_COLS = mxk::BOX_COLS;
   static constexpr int EPI_BUF_BYTES = 32 * BOX_COLS * 4;  // 32 rows x BOX_COLS fp32 (one TMA box)
-  static constexpr int EPI_BUFS = mxk::EPI_BUFS;          // per epilogue warp
   // warps 0 and 10: producers (alternate stages), 1: MMA, 2..9: epilogue
   static constexpr int PRODUCER2 = 2 + EPI_WARPS;
   static constexpr int THREADS = 32 * (PRODUCER2 + 1);
   static constexpr int NUM_BARS = 2 * STAGES + 3;
-  static constexpr int SMEM_FIXED =
-      STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES + NUM_BARS * 8 + 16;
+  static constexpr int SMEM_FIXED = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 +
+                                    static_cast<int>(sizeof(IssueLog<STAGES>)) + 16;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SF_COL0 = 256;
 };
@@ -631,9 +632,10 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
   // [operand tiles of every stage][epilogue buffers][scale blocks][barriers][misc]
   // (the 128-byte-swizzled epilogue boxes need 1024-byte alignment)
   uint8_t* epi = smem + STAGES * C::AB_BYTES;
-  uint8_t* sf_area = epi + C::EPI_WARPS * C::EPI_BUFS * C::EPI_BUF_BYTES;
+  uint8_t* sf_area = epi + C::EPI_WARPS * C::EPI_BUF_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sf_area + STAGES * C::SF_BYTES);
-  int* misc = reinterpret_cast<int*>(bars + C::NUM_BARS);  // [0] tmem base, [1] abort
+  IssueLog<STAGES>* ilog = reinterpret_cast<IssueLog<STAGES>*>(bars + C::NUM_BARS);
+  int* misc = reinterpret_cast<int*>(ilog + 1);  // [0] tmem base, [1] abort
   int* s_off = misc + 4;           // [E+1]
   int* s_qp = s_off + (args.E + 1);  // [E+1] first scale chunk of each expert
   int* s_ord = s_qp + (args.E + 1);  // [E] experts by decreasing rows
@@ -735,10 +737,10 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
       tma_prefetch_desc(&tmG);
       tma_prefetch_desc(&tmX);
       const uint32_t pid = warp == 0 ? 0u : 1u;
+      issue_log_init(ilog, pid);
       uint32_t it = 0;
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0, armed_par = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
         int e, nb, kb;
@@ -767,17 +769,13 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
           bulk_load(sfa_of(stage), args.sfa + (static_cast<int64_t>(nb) * NQ + q) * 512, 512, fb);
           bulk_load(sfb_of(stage), args.sfb + (static_cast<int64_t>(xb0) * NQ + q) * 512, 512, fb);
           bulk_load(sfb_of(stage) + 512, args.sfb + (static_cast<int64_t>(xb1) * NQ + q) * 512, 512, fb);
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          ilog->it[pid][stage] = static_cast<int>(it - 1);
+          ilog->bytes[pid][stage] = C::STAGE_BYTES;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-      }
-      if (!ok) {
-        for (int s = 0; s < STAGES; ++s)
-          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u, guard.limit_ns);
       }
     }
   } else if (warp == 1) {
@@ -829,18 +827,17 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
     }
     if (!ok && lane == 0) {
       umma_commit<1>(drain_bar);
-      mbar_wait_drain(drain_bar, 0, guard.limit_ns);
+      mbar_wait_drain(drain_bar, 0);
     }
     __syncwarp();
   } else {
     // ======================= epilogue (warps 2..9) ===========================
     // Warp w owns TMEM lane quarter q = w % 4 (dW rows n0 + 32q ..) and
     // column half h (128 of the 256 columns), stored as boxes of 32 rows x
-    // BOX_COLS fp32 through EPI_BUFS staging buffers (with two, one box is
-    // written while the previous one is still being read by the TMA unit).
+    // BOX_COLS fp32 through one staging buffer per warp.
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
-    uint8_t* ebuf = epi + (warp - 2) * C::EPI_BUFS * C::EPI_BUF_BYTES;
+    uint8_t* ebuf = epi + (warp - 2) * C::EPI_BUF_BYTES;
     const uint32_t ebuf_s = smem_u32(ebuf);
     int acc = 0;
     bool ok = true;
@@ -895,10 +892,9 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
 #pragma unroll
         for (int b = 0; b < 128 / BC; ++b) {
           if (kc0 + BC * b >= K) break;
-          if (lane == 0) bulk_wait_read<C::EPI_BUFS - 1>();  // the buffer's previous box has left
+          if (lane == 0) bulk_wait_read<0>();  // the buffer's previous box has left
           __syncwarp();
-          uint8_t* buf = ebuf + (b % C::EPI_BUFS) * C::EPI_BUF_BYTES;
-          uint4* rowp = reinterpret_cast<uint4*>(buf + lane * BC * 4);
+          uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * BC * 4);
 #pragma unroll
           for (int j = 0; j < CH; ++j)
             rowp[j ^ sw] = make_uint4(v[BC * b + 4 * j], v[BC * b + 4 * j + 1], v[BC * b + 4 * j + 2],
@@ -906,9 +902,8 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            const uint32_t src = ebuf_s + (b % C::EPI_BUFS) * C::EPI_BUF_BYTES;
-            if (reduce) tma_reduce_add_3d(&tmD, src, kc0 + BC * b, n0, e);
-            else tma_store_3d(&tmD, src, kc0 + BC * b, n0, e);
+            if (reduce) tma_reduce_add_3d(&tmD, ebuf_s, kc0 + BC * b, n0, e);
+            else tma_store_3d(&tmD, ebuf_s, kc0 + BC * b, n0, e);
             bulk_commit();
           }
         }
@@ -919,7 +914,11 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
   }
 
   // ---- teardown --------------------------------------------------------------
+  // the last phase each stage was filled in has landed (after an abort, the
+  // wait for copies still in flight) before the CTA exits
   tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) drain_stages<STAGES>(full_bar(0), ilog, 0u);
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();

@@ -174,12 +174,92 @@ __device__ __forceinline__ bool warp_wait_acc(const WaitGuard& g, uint32_t bar, 
   }
 }
 
-// Bounded wait used while draining after an abort: ignores the abort flag.
-static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+// Bound on each wait of the drain at a kernel's end.  Copies and MMAs that
+// were issued always complete (their operands exist), within microseconds;
+// the bound only keeps the wait finite, and it does not depend on the
+// caller's pipeline-wait limit, which may be much shorter.
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+
+// Bounded wait used while draining: ignores the abort flag.
+static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (globaltimer_ns() - t0 > kDrainLimitNs) return false;
+  }
+}
+
+// Count `bytes` of the current phase's expected transaction bytes as arrived
+// (bytes of a copy that was armed for but will never be issued).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// 32-bit load from the shared memory of a CTA of the cluster (address from mapa_shared).
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+// What each of a CTA's two producer threads last issued into each stage of
+// its ring: the iteration of the (tile, block) walk (-1: nothing yet; stage
+// = it % S, phase = it / S) and the bytes of this CTA's own copies.  Written
+// by the producer that issues, read once at the kernel's end by the drain.
+template <int S>
+struct IssueLog {
+  int it[2][S];
+  uint32_t bytes[2][S];
+};
+
+template <int S>
+__device__ __forceinline__ void issue_log_init(IssueLog<S>* log, uint32_t pid) {
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    log->it[pid][s] = -1;
+    log->bytes[pid][s] = 0;
+  }
+}
+
+// The drain at the end of a kernel, run by one thread of the CTA whose stage
+// barriers receive every copy (the issuing CTA of a pair), once no producer
+// of either CTA issues any more: wait, per stage, until the last phase that
+// either CTA copied into has completed, so that no copy still writes into a
+// CTA's shared memory when it exits.  `peer` is the shared::cluster address
+// of the other CTA's log (0 for a single CTA).  The two CTAs of a pair are at
+// most one phase apart on a stage (a stage is refilled only after both halves
+// of its previous phase landed and were consumed), and a phase that only one
+// of them reached is settled on the barrier: the peer's missing copy is
+// counted as arrived (complete_tx), or the issuing CTA's missing arrival is
+// made with the peer's bytes (arrive.expect_tx).  Waits are bounded by
+// kDrainLimitNs.  After a normal run every last phase is already complete.
+template <int S>
+__device__ void drain_stages(uint32_t full_bar0, const IssueLog<S>* own, uint32_t peer) {
+#pragma unroll 1
+  for (int s = 0; s < S; ++s) {
+    const int k0 = own->it[0][s] >= own->it[1][s] ? 0 : 1;
+    const int i0 = own->it[k0][s];
+    int i1 = -1;
+    uint32_t b1 = 0;
+    if (peer != 0) {
+      const uint32_t f = peer + 4u * s;  // &log->it[0][s] in the peer CTA
+      const int a = static_cast<int>(ld_shared_cluster_u32(f));
+      const int b = static_cast<int>(ld_shared_cluster_u32(f + 4u * S));
+      const int k1 = a >= b ? 0 : 1;
+      i1 = k1 == 0 ? a : b;
+      b1 = ld_shared_cluster_u32(peer + 8u * S + 4u * (k1 * S + s));
+    } else {
+      i1 = i0;
+    }
+    const uint32_t bar = full_bar0 + 8u * s;
+    int last = i0;
+    if (i0 > i1) {
+      mbar_complete_tx(bar, own->bytes[k0][s]);  // the peer's half (same size as ours) never comes
+    } else if (i1 > i0) {
+      mbar_arrive_expect_tx(bar, b1);  // the peer copied into a phase we never armed
+      last = i1;
+    }
+    if (last >= 0) mbar_wait_drain(bar, static_cast<uint32_t>(last / S) & 1u);
   }
 }
 

@@ -75,3 +75,42 @@ def bf16_round_exact(ref: np.ndarray) -> np.ndarray:
     correct fp32-accumulating kernel must produce when every partial sum is
     exactly representable."""
     return W.f32_to_bf16_bits(ref.astype(np.float32))
+
+
+class FullCompare:
+    """The checks of check_bf16 / check_fp32 over an output too large to hold
+    twice in float64: fed chunk by chunk, it accumulates the squared error and
+    reference norms (relative Frobenius error of the whole output) and, for
+    bf16, the worst per-element error relative to |ref| + 1."""
+
+    def __init__(self, kind: str, what: str):
+        assert kind in ("bf16", "fp32")
+        self.kind, self.what = kind, what
+        self.err2 = 0.0
+        self.ref2 = 0.0
+        self.worst = 0.0
+        self.count = 0
+
+    def add(self, gpu: np.ndarray, ref: np.ndarray) -> None:
+        g = (W.bf16_bits_to_f32(gpu) if self.kind == "bf16" else np.asarray(gpu)).astype(np.float64)
+        assert g.shape == ref.shape, (g.shape, ref.shape)
+        assert np.isfinite(g).all(), f"{self.what}: non-finite output"
+        d = g - ref
+        self.err2 += float(np.sum(d * d))
+        self.ref2 += float(np.sum(ref * ref))
+        if self.kind == "bf16" and d.size:
+            self.worst = max(self.worst, float(np.max(np.abs(d) / (np.abs(ref) + 1))))
+        self.count += d.size
+
+    def finish(self) -> dict:
+        fro = float(np.sqrt(self.err2 / self.ref2)) if self.ref2 > 0 else float(np.sqrt(self.err2))
+        rec = {"rel_fro": fro, "elements": self.count}
+        if self.kind == "bf16":
+            rec["elem"] = self.worst
+            _log(self.what, {**rec, "tol_fro": BF16_REL_FRO, "tol_elem": BF16_ELEM})
+            assert fro <= BF16_REL_FRO, f"{self.what}: relative Frobenius error {fro:.3e} > {BF16_REL_FRO}"
+            assert self.worst <= BF16_ELEM, f"{self.what}: element error {self.worst:.3e}*(|ref|+1) > {BF16_ELEM}"
+        else:
+            _log(self.what, {**rec, "tol_fro": FP32_REL_FRO})
+            assert fro <= FP32_REL_FRO, f"{self.what}: relative Frobenius error {fro:.3e} > {FP32_REL_FRO}"
+        return rec

@@ -104,9 +104,22 @@ def test_kgemm_rejects_bad_arguments(lib, args, fn):
 
 def test_other_entry_points_validate(lib):
     assert lib.rg_set_wait_timeout_ns(0) == rg.RG_ERR_INVALID_ARG
+    assert lib.rg_set_wait_timeout_ns(999_999) == rg.RG_ERR_INVALID_ARG  # below the 1 ms floor
+    assert lib.rg_set_wait_timeout_ns(1_000_000) == rg.RG_OK
     assert lib.rg_set_wait_timeout_ns(2_000_000_000) == rg.RG_OK
-    assert lib.rg_get_device_status(None, None) == rg.RG_ERR_INVALID_ARG
     assert lib.rg_selftest_wait_timeout(0, None, None) == rg.RG_ERR_INVALID_ARG
+
+
+def test_status_and_shutdown_without_a_device(lib):
+    """rg_get_device_status returns the bits (>= 0) or a negative error: with
+    no device it is an error, never bits; rg_shutdown releases nothing and
+    always succeeds."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.rg_get_device_status(None) in (rg.RG_ERR_CUDA, rg.RG_ERR_UNSUPPORTED)
+    assert lib.rg_shutdown() == rg.RG_OK
+    assert lib.rg_shutdown() == rg.RG_OK
 
 
 def test_no_device_reports_unsupported_or_cuda_error(lib):
