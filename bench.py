@@ -300,7 +300,7 @@ def config_of(wl) -> dict:
     ws = working_set_bytes(wl)
     return {"workload": workload_desc(wl), "flops_per_step": wl.flops(),
             "l2": f"inputs larger than L2: step working set {ws / 1e9:.2f} GB vs 129 MB L2" if ws >= 4 * L2_BYTES
-                  else f"L2 flushed between steps (a {L2_FLUSH_BYTES >> 20} MB buffer is written; "
+                  else f"L2 flushed between steps (a {L2_FLUSH_BYTES >> 20} MB buffer written, another read; "
                        f"step working set {ws / 1e6:.0f} MB)"}
 
 
@@ -510,15 +510,18 @@ class Timed:
 def time_steps(units, steps, warmup, rg, stream, dev, dist, rank, local, flush=None) -> Timed:
     """W warm-up steps, then K timed steps between a barrier and a device
     synchronisation on both sides, with CUDA events around every launch on the
-    launching stream.  With `flush` (a device buffer larger than L2) the buffer
-    is rewritten before every step and the region's length is the sum of the
-    launch durations, which excludes the flushes."""
+    launching stream.  With `flush` (two device buffers larger than L2) the
+    first is written and the second read before every step, and the region's
+    length is the sum of the launch durations, which excludes the flushes."""
     import torch
     nu = len(units)
 
     def step(evs=None):
         if flush is not None:
-            flush.fill_(1)
+            # write a buffer larger than L2, then read another one, so that the
+            # dirty lines are written back before the step rather than during it
+            flush[0].fill_(1)
+            flush[1].sum()
         for i, u in enumerate(units):
             if evs is not None:
                 evs[i].record(stream)
@@ -734,7 +737,8 @@ def main():
     def flush_buffer(w):
         if working_set_bytes(w) >= 4 * L2_BYTES:
             return None
-        return torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        return [torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev),
+                torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)]
 
     # ---- headline workload: inputs resident in HBM --------------------------
     host, d, off_used, outs, units = prepare(wl, rg, dev)
