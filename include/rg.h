@@ -50,6 +50,8 @@ extern "C" {
 #define RG_DEV_BAD_OFFSETS 0x1u /* offsets[0] != 0, decreasing, or offsets[E] > M */
 #define RG_DEV_TIMEOUT 0x2u     /* a bounded pipeline wait ran out; the kernel stopped */
 #define RG_DEV_LAUNCH_CONFIG 0x4u /* shared-memory window misaligned; the kernel did nothing */
+#define RG_DEV_BOUNDS 0x8u        /* debug-bounds builds only (RG_DEBUG_BOUNDS=1): a copy or store
+                                     coordinate fell outside its operand; that access was skipped */
 
 /* Largest number of experts one call accepts. */
 #define RG_MAX_EXPERTS 1024
@@ -294,7 +296,7 @@ int rg_mgemm_swiglu_dgrad(const void* dy, const void* w2, const int32_t* offsets
  *   dW       device, fp32 [E, N, K], overwritten:
  *            dW[e, n, k] = sum over rows r of expert e of grad[r, n] * X[r, k],
  *            accumulated in FP32 by the tensor cores over chunks of at most
- *            4096 rows, whose partial sums are added in FP32 in row order
+ *            4032 rows, whose partial sums are added in FP32 in row order
  *            (deterministic); an expert with no rows gets dW[e] = 0.
  *            Rows >= offsets[E] are ignored, and no row outside an
  *            expert's range is read for its dW[e]: Inf or NaN in one

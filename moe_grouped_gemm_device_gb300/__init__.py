@@ -41,6 +41,7 @@ RG_ERR_CUDA = -3
 RG_DEV_BAD_OFFSETS = 0x1
 RG_DEV_TIMEOUT = 0x2
 RG_DEV_LAUNCH_CONFIG = 0x4
+RG_DEV_BOUNDS = 0x8
 RG_MAX_EXPERTS = 1024
 RG_MAX_OUTER = 65536
 RG_KGEMM_MAX_EXPERTS = 358

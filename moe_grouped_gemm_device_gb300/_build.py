@@ -18,7 +18,12 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "librg.so")
 SOURCES = ["api.cu", "mgemm.cu", "kgemm.cu", "mxgemm.cu", "selftest.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("ptx.cuh", "internal.h")] + [os.path.join(INCLUDE, "rg.h")]
+HEADERS = [os.path.join(CSRC, h) for h in ("ptx.cuh", "internal.h", "bounds.cuh")] + [os.path.join(INCLUDE, "rg.h")]
+# The debug-bounds build: every copy and store coordinate the kernels compute
+# is checked against its operand; a failed check sets RG_DEV_BOUNDS and the
+# access is skipped.  Built on request into its own directory.
+BOUNDS_DIR = os.path.join(OUT_DIR, "bounds")
+BOUNDS_FLAGS = ("-DRG_DEBUG_BOUNDS=1",)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -36,21 +41,26 @@ def _inputs():
     return [os.path.join(CSRC, s) for s in SOURCES] + HEADERS + [__file__]
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB):
+def is_stale(lib: str = None) -> bool:
+    lib = lib or LIB
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not is_stale():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str = None) -> str:
+    """Build librg.so into out_dir (default: the package's _build directory)
+    with extra nvcc flags; returns the library's path."""
+    out_dir = out_dir or OUT_DIR
+    lib = os.path.join(out_dir, "librg.so")
+    if not force and not is_stale(lib):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -63,13 +73,18 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_bounds(force: bool = False) -> str:
+    """The debug-bounds build of the library (see BOUNDS_FLAGS)."""
+    return build(force=force, extra_flags=BOUNDS_FLAGS, out_dir=BOUNDS_DIR)
 
 
 if __name__ == "__main__":

@@ -62,6 +62,7 @@ constexpr int kCtaGroup = RG_CTA_PAIR ? 2 : 1;
 namespace mxk {
 constexpr int STAGES = RG_MXK_STAGES;
 constexpr int BOX_COLS = RG_MXK_BOX_COLS;
+constexpr int CHUNK_ROWS = 4096;  // rows summed in tensor memory per partial (32 stages of 128)
 static_assert(BOX_COLS == 16 || BOX_COLS == 32, "dW boxes are 16 or 32 fp32 columns wide");
 }  // namespace mxk
 
@@ -83,11 +84,11 @@ constexpr int BM = 128;                  // dW rows per CTA
 constexpr int TILE_M = BM * kCtaGroup;   // dW rows per tile
 constexpr int BN = 256;                  // dW columns per tile
 constexpr int BN_CTA = BN / kCtaGroup;   // X columns loaded per CTA
-constexpr int BR = 128;                  // contraction rows per stage (eight 16-row MMA steps)
+constexpr int BR = 96;                   // contraction rows per stage (six 16-row MMA steps)
 // Rows of one expert accumulated in tensor memory before the partial sum is
 // folded into dW (store for the first chunk, fp32 reduce-add for the rest).
 // Bounds the length of each fp32 accumulation chain inside the tensor cores.
-constexpr int CHUNK_ROWS = 4096;
+constexpr int CHUNK_ROWS = 4032;
 static_assert(CHUNK_ROWS % BR == 0, "chunks must hold whole row blocks");
 }  // namespace kg
 

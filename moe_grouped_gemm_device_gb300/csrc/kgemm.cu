@@ -10,13 +10,15 @@
 //     by index) in shared memory; worker w takes tiles w, w+W, ... of that
 //     list, so every round of W tiles has near-equal cost (longest-first list
 //     scheduling) -- without global scratch or host sync.
-//   * The contraction is fed BR = 128 rows at a time, eight MMA steps of 16
-//     rows per barrier round of the MMA warp.  With CG = 2 (default) a CTA
+//   * The contraction is fed BR = 96 rows at a time, six MMA steps of 16
+//     rows per barrier round of the MMA warp, through a ring of four stages
+//     (48 KB per CTA each): three stages ahead of the tensor cores hide the
+//     copies' latency better than two of 128 rows.  With CG = 2 (default) a CTA
 //     pair computes a 256x256 dW tile with tcgen05.mma.cta_group::2: for the
 //     row block starting at r, CTA c loads grad[r:r+BR, n0+128c : +128] (A,
 //     its 128 rows of dW) and X[r:r+BR, k0+128c : +128] (its half of B); both
-//     are N/K-contiguous, i.e. MN-major operands.  64 KB per stage and CTA,
-//     three stages.  CG = 1: one CTA, 128x256 tiles, two 96 KB stages.
+//     are N/K-contiguous, i.e. MN-major operands.  CG = 1: one CTA, 128x256
+//     tiles, two 72 KB stages.
 //   * Both operands are read through 3-D views {columns, i < BR, j} of the
 //     row-major tensors in which element (c, i, j) is row i + j (both row
 //     strides equal the pitch).  A full block loads box (c, 0, r): rows
@@ -44,6 +46,7 @@
 //     at the end the issuing CTA waits for every copy either CTA issued.
 #include <algorithm>
 
+#include "bounds.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "rg.h"
@@ -222,16 +225,33 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
           const int i0 = min(0, r_end - r - BR);
           const uint32_t fb = full_issuer + 8u * stage;
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES * CG);
+          // (debug-bounds build: every in-range row of the box must be a row
+          // of expert e; a refused copy's bytes are counted as arrived)
+          const bool rows_ok = !RG_DEBUG_BOUNDS || bounds::kgemm_rows(r, i0, BR, r_begin, r_end);
           if (args.kg_wide) {  // one copy per operand: column blocks n0/64 .. and k0/64 ..
-            tma_load_4d_cg<CG>(sa, &tmG, fb, 0, i0, n0 / 64, r);
-            tma_load_4d_cg<CG>(sb, &tmX, fb, 0, i0, k0 / 64, r);
+            if (RG_BOUNDS_OK(rows_ok && n0 % 64 == 0, args.status))
+              tma_load_4d_cg<CG>(sa, &tmG, fb, 0, i0, n0 / 64, r);
+            else
+              mbar_complete_tx_cluster(fb, A_BYTES);
+            if (RG_BOUNDS_OK(rows_ok && k0 % 64 == 0, args.status))
+              tma_load_4d_cg<CG>(sb, &tmX, fb, 0, i0, k0 / 64, r);
+            else
+              mbar_complete_tx_cluster(fb, C::B_BYTES);
           } else {
 #pragma unroll
-            for (int j = 0; j < BM / 64; ++j)
-              tma_load_3d_cg<CG>(sa + j * BOX_BYTES, &tmG, fb, n0 + 64 * j, i0, r);
+            for (int j = 0; j < BM / 64; ++j) {
+              if (RG_BOUNDS_OK(rows_ok && bounds::inner_aligned(n0 + 64 * j, 2), args.status))
+                tma_load_3d_cg<CG>(sa + j * BOX_BYTES, &tmG, fb, n0 + 64 * j, i0, r);
+              else
+                mbar_complete_tx_cluster(fb, BOX_BYTES);
+            }
 #pragma unroll
-            for (int j = 0; j < BN_CTA / 64; ++j)
-              tma_load_3d_cg<CG>(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, i0, r);
+            for (int j = 0; j < BN_CTA / 64; ++j) {
+              if (RG_BOUNDS_OK(rows_ok && bounds::inner_aligned(k0 + 64 * j, 2), args.status))
+                tma_load_3d_cg<CG>(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, i0, r);
+              else
+                mbar_complete_tx_cluster(fb, BOX_BYTES);
+            }
           }
           ilog->it[pid][stage] = static_cast<int>(it - 1);
           ilog->bytes[pid][stage] = STAGE_BYTES;
@@ -342,6 +362,11 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         else mbar_arrive(tempty_bar(buf));
       }
     };
+    // a 32 x 32 fp32 box of dW[e] at (column k, row n): inside dW, 16-byte aligned start
+    auto dw_box_ok = [&](int k, int n, int ee) {
+      return bounds::inner_aligned(k, 4) && bounds::within(k, 32, K) && bounds::within(n, 32, N) &&
+             bounds::index_ok(ee, E);
+    };
     for (int t = worker; t < T && ok; t += nworkers) {
       int e, local;
       tile_at(t, e, local);
@@ -358,7 +383,8 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         for (int c = 0; c < BN / 64 && kh + 32 * c < K; ++c) {
           stage_box(z);
           if (lane == 0) {
-            tma_store_3d(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e);
+            if (RG_BOUNDS_OK(dw_box_ok(kh + 32 * c, n0 + q * 32, e), args.status))
+              tma_store_3d(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e);
             bulk_commit();
           }
         }
@@ -389,7 +415,9 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         for (int c = 0; c < BN / 64; ++c) {
           if (kh + 32 * c >= K) break;
           stage_box(v + 32 * c);
-          if (lane == 0) {
+          if (lane == 0 && !RG_BOUNDS_OK(dw_box_ok(kh + 32 * c, n0 + q * 32, e), args.status)) {
+            bulk_commit();
+          } else if (lane == 0) {
             if (overwrite)
               tma_store_3d_hint(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e, dw_policy);
             else
@@ -423,7 +451,7 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
 
 // Ring depth.  The shared-memory tables of the experts sit beside it, which
 // bounds E (RG_KGEMM_MAX_EXPERTS in rg.h; the host rejects larger E).
-constexpr int kStagesDeep = kCtaGroup == 2 ? 3 : 2;
+constexpr int kStagesDeep = kCtaGroup == 2 ? 4 : 2;
 static_assert(Cfg<kCtaGroup, kStagesDeep>::SMEM_FIXED + (2 * RG_KGEMM_MAX_EXPERTS + 1) * 4 <= 232448,
               "the expert tables of RG_KGEMM_MAX_EXPERTS experts must fit beside the ring");
 

@@ -45,6 +45,7 @@
 //     and the CTAs exit.
 #include <algorithm>
 
+#include "bounds.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -266,7 +267,8 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
         const bool half = is_half(e, local);
         const CUtensorMap* am = half ? &tmAh : &tmA;
         const uint32_t stage_tx = (half ? STAGE_BYTES - A_BYTES / 2 : STAGE_BYTES) * CG;
-        const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * (half ? BM / 2 : BM);
+        const int tile_row0 = s_off[e] + (local / nbn) * TILE_M;
+        const int row0 = tile_row0 + static_cast<int>(rank) * (half ? BM / 2 : BM);
         // B rows this CTA loads: its half of the 256 output columns, or (SwiGLU)
         // the gate rows (CTA 0) / the matching up rows (CTA 1) of 128 features
         const int n0 = SWIGLU ? (local % nbn) * BN_CTA + static_cast<int>(rank) * F
@@ -289,16 +291,34 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
             for (int j = 0; j < KATOMS; ++j) {
               const int kc = kb * BKS + BK * j;
               const uint32_t saj = sa + j * A_ATOM, sbj = sb + j * B_ATOM;
-              if (O == 1) tma_load_2d_cg<CG>(saj, am, fb, kc, row0);
-              else tma_load_3d_cg<CG>(saj, am, fb, kc, o, row0);
+              // (debug-bounds build: a refused copy's bytes are counted as
+              // arrived, so the stage completes without it)
+              if (RG_BOUNDS_OK(bounds::inner_aligned(kc, 2) && bounds::mgemm_rows(tile_row0, s_off[e], s_off[e + 1], args.M) &&
+                                   bounds::index_ok(o, O),
+                               args.status)) {
+                if (O == 1) tma_load_2d_cg<CG>(saj, am, fb, kc, row0);
+                else tma_load_3d_cg<CG>(saj, am, fb, kc, o, row0);
+              } else {
+                mbar_complete_tx_cluster(fb, half ? A_ATOM / 2 : A_ATOM);
+              }
               if constexpr (!TRANS_B) {
-                tma_load_3d_cg<CG>(sbj, &tmB, fb, kc, n0, eb);
+                if (RG_BOUNDS_OK(bounds::inner_aligned(kc, 2) && bounds::index_ok(eb, O * E), args.status))
+                  tma_load_3d_cg<CG>(sbj, &tmB, fb, kc, n0, eb);
+                else
+                  mbar_complete_tx_cluster(fb, B_ATOM);
               } else if (args.mg_wide_b) {  // both 64-column boxes in one copy (4-D view)
-                tma_load_4d_cg<CG>(sbj, &tmB, fb, 0, kc, n0 / 64, eb);
+                if (RG_BOUNDS_OK(n0 % 64 == 0 && bounds::index_ok(eb, O * E), args.status))
+                  tma_load_4d_cg<CG>(sbj, &tmB, fb, 0, kc, n0 / 64, eb);
+                else
+                  mbar_complete_tx_cluster(fb, B_ATOM);
               } else {
 #pragma unroll
-                for (int jj = 0; jj < BN_CTA / 64; ++jj)
-                  tma_load_3d_cg<CG>(sbj + jj * 8192, &tmB, fb, n0 + 64 * jj, kc, eb);
+                for (int jj = 0; jj < BN_CTA / 64; ++jj) {
+                  if (RG_BOUNDS_OK(bounds::inner_aligned(n0 + 64 * jj, 2) && bounds::index_ok(eb, O * E), args.status))
+                    tma_load_3d_cg<CG>(sbj + jj * 8192, &tmB, fb, n0 + 64 * jj, kc, eb);
+                  else
+                    mbar_complete_tx_cluster(fb, 8192);
+                }
               }
             }
             ilog->it[pid][stage] = static_cast<int>(it - 1);
@@ -388,6 +408,7 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
       }
     };
     int o = 0;  // outer group of the current tile
+    int e = 0;  // its inner group (expert)
     // Write one 32-row x 64-column bf16 chunk of this warp (packed pairs p)
     // to out[row0 + q*32 + lane, col0 ..]: a TMA store when all 32 rows
     // belong to the expert and all 64 columns are below col_limit, otherwise
@@ -408,19 +429,25 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if (O == 1) tma_store_2d(map, ebuf_s, col0, row0 + wrow);
-          else tma_store_3d(map, ebuf_s, col0, o, row0 + wrow);
+          if (RG_BOUNDS_OK(bounds::out_box(col0, 64, row0 + wrow, 32, s_off[e], s_off[e + 1], col_limit, 2) &&
+                               bounds::index_ok(o, O),
+                           args.status)) {
+            if (O == 1) tma_store_2d(map, ebuf_s, col0, row0 + wrow);
+            else tma_store_3d(map, ebuf_s, col0, o, row0 + wrow);
+          }
           bulk_commit();
         }
       } else if (wrow + lane < rows_valid) {
         uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<int64_t>(row0 + wrow + lane) * ld + col0));
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (col0 + 8 * j < col_limit) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+          if (col0 + 8 * j < col_limit &&
+              RG_BOUNDS_OK(bounds::out_box(col0 + 8 * j, 8, row0 + wrow + lane, 1, s_off[e], s_off[e + 1], col_limit, 2),
+                           args.status))
+            dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
       }
     };
     int acc = 0;
-    int e = 0;
     for (int t = worker; t < T; t += nworkers, ++acc) {
       const int ti = t / O;
       o = t - ti * O;
@@ -530,6 +557,10 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
             if (lane == 0) {
 #pragma unroll
               for (int h2 = 0; h2 < 2; ++h2) {
+                if (!RG_BOUNDS_OK(bounds::out_box(col0 + 64 * h2, 64, row0 + wrow, 32, s_off[e], s_off[e + 1], N, 2) &&
+                                      bounds::index_ok(o, O),
+                                  args.status))
+                  continue;
                 if (O == 1) tma_store_2d(&tmY, ebuf_s + h2 * 4096, col0 + 64 * h2, row0 + wrow);
                 else tma_store_3d(&tmY, ebuf_s + h2 * 4096, col0 + 64 * h2, o, row0 + wrow);
               }

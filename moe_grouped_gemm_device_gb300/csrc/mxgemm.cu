@@ -41,6 +41,7 @@
 //     sets the device status, the CTA drains and frees tensor memory.
 #include <algorithm>
 
+#include "bounds.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -206,16 +207,37 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
           }
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          tma_load_2d(sa_of(stage), &tmA, fb, kc * BK, row0);
+          // (debug-bounds build: a refused copy's bytes are counted as arrived)
+          if (RG_BOUNDS_OK(bounds::inner_aligned(kc * BK, 1) && bounds::mgemm_rows(row0, s_off[e], s_off[e + 1], args.M),
+                           args.status))
+            tma_load_2d(sa_of(stage), &tmA, fb, kc * BK, row0);
+          else
+            mbar_complete_tx_cluster(fb, BM * BK);
           if constexpr (!TRANS_B) {
-            tma_load_3d(sb_of(stage), &tmB, fb, kc * BK, n0, e);
+            if (RG_BOUNDS_OK(bounds::inner_aligned(kc * BK, 1) && bounds::index_ok(n0, N) && bounds::index_ok(e, E),
+                             args.status))
+              tma_load_3d(sb_of(stage), &tmB, fb, kc * BK, n0, e);
+            else
+              mbar_complete_tx_cluster(fb, BN * BK);
           } else {
-            tma_load_3d(sb_of(stage), &tmB, fb, n0, kc * BK, e);
-            tma_load_3d(sb_of(stage) + 16384, &tmB, fb, n0 + 128, kc * BK, e);
+            if (RG_BOUNDS_OK(bounds::inner_aligned(n0, 1) && bounds::index_ok(e, E), args.status)) {
+              tma_load_3d(sb_of(stage), &tmB, fb, n0, kc * BK, e);
+              tma_load_3d(sb_of(stage) + 16384, &tmB, fb, n0 + 128, kc * BK, e);
+            } else {
+              mbar_complete_tx_cluster(fb, BN * BK);
+            }
           }
-          bulk_load(sfa_of(stage), args.sfa + (static_cast<int64_t>(blk_a) * nkc + kc) * 512, 512, fb);
-          bulk_load(sfb_of(stage), args.sfb + (static_cast<int64_t>(blk_b0) * nkc + kc) * 512, 512, fb);
-          bulk_load(sfb_of(stage) + 512, args.sfb + (static_cast<int64_t>(blk_b1) * nkc + kc) * 512, 512, fb);
+          // scale blocks lie inside the blocked buffers: (M/128 + E) blocks of
+          // A's scales, (E*N/128 + E) of B's, nkc chunks of 512 bytes each
+          if (RG_BOUNDS_OK(bounds::index_ok(blk_a, args.M / 128 + E) && bounds::index_ok(blk_b0, E * N / 128 + E) &&
+                               bounds::index_ok(blk_b1, E * N / 128 + E),
+                           args.status)) {
+            bulk_load(sfa_of(stage), args.sfa + (static_cast<int64_t>(blk_a) * nkc + kc) * 512, 512, fb);
+            bulk_load(sfb_of(stage), args.sfb + (static_cast<int64_t>(blk_b0) * nkc + kc) * 512, 512, fb);
+            bulk_load(sfb_of(stage) + 512, args.sfb + (static_cast<int64_t>(blk_b1) * nkc + kc) * 512, 512, fb);
+          } else {
+            mbar_complete_tx_cluster(fb, 3 * 512);
+          }
           ilog->it[pid][stage] = static_cast<int>(it - 1);
           ilog->bytes[pid][stage] = C::STAGE_BYTES;
           if (++stage == STAGES) {
@@ -320,7 +342,10 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmY, ebuf_s, n0 + 32 * c, row0 + q * 32);
+            if (RG_BOUNDS_OK(bounds::inner_aligned(n0 + 32 * c, 2) && bounds::within(n0 + 32 * c, 32, N) &&
+                                 s_off[e] <= row0 + q * 32 && row0 + q * 32 + 32 <= s_off[e + 1],
+                             args.status))
+              tma_store_2d(&tmY, ebuf_s, n0 + 32 * c, row0 + q * 32);
             bulk_commit();
           }
         }
@@ -599,7 +624,7 @@ struct MxkCfg {
   static constexpr int AB_BYTES = A_BYTES + B_BYTES;
   static constexpr int SF_BYTES = 512 + 1024;
   static constexpr int STAGE_BYTES = AB_BYTES + SF_BYTES;
-  static constexpr int CHUNK_STAGES = kg::CHUNK_ROWS / BR;
+  static constexpr int CHUNK_STAGES = mxk::CHUNK_ROWS / BR;
   static constexpr int EPI_WARPS = 8;
   static constexpr int BOX_COLS = mxk::BOX_COLS;
   static constexpr int EPI_BUF_BYTES = 32 * BOX_COLS * 4;  // 32 rows x BOX_COLS fp32 (one TMA box)
@@ -616,7 +641,7 @@ static_assert(MxkCfg::AB_BYTES % 1024 == 0 && MxkCfg::EPI_BUF_BYTES % (MxkCfg::B
               "operand tiles and epilogue boxes must keep their swizzle alignment");
 static_assert(MxkCfg::SMEM_FIXED + 3 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448,
               "MXFP8 wgrad configuration exceeds the shared memory of a CTA");
-static_assert(kg::CHUNK_ROWS % MxkCfg::BR == 0, "chunks must hold whole stages");
+static_assert(mxk::CHUNK_ROWS % MxkCfg::BR == 0, "chunks must hold whole stages");
 
 __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
     mx_kgemm_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmX,
@@ -762,13 +787,28 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
           }
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          tma_load_2d(sa_of(stage), &tmG, fb, n0, r);
-          tma_load_2d(sb_of(stage), &tmX, fb, k0, r);
-          tma_load_2d(sb_of(stage) + 16384, &tmX, fb, k0 + 128, r);
+          // (debug-bounds build: a refused copy's bytes are counted as arrived)
+          const bool rows_ok = !RG_DEBUG_BOUNDS || (r_begin <= r && r < r_end && (r & 31) == 0);
+          if (RG_BOUNDS_OK(rows_ok && bounds::inner_aligned(n0, 1) && bounds::index_ok(n0, N) &&
+                               bounds::inner_aligned(k0, 1) && bounds::index_ok(k0, K),
+                           args.status)) {
+            tma_load_2d(sa_of(stage), &tmG, fb, n0, r);
+            tma_load_2d(sb_of(stage), &tmX, fb, k0, r);
+            tma_load_2d(sb_of(stage) + 16384, &tmX, fb, k0 + 128, r);
+          } else {
+            mbar_complete_tx_cluster(fb, C::AB_BYTES);
+          }
           const int q = s_qp[e] + c;
-          bulk_load(sfa_of(stage), args.sfa + (static_cast<int64_t>(nb) * NQ + q) * 512, 512, fb);
-          bulk_load(sfb_of(stage), args.sfb + (static_cast<int64_t>(xb0) * NQ + q) * 512, 512, fb);
-          bulk_load(sfb_of(stage) + 512, args.sfb + (static_cast<int64_t>(xb1) * NQ + q) * 512, 512, fb);
+          // scale chunks inside the blocked buffers: ceil(N/128) (or
+          // ceil(K/128)) row blocks of NQ chunks of 512 bytes
+          if (RG_BOUNDS_OK(bounds::index_ok(q, NQ) && bounds::index_ok(nb, (N + 127) / 128) && bounds::index_ok(xb1, nrb_x),
+                           args.status)) {
+            bulk_load(sfa_of(stage), args.sfa + (static_cast<int64_t>(nb) * NQ + q) * 512, 512, fb);
+            bulk_load(sfb_of(stage), args.sfb + (static_cast<int64_t>(xb0) * NQ + q) * 512, 512, fb);
+            bulk_load(sfb_of(stage) + 512, args.sfb + (static_cast<int64_t>(xb1) * NQ + q) * 512, 512, fb);
+          } else {
+            mbar_complete_tx_cluster(fb, 3 * 512);
+          }
           ilog->it[pid][stage] = static_cast<int>(it - 1);
           ilog->bytes[pid][stage] = C::STAGE_BYTES;
           if (++stage == STAGES) {
@@ -849,6 +889,11 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
       const int n0 = nb * BM + 32 * q;
       const int kc0 = kb * BN + 128 * h;
       const bool mine = n0 < N && kc0 < K;  // this warp's boxes hold valid dW elements
+      // a 32-row x BOX_COLS box of dW[e] at column k: inside dW, 16-byte aligned start
+      auto dw_box_ok = [&](int k) {
+        return bounds::inner_aligned(k, 4) && bounds::within(k, C::BOX_COLS, K) && bounds::within(n0, 32, N) &&
+               bounds::index_ok(e, E);
+      };
       if (rows == 0) {  // no rows: dW[e] = 0 (left unchanged when accumulating)
         if (!args.accumulate && mine) {
           if (lane == 0) bulk_wait_read<0>();
@@ -860,7 +905,8 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
           __syncwarp();
           if (lane == 0) {
             for (int b = 0; b < 128 / C::BOX_COLS && kc0 + C::BOX_COLS * b < K; ++b)
-              tma_store_3d(&tmD, ebuf_s, kc0 + C::BOX_COLS * b, n0, e);
+              if (RG_BOUNDS_OK(dw_box_ok(kc0 + C::BOX_COLS * b), args.status))
+                tma_store_3d(&tmD, ebuf_s, kc0 + C::BOX_COLS * b, n0, e);
             bulk_commit();
           }
         }
@@ -902,8 +948,12 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (reduce) tma_reduce_add_3d(&tmD, ebuf_s, kc0 + BC * b, n0, e);
-            else tma_store_3d(&tmD, ebuf_s, kc0 + BC * b, n0, e);
+            if (!RG_BOUNDS_OK(dw_box_ok(kc0 + BC * b), args.status)) {
+            } else if (reduce) {
+              tma_reduce_add_3d(&tmD, ebuf_s, kc0 + BC * b, n0, e);
+            } else {
+              tma_store_3d(&tmD, ebuf_s, kc0 + BC * b, n0, e);
+            }
             bulk_commit();
           }
         }

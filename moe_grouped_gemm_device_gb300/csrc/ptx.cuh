@@ -15,6 +15,7 @@ namespace rg {
 constexpr unsigned int kDevBadOffsets = 0x1u;
 constexpr unsigned int kDevTimeout = 0x2u;
 constexpr unsigned int kDevLaunchConfig = 0x4u;
+constexpr unsigned int kDevBounds = 0x8u;  // debug-bounds builds only
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -193,6 +194,14 @@ static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parit
 // (bytes of a copy that was armed for but will never be issued).
 __device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// complete_tx on a barrier given by its shared::cluster address (own or peer
+// CTA of a pair): the debug-bounds build counts the bytes of a copy it
+// refused to issue, so that the stage completes without them.
+__device__ __forceinline__ void mbar_complete_tx_cluster(uint32_t cluster_addr, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cluster.shared::cluster.b64 [%0], %1;" ::"r"(cluster_addr), "r"(bytes)
+               : "memory");
 }
 
 // 32-bit load from the shared memory of a CTA of the cluster (address from mapa_shared).

@@ -118,9 +118,10 @@ def test_kgemm_nonfinite_rows_stay_in_their_expert(gpu_lib):
 
 
 def test_kgemm_long_experts_bit_exact(gpu_lib):
-    """Experts longer than one accumulation chunk (4096 rows): the partial
-    sums folded into dW must reproduce the exact integer result."""
-    counts = [9000, 0, 4100, 37, 8192]
+    """Experts longer than one accumulation chunk (4032 rows): the partial
+    sums folded into dW must reproduce the exact integer result; chunk
+    boundaries at 4032, 4033 and 8064 rows."""
+    counts = [9000, 0, 4100, 37, 8192, 4032, 4033, 8064]
     off = W.offsets_from_counts(counts)
     M, N, K = int(off[-1]) + 5, 256, 320
     g = ints((M, N), 3, 0)
@@ -143,7 +144,7 @@ def test_kgemm_several_rounds_bit_exact(gpu_lib):
 
 
 def test_kgemm_long_experts_random(gpu_lib):
-    counts = [12000, 5000, 4096, 4097]
+    counts = [12000, 5000, 4032, 4033, 4096]
     off = W.offsets_from_counts(counts)
     M, N, K = int(off[-1]), 384, 256
     g = W.normal_bf16((M, N), 1.0, 31, 0)
@@ -166,7 +167,7 @@ def run_kgemm_acc(rg, g, x, off, init):
 
 def test_kgemm_accumulate_bit_exact(gpu_lib):
     """dW += sum: integer data keeps every partial sum exact, including the
-    chunk-by-chunk additions of experts longer than 4096 rows; the empty
+    chunk-by-chunk additions of experts longer than 4032 rows; the empty
     expert keeps its initial values."""
     counts = [5000, 0, 130, 1]
     off = W.offsets_from_counts(counts)
