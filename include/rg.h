@@ -55,9 +55,10 @@ extern "C" {
 
 /* Largest number of experts one call accepts. */
 #define RG_MAX_EXPERTS 1024
-/* Largest number of experts of rg_kgemm / rg_kgemm_acc: their per-expert
- * tables share a CTA's shared memory with the operand ring. */
-#define RG_KGEMM_MAX_EXPERTS 358
+/* Largest number of experts of rg_kgemm / rg_kgemm_acc (the same as every
+ * other entry point's; beyond about 360 experts their per-expert tables take
+ * the room of one of the four stages of the operand ring). */
+#define RG_KGEMM_MAX_EXPERTS 1024
 /* Largest number of outer groups of rg_mgemm_nested. */
 #define RG_MAX_OUTER 65536
 

@@ -44,7 +44,7 @@ RG_DEV_LAUNCH_CONFIG = 0x4
 RG_DEV_BOUNDS = 0x8
 RG_MAX_EXPERTS = 1024
 RG_MAX_OUTER = 65536
-RG_KGEMM_MAX_EXPERTS = 358
+RG_KGEMM_MAX_EXPERTS = 1024
 
 EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_nested", "rg_mgemm_mxfp8", "rg_mx_scales_blocked", "rg_mx_blocked_bytes", "rg_kgemm_mxfp8", "rg_mx_scales_blocked_k", "rg_mx_blocked_k_bytes", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_shutdown", "rg_set_wait_timeout_ns",
                     "rg_selftest_wait_timeout", "rg_last_cuda_error", "rg_device_supported",

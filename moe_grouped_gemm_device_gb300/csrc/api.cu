@@ -542,7 +542,6 @@ int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, i
                float* dW, int accumulate, cudaStream_t stream) {
   int rc = check_common(offsets, E, M, N, K);
   if (rc != RG_OK) return rc;
-  if (E > RG_KGEMM_MAX_EXPERTS) return RG_ERR_INVALID_ARG;
   if (dW == nullptr || !aligned16(dW)) return RG_ERR_INVALID_ARG;
   if (M > 0 && (grad == nullptr || X == nullptr || !aligned16(grad) || !aligned16(X)))
     return RG_ERR_INVALID_ARG;
@@ -551,7 +550,7 @@ int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, i
   if (tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != RG_OK) return rc;
-  if (rg::kgemm_smem_bytes(E) > ds->max_smem) return RG_ERR_INVALID_ARG;
+  if (rg::kgemm_smem_bytes(E, ds->max_smem) > ds->max_smem) return RG_ERR_INVALID_ARG;
 
   // With M == 0 every valid offsets vector is all zeros, so the kernel only
   // writes zero tiles; the operand maps then describe one row of dW, which is
@@ -588,13 +587,14 @@ int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, i
   {
     const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
     const uint64_t str[2] = {static_cast<uint64_t>(K) * 4, static_cast<uint64_t>(N) * K * 4};
-    const uint32_t box[3] = {32, 32, 1};
-    if (!encode(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dW, dims, str, box)) return RG_ERR_INVALID_ARG;
+    const uint32_t box[3] = {static_cast<uint32_t>(rg::kg::BOX_COLS), 32, 1};
+    const CUtensorMapSwizzle sw = rg::kg::BOX_COLS == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!encode_sw(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dW, dims, str, box, sw)) return RG_ERR_INVALID_ARG;
   }
   rg::GroupArgs args = group_args(ds, offsets, E, M, N, K, dW);
   args.accumulate = accumulate;
   args.kg_wide = wide ? 1 : 0;
-  const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->kg_grid, stream);
+  const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->kg_grid, ds->max_smem, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
 }

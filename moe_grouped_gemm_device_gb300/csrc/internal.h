@@ -59,9 +59,14 @@ constexpr int kCtaGroup = RG_CTA_PAIR ? 2 : 1;
 #ifndef RG_MXK_BOX_COLS
 #define RG_MXK_BOX_COLS 16
 #endif
+#ifndef RG_MXK_EPI_GROUP
+#define RG_MXK_EPI_GROUP 1
+#endif
 namespace mxk {
 constexpr int STAGES = RG_MXK_STAGES;
 constexpr int BOX_COLS = RG_MXK_BOX_COLS;
+constexpr int EPI_GROUP = RG_MXK_EPI_GROUP;  // dW boxes staged and stored per bulk group
+static_assert(EPI_GROUP == 1 || EPI_GROUP == 2 || EPI_GROUP == 4, "1, 2 or 4 boxes per bulk group");
 constexpr int CHUNK_ROWS = 4096;  // rows summed in tensor memory per partial (32 stages of 128)
 static_assert(BOX_COLS == 16 || BOX_COLS == 32, "dW boxes are 16 or 32 fp32 columns wide");
 }  // namespace mxk
@@ -79,18 +84,50 @@ constexpr int BN_CTA = BN / kCtaGroup;   // B rows loaded per CTA
 constexpr int BK = 64;
 }  // namespace mg
 
+// K-grouped pipeline shape (compile-time switches for comparison builds):
+// rows of the contraction per stage, stages in the ring (CTA pairs), and the
+// 32 x 32 fp32 dW boxes an epilogue warp stages and stores per bulk group.
+#ifndef RG_KG_BR
+#define RG_KG_BR 96
+#endif
+#ifndef RG_KG_STAGES
+#define RG_KG_STAGES 4
+#endif
+#ifndef RG_KG_EPI_GROUP
+#define RG_KG_EPI_GROUP 1
+#endif
+// Columns of a dW box (32 x 32 fp32 with a 128-byte swizzle, or 32 x 16 with a 64-byte one).
+#ifndef RG_KG_BOX_COLS
+#define RG_KG_BOX_COLS 32
+#endif
+// An L2 evict-last hint on the operand copies (1) or none (0).
+#ifndef RG_KG_LOAD_HINT
+#define RG_KG_LOAD_HINT 1
+#endif
 namespace kg {
 constexpr int BM = 128;                  // dW rows per CTA
 constexpr int TILE_M = BM * kCtaGroup;   // dW rows per tile
 constexpr int BN = 256;                  // dW columns per tile
 constexpr int BN_CTA = BN / kCtaGroup;   // X columns loaded per CTA
-constexpr int BR = 96;                   // contraction rows per stage (six 16-row MMA steps)
+constexpr int BR = RG_KG_BR;             // contraction rows per stage (BR / 16 MMA steps)
+constexpr int STAGES = RG_KG_STAGES;
+constexpr int EPI_GROUP = RG_KG_EPI_GROUP;
+constexpr int BOX_COLS = RG_KG_BOX_COLS;
+static_assert(BOX_COLS == 16 || BOX_COLS == 32, "dW boxes are 16 or 32 fp32 columns wide");
+static_assert(BR % 16 == 0 && BR >= 16 && BR <= 256, "stages hold whole 16-row MMA steps");
+static_assert(EPI_GROUP == 1 || EPI_GROUP == 2 || EPI_GROUP == 4, "1, 2 or 4 dW boxes per bulk group");
 // Rows of one expert accumulated in tensor memory before the partial sum is
-// folded into dW (store for the first chunk, fp32 reduce-add for the rest).
-// Bounds the length of each fp32 accumulation chain inside the tensor cores.
-constexpr int CHUNK_ROWS = 4032;
-static_assert(CHUNK_ROWS % BR == 0, "chunks must hold whole row blocks");
+// folded into dW (store for the first chunk, fp32 reduce-add for the rest):
+// whole stages, at most 4096 rows.  Bounds the length of each fp32
+// accumulation chain inside the tensor cores.
+constexpr int CHUNK_ROWS = 4096 / BR * BR;
 }  // namespace kg
+
+// Sleep between polls of the accumulator barrier by the epilogue of the
+// one-stage Mgemm tiles (contractions of at most 64; comparison builds).
+#ifndef RG_MG_SHORT_POLL_NS
+#define RG_MG_SHORT_POLL_NS 1000
+#endif
 
 // Mgemm tile variants (CTA pairs only): 64-column tiles for forward outputs at
 // most 64 wide, eight epilogue warps when the contraction fits one 64-deep
@@ -101,7 +138,7 @@ inline int mgemm_b_box_rows(bool transpose_B, int N) { return mgemm_narrow(trans
 
 // Bytes of dynamic shared memory a launch with E experts needs.
 size_t mgemm_smem_bytes(int E);
-size_t kgemm_smem_bytes(int E);
+size_t kgemm_smem_bytes(int E, size_t max_smem);  // of the ring a launch with E experts uses
 
 // One-time per-device kernel attribute setup: allow up to `max_smem` bytes
 // of dynamic shared memory (the device's opt-in limit).
@@ -130,8 +167,9 @@ cudaError_t launch_mgemm_swiglu(const CUtensorMap& tmA, const CUtensorMap& tmB, 
 cudaError_t launch_mgemm_swiglu_dgrad(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                       const CUtensorMap& tmDy13, const GroupArgs& args, int grid,
                                       cudaStream_t stream);
+// Four-stage ring, or three stages when the expert tables would not fit beside four.
 cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
-                         const GroupArgs& args, int grid, cudaStream_t stream);
+                         const GroupArgs& args, int grid, size_t max_smem, cudaStream_t stream);
 // MXFP8 Mgemm (FP8 E4M3 operands, E8M0 scales per 32 K elements in the
 // blocked layout) and the conversion of grouped scales to that layout.
 size_t mx_smem_bytes(int E);

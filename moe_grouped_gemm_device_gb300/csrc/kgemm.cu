@@ -67,7 +67,10 @@ struct Cfg {
   static constexpr int B_BYTES = BN_CTA * BR * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_WARPS = 8;              // two per TMEM lane quarter
-  static constexpr int EPI_BUF_BYTES = 32 * 128;  // one 32x32 fp32 box per epilogue warp
+  static constexpr int EPI_GROUP = kg::EPI_GROUP;  // dW boxes staged per bulk group
+  static constexpr int BOX_COLS = kg::BOX_COLS;    // fp32 columns of a 32-row dW box
+  static constexpr int DW_BOX_BYTES = 32 * BOX_COLS * 4;
+  static constexpr int EPI_BUF_BYTES = DW_BOX_BYTES * EPI_GROUP;  // per epilogue warp
   // warp 0 and the last warp: TMA producers (alternate stages), warp 1: MMA,
   // warps 2..9: epilogue
   static constexpr int PRODUCER2 = 2 + EPI_WARPS;
@@ -82,6 +85,9 @@ struct Cfg {
 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int CHUNK_ROWS = kg::CHUNK_ROWS;
+// An expert whose operand rows take more than half of the 126 MB L2 cannot
+// keep them there between two rounds of its tiles.
+constexpr long long kKmajorBytes = 64ll << 20;
 
 
 template <int CG, int ST>
@@ -180,6 +186,18 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
   // Tile t of the list sorted by decreasing expert rows (longest first);
   // worker w takes tiles w, w+W, ..., so every round of W tiles has
   // near-equal cost.
+  // (n block, k block) of an expert's tile.  The tiles of an expert run over
+  // more than one round of the grid; if its operand rows overflow L2 between
+  // rounds, the second round reads again the operand whose blocks the first
+  // round did not finish.  Tiles go n-major (k blocks vary fastest: grad's
+  // n blocks are finished in turn, X is read again) unless the expert is that
+  // large and grad is the narrower operand (N < K): then k-major.
+  auto kmajor = [&](int e) {
+    const long long bytes = 2ll * (s_off[e + 1] - s_off[e]) * (N + K);
+    return N < K && bytes > kKmajorBytes;
+  };
+  auto nblk = [&](int e, int local) { return kmajor(e) ? local % nbn : local / nbk; };
+  auto kblk = [&](int e, int local) { return kmajor(e) ? local / nbn : local % nbk; };
   auto tile_at = [&](int t, int& e, int& local) {
     const int pe = t / tpe;
     e = s_ord[pe];
@@ -193,6 +211,7 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmG);
       tma_prefetch_desc(&tmX);
+      [[maybe_unused]] const uint64_t op_policy = RG_KG_LOAD_HINT ? l2_policy_evict_last() : 0;
       const uint32_t pid = warp == 0 ? 0u : 1u;
       issue_log_init(ilog, pid);
       uint32_t it = 0;
@@ -203,8 +222,8 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
       for (int t = worker; t < T && ok; t += nworkers) {
         int e, local;
         tile_at(t, e, local);
-        const int n0 = (local / nbk) * TILE_M + static_cast<int>(rank) * BM;
-        const int k0 = (local % nbk) * BN + static_cast<int>(rank) * BN_CTA;
+        const int n0 = nblk(e, local) * TILE_M + static_cast<int>(rank) * BM;
+        const int k0 = kblk(e, local) * BN + static_cast<int>(rank) * BN_CTA;
         const int r_begin = s_off[e], r_end = s_off[e + 1];
         for (int r = r_begin; r < r_end; r += BR) {
           if ((it++ & 1u) != pid) {  // the other producer's stage
@@ -229,14 +248,18 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
           // of expert e; a refused copy's bytes are counted as arrived)
           const bool rows_ok = !RG_DEBUG_BOUNDS || bounds::kgemm_rows(r, i0, BR, r_begin, r_end);
           if (args.kg_wide) {  // one copy per operand: column blocks n0/64 .. and k0/64 ..
-            if (RG_BOUNDS_OK(rows_ok && n0 % 64 == 0, args.status))
-              tma_load_4d_cg<CG>(sa, &tmG, fb, 0, i0, n0 / 64, r);
-            else
+            if (RG_BOUNDS_OK(rows_ok && n0 % 64 == 0, args.status)) {
+              if constexpr (RG_KG_LOAD_HINT && CG == 2) tma_load_4d_pair_hint(sa, &tmG, fb, 0, i0, n0 / 64, r, op_policy);
+              else tma_load_4d_cg<CG>(sa, &tmG, fb, 0, i0, n0 / 64, r);
+            } else {
               mbar_complete_tx_cluster(fb, A_BYTES);
-            if (RG_BOUNDS_OK(rows_ok && k0 % 64 == 0, args.status))
-              tma_load_4d_cg<CG>(sb, &tmX, fb, 0, i0, k0 / 64, r);
-            else
+            }
+            if (RG_BOUNDS_OK(rows_ok && k0 % 64 == 0, args.status)) {
+              if constexpr (RG_KG_LOAD_HINT && CG == 2) tma_load_4d_pair_hint(sb, &tmX, fb, 0, i0, k0 / 64, r, op_policy);
+              else tma_load_4d_cg<CG>(sb, &tmX, fb, 0, i0, k0 / 64, r);
+            } else {
               mbar_complete_tx_cluster(fb, C::B_BYTES);
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < BM / 64; ++j) {
@@ -338,22 +361,38 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     const int h = (warp - 2) >> 2;
     uint8_t* ebuf = epi + (warp - 2) * EPI_BUF_BYTES;
     const uint32_t ebuf_s = smem_u32(ebuf);
-    uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * 128);
+    constexpr int GB = C::EPI_GROUP;
+    constexpr int BC = C::BOX_COLS, BOXB = C::DW_BOX_BYTES;
+    constexpr int NBOX = (BN / 2) / BC;  // boxes of this warp's 128 columns
+    // staging swizzle: 16-byte chunk ^= row % 8 (128-byte rows) or (row / 2) % 4 (64-byte rows)
+    const int sw = BC == 32 ? (lane & 7) : ((lane >> 1) & 3);
     const uint32_t tempty_issuer = CG == 2 ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
     // dW is written once and never read here: first out of L2, so that the
     // operand rows other tiles of the expert still need stay resident
     const uint64_t dw_policy = l2_policy_evict_first();
     int acc = 0;
     bool ok = true;
-    auto stage_box = [&](const uint32_t* v) {
-      if (lane == 0) bulk_wait_read<0>();  // the previous store has left the buffer
+    // Stage the boxes of one bulk group: the values of box b at v + 32 b
+    // (v = null: zeros) into slot b of this warp's buffer, after the previous
+    // group has left the buffer; one proxy fence for all of them.
+    auto stage_group = [&](const uint32_t* v, int nb) {
+      if (lane == 0) bulk_wait_read<0>();
       __syncwarp();
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        rowp[j ^ (lane & 7)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      for (int b = 0; b < GB; ++b) {
+        if (b >= nb) break;
+        uint4* rowp = reinterpret_cast<uint4*>(ebuf + b * BOXB + lane * BC * 4);
+#pragma unroll
+        for (int j = 0; j < BC / 4; ++j)
+          rowp[j ^ sw] = v ? make_uint4(v[BC * b + 4 * j], v[BC * b + 4 * j + 1], v[BC * b + 4 * j + 2],
+                                        v[BC * b + 4 * j + 3])
+                           : make_uint4(0u, 0u, 0u, 0u);
+      }
       fence_proxy_async_smem();
       __syncwarp();
     };
+    // boxes of this warp's 128 columns at kh that lie below K, from box c0 on, at most GB
+    auto group_boxes = [&](int kh, int c0) { return min(GB, (K - kh - BC * c0 + BC - 1) / BC); };
     auto release_acc = [&](int buf) {
       tc_fence_before();
       __syncwarp();
@@ -362,29 +401,28 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         else mbar_arrive(tempty_bar(buf));
       }
     };
-    // a 32 x 32 fp32 box of dW[e] at (column k, row n): inside dW, 16-byte aligned start
+    // a 32-row x BC-column fp32 box of dW[e] at (column k, row n): inside dW, 16-byte aligned start
     auto dw_box_ok = [&](int k, int n, int ee) {
-      return bounds::inner_aligned(k, 4) && bounds::within(k, 32, K) && bounds::within(n, 32, N) &&
+      return bounds::inner_aligned(k, 4) && bounds::within(k, BC, K) && bounds::within(n, 32, N) &&
              bounds::index_ok(ee, E);
     };
     for (int t = worker; t < T && ok; t += nworkers) {
       int e, local;
       tile_at(t, e, local);
-      const int n0 = (local / nbk) * TILE_M + static_cast<int>(rank) * BM;
-      const int kh = (local % nbk) * BN + h * (BN / 2);  // first dW column of this warp
+      const int n0 = nblk(e, local) * TILE_M + static_cast<int>(rank) * BM;
+      const int kh = kblk(e, local) * BN + h * (BN / 2);  // first dW column of this warp
       const int r_begin = s_off[e], r_end = s_off[e + 1];
       const bool warp_rows = n0 + q * 32 < N;  // this warp's 32 rows of dW exist
       if (r_end == r_begin) {  // expert without rows: dW tile = 0 (unchanged when accumulating)
         if (!warp_rows || args.accumulate) continue;
-        uint32_t z[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] = 0u;
 #pragma unroll 1
-        for (int c = 0; c < BN / 64 && kh + 32 * c < K; ++c) {
-          stage_box(z);
+        for (int c0 = 0; c0 < NBOX && kh + BC * c0 < K; c0 += GB) {
+          const int nb = group_boxes(kh, c0);
+          stage_group(nullptr, nb);
           if (lane == 0) {
-            if (RG_BOUNDS_OK(dw_box_ok(kh + 32 * c, n0 + q * 32, e), args.status))
-              tma_store_3d(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e);
+            for (int b = 0; b < nb; ++b)
+              if (RG_BOUNDS_OK(dw_box_ok(kh + BC * (c0 + b), n0 + q * 32, e), args.status))
+                tma_store_3d(&tmD, ebuf_s + b * BOXB, kh + BC * (c0 + b), n0 + q * 32, e);
             bulk_commit();
           }
         }
@@ -412,16 +450,19 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         release_acc(buf);  // accumulator fully read: hand it back
         if (!first && lane == 0) bulk_wait<0>();  // previous partial of this tile is in dW
 #pragma unroll
-        for (int c = 0; c < BN / 64; ++c) {
-          if (kh + 32 * c >= K) break;
-          stage_box(v + 32 * c);
-          if (lane == 0 && !RG_BOUNDS_OK(dw_box_ok(kh + 32 * c, n0 + q * 32, e), args.status)) {
-            bulk_commit();
-          } else if (lane == 0) {
-            if (overwrite)
-              tma_store_3d_hint(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e, dw_policy);
-            else
-              tma_reduce_add_3d_hint(&tmD, ebuf_s, kh + 32 * c, n0 + q * 32, e, dw_policy);
+        for (int c0 = 0; c0 < NBOX; c0 += GB) {
+          if (kh + BC * c0 >= K) break;
+          const int nb = group_boxes(kh, c0);
+          stage_group(v + BC * c0, nb);
+          if (lane == 0) {
+            for (int b = 0; b < nb; ++b) {
+              const int kb = kh + BC * (c0 + b);
+              if (!RG_BOUNDS_OK(dw_box_ok(kb, n0 + q * 32, e), args.status)) continue;
+              if (overwrite)
+                tma_store_3d_hint(&tmD, ebuf_s + b * BOXB, kb, n0 + q * 32, e, dw_policy);
+              else
+                tma_reduce_add_3d_hint(&tmD, ebuf_s + b * BOXB, kb, n0 + q * 32, e, dw_policy);
+            }
             bulk_commit();
           }
         }
@@ -449,16 +490,25 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
   }
 }
 
-// Ring depth.  The shared-memory tables of the experts sit beside it, which
-// bounds E (RG_KGEMM_MAX_EXPERTS in rg.h; the host rejects larger E).
-constexpr int kStagesDeep = kCtaGroup == 2 ? 4 : 2;
-static_assert(Cfg<kCtaGroup, kStagesDeep>::SMEM_FIXED + (2 * RG_KGEMM_MAX_EXPERTS + 1) * 4 <= 232448,
-              "the expert tables of RG_KGEMM_MAX_EXPERTS experts must fit beside the ring");
+// Ring depth.  The shared-memory tables of the experts sit beside the ring:
+// a launch whose tables do not fit beside the deep ring (more than about 360
+// experts with CTA pairs) runs the same kernel with one stage fewer, which
+// leaves room for RG_MAX_EXPERTS_CFG experts.
+constexpr int kStagesDeep = kCtaGroup == 2 ? kg::STAGES : 2;
+constexpr int kStagesShallow =
+    Cfg<kCtaGroup, kStagesDeep>::SMEM_FIXED + (2 * RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 ? kStagesDeep
+                                                                                         : kStagesDeep - 1;
+static_assert(kStagesShallow >= 2, "the shallow ring keeps two stages");
+static_assert(Cfg<kCtaGroup, kStagesShallow>::SMEM_FIXED + (2 * RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448,
+              "the expert tables of RG_MAX_EXPERTS_CFG experts must fit beside the shallow ring");
 
 template <int ST>
 size_t smem_bytes(int E) {
   return Cfg<kCtaGroup, ST>::SMEM_FIXED + (2 * static_cast<size_t>(E) + 1) * 4;
 }
+
+// The deep ring when the expert tables fit beside it in `max_smem` bytes.
+bool use_deep(int E, size_t max_smem) { return smem_bytes<kStagesDeep>(E) <= max_smem; }
 
 void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, size_t smem,
                  cudaStream_t stream) {
@@ -479,12 +529,18 @@ void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, s
 
 }  // namespace
 
-size_t kgemm_smem_bytes(int E) { return smem_bytes<kStagesDeep>(E); }
+size_t kgemm_smem_bytes(int E, size_t max_smem) {
+  return use_deep(E, max_smem) ? smem_bytes<kStagesDeep>(E) : smem_bytes<kStagesShallow>(E);
+}
 
 cudaError_t kgemm_setup(int max_smem) {
-  return cudaFuncSetAttribute(
+  cudaError_t e = cudaFuncSetAttribute(
       kgemm_kernel<kCtaGroup, kStagesDeep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      static_cast<int>(std::min<size_t>(smem_bytes<kStagesDeep>(RG_KGEMM_MAX_EXPERTS), max_smem)));
+      static_cast<int>(std::min<size_t>(smem_bytes<kStagesDeep>(RG_MAX_EXPERTS_CFG), max_smem)));
+  if (e != cudaSuccess || kStagesShallow == kStagesDeep) return e;
+  return cudaFuncSetAttribute(
+      kgemm_kernel<kCtaGroup, kStagesShallow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      static_cast<int>(std::min<size_t>(smem_bytes<kStagesShallow>(RG_MAX_EXPERTS_CFG), max_smem)));
 }
 
 cudaError_t kgemm_max_clusters(int* clusters, int max_smem) {
@@ -495,11 +551,15 @@ cudaError_t kgemm_max_clusters(int* clusters, int max_smem) {
 }
 
 cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const CUtensorMap& tmD,
-                         const GroupArgs& args, int grid, cudaStream_t stream) {
+                         const GroupArgs& args, int grid, size_t max_smem, cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  fill_config(&cfg, attr, grid, smem_bytes<kStagesDeep>(args.E), stream);
-  return cudaLaunchKernelEx(&cfg, kgemm_kernel<kCtaGroup, kStagesDeep>, tmG, tmX, tmD, args);
+  if (use_deep(args.E, max_smem)) {
+    fill_config(&cfg, attr, grid, smem_bytes<kStagesDeep>(args.E), stream);
+    return cudaLaunchKernelEx(&cfg, kgemm_kernel<kCtaGroup, kStagesDeep>, tmG, tmX, tmD, args);
+  }
+  fill_config(&cfg, attr, grid, smem_bytes<kStagesShallow>(args.E), stream);
+  return cudaLaunchKernelEx(&cfg, kgemm_kernel<kCtaGroup, kStagesShallow>, tmG, tmX, tmD, args);
 }
 
 }  // namespace rg

@@ -77,6 +77,10 @@ struct Cfg {
   static constexpr int B_BYTES = B_ATOM * KATOMS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_WARPS = EPIW;
+  // sleep between the epilogue's polls of its accumulator barrier: 1 us for
+  // tiles of many stages (polling costs the copies and MMAs shared-memory
+  // bandwidth), RG_MG_SHORT_POLL_NS for one-stage tiles (a few us each)
+  static constexpr uint32_t ACC_POLL_NS = EPIW == 8 ? RG_MG_SHORT_POLL_NS : 1000;
   // staging per epilogue warp: one 32-row x 64-column bf16 box, or with 8
   // epilogue warps (two chunks per warp and tile) two, written together
   static constexpr int EPI_BUF_BYTES = 32 * 128 * (EPIW == 8 ? 2 : 1);
@@ -360,7 +364,8 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BKS / 16; ++k) {
             const int j = k / (BK / 16), kk = k % (BK / 16);  // atom, 16-deep step in it
-            if (kb * BKS + BK * j < K) {
+            // steps at or past K multiply zero-filled columns: skipped (bit-identical)
+            if (kb * BKS + BK * j + 16 * kk < K) {
               const uint32_t saj = sa + j * A_ATOM, sbj = sb + j * B_ATOM;
               const uint64_t ad = sdesc_sw128(saj + 32 * kk, 16, 1024);
               const uint64_t bd = TRANS_B ? sdesc_sw128(sbj + 2048 * kk, 8192, 1024)
@@ -461,7 +466,7 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
       wrow = half ? (q & 1) * 32 : q * 32;
       const int buf = acc & 1;
       const uint32_t tph = (acc >> 1) & 1;
-      if (!warp_wait_acc<CG>(guard, tfull_bar(buf), tph)) break;
+      if (!warp_wait_acc<CG, C::ACC_POLL_NS>(guard, tfull_bar(buf), tph)) break;
       tc_fence_after();
       if (wrow >= rows_valid) {  // none of this warp's rows belong to the expert
         release_acc(buf);

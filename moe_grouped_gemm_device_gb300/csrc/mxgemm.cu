@@ -627,7 +627,9 @@ struct MxkCfg {
   static constexpr int CHUNK_STAGES = mxk::CHUNK_ROWS / BR;
   static constexpr int EPI_WARPS = 8;
   static constexpr int BOX_COLS = mxk::BOX_COLS;
-  static constexpr int EPI_BUF_BYTES = 32 * BOX_COLS * 4;  // 32 rows x BOX_COLS fp32 (one TMA box)
+  static constexpr int BOX_BYTES = 32 * BOX_COLS * 4;      // 32 rows x BOX_COLS fp32 (one TMA box)
+  static constexpr int EPI_GROUP = mxk::EPI_GROUP;
+  static constexpr int EPI_BUF_BYTES = BOX_BYTES * EPI_GROUP;  // per epilogue warp
   // warps 0 and 10: producers (alternate stages), 1: MMA, 2..9: epilogue
   static constexpr int PRODUCER2 = 2 + EPI_WARPS;
   static constexpr int THREADS = 32 * (PRODUCER2 + 1);
@@ -935,24 +937,34 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
         constexpr int BC = C::BOX_COLS, CH = BC / 4;  // 16-byte chunks per box row
         // swizzle: chunk ^= row % 8 (128-byte rows) or (row / 2) % 4 (64-byte rows)
         const int sw = BC == 32 ? (lane & 7) : ((lane >> 1) & 3);
+        // groups of GB boxes: staged together after the previous group has
+        // left the buffer, one proxy fence, their stores in one bulk group
+        constexpr int GB = C::EPI_GROUP;
 #pragma unroll
-        for (int b = 0; b < 128 / BC; ++b) {
-          if (kc0 + BC * b >= K) break;
-          if (lane == 0) bulk_wait_read<0>();  // the buffer's previous box has left
+        for (int b0 = 0; b0 < 128 / BC; b0 += GB) {
+          if (kc0 + BC * b0 >= K) break;
+          const int nb = min(GB, (K - kc0 - BC * b0 + BC - 1) / BC);
+          if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
-          uint4* rowp = reinterpret_cast<uint4*>(ebuf + lane * BC * 4);
 #pragma unroll
-          for (int j = 0; j < CH; ++j)
-            rowp[j ^ sw] = make_uint4(v[BC * b + 4 * j], v[BC * b + 4 * j + 1], v[BC * b + 4 * j + 2],
-                                      v[BC * b + 4 * j + 3]);
+          for (int g = 0; g < GB; ++g) {
+            if (g >= nb) break;
+            const int b = b0 + g;
+            uint4* rowp = reinterpret_cast<uint4*>(ebuf + g * C::BOX_BYTES + lane * BC * 4);
+#pragma unroll
+            for (int j = 0; j < CH; ++j)
+              rowp[j ^ sw] = make_uint4(v[BC * b + 4 * j], v[BC * b + 4 * j + 1], v[BC * b + 4 * j + 2],
+                                        v[BC * b + 4 * j + 3]);
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (!RG_BOUNDS_OK(dw_box_ok(kc0 + BC * b), args.status)) {
-            } else if (reduce) {
-              tma_reduce_add_3d(&tmD, ebuf_s, kc0 + BC * b, n0, e);
-            } else {
-              tma_store_3d(&tmD, ebuf_s, kc0 + BC * b, n0, e);
+            for (int g = 0; g < nb; ++g) {
+              const int kb = kc0 + BC * (b0 + g);
+              const uint32_t src = ebuf_s + g * C::BOX_BYTES;
+              if (!RG_BOUNDS_OK(dw_box_ok(kb), args.status)) continue;
+              if (reduce) tma_reduce_add_3d(&tmD, src, kb, n0, e);
+              else tma_store_3d(&tmD, src, kb, n0, e);
             }
             bulk_commit();
           }

@@ -164,13 +164,13 @@ static __device__ __noinline__ bool mbar_wait_cl_sleep(const WaitGuard& g, uint3
 // between polls, and the warp takes its answer (measured: the pair kernels'
 // epilogues polling flat out cost the weight-gradient GEMM ~1%); single CTAs
 // use the suspending wait.
-template <int CG>
+template <int CG, uint32_t SLEEP_NS = 1000>
 __device__ __forceinline__ bool warp_wait_acc(const WaitGuard& g, uint32_t bar, uint32_t parity) {
   if constexpr (CG == 1) {
     return __all_sync(0xffffffffu, mbar_wait(g, bar, parity)) != 0;
   } else {
     bool got = true;
-    if ((threadIdx.x & 31) == 0) got = mbar_wait_cl_sleep(g, bar, parity, 1000);
+    if ((threadIdx.x & 31) == 0) got = mbar_wait_cl_sleep(g, bar, parity, SLEEP_NS);
     return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
   }
 }
@@ -340,6 +340,23 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
+}
+
+// The pair load with an L2 cache-policy hint (createpolicy).
+__device__ __forceinline__ void tma_load_4d_pair_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0,
+                                                      int32_t c1, int32_t c2, int32_t c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+      : "memory");
+}
+
+// L2 eviction-priority policy for data that later copies will read again.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 template <int CG>
