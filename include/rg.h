@@ -55,9 +55,9 @@ extern "C" {
 
 /* Largest number of experts one call accepts. */
 #define RG_MAX_EXPERTS 1024
-/* Largest number of experts of rg_kgemm / rg_kgemm_acc (the same as every
- * other entry point's; beyond about 360 experts their per-expert tables take
- * the room of one of the four stages of the operand ring). */
+/* Largest number of experts of rg_kgemm / rg_kgemm_acc / rg_kgemm_ws (the
+ * same as every other entry point's; beyond 239 experts their per-expert
+ * tables take the room of one of the four stages of the operand ring). */
 #define RG_KGEMM_MAX_EXPERTS 1024
 /* Largest number of outer groups of rg_mgemm_nested. */
 #define RG_MAX_OUTER 65536
@@ -321,6 +321,40 @@ int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int
  */
 int rg_kgemm_acc(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M,
                  int N, int K, float* dW, cudaStream_t stream);
+
+/*
+ * rg_kgemm_workspace_bytes -- device workspace that rg_kgemm_ws needs for E
+ * experts and an [N, K] weight gradient: one 4-byte flag per expert, dW tile
+ * (256 x 256) and CTA of a tile's CTA pair,
+ * E * ceil(N/256) * ceil(K/256) * 2 * 4 bytes.  -1 on bad arguments.
+ * Host-only; touches no device.
+ */
+int64_t rg_kgemm_workspace_bytes(int E, int N, int K);
+
+/*
+ * rg_kgemm_ws -- rg_kgemm (accumulate == 0) or rg_kgemm_acc (accumulate != 0)
+ * with a schedule that reads each row of a long expert from DRAM once.  An
+ * expert of more than one accumulation chunk (4032 rows) has all of its dW
+ * tiles work on one chunk of its rows in the same round of the persistent
+ * grid, instead of each tile walking all of the expert's rows; when the
+ * expert's rows exceed the L2 cache, rg_kgemm reads them again for each
+ * round its tiles span.  The chunks of a tile then run on different CTAs,
+ * and each chunk's fp32 reduce-add into dW waits for the previous chunk's
+ * writes through a flag in `workspace`, so the chunks are still added in row
+ * order: results are bit-identical to rg_kgemm's / rg_kgemm_acc's.
+ * (RapidGEMM README, "Kernels", Kgemm; the schedule is this library's.)
+ *
+ *   grad, X, offsets, E, M, N, K, dW  as for rg_kgemm.
+ *   workspace        device memory owned by the caller, 4-byte aligned, at
+ *                    least rg_kgemm_workspace_bytes(E, N, K) bytes; the call
+ *                    zeroes those bytes on `stream` before the kernel.  Two
+ *                    calls that may run at the same time need two workspaces.
+ *   workspace_bytes  its size.
+ * Returns RG_ERR_INVALID_ARG for a null, misaligned or too small workspace,
+ * otherwise as rg_kgemm.
+ */
+int rg_kgemm_ws(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,
+                float* dW, int accumulate, void* workspace, int64_t workspace_bytes, cudaStream_t stream);
 
 /*
  * rg_get_device_status -- after the work already queued on `stream`, read

@@ -30,7 +30,7 @@ import os
 
 from . import _build
 
-__all__ = ["load", "mgemm", "mgemm_nested", "mgemm_mxfp8", "mx_scales_blocked", "mx_blocked_bytes", "kgemm_mxfp8", "mx_scales_blocked_k", "mx_blocked_k_bytes", "mgemm_swiglu", "mgemm_swiglu_dgrad", "kgemm", "device_status", "shutdown", "set_wait_timeout_ns",
+__all__ = ["load", "mgemm", "mgemm_nested", "mgemm_mxfp8", "mx_scales_blocked", "mx_blocked_bytes", "kgemm_mxfp8", "mx_scales_blocked_k", "mx_blocked_k_bytes", "mgemm_swiglu", "mgemm_swiglu_dgrad", "kgemm", "kgemm_workspace_bytes", "device_status", "shutdown", "set_wait_timeout_ns",
            "selftest_wait_timeout", "RGError", "lib_path", "version",
            "RG_DEV_BAD_OFFSETS", "RG_DEV_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -46,7 +46,7 @@ RG_MAX_EXPERTS = 1024
 RG_MAX_OUTER = 65536
 RG_KGEMM_MAX_EXPERTS = 1024
 
-EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_nested", "rg_mgemm_mxfp8", "rg_mx_scales_blocked", "rg_mx_blocked_bytes", "rg_kgemm_mxfp8", "rg_mx_scales_blocked_k", "rg_mx_blocked_k_bytes", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_get_device_status", "rg_shutdown", "rg_set_wait_timeout_ns",
+EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_nested", "rg_mgemm_mxfp8", "rg_mx_scales_blocked", "rg_mx_blocked_bytes", "rg_kgemm_mxfp8", "rg_mx_scales_blocked_k", "rg_mx_blocked_k_bytes", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_kgemm_workspace_bytes", "rg_kgemm_ws", "rg_get_device_status", "rg_shutdown", "rg_set_wait_timeout_ns",
                     "rg_selftest_wait_timeout", "rg_last_cuda_error", "rg_device_supported",
                     "rg_version")
 
@@ -104,6 +104,10 @@ def load() -> ctypes.CDLL:
     lib.rg_kgemm.restype = i32
     lib.rg_kgemm_acc.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, vp]
     lib.rg_kgemm_acc.restype = i32
+    lib.rg_kgemm_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.rg_kgemm_workspace_bytes.restype = i64
+    lib.rg_kgemm_ws.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, i32, vp, i64, vp]
+    lib.rg_kgemm_ws.restype = i32
     lib.rg_get_device_status.argtypes = [vp]
     lib.rg_get_device_status.restype = i32
     lib.rg_shutdown.argtypes = []
@@ -135,6 +139,17 @@ def _stream_ptr(device, stream=None):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_device(t, name):
+    """A contiguous CUDA tensor of any type and shape (raw device memory)."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
 
 
 def _need(t, name, dtype, ndim):
@@ -429,10 +444,21 @@ def mgemm_swiglu_dgrad(dy, w2, offsets, y13, out=None, stream=None):
     return dy13
 
 
-def kgemm(grad, X, offsets, out=None, stream=None, accumulate: bool = False):
+def kgemm_workspace_bytes(E: int, N: int, K: int) -> int:
+    """Bytes of the device workspace ``kgemm(..., workspace=)`` needs."""
+    n = load().rg_kgemm_workspace_bytes(int(E), int(N), int(K))
+    if n < 0:
+        raise ValueError("bad E, N or K")
+    return int(n)
+
+
+def kgemm(grad, X, offsets, out=None, stream=None, accumulate: bool = False, workspace=None):
     """K-grouped weight gradient.  grad [M,N] bf16, X [M,K] bf16, offsets
     int32 [E+1]; returns dW [E,N,K] fp32, overwritten -- or, with
-    ``accumulate=True``, added to the given ``out`` (e.g. an FP32 main grad)."""
+    ``accumulate=True``, added to the given ``out`` (e.g. an FP32 main grad).
+    With ``workspace`` (a device tensor of at least kgemm_workspace_bytes
+    bytes) the call runs rg_kgemm_ws: the same results, each row of a long
+    expert read from DRAM once."""
     import torch
     _need(grad, "grad", torch.bfloat16, 2)
     _need(X, "X", torch.bfloat16, 2)
@@ -451,6 +477,14 @@ def kgemm(grad, X, offsets, out=None, stream=None, accumulate: bool = False):
         if tuple(out.shape) != (E, N, K):
             raise ValueError(f"out must be [{E},{N},{K}]")
     lib = load()
+    if workspace is not None:
+        _need_device(workspace, "workspace")
+        nbytes = workspace.numel() * workspace.element_size()
+        with torch.cuda.device(grad.device):
+            rc = lib.rg_kgemm_ws(grad.data_ptr(), X.data_ptr(), offsets.data_ptr(), E, M, N, K, out.data_ptr(),
+                                 int(bool(accumulate)), workspace.data_ptr(), nbytes, _stream_ptr(grad.device, stream))
+        _check("rg_kgemm_ws", rc)
+        return out
     fn = lib.rg_kgemm_acc if accumulate else lib.rg_kgemm
     with torch.cuda.device(grad.device):
         rc = fn(grad.data_ptr(), X.data_ptr(), offsets.data_ptr(), E, M, N, K,

@@ -215,6 +215,7 @@ rg::GroupArgs group_args(const DeviceState* ds, const int32_t* offsets, int E, i
   a.outer = 1;
   a.kg_wide = 0;
   a.mg_wide_b = 0;
+  a.flags = nullptr;
   return a;
 }
 
@@ -538,8 +539,16 @@ int rg_kgemm_mxfp8(const void* gq, const void* sg_blocked, const void* xq, const
 }  // extern "C"
 
 namespace {
+// Bytes of chunk-mode flags: one int per (expert, dW tile, CTA of the pair).
+int64_t kgemm_flag_bytes(int E, int N, int K) {
+  return static_cast<int64_t>(E) * ((N + rg::kg::TILE_M - 1) / rg::kg::TILE_M) * ((K + rg::kg::BN - 1) / rg::kg::BN) *
+         rg::kCtaGroup * static_cast<int64_t>(sizeof(int));
+}
+
+// flags: null (tile mode) or device memory of kgemm_flag_bytes(E, N, K) bytes that the
+// call zeroes on `stream` before the kernel (chunk mode).
 int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,
-               float* dW, int accumulate, cudaStream_t stream) {
+               float* dW, int accumulate, int* flags, cudaStream_t stream) {
   int rc = check_common(offsets, E, M, N, K);
   if (rc != RG_OK) return rc;
   if (dW == nullptr || !aligned16(dW)) return RG_ERR_INVALID_ARG;
@@ -594,6 +603,11 @@ int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, i
   rg::GroupArgs args = group_args(ds, offsets, E, M, N, K, dW);
   args.accumulate = accumulate;
   args.kg_wide = wide ? 1 : 0;
+  if (flags != nullptr) {
+    cudaError_t e = cudaMemsetAsync(flags, 0, static_cast<size_t>(kgemm_flag_bytes(E, N, K)), stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    args.flags = flags;
+  }
   const cudaError_t e = rg::launch_kgemm(tmG, tmX, tmD, args, ds->kg_grid, ds->max_smem, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
@@ -605,12 +619,25 @@ extern "C" {
 
 int rg_kgemm(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,
              float* dW, cudaStream_t stream) {
-  return kgemm_impl(grad, X, offsets, E, M, N, K, dW, 0, stream);
+  return kgemm_impl(grad, X, offsets, E, M, N, K, dW, 0, nullptr, stream);
 }
 
 int rg_kgemm_acc(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N,
                  int K, float* dW, cudaStream_t stream) {
-  return kgemm_impl(grad, X, offsets, E, M, N, K, dW, 1, stream);
+  return kgemm_impl(grad, X, offsets, E, M, N, K, dW, 1, nullptr, stream);
+}
+
+int64_t rg_kgemm_workspace_bytes(int E, int N, int K) {
+  if (E < 1 || E > RG_KGEMM_MAX_EXPERTS || N < 1 || K < 1) return -1;
+  return kgemm_flag_bytes(E, N, K);
+}
+
+int rg_kgemm_ws(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,
+                float* dW, int accumulate, void* workspace, int64_t workspace_bytes, cudaStream_t stream) {
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0) return RG_ERR_INVALID_ARG;
+  const int64_t need = rg_kgemm_workspace_bytes(E, N, K);
+  if (need < 0 || workspace_bytes < need) return RG_ERR_INVALID_ARG;
+  return kgemm_impl(grad, X, offsets, E, M, N, K, dW, accumulate != 0, static_cast<int*>(workspace), stream);
 }
 
 int rg_get_device_status(cudaStream_t stream) {

@@ -29,6 +29,8 @@ struct GroupArgs {
   int mg_wide_b;            // Mgemm with transpose_B: 1 = the w map is 4-D {64 cols, K, column
                             // block, group} and one copy loads both 64-column boxes of a CTA's
                             // atom (N a multiple of 64); 0 = 3-D {N, K, group}, one copy per box
+  int* flags;               // Kgemm chunk mode: zeroed device flags, one per (expert, tile, CTA
+                            // of the pair); null = tile mode
 };
 
 // Arguments of the MXFP8 Mgemm besides its tensor maps.

@@ -75,8 +75,8 @@ struct Cfg {
   // warps 2..9: epilogue
   static constexpr int PRODUCER2 = 2 + EPI_WARPS;
   static constexpr int THREADS = 32 * (PRODUCER2 + 1);
-  // full[S], empty[S], tfull[2], tempty[2], drain
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  // full[S], empty[S], tfull[2], tempty[2], drain, published
+  static constexpr int NUM_BARS = 2 * STAGES + 6;
   // The dynamic shared-memory window of a CTA without static shared memory
   // starts 1024-byte aligned; the kernel checks this instead of padding.
   static constexpr int SMEM_FIXED = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 +
@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
   int* misc = reinterpret_cast<int*>(ilog + 1);  // [0] tmem base, [1] abort
   int* s_off = misc + 4;                                   // [E+1] offsets
   int* s_ord = s_off + (args.E + 1);                       // [E] experts by decreasing rows
+  int* s_up = s_ord + args.E;                              // [E+1] chunk mode: first item of each
 
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -118,6 +119,9 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  // chunk mode: every epilogue warp's writes of a chunk that a later chunk
+  // of the same tile adds to have completed
+  const uint32_t pub_bar = bar0 + 8u * (2 * STAGES + 5);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -143,7 +147,8 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.status, kDevBadOffsets);
     return;
   }
-  if (worker >= T) return;
+  const bool chunked = args.flags != nullptr;
+  if (!chunked && worker >= T) return;  // (chunk mode: once its item count is known)
 
   // ---- experts ordered by decreasing row count (stable) ---------------------
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -154,6 +159,37 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
       rank_e += (cf > ce) | ((cf == ce) & (f < e));
     }
     s_ord[rank_e] = e;
+  }
+  // Work items.  Tile mode (no flags): item i is tile i of the list, with all
+  // of its row chunks.  Chunk mode (args.flags): item i is one row chunk of
+  // one tile; each expert's items run chunk by chunk (chunk 0 of all its
+  // tiles, then chunk 1, ...), so that the tiles of an expert too long for
+  // one chunk read each chunk of its rows from DRAM once, in the same round
+  // of the grid; a chunk's reduce-add into dW waits for the previous chunk's
+  // writes (a flag per tile half), so the chunks are still added in row order.
+  auto nchunks = [&](int e) { return max(1, (s_off[e + 1] - s_off[e] + CHUNK_ROWS - 1) / CHUNK_ROWS); };
+  if (chunked) {
+    __syncthreads();  // s_ord complete
+    if (warp == 0) {  // s_up[p] = items of the experts before position p of the order (warp scan)
+      const int per = (E + 31) / 32;
+      const int lo = min(E, lane * per), hi = min(E, lo + per);
+      int sum = 0;
+      for (int p = lo; p < hi; ++p) sum += nchunks(s_ord[p]) * tpe;
+      int incl = sum;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      int run = incl - sum;
+      for (int p = lo; p < hi; ++p) {
+        s_up[p] = run;
+        run += nchunks(s_ord[p]) * tpe;
+      }
+      if (lane == 31) s_up[E] = incl;
+    }
+    __syncthreads();
+    if (worker >= s_up[E]) return;  // same decision in both CTAs of a pair
   }
 
   // ---- barriers and tensor memory -------------------------------------------
@@ -167,6 +203,7 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
       mbar_init(tempty_bar(b), C::EPI_WARPS * CG);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(pub_bar, C::EPI_WARPS);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -198,10 +235,30 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
   };
   auto nblk = [&](int e, int local) { return kmajor(e) ? local % nbn : local / nbk; };
   auto kblk = [&](int e, int local) { return kmajor(e) ? local / nbn : local % nbk; };
-  auto tile_at = [&](int t, int& e, int& local) {
-    const int pe = t / tpe;
-    e = s_ord[pe];
-    local = t - pe * tpe;
+  // Item i: expert e, its tile `local`, chunks [c0, c1) of nch.  `pe` is the
+  // caller's position in the expert order, advanced as i grows.
+  struct Item {
+    int e, local, c0, c1, nch;
+  };
+  const int NI = chunked ? s_up[E] : T;
+  auto item_at = [&](int i, int& pe) {
+    Item it;
+    if (chunked) {
+      while (s_up[pe + 1] <= i) ++pe;
+      const int j = i - s_up[pe];
+      it.e = s_ord[pe];
+      it.c0 = j / tpe;
+      it.c1 = it.c0 + 1;
+      it.local = j - it.c0 * tpe;
+    } else {
+      pe = i / tpe;
+      it.e = s_ord[pe];
+      it.local = i - pe * tpe;
+      it.c0 = 0;
+      it.c1 = nchunks(it.e);
+    }
+    it.nch = nchunks(it.e);
+    return it;
   };
   if (warp == 0 || warp == C::PRODUCER2) {
     // ============ TMA producers (lane 0 of warp 0 and of the last warp) =====
@@ -219,13 +276,15 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
       uint32_t phase = 0;
       const uint32_t full_issuer = CG == 2 ? mapa_shared(full_bar(0), 0) : full_bar(0);
       bool ok = true;
-      for (int t = worker; t < T && ok; t += nworkers) {
-        int e, local;
-        tile_at(t, e, local);
-        const int n0 = nblk(e, local) * TILE_M + static_cast<int>(rank) * BM;
-        const int k0 = kblk(e, local) * BN + static_cast<int>(rank) * BN_CTA;
+      int pe = 0;
+      for (int i = worker; i < NI && ok; i += nworkers) {
+        const Item itm = item_at(i, pe);
+        const int e = itm.e;
+        const int n0 = nblk(e, itm.local) * TILE_M + static_cast<int>(rank) * BM;
+        const int k0 = kblk(e, itm.local) * BN + static_cast<int>(rank) * BN_CTA;
         const int r_begin = s_off[e], r_end = s_off[e + 1];
-        for (int r = r_begin; r < r_end; r += BR) {
+        const int rs = r_begin + itm.c0 * CHUNK_ROWS, re = min(r_end, r_begin + itm.c1 * CHUNK_ROWS);
+        for (int r = rs; r < re; r += BR) {
           if ((it++ & 1u) != pid) {  // the other producer's stage
             if (++stage == STAGES) {
               stage = 0;
@@ -292,14 +351,16 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     uint32_t phase = 0;
     int acc = 0;
     bool ok = true;
-    for (int t = worker; t < T && ok; t += nworkers) {
-      int e, local;
-      tile_at(t, e, local);
-      const int r_begin = s_off[e], r_end = s_off[e + 1];
+    int pe = 0;
+    for (int i = worker; i < NI && ok; i += nworkers) {
+      const Item itm = item_at(i, pe);
+      const int r_begin = s_off[itm.e], r_end = s_off[itm.e + 1];
       // zero tile (no rows): no MMA, no accumulator.  Otherwise one
       // accumulator per chunk of at most CHUNK_ROWS rows.
-      for (int cr = r_begin; cr < r_end && ok; cr += CHUNK_ROWS) {
+      for (int c = itm.c0; c < itm.c1 && ok; ++c) {
+        const int cr = r_begin + c * CHUNK_ROWS;
         const int c_end = min(r_end, cr + CHUNK_ROWS);
+        if (cr >= c_end) break;
         const int buf = acc & 1;
         const uint32_t tph = (acc >> 1) & 1;
         ok = __all_sync(0xffffffffu, wait_pair(tempty_bar(buf), tph ^ 1u));
@@ -350,13 +411,14 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     // CTA's half of the tile) and column half h (128 of the 256 columns).  It
     // pulls its whole 32x128 slice into registers with four back-to-back
     // tcgen05.ld, hands the accumulator back at once -- so the MMAs of the
-    // next-but-one tile never wait for the stores -- and then writes the four
-    // 32x32 fp32 boxes: registers -> swizzled staging buffer -> TMA store
-    // (whole 128-byte lines).  The first chunk of an expert's rows is stored
+    // next-but-one tile never wait for the stores -- and then writes the
+    // fp32 boxes: registers -> swizzled staging buffer -> TMA store (whole
+    // 128-byte lines).  The first chunk of an expert's rows is stored
     // (reduce-added when accumulating into dW), later chunks are TMA
-    // reduce-added; before a later chunk the warp waits
-    // until its previous writes have landed, so the adds are applied in chunk
-    // order (deterministic).
+    // reduce-added, in chunk order: in tile mode the warp waits until its
+    // previous writes have landed; in chunk mode, where the chunks of a tile
+    // run on different CTAs, it waits for the tile half's flag, which the CTA
+    // that wrote the previous chunk raises once all of its writes are in dW.
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
     uint8_t* ebuf = epi + (warp - 2) * EPI_BUF_BYTES;
@@ -372,7 +434,7 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     const uint64_t dw_policy = l2_policy_evict_first();
     int acc = 0;
     bool ok = true;
-    // Stage the boxes of one bulk group: the values of box b at v + 32 b
+    // Stage the boxes of one bulk group: the values of box b at v + BC b
     // (v = null: zeros) into slot b of this warp's buffer, after the previous
     // group has left the buffer; one proxy fence for all of them.
     auto stage_group = [&](const uint32_t* v, int nb) {
@@ -406,11 +468,13 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
       return bounds::inner_aligned(k, 4) && bounds::within(k, BC, K) && bounds::within(n, 32, N) &&
              bounds::index_ok(ee, E);
     };
-    for (int t = worker; t < T && ok; t += nworkers) {
-      int e, local;
-      tile_at(t, e, local);
-      const int n0 = nblk(e, local) * TILE_M + static_cast<int>(rank) * BM;
-      const int kh = kblk(e, local) * BN + h * (BN / 2);  // first dW column of this warp
+    int pe = 0;
+    uint32_t pub_par = 0;  // chunk mode, warp 2: parity of pub_bar's next phase
+    for (int i = worker; i < NI && ok; i += nworkers) {
+      const Item itm = item_at(i, pe);
+      const int e = itm.e;
+      const int n0 = nblk(e, itm.local) * TILE_M + static_cast<int>(rank) * BM;
+      const int kh = kblk(e, itm.local) * BN + h * (BN / 2);  // first dW column of this warp
       const int r_begin = s_off[e], r_end = s_off[e + 1];
       const bool warp_rows = n0 + q * 32 < N;  // this warp's 32 rows of dW exist
       if (r_end == r_begin) {  // expert without rows: dW tile = 0 (unchanged when accumulating)
@@ -428,8 +492,11 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         }
         continue;
       }
-      for (int cr = r_begin; cr < r_end; cr += CHUNK_ROWS) {
-        const bool first = cr == r_begin;
+      // chunk mode: this CTA's half of the tile is handed from chunk to chunk
+      // through its flag (the number of chunks whose writes are in dW)
+      int* flag = chunked ? args.flags + (static_cast<int64_t>(e) * tpe + itm.local) * CG + rank : nullptr;
+      for (int c = itm.c0; c < itm.c1 && ok; ++c) {
+        const bool first = c == 0;
         const bool overwrite = first && !args.accumulate;
         const int buf = acc & 1;
         const uint32_t tph = (acc >> 1) & 1;
@@ -439,32 +506,52 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
         tc_fence_after();
         if (!warp_rows) {
           release_acc(buf);
-          continue;
-        }
-        uint32_t v[BN / 2];
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + h * (BN / 2);
+        } else {
+          uint32_t v[BN / 2];
+          const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + h * (BN / 2);
 #pragma unroll
-        for (int c = 0; c < BN / 64; ++c)
-          tmem_ld_32x32b_x32(taddr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
-        tmem_ld_wait();
-        release_acc(buf);  // accumulator fully read: hand it back
-        if (!first && lane == 0) bulk_wait<0>();  // previous partial of this tile is in dW
-#pragma unroll
-        for (int c0 = 0; c0 < NBOX; c0 += GB) {
-          if (kh + BC * c0 >= K) break;
-          const int nb = group_boxes(kh, c0);
-          stage_group(v + BC * c0, nb);
-          if (lane == 0) {
-            for (int b = 0; b < nb; ++b) {
-              const int kb = kh + BC * (c0 + b);
-              if (!RG_BOUNDS_OK(dw_box_ok(kb, n0 + q * 32, e), args.status)) continue;
-              if (overwrite)
-                tma_store_3d_hint(&tmD, ebuf_s + b * BOXB, kb, n0 + q * 32, e, dw_policy);
-              else
-                tma_reduce_add_3d_hint(&tmD, ebuf_s + b * BOXB, kb, n0 + q * 32, e, dw_policy);
+          for (int b = 0; b < BN / 64; ++b)
+            tmem_ld_32x32b_x32(taddr + 32 * b, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * b));
+          tmem_ld_wait();
+          release_acc(buf);  // accumulator fully read: hand it back
+          if (!first) {  // the previous chunk of this tile half must be in dW
+            if (!chunked) {
+              if (lane == 0) bulk_wait<0>();
+            } else {
+              ok = __shfl_sync(0xffffffffu, lane == 0 ? (flag_wait_ge(guard, flag, c) ? 1 : 0) : 0, 0) != 0;
+              if (!ok) break;
             }
-            bulk_commit();
           }
+#pragma unroll
+          for (int c0 = 0; c0 < NBOX; c0 += GB) {
+            if (kh + BC * c0 >= K) break;
+            const int nb = group_boxes(kh, c0);
+            stage_group(v + BC * c0, nb);
+            if (lane == 0) {
+              for (int b = 0; b < nb; ++b) {
+                const int kb = kh + BC * (c0 + b);
+                if (!RG_BOUNDS_OK(dw_box_ok(kb, n0 + q * 32, e), args.status)) continue;
+                if (overwrite)
+                  tma_store_3d_hint(&tmD, ebuf_s + b * BOXB, kb, n0 + q * 32, e, dw_policy);
+                else
+                  tma_reduce_add_3d_hint(&tmD, ebuf_s + b * BOXB, kb, n0 + q * 32, e, dw_policy);
+              }
+              bulk_commit();
+            }
+          }
+        }
+        if (chunked && c + 1 < itm.nch) {  // a later chunk of this tile adds onto these writes
+          if (lane == 0) {
+            bulk_wait<0>();  // this warp's writes are complete
+            fence_proxy_async_global();
+            mbar_arrive(pub_bar);
+          }
+          if (warp == 2) {  // once all eight warps' writes are complete: publish
+            ok = __shfl_sync(0xffffffffu, lane == 0 ? (mbar_wait(guard, pub_bar, pub_par) ? 1 : 0) : 0, 0) != 0;
+            pub_par ^= 1u;
+            if (ok && lane == 0) flag_publish(flag, c + 1);
+          }
+          __syncwarp();
         }
       }
     }
@@ -491,20 +578,21 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
 }
 
 // Ring depth.  The shared-memory tables of the experts sit beside the ring:
-// a launch whose tables do not fit beside the deep ring (more than about 360
+// a launch whose tables do not fit beside the deep ring (more than 239
 // experts with CTA pairs) runs the same kernel with one stage fewer, which
 // leaves room for RG_MAX_EXPERTS_CFG experts.
 constexpr int kStagesDeep = kCtaGroup == 2 ? kg::STAGES : 2;
 constexpr int kStagesShallow =
-    Cfg<kCtaGroup, kStagesDeep>::SMEM_FIXED + (2 * RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 ? kStagesDeep
+    Cfg<kCtaGroup, kStagesDeep>::SMEM_FIXED + (3 * RG_MAX_EXPERTS_CFG + 2) * 4 <= 232448 ? kStagesDeep
                                                                                          : kStagesDeep - 1;
 static_assert(kStagesShallow >= 2, "the shallow ring keeps two stages");
-static_assert(Cfg<kCtaGroup, kStagesShallow>::SMEM_FIXED + (2 * RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448,
+static_assert(Cfg<kCtaGroup, kStagesShallow>::SMEM_FIXED + (3 * RG_MAX_EXPERTS_CFG + 2) * 4 <= 232448,
               "the expert tables of RG_MAX_EXPERTS_CFG experts must fit beside the shallow ring");
 
+// Ring and barriers, then offsets [E+1], order [E] and (chunk mode) item prefix [E+1].
 template <int ST>
 size_t smem_bytes(int E) {
-  return Cfg<kCtaGroup, ST>::SMEM_FIXED + (2 * static_cast<size_t>(E) + 1) * 4;
+  return Cfg<kCtaGroup, ST>::SMEM_FIXED + (3 * static_cast<size_t>(E) + 2) * 4;
 }
 
 // The deep ring when the expert tables fit beside it in `max_smem` bytes.

@@ -457,6 +457,41 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's global-memory accesses through the async proxy (TMA
+// stores, reduce-adds) with its accesses through the generic proxy.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Hand-over flags between CTAs (the K-grouped GEMM's chunk mode): a flag in
+// global memory counts the chunks whose writes are complete.  publish raises
+// it with release semantics at GPU scope; flag_wait_ge polls it with acquire
+// semantics, bounded like every other wait (running out sets kDevTimeout and
+// the CTA's abort flag), then orders the caller's later async-proxy accesses
+// after what it saw.
+__device__ __forceinline__ void flag_publish(int* flag, int value) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(flag), "r"(value) : "memory");
+}
+
+__device__ __forceinline__ bool flag_wait_ge(const WaitGuard& g, const int* flag, int target) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v >= target) {
+      fence_proxy_async_global();
+      return true;
+    }
+    __nanosleep(100);
+    if (*g.abort) return false;
+    if (globaltimer_ns() - t0 > g.limit_ns) {
+      atomicOr(g.status, kDevTimeout);
+      *g.abort = 1;
+      return false;
+    }
+  }
+}
+
 // ----------------------------------------------------------------- tcgen05
 
 // Tensor-memory allocation.  With CG == 2 one warp of each CTA of the pair

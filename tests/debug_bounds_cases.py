@@ -92,6 +92,10 @@ def main(lib_path):
         rg.kgemm(to_dev(g), to_dev(xx), kdoff, out=init, accumulate=True)
         status(f"kgemm_acc N={N} K={K}")
         np.testing.assert_array_equal(init.cpu().numpy().astype(np.float64), oracle.kgemm(g, xx, koff) + 1.0)
+        ws = torch.empty(rg.kgemm_workspace_bytes(len(kcounts), N, K), dtype=torch.uint8, device="cuda")
+        dW2 = rg.kgemm(to_dev(g), to_dev(xx), kdoff, workspace=ws)
+        status(f"kgemm_ws N={N} K={K}")
+        assert torch.equal(dW2.view(torch.int32), dW.view(torch.int32))
     # MXFP8: forward, input gradient and weight gradient
     mcounts = [128, 0, 32, 96, 160]
     moff = W.offsets_from_counts(mcounts)

@@ -110,6 +110,22 @@ def test_other_entry_points_validate(lib):
     assert lib.rg_selftest_wait_timeout(0, None, None) == rg.RG_ERR_INVALID_ARG
 
 
+def test_kgemm_workspace_entry_points_validate(lib):
+    # one 4-byte flag per expert, 256 x 256 dW tile and CTA of the pair
+    assert lib.rg_kgemm_workspace_bytes(4, 128, 256) == 4 * 1 * 1 * 2 * 4
+    assert lib.rg_kgemm_workspace_bytes(128, 2560, 3072) == 128 * 10 * 12 * 2 * 4
+    assert lib.rg_kgemm_workspace_bytes(1024, 257, 1) == 1024 * 2 * 1 * 2 * 4
+    for bad in ((0, 128, 128), (1025, 128, 128), (4, 0, 128), (4, 128, 0)):
+        assert lib.rg_kgemm_workspace_bytes(*bad) == -1
+    need = lib.rg_kgemm_workspace_bytes(4, 128, 256)
+    args = (DEV, DEV, DEV, 4, 512, 128, 256, DEV, 0)
+    assert lib.rg_kgemm_ws(*args, None, need, None) == rg.RG_ERR_INVALID_ARG       # no workspace
+    assert lib.rg_kgemm_ws(*args, ctypes.c_void_p(0x10002), need, None) == rg.RG_ERR_INVALID_ARG  # misaligned
+    assert lib.rg_kgemm_ws(*args, DEV, need - 4, None) == rg.RG_ERR_INVALID_ARG    # too small
+    bad_e = (DEV, DEV, DEV, 0, 512, 128, 256, DEV, 0)
+    assert lib.rg_kgemm_ws(*bad_e, DEV, 1 << 20, None) == rg.RG_ERR_INVALID_ARG
+
+
 def test_status_and_shutdown_without_a_device(lib):
     """rg_get_device_status returns the bits (>= 0) or a negative error: with
     no device it is an error, never bits; rg_shutdown releases nothing and

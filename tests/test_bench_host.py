@@ -134,3 +134,25 @@ def test_every_workload_maps_to_kernels_and_bytes(name):
         assert bench.algorithmic_bytes(op, wl.counts) > 0
     assert bench.working_set_bytes(wl) > 0
     assert bench.workload_desc(wl).startswith(wl.name + ":")
+
+
+@pytest.mark.parametrize("name", ["a3b", "skewed", "a3b_acc", "a3b_swiglu", "lora_a3b"])
+def test_step_buffers_have_the_outputs_types(name):
+    """Output buffers of every op as bench.py makes them (on the host here):
+    fp32 dW [E, N, K] for the weight gradients, bf16 elsewhere; a flag
+    workspace only for weight gradients of workloads with an expert longer
+    than one accumulation chunk."""
+    torch = pytest.importorskip("torch")
+    import moe_grouped_gemm_device_gb300 as rg
+    wl = W.ALL[name]()
+    outs, scratch = bench.make_buffers(wl, rg, "cpu")
+    long_expert = int(np.max(wl.counts)) > bench.KGEMM_CHUNK_ROWS
+    for op in wl.ops:
+        out = outs[op.name]
+        if op.kind == "kgemm":
+            assert out.dtype == torch.float32 and tuple(out.shape) == (wl.E, op.N, op.K)
+            assert (op.name + ":ws" in scratch) == long_expert
+            if long_expert:
+                assert scratch[op.name + ":ws"].numel() == rg.kgemm_workspace_bytes(wl.E, op.N, op.K)
+        else:
+            assert out.dtype == torch.bfloat16

@@ -334,10 +334,10 @@ def test_bounded_wait_times_out_with_status(gpu_lib):
     assert float(a.sum()) == 4.0
 
 
-@pytest.mark.parametrize("E", [360, 361, 1024], ids=["deep-ring-limit", "shallow-ring", "max"])
+@pytest.mark.parametrize("E", [239, 240, 1024], ids=["deep-ring-limit", "shallow-ring", "max"])
 def test_kgemm_most_experts(gpu_lib, E):
-    """Many experts, most of them tiny or empty, against the oracle: 360 is
-    the most whose tables fit beside the four-stage ring, 361 runs the
+    """Many experts, most of them tiny or empty, against the oracle: 239 is
+    the most whose tables fit beside the four-stage ring, 240 runs the
     three-stage ring, 1024 is RG_KGEMM_MAX_EXPERTS."""
     assert gpu_lib.RG_KGEMM_MAX_EXPERTS == 1024
     rng = np.random.default_rng(77)
