@@ -45,6 +45,8 @@ extern "C" {
 #define RG_ERR_INVALID_ARG (-1) /* null/misaligned pointer, bad size or stride */
 #define RG_ERR_UNSUPPORTED (-2) /* device is not an sm_103 (GB300-class) GPU */
 #define RG_ERR_CUDA (-3)        /* a CUDA call failed; see rg_last_cuda_error() */
+#define RG_ERR_SCRATCH (-4)     /* rg_kgemm_noalloc: the problem needs more than the library's
+                                   fixed scratch holds (RG_KGEMM_NOALLOC_MAX_FLAGS) */
 
 /* Bits of the device status word (rg_get_device_status). */
 #define RG_DEV_BAD_OFFSETS 0x1u /* offsets[0] != 0, decreasing, or offsets[E] > M */
@@ -61,6 +63,8 @@ extern "C" {
 #define RG_KGEMM_MAX_EXPERTS 1024
 /* Largest number of outer groups of rg_mgemm_nested. */
 #define RG_MAX_OUTER 65536
+/* Hand-over flags in the fixed scratch of rg_kgemm_noalloc (4 bytes each). */
+#define RG_KGEMM_NOALLOC_MAX_FLAGS 65536
 
 /*
  * rg_mgemm -- M-grouped GEMM, forward (transpose_B == 0) or input gradient
@@ -355,6 +359,38 @@ int64_t rg_kgemm_workspace_bytes(int E, int N, int K);
  */
 int rg_kgemm_ws(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,
                 float* dW, int accumulate, void* workspace, int64_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * rg_kgemm_noalloc -- rg_kgemm_ws for callers that cannot allocate device
+ * memory.  Nothing in the paper corresponds to it; it exists for this
+ * library's users.  Some callers have no way to call cudaMalloc, or must not:
+ * a framework or serving runtime that has handed all device memory to its own
+ * pool (a cudaMalloc there fails or fragments the pool), a plugin running
+ * inside another system that offers it no allocator, a runtime that forbids
+ * allocation once it has started.  Such a caller cannot provide
+ * rg_kgemm_ws's workspace, so this entry point takes the hand-over flags from
+ * a fixed array in the library's device memory: RG_KGEMM_NOALLOC_MAX_FLAGS
+ * 4-byte flags (256 KB), held on every GPU that loads the library until the
+ * process exits.  It allocates nothing, on the device or the host.
+ *
+ *   grad, X, offsets, E, M, N, K, dW, accumulate, stream  as for rg_kgemm_ws.
+ *
+ * Results are those of rg_kgemm_ws (and so of rg_kgemm / rg_kgemm_acc).
+ * The call zeroes the flags the problem uses on `stream`, then launches the
+ * kernel.  Every call on a device shares that one array: two calls whose
+ * work overlaps on the GPU (other streams, or graphs replayed concurrently)
+ * race on it and may give wrong results or report RG_DEV_TIMEOUT; calls
+ * ordered on one stream are safe.  The first call on a device looks up the
+ * array's device address (that device must be current, as for every entry
+ * point); make that first call before capturing stream work, as with every
+ * other first call on a device.
+ * Returns RG_ERR_SCRATCH if the problem needs more flags than the array
+ * holds, that is if rg_kgemm_workspace_bytes(E, N, K) exceeds
+ * 4 * RG_KGEMM_NOALLOC_MAX_FLAGS (for example E = 128, N = 2560, K = 3072
+ * needs 30720 flags); otherwise as rg_kgemm_ws.
+ */
+int rg_kgemm_noalloc(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,
+                     float* dW, int accumulate, cudaStream_t stream);
 
 /*
  * rg_get_device_status -- after the work already queued on `stream`, read

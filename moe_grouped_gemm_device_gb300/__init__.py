@@ -38,6 +38,8 @@ RG_OK = 0
 RG_ERR_INVALID_ARG = -1
 RG_ERR_UNSUPPORTED = -2
 RG_ERR_CUDA = -3
+RG_ERR_SCRATCH = -4
+RG_KGEMM_NOALLOC_MAX_FLAGS = 65536
 RG_DEV_BAD_OFFSETS = 0x1
 RG_DEV_TIMEOUT = 0x2
 RG_DEV_LAUNCH_CONFIG = 0x4
@@ -46,11 +48,12 @@ RG_MAX_EXPERTS = 1024
 RG_MAX_OUTER = 65536
 RG_KGEMM_MAX_EXPERTS = 1024
 
-EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_nested", "rg_mgemm_mxfp8", "rg_mx_scales_blocked", "rg_mx_blocked_bytes", "rg_kgemm_mxfp8", "rg_mx_scales_blocked_k", "rg_mx_blocked_k_bytes", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_kgemm_workspace_bytes", "rg_kgemm_ws", "rg_get_device_status", "rg_shutdown", "rg_set_wait_timeout_ns",
+EXPORTED_SYMBOLS = ("rg_mgemm", "rg_mgemm_nested", "rg_mgemm_mxfp8", "rg_mx_scales_blocked", "rg_mx_blocked_bytes", "rg_kgemm_mxfp8", "rg_mx_scales_blocked_k", "rg_mx_blocked_k_bytes", "rg_mgemm_swiglu", "rg_mgemm_swiglu_dgrad", "rg_kgemm", "rg_kgemm_acc", "rg_kgemm_workspace_bytes", "rg_kgemm_ws", "rg_kgemm_noalloc", "rg_get_device_status", "rg_shutdown", "rg_set_wait_timeout_ns",
                     "rg_selftest_wait_timeout", "rg_last_cuda_error", "rg_device_supported",
                     "rg_version")
 
-_ERRNAMES = {RG_ERR_INVALID_ARG: "RG_ERR_INVALID_ARG", RG_ERR_UNSUPPORTED: "RG_ERR_UNSUPPORTED",
+_ERRNAMES = {RG_ERR_SCRATCH: "RG_ERR_SCRATCH", RG_ERR_INVALID_ARG: "RG_ERR_INVALID_ARG",
+             RG_ERR_UNSUPPORTED: "RG_ERR_UNSUPPORTED",
              RG_ERR_CUDA: "RG_ERR_CUDA"}
 
 _lib = None
@@ -108,6 +111,8 @@ def load() -> ctypes.CDLL:
     lib.rg_kgemm_workspace_bytes.restype = i64
     lib.rg_kgemm_ws.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, i32, vp, i64, vp]
     lib.rg_kgemm_ws.restype = i32
+    lib.rg_kgemm_noalloc.argtypes = [vp, vp, vp, i32, i64, i32, i32, vp, i32, vp]
+    lib.rg_kgemm_noalloc.restype = i32
     lib.rg_get_device_status.argtypes = [vp]
     lib.rg_get_device_status.restype = i32
     lib.rg_shutdown.argtypes = []

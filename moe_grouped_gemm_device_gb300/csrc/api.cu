@@ -25,6 +25,13 @@ __device__ unsigned int g_status_word;    // bits set by the GEMM and conversion
 __device__ unsigned int g_selftest_word;  // bits set by the wait self-test
 __device__ unsigned int g_status_taken;   // last value taken from a status word, read by the host
 
+// Hand-over flags of rg_kgemm_noalloc: the scratch of the chunk-mode Kgemm
+// for callers that cannot allocate, held by every GPU that loads the library
+// until the process exits.  Host code must not pass this name to a kernel
+// (on the host it is a stand-in, not a device address): its device address
+// is looked up once per device in device_state() and kept in DeviceState.
+static __device__ __align__(256) int g_kgemm_noalloc_flags[RG_KGEMM_NOALLOC_MAX_FLAGS];
+
 // Read a status word and clear it in one atomic step, on the caller's stream.
 __global__ void take_status_kernel(unsigned int* word, unsigned int* taken) { *taken = atomicExch(word, 0u); }
 
@@ -45,6 +52,7 @@ struct DeviceState {
   unsigned int* status = nullptr;    // &g_status_word on this device
   unsigned int* selftest = nullptr;  // &g_selftest_word
   unsigned int* taken = nullptr;     // &g_status_taken
+  int* noalloc_flags = nullptr;      // &g_kgemm_noalloc_flags on this device
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -96,6 +104,10 @@ int device_state(DeviceState** out) {
       ds.selftest = static_cast<unsigned int*>(p);
       if ((e = cudaGetSymbolAddress(&p, g_status_taken)) != cudaSuccess) return fail_cuda(e);
       ds.taken = static_cast<unsigned int*>(p);
+      int* flags = nullptr;
+      if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&flags), g_kgemm_noalloc_flags)) != cudaSuccess)
+        return fail_cuda(e);
+      ds.noalloc_flags = flags;
       if ((e = rg::mgemm_setup(smem)) != cudaSuccess) return fail_cuda(e);
       if ((e = rg::kgemm_setup(smem)) != cudaSuccess) return fail_cuda(e);
       if ((e = rg::mx_setup(smem)) != cudaSuccess) return fail_cuda(e);
@@ -630,6 +642,19 @@ int rg_kgemm_acc(const void* grad, const void* X, const int32_t* offsets, int E,
 int64_t rg_kgemm_workspace_bytes(int E, int N, int K) {
   if (E < 1 || E > RG_KGEMM_MAX_EXPERTS || N < 1 || K < 1) return -1;
   return kgemm_flag_bytes(E, N, K);
+}
+
+int rg_kgemm_noalloc(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,
+                     float* dW, int accumulate, cudaStream_t stream) {
+  const int64_t need = rg_kgemm_workspace_bytes(E, N, K);
+  if (need < 0) return RG_ERR_INVALID_ARG;
+  if (need > static_cast<int64_t>(sizeof(g_kgemm_noalloc_flags))) return RG_ERR_SCRATCH;
+  DeviceState* ds = nullptr;
+  const int rc = device_state(&ds);
+  if (rc != RG_OK) return rc;
+  // kgemm_impl zeroes the flags the problem uses (cudaMemsetAsync on
+  // `stream`) before it launches the kernel; nothing is allocated
+  return kgemm_impl(grad, X, offsets, E, M, N, K, dW, accumulate != 0, ds->noalloc_flags, stream);
 }
 
 int rg_kgemm_ws(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,

@@ -126,6 +126,15 @@ def test_kgemm_workspace_entry_points_validate(lib):
     assert lib.rg_kgemm_ws(*bad_e, DEV, 1 << 20, None) == rg.RG_ERR_INVALID_ARG
 
 
+def test_kgemm_noalloc_rejects_problems_beyond_its_scratch(lib):
+    # 1024 experts of 32 x 32 dW tiles need 2M flags, more than the fixed
+    # scratch holds: refused before any device work
+    assert lib.rg_kgemm_workspace_bytes(1024, 8192, 8192) > 4 * rg.RG_KGEMM_NOALLOC_MAX_FLAGS
+    rc = lib.rg_kgemm_noalloc(DEV, DEV, DEV, 1024, 512, 8192, 8192, DEV, 0, None)
+    assert rc == rg.RG_ERR_SCRATCH
+    assert lib.rg_kgemm_noalloc(DEV, DEV, DEV, 0, 512, 128, 128, DEV, 0, None) == rg.RG_ERR_INVALID_ARG
+
+
 def test_status_and_shutdown_without_a_device(lib):
     """rg_get_device_status returns the bits (>= 0) or a negative error: with
     no device it is an error, never bits; rg_shutdown releases nothing and

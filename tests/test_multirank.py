@@ -33,7 +33,7 @@ def _rank(rank, world, port, times, out):
 def test_two_ranks_report_the_slowest_rank_and_the_job_total():
     world, times = 2, [3.0, 5.0]
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_rank, args=(world, port, times, out), nprocs=world, start_method="spawn")
         res = dict(out)
