@@ -337,12 +337,13 @@ int64_t rg_kgemm_workspace_bytes(int E, int N, int K);
 
 /*
  * rg_kgemm_ws -- rg_kgemm (accumulate == 0) or rg_kgemm_acc (accumulate != 0)
- * with a schedule that reads each row of a long expert from DRAM once.  An
- * expert of more than one accumulation chunk (4032 rows) has all of its dW
- * tiles work on one chunk of its rows in the same round of the persistent
- * grid, instead of each tile walking all of the expert's rows; when the
- * expert's rows exceed the L2 cache, rg_kgemm reads them again for each
- * round its tiles span.  The chunks of a tile then run on different CTAs,
+ * with a schedule that reads each row of a long expert from DRAM once.  When
+ * an expert has more dW tiles (256 x 256) than the GPU runs at once and is
+ * longer than one accumulation chunk (4032 rows), rg_kgemm's tiles span
+ * several rounds of the persistent grid and, once the expert's rows exceed
+ * the L2 cache, read them again in each round.  Here all of its tiles work on
+ * one chunk of its rows in the same round instead.  (Otherwise the schedule
+ * is rg_kgemm's.)  The chunks of a tile then run on different CTAs,
  * and each chunk's fp32 reduce-add into dW waits for the previous chunk's
  * writes through a flag in `workspace`, so the chunks are still added in row
  * order: results are bit-identical to rg_kgemm's / rg_kgemm_acc's.
@@ -350,9 +351,13 @@ int64_t rg_kgemm_workspace_bytes(int E, int N, int K);
  *
  *   grad, X, offsets, E, M, N, K, dW  as for rg_kgemm.
  *   workspace        device memory owned by the caller, 4-byte aligned, at
- *                    least rg_kgemm_workspace_bytes(E, N, K) bytes; the call
- *                    zeroes those bytes on `stream` before the kernel.  Two
- *                    calls that may run at the same time need two workspaces.
+ *                    least rg_kgemm_workspace_bytes(E, N, K) bytes.  When
+ *                    an expert has more dW tiles than the grid has CTA
+ *                    pairs (half the SMs: 76 on a GB300), the call zeroes
+ *                    those bytes on `stream` before the kernel; otherwise
+ *                    the kernel cannot take the chunk-major schedule and
+ *                    the workspace is not touched.  Two calls that may run
+ *                    at the same time need two workspaces.
  *   workspace_bytes  its size.
  * Returns RG_ERR_INVALID_ARG for a null, misaligned or too small workspace,
  * otherwise as rg_kgemm.
@@ -376,8 +381,8 @@ int rg_kgemm_ws(const void* grad, const void* X, const int32_t* offsets, int E, 
  *   grad, X, offsets, E, M, N, K, dW, accumulate, stream  as for rg_kgemm_ws.
  *
  * Results are those of rg_kgemm_ws (and so of rg_kgemm / rg_kgemm_acc).
- * The call zeroes the flags the problem uses on `stream`, then launches the
- * kernel.  Every call on a device shares that one array: two calls whose
+ * The call zeroes the flags the problem uses on `stream` (where the kernel
+ * may use them, as for rg_kgemm_ws's workspace), then launches the kernel.  Every call on a device shares that one array: two calls whose
  * work overlaps on the GPU (other streams, or graphs replayed concurrently)
  * race on it and may give wrong results or report RG_DEV_TIMEOUT; calls
  * ordered on one stream are safe.  The first call on a device looks up the

@@ -558,7 +558,9 @@ int64_t kgemm_flag_bytes(int E, int N, int K) {
 }
 
 // flags: null (tile mode) or device memory of kgemm_flag_bytes(E, N, K) bytes that the
-// call zeroes on `stream` before the kernel (chunk mode).
+// call zeroes on `stream` before the kernel (chunk mode) -- when the shape has more
+// tiles per expert than the grid has CTA pairs; otherwise the kernel cannot take the
+// chunk-major schedule, and the flags are neither cleared nor passed.
 int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, int64_t M, int N, int K,
                float* dW, int accumulate, int* flags, cudaStream_t stream) {
   int rc = check_common(offsets, E, M, N, K);
@@ -615,7 +617,8 @@ int kgemm_impl(const void* grad, const void* X, const int32_t* offsets, int E, i
   rg::GroupArgs args = group_args(ds, offsets, E, M, N, K, dW);
   args.accumulate = accumulate;
   args.kg_wide = wide ? 1 : 0;
-  if (flags != nullptr) {
+  const int64_t tiles_per_expert = kgemm_flag_bytes(1, N, K) / (rg::kCtaGroup * static_cast<int64_t>(sizeof(int)));
+  if (flags != nullptr && tiles_per_expert > ds->kg_grid / rg::kCtaGroup) {
     cudaError_t e = cudaMemsetAsync(flags, 0, static_cast<size_t>(kgemm_flag_bytes(E, N, K)), stream);
     if (e != cudaSuccess) return fail_cuda(e);
     args.flags = flags;
@@ -653,7 +656,8 @@ int rg_kgemm_noalloc(const void* grad, const void* X, const int32_t* offsets, in
   const int rc = device_state(&ds);
   if (rc != RG_OK) return rc;
   // kgemm_impl zeroes the flags the problem uses (cudaMemsetAsync on
-  // `stream`) before it launches the kernel; nothing is allocated
+  // `stream`) before it launches the kernel, where the kernel may use them;
+  // nothing is allocated
   return kgemm_impl(grad, X, offsets, E, M, N, K, dW, accumulate != 0, ds->noalloc_flags, stream);
 }
 

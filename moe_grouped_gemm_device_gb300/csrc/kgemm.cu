@@ -147,7 +147,17 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.status, kDevBadOffsets);
     return;
   }
-  const bool chunked = args.flags != nullptr;
+  // Chunk mode changes the schedule only where an expert's tiles outnumber
+  // the workers (they then run in more than one round) and some expert is
+  // longer than one chunk; otherwise all of an expert's tiles walk its rows
+  // together in one round, which reads them once, and the tile list is used.
+  // (The first two conditions are the same in every CTA.)
+  bool chunked = args.flags != nullptr && tpe > nworkers;
+  if (chunked) {
+    int longest = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) longest |= (s_off[e + 1] - s_off[e]) > CHUNK_ROWS;
+    chunked = __syncthreads_or(longest);
+  }
   if (!chunked && worker >= T) return;  // (chunk mode: once its item count is known)
 
   // ---- experts ordered by decreasing row count (stable) ---------------------

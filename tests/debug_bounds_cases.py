@@ -96,6 +96,20 @@ def main(lib_path):
         dW2 = rg.kgemm(to_dev(g), to_dev(xx), kdoff, workspace=ws)
         status(f"kgemm_ws N={N} K={K}")
         assert torch.equal(dW2.view(torch.int32), dW.view(torch.int32))
+    # K-grouped, chunk-major schedule (more dW tiles per expert than CTA pairs)
+    for N, K in [(2560, 2304), (2248, 2120)]:
+        M = int(koff[-1]) + 5
+        g, xx = ints((M, N), 9, 0), ints((M, K), 9, 1)
+        dW = rg.kgemm(to_dev(g), to_dev(xx), kdoff)
+        status(f"kgemm N={N} K={K}")
+        ws = torch.empty(rg.kgemm_workspace_bytes(len(kcounts), N, K), dtype=torch.uint8, device="cuda")
+        dW2 = rg.kgemm(to_dev(g), to_dev(xx), kdoff, workspace=ws)
+        status(f"kgemm_ws N={N} K={K}")
+        assert torch.equal(dW2.view(torch.int32), dW.view(torch.int32))
+        es = np.array([0, 0, 3, 4, 4, 4, 5], np.int32)
+        ns = np.array([0, N - 1, 7, 0, 1000, N - 1, 33], np.int32)
+        got = dW2[torch.from_numpy(es).long().cuda(), torch.from_numpy(ns).long().cuda()].cpu().numpy()
+        np.testing.assert_array_equal(got.astype(np.float64), oracle.kgemm(g, xx, koff, sel=(es, ns)))
     # MXFP8: forward, input gradient and weight gradient
     mcounts = [128, 0, 32, 96, 160]
     moff = W.offsets_from_counts(mcounts)

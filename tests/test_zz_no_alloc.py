@@ -21,9 +21,14 @@ pytestmark = pytest.mark.gpu
 def test_noalloc_matches_the_workspace_entry_point_twice(gpu_lib):
     import torch
     lib = gpu_lib.load()
-    counts = [9000, 0, 37, 4100, 8192, 4033, 1]  # experts of several accumulation chunks
+    # Experts of several accumulation chunks and 90 dW tiles each (more than
+    # the grid's CTA pairs), so that the kernel takes the chunk-major
+    # schedule and hands tiles over through the flags in the fixed scratch.
+    counts = [9000, 0, 37, 4100, 8192, 4033, 1]
     off = W.offsets_from_counts(counts)
-    E, M, N, K = len(counts), int(off[-1]) + 5, 512, 384
+    E, M, N, K = len(counts), int(off[-1]) + 5, 2560, 2304
+    assert (N // 256) * (K // 256) > torch.cuda.get_device_properties(0).multi_processor_count // 2
+    assert gpu_lib.kgemm_workspace_bytes(E, N, K) <= 4 * gpu_lib.RG_KGEMM_NOALLOC_MAX_FLAGS
     g = to_dev(W.normal_bf16((M, N), 1.0, 91, 0))
     x = to_dev(W.normal_bf16((M, K), 1.0, 91, 1))
     od = offsets_dev(off)
