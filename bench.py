@@ -51,11 +51,24 @@ KERNEL_OF = {"mgemm": "mgemm_kernel<false>", "mgemm_t": "mgemm_kernel<true>", "k
              "swiglu": "mgemm_kernel<false,swiglu>", "swiglu_bwd": "mgemm_kernel<true,swiglu_bwd>",
              "mx": "mx_mgemm_kernel<false>", "mx_t": "mx_mgemm_kernel<true>", "mx_blocked": "mx_blocked_kernel",
              "mxk": "mx_kgemm_kernel", "mx_blocked_k": "mx_blocked_k_kernel"}
-KERNEL_SOURCES = {"mgemm_kernel<false>": "mgemm.cu", "mgemm_kernel<true>": "mgemm.cu",
-                  "mgemm_kernel<false,swiglu>": "mgemm.cu", "mgemm_kernel<true,swiglu_bwd>": "mgemm.cu",
-                  "kgemm_kernel": "kgemm.cu", "mx_mgemm_kernel<false>": "mxgemm.cu",
-                  "mx_mgemm_kernel<true>": "mxgemm.cu", "mx_blocked_kernel": "mxgemm.cu",
-                  "mx_kgemm_kernel": "mxgemm.cu", "mx_blocked_k_kernel": "mxgemm.cu"}
+# The sources a kernel's behaviour depends on: its translation unit and the
+# package headers it includes.  A traffic record holds their hash.
+_COMMON = ("ptx.cuh", "internal.h", "bounds.cuh")
+_MG, _KG, _MX = ("mgemm.cu",) + _COMMON, ("kgemm.cu", "kgemm_plan.cuh") + _COMMON, ("mxgemm.cu",) + _COMMON
+KERNEL_SOURCES = {"mgemm_kernel<false>": _MG, "mgemm_kernel<true>": _MG, "mgemm_kernel<false,swiglu>": _MG,
+                  "mgemm_kernel<true,swiglu_bwd>": _MG, "kgemm_kernel": _KG, "mx_mgemm_kernel<false>": _MX,
+                  "mx_mgemm_kernel<true>": _MX, "mx_blocked_kernel": _MX, "mx_kgemm_kernel": _MX,
+                  "mx_blocked_k_kernel": _MX}
+
+
+def source_hash(kernel: str, root: str = None) -> str:
+    """First 16 hex digits of the SHA-256 of the kernel's sources, in order."""
+    csrc = os.path.join(root or ROOT, "moe_grouped_gemm_device_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 FP8_KERNELS = ("mx_mgemm_kernel<false>", "mx_mgemm_kernel<true>", "mx_kgemm_kernel")
 CONVERSION_KERNELS = ("mx_blocked_kernel", "mx_blocked_k_kernel")
 
@@ -365,8 +378,7 @@ def traffic_for(kernel: str, op_names, workload: str):
     ent = json.load(open(path)).get(kernel)
     if not ent:
         return None
-    src = os.path.join(ROOT, "moe_grouped_gemm_device_gb300", "csrc", KERNEL_SOURCES[kernel])
-    if ent.get("source_sha256_16") != hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]:
+    if ent.get("source_sha256_16") != source_hash(kernel):
         return None
     per_op = ent.get("workloads", {}).get(workload, {})
     if not op_names or any(o not in per_op for o in op_names):

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "librg.so")
 SOURCES = ["api.cu", "mgemm.cu", "kgemm.cu", "mxgemm.cu", "selftest.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("ptx.cuh", "internal.h", "bounds.cuh")] + [os.path.join(INCLUDE, "rg.h")]
+HEADERS = [os.path.join(CSRC, h) for h in ("ptx.cuh", "internal.h", "bounds.cuh", "kgemm_plan.cuh")] + [os.path.join(INCLUDE, "rg.h")]
 # The debug-bounds build: every copy and store coordinate the kernels compute
 # is checked against its operand; a failed check sets RG_DEV_BOUNDS and the
 # access is skipped.  Built on request into its own directory.

@@ -21,10 +21,12 @@
 // exercise them, including boxes that break each rule.
 #pragma once
 
+#ifndef RG_HD
 #if defined(__CUDACC__)
 #define RG_HD __host__ __device__ __forceinline__
 #else
 #define RG_HD inline
+#endif
 #endif
 
 namespace rg {

@@ -106,6 +106,11 @@ constexpr int BK = 64;
 #ifndef RG_KG_LOAD_HINT
 #define RG_KG_LOAD_HINT 1
 #endif
+// Experts of fewer rows than this are light in the K-grouped schedule: their
+// tiles are interleaved with the row blocks of the longer experts' tiles.
+#ifndef RG_KG_LIGHT_ROWS
+#define RG_KG_LIGHT_ROWS 512
+#endif
 namespace kg {
 constexpr int BM = 128;                  // dW rows per CTA
 constexpr int TILE_M = BM * kCtaGroup;   // dW rows per tile
@@ -123,6 +128,8 @@ static_assert(EPI_GROUP == 1 || EPI_GROUP == 2 || EPI_GROUP == 4, "1, 2 or 4 dW 
 // whole stages, at most 4096 rows.  Bounds the length of each fp32
 // accumulation chain inside the tensor cores.
 constexpr int CHUNK_ROWS = 4096 / BR * BR;
+constexpr int LIGHT_ROWS = RG_KG_LIGHT_ROWS;
+static_assert(LIGHT_ROWS >= 1 && LIGHT_ROWS <= CHUNK_ROWS, "a light expert has rows, and fewer than one chunk");
 }  // namespace kg
 
 // Sleep between polls of the accumulator barrier by the epilogue of the

@@ -48,6 +48,7 @@
 
 #include "bounds.cuh"
 #include "internal.h"
+#include "kgemm_plan.cuh"
 #include "ptx.cuh"
 #include "rg.h"
 
@@ -85,6 +86,7 @@ struct Cfg {
 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int CHUNK_ROWS = kg::CHUNK_ROWS;
+constexpr int LIGHT_ROWS = kg::LIGHT_ROWS;
 // An expert whose operand rows take more than half of the 126 MB L2 cannot
 // keep them there between two rounds of its tiles.
 constexpr long long kKmajorBytes = 64ll << 20;
@@ -177,14 +179,14 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
   // one chunk read each chunk of its rows from DRAM once, in the same round
   // of the grid; a chunk's reduce-add into dW waits for the previous chunk's
   // writes (a flag per tile half), so the chunks are still added in row order.
-  auto nchunks = [&](int e) { return max(1, (s_off[e + 1] - s_off[e] + CHUNK_ROWS - 1) / CHUNK_ROWS); };
+  const kgplan::Tables tb{s_off, s_ord, s_up, E, tpe, chunked, CHUNK_ROWS};
   if (chunked) {
     __syncthreads();  // s_ord complete
     if (warp == 0) {  // s_up[p] = items of the experts before position p of the order (warp scan)
       const int per = (E + 31) / 32;
       const int lo = min(E, lane * per), hi = min(E, lo + per);
       int sum = 0;
-      for (int p = lo; p < hi; ++p) sum += nchunks(s_ord[p]) * tpe;
+      for (int p = lo; p < hi; ++p) sum += tb.nchunks(s_ord[p]) * tpe;
       int incl = sum;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
       int run = incl - sum;
       for (int p = lo; p < hi; ++p) {
         s_up[p] = run;
-        run += nchunks(s_ord[p]) * tpe;
+        run += tb.nchunks(s_ord[p]) * tpe;
       }
       if (lane == 31) s_up[E] = incl;
     }
@@ -245,31 +247,12 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
   };
   auto nblk = [&](int e, int local) { return kmajor(e) ? local % nbn : local / nbk; };
   auto kblk = [&](int e, int local) { return kmajor(e) ? local / nbn : local % nbk; };
-  // Item i: expert e, its tile `local`, chunks [c0, c1) of nch.  `pe` is the
-  // caller's position in the expert order, advanced as i grows.
-  struct Item {
-    int e, local, c0, c1, nch;
-  };
-  const int NI = chunked ? s_up[E] : T;
-  auto item_at = [&](int i, int& pe) {
-    Item it;
-    if (chunked) {
-      while (s_up[pe + 1] <= i) ++pe;
-      const int j = i - s_up[pe];
-      it.e = s_ord[pe];
-      it.c0 = j / tpe;
-      it.c1 = it.c0 + 1;
-      it.local = j - it.c0 * tpe;
-    } else {
-      pe = i / tpe;
-      it.e = s_ord[pe];
-      it.local = i - pe * tpe;
-      it.c0 = 0;
-      it.c1 = nchunks(it.e);
-    }
-    it.nch = nchunks(it.e);
-    return it;
-  };
+  // The worker's issue order: heavy items' row blocks with the light items
+  // interleaved (kgemm_plan.cuh).
+  using kgplan::Acc;
+  using kgplan::Item;
+  const kgplan::Plan plan = kgplan::make_plan(tb, worker, nworkers, BR, LIGHT_ROWS);
+  auto walk = [&](auto&& on_segment, auto&& on_zero) { return kgplan::walk(tb, plan, on_segment, on_zero); };
   if (warp == 0 || warp == C::PRODUCER2) {
     // ============ TMA producers (lane 0 of warp 0 and of the last warp) =====
     // One thread issuing every copy caps the copy rate of a CTA below what
@@ -285,129 +268,124 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       const uint32_t full_issuer = CG == 2 ? mapa_shared(full_bar(0), 0) : full_bar(0);
-      bool ok = true;
-      int pe = 0;
-      for (int i = worker; i < NI && ok; i += nworkers) {
-        const Item itm = item_at(i, pe);
-        const int e = itm.e;
-        const int n0 = nblk(e, itm.local) * TILE_M + static_cast<int>(rank) * BM;
-        const int k0 = kblk(e, itm.local) * BN + static_cast<int>(rank) * BN_CTA;
-        const int r_begin = s_off[e], r_end = s_off[e + 1];
-        const int rs = r_begin + itm.c0 * CHUNK_ROWS, re = min(r_end, r_begin + itm.c1 * CHUNK_ROWS);
-        for (int r = rs; r < re; r += BR) {
-          if ((it++ & 1u) != pid) {  // the other producer's stage
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
+      int e = -1, local = -1, n0 = 0, k0 = 0, r_begin = 0, r_end = 0;  // the item of the last copy
+      walk(
+          [&](const Item& itm, int, int, int, int r0, int r1, Acc, bool, bool) {
+            if (itm.e != e || itm.local != local) {
+              e = itm.e;
+              local = itm.local;
+              n0 = nblk(e, local) * TILE_M + static_cast<int>(rank) * BM;
+              k0 = kblk(e, local) * BN + static_cast<int>(rank) * BN_CTA;
+              r_begin = s_off[e];
+              r_end = s_off[e + 1];
             }
-            continue;
-          }
-          if (!wait_pair(empty_bar(stage), phase ^ 1u)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          // i0 < 0 for the expert's ragged last block: its leading -i0 rows
-          // are zero-filled and its last rows are r .. r_end-1.
-          const int i0 = min(0, r_end - r - BR);
-          const uint32_t fb = full_issuer + 8u * stage;
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES * CG);
-          // (debug-bounds build: every in-range row of the box must be a row
-          // of expert e; a refused copy's bytes are counted as arrived)
-          const bool rows_ok = !RG_DEBUG_BOUNDS || bounds::kgemm_rows(r, i0, BR, r_begin, r_end);
-          if (args.kg_wide) {  // one copy per operand: column blocks n0/64 .. and k0/64 ..
-            if (RG_BOUNDS_OK(rows_ok && n0 % 64 == 0, args.status)) {
-              if constexpr (RG_KG_LOAD_HINT && CG == 2) tma_load_4d_pair_hint(sa, &tmG, fb, 0, i0, n0 / 64, r, op_policy);
-              else tma_load_4d_cg<CG>(sa, &tmG, fb, 0, i0, n0 / 64, r);
-            } else {
-              mbar_complete_tx_cluster(fb, A_BYTES);
+            for (int r = r0; r < r1; r += BR) {
+              if ((it++ & 1u) != pid) {  // the other producer's stage
+                if (++stage == STAGES) {
+                  stage = 0;
+                  phase ^= 1u;
+                }
+                continue;
+              }
+              // Everything about the copy is worked out before the wait: between
+              // the stage becoming free and its copy starting is the critical path.
+              const uint32_t sa = sbase + stage * STAGE_BYTES;
+              const uint32_t sb = sa + A_BYTES;
+              // i0 < 0 for the expert's ragged last block: its leading -i0 rows
+              // are zero-filled and its last rows are r .. r_end-1.
+              const int i0 = min(0, r_end - r - BR);
+              const uint32_t fb = full_issuer + 8u * stage;
+              // (debug-bounds build: every in-range row of the box must be a row
+              // of expert e; a refused copy's bytes are counted as arrived)
+              const bool rows_ok = !RG_DEBUG_BOUNDS || bounds::kgemm_rows(r, i0, BR, r_begin, r_end);
+              if (!wait_pair(empty_bar(stage), phase ^ 1u)) return false;
+              if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES * CG);
+              if (args.kg_wide) {  // one copy per operand: column blocks n0/64 .. and k0/64 ..
+                if (RG_BOUNDS_OK(rows_ok && n0 % 64 == 0, args.status)) {
+                  if constexpr (RG_KG_LOAD_HINT && CG == 2) tma_load_4d_pair_hint(sa, &tmG, fb, 0, i0, n0 / 64, r, op_policy);
+                  else tma_load_4d_cg<CG>(sa, &tmG, fb, 0, i0, n0 / 64, r);
+                } else {
+                  mbar_complete_tx_cluster(fb, A_BYTES);
+                }
+                if (RG_BOUNDS_OK(rows_ok && k0 % 64 == 0, args.status)) {
+                  if constexpr (RG_KG_LOAD_HINT && CG == 2) tma_load_4d_pair_hint(sb, &tmX, fb, 0, i0, k0 / 64, r, op_policy);
+                  else tma_load_4d_cg<CG>(sb, &tmX, fb, 0, i0, k0 / 64, r);
+                } else {
+                  mbar_complete_tx_cluster(fb, C::B_BYTES);
+                }
+              } else {
+    #pragma unroll
+                for (int j = 0; j < BM / 64; ++j) {
+                  if (RG_BOUNDS_OK(rows_ok && bounds::inner_aligned(n0 + 64 * j, 2), args.status))
+                    tma_load_3d_cg<CG>(sa + j * BOX_BYTES, &tmG, fb, n0 + 64 * j, i0, r);
+                  else
+                    mbar_complete_tx_cluster(fb, BOX_BYTES);
+                }
+    #pragma unroll
+                for (int j = 0; j < BN_CTA / 64; ++j) {
+                  if (RG_BOUNDS_OK(rows_ok && bounds::inner_aligned(k0 + 64 * j, 2), args.status))
+                    tma_load_3d_cg<CG>(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, i0, r);
+                  else
+                    mbar_complete_tx_cluster(fb, BOX_BYTES);
+                }
+              }
+              ilog->it[pid][stage] = static_cast<int>(it - 1);
+              ilog->bytes[pid][stage] = STAGE_BYTES;
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+              }
             }
-            if (RG_BOUNDS_OK(rows_ok && k0 % 64 == 0, args.status)) {
-              if constexpr (RG_KG_LOAD_HINT && CG == 2) tma_load_4d_pair_hint(sb, &tmX, fb, 0, i0, k0 / 64, r, op_policy);
-              else tma_load_4d_cg<CG>(sb, &tmX, fb, 0, i0, k0 / 64, r);
-            } else {
-              mbar_complete_tx_cluster(fb, C::B_BYTES);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < BM / 64; ++j) {
-              if (RG_BOUNDS_OK(rows_ok && bounds::inner_aligned(n0 + 64 * j, 2), args.status))
-                tma_load_3d_cg<CG>(sa + j * BOX_BYTES, &tmG, fb, n0 + 64 * j, i0, r);
-              else
-                mbar_complete_tx_cluster(fb, BOX_BYTES);
-            }
-#pragma unroll
-            for (int j = 0; j < BN_CTA / 64; ++j) {
-              if (RG_BOUNDS_OK(rows_ok && bounds::inner_aligned(k0 + 64 * j, 2), args.status))
-                tma_load_3d_cg<CG>(sb + j * BOX_BYTES, &tmX, fb, k0 + 64 * j, i0, r);
-              else
-                mbar_complete_tx_cluster(fb, BOX_BYTES);
-            }
-          }
-          ilog->it[pid][stage] = static_cast<int>(it - 1);
-          ilog->bytes[pid][stage] = STAGE_BYTES;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
+            return true;
+          },
+          [](const Item&) { return true; });
     }
   } else if (warp == 1 && rank == 0) {
     // ========================= MMA issuer (warp 1) ===========================
     constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN, true, true);
     int stage = 0;
     uint32_t phase = 0;
-    int acc = 0;
-    bool ok = true;
-    int pe = 0;
-    for (int i = worker; i < NI && ok; i += nworkers) {
-      const Item itm = item_at(i, pe);
-      const int r_begin = s_off[itm.e], r_end = s_off[itm.e + 1];
-      // zero tile (no rows): no MMA, no accumulator.  Otherwise one
-      // accumulator per chunk of at most CHUNK_ROWS rows.
-      for (int c = itm.c0; c < itm.c1 && ok; ++c) {
-        const int cr = r_begin + c * CHUNK_ROWS;
-        const int c_end = min(r_end, cr + CHUNK_ROWS);
-        if (cr >= c_end) break;
-        const int buf = acc & 1;
-        const uint32_t tph = (acc >> 1) & 1;
-        ok = __all_sync(0xffffffffu, wait_pair(tempty_bar(buf), tph ^ 1u));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + buf * BN;
-        for (int r = cr; r < c_end; r += BR) {
-          ok = __all_sync(0xffffffffu, wait_pair(full_bar(stage), phase));
-          if (!ok) break;
-          tc_fence_after();
-          if (lane == 0) {
+    // One accumulator per chunk of at most CHUNK_ROWS rows of an item; an
+    // item without rows has neither MMAs nor an accumulator.
+    const bool ok = walk(
+        [&](const Item&, int, int cs, int ce, int r0, int r1, Acc a, bool first, bool last) {
+          const uint32_t d_tmem = tmem + a.buf * BN;
+          if (first) {
+            if (!__all_sync(0xffffffffu, wait_pair(tempty_bar(a.buf), a.par ^ 1u))) return false;
+            tc_fence_after();
+          }
+          for (int r = r0; r < r1; r += BR) {
             // the expert's ragged last block starts with all-zero 16-row steps
-            const int k_first = max(0, r + BR - r_end) / 16;
+            // (a chunk that ends before the expert ends is whole row blocks)
+            const int k_first = max(0, r + BR - ce) / 16;
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_BYTES;
+            if (!__all_sync(0xffffffffu, wait_pair(full_bar(stage), phase))) return false;
+            tc_fence_after();
+            if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < BR / 16; ++k) {
-              if (k >= k_first) {
-                const uint64_t ad = sdesc_sw128(sa + 2048 * k, BOX_BYTES, 1024);
-                const uint64_t bd = sdesc_sw128(sb + 2048 * k, BOX_BYTES, 1024);
-                umma_bf16<CG>(d_tmem, ad, bd, IDESC, (r != cr) | (k != k_first));
+              for (int k = 0; k < BR / 16; ++k) {
+                if (k >= k_first) {
+                  const uint64_t ad = sdesc_sw128(sa + 2048 * k, BOX_BYTES, 1024);
+                  const uint64_t bd = sdesc_sw128(sb + 2048 * k, BOX_BYTES, 1024);
+                  umma_bf16<CG>(d_tmem, ad, bd, IDESC, (r != cs) | (k != k_first));
+                }
               }
+              umma_commit<CG>(empty_bar(stage));
             }
-            umma_commit<CG>(empty_bar(stage));
+            __syncwarp();
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          __syncwarp();
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          if (last) {
+            if (lane == 0) umma_commit<CG>(tfull_bar(a.buf));
+            __syncwarp();
           }
-        }
-        if (!ok) break;
-        if (lane == 0) umma_commit<CG>(tfull_bar(buf));
-        __syncwarp();
-        ++acc;
-      }
-    }
+          return true;
+        },
+        [](const Item&) { return true; });
     if (!ok && lane == 0) {  // wait for issued MMAs before tensor memory is freed
       umma_commit_local<CG>(drain_bar);
       mbar_wait_drain(drain_bar, 0);
@@ -442,8 +420,6 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     // dW is written once and never read here: first out of L2, so that the
     // operand rows other tiles of the expert still need stay resident
     const uint64_t dw_policy = l2_policy_evict_first();
-    int acc = 0;
-    bool ok = true;
     // Stage the boxes of one bulk group: the values of box b at v + BC b
     // (v = null: zeros) into slot b of this warp's buffer, after the previous
     // group has left the buffer; one proxy fence for all of them.
@@ -478,93 +454,91 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
       return bounds::inner_aligned(k, 4) && bounds::within(k, BC, K) && bounds::within(n, 32, N) &&
              bounds::index_ok(ee, E);
     };
-    int pe = 0;
     uint32_t pub_par = 0;  // chunk mode, warp 2: parity of pub_bar's next phase
-    for (int i = worker; i < NI && ok; i += nworkers) {
-      const Item itm = item_at(i, pe);
-      const int e = itm.e;
-      const int n0 = nblk(e, itm.local) * TILE_M + static_cast<int>(rank) * BM;
-      const int kh = kblk(e, itm.local) * BN + h * (BN / 2);  // first dW column of this warp
-      const int r_begin = s_off[e], r_end = s_off[e + 1];
-      const bool warp_rows = n0 + q * 32 < N;  // this warp's 32 rows of dW exist
-      if (r_end == r_begin) {  // expert without rows: dW tile = 0 (unchanged when accumulating)
-        if (!warp_rows || args.accumulate) continue;
-#pragma unroll 1
-        for (int c0 = 0; c0 < NBOX && kh + BC * c0 < K; c0 += GB) {
-          const int nb = group_boxes(kh, c0);
-          stage_group(nullptr, nb);
-          if (lane == 0) {
-            for (int b = 0; b < nb; ++b)
-              if (RG_BOUNDS_OK(dw_box_ok(kh + BC * (c0 + b), n0 + q * 32, e), args.status))
-                tma_store_3d(&tmD, ebuf_s + b * BOXB, kh + BC * (c0 + b), n0 + q * 32, e);
-            bulk_commit();
-          }
-        }
-        continue;
-      }
-      // chunk mode: this CTA's half of the tile is handed from chunk to chunk
-      // through its flag (the number of chunks whose writes are in dW)
-      int* flag = chunked ? args.flags + (static_cast<int64_t>(e) * tpe + itm.local) * CG + rank : nullptr;
-      for (int c = itm.c0; c < itm.c1 && ok; ++c) {
-        const bool first = c == 0;
-        const bool overwrite = first && !args.accumulate;
-        const int buf = acc & 1;
-        const uint32_t tph = (acc >> 1) & 1;
-        ++acc;
-        ok = warp_wait_acc<CG>(guard, tfull_bar(buf), tph);
-        if (!ok) break;
-        tc_fence_after();
-        if (!warp_rows) {
-          release_acc(buf);
-        } else {
-          uint32_t v[BN / 2];
-          const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + h * (BN / 2);
+    walk(  // the accumulators in the order they end
+        [&](const Item& itm, int c, int, int, int, int, Acc a, bool, bool last) {
+          if (!last) return true;
+          const int e = itm.e;
+          const int n0 = nblk(e, itm.local) * TILE_M + static_cast<int>(rank) * BM;
+          const int kh = kblk(e, itm.local) * BN + h * (BN / 2);  // first dW column of this warp
+          const bool warp_rows = n0 + q * 32 < N;  // this warp's 32 rows of dW exist
+          // chunk mode: this CTA's half of the tile is handed from chunk to
+          // chunk through its flag (the number of chunks whose writes are in dW)
+          int* flag = chunked ? args.flags + (static_cast<int64_t>(e) * tpe + itm.local) * CG + rank : nullptr;
+          const bool first = c == 0;
+          const bool overwrite = first && !args.accumulate;
+          if (!warp_wait_acc<CG>(guard, tfull_bar(a.buf), a.par)) return false;
+          tc_fence_after();
+          if (!warp_rows) {
+            release_acc(a.buf);
+          } else {
+            uint32_t v[BN / 2];
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + a.buf * BN + h * (BN / 2);
 #pragma unroll
-          for (int b = 0; b < BN / 64; ++b)
-            tmem_ld_32x32b_x32(taddr + 32 * b, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * b));
-          tmem_ld_wait();
-          release_acc(buf);  // accumulator fully read: hand it back
-          if (!first) {  // the previous chunk of this tile half must be in dW
-            if (!chunked) {
-              if (lane == 0) bulk_wait<0>();
-            } else {
-              ok = __shfl_sync(0xffffffffu, lane == 0 ? (flag_wait_ge(guard, flag, c) ? 1 : 0) : 0, 0) != 0;
-              if (!ok) break;
+            for (int b = 0; b < BN / 64; ++b)
+              tmem_ld_32x32b_x32(taddr + 32 * b, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * b));
+            tmem_ld_wait();
+            release_acc(a.buf);  // accumulator fully read: hand it back
+            if (!first) {  // the previous chunk of this tile half must be in dW
+              if (!chunked) {
+                if (lane == 0) bulk_wait<0>();
+              } else if (__shfl_sync(0xffffffffu, lane == 0 ? (flag_wait_ge(guard, flag, c) ? 1 : 0) : 0, 0) == 0) {
+                return false;
+              }
+            }
+#pragma unroll
+            for (int c0 = 0; c0 < NBOX; c0 += GB) {
+              if (kh + BC * c0 >= K) break;
+              const int nb = group_boxes(kh, c0);
+              stage_group(v + BC * c0, nb);
+              if (lane == 0) {
+                for (int b = 0; b < nb; ++b) {
+                  const int kb = kh + BC * (c0 + b);
+                  if (!RG_BOUNDS_OK(dw_box_ok(kb, n0 + q * 32, e), args.status)) continue;
+                  if (overwrite)
+                    tma_store_3d_hint(&tmD, ebuf_s + b * BOXB, kb, n0 + q * 32, e, dw_policy);
+                  else
+                    tma_reduce_add_3d_hint(&tmD, ebuf_s + b * BOXB, kb, n0 + q * 32, e, dw_policy);
+                }
+                bulk_commit();
+              }
             }
           }
-#pragma unroll
-          for (int c0 = 0; c0 < NBOX; c0 += GB) {
-            if (kh + BC * c0 >= K) break;
-            const int nb = group_boxes(kh, c0);
-            stage_group(v + BC * c0, nb);
+          if (chunked && c + 1 < itm.nch) {  // a later chunk of this tile adds onto these writes
             if (lane == 0) {
-              for (int b = 0; b < nb; ++b) {
-                const int kb = kh + BC * (c0 + b);
-                if (!RG_BOUNDS_OK(dw_box_ok(kb, n0 + q * 32, e), args.status)) continue;
-                if (overwrite)
-                  tma_store_3d_hint(&tmD, ebuf_s + b * BOXB, kb, n0 + q * 32, e, dw_policy);
-                else
-                  tma_reduce_add_3d_hint(&tmD, ebuf_s + b * BOXB, kb, n0 + q * 32, e, dw_policy);
-              }
+              bulk_wait<0>();  // this warp's writes are complete
+              fence_proxy_async_global();
+              mbar_arrive(pub_bar);
+            }
+            bool pub_ok = true;
+            if (warp == 2) {  // once all eight warps' writes are complete: publish
+              pub_ok = __shfl_sync(0xffffffffu, lane == 0 ? (mbar_wait(guard, pub_bar, pub_par) ? 1 : 0) : 0, 0) != 0;
+              pub_par ^= 1u;
+              if (pub_ok && lane == 0) flag_publish(flag, c + 1);
+            }
+            __syncwarp();
+            if (!pub_ok) return false;
+          }
+          return true;
+        },
+        [&](const Item& itm) {  // expert without rows: dW tile = 0 (unchanged when accumulating)
+          const int e = itm.e;
+          const int n0 = nblk(e, itm.local) * TILE_M + static_cast<int>(rank) * BM;
+          const int kh = kblk(e, itm.local) * BN + h * (BN / 2);
+          if (n0 + q * 32 >= N || args.accumulate) return true;
+#pragma unroll 1
+          for (int c0 = 0; c0 < NBOX && kh + BC * c0 < K; c0 += GB) {
+            const int nb = group_boxes(kh, c0);
+            stage_group(nullptr, nb);
+            if (lane == 0) {
+              for (int b = 0; b < nb; ++b)
+                if (RG_BOUNDS_OK(dw_box_ok(kh + BC * (c0 + b), n0 + q * 32, e), args.status))
+                  tma_store_3d(&tmD, ebuf_s + b * BOXB, kh + BC * (c0 + b), n0 + q * 32, e);
               bulk_commit();
             }
           }
-        }
-        if (chunked && c + 1 < itm.nch) {  // a later chunk of this tile adds onto these writes
-          if (lane == 0) {
-            bulk_wait<0>();  // this warp's writes are complete
-            fence_proxy_async_global();
-            mbar_arrive(pub_bar);
-          }
-          if (warp == 2) {  // once all eight warps' writes are complete: publish
-            ok = __shfl_sync(0xffffffffu, lane == 0 ? (mbar_wait(guard, pub_bar, pub_par) ? 1 : 0) : 0, 0) != 0;
-            pub_par ^= 1u;
-            if (ok && lane == 0) flag_publish(flag, c + 1);
-          }
-          __syncwarp();
-        }
-      }
-    }
+          return true;
+        });
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
   }

@@ -17,13 +17,16 @@ def fake_tree(tmp_path, source: bytes, entry: dict):
     csrc = tmp_path / "moe_grouped_gemm_device_gb300" / "csrc"
     csrc.mkdir(parents=True)
     (csrc / "kgemm.cu").write_bytes(source)
+    for h in bench.KERNEL_SOURCES["kgemm_kernel"][1:]:  # the headers, as in the package
+        (csrc / h).write_bytes(b"// header " + h.encode() + b"\n")
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"kgemm_kernel": entry}))
 
 
 def test_traffic_only_for_the_captured_source_and_workload(tmp_path, monkeypatch):
     src = b"// kernel source as captured\n"
-    h = hashlib.sha256(src).hexdigest()[:16]
+    h = hashlib.sha256(src + b"".join(b"// header " + n.encode() + b"\n"
+                                      for n in bench.KERNEL_SOURCES["kgemm_kernel"][1:])).hexdigest()[:16]
     fake_tree(tmp_path, src, {"source_sha256_16": h,
                               "workloads": {"a3b": {"wgrad_gw2": 700, "wgrad_gw13": 1300},
                                             "skewed": {"wgrad_gw13": 5000}}})
@@ -37,7 +40,13 @@ def test_traffic_only_for_the_captured_source_and_workload(tmp_path, monkeypatch
     assert bench.traffic_for("kgemm_kernel", [], "a3b") is None
     assert bench.traffic_for("mx_kgemm_kernel", ["wgrad_gw2"], "a3b") is None  # no entry
     # the kernel changed since the capture: no traffic figure
+    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw2"], "a3b") == 700
     (tmp_path / "moe_grouped_gemm_device_gb300" / "csrc" / "kgemm.cu").write_bytes(src + b"// edit\n")
+    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw2"], "a3b") is None
+    # or a header it includes changed
+    (tmp_path / "moe_grouped_gemm_device_gb300" / "csrc" / "kgemm.cu").write_bytes(src)
+    assert bench.traffic_for("kgemm_kernel", ["wgrad_gw2"], "a3b") == 700
+    (tmp_path / "moe_grouped_gemm_device_gb300" / "csrc" / "ptx.cuh").write_bytes(b"// edited\n")
     assert bench.traffic_for("kgemm_kernel", ["wgrad_gw2"], "a3b") is None
 
 
