@@ -55,8 +55,16 @@ constexpr int kCtaGroup = RG_CTA_PAIR ? 2 : 1;
 // epilogue's TMA boxes (32 rows x BOX_COLS columns; 16 columns use a 64-byte
 // swizzle, 32 a 128-byte one), one staging buffer per epilogue warp.
 // Compile-time switches for comparison builds.
+// dW columns per tile: 256 (one tensor-memory accumulator beside the scale
+// slots) or 128 (two accumulators, so the stores of one tile overlap the next
+// tile's MMAs; a comparison build: each stage then carries half the MMA work
+// for two thirds of the operand bytes, and the kernel is bound by operand
+// delivery, not by the stores)
+#ifndef RG_MXK_BN
+#define RG_MXK_BN 256
+#endif
 #ifndef RG_MXK_STAGES
-#define RG_MXK_STAGES 4
+#define RG_MXK_STAGES (RG_MXK_BN == 128 ? 6 : 4)
 #endif
 #ifndef RG_MXK_BOX_COLS
 #define RG_MXK_BOX_COLS 16
@@ -66,6 +74,8 @@ constexpr int kCtaGroup = RG_CTA_PAIR ? 2 : 1;
 #endif
 namespace mxk {
 constexpr int STAGES = RG_MXK_STAGES;
+constexpr int BN = RG_MXK_BN;
+static_assert(BN == 128 || BN == 256, "MXFP8 wgrad tiles are 128 or 256 dW columns wide");
 constexpr int BOX_COLS = RG_MXK_BOX_COLS;
 constexpr int EPI_GROUP = RG_MXK_EPI_GROUP;  // dW boxes staged and stored per bulk group
 static_assert(EPI_GROUP == 1 || EPI_GROUP == 2 || EPI_GROUP == 4, "1, 2 or 4 boxes per bulk group");

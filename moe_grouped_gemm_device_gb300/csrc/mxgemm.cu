@@ -605,24 +605,27 @@ __global__ void __launch_bounds__(kConvThreads) mx_blocked_k_kernel(const uint8_
 // (gq * 2^sg)^T (xq * 2^sx): FP8 E4M3 operands quantized along the rows
 // (one E8M0 scale per column and 32-row block), every expert's row range a
 // whole number of 32-row blocks.  Tile = 128 dW rows (n) x 256 dW columns (k)
-// of one expert, tcgen05 M=128 N=256 with both operands MN-major.  A stage is
-// 128 rows of the expert: the MMAs of the 32-row steps that lie inside the
-// expert are issued, so no row of the next expert enters an accumulation and
-// nothing needs zeroing.  Scales come from the layout for groups along the
+// of one expert (BN = 256; a comparison build takes BN = 128 with two
+// tensor-memory accumulators, since the scale slots leave no room for two
+// 256-column ones), tcgen05 M=128 N=BN with both operands MN-major.  A stage is 128 rows of the expert: the MMAs of the
+// 32-row steps that lie inside the expert are issued, so no row of the next
+// expert enters an accumulation and nothing needs zeroing.  Scales come from the layout for groups along the
 // contraction.  Tiles are taken longest expert first; rows are summed in
 // tensor memory in chunks of at most CHUNK_ROWS, the first chunk's partial
 // stored (or reduce-added when accumulating into dW), later ones TMA
 // reduce-added in row order.  Empty experts get dW[e] = 0 (unchanged when
 // accumulating).
 struct MxkCfg {
-  static constexpr int BM = 128;  // dW rows per tile (MMA M)
-  static constexpr int BN = 256;  // dW columns per tile (MMA N)
-  static constexpr int BR = 128;  // expert rows per stage (4 scale blocks)
+  static constexpr int BM = 128;        // dW rows per tile (MMA M)
+  static constexpr int BN = mxk::BN;    // dW columns per tile (MMA N)
+  static constexpr int XB = BN / 128;   // 128-column boxes of X (and scale chunks of X) per stage
+  static constexpr int ACC_BUFS = BN == 128 ? 2 : 1;  // accumulators in tensor memory
+  static constexpr int BR = 128;        // expert rows per stage (4 scale blocks)
   static constexpr int STAGES = mxk::STAGES;
   static constexpr int A_BYTES = BM * BR;
   static constexpr int B_BYTES = BN * BR;
   static constexpr int AB_BYTES = A_BYTES + B_BYTES;
-  static constexpr int SF_BYTES = 512 + 1024;
+  static constexpr int SF_BYTES = 512 + 512 * XB;
   static constexpr int STAGE_BYTES = AB_BYTES + SF_BYTES;
   static constexpr int CHUNK_STAGES = mxk::CHUNK_ROWS / BR;
   static constexpr int EPI_WARPS = 8;
@@ -633,12 +636,15 @@ struct MxkCfg {
   // warps 0 and 10: producers (alternate stages), 1: MMA, 2..9: epilogue
   static constexpr int PRODUCER2 = 2 + EPI_WARPS;
   static constexpr int THREADS = 32 * (PRODUCER2 + 1);
-  static constexpr int NUM_BARS = 2 * STAGES + 3;
+  // full[S], empty[S], tfull[ACC_BUFS], tempty[ACC_BUFS], drain
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
   static constexpr int SMEM_FIXED = STAGES * STAGE_BYTES + EPI_WARPS * EPI_BUF_BYTES + NUM_BARS * 8 +
                                     static_cast<int>(sizeof(IssueLog<STAGES>)) + 16;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t SF_COL0 = 256;
+  static constexpr uint32_t SF_COL0 = ACC_BUFS * BN;  // scale slots (16 columns per stage) after the accumulators
 };
+static_assert(MxkCfg::SF_COL0 + 16 * MxkCfg::STAGES <= MxkCfg::TMEM_COLS,
+              "accumulators and scale slots must fit in tensor memory");
 static_assert(MxkCfg::AB_BYTES % 1024 == 0 && MxkCfg::EPI_BUF_BYTES % (MxkCfg::BOX_COLS * 32) == 0,
               "operand tiles and epilogue boxes must keep their swizzle alignment");
 static_assert(MxkCfg::SMEM_FIXED + 3 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448,
@@ -670,9 +676,10 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES);
-  const uint32_t tempty_bar = bar0 + 8u * (2 * STAGES + 1);
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2);
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + C::ACC_BUFS + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * C::ACC_BUFS);
+  constexpr int XB = C::XB, ACC_BUFS = C::ACC_BUFS;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -732,8 +739,10 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    mbar_init(tfull_bar, 1);
-    mbar_init(tempty_bar, C::EPI_WARPS);
+    for (int b = 0; b < ACC_BUFS; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), C::EPI_WARPS);
+    }
     mbar_init(drain_bar, 1);
     fence_mbar_init();
   }
@@ -774,7 +783,8 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
         tile_at(t, e, nb, kb);
         const int r_begin = s_off[e], r_end = s_off[e + 1];
         const int n0 = nb * BM, k0 = kb * BN;
-        const int xb0 = 2 * kb, xb1 = min(2 * kb + 1, nrb_x - 1);  // past K: zero-filled rows, any scale
+        // X's 128-column scale blocks of this tile (past K: zero-filled rows, any scale)
+        const int xb0 = XB * kb, xb1 = min(XB * kb + XB - 1, nrb_x - 1);
         for (int r = r_begin, c = 0; r < r_end; r += BR, ++c) {
           if ((it++ & 1u) != pid) {  // the other producer's stage
             if (++stage == STAGES) {
@@ -795,8 +805,8 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
                                bounds::inner_aligned(k0, 1) && bounds::index_ok(k0, K),
                            args.status)) {
             tma_load_2d(sa_of(stage), &tmG, fb, n0, r);
-            tma_load_2d(sb_of(stage), &tmX, fb, k0, r);
-            tma_load_2d(sb_of(stage) + 16384, &tmX, fb, k0 + 128, r);
+#pragma unroll
+            for (int x = 0; x < XB; ++x) tma_load_2d(sb_of(stage) + 16384 * x, &tmX, fb, k0 + 128 * x, r);
           } else {
             mbar_complete_tx_cluster(fb, C::AB_BYTES);
           }
@@ -807,9 +817,9 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
                            args.status)) {
             bulk_load(sfa_of(stage), args.sfa + (static_cast<int64_t>(nb) * NQ + q) * 512, 512, fb);
             bulk_load(sfb_of(stage), args.sfb + (static_cast<int64_t>(xb0) * NQ + q) * 512, 512, fb);
-            bulk_load(sfb_of(stage) + 512, args.sfb + (static_cast<int64_t>(xb1) * NQ + q) * 512, 512, fb);
+            if (XB == 2) bulk_load(sfb_of(stage) + 512, args.sfb + (static_cast<int64_t>(xb1) * NQ + q) * 512, 512, fb);
           } else {
-            mbar_complete_tx_cluster(fb, 3 * 512);
+            mbar_complete_tx_cluster(fb, (1 + XB) * 512);
           }
           ilog->it[pid][stage] = static_cast<int>(it - 1);
           ilog->bytes[pid][stage] = C::STAGE_BYTES;
@@ -832,9 +842,12 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
       const int rows = s_off[e + 1] - s_off[e];
       const int nst = (rows + BR - 1) / BR;
       for (int c0 = 0; c0 < nst && ok; c0 += C::CHUNK_STAGES, ++acc) {
-        ok = __all_sync(0xffffffffu, mbar_wait(guard, tempty_bar, (acc & 1) ^ 1u));
+        const int buf = acc % ACC_BUFS;
+        const uint32_t tph = static_cast<uint32_t>(acc / ACC_BUFS) & 1u;
+        ok = __all_sync(0xffffffffu, mbar_wait(guard, tempty_bar(buf), tph ^ 1u));
         if (!ok) break;
         tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * BN;
         const int c1 = min(nst, c0 + C::CHUNK_STAGES);
         for (int c = c0; c < c1; ++c) {
           ok = __all_sync(0xffffffffu, mbar_wait(guard, full_bar(stage), phase));
@@ -844,14 +857,14 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
             const uint32_t sfa_t = tmem + C::SF_COL0 + 16u * stage;
             const uint32_t sfb_t = sfa_t + 4u;
             tmem_cp_32x128b_x4(sfa_t, sdesc_plain16(sfa_of(stage)));
-            tmem_cp_32x128b_x4(sfb_t, sdesc_plain16(sfb_of(stage)));
-            tmem_cp_32x128b_x4(sfb_t + 4u, sdesc_plain16(sfb_of(stage) + 512));
+#pragma unroll
+            for (int x = 0; x < XB; ++x) tmem_cp_32x128b_x4(sfb_t + 4u * x, sdesc_plain16(sfb_of(stage) + 512 * x));
             const int ksteps = min(4, (rows - BR * c) / 32);  // 32-row steps inside the expert
             const uint32_t sa = sa_of(stage), sb = sb_of(stage);
             for (int k = 0; k < ksteps; ++k) {
               const uint64_t ad = sdesc_sw128(sa + 4096 * k, 16384, 1024);
               const uint64_t bd = sdesc_sw128(sb + 4096 * k, 16384, 1024);
-              umma_mxf8(tmem, ad, bd, idesc_mxf8_f32(BM, BN, true, true, k), sfa_t, sfb_t,
+              umma_mxf8(d_tmem, ad, bd, idesc_mxf8_f32(BM, BN, true, true, k), sfa_t, sfb_t,
                         (c != c0) | (k != 0));
             }
             umma_commit<1>(empty_bar(stage));
@@ -863,7 +876,7 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
           }
         }
         if (!ok) break;
-        if (lane == 0) umma_commit<1>(tfull_bar);
+        if (lane == 0) umma_commit<1>(tfull_bar(buf));
         __syncwarp();
       }
     }
@@ -875,7 +888,7 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
   } else {
     // ======================= epilogue (warps 2..9) ===========================
     // Warp w owns TMEM lane quarter q = w % 4 (dW rows n0 + 32q ..) and
-    // column half h (128 of the 256 columns), stored as boxes of 32 rows x
+    // column half h (WC = BN / 2 columns), stored as boxes of 32 rows x
     // BOX_COLS fp32 through one staging buffer per warp.
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
@@ -888,8 +901,9 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
       tile_at(t, e, nb, kb);
       const int rows = s_off[e + 1] - s_off[e];
       const int nst = (rows + BR - 1) / BR;
+      constexpr int WC = BN / 2;  // dW columns of this warp
       const int n0 = nb * BM + 32 * q;
-      const int kc0 = kb * BN + 128 * h;
+      const int kc0 = kb * BN + WC * h;
       const bool mine = n0 < N && kc0 < K;  // this warp's boxes hold valid dW elements
       // a 32-row x BOX_COLS box of dW[e] at column k: inside dW, 16-byte aligned start
       auto dw_box_ok = [&](int k) {
@@ -906,7 +920,7 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            for (int b = 0; b < 128 / C::BOX_COLS && kc0 + C::BOX_COLS * b < K; ++b)
+            for (int b = 0; b < WC / C::BOX_COLS && kc0 + C::BOX_COLS * b < K; ++b)
               if (RG_BOUNDS_OK(dw_box_ok(kc0 + C::BOX_COLS * b), args.status))
                 tma_store_3d(&tmD, ebuf_s, kc0 + C::BOX_COLS * b, n0, e);
             bulk_commit();
@@ -915,21 +929,21 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
         continue;
       }
       for (int c0 = 0; c0 < nst; c0 += C::CHUNK_STAGES, ++acc) {
-        if (!__all_sync(0xffffffffu, mbar_wait(guard, tfull_bar, acc & 1))) {
+        const int buf = acc % ACC_BUFS;
+        if (!__all_sync(0xffffffffu, mbar_wait(guard, tfull_bar(buf), static_cast<uint32_t>(acc / ACC_BUFS) & 1u))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t v[128];
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + 128u * h;
-        tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tmem_ld_32x32b_x32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
-        tmem_ld_32x32b_x32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+        uint32_t v[WC];
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + WC * h;
+#pragma unroll
+        for (int b = 0; b < WC / 32; ++b)
+          tmem_ld_32x32b_x32(taddr + 32 * b, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * b));
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar);  // the accumulator is free again
+        if (lane == 0) mbar_arrive(tempty_bar(buf));  // the accumulator is free again
         if (!mine) continue;
         const bool reduce = args.accumulate || c0 > 0;
         // a later chunk is added onto the earlier chunk's writes: let them land first
@@ -941,7 +955,7 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
         // left the buffer, one proxy fence, their stores in one bulk group
         constexpr int GB = C::EPI_GROUP;
 #pragma unroll
-        for (int b0 = 0; b0 < 128 / BC; b0 += GB) {
+        for (int b0 = 0; b0 < WC / BC; b0 += GB) {
           if (kc0 + BC * b0 >= K) break;
           const int nb = min(GB, (K - kc0 - BC * b0 + BC - 1) / BC);
           if (lane == 0) bulk_wait_read<0>();

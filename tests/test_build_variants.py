@@ -1,7 +1,8 @@
-"""The single-CTA comparison build (RG_CTA_PAIR=0: tcgen05 MMAs of one CTA,
-M=128, instead of CTA pairs) keeps compiling: every translation unit of the
-library is compiled for sm_103a with that switch into a scratch directory.
-No GPU is needed (nvcc cross-compiles); skipped where nvcc is missing."""
+"""Comparison builds keep compiling: the single-CTA build (RG_CTA_PAIR=0:
+tcgen05 MMAs of one CTA, M=128, instead of CTA pairs; every translation unit
+of the library, compiled for sm_103a into a scratch directory) and the MXFP8
+weight gradient with 128-column tiles (RG_MXK_BN=128).  No GPU is needed
+(nvcc cross-compiles); skipped where nvcc is missing."""
 import os
 import shutil
 import subprocess
@@ -34,3 +35,13 @@ def test_single_cta_build_compiles(tmp_path):
     failed = [(s, err) for s, rc, err in results if rc != 0]
     assert not failed, failed
     shutil.rmtree(tmp_path, ignore_errors=True)
+
+
+@pytest.mark.skipif(_nvcc() is None, reason="nvcc not available")
+def test_mx_wgrad_128_column_build_compiles(tmp_path):
+    """The MXFP8 weight gradient's comparison build with 128-column tiles and
+    two tensor-memory accumulators (RG_MXK_BN=128)."""
+    cmd = [_nvcc(), *_build.ARCH, *_build.NVCC_FLAGS, "-DRG_MXK_BN=128", "-c",
+           os.path.join(_build.CSRC, "mxgemm.cu"), "-o", str(tmp_path / "mxgemm.o")]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
