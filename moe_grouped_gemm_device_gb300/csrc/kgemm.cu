@@ -9,7 +9,12 @@
 //     ceil(K/256).  Every CTA sorts the experts by decreasing row count (ties
 //     by index) in shared memory; worker w takes tiles w, w+W, ... of that
 //     list, so every round of W tiles has near-equal cost (longest-first list
-//     scheduling) -- without global scratch or host sync.
+//     scheduling) -- without global scratch or host sync.  A worker issues
+//     the tiles of its experts below LIGHT_ROWS rows (whose stores outlast
+//     their MMAs) one at a time between the row blocks of its other tiles,
+//     so that their stores overlap tensor-core work (kgemm_plan.cuh).  With a
+//     flag workspace (chunk mode) a long expert's tiles instead share each
+//     row chunk in one round, handing the partial sums on through flags.
 //   * The contraction is fed BR = 96 rows at a time, six MMA steps of 16
 //     rows per barrier round of the MMA warp, through a ring of four stages
 //     (48 KB per CTA each): three stages ahead of the tensor cores hide the
@@ -232,9 +237,6 @@ __global__ void __launch_bounds__(Cfg<CG, ST>::THREADS, 1)
     if constexpr (CG == 2) return mbar_wait_cl(guard, bar, par);
     else return mbar_wait(guard, bar, par);
   };
-  // Tile t of the list sorted by decreasing expert rows (longest first);
-  // worker w takes tiles w, w+W, ..., so every round of W tiles has
-  // near-equal cost.
   // (n block, k block) of an expert's tile.  The tiles of an expert run over
   // more than one round of the grid; if its operand rows overflow L2 between
   // rounds, the second round reads again the operand whose blocks the first
