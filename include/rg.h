@@ -25,11 +25,14 @@
  *     in a per-device status word read by rg_get_device_status().
  *   - No C++ exception crosses this interface.
  *   - Thread safety: calls may be made from several host threads, on one or
- *     several streams; calls on different streams are independent.
+ *     several streams; calls on different streams are independent (except
+ *     rg_kgemm_noalloc, whose calls share one fixed array: see there).
  *   - CUDA graphs: the first call on a device sets up the library's state for
  *     it (kernel attributes, grid sizes); every later call enqueues only
- *     kernel launches, so a sequence of calls may be captured in a CUDA graph
- *     and replayed with new contents in the same buffers.
+ *     kernel launches (rg_kgemm_ws also a memset of its workspace), so a
+ *     sequence of calls may be captured in a CUDA graph and replayed with new
+ *     contents in the same buffers.  This note does not cover
+ *     rg_kgemm_noalloc.
  */
 #ifndef RG_H_
 #define RG_H_
