@@ -143,6 +143,43 @@ def test_kgemm_several_rounds_bit_exact(gpu_lib):
     np.testing.assert_array_equal(dW.astype(np.float64), oracle.kgemm(g, x, off))
 
 
+@pytest.mark.parametrize("N,K,ws", [(1280, 1024, False), (2560, 2304, False), (2560, 2304, True)],
+                         ids=["20-tiles", "90-tiles", "90-tiles-chunk-major"])
+@pytest.mark.parametrize("accumulate", [False, True], ids=["overwrite", "accumulate"])
+def test_kgemm_light_and_heavy_experts_bit_exact(gpu_lib, N, K, ws, accumulate):
+    """Experts on both sides of the 512-row light/heavy threshold of the issue
+    order (511, 512, 513 rows) beside empty, one-row, ragged and multi-chunk
+    experts: light tiles run between the heavy tiles' row blocks, in the
+    other tensor-memory buffer, and every dW element must still be the exact
+    integer result; with 90 tiles per expert and a workspace the long experts
+    take the chunk-major schedule at the same time."""
+    import torch
+    counts = [511, 9000, 0, 512, 1, 513, 4100, 97, 300, 2000, 96, 5000, 7]
+    off = W.offsets_from_counts(counts)
+    E, M = len(counts), int(off[-1]) + 2
+    g, x = ints((M, N), 21, 0), ints((M, K), 21, 1)
+    init = W.integer_bf16((E, N, K), -3, 3, 21, 2)
+    dW = torch.from_numpy(W.bf16_bits_to_f32(init)).cuda() if accumulate else None
+    ws_t = torch.empty(gpu_lib.kgemm_workspace_bytes(E, N, K), dtype=torch.uint8, device="cuda") if ws else None
+    out = gpu_lib.kgemm(to_dev(g), to_dev(x), offsets_dev(off), out=dW, accumulate=accumulate, workspace=ws_t)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    got = out.cpu().numpy().astype(np.float64)
+    if N * K <= 1280 * 1024:  # every element
+        want = oracle.kgemm(g, x, off)
+        if accumulate:
+            want = want + W.bf16_bits_to_f32(init).astype(np.float64)
+        np.testing.assert_array_equal(got, want)
+    else:  # the first and last dW row of every expert and 64 others (the oracle row by row)
+        rng = np.random.default_rng(21)
+        es = np.concatenate([np.arange(E), np.arange(E), rng.integers(0, E, 64)]).astype(np.int32)
+        ns = np.concatenate([np.zeros(E), np.full(E, N - 1), rng.integers(0, N, 64)]).astype(np.int32)
+        want = oracle.kgemm(g, x, off, sel=(es, ns))
+        if accumulate:
+            want = want + W.bf16_bits_to_f32(init)[es, ns].astype(np.float64)
+        np.testing.assert_array_equal(got[es, ns], want)
+
+
 def test_kgemm_long_experts_random(gpu_lib):
     counts = [12000, 5000, 4032, 4033, 4096]
     off = W.offsets_from_counts(counts)
