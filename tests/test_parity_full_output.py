@@ -2,8 +2,10 @@
 kernel family, in the launch configuration the benchmark times: the M-grouped
 forward and input gradient (30B-A3B gate-up), the K-grouped FP32 weight
 gradient (30B-A3B gw13, and the skewed workload with tiny and empty experts,
-whose 18k-row expert is the longest FP32 accumulation), and the MXFP8 weight
-gradient.  The oracle computes every output (chunk by chunk, so host memory
+whose 18k-row expert is the longest FP32 accumulation), the MXFP8 forward
+(down projection: its oracle decodes every element, the slowest to compute)
+and weight gradient, and the nested grouped GEMM of the LoRA
+workload (the 64-column shrink tile and the two-outer-group expand).  The oracle computes every output (chunk by chunk, so host memory
 stays bounded) and the relative Frobenius error is that of the whole output;
 bf16 outputs also meet the per-element bound everywhere.  Rows of y at or past
 offsets[E] must keep their sentinel, and experts without rows must get dW = 0
@@ -92,3 +94,55 @@ def test_full_output_mx_kgemm(gpu_lib):
         cmp.add(dW[int(es[0]):int(es[-1]) + 1].reshape(-1, op.K).cpu().numpy(), ref)
     rec = cmp.finish()
     assert rec["elements"] == wl.E * op.N * op.K
+
+
+NESTED = [("lora_a3b", "lora_shrink"), ("lora_a3b", "lora_expand")]
+
+
+@pytest.mark.parametrize("wname,opname", NESTED, ids=[f"{w}-{o}" for w, o in NESTED])
+def test_full_output_nested(gpu_lib, wname, opname):
+    import torch
+    wl = W.ALL[wname]()
+    op = wl.op(opname)
+    off = wl.offsets
+    a_h, b_h = wl.tensor(op.a), wl.tensor(op.b)
+    y = torch.full((wl.M, op.outer * op.N), 7.0, dtype=torch.bfloat16, device="cuda")  # sentinel
+    gpu_lib.mgemm_nested(to_dev(a_h), to_dev(b_h), offsets_dev(off), transpose_B=op.transpose_B, out=y)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    cmp = FullCompare("bf16", f"{wname}/{opname}/full")
+    n = int(off[-1])
+    for r0 in range(0, n, ROW_CHUNK):
+        rows = np.arange(r0, min(n, r0 + ROW_CHUNK), dtype=np.int64)
+        ref = oracle.mgemm_nested(a_h, b_h, off, transpose_B=op.transpose_B, rows=rows)
+        cmp.add(to_host_bits(y[r0:r0 + len(rows)]), ref)
+    rec = cmp.finish()
+    assert rec["elements"] == n * op.outer * op.N
+    if n < wl.M:
+        assert bool((y[n:] == 7.0).all()), "rows past offsets[L] were written"
+
+
+def test_full_output_mx_mgemm(gpu_lib):
+    import torch
+    wl = W.ALL["a3b_mxfp8"]()
+    op = wl.op("mx_fwd_down")
+    off = wl.offsets
+    h = {k: wl.tensor(k) for k in (op.a, op.b, op.sa, op.sb)}
+    d = {k: torch.from_numpy(v).cuda() for k, v in h.items()}
+    doff = offsets_dev(off)
+    sab = gpu_lib.mx_scales_blocked(d[op.sa], doff)
+    sbb = gpu_lib.mx_scales_blocked(d[op.sb].view(-1, d[op.sb].shape[-1]), gpu_lib.mx_weight_offsets(wl.E, op.N))
+    y = torch.full((wl.M, op.N), 7.0, dtype=torch.bfloat16, device="cuda")  # sentinel
+    gpu_lib.mgemm_mxfp8(d[op.a], sab, d[op.b], sbb, doff, transpose_B=op.transpose_B, out=y)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    cmp = FullCompare("bf16", "a3b_mxfp8/mx_fwd_down/full")
+    n = int(off[-1])
+    for r0 in range(0, n, ROW_CHUNK):
+        rows = np.arange(r0, min(n, r0 + ROW_CHUNK), dtype=np.int64)
+        ref = oracle.mgemm_mx(h[op.a], h[op.sa], h[op.b], h[op.sb], off, transpose_B=op.transpose_B, rows=rows)
+        cmp.add(to_host_bits(y[r0:r0 + len(rows)]), ref)
+    rec = cmp.finish()
+    assert rec["elements"] == n * op.N
+    if n < wl.M:
+        assert bool((y[n:] == 7.0).all()), "rows past offsets[E] were written"
