@@ -4,8 +4,10 @@ forward and input gradient (30B-A3B gate-up), the K-grouped FP32 weight
 gradient (30B-A3B gw13, and the skewed workload with tiny and empty experts,
 whose 18k-row expert is the longest FP32 accumulation), the MXFP8 forward
 (down projection: its oracle decodes every element, the slowest to compute)
-and weight gradient, and the nested grouped GEMM of the LoRA
-workload (the 64-column shrink tile and the two-outer-group expand).  The oracle computes every output (chunk by chunk, so host memory
+and weight gradient, the nested grouped GEMM of the LoRA workload (the
+64-column shrink tile and the two-outer-group expand), and both fused SwiGLU
+kernels (gate-up forward with h and the saved pre-activation, down-projection
+input gradient with the SwiGLU backward).  The oracle computes every output (chunk by chunk, so host memory
 stays bounded) and the relative Frobenius error is that of the whole output;
 bf16 outputs also meet the per-element bound everywhere.  Rows of y at or past
 offsets[E] must keep their sentinel, and experts without rows must get dW = 0
@@ -146,3 +148,42 @@ def test_full_output_mx_mgemm(gpu_lib):
     assert rec["elements"] == n * op.N
     if n < wl.M:
         assert bool((y[n:] == 7.0).all()), "rows past offsets[E] were written"
+
+
+def test_full_output_swiglu_forward(gpu_lib):
+    import torch
+    wl = W.ALL["a3b_swiglu"]()
+    op = wl.op("fwd_gate_up_swiglu")
+    off = wl.offsets
+    a_h, b_h = wl.tensor(op.a), wl.tensor(op.b)
+    h, y13 = gpu_lib.mgemm_swiglu(to_dev(a_h), to_dev(b_h), offsets_dev(off), y13=True)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    cmp_h = FullCompare("bf16", "a3b_swiglu/fwd_gate_up_swiglu/h/full")
+    cmp_y = FullCompare("bf16", "a3b_swiglu/fwd_gate_up_swiglu/y13/full")
+    n = int(off[-1])
+    for r0 in range(0, n, ROW_CHUNK):
+        rows = np.arange(r0, min(n, r0 + ROW_CHUNK), dtype=np.int64)
+        y_ref = oracle.mgemm(a_h, b_h, off, rows=rows)
+        cmp_y.add(to_host_bits(y13[r0:r0 + len(rows)]), y_ref)
+        cmp_h.add(to_host_bits(h[r0:r0 + len(rows)]), oracle.swiglu(y_ref))
+    assert cmp_y.finish()["elements"] == n * op.N
+    assert cmp_h.finish()["elements"] == n * op.N // 2
+
+
+def test_full_output_swiglu_input_gradient(gpu_lib):
+    import torch
+    wl = W.ALL["a3b_swiglu"]()
+    op = wl.op("dgrad_down_swiglu")
+    off = wl.offsets
+    a_h, b_h, c_h = wl.tensor(op.a), wl.tensor(op.b), wl.tensor(op.c)
+    dy13 = gpu_lib.mgemm_swiglu_dgrad(to_dev(a_h), to_dev(b_h), offsets_dev(off), to_dev(c_h))
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    cmp = FullCompare("bf16", "a3b_swiglu/dgrad_down_swiglu/full")
+    n = int(off[-1])
+    for r0 in range(0, n, ROW_CHUNK):
+        rows = np.arange(r0, min(n, r0 + ROW_CHUNK), dtype=np.int64)
+        dh = oracle.mgemm(a_h, b_h, off, transpose_B=True, rows=rows)
+        cmp.add(to_host_bits(dy13[r0:r0 + len(rows)]), oracle.swiglu_bwd(dh, W.bf16_bits_to_f32(c_h[rows])))
+    assert cmp.finish()["elements"] == n * 2 * op.N
