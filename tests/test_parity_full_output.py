@@ -5,9 +5,11 @@ gradient (30B-A3B gw13, and the skewed workload with tiny and empty experts,
 whose 18k-row expert is the longest FP32 accumulation), the MXFP8 forward
 (down projection: its oracle decodes every element, the slowest to compute)
 and weight gradient, the nested grouped GEMM of the LoRA workload (the
-64-column shrink tile and the two-outer-group expand), and both fused SwiGLU
+64-column shrink tile and the two-outer-group expand), both fused SwiGLU
 kernels (gate-up forward with h and the saved pre-activation, down-projection
-input gradient with the SwiGLU backward).  The oracle computes every output (chunk by chunk, so host memory
+input gradient with the SwiGLU backward), the weight gradient accumulated
+into an FP32 main grad, and, bit for bit, every scale-layout conversion of
+the MXFP8 benchmark step.  The oracle computes every output (chunk by chunk, so host memory
 stays bounded) and the relative Frobenius error is that of the whole output;
 bf16 outputs also meet the per-element bound everywhere.  Rows of y at or past
 offsets[E] must keep their sentinel, and experts without rows must get dW = 0
@@ -187,3 +189,70 @@ def test_full_output_swiglu_input_gradient(gpu_lib):
         dh = oracle.mgemm(a_h, b_h, off, transpose_B=True, rows=rows)
         cmp.add(to_host_bits(dy13[r0:r0 + len(rows)]), oracle.swiglu_bwd(dh, W.bf16_bits_to_f32(c_h[rows])))
     assert cmp.finish()["elements"] == n * 2 * op.N
+
+
+def test_full_output_kgemm_accumulate(gpu_lib):
+    import torch
+    wl = W.ALL["a3b_acc"]()
+    op = wl.op("wgrad_gw2_acc")
+    off = wl.offsets
+    a_h, b_h = wl.tensor(op.a), wl.tensor(op.b)
+    init = W.bf16_bits_to_f32(W.normal_bf16((wl.E, op.N, op.K), 1.0, wl.seed, 90))
+    dW = torch.from_numpy(init).cuda()
+    gpu_lib.kgemm(to_dev(a_h), to_dev(b_h), offsets_dev(off), out=dW, accumulate=True)
+    torch.cuda.synchronize()
+    assert gpu_lib.device_status() == 0
+    cmp = FullCompare("fp32", "a3b_acc/wgrad_gw2_acc/full")
+    per = max(1, EXPERT_BYTES // (8 * op.N * op.K))
+    for e0 in range(0, wl.E, per):
+        es = np.arange(e0, min(wl.E, e0 + per), dtype=np.int32)
+        sel = (np.repeat(es, op.N), np.tile(np.arange(op.N, dtype=np.int32), len(es)))
+        ref = oracle.kgemm(a_h, b_h, off, sel=sel) + init[e0:e0 + len(es)].reshape(-1, op.K).astype(np.float64)
+        cmp.add(dW[int(es[0]):int(es[-1]) + 1].reshape(-1, op.K).cpu().numpy(), ref)
+    assert cmp.finish()["elements"] == wl.E * op.N * op.K
+
+
+def test_full_output_mx_scale_layouts(gpu_lib):
+    """Every conversion of the MXFP8 step at its full size, bit for bit: the
+    activation and weight scales of the four M-grouped GEMMs (blocked layout,
+    groups along the rows) and the scales of the two weight gradients (groups
+    along the contraction); nothing past the used blocks is written."""
+    import torch
+    wl = W.ALL["a3b_mxfp8"]()
+    off = wl.offsets
+    doff = offsets_dev(off)
+
+    def rows_grouped(src, goff):
+        R, KS = src.shape
+        G = len(goff) - 1
+        used = sum((int(goff[g + 1]) - int(goff[g]) + 127) // 128 for g in range(G)) * ((KS + 3) // 4) * 512
+        out = torch.full((gpu_lib.mx_blocked_bytes(R, KS, G),), 0xEE, dtype=torch.uint8, device="cuda")
+        gpu_lib.mx_scales_blocked(torch.from_numpy(src).cuda(), offsets_dev(goff), out=out)
+        return out, used, oracle.mx_blocked(src, goff)
+
+    def contraction_grouped(src, goff):
+        R, KS = src.shape
+        G = len(goff) - 1
+        nq = sum((int(goff[g + 1]) - int(goff[g]) + 127) // 128 for g in range(G))
+        used = ((R + 127) // 128) * nq * 512
+        out = torch.full((gpu_lib.mx_blocked_k_bytes(R, KS, G),), 0xEE, dtype=torch.uint8, device="cuda")
+        gpu_lib.mx_scales_blocked_k(torch.from_numpy(src).cuda(), doff, out=out)
+        return out, used, oracle.mx_blocked_k(src, goff)
+
+    checked = 0
+    for op in wl.ops:
+        if op.kind == "mx":
+            sa = wl.tensor(op.sa)
+            sb = wl.tensor(op.sb)
+            cases = [rows_grouped(sa, off),
+                     rows_grouped(sb.reshape(-1, sb.shape[-1]), np.arange(0, (wl.E + 1) * op.N, op.N, dtype=np.int32))]
+        else:
+            cases = [contraction_grouped(wl.tensor(op.sa), off), contraction_grouped(wl.tensor(op.sb), off)]
+        for out, used, want in cases:
+            torch.cuda.synchronize()
+            assert gpu_lib.device_status() == 0
+            got = out.cpu().numpy()
+            np.testing.assert_array_equal(got[:used], want[:used], err_msg=op.name)
+            assert (got[used:] == 0xEE).all(), f"{op.name}: bytes past the used blocks were written"
+            checked += 1
+    assert checked == 12
