@@ -1,7 +1,8 @@
 """Stream semantics of the C ABI: calls on different streams run
 independently and give the same bits as one stream, and a sequence of calls
 (no host synchronisation, no allocation inside the library) can be captured
-in a CUDA graph and replayed with new inputs."""
+in a CUDA graph and replayed with new inputs -- the workspace entry point's
+flag clear included."""
 import numpy as np
 import pytest
 
@@ -85,3 +86,38 @@ def test_graph_capture_and_replay(gpu_lib):
         run_ops(gpu_lib, src, ref)
         torch.cuda.synchronize()
         same_bits(outs, ref, int(p["off"][-1]))
+
+
+def test_graph_capture_of_the_workspace_entry_point(gpu_lib):
+    """rg_kgemm_ws in a captured graph: its flag clear (a memset node) and the
+    chunk-major kernel (90 dW tiles per expert, experts of several chunks)
+    replayed with new inputs give rg_kgemm's bits each time."""
+    import torch
+    counts = [5000, 0, 300, 9000, 37]
+    off = W.offsets_from_counts(counts)
+    E, N, K = len(counts), 2560, 2304
+    M = int(off[-1]) + 2
+
+    def inputs(seed):
+        return dict(g=to_dev(W.normal_bf16((M, N), 1.0, seed, 0)), x=to_dev(W.normal_bf16((M, K), 1.0, seed, 1)))
+
+    static = inputs(45)
+    doff = offsets_dev(off)
+    ws = torch.empty(gpu_lib.kgemm_workspace_bytes(E, N, K), dtype=torch.uint8, device="cuda")
+    dw = torch.empty((E, N, K), dtype=torch.float32, device="cuda")
+    gpu_lib.kgemm(static["g"], static["x"], doff, out=dw, workspace=ws)  # set-up before the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gpu_lib.kgemm(static["g"], static["x"], doff, out=dw, workspace=ws)
+    for seed in (46, 45, 47):
+        src = inputs(seed)
+        static["g"].copy_(src["g"])
+        static["x"].copy_(src["x"])
+        dw.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gpu_lib.device_status() == 0
+        ref = gpu_lib.kgemm(src["g"], src["x"], doff)
+        torch.cuda.synchronize()
+        assert torch.equal(dw.view(torch.int32), ref.view(torch.int32))
