@@ -48,6 +48,7 @@ struct DeviceState {
   int num_sms = 0;
   int mg_grid = 0;      // persistent grid of each kernel (CTAs)
   int kg_grid = 0;
+  int mx_grid = 0;      // MXFP8 Mgemm
   size_t max_smem = 0;  // opt-in dynamic shared memory per block
   unsigned int* status = nullptr;    // &g_status_word on this device
   unsigned int* selftest = nullptr;  // &g_selftest_word
@@ -115,7 +116,7 @@ int device_state(DeviceState** out) {
       if (encode_fn() == nullptr) return fail_cuda(cudaErrorNotSupported);
       // One CTA per SM (shared memory limits residency to one); with CTA
       // pairs, as many 2-CTA clusters as can be resident at once.
-      ds.mg_grid = ds.kg_grid = sms;
+      ds.mg_grid = ds.kg_grid = ds.mx_grid = sms;
       if (rg::kCtaGroup == 2) {
         int mc = 0, kc = 0;
         if ((e = rg::mgemm_max_clusters(&mc, smem)) != cudaSuccess) return fail_cuda(e);
@@ -123,6 +124,12 @@ int device_state(DeviceState** out) {
         if (mc < 1 || kc < 1) return fail_cuda(cudaErrorLaunchOutOfResources);
         ds.mg_grid = 2 * std::min(mc, sms / 2);
         ds.kg_grid = 2 * std::min(kc, sms / 2);
+      }
+      if (rg::mxm::CG == 2) {
+        int xc = 0;
+        if ((e = rg::mx_max_clusters(&xc, smem)) != cudaSuccess) return fail_cuda(e);
+        if (xc < 1) return fail_cuda(cudaErrorLaunchOutOfResources);
+        ds.mx_grid = 2 * std::min(xc, sms / 2);
       }
     }
     ds.ready = true;
@@ -429,13 +436,13 @@ int rg_mgemm_mxfp8(const void* xq, const void* sx_blocked, const void* wq, const
     if (!encode_sw(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, xq, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return RG_ERR_INVALID_ARG;
   }
-  if (!transpose_B) {  // wq [E, N, K]: one 128 (K) x 256 (N) box per stage
+  if (!transpose_B) {  // wq [E, N, K]: one 128 (K) x BN_CTA (N) box per stage (256 N, or 128 per CTA of a pair)
     const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
     const uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N) * K};
-    const uint32_t box[3] = {128, 256, 1};
+    const uint32_t box[3] = {128, static_cast<uint32_t>(rg::mxm::BN_CTA), 1};
     if (!encode_sw(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, wq, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return RG_ERR_INVALID_ARG;
-  } else {  // wq [E, K, N]: two 128 (N) x 128 (K) boxes per stage
+  } else {  // wq [E, K, N]: 128 (N) x 128 (K) boxes, two per stage (one per CTA of a pair)
     const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(E)};
     const uint64_t str[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K) * N};
     const uint32_t box[3] = {128, 128, 1};
@@ -447,6 +454,19 @@ int rg_mgemm_mxfp8(const void* xq, const void* sx_blocked, const void* wq, const
     const uint64_t str[1] = {static_cast<uint64_t>(N) * 2};
     const uint32_t box[2] = {32, 32};
     if (!encode_sw(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B))
+      return RG_ERR_INVALID_ARG;
+  }
+  // CTA pairs: the blocked scale buffers as rows of 256 bytes (a 512-byte
+  // chunk is two rows); a single CTA reads them with plain bulk copies
+  CUtensorMap tmSA = {}, tmSB = {};
+  if (rg::mxm::CG == 2) {
+    const uint64_t rows_a = static_cast<uint64_t>(rg_mx_blocked_bytes(M, K / 32, E)) / 256;
+    const uint64_t rows_b = static_cast<uint64_t>(rg_mx_blocked_bytes(static_cast<int64_t>(E) * N, K / 32, E)) / 256;
+    const uint64_t da[2] = {256, rows_a}, db[2] = {256, rows_b};
+    const uint64_t str[1] = {256};
+    const uint32_t box[2] = {256, 2};
+    if (!encode_sw(&tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, sx_blocked, da, str, box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_sw(&tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, sw_blocked, db, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
       return RG_ERR_INVALID_ARG;
   }
   rg::MxArgs a;
@@ -461,7 +481,7 @@ int rg_mgemm_mxfp8(const void* xq, const void* sx_blocked, const void* wq, const
   a.status = ds->status;
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.accumulate = 0;
-  const cudaError_t e = rg::launch_mx_mgemm(transpose_B != 0, tmA, tmB, tmY, a, ds->num_sms, stream);
+  const cudaError_t e = rg::launch_mx_mgemm(transpose_B != 0, tmA, tmB, tmY, tmSA, tmSB, a, ds->mx_grid, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
 }

@@ -83,6 +83,18 @@ constexpr int CHUNK_ROWS = 4096;  // rows summed in tensor memory per partial (3
 static_assert(BOX_COLS == 16 || BOX_COLS == 32, "dW boxes are 16 or 32 fp32 columns wide");
 }  // namespace mxk
 
+// MXFP8 Mgemm: 0 (default) = one CTA per 128 x 256 tile; 1 = a CTA pair
+// computes a 256 x 256 tile with the block-scaled tcgen05.mma.cta_group::2
+// (comparison build: measured 13-22% slower on the 30B-A3B layer, the
+// per-stage scale copies into tensor memory costing a pair more than a CTA).
+#ifndef RG_MX_PAIR
+#define RG_MX_PAIR 0
+#endif
+namespace mxm {
+constexpr int CG = RG_MX_PAIR ? 2 : 1;
+constexpr int BN_CTA = 256 / CG;  // B rows (output columns) loaded per CTA
+}  // namespace mxm
+
 // Largest E the kernels are set up for (shared-memory tables of E+1 ints).
 constexpr int RG_MAX_EXPERTS_CFG = 1024;
 
@@ -193,8 +205,13 @@ cudaError_t launch_kgemm(const CUtensorMap& tmG, const CUtensorMap& tmX, const C
 // blocked layout) and the conversion of grouped scales to that layout.
 size_t mx_smem_bytes(int E);
 cudaError_t mx_setup(int max_smem);
+// CTA pairs: 2-CTA clusters of the MXFP8 Mgemm resident at once.
+cudaError_t mx_max_clusters(int* clusters, int max_smem);
+// tmSA / tmSB: the blocked scale buffers of A and B as rows of 256 bytes
+// (the CTA-pair kernel copies its scale blocks through them).
 cudaError_t launch_mx_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                            const CUtensorMap& tmY, const MxArgs& args, int grid, cudaStream_t stream);
+                            const CUtensorMap& tmY, const CUtensorMap& tmSA, const CUtensorMap& tmSB,
+                            const MxArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_mx_blocked(const uint8_t* src, const int32_t* offsets, int G, int R, int KS, uint8_t* dst,
                               unsigned int* status, int num_sms, cudaStream_t stream);
 // MXFP8 Kgemm (FP8 operands quantized along the rows, experts on 32-row

@@ -17,26 +17,44 @@
 // consecutive 32-bit columns, one scale byte per 32-element K block.
 //
 // GEMM design (mx_mgemm_kernel)
-//   * Persistent grid, one CTA per SM, tile = 128 rows of one expert x 256
-//     output columns, tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale
-//     (M=128, N=256, K=32).  The tile list is built on the device from the
-//     offsets exactly as in the BF16 Mgemm (expert by expert, n fastest).
-//   * One stage = 128 K elements: A 128x128 B (16 KB), B 256x128 B (32 KB,
-//     K-major; or two 128x128 MN-major boxes for transpose_B), the A scale
-//     block (512 B) and the two B scale blocks (1 KB) -- four stages.
-//   * Lane 0 of warps 0 and 10: TMA loads and bulk copies of the scale
-//     blocks, alternate stages (one thread cannot issue copies fast enough).  Warp 1:
-//     tensor memory; its lane 0 copies each stage's scales into a per-stage
-//     slot of tensor memory (tcgen05.cp) and issues the four MMAs of the
-//     stage, scale byte k of each 32-bit scale word for MMA k.  Warps 2..9:
-//     epilogue, two per tensor-memory lane quarter (128 columns each).
-//   * Tensor memory: the fp32 accumulator (256 columns) and 4 x 12 scale
-//     columns; a second accumulator does not fit, so the epilogue drains the
-//     accumulator into registers and releases it before converting and
-//     storing, which lets the next tile's MMAs start almost at once.
+//   * Persistent grid.  The tile list is built on the device from the offsets
+//     exactly as in the BF16 Mgemm (expert by expert, n fastest); worker w (a
+//     CTA pair, or a CTA) takes tiles w, w+W, ...
+//   * CG = 1 (default): one CTA computes 128 rows of one expert x 256 output
+//     columns with tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale
+//     (M=128, N=256, K=32), four stages; scale blocks arrive by bulk copies.
+//   * CG = 2 (RG_MX_PAIR=1, comparison build): a CTA pair computes 256 rows
+//     x 256 columns with the cta_group::2 form (M=256).  Each CTA loads its
+//     own 128 rows of A and its 128 rows of B, 32 KB of operands per stage
+//     instead of 48 KB, in six stages.  The peer CTA's copies complete on the
+//     issuing CTA's stage barrier; scale blocks come through tensor maps
+//     over the blocked buffers (rows of 256 bytes) for that reason.  Each
+//     CTA's tensor memory needs the B scales of all 256 columns, so a pair
+//     copies as many scale blocks into tensor memory per MMA as a single
+//     CTA.  Measured on the 30B-A3B layer, the pair is 13-22% slower: with
+//     neither operand nor scale copies it reaches 2.9 PFLOP/s on the
+//     forward gate-up, the scale copies into tensor memory take a fifth of
+//     that away and the operand copies a further 8%.
+//   * One stage = 128 K elements: A 128x128 B, this CTA's B rows (K-major; or
+//     128-column MN-major boxes for transpose_B), the A scale block of this
+//     CTA's rows (512 B) and both B scale blocks of the tile (1 KB).
+//   * Lane 0 of warps 0 and 10: copies of alternate stages (one thread cannot
+//     issue copies fast enough).  Warp 1: tensor memory; in the issuing CTA
+//     its lane 0 copies each stage's scales into a per-stage slot of tensor
+//     memory (tcgen05.cp; with pairs every CTA's own blocks into its own
+//     tensor memory) and issues the four MMAs of the stage, scale byte k of
+//     each 32-bit scale word for MMA k.  Warps 2..9: epilogue, two per
+//     tensor-memory lane quarter (128 columns each).
+//   * Tensor memory: the fp32 accumulator (256 columns) and STAGES x 16
+//     scale columns; a second accumulator does not fit, so the epilogue
+//     drains the accumulator into registers and releases it before
+//     converting and storing, which lets the next tile's MMAs start almost at
+//     once.
 //   * Epilogue: bf16 (round to nearest even), 32-row x 32-column TMA stores
 //     through a 64-byte-swizzled staging buffer when all 32 rows belong to
-//     the expert, masked 16-byte stores otherwise.
+//     the expert, masked 16-byte stores otherwise.  A pair tile's second CTA
+//     may hold no row of the expert (its last tile of at most 128 rows); it
+//     stores nothing.
 //   * Bounded waits as in the BF16 kernels (WaitGuard): a wait that runs out
 //     sets the device status, the CTA drains and frees tensor memory.
 #include <algorithm>
@@ -48,18 +66,25 @@
 namespace rg {
 namespace {
 
+template <int CG>
 struct MxCfg {
-  static constexpr int BM = 128;
-  static constexpr int BN = 256;
-  static constexpr int BK = 128;  // K elements (bytes) per stage
-  static constexpr int STAGES = 4;
+  static constexpr int BM = 128;             // rows of A (and of D) per CTA
+  static constexpr int TILE_M = BM * CG;     // rows per tile
+  static constexpr int BN = 256;             // tile columns = MMA N
+  static constexpr int BN_CTA = BN / CG;     // B rows (output columns) loaded per CTA
+  static constexpr int BK = 128;             // K elements (bytes) per stage
+  static constexpr int STAGES = CG == 2 ? 6 : 4;
   static constexpr int A_BYTES = BM * BK;
-  static constexpr int B_BYTES = BN * BK;
+  static constexpr int B_BYTES = BN_CTA * BK;
   static constexpr int SFA_BYTES = 512;
+  // both 128-column B scale blocks of the tile, in every CTA of a pair: each
+  // CTA's tensor core reads the scales of all N columns from its own tensor
+  // memory (measured: a CTA holding only its own columns' block gives wrong
+  // products in the other half)
   static constexpr int SFB_BYTES = 1024;
   static constexpr int AB_BYTES = A_BYTES + B_BYTES;   // operand tiles of a stage (1024-aligned)
   static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
-  static constexpr int STAGE_BYTES = AB_BYTES + SF_BYTES;  // bytes one stage's copies deliver
+  static constexpr int STAGE_BYTES = AB_BYTES + SF_BYTES;  // bytes one stage's copies deliver to a CTA
   static constexpr int EPI_WARPS = 8;
   static constexpr int EPI_BUF_BYTES = 32 * 64;  // 32 rows x 32 bf16 columns
   // warps 0 and 10: producers (alternate stages), 1: MMA, 2..9: epilogue
@@ -73,14 +98,18 @@ struct MxCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SF_COL0 = 256;  // scale slots: stage s at SF_COL0 + 16 s (A: 4 cols, B: 8 cols)
 };
-static_assert(MxCfg::AB_BYTES % 1024 == 0, "operand tiles must keep the 1024-byte swizzle alignment");
+static_assert(MxCfg<mxm::CG>::AB_BYTES % 1024 == 0, "operand tiles must keep the 1024-byte swizzle alignment");
+static_assert(MxCfg<mxm::CG>::SF_COL0 + 16 * MxCfg<mxm::CG>::STAGES <= MxCfg<mxm::CG>::TMEM_COLS,
+              "the accumulator and the scale slots must fit in tensor memory");
 
-template <bool TRANS_B>
-__global__ void __launch_bounds__(MxCfg::THREADS, 1)
+template <bool TRANS_B, int CG>
+__global__ void __launch_bounds__(MxCfg<CG>::THREADS, 1)
     mx_mgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmY, const MxArgs args) {
-  using C = MxCfg;
-  constexpr int BM = C::BM, BN = C::BN, BK = C::BK, STAGES = C::STAGES;
+                    const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmSA,
+                    const __grid_constant__ CUtensorMap tmSB, const MxArgs args) {
+  using C = MxCfg<CG>;
+  constexpr int BM = C::BM, TILE_M = C::TILE_M, BN = C::BN, BN_CTA = C::BN_CTA, BK = C::BK;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {
@@ -103,10 +132,13 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;  // rank 0 issues the MMAs
+  const int worker = blockIdx.x / CG;
+  const int nworkers = gridDim.x / CG;
   const int E = args.E, N = args.N, K = args.K;
   const int nbn = (N + BN - 1) / BN;
   const int nkc = (K + BK - 1) / BK;      // stages per tile = scale chunks per block
-  const int nb_w = (N + BM - 1) / BM;     // 128-row scale blocks of one expert's B
+  const int nb_w = (N + 127) / 128;       // 128-row scale blocks of one expert's B
 
   // ---- offsets -> shared memory, validation, tile prefix ---------------------
   if (threadIdx.x == 0) misc[1] = 0;
@@ -115,7 +147,7 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
   int bad = 0;
   for (int i = threadIdx.x; i < E; i += blockDim.x) bad |= (s_off[i + 1] < s_off[i]);
   if (threadIdx.x == 0) bad |= (s_off[0] != 0) | (s_off[E] > args.M);
-  if (__syncthreads_or(bad)) {
+  if (__syncthreads_or(bad)) {  // both CTAs of a pair see the same offsets and leave together
     if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(args.status, kDevBadOffsets);
     return;
   }
@@ -123,7 +155,7 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
     const int per = (E + 31) / 32;
     const int lo = min(E, lane * per), hi = min(E, lo + per);
     int s = 0;
-    for (int e = lo; e < hi; ++e) s += ((s_off[e + 1] - s_off[e] + BM - 1) / BM) * nbn;
+    for (int e = lo; e < hi; ++e) s += ((s_off[e + 1] - s_off[e] + TILE_M - 1) / TILE_M) * nbn;
     int incl = s;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -133,13 +165,13 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
     int run = incl - s;
     for (int e = lo; e < hi; ++e) {
       s_pre[e] = run;
-      run += ((s_off[e + 1] - s_off[e] + BM - 1) / BM) * nbn;
+      run += ((s_off[e + 1] - s_off[e] + TILE_M - 1) / TILE_M) * nbn;
     }
     if (lane == 31) s_pre[E] = incl;
   }
   __syncthreads();
   const int T = s_pre[E];
-  if (static_cast<int>(blockIdx.x) >= T) return;
+  if (worker >= T) return;  // same decision in both CTAs of a pair
 
   // ---- barriers and tensor memory -------------------------------------------
   if (threadIdx.x == 0) {
@@ -148,19 +180,25 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
       mbar_init(empty_bar(s), 1);
     }
     mbar_init(tfull_bar, 1);
-    mbar_init(tempty_bar, C::EPI_WARPS);
+    mbar_init(tempty_bar, C::EPI_WARPS * CG);  // one arrival per epilogue warp of the pair
     mbar_init(drain_bar, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc<1>(smem_u32(&misc[0]), C::TMEM_COLS);
-    tmem_relinquish<1>();
+    tmem_alloc<CG>(smem_u32(&misc[0]), C::TMEM_COLS);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // peer barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
   const WaitGuard guard{args.status, args.wait_limit_ns, reinterpret_cast<volatile int*>(&misc[1])};
+  // barriers that the peer CTA (or the issuing CTA's tensor-core commits) arrive on
+  auto wait_pair = [&](uint32_t bar, uint32_t par) {
+    if constexpr (CG == 2) return mbar_wait_cl(guard, bar, par);
+    else return mbar_wait(guard, bar, par);
+  };
   // stage s: A at s*AB_BYTES and B after it; its scale blocks after all operand tiles
   auto sa_of = [&](int s) { return sbase + s * C::AB_BYTES; };
   auto sb_of = [&](int s) { return sa_of(s) + C::A_BYTES; };
@@ -174,6 +212,10 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      if constexpr (CG == 2) {
+        tma_prefetch_desc(&tmSA);
+        tma_prefetch_desc(&tmSB);
+      }
       const uint32_t pid = warp == 0 ? 0u : 1u;
       issue_log_init(ilog, pid);
       uint32_t it = 0;
@@ -181,16 +223,25 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       int e = 0;
-      for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-        while (s_pre[e + 1] <= t) ++e;
+      int blk_e = 0;  // 128-row scale blocks of A of the experts before e
+      const uint32_t full_issuer = CG == 2 ? mapa_shared(full_bar(0), 0) : full_bar(0);
+      for (int t = worker; t < T && ok; t += nworkers) {
+        while (s_pre[e + 1] <= t) {
+          blk_e += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+          ++e;
+        }
         const int local = t - s_pre[e];
         const int mb = local / nbn, nt = local % nbn;
-        const int row0 = s_off[e] + mb * BM;
-        const int n0 = nt * BN;
-        // scale blocks: A block (rows of expert e, block mb), B blocks 2nt and
+        const int tile_row0 = s_off[e] + mb * TILE_M;
+        const int row0 = tile_row0 + static_cast<int>(rank) * BM;  // this CTA's rows
+        const int n0 = nt * BN + static_cast<int>(rank) * BN_CTA;  // this CTA's B rows
+        // scale blocks: A's block of this CTA's rows (a pair tile's second
+        // CTA past the expert's end repeats the expert's last block: its
+        // rows are never stored, any finite scale will do), B blocks 2nt and
         // 2nt+1 of expert e (the second repeats the first past the last
-        // block: those B rows are zero-filled, any finite scale will do)
-        const int blk_a = s_pre[e] / nbn + mb;
+        // block: those B rows are zero-filled)
+        const int nblk = (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+        const int blk_a = blk_e + min(mb * CG + static_cast<int>(rank), nblk - 1);
         const int blk_b0 = e * nb_w + 2 * nt;
         const int blk_b1 = e * nb_w + min(2 * nt + 1, nb_w - 1);
         for (int kc = 0; kc < nkc; ++kc) {
@@ -201,30 +252,38 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
             }
             continue;
           }
-          if (!mbar_wait(guard, empty_bar(stage), phase ^ 1u)) {
+          if (!wait_pair(empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
           }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          // both CTAs' copies complete on the issuing CTA's full barrier,
+          // which expects the bytes of the whole pair
+          const uint32_t fb = full_issuer + 8u * stage;
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES * CG);
           // (debug-bounds build: a refused copy's bytes are counted as arrived)
-          if (RG_BOUNDS_OK(bounds::inner_aligned(kc * BK, 1) && bounds::mgemm_rows(row0, s_off[e], s_off[e + 1], args.M),
+          if (RG_BOUNDS_OK(bounds::inner_aligned(kc * BK, 1) &&
+                               bounds::mgemm_rows(tile_row0, s_off[e], s_off[e + 1], args.M),
                            args.status))
-            tma_load_2d(sa_of(stage), &tmA, fb, kc * BK, row0);
+            tma_load_2d_cg<CG>(sa_of(stage), &tmA, fb, kc * BK, row0);
           else
-            mbar_complete_tx_cluster(fb, BM * BK);
-          if constexpr (!TRANS_B) {
+            mbar_complete_tx_cluster(fb, C::A_BYTES);
+          if (n0 >= N) {
+            // a pair tile's second CTA past the last output column (N tail):
+            // no B rows to load, and the columns they would give are not stored
+            mbar_complete_tx_cluster(fb, C::B_BYTES);
+          } else if constexpr (!TRANS_B) {
             if (RG_BOUNDS_OK(bounds::inner_aligned(kc * BK, 1) && bounds::index_ok(n0, N) && bounds::index_ok(e, E),
                              args.status))
-              tma_load_3d(sb_of(stage), &tmB, fb, kc * BK, n0, e);
+              tma_load_3d_cg<CG>(sb_of(stage), &tmB, fb, kc * BK, n0, e);
             else
-              mbar_complete_tx_cluster(fb, BN * BK);
+              mbar_complete_tx_cluster(fb, C::B_BYTES);
           } else {
-            if (RG_BOUNDS_OK(bounds::inner_aligned(n0, 1) && bounds::index_ok(e, E), args.status)) {
-              tma_load_3d(sb_of(stage), &tmB, fb, n0, kc * BK, e);
-              tma_load_3d(sb_of(stage) + 16384, &tmB, fb, n0 + 128, kc * BK, e);
-            } else {
-              mbar_complete_tx_cluster(fb, BN * BK);
+#pragma unroll
+            for (int j = 0; j < BN_CTA / 128; ++j) {
+              if (RG_BOUNDS_OK(bounds::inner_aligned(n0 + 128 * j, 1) && bounds::index_ok(e, E), args.status))
+                tma_load_3d_cg<CG>(sb_of(stage) + 16384 * j, &tmB, fb, n0 + 128 * j, kc * BK, e);
+              else
+                mbar_complete_tx_cluster(fb, 16384);
             }
           }
           // scale blocks lie inside the blocked buffers: (M/128 + E) blocks of
@@ -232,11 +291,17 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
           if (RG_BOUNDS_OK(bounds::index_ok(blk_a, args.M / 128 + E) && bounds::index_ok(blk_b0, E * N / 128 + E) &&
                                bounds::index_ok(blk_b1, E * N / 128 + E),
                            args.status)) {
-            bulk_load(sfa_of(stage), args.sfa + (static_cast<int64_t>(blk_a) * nkc + kc) * 512, 512, fb);
-            bulk_load(sfb_of(stage), args.sfb + (static_cast<int64_t>(blk_b0) * nkc + kc) * 512, 512, fb);
-            bulk_load(sfb_of(stage) + 512, args.sfb + (static_cast<int64_t>(blk_b1) * nkc + kc) * 512, 512, fb);
+            if constexpr (CG == 2) {  // 512-byte chunk = two 256-byte rows of the maps
+              tma_load_2d_cg<2>(sfa_of(stage), &tmSA, fb, 0, 2 * (blk_a * nkc + kc));
+              tma_load_2d_cg<2>(sfb_of(stage), &tmSB, fb, 0, 2 * (blk_b0 * nkc + kc));
+              tma_load_2d_cg<2>(sfb_of(stage) + 512, &tmSB, fb, 0, 2 * (blk_b1 * nkc + kc));
+            } else {
+              bulk_load(sfa_of(stage), args.sfa + (static_cast<int64_t>(blk_a) * nkc + kc) * 512, 512, fb);
+              bulk_load(sfb_of(stage), args.sfb + (static_cast<int64_t>(blk_b0) * nkc + kc) * 512, 512, fb);
+              bulk_load(sfb_of(stage) + 512, args.sfb + (static_cast<int64_t>(blk_b1) * nkc + kc) * 512, 512, fb);
+            }
           } else {
-            mbar_complete_tx_cluster(fb, 3 * 512);
+            mbar_complete_tx_cluster(fb, C::SF_BYTES);
           }
           ilog->it[pid][stage] = static_cast<int>(it - 1);
           ilog->bytes[pid][stage] = C::STAGE_BYTES;
@@ -247,36 +312,36 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ============= scale copies and MMAs (warp 1, lane 0) =====================
+  } else if (warp == 1 && rank == 0) {
+    // ============= scale copies and MMAs (warp 1 of the issuing CTA) ==========
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < T; t += gridDim.x, ++acc) {
-      ok = __all_sync(0xffffffffu, mbar_wait(guard, tempty_bar, (acc & 1) ^ 1u));
+    for (int t = worker; t < T; t += nworkers, ++acc) {
+      ok = __all_sync(0xffffffffu, wait_pair(tempty_bar, (acc & 1) ^ 1u));
       if (!ok) break;
       tc_fence_after();
       for (int kc = 0; kc < nkc; ++kc) {
-        ok = __all_sync(0xffffffffu, mbar_wait(guard, full_bar(stage), phase));
+        ok = __all_sync(0xffffffffu, wait_pair(full_bar(stage), phase));
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t sfa_t = tmem + C::SF_COL0 + 16u * stage;
           const uint32_t sfb_t = sfa_t + 4u;
-          tmem_cp_32x128b_x4(sfa_t, sdesc_plain16(sfa_of(stage)));
-          tmem_cp_32x128b_x4(sfb_t, sdesc_plain16(sfb_of(stage)));
-          tmem_cp_32x128b_x4(sfb_t + 4u, sdesc_plain16(sfb_of(stage) + 512));
+          tmem_cp_32x128b_x4<CG>(sfa_t, sdesc_plain16(sfa_of(stage)));
+          tmem_cp_32x128b_x4<CG>(sfb_t, sdesc_plain16(sfb_of(stage)));
+          tmem_cp_32x128b_x4<CG>(sfb_t + 4u, sdesc_plain16(sfb_of(stage) + 512));
           const uint32_t sa = sa_of(stage), sb = sb_of(stage);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k) {
             const uint64_t ad = sdesc_sw128(sa + 32 * k, 16, 1024);
             const uint64_t bd = TRANS_B ? sdesc_sw128(sb + 4096 * k, 16384, 1024)
                                         : sdesc_sw128(sb + 32 * k, 16, 1024);
-            umma_mxf8(tmem, ad, bd, idesc_mxf8_f32(BM, BN, false, TRANS_B, k), sfa_t, sfb_t,
-                      (kc | k) != 0);
+            umma_mxf8<CG>(tmem, ad, bd, idesc_mxf8_f32(TILE_M, BN, false, TRANS_B, k), sfa_t, sfb_t,
+                          (kc | k) != 0);
           }
-          umma_commit<1>(empty_bar(stage));
+          umma_commit<CG>(empty_bar(stage));  // frees the stage (in both CTAs) once these MMAs finish
         }
         __syncwarp();
         if (++stage == STAGES) {
@@ -285,14 +350,16 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) umma_commit<1>(tfull_bar);
+      if (lane == 0) umma_commit<CG>(tfull_bar);  // accumulator ready for the epilogue(s)
       __syncwarp();
     }
-    if (!ok && lane == 0) {
-      umma_commit<1>(drain_bar);
+    if (!ok && lane == 0) {  // wait for issued MMAs before tensor memory is freed
+      umma_commit_local<CG>(drain_bar);
       mbar_wait_drain(drain_bar, 0);
     }
     __syncwarp();
+  } else if (warp == 1) {
+    // warp 1 of the peer CTA only takes part in the tensor-memory allocation
   } else {
     // ======================= epilogue (warps 2..9) ===========================
     // Warp w reads TMEM lane quarter q = w % 4 and column half h.
@@ -302,15 +369,18 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
     uint8_t* ebuf = epi + (warp - 2) * C::EPI_BUF_BYTES;
     const uint32_t ebuf_s = smem_u32(ebuf);
     __nv_bfloat16* y = static_cast<__nv_bfloat16*>(args.out);
+    const uint32_t tempty_issuer = CG == 2 ? mapa_shared(tempty_bar, 0) : tempty_bar;
     int acc = 0;
     int e = 0;
-    for (int t = blockIdx.x; t < T; t += gridDim.x, ++acc) {
+    for (int t = worker; t < T; t += nworkers, ++acc) {
       while (s_pre[e + 1] <= t) ++e;
       const int local = t - s_pre[e];
-      const int row0 = s_off[e] + (local / nbn) * BM;
+      const int row0 = s_off[e] + (local / nbn) * TILE_M + static_cast<int>(rank) * BM;
       const int n0 = (local % nbn) * BN + 128 * h;
-      const int rows_valid = min(BM, s_off[e + 1] - row0);
-      if (!__all_sync(0xffffffffu, mbar_wait(guard, tfull_bar, acc & 1))) break;
+      const int rows_valid = min(BM, s_off[e + 1] - row0);  // <= 0: this CTA's rows are past the expert
+      // the single accumulator is on the MMAs' critical path: lane 0 polls
+      // without sleeping (CTA pairs), the warp waits (one CTA)
+      if (!warp_wait_acc<CG, 32>(guard, tfull_bar, acc & 1)) break;
       tc_fence_after();
       uint32_t v[128];
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + 128u * h;
@@ -321,7 +391,10 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar);  // the accumulator is free for the next tile
+      if (lane == 0) {  // the accumulator is free for the next tile
+        if constexpr (CG == 2) mbar_arrive_cluster(tempty_issuer);
+        else mbar_arrive(tempty_bar);
+      }
       if (q * 32 >= rows_valid || n0 >= N) continue;
       uint32_t p[64];
 #pragma unroll
@@ -361,15 +434,21 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
   }
 
   // ---- teardown --------------------------------------------------------------
-  // the last phase each stage was filled in has landed (after an abort, the
-  // wait for copies still in flight) before the CTA exits
+  // The last phase each stage was filled in has landed (after an abort, the
+  // wait for copies still in flight) before the CTAs exit; with pairs the
+  // issuing CTA settles the stages of both (drain_stages), and the peer
+  // leaves only after that, since its copies complete on the issuer's
+  // barriers.
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0) drain_stages<STAGES>(full_bar(0), ilog, 0u);
-  __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // no remote arrive or MMA still targets either CTA
+  if (threadIdx.x == 0 && rank == 0)
+    drain_stages<STAGES>(full_bar(0), ilog, CG == 2 ? mapa_shared(smem_u32(ilog), 1) : 0u);
+  if constexpr (CG == 2) cluster_sync();
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc<1>(tmem, C::TMEM_COLS);
+    tmem_dealloc<CG>(tmem, C::TMEM_COLS);
   }
 }
 
@@ -1004,25 +1083,55 @@ __global__ void __launch_bounds__(MxkCfg::THREADS, 1)
 
 }  // namespace
 
-static_assert(MxCfg::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448,
+using MxSel = MxCfg<mxm::CG>;
+static_assert(MxSel::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448,
               "MXFP8 Mgemm configuration exceeds the shared memory of a CTA at the largest group count");
-size_t mx_smem_bytes(int E) { return MxCfg::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4; }
+size_t mx_smem_bytes(int E) { return MxSel::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4; }
 
 cudaError_t mx_setup(int max_smem) {
   const int bytes = static_cast<int>(std::min<size_t>(mx_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem));
-  cudaError_t e = cudaFuncSetAttribute(mx_mgemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = cudaFuncSetAttribute(mx_mgemm_kernel<false, mxm::CG>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(mx_mgemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return cudaFuncSetAttribute(mx_mgemm_kernel<true, mxm::CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+cudaError_t mx_max_clusters(int* clusters, int max_smem) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(4);
+  cfg.blockDim = dim3(MxSel::THREADS);
+  cfg.dynamicSmemBytes = std::min<size_t>(mx_smem_bytes(RG_MAX_EXPERTS_CFG), max_smem);
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(clusters, mx_mgemm_kernel<false, mxm::CG>, &cfg);
+}
+
+// grid: CTAs (a multiple of 2 with CTA pairs, launched as clusters of 2)
 cudaError_t launch_mx_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                            const CUtensorMap& tmY, const MxArgs& args, int grid, cudaStream_t stream) {
-  const size_t smem = mx_smem_bytes(args.E);
+                            const CUtensorMap& tmY, const CUtensorMap& tmSA, const CUtensorMap& tmSB,
+                            const MxArgs& args, int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(MxSel::THREADS);
+  cfg.dynamicSmemBytes = mx_smem_bytes(args.E);
+  cfg.stream = stream;
+  if (mxm::CG == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
   if (transpose_B)
-    mx_mgemm_kernel<true><<<grid, MxCfg::THREADS, smem, stream>>>(tmA, tmB, tmY, args);
-  else
-    mx_mgemm_kernel<false><<<grid, MxCfg::THREADS, smem, stream>>>(tmA, tmB, tmY, args);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, mx_mgemm_kernel<true, mxm::CG>, tmA, tmB, tmY, tmSA, tmSB, args);
+  return cudaLaunchKernelEx(&cfg, mx_mgemm_kernel<false, mxm::CG>, tmA, tmB, tmY, tmSA, tmSB, args);
 }
 
 cudaError_t launch_mx_blocked(const uint8_t* src, const int32_t* offsets, int G, int R, int KS, uint8_t* dst,

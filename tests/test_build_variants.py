@@ -1,7 +1,8 @@
 """Comparison builds keep compiling: the single-CTA build (RG_CTA_PAIR=0:
 tcgen05 MMAs of one CTA, M=128, instead of CTA pairs; every translation unit
-of the library, compiled for sm_103a into a scratch directory) and the MXFP8
-weight gradient with 128-column tiles (RG_MXK_BN=128).  No GPU is needed
+of the library, compiled for sm_103a into a scratch directory), the MXFP8
+weight gradient with 128-column tiles (RG_MXK_BN=128) and the MXFP8 Mgemm
+with CTA pairs (RG_MX_PAIR=1).  No GPU is needed
 (nvcc cross-compiles); skipped where nvcc is missing."""
 import os
 import shutil
@@ -45,3 +46,15 @@ def test_mx_wgrad_128_column_build_compiles(tmp_path):
            os.path.join(_build.CSRC, "mxgemm.cu"), "-o", str(tmp_path / "mxgemm.o")]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr[-2000:]
+
+
+@pytest.mark.skipif(_nvcc() is None, reason="nvcc not available")
+def test_mx_pair_build_compiles(tmp_path):
+    """The MXFP8 Mgemm's comparison build with CTA pairs (RG_MX_PAIR=1); the
+    host side (tensor-map boxes, grid) is in api.cu."""
+    cc = _nvcc()
+    for src in ("mxgemm.cu", "api.cu"):
+        cmd = [cc, *_build.ARCH, *_build.NVCC_FLAGS, "-DRG_MX_PAIR=1", "-c",
+               os.path.join(_build.CSRC, src), "-o", str(tmp_path / (src + ".o"))]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, (src, r.stderr[-2000:])
