@@ -184,15 +184,16 @@ bool encode_sw(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr
 // Transposed weights w [G, K, N] (N contiguous) as read by the input-gradient
 // Mgemm: 64 columns x 64 K rows per box.  With N a multiple of 64 the map is
 // the 4-D view {64 cols, K, column block, group} (column-block stride 128
-// bytes), whose boxes of two column blocks land in shared memory exactly as
-// two 64-column boxes side by side: one copy per atom instead of two.
+// bytes), whose boxes of box_cols / 64 column blocks (two for pair tiles,
+// four for single-CTA tiles) land in shared memory exactly as that many
+// 64-column boxes side by side: one copy per atom instead of one per box.
 // Returns the view used (1 = 4-D) or -1 when encoding fails.
-int encode_weight_t(CUtensorMap* m, const void* w, int G, int N, int K) {
+int encode_weight_t(CUtensorMap* m, const void* w, int G, int N, int K, int box_cols = rg::mg::BN_CTA) {
   if (N % 64 == 0) {
     const uint64_t dims[4] = {64, static_cast<uint64_t>(K), static_cast<uint64_t>(N / 64),
                               static_cast<uint64_t>(G)};
     const uint64_t str[3] = {static_cast<uint64_t>(N) * 2, 128, static_cast<uint64_t>(K) * N * 2};
-    const uint32_t box[4] = {64, rg::mg::BK, rg::mg::BN_CTA / 64, 1};
+    const uint32_t box[4] = {64, rg::mg::BK, static_cast<uint32_t>(box_cols / 64), 1};
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, w, dims, str, box) ? 1 : -1;
   }
   const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(G)};
@@ -259,8 +260,8 @@ int mgemm_impl(const void* x, const void* w, const int32_t* offsets, int O, int 
   if (w == nullptr || !aligned16(w)) return RG_ERR_INVALID_ARG;
   if (M > 0 && (x == nullptr || y == nullptr || !aligned16(x) || !aligned16(y)))
     return RG_ERR_INVALID_ARG;
-  // the tile list is indexed with 32-bit integers
-  const int64_t max_tiles = (M / rg::mg::TILE_M + L) * ((N + rg::mg::BN - 1) / rg::mg::BN) * O;
+  // the tile list is indexed with 32-bit integers (single-CTA tiles have BM rows)
+  const int64_t max_tiles = (M / rg::mg::BM + L) * ((N + rg::mg::BN - 1) / rg::mg::BN) * O;
   if (max_tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != RG_OK) return rc;
@@ -290,14 +291,16 @@ int mgemm_impl(const void* x, const void* w, const int32_t* offsets, int O, int 
   }
   int wide_b = 0;
   if (!transpose_B) {  // w [G, N, K], K contiguous: one 64-wide K box of the tile's B rows per stage and CTA
-    if (!encode_weight(&tmB, w, G, N, K, rg::mgemm_b_box_rows(false, N))) return RG_ERR_INVALID_ARG;
-  } else if ((wide_b = encode_weight_t(&tmB, w, G, N, K)) < 0) {  // w [G, K, N], N contiguous
+    if (!encode_weight(&tmB, w, G, N, K, rg::mgemm_b_box_rows(false, N, K))) return RG_ERR_INVALID_ARG;
+  } else if ((wide_b = encode_weight_t(&tmB, w, G, N, K, rg::mgemm_b_box_rows(true, N, K))) < 0) {
+    // w [G, K, N], N contiguous
     return RG_ERR_INVALID_ARG;
   }
   rg::GroupArgs args = group_args(ds, offsets, L, M, N, K, y);
   args.outer = O;
   args.mg_wide_b = wide_b;
-  const cudaError_t e = rg::launch_mgemm(transpose_B != 0, tmA, tmAh, tmB, tmY, args, ds->mg_grid, stream);
+  const cudaError_t e =
+      rg::launch_mgemm(transpose_B != 0, tmA, tmAh, tmB, tmY, args, ds->mg_grid, ds->num_sms, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return RG_OK;
 }

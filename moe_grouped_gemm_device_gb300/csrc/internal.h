@@ -160,12 +160,25 @@ static_assert(LIGHT_ROWS >= 1 && LIGHT_ROWS <= CHUNK_ROWS, "a light expert has r
 #define RG_MG_SHORT_POLL_NS 1000
 #endif
 
-// Mgemm tile variants (CTA pairs only): 64-column tiles for forward outputs at
-// most 64 wide, eight epilogue warps when the contraction fits one 64-deep
-// stage.  The host encodes B's tensor map for the tile the launch uses.
+// Mgemm tile variants of the CTA-pair build: 64-column pair tiles for
+// forward outputs at most 64 wide; a contraction that fits one 64-deep stage
+// (one MMA per tile, the epilogue and the accumulator hand-over set the pace)
+// runs on single CTAs, 128 x 256 tiles with RG_MG_ONE_STAGE_EPIW epilogue
+// warps: the hand-over between the MMA and the epilogue inside one CTA is
+// much shorter than across a pair.  The host encodes B's tensor map for the
+// tile the launch uses and launches single-CTA tiles on a grid of one CTA
+// per SM.
+#ifndef RG_MG_ONE_STAGE_EPIW
+#define RG_MG_ONE_STAGE_EPIW 8
+#endif
 inline bool mgemm_narrow(bool transpose_B, int N) { return kCtaGroup == 2 && !transpose_B && N <= 64; }
-inline bool mgemm_wide_epilogue(int K) { return kCtaGroup == 2 && K <= mg::BK; }
-inline int mgemm_b_box_rows(bool transpose_B, int N) { return mgemm_narrow(transpose_B, N) ? 32 : mg::BN_CTA; }
+inline bool mgemm_one_cta(bool transpose_B, int N, int K) {
+  return kCtaGroup == 2 && !mgemm_narrow(transpose_B, N) && K <= mg::BK;
+}
+// B rows (output columns) per CTA of the launch's tile
+inline int mgemm_b_box_rows(bool transpose_B, int N, int K) {
+  return mgemm_narrow(transpose_B, N) ? 32 : mgemm_one_cta(transpose_B, N, K) ? mg::BN : mg::BN_CTA;
+}
 
 // Bytes of dynamic shared memory a launch with E experts needs.
 size_t mgemm_smem_bytes(int E);
@@ -183,9 +196,10 @@ cudaError_t kgemm_max_clusters(int* clusters, int max_smem);
 // tmA: x with boxes of 128 rows; tmAh: the same tensor with boxes of 64 rows
 // (an expert's last row block of at most 128 rows, split 64 / 64 between the
 // CTAs of a pair).
+// grid: CTAs of the pair tiles; sms: CTAs of the single-CTA tiles (one per SM)
 cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmAh,
                          const CUtensorMap& tmB, const CUtensorMap& tmY, const GroupArgs& args, int grid,
-                         cudaStream_t stream);
+                         int sms, cudaStream_t stream);
 // Forward gate-up GEMM with the SwiGLU activation in the epilogue: B = w13
 // [E, 2F, K] (gate rows then up rows), args.N = 2F, tmH/args.out = h [M, F],
 // tmY13/args.out2 = y13 [M, 2F] or null.  CTA pairs only.

@@ -69,8 +69,9 @@ struct Cfg {
   static constexpr int KATOMS = CG == 2 && (EPIW == 4) ? 2 : 1;
   static constexpr int BKS = BK * KATOMS;   // K per stage
   // 256-column tiles: three 64 KB stages; 64-column tiles (N = 64 MMAs, a
-  // quarter as long): five 40 KB stages; one-stage contractions: three
-  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 5 : 3) : 4;
+  // quarter as long): five 40 KB stages; single CTAs: four 48 KB stages, or
+  // three beside the staging of eight epilogue warps (one-stage contractions)
+  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 5 : 3) : (EPIW == 8 ? 3 : 4);
   static constexpr int A_ATOM = BM * BK * 2;       // one atom of A (bytes)
   static constexpr int B_ATOM = BN_CTA * BK * 2;   // one atom of B
   static constexpr int A_BYTES = A_ATOM * KATOMS;
@@ -649,32 +650,36 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
 
 // every variant holds the tables of RG_MAX_EXPERTS_CFG groups beside its pipeline
 // (the 8-epilogue-warp and 64-column tiles exist for CTA pairs only)
+constexpr int kOneEpiw = RG_MG_ONE_STAGE_EPIW;
+static_assert(kOneEpiw == 4 || kOneEpiw == 8, "single-CTA one-stage tiles: 4 or 8 epilogue warps");
 static_assert(Cfg<kCtaGroup, 256, 4>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 &&
                   (kCtaGroup == 1 ||
                    (Cfg<kCtaGroup, 256, 8>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 &&
-                    Cfg<kCtaGroup, 64, 4>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448)),
+                    Cfg<kCtaGroup, 64, 4>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 &&
+                    Cfg<1, 256, kOneEpiw>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448)),
               "an Mgemm variant exceeds the shared memory of a CTA at the largest group count");
 
-template <int BNT, int EPIW>
+template <int BNT, int EPIW, int CG = kCtaGroup>
 size_t smem_of(int E) {
-  return Cfg<kCtaGroup, BNT, EPIW>::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4;
+  return Cfg<CG, BNT, EPIW>::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4;
 }
 
-template <bool TB, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4>
+template <bool TB, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4, int CG = kCtaGroup>
 cudaError_t set_smem(int max_smem) {
-  const int bytes = static_cast<int>(std::min<size_t>(smem_of<BNT, EPIW>(RG_MAX_EXPERTS_CFG), max_smem));
-  return cudaFuncSetAttribute(mgemm_kernel<TB, kCtaGroup, EPI, BNT, EPIW>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  const int bytes = static_cast<int>(std::min<size_t>(smem_of<BNT, EPIW, CG>(RG_MAX_EXPERTS_CFG), max_smem));
+  return cudaFuncSetAttribute(mgemm_kernel<TB, CG, EPI, BNT, EPIW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              bytes);
 }
 
+// launch configuration; CTA pairs (cg == 2) as clusters of two
 void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, size_t smem, int threads,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, int cg = kCtaGroup) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(grid);
   cfg->blockDim = dim3(threads);
   cfg->dynamicSmemBytes = smem;
   cfg->stream = stream;
-  if (kCtaGroup == 2) {
+  if (cg == 2) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
@@ -684,21 +689,21 @@ void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, s
   }
 }
 
-template <bool TB, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4>
+template <bool TB, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4, int CG = kCtaGroup>
 cudaError_t launch_variant(const CUtensorMap& tmA, const CUtensorMap& tmAh, const CUtensorMap& tmB,
                            const CUtensorMap& tmY, const CUtensorMap& tmY2, const GroupArgs& args, int grid,
                            cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  fill_config(&cfg, attr, grid, smem_of<BNT, EPIW>(args.E), Cfg<kCtaGroup, BNT, EPIW>::THREADS, stream);
-  return cudaLaunchKernelEx(&cfg, mgemm_kernel<TB, kCtaGroup, EPI, BNT, EPIW>, tmA, tmAh, tmB, tmY, tmY2, args);
+  fill_config(&cfg, attr, grid, smem_of<BNT, EPIW, CG>(args.E), Cfg<CG, BNT, EPIW>::THREADS, stream, CG);
+  return cudaLaunchKernelEx(&cfg, mgemm_kernel<TB, CG, EPI, BNT, EPIW>, tmA, tmAh, tmB, tmY, tmY2, args);
 }
 
 }  // namespace
 
 size_t mgemm_smem_bytes(int E) {  // the largest of the variants built
   if constexpr (kCtaGroup == 1) return smem_of<256, 4>(E);
-  return std::max({smem_of<256, 4>(E), smem_of<256, 8>(E), smem_of<64, 4>(E)});
+  return std::max({smem_of<256, 4>(E), smem_of<256, 8>(E), smem_of<64, 4>(E), smem_of<256, kOneEpiw, 1>(E)});
 }
 
 cudaError_t mgemm_setup(int max_smem) {
@@ -709,8 +714,8 @@ cudaError_t mgemm_setup(int max_smem) {
   if constexpr (kCtaGroup == 2) {
     if ((e = set_smem<false, kEpiSwiglu>(max_smem)) != cudaSuccess) return e;
     if ((e = set_smem<false, kEpiPlain, 64, 4>(max_smem)) != cudaSuccess) return e;
-    if ((e = set_smem<false, kEpiPlain, 256, 8>(max_smem)) != cudaSuccess) return e;
-    if ((e = set_smem<true, kEpiPlain, 256, 8>(max_smem)) != cudaSuccess) return e;
+    if ((e = set_smem<false, kEpiPlain, 256, kOneEpiw, 1>(max_smem)) != cudaSuccess) return e;
+    if ((e = set_smem<true, kEpiPlain, 256, kOneEpiw, 1>(max_smem)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
@@ -725,14 +730,14 @@ cudaError_t mgemm_max_clusters(int* clusters, int max_smem) {
 
 cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtensorMap& tmAh,
                          const CUtensorMap& tmB, const CUtensorMap& tmY, const GroupArgs& args, int grid,
-                         cudaStream_t stream) {
+                         int sms, cudaStream_t stream) {
   if constexpr (kCtaGroup == 2) {
     if (mgemm_narrow(transpose_B != 0, args.N))
       return launch_variant<false, kEpiPlain, 64, 4>(tmA, tmAh, tmB, tmY, tmY, args, grid, stream);
-    if (mgemm_wide_epilogue(args.K)) {
+    if (mgemm_one_cta(transpose_B != 0, args.N, args.K)) {
       if (transpose_B)
-        return launch_variant<true, kEpiPlain, 256, 8>(tmA, tmAh, tmB, tmY, tmY, args, grid, stream);
-      return launch_variant<false, kEpiPlain, 256, 8>(tmA, tmAh, tmB, tmY, tmY, args, grid, stream);
+        return launch_variant<true, kEpiPlain, 256, kOneEpiw, 1>(tmA, tmAh, tmB, tmY, tmY, args, sms, stream);
+      return launch_variant<false, kEpiPlain, 256, kOneEpiw, 1>(tmA, tmAh, tmB, tmY, tmY, args, sms, stream);
     }
   }
   if (transpose_B) return launch_variant<true>(tmA, tmAh, tmB, tmY, tmY, args, grid, stream);

@@ -153,9 +153,9 @@ def test_nested_bad_offsets_flagged(gpu_lib):
                          ids=["narrow48", "narrow64", "narrow16_longK", "shallow40", "shallow64_dgrad",
                               "shallow16_dgrad", "shallow8"])
 def test_mgemm_small_tile_variants_bit_exact(gpu_lib, N, K, transpose_B):
-    """Outputs at most 64 wide (64-column tiles) and contractions of one
-    64-deep stage (eight epilogue warps) run their own tile variants; integer
-    inputs make the expected bf16 outputs exact."""
+    """Outputs at most 64 wide (64-column pair tiles) and contractions of one
+    64-deep stage (single-CTA 128 x 256 tiles, eight epilogue warps) run their
+    own tile variants; integer inputs make the expected bf16 outputs exact."""
     counts = [300, 0, 1, 129, 77]
     off = W.offsets_from_counts(counts)
     M = int(off[-1]) + 5
