@@ -188,35 +188,46 @@ bool encode_sw(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr
 // four for single-CTA tiles) land in shared memory exactly as that many
 // 64-column boxes side by side: one copy per atom instead of one per box.
 // Returns the view used (1 = 4-D) or -1 when encoding fails.
-int encode_weight_t(CUtensorMap* m, const void* w, int G, int N, int K, int box_cols = rg::mg::BN_CTA) {
+// kbox K rows per box (64, or 16 / 32 for the narrow boxes of single-CTA
+// one-stage tiles; the rows stay 128 bytes of N, 128-byte swizzle).
+int encode_weight_t(CUtensorMap* m, const void* w, int G, int N, int K, int box_cols = rg::mg::BN_CTA,
+                    int kbox = rg::mg::BK) {
   if (N % 64 == 0) {
     const uint64_t dims[4] = {64, static_cast<uint64_t>(K), static_cast<uint64_t>(N / 64),
                               static_cast<uint64_t>(G)};
     const uint64_t str[3] = {static_cast<uint64_t>(N) * 2, 128, static_cast<uint64_t>(K) * N * 2};
-    const uint32_t box[4] = {64, rg::mg::BK, static_cast<uint32_t>(box_cols / 64), 1};
+    const uint32_t box[4] = {64, static_cast<uint32_t>(kbox), static_cast<uint32_t>(box_cols / 64), 1};
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, w, dims, str, box) ? 1 : -1;
   }
   const uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(G)};
   const uint64_t str[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(K) * N * 2};
-  const uint32_t box[3] = {64, rg::mg::BK, 1};
+  const uint32_t box[3] = {64, static_cast<uint32_t>(kbox), 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box) ? 0 : -1;
 }
 
-// Row-major bf16 [rows, cols] tensor, boxes of 64 columns x box_rows rows.
-bool encode_rows(CUtensorMap* m, const void* ptr, int64_t rows, int cols, uint32_t box_rows) {
-  const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
-  const uint64_t str[1] = {static_cast<uint64_t>(cols) * 2};
-  const uint32_t box[2] = {64, box_rows};
-  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, str, box);
+// Swizzle of a K-major box whose rows are kbox bf16 (32, 64 or 128 bytes):
+// the swizzle of the row's width, as the kernels' shared-memory descriptors
+// expect.
+CUtensorMapSwizzle kswizzle(int kbox) {
+  return kbox == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : kbox == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
 }
 
-// Forward weight [E, N, K] (K contiguous): boxes of 64 K x (B rows per CTA of
-// the tile the launch uses).
-bool encode_weight(CUtensorMap* m, const void* w, int E, int N, int K, int box_rows) {
+// Row-major bf16 [rows, cols] tensor, boxes of kbox columns x box_rows rows.
+bool encode_rows(CUtensorMap* m, const void* ptr, int64_t rows, int cols, uint32_t box_rows,
+                 int kbox = rg::mg::BK) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+  const uint64_t str[1] = {static_cast<uint64_t>(cols) * 2};
+  const uint32_t box[2] = {static_cast<uint32_t>(kbox), box_rows};
+  return encode_sw(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, str, box, kswizzle(kbox));
+}
+
+// Forward weight [E, N, K] (K contiguous): boxes of kbox K x (B rows per CTA
+// of the tile the launch uses).
+bool encode_weight(CUtensorMap* m, const void* w, int E, int N, int K, int box_rows, int kbox = rg::mg::BK) {
   const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
   const uint64_t str[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(N) * K * 2};
-  const uint32_t box[3] = {64, static_cast<uint32_t>(box_rows), 1};
-  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box);
+  const uint32_t box[3] = {static_cast<uint32_t>(kbox), static_cast<uint32_t>(box_rows), 1};
+  return encode_sw(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box, kswizzle(kbox));
 }
 
 rg::GroupArgs group_args(const DeviceState* ds, const int32_t* offsets, int E, int64_t M, int N, int K,
@@ -270,20 +281,23 @@ int mgemm_impl(const void* x, const void* w, const int32_t* offsets, int O, int 
 
   // The weights of all (outer, inner) groups form one stack of O*L matrices.
   const int G = O * L;
+  const int kbox = rg::mgemm_kbox(transpose_B != 0, N, K);  // K columns per operand box
   CUtensorMap tmA, tmAh, tmB, tmY;
   if (O == 1) {
-    if (!encode_rows(&tmA, x, M, K, rg::mg::BM)) return RG_ERR_INVALID_ARG;
-    if (!encode_rows(&tmAh, x, M, K, rg::mg::BM / 2)) return RG_ERR_INVALID_ARG;
+    if (!encode_rows(&tmA, x, M, K, rg::mg::BM, kbox)) return RG_ERR_INVALID_ARG;
+    if (!encode_rows(&tmAh, x, M, K, rg::mg::BM / 2, kbox)) return RG_ERR_INVALID_ARG;
     if (!encode_rows(&tmY, y, M, N, 32)) return RG_ERR_INVALID_ARG;
   } else {
     // x [M, O*K] as {K, O, M}; y [M, O*N] as {N, O, M}: one outer group's
     // column block per box, so a box never reads or writes a neighbour's columns
     const uint64_t xd[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(O), static_cast<uint64_t>(M)};
     const uint64_t xs[2] = {static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(O) * K * 2};
-    const uint32_t xb[3] = {64, 1, rg::mg::BM};
-    if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, xd, xs, xb)) return RG_ERR_INVALID_ARG;
-    const uint32_t xbh[3] = {64, 1, rg::mg::BM / 2};
-    if (!encode(&tmAh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, xd, xs, xbh)) return RG_ERR_INVALID_ARG;
+    const uint32_t xb[3] = {static_cast<uint32_t>(kbox), 1, rg::mg::BM};
+    if (!encode_sw(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, xd, xs, xb, kswizzle(kbox)))
+      return RG_ERR_INVALID_ARG;
+    const uint32_t xbh[3] = {static_cast<uint32_t>(kbox), 1, rg::mg::BM / 2};
+    if (!encode_sw(&tmAh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, xd, xs, xbh, kswizzle(kbox)))
+      return RG_ERR_INVALID_ARG;
     const uint64_t yd[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(O), static_cast<uint64_t>(M)};
     const uint64_t ys[2] = {static_cast<uint64_t>(N) * 2, static_cast<uint64_t>(O) * N * 2};
     const uint32_t yb[3] = {64, 1, 32};
@@ -291,8 +305,8 @@ int mgemm_impl(const void* x, const void* w, const int32_t* offsets, int O, int 
   }
   int wide_b = 0;
   if (!transpose_B) {  // w [G, N, K], K contiguous: one 64-wide K box of the tile's B rows per stage and CTA
-    if (!encode_weight(&tmB, w, G, N, K, rg::mgemm_b_box_rows(false, N, K))) return RG_ERR_INVALID_ARG;
-  } else if ((wide_b = encode_weight_t(&tmB, w, G, N, K, rg::mgemm_b_box_rows(true, N, K))) < 0) {
+    if (!encode_weight(&tmB, w, G, N, K, rg::mgemm_b_box_rows(false, N, K), kbox)) return RG_ERR_INVALID_ARG;
+  } else if ((wide_b = encode_weight_t(&tmB, w, G, N, K, rg::mgemm_b_box_rows(true, N, K), kbox)) < 0) {
     // w [G, K, N], N contiguous
     return RG_ERR_INVALID_ARG;
   }

@@ -175,6 +175,14 @@ inline bool mgemm_narrow(bool transpose_B, int N) { return kCtaGroup == 2 && !tr
 inline bool mgemm_one_cta(bool transpose_B, int N, int K) {
   return kCtaGroup == 2 && !mgemm_narrow(transpose_B, N) && K <= mg::BK;
 }
+// K columns per operand box: 64 (128-byte rows), or for single-CTA
+// one-stage tiles of shorter contractions 16 or 32 (rows of 32 or 64 bytes
+// with the swizzle of that width), so that the copies do not fill three
+// quarters or half of each box with zeros.
+inline int mgemm_kbox(bool transpose_B, int N, int K) {
+  if (!mgemm_one_cta(transpose_B, N, K) || RG_MG_ONE_STAGE_EPIW != 8) return mg::BK;
+  return K <= 16 ? 16 : K <= 32 ? 32 : mg::BK;
+}
 // B rows (output columns) per CTA of the launch's tile
 inline int mgemm_b_box_rows(bool transpose_B, int N, int K) {
   return mgemm_narrow(transpose_B, N) ? 32 : mgemm_one_cta(transpose_B, N, K) ? mg::BN : mg::BN_CTA;

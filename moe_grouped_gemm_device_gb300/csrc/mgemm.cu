@@ -56,13 +56,22 @@ namespace {
 // otherwise be mostly padding).  EPIW: epilogue warps (4; 8 when the
 // contraction fits one stage and the epilogue, not the MMAs, sets the pace --
 // two warps per tensor-memory lane quarter then split the columns).
-template <int CG, int BNT = 256, int EPIW = 4>
+// operand stages of the narrow-box one-stage tiles (3, 4 and 6 measured
+// alike; 10 slower)
+#ifndef RG_MG_NARROW_STAGES
+#define RG_MG_NARROW_STAGES 4
+#endif
+// BKW: K columns per operand box (64: rows of 128 bytes, 128-byte swizzle;
+// 16 or 32 for the single-CTA one-stage tiles of contractions that short,
+// rows of 32 or 64 bytes with the swizzle of that width, instead of boxes
+// three quarters or half zero-filled).
+template <int CG, int BNT = 256, int EPIW = 4, int BKW = 64>
 struct Cfg {
   static constexpr int BM = 128;            // rows of A (and of D) per CTA
   static constexpr int TILE_M = BM * CG;    // rows per tile
   static constexpr int BN = BNT;            // tile columns = MMA N
   static constexpr int BN_CTA = BN / CG;    // B rows (output columns) loaded per CTA
-  static constexpr int BK = 64;             // K of one 128-byte swizzle atom (bf16)
+  static constexpr int BK = BKW;            // K of one operand box (bf16)
   // Atoms per stage: two for the 256- and 64-column tiles, so that one
   // barrier round of the MMA warp issues eight MMAs (four cost a fixed share
   // of its time); the 8-epilogue-warp tile (K <= 64) has one.
@@ -70,8 +79,9 @@ struct Cfg {
   static constexpr int BKS = BK * KATOMS;   // K per stage
   // 256-column tiles: three 64 KB stages; 64-column tiles (N = 64 MMAs, a
   // quarter as long): five 40 KB stages; single CTAs: four 48 KB stages, or
-  // three beside the staging of eight epilogue warps (one-stage contractions)
-  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 5 : 3) : (EPIW == 8 ? 3 : 4);
+  // three beside the staging of eight epilogue warps (one-stage contractions;
+  // RG_MG_NARROW_STAGES with narrow operand boxes)
+  static constexpr int STAGES = CG == 2 ? (BNT == 64 ? 5 : 3) : (EPIW == 8 ? (BKW == 64 ? 3 : RG_MG_NARROW_STAGES) : 4);
   static constexpr int A_ATOM = BM * BK * 2;       // one atom of A (bytes)
   static constexpr int B_ATOM = BN_CTA * BK * 2;   // one atom of B
   static constexpr int A_BYTES = A_ATOM * KATOMS;
@@ -112,8 +122,20 @@ constexpr uint32_t TMEM_COLS = 512;
 //                  and the epilogue writes dy13 = [dh*up*SiLU'(gate), dh*SiLU(gate)].
 constexpr int kEpiPlain = 0, kEpiSwiglu = 1, kEpiSwigluBwd = 2;
 
-template <bool TRANS_B, int CG, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4>
-__global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
+// Shared-memory descriptor of a K-major operand whose rows are SW bytes
+// (SW = 32, 64 or 128) with the SW-byte swizzle: 8-row atoms of 8 x SW bytes
+// packed one after the other (SBO), the K extent of one MMA inside a row
+// (LBO unused).  Swizzle mode bits: 2 = 128 B, 4 = 64 B, 6 = 32 B.
+template <int SW>
+__device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t saddr) {
+  static_assert(SW == 32 || SW == 64 || SW == 128, "swizzle width");
+  constexpr uint64_t mode = SW == 128 ? 2 : SW == 64 ? 4 : 6;
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(16 >> 4) << 16) |
+         (static_cast<uint64_t>((8 * SW) >> 4) << 32) | (1ull << 46) | (mode << 61);
+}
+
+template <bool TRANS_B, int CG, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4, int BKW = 64>
+__global__ void __launch_bounds__(Cfg<CG, BNT, EPIW, BKW>::THREADS, 1)
     mgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAh,
                  const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmY2,
@@ -124,7 +146,9 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
   static_assert((BNT == 256 && (EPIW == 4 || EPIW == 8)) || (BNT == 64 && EPIW == 4 && CG == 2 && !TRANS_B),
                 "tile variants: 256 columns with 4 or 8 epilogue warps; 64 columns (forward, CTA pairs)");
   static_assert(EPI == kEpiPlain || (BNT == 256 && EPIW == 4), "fused epilogues use the default tile");
-  using C = Cfg<CG, BNT, EPIW>;
+  static_assert(BKW == 64 || ((BKW == 16 || BKW == 32) && CG == 1 && EPIW == 8 && BNT == 256 && EPI == kEpiPlain),
+                "narrow operand boxes: single-CTA one-stage tiles only");
+  using C = Cfg<CG, BNT, EPIW, BKW>;
   constexpr int BM = C::BM, TILE_M = C::TILE_M, BN = C::BN, BN_CTA = C::BN_CTA, BK = C::BK;
   constexpr int KATOMS = C::KATOMS, BKS = C::BKS, A_ATOM = C::A_ATOM, B_ATOM = C::B_ATOM;
   constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
@@ -318,11 +342,11 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
                   mbar_complete_tx_cluster(fb, B_ATOM);
               } else {
 #pragma unroll
-                for (int jj = 0; jj < BN_CTA / 64; ++jj) {
+                for (int jj = 0; jj < BN_CTA / 64; ++jj) {  // 64 columns x BK K rows per box
                   if (RG_BOUNDS_OK(bounds::inner_aligned(n0 + 64 * jj, 2) && bounds::index_ok(eb, O * E), args.status))
-                    tma_load_3d_cg<CG>(sbj + jj * 8192, &tmB, fb, n0 + 64 * jj, kc, eb);
+                    tma_load_3d_cg<CG>(sbj + jj * (BK * 128), &tmB, fb, n0 + 64 * jj, kc, eb);
                   else
-                    mbar_complete_tx_cluster(fb, 8192);
+                    mbar_complete_tx_cluster(fb, BK * 128);
                 }
               }
             }
@@ -368,9 +392,10 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW>::THREADS, 1)
             // steps at or past K multiply zero-filled columns: skipped (bit-identical)
             if (kb * BKS + BK * j + 16 * kk < K) {
               const uint32_t saj = sa + j * A_ATOM, sbj = sb + j * B_ATOM;
-              const uint64_t ad = sdesc_sw128(saj + 32 * kk, 16, 1024);
-              const uint64_t bd = TRANS_B ? sdesc_sw128(sbj + 2048 * kk, 8192, 1024)
-                                          : sdesc_sw128(sbj + 32 * kk, 16, 1024);
+              const uint64_t ad = sdesc_kmajor<BK * 2>(saj + 32 * kk);
+              // transposed B: 128-byte rows of 64 columns, BK K rows per 64-column block
+              const uint64_t bd = TRANS_B ? sdesc_sw128(sbj + 2048 * kk, BK * 128, 1024)
+                                          : sdesc_kmajor<BK * 2>(sbj + 32 * kk);
               umma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0);
             }
           }
@@ -659,16 +684,17 @@ static_assert(Cfg<kCtaGroup, 256, 4>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) 
                     Cfg<1, 256, kOneEpiw>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448)),
               "an Mgemm variant exceeds the shared memory of a CTA at the largest group count");
 
-template <int BNT, int EPIW, int CG = kCtaGroup>
+template <int BNT, int EPIW, int CG = kCtaGroup, int BKW = 64>
 size_t smem_of(int E) {
-  return Cfg<CG, BNT, EPIW>::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4;
+  return Cfg<CG, BNT, EPIW, BKW>::SMEM_FIXED + 2 * (static_cast<size_t>(E) + 1) * 4;
 }
 
-template <bool TB, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4, int CG = kCtaGroup>
+template <bool TB, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4, int CG = kCtaGroup, int BKW = 64>
 cudaError_t set_smem(int max_smem) {
-  const int bytes = static_cast<int>(std::min<size_t>(smem_of<BNT, EPIW, CG>(RG_MAX_EXPERTS_CFG), max_smem));
-  return cudaFuncSetAttribute(mgemm_kernel<TB, CG, EPI, BNT, EPIW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              bytes);
+  const int bytes =
+      static_cast<int>(std::min<size_t>(smem_of<BNT, EPIW, CG, BKW>(RG_MAX_EXPERTS_CFG), max_smem));
+  return cudaFuncSetAttribute(mgemm_kernel<TB, CG, EPI, BNT, EPIW, BKW>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 // launch configuration; CTA pairs (cg == 2) as clusters of two
@@ -689,14 +715,29 @@ void fill_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, s
   }
 }
 
-template <bool TB, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4, int CG = kCtaGroup>
+template <bool TB, int EPI = kEpiPlain, int BNT = 256, int EPIW = 4, int CG = kCtaGroup, int BKW = 64>
 cudaError_t launch_variant(const CUtensorMap& tmA, const CUtensorMap& tmAh, const CUtensorMap& tmB,
                            const CUtensorMap& tmY, const CUtensorMap& tmY2, const GroupArgs& args, int grid,
                            cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  fill_config(&cfg, attr, grid, smem_of<BNT, EPIW, CG>(args.E), Cfg<CG, BNT, EPIW>::THREADS, stream, CG);
-  return cudaLaunchKernelEx(&cfg, mgemm_kernel<TB, CG, EPI, BNT, EPIW>, tmA, tmAh, tmB, tmY, tmY2, args);
+  fill_config(&cfg, attr, grid, smem_of<BNT, EPIW, CG, BKW>(args.E), Cfg<CG, BNT, EPIW, BKW>::THREADS, stream,
+              CG);
+  return cudaLaunchKernelEx(&cfg, mgemm_kernel<TB, CG, EPI, BNT, EPIW, BKW>, tmA, tmAh, tmB, tmY, tmY2, args);
+}
+
+// the single-CTA one-stage tile with operand boxes BKW deep
+template <bool TB>
+cudaError_t launch_one_cta(const CUtensorMap& tmA, const CUtensorMap& tmAh, const CUtensorMap& tmB,
+                           const CUtensorMap& tmY, const GroupArgs& args, int sms, cudaStream_t stream) {
+  switch (mgemm_kbox(TB, args.N, args.K)) {
+    case 16:
+      return launch_variant<TB, kEpiPlain, 256, kOneEpiw, 1, 16>(tmA, tmAh, tmB, tmY, tmY, args, sms, stream);
+    case 32:
+      return launch_variant<TB, kEpiPlain, 256, kOneEpiw, 1, 32>(tmA, tmAh, tmB, tmY, tmY, args, sms, stream);
+    default:
+      return launch_variant<TB, kEpiPlain, 256, kOneEpiw, 1>(tmA, tmAh, tmB, tmY, tmY, args, sms, stream);
+  }
 }
 
 }  // namespace
@@ -716,6 +757,12 @@ cudaError_t mgemm_setup(int max_smem) {
     if ((e = set_smem<false, kEpiPlain, 64, 4>(max_smem)) != cudaSuccess) return e;
     if ((e = set_smem<false, kEpiPlain, 256, kOneEpiw, 1>(max_smem)) != cudaSuccess) return e;
     if ((e = set_smem<true, kEpiPlain, 256, kOneEpiw, 1>(max_smem)) != cudaSuccess) return e;
+    if constexpr (kOneEpiw == 8) {
+      if ((e = set_smem<false, kEpiPlain, 256, 8, 1, 16>(max_smem)) != cudaSuccess) return e;
+      if ((e = set_smem<true, kEpiPlain, 256, 8, 1, 16>(max_smem)) != cudaSuccess) return e;
+      if ((e = set_smem<false, kEpiPlain, 256, 8, 1, 32>(max_smem)) != cudaSuccess) return e;
+      if ((e = set_smem<true, kEpiPlain, 256, 8, 1, 32>(max_smem)) != cudaSuccess) return e;
+    }
   }
   return cudaSuccess;
 }
@@ -735,9 +782,8 @@ cudaError_t launch_mgemm(bool transpose_B, const CUtensorMap& tmA, const CUtenso
     if (mgemm_narrow(transpose_B != 0, args.N))
       return launch_variant<false, kEpiPlain, 64, 4>(tmA, tmAh, tmB, tmY, tmY, args, grid, stream);
     if (mgemm_one_cta(transpose_B != 0, args.N, args.K)) {
-      if (transpose_B)
-        return launch_variant<true, kEpiPlain, 256, kOneEpiw, 1>(tmA, tmAh, tmB, tmY, tmY, args, sms, stream);
-      return launch_variant<false, kEpiPlain, 256, kOneEpiw, 1>(tmA, tmAh, tmB, tmY, tmY, args, sms, stream);
+      if (transpose_B) return launch_one_cta<true>(tmA, tmAh, tmB, tmY, args, sms, stream);
+      return launch_one_cta<false>(tmA, tmAh, tmB, tmY, args, sms, stream);
     }
   }
   if (transpose_B) return launch_variant<true>(tmA, tmAh, tmB, tmY, tmY, args, grid, stream);

@@ -149,12 +149,16 @@ def test_nested_bad_offsets_flagged(gpu_lib):
 
 
 @pytest.mark.parametrize("N,K,transpose_B", [(48, 320, False), (64, 128, False), (16, 2048, False),
-                                             (384, 40, False), (384, 64, True), (200, 16, True), (72, 8, False)],
+                                             (384, 40, False), (384, 64, True), (200, 16, True), (72, 8, False),
+                                             (384, 32, False), (256, 16, True), (320, 24, True), (136, 16, False)],
                          ids=["narrow48", "narrow64", "narrow16_longK", "shallow40", "shallow64_dgrad",
-                              "shallow16_dgrad", "shallow8"])
+                              "shallow16_dgrad", "shallow8", "shallow32", "shallow16_dgrad_4d",
+                              "shallow24_dgrad_4d", "shallow16_136"])
 def test_mgemm_small_tile_variants_bit_exact(gpu_lib, N, K, transpose_B):
     """Outputs at most 64 wide (64-column pair tiles) and contractions of one
-    64-deep stage (single-CTA 128 x 256 tiles, eight epilogue warps) run their
+    64-deep stage (single-CTA 128 x 256 tiles, eight epilogue warps; operand
+    boxes 16 K wide with the 32-byte swizzle for K <= 16, 32 wide with the
+    64-byte swizzle for K <= 32, both for plain and transposed B) run their
     own tile variants; integer inputs make the expected bf16 outputs exact."""
     counts = [300, 0, 1, 129, 77]
     off = W.offsets_from_counts(counts)
