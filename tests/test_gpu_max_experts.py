@@ -38,8 +38,10 @@ def test_abi_limit_is_1024(gpu_lib):
 
 @pytest.mark.parametrize("transpose_B,N,K", [(False, 256, 128), (True, 256, 128),   # default tile
                                              (False, 64, 128),                      # 64-column tiles
-                                             (False, 256, 64), (True, 320, 64)],    # 8 epilogue warps
-                         ids=["fwd", "dgrad", "fwd-narrow", "fwd-wide", "dgrad-wide"])
+                                             (False, 256, 64), (True, 320, 64),     # single-CTA one-stage
+                                             (False, 256, 32), (True, 320, 16)],    # ... narrow operand boxes
+                         ids=["fwd", "dgrad", "fwd-narrow", "fwd-one-stage", "dgrad-one-stage",
+                              "fwd-one-stage-k32", "dgrad-one-stage-k16"])
 def test_mgemm_max_experts_bit_exact(gpu_lib, transpose_B, N, K):
     import torch
     counts = max_counts(1)
