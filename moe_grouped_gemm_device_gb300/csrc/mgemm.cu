@@ -22,6 +22,14 @@
 //     bytes directly on the issuing CTA's stage barrier (.cta_group::2), and
 //     MMA completion is multicast to the barriers of both CTAs.
 //     CG = 1: one CTA computes a 128x256 tile (tcgen05 M=128), four 48 KB stages.
+//   * Tile variants (CTA-pair build; the host picks one per launch and
+//     encodes B's map for it): forward outputs at most 64 wide run 64-column
+//     pair tiles (N = 64 MMAs, five stages); contractions of one 64-deep stage
+//     run on single CTAs (128 x 256 tiles, no cluster, eight epilogue warps),
+//     whose accumulator hand-over between the MMA issuer and the epilogue
+//     is much shorter than a pair's and sets the pace when a tile has one
+//     MMA, with operand boxes as deep as the contraction (16 or 32 K columns,
+//     32- or 64-byte swizzle) instead of 64-column boxes mostly zero-filled.
 //   * Transposed B (input gradient, w [E, K, N]) is read N-contiguous in
 //     64-column boxes; with N a multiple of 64 the map is a 4-D view whose
 //     box of two column blocks fills both boxes of a CTA's atom in one copy.
