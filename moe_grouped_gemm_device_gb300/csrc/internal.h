@@ -154,8 +154,9 @@ constexpr int LIGHT_ROWS = RG_KG_LIGHT_ROWS;
 static_assert(LIGHT_ROWS >= 1 && LIGHT_ROWS <= CHUNK_ROWS, "a light expert has rows, and fewer than one chunk");
 }  // namespace kg
 
-// Sleep between polls of the accumulator barrier by the epilogue of the
-// one-stage Mgemm tiles (contractions of at most 64; comparison builds).
+// Sleep between polls of the accumulator barrier by the epilogue of Mgemm
+// pair tiles with eight epilogue warps (comparison builds; the one-stage
+// tiles run on single CTAs, whose epilogue uses the suspending wait).
 #ifndef RG_MG_SHORT_POLL_NS
 #define RG_MG_SHORT_POLL_NS 1000
 #endif

@@ -96,9 +96,10 @@ struct Cfg {
   static constexpr int B_BYTES = B_ATOM * KATOMS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_WARPS = EPIW;
-  // sleep between the epilogue's polls of its accumulator barrier: 1 us for
-  // tiles of many stages (polling costs the copies and MMAs shared-memory
-  // bandwidth), RG_MG_SHORT_POLL_NS for one-stage tiles (a few us each)
+  // sleep between the epilogue's polls of its accumulator barrier (CTA
+  // pairs): 1 us for tiles of many stages (polling costs the copies and MMAs
+  // shared-memory bandwidth), RG_MG_SHORT_POLL_NS for pair tiles with eight
+  // epilogue warps (single CTAs use the suspending wait instead)
   static constexpr uint32_t ACC_POLL_NS = EPIW == 8 ? RG_MG_SHORT_POLL_NS : 1000;
   // staging per epilogue warp: one 32-row x 64-column bf16 box, or with 8
   // epilogue warps (two chunks per warp and tile) two, written together
@@ -682,13 +683,13 @@ __global__ void __launch_bounds__(Cfg<CG, BNT, EPIW, BKW>::THREADS, 1)
 }
 
 // every variant holds the tables of RG_MAX_EXPERTS_CFG groups beside its pipeline
-// (the 8-epilogue-warp and 64-column tiles exist for CTA pairs only)
+// (the 64-column pair tiles and the single-CTA one-stage tiles exist in the
+// CTA-pair build only)
 constexpr int kOneEpiw = RG_MG_ONE_STAGE_EPIW;
 static_assert(kOneEpiw == 4 || kOneEpiw == 8, "single-CTA one-stage tiles: 4 or 8 epilogue warps");
 static_assert(Cfg<kCtaGroup, 256, 4>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 &&
                   (kCtaGroup == 1 ||
-                   (Cfg<kCtaGroup, 256, 8>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 &&
-                    Cfg<kCtaGroup, 64, 4>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 &&
+                   (Cfg<kCtaGroup, 64, 4>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448 &&
                     Cfg<1, 256, kOneEpiw>::SMEM_FIXED + 2 * (RG_MAX_EXPERTS_CFG + 1) * 4 <= 232448)),
               "an Mgemm variant exceeds the shared memory of a CTA at the largest group count");
 
@@ -752,7 +753,7 @@ cudaError_t launch_one_cta(const CUtensorMap& tmA, const CUtensorMap& tmAh, cons
 
 size_t mgemm_smem_bytes(int E) {  // the largest of the variants built
   if constexpr (kCtaGroup == 1) return smem_of<256, 4>(E);
-  return std::max({smem_of<256, 4>(E), smem_of<256, 8>(E), smem_of<64, 4>(E), smem_of<256, kOneEpiw, 1>(E)});
+  return std::max({smem_of<256, 4>(E), smem_of<64, 4>(E), smem_of<256, kOneEpiw, 1>(E)});
 }
 
 cudaError_t mgemm_setup(int max_smem) {
