@@ -271,8 +271,10 @@ int mgemm_impl(const void* x, const void* w, const int32_t* offsets, int O, int 
   if (w == nullptr || !aligned16(w)) return RG_ERR_INVALID_ARG;
   if (M > 0 && (x == nullptr || y == nullptr || !aligned16(x) || !aligned16(y)))
     return RG_ERR_INVALID_ARG;
-  // the tile list is indexed with 32-bit integers (single-CTA tiles have BM rows)
-  const int64_t max_tiles = (M / rg::mg::BM + L) * ((N + rg::mg::BN - 1) / rg::mg::BN) * O;
+  // the tile list is indexed with 32-bit integers (the launch's tiles have
+  // TILE_M rows, or BM for the single-CTA one-stage tiles)
+  const int64_t tile_rows = rg::mgemm_one_cta(transpose_B != 0, N, K) ? rg::mg::BM : rg::mg::TILE_M;
+  const int64_t max_tiles = (M / tile_rows + L) * ((N + rg::mg::BN - 1) / rg::mg::BN) * O;
   if (max_tiles > INT32_MAX) return RG_ERR_INVALID_ARG;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != RG_OK) return rc;
