@@ -28,10 +28,13 @@ def run_nested(rg, x, w, off, transpose_B, M, O, N):
 
 @pytest.mark.parametrize("transpose_B", [False, True], ids=["fwd", "dgrad"])
 @pytest.mark.parametrize("O", [1, 3])
-def test_nested_integer_inputs_bit_exact(gpu_lib, transpose_B, O):
+@pytest.mark.parametrize("K", [320, 16, 32], ids=["k320", "k16", "k32"])
+def test_nested_integer_inputs_bit_exact(gpu_lib, transpose_B, O, K):
+    """K = 320: pair tiles; K = 16 / 32: single-CTA one-stage tiles with 16- /
+    32-column operand boxes, through the outer groups' 3-D activation map."""
     counts = [130, 0, 1, 200, 0]
     off = W.offsets_from_counts(counts)
-    L, N, K = len(counts), 192, 320  # N: one full and one partial 256-column tile per outer group
+    L, N = len(counts), 192  # N: one partial 256-column tile per outer group
     M = int(off[-1]) + 9
     x = W.integer_bf16((M, O * K), -2, 2, 21, 0)
     w = W.integer_bf16((O, L, K, N) if transpose_B else (O, L, N, K), -2, 2, 21, 1)

@@ -18,29 +18,34 @@ def layer_inputs(seed):
     E, N, K = len(counts), 384, 256
     M = int(off[-1]) + 4
     return dict(off=off, x=W.normal_bf16((M, K), 1.0, seed, 0), w=W.normal_bf16((E, N, K), 0.06, seed, 1),
-                g=W.normal_bf16((M, N), 1.0, seed, 2), E=E, N=N, K=K, M=M)
+                g=W.normal_bf16((M, N), 1.0, seed, 2), E=E, N=N, K=K, M=M,
+                # a contraction of 16: single-CTA one-stage tiles with 16-column operand boxes
+                x16=W.normal_bf16((M, 16), 1.0, seed, 3), w16=W.normal_bf16((E, N, 16), 0.25, seed, 4))
 
 
 def run_ops(rg, d, outs, stream=None):
     rg.mgemm(d["x"], d["w"], d["off"], out=outs["y"], stream=stream)
     rg.mgemm(d["g"], d["w"], d["off"], transpose_B=True, out=outs["dx"], stream=stream)
     rg.kgemm(d["g"], d["x"], d["off"], out=outs["dw"], stream=stream)
+    rg.mgemm(d["x16"], d["w16"], d["off"], out=outs["y16"], stream=stream)
 
 
 def device_inputs(p):
-    return dict(off=offsets_dev(p["off"]), x=to_dev(p["x"]), w=to_dev(p["w"]), g=to_dev(p["g"]))
+    return dict(off=offsets_dev(p["off"]), x=to_dev(p["x"]), w=to_dev(p["w"]), g=to_dev(p["g"]),
+                x16=to_dev(p["x16"]), w16=to_dev(p["w16"]))
 
 
 def empty_outputs(p):
     import torch
     return dict(y=torch.empty((p["M"], p["N"]), dtype=torch.bfloat16, device="cuda"),
                 dx=torch.empty((p["M"], p["K"]), dtype=torch.bfloat16, device="cuda"),
-                dw=torch.empty((p["E"], p["N"], p["K"]), dtype=torch.float32, device="cuda"))
+                dw=torch.empty((p["E"], p["N"], p["K"]), dtype=torch.float32, device="cuda"),
+                y16=torch.empty((p["M"], p["N"]), dtype=torch.bfloat16, device="cuda"))
 
 
 def same_bits(a, b, rows):
     import torch
-    for k in ("y", "dx"):
+    for k in ("y", "dx", "y16"):
         assert torch.equal(a[k][:rows].view(torch.int16), b[k][:rows].view(torch.int16)), k
     assert torch.equal(a["dw"].view(torch.int32), b["dw"].view(torch.int32)), "dw"
 
@@ -77,7 +82,7 @@ def test_graph_capture_and_replay(gpu_lib):
         run_ops(gpu_lib, static, outs)
     for p in (p1, p0, p1):  # new inputs copied into the captured buffers
         src = device_inputs(p)
-        for k in ("x", "w", "g", "off"):
+        for k in ("x", "w", "g", "off", "x16", "w16"):
             static[k].copy_(src[k])
         graph.replay()
         torch.cuda.synchronize()
