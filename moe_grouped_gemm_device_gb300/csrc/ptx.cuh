@@ -373,14 +373,6 @@ __device__ __forceinline__ void tma_load_3d_cg(uint32_t dst, const CUtensorMap* 
   else tma_load_3d_pair(dst, m, bar, c0, c1, c2);
 }
 
-// Bounded spin (used by a peer CTA after an abort, whose own copies signal the
-// issuing CTA's barriers, to let them land before it leaves).
-__device__ __forceinline__ void spin_ns(uint64_t ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (globaltimer_ns() - t0 < ns) {
-  }
-}
-
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t c0,
                                              int32_t c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
