@@ -51,16 +51,27 @@ def test_traffic_only_for_the_captured_source_and_workload(tmp_path, monkeypatch
 
 
 def test_committed_traffic_entries_name_known_kernels_and_workloads():
+    """Every record names a kernel the bench knows, a workload and ops of that
+    workload which the bench maps to that kernel, and bytes within a plausible
+    band of the op's algorithmic bytes (outputs still in L2 at the kernel's end
+    lower them, re-reads raise them): a record keyed to the wrong op or kernel
+    fails here."""
     d = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
-    names = {W.ALL[n]().name for n in W.ALL}
+    by_name = {W.ALL[n]().name: W.ALL[n]() for n in W.ALL}
     for k, ent in d.items():
         if k.startswith("_"):
             continue
         assert k in bench.KERNEL_SOURCES, k
         assert len(ent["source_sha256_16"]) == 16
         for wl, per_op in ent["workloads"].items():
-            assert wl in names, wl
-            assert all(isinstance(v, int) and v > 0 for v in per_op.values())
+            assert wl in by_name, wl
+            ops = {op.name: op for op in by_name[wl].ops}
+            for name, v in per_op.items():
+                assert isinstance(v, int) and v > 0, (k, wl, name)
+                assert name in ops, (k, wl, name)
+                assert bench.kernel_of(ops[name]) == k, (k, wl, name)
+                ratio = v / bench.algorithmic_bytes(ops[name], by_name[wl].counts)
+                assert 0.4 <= ratio <= 2.5, (k, wl, name, ratio)
 
 
 def test_peak_kind_follows_the_timed_region():
